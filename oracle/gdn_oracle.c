@@ -41,7 +41,7 @@
  * this changes memory use only, not the result.
  *
  * Build: plain C99, no fused multiply-add contraction (-ffp-contract=off), optional
- * OpenMP over independent (batch row, kv head) groups.
+ * OpenMP over independent (batch row, value head) pairs.
  */
 #include <stdlib.h>
 #include <string.h>
@@ -65,6 +65,10 @@ static size_t off_qk(const oracle_shape *s, int b, int t, int hk) {
 }
 static size_t off_v(const oracle_shape *s, int b, int t, int h) {
     return (((size_t)b * s->T + t) * s->Hv + h) * (size_t)s->Dv;
+}
+/* per-value-head rows of dq/dk before the kv-head sum: [B, T, Hv, Dk] */
+static size_t off_qh(const oracle_shape *s, int b, int t, int h) {
+    return (((size_t)b * s->T + t) * s->Hv + h) * (size_t)s->Dk;
 }
 static size_t off_gate(const oracle_shape *s, int b, int t, int h) {
     return ((size_t)b * s->T + t) * s->Hv + h;
@@ -153,9 +157,9 @@ int oracle_fwd(const oracle_shape *s, const double *q, const double *k, const do
     return err;
 }
 
-/* Reverse-time VJP of one value head (b, h). dq and dk receive this head's
- * contribution added onto what they hold (the caller visits the heads of a kv group
- * in ascending order); dv, dg, dbeta are written; dS0 (if not NULL) is written.
+/* Reverse-time VJP of one value head (b, h). dqh and dkh ([B, T, Hv, Dk], zeroed by
+ * the caller) receive this head's own dq and dk; dv, dg, dbeta are written; dS0 (if not
+ * NULL) is written.
  *
  * Per step t, going backwards, with Sh = dL/dS_t accumulated so far:
  *   y_t = S_t q_t            ->  Sh += dy_t q_t^T ;       dq_t += S_t^T dy_t
@@ -167,8 +171,8 @@ int oracle_fwd(const oracle_shape *s, const double *q, const double *k, const do
  * and dS_0 is Sh after step 0. */
 static int head_backward(const oracle_shape *s, int b, int h, const double *q, const double *k,
                          const double *v, const double *g, const double *beta, const double *S0,
-                         const double *dy, const double *dS_T, double *dq, double *dk, double *dv,
-                         double *dg, double *dbeta, double *dS0) {
+                         const double *dy, const double *dS_T, double *dqh, double *dkh,
+                         double *dv, double *dg, double *dbeta, double *dS0) {
     const int rep = s->Hv / s->Hk, hk = h / rep, Dv = s->Dv, Dk = s->Dk, C = s->C;
     const int NC = n_chunks(s);
     const size_t nstate = (size_t)Dv * Dk;
@@ -210,7 +214,7 @@ static int head_backward(const oracle_shape *s, int b, int h, const double *q, c
             const double *vt = v + off_v(s, b, t, h), *dyt = dy + off_v(s, b, t, h);
             const double *u = us + (size_t)tau * Dv, *delta = ds + (size_t)tau * Dv;
             const double gt = g[off_gate(s, b, t, h)], bt = beta[off_gate(s, b, t, h)];
-            double *dqt = dq + off_qk(s, b, t, hk), *dkt = dk + off_qk(s, b, t, hk);
+            double *dqt = dqh + off_qh(s, b, t, h), *dkt = dkh + off_qh(s, b, t, h);
 
             /* y_t = S_t q_t */
             for (int i = 0; i < Dv; ++i)
@@ -261,8 +265,9 @@ done:
 }
 
 /* Backward over all heads. S0 and dS_T may be NULL (zeros); dS0 may be NULL (skipped).
- * Work is split over (b, hk) groups so that each group's dq/dk sums run in one thread
- * in ascending value-head order. nthreads <= 0 uses the OpenMP default. */
+ * Heads run in parallel, each into its own dq/dk rows; then dq and dk of every kv head
+ * are the sums of its value heads' rows taken in ascending value-head order.
+ * nthreads <= 0 uses the OpenMP default. */
 int oracle_bwd(const oracle_shape *s, const double *q, const double *k, const double *v,
                const double *g, const double *beta, const double *S0, const double *dy,
                const double *dS_T, double *dq, double *dk, double *dv, double *dg,
@@ -270,22 +275,32 @@ int oracle_bwd(const oracle_shape *s, const double *q, const double *k, const do
     if (!shape_ok(s) || !q || !k || !v || !g || !beta || !dy || !dq || !dk || !dv || !dg ||
         !dbeta)
         return ORACLE_EINVAL;
-    const int rep = s->Hv / s->Hk, ngroups = s->B * s->Hk;
+    const int rep = s->Hv / s->Hk, nheads = s->B * s->Hv;
+    const size_t nh = (size_t)s->B * s->T * s->Hv * s->Dk;
+    double *dqh = calloc(nh, sizeof(double));
+    double *dkh = calloc(nh, sizeof(double));
+    if (!dqh || !dkh) { free(dqh); free(dkh); return ORACLE_ENOMEM; }
     int err = ORACLE_OK;
-    memset(dq, 0, (size_t)s->B * s->T * s->Hk * s->Dk * sizeof(double));
-    memset(dk, 0, (size_t)s->B * s->T * s->Hk * s->Dk * sizeof(double));
 #ifdef _OPENMP
     if (nthreads <= 0) nthreads = omp_get_max_threads();
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
 #endif
-    for (int bg = 0; bg < ngroups; ++bg) {
-        const int b = bg / s->Hk, hk = bg % s->Hk;
-        for (int h = hk * rep; h < (hk + 1) * rep; ++h) {
-            int e = head_backward(s, b, h, q, k, v, g, beta, S0, dy, dS_T, dq, dk, dv, dg, dbeta,
-                                  dS0);
-            if (e) err = e;
-        }
+    for (int bh = 0; bh < nheads; ++bh) {
+        const int b = bh / s->Hv, h = bh % s->Hv;
+        int e = head_backward(s, b, h, q, k, v, g, beta, S0, dy, dS_T, dqh, dkh, dv, dg, dbeta, dS0);
+        if (e) err = e;
     }
+    for (int b = 0; b < s->B; ++b)
+        for (int t = 0; t < s->T; ++t)
+            for (int hk = 0; hk < s->Hk; ++hk) {
+                double *dqt = dq + off_qk(s, b, t, hk), *dkt = dk + off_qk(s, b, t, hk);
+                for (int j = 0; j < s->Dk; ++j) { dqt[j] = 0.0; dkt[j] = 0.0; }
+                for (int h = hk * rep; h < (hk + 1) * rep; ++h) {
+                    const double *qh = dqh + off_qh(s, b, t, h), *kh = dkh + off_qh(s, b, t, h);
+                    for (int j = 0; j < s->Dk; ++j) { dqt[j] += qh[j]; dkt[j] += kh[j]; }
+                }
+            }
+    free(dqh); free(dkh);
     (void)nthreads;
     return err;
 }
