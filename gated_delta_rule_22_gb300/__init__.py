@@ -1,0 +1,9 @@
+"""Gated delta rule training kernels for NVIDIA GB300 (sm_103a).
+
+The compute lives in libgdn.so, a C-ABI library of hand-written CUDA kernels
+(include/gdn.h). This package is its thin Python binding.
+"""
+from .binding import (  # noqa: F401
+    GDN_BF16, GDN_F32, GdnError, GdnShape, gdn_bwd, gdn_bwd_workspace_bytes, gdn_ckpt_bytes, gdn_fwd,
+    header_functions, load_library, make_shape,
+)

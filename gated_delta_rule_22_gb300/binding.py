@@ -1,0 +1,183 @@
+"""Thin ctypes binding of libgdn.so (include/gdn.h). Argument marshalling only.
+
+Every computation happens in the CUDA kernels behind the C ABI; PyTorch is used here
+only to hold device memory and to supply the current CUDA stream. If the compiled
+library is missing, loading fails with an ImportError; there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "gdn.h")
+
+GDN_F32, GDN_BF16 = 0, 1
+GDN_OK = 0
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("Hk", ctypes.c_int), ("Hv", ctypes.c_int),
+                ("Dk", ctypes.c_int), ("Dv", ctypes.c_int), ("chunk", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn, code, lib):
+        self.code = code
+        msg = lib.gdn_strerror(code).decode()
+        detail = lib.gdn_last_error().decode()
+        super().__init__(f"{fn} returned {code}: {msg}" + (f" [{detail}]" if detail else ""))
+
+
+_VP = ctypes.c_void_p
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libgdn.so and declare the signatures of include/gdn.h."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    SP = ctypes.POINTER(GdnShape)
+    lib.gdn_ckpt_bytes.restype = ctypes.c_size_t
+    lib.gdn_ckpt_bytes.argtypes = [SP]
+    lib.gdn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_bwd_workspace_bytes.argtypes = [SP]
+    lib.gdn_fwd.restype = ctypes.c_int
+    lib.gdn_fwd.argtypes = [SP] + [_VP] * 10
+    lib.gdn_bwd.restype = ctypes.c_int
+    lib.gdn_bwd.argtypes = [SP] + [_VP] * 15 + [ctypes.c_size_t, _VP]
+    lib.gdn_strerror.restype = ctypes.c_char_p
+    lib.gdn_strerror.argtypes = [ctypes.c_int]
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    lib.gdn_last_error.argtypes = []
+    lib.gdn_version.restype = ctypes.c_int
+    lib.gdn_version.argtypes = []
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def header_functions(header: str = HEADER):
+    """Names of the functions declared in include/gdn.h."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return GDN_F32
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; the library takes float32 or bfloat16")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(name, t, shape, dtype, device):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def make_shape(B, T, Hk, Hv, Dk, Dv, chunk=64, dtype=GDN_F32) -> GdnShape:
+    return GdnShape(B, T, Hk, Hv, Dk, Dv, chunk, dtype)
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def gdn_ckpt_bytes(shape: GdnShape) -> int:
+    return load_library().gdn_ckpt_bytes(ctypes.byref(shape))
+
+
+def gdn_bwd_workspace_bytes(shape: GdnShape) -> int:
+    return load_library().gdn_bwd_workspace_bytes(ctypes.byref(shape))
+
+
+def _shape_of(q, v, chunk):
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    return make_shape(B, T, Hk, Hv, Dk, Dv, chunk, _dtype_code(q))
+
+
+def gdn_fwd(q, k, v, g, beta, S0=None, chunk=64, *, y=None, S_T=None, ckpt=None, want_S_T=True,
+            stream=None):
+    """y, S_T, ckpt = gdn_fwd(q, k, v, g, beta[, S0]) on CUDA tensors (see include/gdn.h)."""
+    torch = _torch()
+    lib = load_library()
+    shape = _shape_of(q, v, chunk)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    dev, dt = q.device, q.dtype
+    for name, t, shp in (("q", q, q.shape), ("k", k, q.shape), ("v", v, (B, T, Hv, Dv)),
+                         ("g", g, (B, T, Hv)), ("beta", beta, (B, T, Hv))):
+        _check(name, t, shp, dt, dev)
+    if S0 is not None:
+        _check("S0", S0, (B, Hv, Dv, Dk), torch.float32, dev)
+    NC = -(-T // (chunk or 64))
+    if y is None:
+        y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
+    if S_T is None and want_S_T:
+        S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
+    if ckpt is None:
+        ckpt = torch.empty((B, Hv, NC, Dv, Dk), dtype=torch.float32, device=dev)
+    rc = lib.gdn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0),
+                     _ptr(y), _ptr(S_T), _ptr(ckpt), _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError("gdn_fwd", rc, lib)
+    return y, S_T, ckpt
+
+
+def gdn_bwd(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, workspace=None, out=None,
+            want_dS0=True, stream=None):
+    """dict(dq, dk, dv, dg, dbeta, dS0) = gdn_bwd(...) on CUDA tensors (see include/gdn.h)."""
+    torch = _torch()
+    lib = load_library()
+    shape = _shape_of(q, v, chunk)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    dev, dt = q.device, q.dtype
+    for name, t, shp in (("q", q, q.shape), ("k", k, q.shape), ("v", v, (B, T, Hv, Dv)),
+                         ("g", g, (B, T, Hv)), ("beta", beta, (B, T, Hv)), ("dy", dy, (B, T, Hv, Dv))):
+        _check(name, t, shp, dt, dev)
+    NC = -(-T // (chunk or 64))
+    _check("ckpt", ckpt, (B, Hv, NC, Dv, Dk), torch.float32, dev)
+    if dS_T is not None:
+        _check("dS_T", dS_T, (B, Hv, Dv, Dk), torch.float32, dev)
+    if out is None:
+        out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+               "dg": torch.empty_like(g), "dbeta": torch.empty_like(beta),
+               "dS0": torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev) if want_dS0 else None}
+    need = lib.gdn_bwd_workspace_bytes(ctypes.byref(shape))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    rc = lib.gdn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ckpt),
+                     _ptr(dy), _ptr(dS_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                     _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out.get("dS0")), _ptr(workspace),
+                     workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError("gdn_bwd", rc, lib)
+    return out

@@ -1,0 +1,169 @@
+// gdn_api.cu -- the C ABI declared in include/gdn.h: argument checks (all on the host,
+// before anything is enqueued), scratch layout, and dispatch to the kernels.
+#include "gdn.h"
+#include "gdn_common.cuh"
+
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+struct Plan {
+    int B, T, Hk, Hv, Dk, Dv, C, NC, dtype;
+    int warps;     // warps per CTA (both kernels)
+    int RB;        // rows of a state per CTA
+    int nsplit;    // CTAs per (b, h)
+    int nsub_max;  // sub-blocks per chunk
+};
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int make_plan(const gdn_shape *s, Plan *p) {
+    if (s == nullptr) return GDN_ERR_INVALID_ARG;
+    if (s->B <= 0 || s->T <= 0 || s->Hk <= 0 || s->Hv <= 0 || s->Dk <= 0 || s->Dv <= 0 || s->chunk < 0)
+        return GDN_ERR_INVALID_ARG;
+    if (s->dtype != GDN_F32 && s->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (s->Hv % s->Hk != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (s->Dk % 32 != 0 || s->Dk > 256) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (s->Dv % 4 != 0 || s->Dv > gdn::kMaxDv) return GDN_ERR_UNSUPPORTED_SHAPE;
+    const int C = s->chunk == 0 ? 64 : s->chunk;
+    if (C > gdn::kMaxChunk) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (s->Hv > 65535 || s->B > 65535) return GDN_ERR_UNSUPPORTED_SHAPE;
+    // every tensor and scratch region must be indexable with 62-bit offsets
+    const double rows = (double)s->B * s->Hv * s->Dv;
+    const double big = (double)s->T * rows * (s->Dk + 8.0) * 8.0;
+    if (big > 4.0e18) return GDN_ERR_UNSUPPORTED_SHAPE;
+    p->B = s->B; p->T = s->T; p->Hk = s->Hk; p->Hv = s->Hv; p->Dk = s->Dk; p->Dv = s->Dv;
+    p->C = C;
+    p->NC = (s->T + C - 1) / C;
+    p->dtype = s->dtype;
+    int warps = (s->Dv + gdn::kRowsPerWarp - 1) / gdn::kRowsPerWarp;
+    if (warps > 8) warps = 8;
+    p->warps = warps;
+    p->RB = warps * gdn::kRowsPerWarp;
+    p->nsplit = (s->Dv + p->RB - 1) / p->RB;
+    p->nsub_max = (C + gdn::kSub - 1) / gdn::kSub;
+    return GDN_OK;
+}
+
+struct Workspace {
+    size_t dq, dk, dg, db, state, total;  // byte offsets and total
+};
+
+Workspace workspace_layout(const Plan &p) {
+    Workspace w;
+    const size_t nqk = (size_t)p.B * p.T * p.Hv * p.nsplit * p.Dk;
+    const size_t ngate = (size_t)p.B * p.T * p.Hv * p.nsplit;
+    const size_t nstate = (size_t)p.B * p.Hv * p.nsplit * (p.nsub_max + gdn::kSub - 1) * p.RB * p.Dk;
+    size_t off = 0;
+    w.dq = off; off += round_up(nqk * 4);
+    w.dk = off; off += round_up(nqk * 4);
+    w.dg = off; off += round_up(ngate * 4);
+    w.db = off; off += round_up(ngate * 4);
+    w.state = off; off += round_up(nstate * 4);
+    w.total = off;
+    return w;
+}
+
+bool aligned(const void *ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return GDN_OK;
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_ckpt_bytes(const gdn_shape *shape) {
+    Plan p;
+    if (make_plan(shape, &p) != GDN_OK) return 0;
+    return (size_t)p.B * p.Hv * p.NC * p.Dv * p.Dk * sizeof(float);
+}
+
+size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
+    Plan p;
+    if (make_plan(shape, &p) != GDN_OK) return 0;
+    return workspace_layout(p).total;
+}
+
+int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
+            const void *beta, const float *S0, void *y, float *S_T, float *ckpt, void *stream) {
+    Plan p;
+    int rc = make_plan(shape, &p);
+    if (rc != GDN_OK) return rc;
+    if (!q || !k || !v || !g || !beta || !y || !ckpt) return GDN_ERR_INVALID_ARG;
+    const void *all[] = {q, k, v, g, beta, S0, y, S_T, ckpt};
+    for (const void *ptr : all)
+        if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    gdn::FwdParams fp;
+    fp.q = q; fp.k = k; fp.v = v; fp.g = g; fp.beta = beta; fp.S0 = S0;
+    fp.y = y; fp.S_T = S_T; fp.ckpt = ckpt;
+    fp.B = p.B; fp.T = p.T; fp.Hk = p.Hk; fp.Hv = p.Hv; fp.Dv = p.Dv; fp.C = p.C; fp.NC = p.NC;
+    g_last_error[0] = '\0';
+    return cuda_status(gdn::launch_fwd(fp, p.Dk, p.dtype, p.warps, (cudaStream_t)stream));
+}
+
+int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
+            const void *beta, const float *ckpt, const void *dy, const float *dS_T, void *dq,
+            void *dk, void *dv, void *dg, void *dbeta, float *dS0, void *workspace,
+            size_t workspace_bytes, void *stream) {
+    Plan p;
+    int rc = make_plan(shape, &p);
+    if (rc != GDN_OK) return rc;
+    if (!q || !k || !v || !g || !beta || !ckpt || !dy || !dq || !dk || !dv || !dg || !dbeta || !workspace)
+        return GDN_ERR_INVALID_ARG;
+    const void *all[] = {q, k, v, g, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace};
+    for (const void *ptr : all)
+        if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    const Workspace w = workspace_layout(p);
+    if (workspace_bytes < w.total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    char *ws = static_cast<char *>(workspace);
+
+    gdn::BwdParams bp;
+    bp.q = q; bp.k = k; bp.v = v; bp.g = g; bp.beta = beta; bp.ckpt = ckpt; bp.dy = dy;
+    bp.dS_T = dS_T; bp.dS0 = dS0; bp.dv = dv;
+    bp.ws_dq = reinterpret_cast<float *>(ws + w.dq);
+    bp.ws_dk = reinterpret_cast<float *>(ws + w.dk);
+    bp.ws_dg = reinterpret_cast<float *>(ws + w.dg);
+    bp.ws_db = reinterpret_cast<float *>(ws + w.db);
+    bp.ws_state = reinterpret_cast<float *>(ws + w.state);
+    bp.B = p.B; bp.T = p.T; bp.Hk = p.Hk; bp.Hv = p.Hv; bp.Dv = p.Dv; bp.C = p.C; bp.NC = p.NC;
+    bp.nsplit = p.nsplit; bp.nsub_max = p.nsub_max;
+
+    gdn::ReduceParams rp;
+    rp.ws_dq = bp.ws_dq; rp.ws_dk = bp.ws_dk; rp.ws_dg = bp.ws_dg; rp.ws_db = bp.ws_db;
+    rp.dq = dq; rp.dk = dk; rp.dg = dg; rp.dbeta = dbeta;
+    rp.B = p.B; rp.T = p.T; rp.Hk = p.Hk; rp.Hv = p.Hv; rp.Dk = p.Dk; rp.nsplit = p.nsplit;
+
+    g_last_error[0] = '\0';
+    rc = cuda_status(gdn::launch_bwd(bp, p.Dk, p.dtype, p.warps, (cudaStream_t)stream));
+    if (rc != GDN_OK) return rc;
+    return cuda_status(gdn::launch_reduce(rp, p.dtype, (cudaStream_t)stream));
+}
+
+const char *gdn_strerror(int code) {
+    switch (code) {
+        case GDN_OK: return "success";
+        case GDN_ERR_INVALID_ARG: return "invalid argument (NULL shape or required pointer, size <= 0, or bad dtype)";
+        case GDN_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
+        case GDN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (Hv % Hk, Dk, Dv, chunk or tensor size)";
+        case GDN_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than gdn_bwd_workspace_bytes()";
+        case GDN_ERR_CUDA: return "CUDA runtime error (see gdn_last_error)";
+        case GDN_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+        default: return "unknown gdn error code";
+    }
+}
+
+const char *gdn_last_error(void) { return g_last_error; }
+
+int gdn_version(void) { return GDN_VERSION; }
+
+}  // extern "C"

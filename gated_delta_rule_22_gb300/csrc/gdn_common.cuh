@@ -1,0 +1,106 @@
+// gdn_common.cuh -- device helpers and parameter blocks shared by the forward and
+// backward kernels of the gated delta rule library (internal; not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace gdn {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// Thread layout of every state tile: a warp owns kRowsPerWarp rows of one value head's
+// [Dv, Dk] state; lane l holds columns l, l+32, ..., l+32*(E-1) of each of those rows
+// (E = Dk/32). Row dot products (S k, S q, Sh k) are therefore sums across the 32
+// lanes; column sums (for dq, dk) are sums over a thread's rows, then over warps.
+constexpr int kRowsPerWarp = 8;
+// Steps per forward staging tile.
+constexpr int kFwdTile = 16;
+// Steps per backward sub-block: states inside a sub-block are re-computed and kept
+// so that the reverse sweep can read S_{t-1} for each step.
+constexpr int kSub = 8;
+constexpr int kMaxChunk = 128;
+constexpr int kMaxDv = 4096;
+
+struct FwdParams {
+    const void *q, *k, *v, *g, *beta;
+    const float *S0;
+    void *y;
+    float *S_T, *ckpt;
+    int B, T, Hk, Hv, Dv, C, NC;
+};
+
+struct BwdParams {
+    const void *q, *k, *v, *g, *beta;
+    const float *ckpt;
+    const void *dy;
+    const float *dS_T;
+    float *dS0;
+    float *ws_dq, *ws_dk;   // [B, T, Hv, nsplit, Dk] per-CTA column partials
+    float *ws_dg, *ws_db;   // [B, T, Hv, nsplit]
+    float *ws_state;        // per CTA: (nsub_max + kSub - 1) states of [RB, Dk]
+    void *dv;
+    int B, T, Hk, Hv, Dv, C, NC, nsplit, nsub_max;
+};
+
+struct ReduceParams {
+    const float *ws_dq, *ws_dk, *ws_dg, *ws_db;
+    void *dq, *dk, *dg, *dbeta;
+    int B, T, Hk, Hv, Dk, nsplit;
+};
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Sum N values (N a power of two, 2 <= N <= 32) across the 32 lanes of a warp with
+// (N - 1) + (5 - log2 N) shuffles instead of 5 N: at each of the first log2(N) levels a
+// lane keeps half of its values, sends the other half to its partner (lane ^ m) and
+// adds what it receives. Afterwards lane l holds the full sum of value index
+// (l >> (5 - log2 N)) -- bit i of the index is lane bit (5 - log2 N + i) -- and the
+// 32/N lanes that share that index hold the same sum. Summation order is fixed.
+template <int N>
+__device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
+    static_assert(N >= 2 && N <= 32 && (N & (N - 1)) == 0, "N must be a power of two");
+    int m = 16;
+#pragma unroll
+    for (int n = N; n > 1; n >>= 1, m >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = upper ? v[i] : v[i + n / 2];
+            const float keep = upper ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFullMask, send, m);
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (; m >= 1; m >>= 1) x += __shfl_xor_sync(kFullMask, x, m);
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(kFullMask, x, m);
+    return x;
+}
+
+// Launchers (one per kernel family); each returns the cudaError_t of its launch.
+cudaError_t launch_fwd(const FwdParams &p, int Dk, int dtype, int warps, cudaStream_t s);
+cudaError_t launch_bwd(const BwdParams &p, int Dk, int dtype, int warps, cudaStream_t s);
+cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
+size_t bwd_smem_bytes(int DK, int nw, int C);
+
+}  // namespace gdn

@@ -1,0 +1,138 @@
+/*
+ * gdn.h -- C ABI of the gated delta rule training kernels (forward with chunk
+ * checkpoints, and the reverse-time vector-Jacobian product), for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operation (mlx issue #4614 "mx.fast.gated_delta_update VJP: wrong gradient
+ * w.r.t. g ...", section "Recurrence used for the references"): for every batch row b
+ * and value head h, with kv head hk = h / (Hv / Hk), a state S of shape [Dv, Dk]
+ * evolves over t = 0 .. T-1 as
+ *
+ *     S <- g_t * S
+ *     S <- S + outer(beta_t * (v_t - S k_t), k_t)
+ *     y_t = S q_t
+ *
+ * starting from S_0 (zeros unless given). The training path (mlx-lm PR #1217 "Add
+ * Metal VJP kernel for gated_delta_update", section "What this PR adds") runs the
+ * forward once, saving the state at the start of every chunk of C steps, and a
+ * reverse sweep that re-runs each chunk from its checkpoint to return the gradients.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are device pointers to contiguous, row-major arrays,
+ *     16-byte aligned, owned by the caller. The library allocates nothing and keeps
+ *     no state between calls.
+ *   - Layouts: q, k, dq, dk       [B, T, Hk, Dk]
+ *              v, y, dy, dv       [B, T, Hv, Dv]
+ *              g, beta, dg, dbeta [B, T, Hv]
+ *              S0, S_T, dS_T, dS0 [B, Hv, Dv, Dk]      (float32, row index = Dv index)
+ *              ckpt               [B, Hv, NC, Dv, Dk]  (float32, NC = ceil(T / C))
+ *   - q, k, v, g, beta, dy and every output except the states and checkpoints have
+ *     the element type `shape->dtype` (float32 or bfloat16). Arithmetic and state are
+ *     float32; outputs are rounded to nearest even.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and the call returns without waiting for it.
+ *   - Every argument check runs on the host before anything is enqueued: a call
+ *     that returns an error has launched nothing and written nothing.
+ *   - Results are bitwise deterministic: no atomics; every reduction (over rows,
+ *     over the value heads that share a kv head) runs in a fixed order.
+ *   - There is no host fallback: if the GPU cannot run a kernel the call returns
+ *     GDN_ERR_CUDA.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_VERSION 1
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+typedef enum {
+    GDN_F32 = 0,  /* IEEE float32 */
+    GDN_BF16 = 1  /* bfloat16 */
+} gdn_dtype;
+
+typedef struct {
+    int B, T, Hk, Hv, Dk, Dv; /* batch rows, steps, kv heads, value heads, key dim, value dim */
+    int chunk;                /* checkpoint interval C, 1..128; 0 selects 64 */
+    int dtype;                /* a gdn_dtype */
+} gdn_shape;
+
+/* Return codes. */
+enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = -1,       /* NULL shape or required pointer, a size <= 0, bad dtype */
+    GDN_ERR_MISALIGNED = -2,        /* a pointer not 16-byte aligned */
+    GDN_ERR_UNSUPPORTED_SHAPE = -3, /* Hv % Hk != 0, Dk not in {32,64,96,128,160,192,224,256},
+                                       Dv % 4 != 0 or Dv > 4096, chunk outside 1..128,
+                                       B or Hv > 65535, or a tensor too large to index */
+    GDN_ERR_WORKSPACE_TOO_SMALL = -4,
+    GDN_ERR_CUDA = -5,              /* the CUDA runtime reported an error (see gdn_last_error) */
+    GDN_ERR_TIMEOUT = -6            /* reserved for bounded device-side waits */
+};
+
+/* Bytes of the checkpoint buffer gdn_fwd writes: B*Hv*NC*Dv*Dk*4. 0 for an invalid shape. */
+GDN_API size_t gdn_ckpt_bytes(const gdn_shape *shape);
+
+/* Bytes of device scratch gdn_bwd needs (fp32 partial sums for the fixed-order
+ * reductions, and the states it re-computes). 0 for an invalid shape. */
+GDN_API size_t gdn_bwd_workspace_bytes(const gdn_shape *shape);
+
+/*
+ * Forward with checkpoints.
+ *   in : q, k, v, g, beta            (dtype)
+ *        S0                          (float32, may be NULL: zeros)
+ *   out: y                           (dtype)
+ *        S_T                         (float32, may be NULL: not written)
+ *        ckpt                        (float32, gdn_ckpt_bytes(shape) bytes):
+ *                                    ckpt[b, h, c] = state before step c*C
+ * Returns GDN_OK or an error code.
+ */
+GDN_API int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                    const void *g, const void *beta, const float *S0, void *y, float *S_T,
+                    float *ckpt, void *stream);
+
+/*
+ * Reverse-time VJP. Gradients of L = <dy, y> + <dS_T, S_T> with respect to q, k, v, g,
+ * beta and S0, for the forward defined by the same inputs. The pages print no backward
+ * formula; this is the chain rule applied to the recurrence above, in reverse time.
+ *   in : q, k, v, g, beta, dy        (dtype)
+ *        ckpt                        (float32) as written by gdn_fwd for the same inputs,
+ *                                    shape and S0
+ *        dS_T                        (float32, may be NULL: zeros)
+ *   out: dq, dk                      (dtype) summed over the value heads of each kv head,
+ *                                    in ascending value-head order
+ *        dv, dg, dbeta               (dtype)
+ *        dS0                         (float32, may be NULL: not written)
+ *   scratch: workspace of at least gdn_bwd_workspace_bytes(shape) bytes (device,
+ *            16-byte aligned, owned by the caller); its contents on entry do not matter.
+ *            Two calls that overlap on the GPU must not share a workspace.
+ * Returns GDN_OK or an error code.
+ */
+GDN_API int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                    const void *g, const void *beta, const float *ckpt, const void *dy,
+                    const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta,
+                    float *dS0, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static description of a return code. */
+GDN_API const char *gdn_strerror(int code);
+
+/* Text of the last CUDA error seen by a gdn_* call on this host thread ("" if none). */
+GDN_API const char *gdn_last_error(void);
+
+/* GDN_VERSION of the library that was loaded. */
+GDN_API int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

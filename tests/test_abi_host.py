@@ -1,0 +1,121 @@
+"""The C-ABI library without a GPU: it loads, exports every function include/gdn.h
+declares, sizes its buffers, and rejects bad arguments on the host before any CUDA call.
+
+Pointers here are fake addresses that are never dereferenced: every call below returns
+an error from the host-side checks, which run before anything is enqueued."""
+import ctypes
+import os
+
+import pytest
+
+from gated_delta_rule_22_gb300 import binding as B
+
+OK, INVALID, MISALIGNED, UNSUPPORTED, WS_SMALL, CUDA, TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+FAKE = 0x7F0000000000  # 16-byte aligned, never touched
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        from gated_delta_rule_22_gb300 import build
+        build.build()
+    return B.load_library()
+
+
+def shape(**kw):
+    base = dict(B=1, T=16, Hk=2, Hv=4, Dk=64, Dv=32, chunk=0, dtype=0)
+    base.update(kw)
+    return B.GdnShape(**base)
+
+
+def fwd(lib, s, **ptrs):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, S0=None, y=FAKE, S_T=None, ckpt=FAKE)
+    p.update(ptrs)
+    args = [ctypes.c_void_p(p[n]) if p[n] is not None else None for n in
+            ("q", "k", "v", "g", "beta", "S0", "y", "S_T", "ckpt")]
+    return lib.gdn_fwd(ctypes.byref(s) if s is not None else None, *args, None)
+
+
+def bwd(lib, s, ws_bytes=None, **ptrs):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, ckpt=FAKE, dy=FAKE, dS_T=None, dq=FAKE, dk=FAKE,
+             dv=FAKE, dg=FAKE, dbeta=FAKE, dS0=None, ws=FAKE)
+    p.update(ptrs)
+    names = ("q", "k", "v", "g", "beta", "ckpt", "dy", "dS_T", "dq", "dk", "dv", "dg", "dbeta", "dS0", "ws")
+    args = [ctypes.c_void_p(p[n]) if p[n] is not None else None for n in names]
+    if ws_bytes is None:
+        ws_bytes = lib.gdn_bwd_workspace_bytes(ctypes.byref(s)) if s is not None else 0
+    return lib.gdn_bwd(ctypes.byref(s) if s is not None else None, *args, ws_bytes, None)
+
+
+def test_exports_every_header_function(lib):
+    names = B.header_functions()
+    assert set(names) >= {"gdn_fwd", "gdn_bwd", "gdn_ckpt_bytes", "gdn_bwd_workspace_bytes",
+                          "gdn_strerror", "gdn_last_error", "gdn_version"}
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/gdn.h but not exported"
+    assert lib.gdn_version() == 1
+
+
+def test_checkpoint_bytes(lib):
+    for T, C in ((16, 0), (37, 16), (1, 1), (128, 128), (2048, 64)):
+        s = shape(T=T, chunk=C, Hv=6, Hk=3, Dk=96, Dv=20)
+        nc = -(-T // (C or 64))
+        assert lib.gdn_ckpt_bytes(ctypes.byref(s)) == 1 * 6 * nc * 20 * 96 * 4
+    assert lib.gdn_ckpt_bytes(ctypes.byref(shape(Hv=3))) == 0
+    assert lib.gdn_ckpt_bytes(None) == 0
+
+
+def test_workspace_bytes(lib):
+    a = lib.gdn_bwd_workspace_bytes(ctypes.byref(shape(T=16)))
+    b = lib.gdn_bwd_workspace_bytes(ctypes.byref(shape(T=1024)))
+    assert 0 < a < b and a % 256 == 0 and b % 256 == 0
+    assert lib.gdn_bwd_workspace_bytes(ctypes.byref(shape(Dk=40))) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=0), INVALID), (dict(B=-1), INVALID), (dict(Dv=0), INVALID), (dict(dtype=7), INVALID),
+    (dict(chunk=-1), INVALID), (dict(Hv=3), UNSUPPORTED), (dict(Dk=48), UNSUPPORTED),
+    (dict(Dk=288), UNSUPPORTED), (dict(Dv=6), UNSUPPORTED), (dict(Dv=4100), UNSUPPORTED),
+    (dict(chunk=129), UNSUPPORTED), (dict(Hv=70000, Hk=1), UNSUPPORTED),
+])
+def test_bad_shapes_rejected(lib, kw, code):
+    s = shape(**kw)
+    assert fwd(lib, s) == code
+    assert bwd(lib, s, ws_bytes=1 << 40) == code
+
+
+def test_null_shape_and_pointers(lib):
+    assert fwd(lib, None) == INVALID
+    assert bwd(lib, None, ws_bytes=0) == INVALID
+    s = shape()
+    for n in ("q", "k", "v", "g", "beta", "y", "ckpt"):
+        assert fwd(lib, s, **{n: None}) == INVALID, n
+    for n in ("q", "k", "v", "g", "beta", "ckpt", "dy", "dq", "dk", "dv", "dg", "dbeta", "ws"):
+        assert bwd(lib, s, **{n: None}) == INVALID, n
+
+
+def test_misaligned_pointers(lib):
+    s = shape()
+    for n in ("q", "k", "v", "g", "beta", "S0", "y", "S_T", "ckpt"):
+        assert fwd(lib, s, **{n: FAKE + 4}) == MISALIGNED, n
+    for n in ("q", "dS_T", "dq", "dS0", "ws"):
+        assert bwd(lib, s, **{n: FAKE + 8}) == MISALIGNED, n
+
+
+def test_workspace_too_small(lib):
+    s = shape()
+    need = lib.gdn_bwd_workspace_bytes(ctypes.byref(s))
+    assert bwd(lib, s, ws_bytes=need - 1) == WS_SMALL
+    assert bwd(lib, s, ws_bytes=0) == WS_SMALL
+
+
+def test_error_strings(lib):
+    texts = {c: lib.gdn_strerror(c).decode() for c in (OK, INVALID, MISALIGNED, UNSUPPORTED, WS_SMALL, CUDA, TIMEOUT)}
+    assert len(set(texts.values())) == len(texts)
+    assert "unknown" in lib.gdn_strerror(42).decode()
+    assert lib.gdn_last_error().decode() == ""
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(ImportError):
+        B.load_library(str(tmp_path / "libgdn.so"))
