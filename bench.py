@@ -1,0 +1,368 @@
+"""Benchmark of the gated delta rule training hot path (forward with checkpoints +
+reverse-time VJP) on GB300, printing one JSON line.
+
+A step is one gdn_fwd + one gdn_bwd over one batch of the workload (every step of the
+hot path). Default workload: the 9B-like linear-attention layer of mlx-lm PR #1217's
+performance table (B=1, Hk=16, Hv=64, Dk=192, Dv=128, T=2048, bf16 inputs, fp32 state,
+weak decay, checkpoint interval 64), synthetic inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle (the only reference this method has) on
+the host cores, on a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs its own copy of the workload (weak scaling; the
+path shards over independent (batch row, kv head) groups with no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdn_synthetic as gs  # noqa: E402
+
+METRIC = "gated-delta fwd+bwd tokens/s (Hv64,Dk192,Dv128,T2048 bf16); % of roofline"
+UNIT = "tokens/s"
+# Peaks. HBM: measured copy bandwidth. FP32 (the bound of this path): derived from
+# unit counts and clock, 152 SMs x 128 FP32 lanes x 2 flop (FFMA) x 2.07 GHz max SM clock.
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# Apple-silicon Metal VJP, fwd+bwd at this exact shape (149.8 ms for T=2048, mlx-lm
+# PR #1217 performance table): another machine's number, quoted as context.
+PAGES_TOKENS_PER_S = 2048 / 0.1498
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant call from one
+# ncu capture, keyed by a hash of the kernel sources it was taken on (None: not measured
+# for the current sources).
+TRAFFIC = {}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs"
+    return 6800.0, "fallback 6.8 TB/s"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gdn_common.cuh", "gdn_fwd.cu", "gdn_bwd.cu", "gdn_api.cu"):
+        h.update(open(os.path.join(ROOT, "gated_delta_rule_22_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def flops_per_step(w, count=28):
+    """Algorithmic FP32 flops: per token and value head, forward 7 Dv Dk (decay 1, S k 2,
+    write 2, S q 2), backward 15 Dv Dk, plus one within-chunk re-computation of the state
+    path (6 Dv Dk) that the checkpoint scheme prescribes: 28 in all (22 without it)."""
+    return float(count) * w.B * w.T * w.Hv * w.Dv * w.Dk
+
+
+def bytes_per_step(w):
+    """Algorithmic HBM bytes of one fwd + bwd: every input and output once, plus the fp32
+    checkpoints written by the forward and read by the backward (scratch excluded)."""
+    e = 2 if w.dtype == "bf16" else 4
+    nc = -(-w.T // w.chunk)
+    qk = w.B * w.T * w.Hk * w.Dk * e
+    vv = w.B * w.T * w.Hv * w.Dv * e
+    gate = w.B * w.T * w.Hv * e
+    st = w.B * w.Hv * w.Dv * w.Dk * 4
+    ck = w.B * w.Hv * nc * w.Dv * w.Dk * 4
+    fwd = 2 * qk + vv + 2 * gate + vv + (st if w.with_S0 else 0) + st + ck
+    bwd = 2 * qk + vv + 2 * gate + ck + vv + (st if w.with_dST else 0) + 2 * qk + vv + 2 * gate + st
+    return float(fwd + bwd)
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- CPU baseline
+def oracle_sample(w, seconds_budget, max_T=None):
+    """Time the float64 oracle (forward + backward, all heads of the workload) on its first
+    T' steps, T' grown until one run takes about `seconds_budget` seconds. Returns
+    (tokens/s, threads, sample text, seconds of the timed run, T')."""
+    import oracle
+    lib = oracle.load()
+    threads = oracle.max_threads(lib)
+    max_T = max_T or w.T
+    Tp = min(16, max_T)
+    while True:
+        inp = gs.make_inputs(w, T=Tp)
+        t0 = time.perf_counter()
+        oracle.fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["S0"], chunk=w.chunk, lib=lib)
+        oracle.bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["dy"], inp["S0"], inp["dS_T"],
+                   chunk=w.chunk, lib=lib)
+        dt = time.perf_counter() - t0
+        if dt >= seconds_budget * 0.5 or Tp >= max_T:
+            break
+        Tp = min(max_T, max(Tp * 2, int(Tp * seconds_budget / max(dt, 1e-3) * 0.9)))
+    sample = (f"oracle fwd+bwd over all {w.B * w.Hv} value heads, first {Tp} of {w.T} steps "
+              f"(cost is linear in T), {threads} OpenMP threads")
+    return w.B * Tp / dt, threads, sample, dt, Tp
+
+
+# ---------------------------------------------------------------------------- runs
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    budget = max(1.0, 150.0 / (args.steps + args.warmup))
+    _, threads, sample, _, Tp = oracle_sample(w, budget)
+    import oracle
+    lib = oracle.load()
+    inp = gs.make_inputs(w, T=Tp)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["S0"], chunk=w.chunk, lib=lib)
+        oracle.bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["dy"], inp["S0"], inp["dS_T"],
+                   chunk=w.chunk, lib=lib)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per = sum(times) / len(times)
+    value = w.B * Tp / per
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, l2="host run"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, l2):
+    return {"workload": f"{w.name}: B={w.B} T={w.T} Hk={w.Hk} Hv={w.Hv} Dk={w.Dk} Dv={w.Dv}, "
+                        f"{w.dtype} inputs, fp32 state, {w.decay} decay, checkpoint interval {w.chunk}",
+            "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "chunk": w.chunk,
+            "input_dtype": w.dtype, "decay": w.decay, "l2": l2}
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    import gated_delta_rule_22_gb300 as gdn
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gdn.load_library()
+
+    inp = gs.make_inputs(w)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    names = ("q", "k", "v", "g", "beta", "dy")
+    t = {n: torch.from_numpy(inp[n]).to(dev).to(dt) for n in names}
+    for n in ("S0", "dS_T"):
+        t[n] = None if inp[n] is None else torch.from_numpy(inp[n]).to(dev)
+    B, T, Hk, Hv, Dk, Dv = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv
+    NC = -(-T // w.chunk)
+    y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
+    S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
+    ckpt = torch.empty((B, Hv, NC, Dv, Dk), dtype=torch.float32, device=dev)
+    grads = {"dq": torch.empty_like(t["q"]), "dk": torch.empty_like(t["k"]), "dv": torch.empty_like(t["v"]),
+             "dg": torch.empty_like(t["g"]), "dbeta": torch.empty_like(t["beta"]),
+             "dS0": torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)}
+    shape = gdn.make_shape(B, T, Hk, Hv, Dk, Dv, w.chunk, 1 if w.dtype == "bf16" else 0)
+    ws = torch.empty(gdn.gdn_bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MiB > 129 MB L2
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"], w.chunk, y=y, S_T=S_T, ckpt=ckpt)
+        gdn.gdn_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], ckpt, t["dy"], t["dS_T"], w.chunk,
+                    workspace=ws, out=grads)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.fill_(i & 0xFF)                       # untimed: evicts L2 between steps
+            ev[i][0].record(stream)
+            gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"], w.chunk, y=y, S_T=S_T, ckpt=ckpt)
+            ev[i][1].record(stream)
+            gdn.gdn_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], ckpt, t["dy"], t["dS_T"], w.chunk,
+                        workspace=ws, out=grads)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    step_ms = fwd_ms + bwd_ms
+    if world > 1:
+        m = torch.tensor([step_ms, fwd_ms, bwd_ms], device=dev)
+        dist.all_reduce(m, op=dist.ReduceOp.MAX)
+        step_ms, fwd_ms, bwd_ms = (float(x) for x in m.tolist())
+    clocks = clk.summary()
+
+    # end to end through the public API: pinned host inputs in, host results out
+    host_in = {n: torch.from_numpy(inp[n]).to(dt).pin_memory() for n in names}
+    host_out = {n: torch.empty(x.shape, dtype=x.dtype).pin_memory() for n, x in
+                list(grads.items()) + [("y", y), ("S_T", S_T)]}
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in host_out.values())
+
+    def e2e_step():
+        d = {n: host_in[n].to(dev, non_blocking=True) for n in names}
+        yy, st, ck = gdn.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], t["S0"], w.chunk)
+        gr = gdn.gdn_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], ck, d["dy"], t["dS_T"], w.chunk, workspace=ws)
+        for n in grads:
+            host_out[n].copy_(gr[n], non_blocking=True)
+        host_out["y"].copy_(yy, non_blocking=True)
+        host_out["S_T"].copy_(st, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        m = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(m, op=dist.ReduceOp.MAX)
+        e2e_ms = float(m.item())
+
+    tokens = w.B * w.T * world
+    value = tokens / (step_ms * 1e-3)
+    hbm_gbs, hbm_src = load_peaks()
+    f28, f22 = flops_per_step(w, 28), flops_per_step(w, 22)
+    bwd_flops = flops_per_step(w, 21)   # backward 15 + one re-computation 6
+    nbytes = bytes_per_step(w)
+    t_roof = max(nbytes / (hbm_gbs * 1e9), f28 / (FP32_PEAK_TFLOPS * 1e12))
+    src_hash = kernel_source_hash()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / PAGES_TOKENS_PER_S if w.name == "linattn-T2048" else None,
+        "vs_baseline_note": "ratio to the Apple-silicon Metal VJP figure on the pages (another machine; context)",
+        "dtype": "f32", "data": "synthetic",
+        "config": config_of(w, l2="flushed between steps by an untimed 256 MiB write"),
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "roofline": {
+            "bound": "alu", "kernel": "gdn_bwd (bwd_kernel + reduce_kernel)",
+            "achieved": bwd_flops / (bwd_ms * 1e-3) / 1e12, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+            "frac": bwd_flops / (bwd_ms * 1e-3) / 1e12 / FP32_PEAK_TFLOPS,
+            "traffic": TRAFFIC.get(src_hash),
+            "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz",
+            "flops_per_launch": bwd_flops,
+        },
+        "roofline_step": {
+            "bound": "alu", "flops_28": f28, "flops_22": f22, "bytes": nbytes,
+            "roofline_ms": t_roof * 1e3, "frac": t_roof * 1e3 / step_ms,
+            "achieved_tflops": f28 / (step_ms * 1e-3) / 1e12,
+            "frac_22": f22 / (step_ms * 1e-3) / 1e12 / FP32_PEAK_TFLOPS,
+            "achieved_gbs": nbytes / (step_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm_gbs, "hbm_peak_source": hbm_src,
+        },
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "kernel_sources": src_hash,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, threads, sample, _, _ = oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="linattn-T2048", choices=sorted(gs.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "ours":
+        args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    w = gs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()
