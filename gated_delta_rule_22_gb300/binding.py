@@ -52,6 +52,8 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_fwd.argtypes = [SP] + [_VP] * 10
     lib.gdn_bwd.restype = ctypes.c_int
     lib.gdn_bwd.argtypes = [SP] + [_VP] * 15 + [ctypes.c_size_t, _VP]
+    lib.gdn_bwd_noalloc.restype = ctypes.c_int
+    lib.gdn_bwd_noalloc.argtypes = [SP] + [_VP] * 15
     lib.gdn_strerror.restype = ctypes.c_char_p
     lib.gdn_strerror.argtypes = [ctypes.c_int]
     lib.gdn_last_error.restype = ctypes.c_char_p

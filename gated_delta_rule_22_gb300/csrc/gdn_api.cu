@@ -3,6 +3,7 @@
 #include "gdn.h"
 #include "gdn_common.cuh"
 
+#include <mutex>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
@@ -149,6 +150,65 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     return cuda_status(gdn::launch_reduce(rp, p.dtype, (cudaStream_t)stream));
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// gdn_bwd_noalloc: gdn_bwd with its scratch in a fixed device array instead of a caller
+// workspace, for callers that cannot allocate device memory.
+namespace {
+
+// The scratch itself: one copy per device, allocated by the CUDA runtime when this
+// library's device code is loaded on that device, kept until the process exits.
+static __device__ __align__(256) unsigned char g_bwd_static_scratch[GDN_BWD_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxDevices];  // device address of g_bwd_static_scratch, per device
+
+// Host code cannot use g_bwd_static_scratch's name as a device address (on the host it
+// names a stand-in). Look the address up once per device, with that device current.
+int static_scratch_address(void **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_status(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_bwd_static_scratch);
+        if (e != cudaSuccess) return cuda_status(e);
+        g_scratch_addr[dev] = addr;
+    }
+    *out = g_scratch_addr[dev];
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                    const void *g, const void *beta, const float *ckpt, const void *dy,
+                    const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta,
+                    float *dS0, void *stream) {
+    Plan p;
+    int rc = make_plan(shape, &p);
+    if (rc != GDN_OK) return rc;
+    const size_t need = workspace_layout(p).total;
+    if (need > GDN_BWD_NOALLOC_SCRATCH_BYTES) return GDN_ERR_SCRATCH_LIMIT;
+    if (!q || !k || !v || !g || !beta || !ckpt || !dy || !dq || !dk || !dv || !dg || !dbeta)
+        return GDN_ERR_INVALID_ARG;
+    const void *all[] = {q, k, v, g, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0};
+    for (const void *ptr : all)
+        if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    g_last_error[0] = '\0';
+    void *scratch = nullptr;
+    rc = static_scratch_address(&scratch);
+    if (rc != GDN_OK) return rc;
+    return gdn_bwd(shape, q, k, v, g, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, scratch,
+                   GDN_BWD_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 const char *gdn_strerror(int code) {
     switch (code) {
         case GDN_OK: return "success";
@@ -158,6 +218,9 @@ const char *gdn_strerror(int code) {
         case GDN_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than gdn_bwd_workspace_bytes()";
         case GDN_ERR_CUDA: return "CUDA runtime error (see gdn_last_error)";
         case GDN_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+        case GDN_ERR_SCRATCH_LIMIT:
+            return "problem needs more scratch than gdn_bwd_noalloc's fixed GDN_BWD_NOALLOC_SCRATCH_BYTES "
+                   "(compare gdn_bwd_workspace_bytes; use gdn_bwd with a workspace instead)";
         default: return "unknown gdn error code";
     }
 }

@@ -20,7 +20,8 @@
  * Conventions shared by every entry point
  *   - All tensor arguments are device pointers to contiguous, row-major arrays,
  *     16-byte aligned, owned by the caller. The library allocates nothing and keeps
- *     no state between calls.
+ *     no state between calls (gdn_bwd_noalloc's fixed scratch array is the one
+ *     exception; see there).
  *   - Layouts: q, k, dq, dk       [B, T, Hk, Dk]
  *              v, y, dy, dv       [B, T, Hv, Dv]
  *              g, beta, dg, dbeta [B, T, Hv]
@@ -76,7 +77,9 @@ enum {
                                        B or Hv > 65535, or a tensor too large to index */
     GDN_ERR_WORKSPACE_TOO_SMALL = -4,
     GDN_ERR_CUDA = -5,              /* the CUDA runtime reported an error (see gdn_last_error) */
-    GDN_ERR_TIMEOUT = -6            /* reserved for bounded device-side waits */
+    GDN_ERR_TIMEOUT = -6,           /* reserved for bounded device-side waits */
+    GDN_ERR_SCRATCH_LIMIT = -7      /* gdn_bwd_noalloc: the problem needs more scratch than
+                                       GDN_BWD_NOALLOC_SCRATCH_BYTES */
 };
 
 /* Bytes of the checkpoint buffer gdn_fwd writes: B*Hv*NC*Dv*Dk*4. 0 for an invalid shape. */
@@ -121,6 +124,36 @@ GDN_API int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const 
                     const void *g, const void *beta, const float *ckpt, const void *dy,
                     const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta,
                     float *dS0, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward without any allocation (no counterpart on the pages: it is a convenience of this
+ * library). Same operation, arguments, results and checks as gdn_bwd, but without the
+ * workspace arguments: the scratch lives in a fixed array of GDN_BWD_NOALLOC_SCRATCH_BYTES
+ * bytes that the library keeps in device memory.
+ *
+ * Who needs it: callers that may not call cudaMalloc or any other allocator -- for example
+ * code hosted inside a runtime that owns all device memory and hands out no allocator,
+ * code that must not add device memory after start-up, or code for which the implicit
+ * device-wide synchronisation of cudaMalloc/cudaFree is not acceptable. They pass only
+ * inputs and outputs.
+ *
+ * Limits and behaviour:
+ *   - The scratch array exists once per GPU that loads the library and stays allocated until
+ *     the process exits (a fixed GDN_BWD_NOALLOC_SCRATCH_BYTES per GPU).
+ *   - Problems whose gdn_bwd_workspace_bytes(shape) exceeds GDN_BWD_NOALLOC_SCRATCH_BYTES are
+ *     rejected with GDN_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *   - The first call on a device (with that device current) looks up the array's device
+ *     address once (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call on a device uses the same array. Nothing in it has to start at zero (each
+ *     scratch value is written before it is read within a call), but two calls that overlap
+ *     on the GPU (different streams, or different host threads) race on it: serialise them.
+ *   - The work is enqueued on `stream`, which must belong to the current device.
+ */
+#define GDN_BWD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+GDN_API int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                            const void *g, const void *beta, const float *ckpt, const void *dy,
+                            const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta,
+                            float *dS0, void *stream);
 
 /* Static description of a return code. */
 GDN_API const char *gdn_strerror(int code);
