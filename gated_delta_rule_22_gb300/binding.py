@@ -58,6 +58,8 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_strerror.argtypes = [ctypes.c_int]
     lib.gdn_last_error.restype = ctypes.c_char_p
     lib.gdn_last_error.argtypes = []
+    lib.gdn_device_status.restype = ctypes.c_int
+    lib.gdn_device_status.argtypes = []
     lib.gdn_version.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
     if path == LIB_PATH:

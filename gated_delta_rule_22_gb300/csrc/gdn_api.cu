@@ -3,6 +3,8 @@
 #include "gdn.h"
 #include "gdn_common.cuh"
 
+#include <cudaTypedefs.h>
+
 #include <mutex>
 #include <stdint.h>
 #include <stdio.h>
@@ -79,6 +81,66 @@ int cuda_status(cudaError_t e) {
     return GDN_ERR_CUDA;
 }
 
+// ---- per-device status word: kernels record GDN_ERR_TIMEOUT there when a bounded wait
+// runs out. Its device address is looked up once per device.
+static __device__ int g_device_status;
+constexpr int kMaxDevs = 256;
+std::mutex g_status_mutex;
+int *g_status_addr[kMaxDevs];
+
+int device_status_address(int **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevs) return cuda_status(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (g_status_addr[dev] == nullptr) {
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_device_status);
+        if (e != cudaSuccess) return cuda_status(e);
+        g_status_addr[dev] = static_cast<int *>(addr);
+    }
+    *out = g_status_addr[dev];
+    return GDN_OK;
+}
+
+// ---- TMA tensor maps of q and k: 4-D [B, T, Hk, Dk], box {Dk, 1, box_t, 1}
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+int make_qk_map(CUtensorMap *map, const void *ptr, const Plan &p, int box_t) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available from the driver");
+        return GDN_ERR_CUDA;
+    }
+    const cuuint64_t e = p.dtype == GDN_F32 ? 4 : 2;
+    const cuuint64_t dims[4] = {(cuuint64_t)p.Dk, (cuuint64_t)p.Hk, (cuuint64_t)p.T, (cuuint64_t)p.B};
+    const cuuint64_t strides[3] = {p.Dk * e, (cuuint64_t)p.Hk * p.Dk * e, (cuuint64_t)p.T * p.Hk * p.Dk * e};
+    const cuuint32_t box[4] = {(cuuint32_t)p.Dk, 1, (cuuint32_t)box_t, 1};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, p.dtype == GDN_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           4, const_cast<void *>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -104,12 +166,17 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     const void *all[] = {q, k, v, g, beta, S0, y, S_T, ckpt};
     for (const void *ptr : all)
         if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    g_last_error[0] = '\0';
     gdn::FwdParams fp;
     fp.q = q; fp.k = k; fp.v = v; fp.g = g; fp.beta = beta; fp.S0 = S0;
     fp.y = y; fp.S_T = S_T; fp.ckpt = ckpt;
     fp.B = p.B; fp.T = p.T; fp.Hk = p.Hk; fp.Hv = p.Hv; fp.Dv = p.Dv; fp.C = p.C; fp.NC = p.NC;
-    g_last_error[0] = '\0';
-    return cuda_status(gdn::launch_fwd(fp, p.Dk, p.dtype, p.warps, (cudaStream_t)stream));
+    rc = device_status_address(&fp.status);
+    if (rc != GDN_OK) return rc;
+    CUtensorMap tm_q, tm_k;
+    if ((rc = make_qk_map(&tm_q, q, p, gdn::kFwdTile)) != GDN_OK) return rc;
+    if ((rc = make_qk_map(&tm_k, k, p, gdn::kFwdTile)) != GDN_OK) return rc;
+    return cuda_status(gdn::launch_fwd(fp, tm_q, tm_k, p.Dk, p.dtype, p.warps, (cudaStream_t)stream));
 }
 
 int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
@@ -226,6 +293,18 @@ const char *gdn_strerror(int code) {
 }
 
 const char *gdn_last_error(void) { return g_last_error; }
+
+int gdn_device_status(void) {
+    int *addr = nullptr;
+    int rc = device_status_address(&addr);
+    if (rc != GDN_OK) return rc;
+    int value = 0;
+    const int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&value, g_device_status, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_status(e);
+    return value;
+}
 
 int gdn_version(void) { return GDN_VERSION; }
 

@@ -2,6 +2,7 @@
 // backward kernels of the gated delta rule library (internal; not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -29,6 +30,7 @@ struct FwdParams {
     const float *S0;
     void *y;
     float *S_T, *ckpt;
+    int *status;            // device status word (bounded-wait timeouts), may be null
     int B, T, Hk, Hv, Dv, C, NC;
 };
 
@@ -91,6 +93,85 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
     return x;
 }
 
+// Same as transpose_reduce, within aligned groups of G lanes (G = 16 or 32): afterwards
+// lane l holds the group sum of value index ((l & (G-1)) >> (log2 G - log2 N)).
+template <int N, int G>
+__device__ __forceinline__ float group_transpose_reduce(float (&v)[N], int lane) {
+    static_assert(N >= 1 && N <= G && (N & (N - 1)) == 0 && (G == 16 || G == 32), "bad sizes");
+    int m = G / 2;
+#pragma unroll
+    for (int n = N; n > 1; n >>= 1, m >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = upper ? v[i] : v[i + n / 2];
+            const float keep = upper ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFullMask, send, m);
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (; m >= 1; m >>= 1) x += __shfl_xor_sync(kFullMask, x, m);
+    return x;
+}
+
+// ---------------------------------------------------------------- TMA and mbarriers
+// Spin limit of every mbarrier wait: far above any legitimate copy latency. A wait that
+// runs out records GDN_ERR_TIMEOUT (-6) in the status word and the CTA stops early.
+constexpr unsigned kWaitLimit = 1u << 24;
+constexpr int kStatusTimeout = -6;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase with the given parity to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
+    const uint32_t a = smem_addr(bar);
+    for (unsigned it = 0; it < kWaitLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// 4-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
+                                            int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void report_status(int *status, int code) {
+    if (status != nullptr) atomicExch(status, code);
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(kFullMask, x, m);
@@ -98,7 +179,9 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 // Launchers (one per kernel family); each returns the cudaError_t of its launch.
-cudaError_t launch_fwd(const FwdParams &p, int Dk, int dtype, int warps, cudaStream_t s);
+// tm_q / tm_k: 4-D tensor maps of q and k ([B, T, Hk, Dk], box {Dk, 1, kFwdTile, 1}).
+cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k, int Dk, int dtype,
+                       int warps, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams &p, int Dk, int dtype, int warps, cudaStream_t s);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
 size_t bwd_smem_bytes(int DK, int nw, int C);

@@ -161,6 +161,12 @@ GDN_API const char *gdn_strerror(int code);
 /* Text of the last CUDA error seen by a gdn_* call on this host thread ("" if none). */
 GDN_API const char *gdn_last_error(void);
 
+/* Reads and clears the status word of the current device. Kernels never spin without a
+ * bound: a wait inside a kernel that runs out records GDN_ERR_TIMEOUT here and the kernel
+ * stops early (its outputs are then incomplete). Returns GDN_OK, GDN_ERR_TIMEOUT, or
+ * GDN_ERR_CUDA if the word cannot be read. Synchronises with the device. */
+GDN_API int gdn_device_status(void);
+
 /* GDN_VERSION of the library that was loaded. */
 GDN_API int gdn_version(void);
 
