@@ -17,8 +17,8 @@ constexpr unsigned kFullMask = 0xffffffffu;
 // (E = Dk/32). Row dot products (S k, S q, Sh k) are therefore sums across the 32
 // lanes; column sums (for dq, dk) are sums over a thread's rows, then over warps.
 constexpr int kRowsPerWarp = 8;
-// Steps per forward staging tile.
-constexpr int kFwdTile = 16;
+// Steps per forward staging tile (a multiple of 16).
+constexpr int kFwdTile = 32;
 // Steps per backward sub-block: states inside a sub-block are re-computed and kept
 // so that the reverse sweep can read S_{t-1} for each step.
 constexpr int kSub = 8;

@@ -128,22 +128,24 @@ __global__ void __launch_bounds__(256, 1)
         tma_load_4d(raw + TS * DK, &tm_q, &bar[0], 0, hk, 0, b);
     }
 
-    // v (4 consecutive rows of one step per thread), g and beta of a tile, one tile ahead
-    const int nquads = TS * (RB / 4);
-    const int q_tt = tid / (RB / 4), q_r = (tid % (RB / 4)) * 4;
-    QuadT vq = Quad<TIn>::zero();
-    float gb = 0.f;
+    // v (groups of 4 consecutive rows of one step), g and beta of a tile, one tile ahead.
+    // A tile holds TS * RB / 4 = (TS / 16) * nthreads quads: QPT per thread.
+    constexpr int QPT = TS / 16;
+    QuadT vq[QPT];
+    float gq = 1.f, bq = 0.f;
     auto prefetch = [&](int i) {
-        const int t = i * TS + q_tt;
-        vq = Quad<TIn>::zero();
-        if (tid < nquads && t < T && row0 + q_r < Dv)
-            vq = *reinterpret_cast<const QuadT *>(v + ((((size_t)b * T + t) * Hv + h) * Dv + row0 + q_r));
+#pragma unroll
+        for (int j = 0; j < QPT; ++j) {
+            const int qd = tid + j * nthreads, q_tt = qd / (RB / 4), q_r = (qd % (RB / 4)) * 4;
+            const int t = i * TS + q_tt;
+            vq[j] = Quad<TIn>::zero();
+            if (t < T && row0 + q_r < Dv)
+                vq[j] = *reinterpret_cast<const QuadT *>(v + ((((size_t)b * T + t) * Hv + h) * Dv + row0 + q_r));
+        }
         if (tid < TS) {
             const int tg = i * TS + tid;
-            gb = tg < T ? to_f32(g[((size_t)b * T + tg) * Hv + h]) : 1.f;
-        } else if (tid < 2 * TS) {
-            const int tg = i * TS + tid - TS;
-            gb = tg < T ? to_f32(beta[((size_t)b * T + tg) * Hv + h]) : 0.f;
+            gq = tg < T ? to_f32(g[((size_t)b * T + tg) * Hv + h]) : 1.f;
+            bq = tg < T ? to_f32(beta[((size_t)b * T + tg) * Hv + h]) : 0.f;
         }
     };
     prefetch(0);
@@ -158,20 +160,24 @@ __global__ void __launch_bounds__(256, 1)
                           ? *reinterpret_cast<const float2 *>(p.S0 + (head * Dv + row) * DK + col + 32 * m)
                           : make_float2(0.f, 0.f);
     }
-    float delta[R];
+    float delta[R];      // delta_t of the thread's 4 rows
+    int to_ckpt = 0;     // steps until the next checkpoint
 
     for (int i = 0; i < ntiles; ++i) {
         const int t0 = i * TS, tl = min(TS, T - t0);
         const int buf = i & 1;
         // stage the prefetched registers; wait for and widen this tile's k and q
-        if (tid < nquads) {
-            float o[4];
-            Quad<TIn>::unpack(vq, o);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) fv[q_tt * RB + q_r + j] = o[j];
+        for (int j = 0; j < QPT; ++j) {
+            const int qd = tid + j * nthreads;
+            float o[4];
+            Quad<TIn>::unpack(vq[j], o);
+            *reinterpret_cast<float4 *>(fv + (qd / (RB / 4)) * RB + (qd % (RB / 4)) * 4) = make_float4(o[0], o[1], o[2], o[3]);
         }
-        if (tid < TS) fg[tid] = gb;
-        else if (tid < 2 * TS) fb[tid - TS] = gb;
+        if (tid < TS) {
+            fg[tid] = gq;
+            fb[tid] = bq;
+        }
         const bool ok = mbar_wait(&bar[buf], (i >> 1) & 1);
         const TIn *rk = raw + (size_t)buf * 2 * TS * DK;
         if (kConv && ok) {
@@ -197,7 +203,6 @@ __global__ void __launch_bounds__(256, 1)
         if (i + 1 < ntiles) prefetch(i + 1);
         const float *kt = kConv ? fk : reinterpret_cast<const float *>(rk);
         const float *qt = kConv ? fq : reinterpret_cast<const float *>(rk) + TS * DK;
-
         // prediction of the tile's first step: delta_{t0} = beta (v - g S k_{t0})
         {
             float part[R];
@@ -217,7 +222,9 @@ __global__ void __launch_bounds__(256, 1)
 
         for (int tt = 0; tt < tl; ++tt) {
             const int t = t0 + tt;
-            if (t % p.C == 0) {
+            if (to_ckpt == 0) {
+                // checkpoint: the state before step t
+                to_ckpt = p.C;
                 float *ck = p.ckpt + (head * p.NC + t / p.C) * (size_t)Dv * DK;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
@@ -229,6 +236,7 @@ __global__ void __launch_bounds__(256, 1)
                     }
                 }
             }
+            --to_ckpt;
             float2 kc[P], qv[P], kn[P];
 #pragma unroll
             for (int m = 0; m < P; ++m) {
