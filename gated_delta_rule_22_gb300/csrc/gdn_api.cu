@@ -19,8 +19,12 @@ struct Plan {
     int warps;     // warps per CTA (both kernels)
     int RB;        // rows of a state per CTA
     int nsplit;    // CTAs per (b, h)
+    int sub;       // backward sub-block length
     int nsub_max;  // sub-blocks per chunk
+    int flush;     // backward steps per column-partial reduction
 };
+
+constexpr size_t kMaxSmem = 232448;   // opt-in shared memory per block on sm_103
 
 constexpr size_t kAlign = 256;
 
@@ -50,7 +54,11 @@ int make_plan(const gdn_shape *s, Plan *p) {
     p->warps = warps;
     p->RB = warps * gdn::kRowsPerWarp;
     p->nsplit = (s->Dv + p->RB - 1) / p->RB;
-    p->nsub_max = (C + gdn::kSub - 1) / gdn::kSub;
+    p->sub = gdn::bwd_sub(s->Dk);
+    p->nsub_max = (C + p->sub - 1) / p->sub;
+    p->flush = p->sub;
+    if (gdn::bwd_smem_bytes(s->Dk, warps, C, p->flush, s->dtype) > kMaxSmem) p->flush = (p->sub + 1) / 2;
+    if (gdn::bwd_smem_bytes(s->Dk, warps, C, p->flush, s->dtype) > kMaxSmem) return GDN_ERR_UNSUPPORTED_SHAPE;
     return GDN_OK;
 }
 
@@ -62,7 +70,7 @@ Workspace workspace_layout(const Plan &p) {
     Workspace w;
     const size_t nqk = (size_t)p.B * p.T * p.Hv * p.nsplit * p.Dk;
     const size_t ngate = (size_t)p.B * p.T * p.Hv * p.nsplit;
-    const size_t nstate = (size_t)p.B * p.Hv * p.nsplit * (p.nsub_max + gdn::kSub - 1) * p.RB * p.Dk;
+    const size_t nstate = (size_t)p.B * p.Hv * p.nsplit * p.nsub_max * p.RB * gdn::bwd_pairs(p.Dk) * 64;
     size_t off = 0;
     w.dq = off; off += round_up(nqk * 4);
     w.dk = off; off += round_up(nqk * 4);
@@ -204,7 +212,7 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     bp.ws_db = reinterpret_cast<float *>(ws + w.db);
     bp.ws_state = reinterpret_cast<float *>(ws + w.state);
     bp.B = p.B; bp.T = p.T; bp.Hk = p.Hk; bp.Hv = p.Hv; bp.Dv = p.Dv; bp.C = p.C; bp.NC = p.NC;
-    bp.nsplit = p.nsplit; bp.nsub_max = p.nsub_max;
+    bp.nsplit = p.nsplit; bp.nsub_max = p.nsub_max; bp.flush = p.flush;
 
     gdn::ReduceParams rp;
     rp.ws_dq = bp.ws_dq; rp.ws_dk = bp.ws_dk; rp.ws_dg = bp.ws_dg; rp.ws_db = bp.ws_db;
@@ -212,7 +220,12 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     rp.B = p.B; rp.T = p.T; rp.Hk = p.Hk; rp.Hv = p.Hv; rp.Dk = p.Dk; rp.nsplit = p.nsplit;
 
     g_last_error[0] = '\0';
-    rc = cuda_status(gdn::launch_bwd(bp, p.Dk, p.dtype, p.warps, (cudaStream_t)stream));
+    rc = device_status_address(&bp.status);
+    if (rc != GDN_OK) return rc;
+    CUtensorMap tm_q, tm_k;
+    if ((rc = make_qk_map(&tm_q, q, p, p.sub + 1)) != GDN_OK) return rc;
+    if ((rc = make_qk_map(&tm_k, k, p, p.sub + 1)) != GDN_OK) return rc;
+    rc = cuda_status(gdn::launch_bwd(bp, tm_q, tm_k, p.Dk, p.dtype, p.warps, (cudaStream_t)stream));
     if (rc != GDN_OK) return rc;
     return cuda_status(gdn::launch_reduce(rp, p.dtype, (cudaStream_t)stream));
 }

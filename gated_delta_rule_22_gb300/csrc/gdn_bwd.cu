@@ -12,314 +12,545 @@
 //     dg_t   = <dA, S_{t-1}>
 //     Sh     = g_t dA                                (= dL/dS_{t-1})
 // Every element of the [Dv, Dk] tile is touched once per step in one fused pass of 8
-// FP32 operations; ddelta needs Sc k_t = Sh k_t + dy_t (q_t . k_t), so the row dot
-// Sh k_t is formed in the previous step's pass (against k_{t-1}) and is the only
-// cross-lane reduction on the serial chain.
+// packed f32x2 operations per two elements; ddelta needs Sc k_t = Sh k_t + dy_t (q_t . k_t),
+// so the row dot Sh k_t is formed in the previous step's pass (against k_{t-1}) and is the
+// only cross-lane reduction on the serial chain.
 //
 // Checkpointing (mlx-lm PR #1217, "What this PR adds": forward-with-save, then a reverse
-// sweep in the same chunked layout): for each chunk, going backwards,
+// sweep in the same chunked layout). Per chunk, going backwards:
 //   pass A  re-runs the chunk from its checkpoint, keeping delta_t and v_t - u_t per row
-//           and step in shared memory and the state at every kSub-th step (sub-block
-//           start) in scratch;
-//   pass B  for each sub-block, going backwards, re-builds the states inside it from its
-//           start state with the kept delta (S <- g S + delta k^T: 2 FP32 ops/element);
-//   core    runs the reverse steps of the sub-block reading S_{t-1} from scratch.
+//           and step in shared memory and the state at the start of every sub-block of
+//           SUB = bwd_sub(Dk) steps in an L2-resident scratch;
+//   per sub-block, going backwards:
+//     pass B  brings the sub-block's start state back (1-D TMA bulk copy, prefetched one
+//             sub-block ahead) and re-builds the states inside it with the kept delta
+//             (S <- g S + delta k^T), writing them to tensor memory (TMEM); the last one
+//             stays in registers;
+//     core    runs the reverse steps, each reading S_{t-1} from TMEM one step ahead.
 //
-// Reductions: a CTA owns RB rows of one (b, h). Column sums (dq, dk) are summed over a
-// thread's rows in registers, over the CTA's warps in shared memory in ascending warp
-// order, and written per (b, t, h, row split) to fp32 scratch; dg and dbeta likewise.
-// reduce_kernel then adds the row splits (ascending) and the value heads of each kv
-// head (ascending) and rounds to the output type. No atomics anywhere.
+// Layout: a CTA owns RB = 8 * warps rows of one (b, h); a warp owns 8 rows; lane l holds
+// the column pairs (l + 64m, l + 32 + 64m) of each row, so row dot products are 32-lane
+// reductions and a warp's column sums are complete per lane. Column sums (dq, dk) and dg
+// are reduced over the warps in shared memory in ascending warp order and written per
+// (b, t, h, row split) to fp32 scratch; reduce_kernel adds the row splits (ascending) and
+// the value heads of each kv head (ascending). No atomics.
+//
+// Staging: k and q tiles of SUB + 1 steps arrive by TMA (tiled tensor maps, one tile
+// ahead, two buffers); v or dy, g and beta are loaded one tile ahead into registers.
 #include "gdn_common.cuh"
 
 namespace gdn {
 
+namespace {
+
+template <typename T>
+struct IsF32B { static constexpr bool value = false; };
+template <>
+struct IsF32B<float> { static constexpr bool value = true; };
+
+template <typename T>
+struct QuadB;
+template <>
+struct QuadB<float> {
+    using type = float4;
+    static __device__ __forceinline__ type zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+    static __device__ __forceinline__ float4 unpack(const type &q) { return q; }
+};
+template <>
+struct QuadB<__nv_bfloat16> {
+    using type = uint2;
+    static __device__ __forceinline__ type zero() { return make_uint2(0u, 0u); }
+    static __device__ __forceinline__ float4 unpack(const type &q) {
+        return make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
+                           __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
+    }
+};
+
+__host__ __device__ inline size_t align_upb(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory layout of bwd_kernel (byte offsets from a 128-byte aligned base).
+struct BwdSmem {
+    size_t raw, kf, qf, scb, dl, vm, xs, dd, cp, gp, gs, bs, kq, dd2, bar, tslot, total;
+    __host__ __device__ BwdSmem(int DK, int RB, int nw, int esize, int C, int F) {
+        const int P2 = bwd_pairs(DK), SUB = bwd_sub(DK), TR = SUB + 1;
+        size_t o = 0;
+        raw = o; o += align_upb((size_t)2 * 2 * TR * DK * esize, 128);   // [buf][k|q][TR][DK], input type
+        kf = o; o += (size_t)TR * P2 * 64 * 4;                             // fp32, pair layout
+        qf = o; o += (size_t)TR * P2 * 64 * 4;
+        o = align_upb(o, 128);
+        scb = o; o += (size_t)RB * P2 * 64 * 4;                            // incoming sub-block start state
+        dl = o; o += (size_t)C * RB * 4;
+        vm = o; o += (size_t)C * RB * 4;
+        xs = o; o += (size_t)SUB * RB * 4;                                  // v (pass A) or dy (reverse)
+        dd = o; o += (size_t)SUB * RB * 4;
+        cp = o; o += (size_t)F * nw * 2 * P2 * 64 * 4;
+        gp = o; o += (size_t)F * nw * 4;
+        gs = o; o += SUB * 4;
+        bs = o; o += SUB * 4;
+        kq = o; o += SUB * 4;
+        dd2 = o; o += SUB * 4;
+        bar = align_upb(o, 8); o = bar + 3 * 8;
+        tslot = o; o += 16;
+        total = o + 128;
+    }
+};
+
+struct TileRef {
+    int kind;  // 0 = pass A, 1 = reverse, -1 = none
+    int c, m;
+};
+
+}  // namespace
+
 template <int E, typename TIn>
-__global__ void __launch_bounds__(256, 1) bwd_kernel(BwdParams p) {
-    constexpr int RW = kRowsPerWarp;
+__global__ void __launch_bounds__(256, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, BwdParams p) {
+    constexpr int R = kBwdRowsPerWarp;
     constexpr int DK = 32 * E;
-    constexpr int SUB = kSub;
-    const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int RB = nw * RW;
+    constexpr int P2 = bwd_pairs(DK);
+    constexpr int SUB = bwd_sub(DK);
+    constexpr int TR = SUB + 1;
+    constexpr int NPAIR = R * P2;         // float2 pairs of one state per thread
+    constexpr int SW = 2 * NPAIR;         // TMEM columns of one state per thread
+    constexpr bool kConv = !IsF32B<TIn>::value;
+    using QuadT = typename QuadB<TIn>::type;
+    static_assert(NPAIR % 8 == 0, "state must be a whole number of 16-column TMEM chunks");
+    static_assert((SUB - 1) * SW <= 256, "sub-block states exceed the TMEM share");
+
+    const int tid = threadIdx.x, nthreads = blockDim.x, nw = nthreads >> 5;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int RB = nw * R;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int row0 = split * RB;
-    const int rep = p.Hv / p.Hk, hk = h / rep;
-    const int T = p.T, Dv = p.Dv, C = p.C, Hv = p.Hv, nsplit = p.nsplit;
-    const int wrow = warp * RW;
-    const int my_row = lane >> 2;   // row held by this lane after a transpose_reduce<RW>
+    const int row0 = split * RB, hk = h / (p.Hv / p.Hk);
+    const int T = p.T, Dv = p.Dv, C = p.C, Hv = p.Hv, nsplit = p.nsplit, F = p.flush;
+    const int wrow = warp * R;
+    const int my_row = lane >> 2;         // row held by this lane after a transpose reduction of 8
 
-    extern __shared__ float smem[];
-    float *dl_s = smem;                      // [C][RB]   delta_t per row (pass A)
-    float *vm_s = dl_s + C * RB;             // [C][RB]   v_t - u_t per row (pass A)
-    float *k_s = vm_s + C * RB;              // [SUB+1][DK]
-    float *q_s = k_s + (SUB + 1) * DK;       // [SUB][DK]
-    float *v_s = q_s + SUB * DK;             // [SUB][RB]  (pass A)
-    float *dy_s = v_s + SUB * RB;            // [SUB][RB]
-    float *dd_s = dy_s + SUB * RB;           // [SUB][RB]  ddelta per row
-    float *cp_s = dd_s + SUB * RB;           // [SUB][nw][2][DK] per-warp column partials (dk, dq)
-    float *gp_s = cp_s + SUB * nw * 2 * DK;  // [SUB][nw] per-warp dg partials
-    float *g_s = gp_s + SUB * nw;            // [SUB]
-    float *b_s = g_s + SUB;                  // [SUB]
-    float *kq_s = b_s + SUB;                 // [SUB] k_t . q_t
-    float *dd2_s = kq_s + SUB;               // [SUB] delta_t . dy_t over the CTA's rows
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(align_upb(reinterpret_cast<size_t>(smem_raw), 128));
+    const BwdSmem L(DK, RB, nw, (int)sizeof(TIn), C, F);
+    TIn *raw = reinterpret_cast<TIn *>(base + L.raw);
+    float *kf = reinterpret_cast<float *>(base + L.kf);
+    float *qf = reinterpret_cast<float *>(base + L.qf);
+    float *scb = reinterpret_cast<float *>(base + L.scb);
+    float *dl_s = reinterpret_cast<float *>(base + L.dl);
+    float *vm_s = reinterpret_cast<float *>(base + L.vm);
+    float *xs = reinterpret_cast<float *>(base + L.xs);
+    float *dd_s = reinterpret_cast<float *>(base + L.dd);
+    float *cp_s = reinterpret_cast<float *>(base + L.cp);
+    float *gp_s = reinterpret_cast<float *>(base + L.gp);
+    float *g_s = reinterpret_cast<float *>(base + L.gs);
+    float *b_s = reinterpret_cast<float *>(base + L.bs);
+    float *kq_s = reinterpret_cast<float *>(base + L.kq);
+    float *dd2_s = reinterpret_cast<float *>(base + L.dd2);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);   // [0], [1]: tiles; [2]: sub-block state
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
-    const TIn *q = static_cast<const TIn *>(p.q);
-    const TIn *k = static_cast<const TIn *>(p.k);
     const TIn *v = static_cast<const TIn *>(p.v);
     const TIn *g = static_cast<const TIn *>(p.g);
     const TIn *beta = static_cast<const TIn *>(p.beta);
     const TIn *dy = static_cast<const TIn *>(p.dy);
+    const TIn *k = static_cast<const TIn *>(p.k);
     TIn *dv = static_cast<TIn *>(p.dv);
 
-    const size_t state_off = ((size_t)b * Hv + h) * Dv;
-    const size_t cta = ((size_t)b * Hv + h) * nsplit + split;
-    const int nslots = p.nsub_max + SUB - 1;
-    float *scratch = p.ws_state + cta * nslots * (size_t)RB * DK;
-    // element (r, e) of this thread inside a scratch state slot is my_off + r*DK + 32*e
-    const int my_off = wrow * DK + lane;
+    const size_t head = (size_t)b * Hv + h;
+    const size_t cta = head * nsplit + split;
+    const size_t slot_floats = (size_t)RB * P2 * 64;
+    float *scratch = p.ws_state + cta * (size_t)p.nsub_max * slot_floats;
+    const int pair_off = wrow * P2 * 64 + 2 * lane;   // this thread's pair (r, m) is at + (r * P2 + m) * 64
 
-    float Sh[RW][E];
+    // ---- set-up: barriers, tensor memory
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * 256);
+
+    auto nsub_of = [&](int c) {
+        const int len = min(C, T - c * C);
+        return (len + SUB - 1) / SUB;
+    };
+    auto tile_after = [&](TileRef t) -> TileRef {
+        if (t.kind == 0) {
+            if (t.m + 1 < nsub_of(t.c)) return {0, t.c, t.m + 1};
+            return {1, t.c, nsub_of(t.c) - 1};
+        }
+        if (t.m > 0) return {1, t.c, t.m - 1};
+        if (t.c > 0) return {0, t.c - 1, 0};
+        return {-1, 0, 0};
+    };
+
+    // register prefetch of one tile's per-row input (v for pass A, dy for reverse), g, beta
+    const int nquads = SUB * (RB / 4);
+    QuadT xq = QuadB<TIn>::zero();
+    float gq = 1.f, bq = 0.f;
+    auto issue_tile = [&](TileRef t, int buf) {
+        const int s0 = t.c * C + t.m * SUB;
+        const int slen = min(SUB, min(t.c * C + C, T) - s0);
+        if (tid == 0) {
+            fence_proxy_async();
+            TIn *dst = raw + (size_t)buf * 2 * TR * DK;
+            mbar_expect_tx(&bar[buf], (t.kind == 1 ? 2u : 1u) * TR * DK * (unsigned)sizeof(TIn));
+            tma_load_4d(dst, &tm_k, &bar[buf], 0, hk, s0 - 1, b);
+            if (t.kind == 1) tma_load_4d(dst + TR * DK, &tm_q, &bar[buf], 0, hk, s0 - 1, b);
+        }
+        const TIn *x = t.kind == 1 ? dy : v;
+        xq = QuadB<TIn>::zero();
+        if (tid < nquads) {
+            const int j = tid / (RB / 4), r4 = (tid % (RB / 4)) * 4;
+            if (j < slen && row0 + r4 < Dv)
+                xq = *reinterpret_cast<const QuadT *>(x + ((((size_t)b * T + s0 + j) * Hv + h) * Dv + row0 + r4));
+        }
+        if (tid < SUB) {
+            gq = tid < slen ? to_f32(g[((size_t)b * T + s0 + tid) * Hv + h]) : 1.f;
+            bq = tid < slen ? to_f32(beta[((size_t)b * T + s0 + tid) * Hv + h]) : 0.f;
+        }
+    };
+    // Consume the tile in `buf`: stage the prefetched registers, wait for and widen the TMA
+    // rows into the pair layout, then start the next tile. Returns false on a timeout.
+    unsigned tile_phase0 = 0u, tile_phase1 = 0u;
+    auto begin_tile = [&](TileRef t, int buf) -> bool {
+        __syncthreads();   // the previous tile's staging buffers are no longer read
+        if (tid < nquads) {
+            const float4 f = QuadB<TIn>::unpack(xq);
+            *reinterpret_cast<float4 *>(xs + (tid / (RB / 4)) * RB + (tid % (RB / 4)) * 4) = f;
+        }
+        if (tid < SUB) {
+            g_s[tid] = gq;
+            b_s[tid] = bq;
+        }
+        const bool ok = mbar_wait(&bar[buf], buf ? tile_phase1 : tile_phase0);
+        if (buf) tile_phase1 ^= 1u;
+        else tile_phase0 ^= 1u;
+        if (ok) {
+            const TIn *rk = raw + (size_t)buf * 2 * TR * DK;
+            const int nrows = t.kind == 1 ? 2 * TR : TR;   // k rows, then q rows
+            for (int i = tid; i < nrows * P2 * 64; i += nthreads) {
+                const int row = i / (P2 * 64), rem = i - row * (P2 * 64);
+                const int pr = rem >> 1, x = rem & 1, m = pr >> 5, l = pr & 31;
+                const int col = l + 32 * (2 * m + x);
+                const float val = col < DK ? to_f32(rk[row * DK + col]) : 0.f;
+                if (row < TR) kf[row * P2 * 64 + rem] = val;
+                else qf[(row - TR) * P2 * 64 + rem] = val;
+            }
+        }
+        if (__syncthreads_or(!ok)) return false;
+        const TileRef nt = tile_after(t);
+        if (nt.kind >= 0) issue_tile(nt, buf ^ 1);
+        return true;
+    };
+    auto load_pair = [&](const float *rowbase, int m) {
+        return *reinterpret_cast<const float2 *>(rowbase + m * 64 + 2 * lane);
+    };
+
+    // ---- adjoint state Sh from dS_T, and its first row dot with k_{T-1}
+    float2 Sh[R][P2];
 #pragma unroll
-    for (int r = 0; r < RW; ++r) {
+    for (int r = 0; r < R; ++r) {
         const int row = row0 + wrow + r;
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-            Sh[r][e] = (p.dS_T != nullptr && row < Dv) ? p.dS_T[(state_off + row) * DK + lane + 32 * e] : 0.f;
-    }
-    float p_own;  // (Sh k_t) of row my_row for the next reverse step t
-    {
-        float part[RW];
-#pragma unroll
-        for (int r = 0; r < RW; ++r) part[r] = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const float kk = to_f32(k[(((size_t)b * T + T - 1) * p.Hk + hk) * DK + lane + 32 * e]);
-#pragma unroll
-            for (int r = 0; r < RW; ++r) part[r] = fmaf(Sh[r][e], kk, part[r]);
+        for (int m = 0; m < P2; ++m) {
+            float2 e = make_float2(0.f, 0.f);
+            if (p.dS_T != nullptr && row < Dv) {
+                const float *src = p.dS_T + (head * Dv + row) * DK;
+                e.x = src[lane + 64 * m];
+                if (lane + 64 * m + 32 < DK) e.y = src[lane + 64 * m + 32];
+            }
+            Sh[r][m] = e;
         }
-        p_own = transpose_reduce<RW>(part, lane);
+    }
+    float p_own;   // Sh . k_t of row my_row, for the next reverse step t
+    {
+        float part[R];
+        float2 kk[P2];
+#pragma unroll
+        for (int m = 0; m < P2; ++m) {
+            const TIn *src = k + (((size_t)b * T + T - 1) * p.Hk + hk) * DK;
+            kk[m].x = to_f32(src[lane + 64 * m]);
+            kk[m].y = lane + 64 * m + 32 < DK ? to_f32(src[lane + 64 * m + 32]) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int m = 0; m < P2; ++m) acc = __ffma2_rn(Sh[r][m], kk[m], acc);
+            part[r] = acc.x + acc.y;
+        }
+        p_own = group_transpose_reduce<R, 32>(part, lane);
     }
 
-    for (int c = p.NC - 1; c >= 0; --c) {
+    bool failed = false;
+    unsigned scb_phase = 0u;
+    int buf = 0;
+    issue_tile(TileRef{0, p.NC - 1, 0}, 0);
+
+    for (int c = p.NC - 1; c >= 0 && !failed; --c) {
         const int t0 = c * C, len = min(C, T - t0), nsub = (len + SUB - 1) / SUB;
 
-        // ---------------- pass A: forward through the chunk from its checkpoint ----------------
-        float S[RW][E];
+        // ============ pass A: forward through the chunk from its checkpoint ============
+        float2 S[R][P2];
         {
-            const float *ck = p.ckpt + ((state_off * p.NC) + (size_t)c * Dv) * DK;
+            const float *ck = p.ckpt + (head * p.NC + c) * (size_t)Dv * DK;
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
+            for (int r = 0; r < R; ++r) {
                 const int row = row0 + wrow + r;
 #pragma unroll
-                for (int e = 0; e < E; ++e) S[r][e] = row < Dv ? ck[(size_t)row * DK + lane + 32 * e] : 0.f;
+                for (int m = 0; m < P2; ++m) {
+                    float2 e = make_float2(0.f, 0.f);
+                    if (row < Dv) {
+                        e.x = ck[(size_t)row * DK + lane + 64 * m];
+                        if (lane + 64 * m + 32 < DK) e.y = ck[(size_t)row * DK + lane + 64 * m + 32];
+                    }
+                    S[r][m] = e;
+                }
             }
         }
         for (int m = 0; m < nsub; ++m) {
             const int s0 = t0 + m * SUB, slen = min(SUB, t0 + len - s0);
-            float *slot = scratch + (size_t)m * RB * DK + my_off;
+            if (!begin_tile(TileRef{0, c, m}, buf)) { failed = true; break; }
+            float *slot = scratch + (size_t)m * slot_floats + pair_off;
 #pragma unroll
-            for (int r = 0; r < RW; ++r)
+            for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int e = 0; e < E; ++e) slot[r * DK + 32 * e] = S[r][e];
-            __syncthreads();
-            for (int i = threadIdx.x; i < slen * DK; i += blockDim.x) {
-                const int j = i / DK, col = i - j * DK;
-                k_s[i] = to_f32(k[(((size_t)b * T + s0 + j) * p.Hk + hk) * DK + col]);
-            }
-            for (int i = threadIdx.x; i < slen * RB; i += blockDim.x) {
-                const int j = i / RB, rr = i - j * RB, row = row0 + rr;
-                v_s[i] = row < Dv ? to_f32(v[(((size_t)b * T + s0 + j) * Hv + h) * Dv + row]) : 0.f;
-            }
-            for (int i = threadIdx.x; i < slen; i += blockDim.x) {
-                g_s[i] = to_f32(g[((size_t)b * T + s0 + i) * Hv + h]);
-                b_s[i] = to_f32(beta[((size_t)b * T + s0 + i) * Hv + h]);
-            }
-            __syncthreads();
+                for (int mm = 0; mm < P2; ++mm) *reinterpret_cast<float2 *>(slot + (r * P2 + mm) * 64) = S[r][mm];
             for (int j = 0; j < slen; ++j) {
-                float kv[E];
+                float2 kv[P2];
 #pragma unroll
-                for (int e = 0; e < E; ++e) kv[e] = k_s[j * DK + lane + 32 * e];
-                float part[RW];
+                for (int mm = 0; mm < P2; ++mm) kv[mm] = load_pair(kf + (j + 1) * P2 * 64, mm);
+                float part[R];
 #pragma unroll
-                for (int r = 0; r < RW; ++r) {
-                    float a = 0.f;
+                for (int r = 0; r < R; ++r) {
+                    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) a = fmaf(S[r][e], kv[e], a);
-                    part[r] = a;
+                    for (int mm = 0; mm < P2; ++mm) acc = __ffma2_rn(S[r][mm], kv[mm], acc);
+                    part[r] = acc.x + acc.y;
                 }
-                const float a = transpose_reduce<RW>(part, lane);
+                const float a = group_transpose_reduce<R, 32>(part, lane);
                 const float gt = g_s[j], bt = b_s[j];
-                const float vm = v_s[j * RB + wrow + my_row] - gt * a;
-                const float dl = bt * vm;
+                const float vmv = xs[j * RB + wrow + my_row] - gt * a;
+                const float dlv = bt * vmv;
                 if ((lane & 3) == 0) {
-                    dl_s[(s0 - t0 + j) * RB + wrow + my_row] = dl;
-                    vm_s[(s0 - t0 + j) * RB + wrow + my_row] = vm;
+                    dl_s[(s0 - t0 + j) * RB + wrow + my_row] = dlv;
+                    vm_s[(s0 - t0 + j) * RB + wrow + my_row] = vmv;
                 }
-                float d[RW];
+                const float2 gg = make_float2(gt, gt);
 #pragma unroll
-                for (int r = 0; r < RW; ++r) d[r] = __shfl_sync(kFullMask, dl, 4 * r);
+                for (int r = 0; r < R; ++r) {
+                    const float d = __shfl_sync(kFullMask, dlv, 4 * r);
+                    const float2 dd = make_float2(d, d);
 #pragma unroll
-                for (int r = 0; r < RW; ++r)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) S[r][e] = fmaf(d[r], kv[e], gt * S[r][e]);
+                    for (int mm = 0; mm < P2; ++mm) S[r][mm] = __ffma2_rn(dd, kv[mm], __fmul2_rn(gg, S[r][mm]));
+                }
             }
+            buf ^= 1;
         }
+        if (failed) break;
+        fence_proxy_async_global();   // the sub-block start states are read back by TMA
 
-        // ---------------- reverse sweep over the chunk's sub-blocks ----------------
+        // ============ reverse sweep over the chunk's sub-blocks ============
         for (int m = nsub - 1; m >= 0; --m) {
             const int s0 = t0 + m * SUB, slen = min(SUB, t0 + len - s0);
-            __syncthreads();
-            for (int i = threadIdx.x; i < (slen + 1) * DK; i += blockDim.x) {
-                const int j = i / DK, col = i - j * DK, t = s0 - 1 + j;
-                k_s[i] = t >= 0 ? to_f32(k[(((size_t)b * T + t) * p.Hk + hk) * DK + col]) : 0.f;
+            if (!begin_tile(TileRef{1, c, m}, buf)) { failed = true; break; }
+            if (m == nsub - 1 && tid == 0) {
+                mbar_expect_tx(&bar[2], (unsigned)(slot_floats * 4));
+                bulk_load(scb, scratch + (size_t)m * slot_floats, (unsigned)(slot_floats * 4), &bar[2]);
             }
-            for (int i = threadIdx.x; i < slen * DK; i += blockDim.x) {
-                const int j = i / DK, col = i - j * DK;
-                q_s[i] = to_f32(q[(((size_t)b * T + s0 + j) * p.Hk + hk) * DK + col]);
-            }
-            for (int i = threadIdx.x; i < slen * RB; i += blockDim.x) {
-                const int j = i / RB, rr = i - j * RB, row = row0 + rr;
-                dy_s[i] = row < Dv ? to_f32(dy[(((size_t)b * T + s0 + j) * Hv + h) * Dv + row]) : 0.f;
-            }
-            for (int i = threadIdx.x; i < slen; i += blockDim.x) {
-                g_s[i] = to_f32(g[((size_t)b * T + s0 + i) * Hv + h]);
-                b_s[i] = to_f32(beta[((size_t)b * T + s0 + i) * Hv + h]);
-            }
-            __syncthreads();
+            // per-step k_t . q_t
             for (int j = warp; j < slen; j += nw) {
                 float a = 0.f;
-                for (int col = lane; col < DK; col += 32) a = fmaf(k_s[(j + 1) * DK + col], q_s[j * DK + col], a);
+                for (int i = lane; i < P2 * 64; i += 32) a = fmaf(kf[(j + 1) * P2 * 64 + i], qf[(j + 1) * P2 * 64 + i], a);
                 a = warp_sum(a);
                 if (lane == 0) kq_s[j] = a;
             }
+            // the sub-block's start state
+            const bool ok = mbar_wait(&bar[2], scb_phase);
+            scb_phase ^= 1u;
+            float2 Sa[R][P2];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int mm = 0; mm < P2; ++mm) Sa[r][mm] = *reinterpret_cast<const float2 *>(scb + pair_off + (r * P2 + mm) * 64);
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+            if (m > 0 && tid == 0) {
+                fence_proxy_async();
+                mbar_expect_tx(&bar[2], (unsigned)(slot_floats * 4));
+                bulk_load(scb, scratch + (size_t)(m - 1) * slot_floats, (unsigned)(slot_floats * 4), &bar[2]);
+            }
 
-            // pass B: states before steps s0+1 .. s0+slen-1, from the sub-block's start state
-            {
-                float S2[RW][E];
-                const float *slot0 = scratch + (size_t)m * RB * DK + my_off;
+            // ---- pass B: states before steps s0 .. s0+slen-2 to TMEM; the last stays in Sa
+            for (int j = 0; j + 1 < slen; ++j) {
+                const uint32_t ts = tmem + (uint32_t)(j * SW);
 #pragma unroll
-                for (int r = 0; r < RW; ++r)
+                for (int q = 0; q < NPAIR / 8; ++q) {
+                    float2 chunk[8];
 #pragma unroll
-                    for (int e = 0; e < E; ++e) S2[r][e] = slot0[r * DK + 32 * e];
-                for (int j = 0; j + 1 < slen; ++j) {
-                    const float gt = g_s[j];
-                    float *slot = scratch + (size_t)(p.nsub_max + j) * RB * DK + my_off;
+                    for (int i = 0; i < 8; ++i) chunk[i] = Sa[(q * 8 + i) / P2][(q * 8 + i) % P2];
+                    tmem_st16(ts + q * 16, chunk);
+                }
+                const float gt = g_s[j];
+                const float2 gg = make_float2(gt, gt);
+                float2 kv[P2];
 #pragma unroll
-                    for (int r = 0; r < RW; ++r) {
-                        const float d = dl_s[(s0 - t0 + j) * RB + wrow + r];
+                for (int mm = 0; mm < P2; ++mm) kv[mm] = load_pair(kf + (j + 1) * P2 * 64, mm);
 #pragma unroll
-                        for (int e = 0; e < E; ++e) {
-                            S2[r][e] = fmaf(d, k_s[(j + 1) * DK + lane + 32 * e], gt * S2[r][e]);
-                            slot[r * DK + 32 * e] = S2[r][e];
-                        }
-                    }
+                for (int r = 0; r < R; ++r) {
+                    const float d = dl_s[(s0 - t0 + j) * RB + wrow + r];
+                    const float2 dd = make_float2(d, d);
+#pragma unroll
+                    for (int mm = 0; mm < P2; ++mm) Sa[r][mm] = __ffma2_rn(dd, kv[mm], __fmul2_rn(gg, Sa[r][mm]));
                 }
             }
-            __syncthreads();
+            tmem_wait_st();
 
-            // core: reverse steps of the sub-block
-            for (int j = slen - 1; j >= 0; --j) {
-                const float *sp = scratch + (size_t)(j == 0 ? m : p.nsub_max + j - 1) * RB * DK + my_off;
+            // ---- core: reverse steps j = slen-1 .. 0, S_{t-1} in Sa / Sb alternately
+            float2 Sb[R][P2];
+            auto tmem_load_state = [&](int j, float2 (&dst)[R][P2]) {
+                const uint32_t ts = tmem + (uint32_t)(j * SW);
+#pragma unroll
+                for (int q = 0; q < NPAIR / 8; ++q) {
+                    float2 chunk[8];
+                    tmem_ld16(ts + q * 16, chunk);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) dst[(q * 8 + i) / P2][(q * 8 + i) % P2] = chunk[i];
+                }
+            };
+            auto flush = [&](int jlo, int jhi) {   // steps jlo .. jhi of this sub-block (jhi >= jlo)
+                __syncthreads();
+                for (int j = jlo + warp; j <= jhi; j += nw) {
+                    const int t = s0 + j, tc = t - t0, jf = (slen - 1 - j) % F;
+                    float s1 = 0.f, s2 = 0.f;
+                    for (int rr = lane; rr < RB; rr += 32) {
+                        s1 = fmaf(dl_s[tc * RB + rr], xs[j * RB + rr], s1);
+                        s2 = fmaf(dd_s[j * RB + rr], vm_s[tc * RB + rr], s2);
+                    }
+                    s1 = warp_sum(s1);
+                    s2 = warp_sum(s2);
+                    if (lane == 0) {
+                        float dgs = 0.f;
+                        for (int w = 0; w < nw; ++w) dgs += gp_s[jf * nw + w];
+                        const size_t o = (((size_t)b * T + t) * Hv + h) * nsplit + split;
+                        p.ws_dg[o] = dgs;
+                        p.ws_db[o] = s2;
+                        dd2_s[j] = s1;
+                    }
+                }
+                __syncthreads();
+                for (int i = tid; i < (jhi - jlo + 1) * DK; i += nthreads) {
+                    const int j = jlo + i / DK, col = i % DK, t = s0 + j, jf = (slen - 1 - j) % F;
+                    const int e = col >> 5, l = col & 31;
+                    const int pidx = ((e >> 1) * 32 + l) * 2 + (e & 1);   // pair-layout index of `col`
+                    float a = 0.f, bq2 = 0.f;
+                    for (int w = 0; w < nw; ++w) {
+                        a += cp_s[((size_t)(jf * nw + w) * 2) * P2 * 64 + pidx];
+                        bq2 += cp_s[((size_t)(jf * nw + w) * 2 + 1) * P2 * 64 + pidx];
+                    }
+                    bq2 = fmaf(kf[(j + 1) * P2 * 64 + pidx], dd2_s[j], bq2);
+                    const size_t o = ((((size_t)b * T + t) * Hv + h) * nsplit + split) * DK + col;
+                    p.ws_dk[o] = a;
+                    p.ws_dq[o] = bq2;
+                }
+                for (int i = tid; i < (jhi - jlo + 1) * RB; i += nthreads) {
+                    const int j = jlo + i / RB, rr = i % RB, row = row0 + rr;
+                    if (row < Dv)
+                        dv[(((size_t)b * T + s0 + j) * Hv + h) * Dv + row] = from_f32<TIn>(b_s[j] * dd_s[j * RB + rr]);
+                }
+                __syncthreads();
+            };
+            auto core_step = [&](int j, const float2 (&Sp)[R][P2]) {
+                const int tc = s0 + j - t0, jf = (slen - 1 - j) % F;
                 const float gt = g_s[j], bt = b_s[j];
-                const float dyo = dy_s[j * RB + wrow + my_row];
+                const float dyo = xs[j * RB + wrow + my_row];
                 const float ddo = p_own + dyo * kq_s[j];
                 const float duo = -bt * ddo;
                 if ((lane & 3) == 0) dd_s[j * RB + wrow + my_row] = ddo;
-                float kt[E], qt[E], kp[E];
+                float2 kt[P2], qt[P2], kp[P2];
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    kt[e] = k_s[(j + 1) * DK + lane + 32 * e];
-                    qt[e] = q_s[j * DK + lane + 32 * e];
-                    kp[e] = k_s[j * DK + lane + 32 * e];
+                for (int mm = 0; mm < P2; ++mm) {
+                    kt[mm] = load_pair(kf + (j + 1) * P2 * 64, mm);
+                    qt[mm] = load_pair(qf + (j + 1) * P2 * 64, mm);
+                    kp[mm] = load_pair(kf + j * P2 * 64, mm);
                 }
-                float dkacc[E], dqacc[E], pn[RW];
+                float2 dkacc[P2], dqacc[P2];
 #pragma unroll
-                for (int e = 0; e < E; ++e) dkacc[e] = dqacc[e] = 0.f;
-                float dgacc = 0.f;
-                const int tc = s0 + j - t0;
+                for (int mm = 0; mm < P2; ++mm) dkacc[mm] = dqacc[mm] = make_float2(0.f, 0.f);
+                float2 dg2 = make_float2(0.f, 0.f);
+                float pn[R];
+                const float2 gg = make_float2(gt, gt);
 #pragma unroll
-                for (int r = 0; r < RW; ++r) {
+                for (int r = 0; r < R; ++r) {
                     const float du = __shfl_sync(kFullMask, duo, 4 * r);
-                    const float dyr = dy_s[j * RB + wrow + r];
+                    const float dyr = xs[j * RB + wrow + r];
                     const float dr = dl_s[tc * RB + wrow + r];
-                    const float gdu = gt * du, gdy = gt * dyr;
-                    float acc = 0.f;
+                    const float2 du2 = make_float2(du, du), dy2 = make_float2(dyr, dyr), dr2 = make_float2(dr, dr);
+                    const float2 gdu2 = make_float2(gt * du, gt * du), gdy2 = make_float2(gt * dyr, gt * dyr);
+                    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float spe = sp[r * DK + 32 * e];
-                        const float sc = fmaf(dyr, qt[e], Sh[r][e]);
-                        dkacc[e] = fmaf(sc, dr, dkacc[e]);
-                        const float dA = fmaf(du, kt[e], sc);
-                        dgacc = fmaf(dA, spe, dgacc);
-                        dkacc[e] = fmaf(spe, gdu, dkacc[e]);
-                        dqacc[e] = fmaf(spe, gdy, dqacc[e]);
-                        const float shn = gt * dA;
-                        Sh[r][e] = shn;
-                        acc = fmaf(shn, kp[e], acc);
+                    for (int mm = 0; mm < P2; ++mm) {
+                        const float2 sp = Sp[r][mm];
+                        const float2 sc = __ffma2_rn(dy2, qt[mm], Sh[r][mm]);
+                        dkacc[mm] = __ffma2_rn(sc, dr2, dkacc[mm]);
+                        const float2 dA = __ffma2_rn(du2, kt[mm], sc);
+                        dg2 = __ffma2_rn(dA, sp, dg2);
+                        dkacc[mm] = __ffma2_rn(sp, gdu2, dkacc[mm]);
+                        dqacc[mm] = __ffma2_rn(sp, gdy2, dqacc[mm]);
+                        const float2 shn = __fmul2_rn(gg, dA);
+                        Sh[r][mm] = shn;
+                        acc = __ffma2_rn(shn, kp[mm], acc);
                     }
-                    pn[r] = acc;
+                    pn[r] = acc.x + acc.y;
                 }
-                float *cp = cp_s + (size_t)(j * nw + warp) * 2 * DK + lane;
+                float *cpw = cp_s + (size_t)(jf * nw + warp) * 2 * P2 * 64 + 2 * lane;
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    cp[32 * e] = dkacc[e];
-                    cp[DK + 32 * e] = dqacc[e];
+                for (int mm = 0; mm < P2; ++mm) {
+                    *reinterpret_cast<float2 *>(cpw + mm * 64) = dkacc[mm];
+                    *reinterpret_cast<float2 *>(cpw + P2 * 64 + mm * 64) = dqacc[mm];
                 }
-                dgacc = warp_sum(dgacc);
-                if (lane == 0) gp_s[j * nw + warp] = dgacc;
-                p_own = transpose_reduce<RW>(pn, lane);
-            }
-            __syncthreads();
-
-            // fixed-order reductions of the sub-block's per-step partials
-            for (int j = warp; j < slen; j += nw) {
-                const int t = s0 + j, tc = t - t0;
-                float s1 = 0.f, s2 = 0.f;
-                for (int rr = lane; rr < RB; rr += 32) {
-                    s1 = fmaf(dl_s[tc * RB + rr], dy_s[j * RB + rr], s1);
-                    s2 = fmaf(dd_s[j * RB + rr], vm_s[tc * RB + rr], s2);
-                }
-                s1 = warp_sum(s1);
-                s2 = warp_sum(s2);
-                if (lane == 0) {
-                    float dgs = 0.f;
-                    for (int w = 0; w < nw; ++w) dgs += gp_s[j * nw + w];
-                    const size_t o = (((size_t)b * T + t) * Hv + h) * nsplit + split;
-                    p.ws_dg[o] = dgs;
-                    p.ws_db[o] = s2;
-                    dd2_s[j] = s1;
+                const float dgs = warp_sum(dg2.x + dg2.y);
+                if (lane == 0) gp_s[jf * nw + warp] = dgs;
+                p_own = group_transpose_reduce<R, 32>(pn, lane);
+                if (jf == F - 1 || j == 0) flush(j, j + jf);
+            };
+            // Sa holds S_{t-1} for the last step; the others come from TMEM one step ahead
+            for (int j = slen - 1; j >= 0; j -= 2) {
+                if (j >= 1) tmem_load_state(j - 1, Sb);
+                core_step(j, Sa);
+                if (j >= 1) {
+                    tmem_wait_ld();
+                    if (j >= 2) tmem_load_state(j - 2, Sa);
+                    core_step(j - 1, Sb);
+                    if (j >= 2) tmem_wait_ld();
                 }
             }
-            __syncthreads();
-            for (int i = threadIdx.x; i < slen * DK; i += blockDim.x) {
-                const int j = i / DK, col = i - j * DK, t = s0 + j;
-                float a = 0.f, bq = 0.f;
-                for (int w = 0; w < nw; ++w) {
-                    a += cp_s[((size_t)(j * nw + w) * 2) * DK + col];
-                    bq += cp_s[((size_t)(j * nw + w) * 2 + 1) * DK + col];
-                }
-                bq = fmaf(k_s[(j + 1) * DK + col], dd2_s[j], bq);
-                const size_t o = ((((size_t)b * T + t) * Hv + h) * nsplit + split) * DK + col;
-                p.ws_dk[o] = a;
-                p.ws_dq[o] = bq;
-            }
-            for (int i = threadIdx.x; i < slen * RB; i += blockDim.x) {
-                const int j = i / RB, rr = i - j * RB, row = row0 + rr;
-                if (row < Dv)
-                    dv[(((size_t)b * T + s0 + j) * Hv + h) * Dv + row] = from_f32<TIn>(b_s[j] * dd_s[j * RB + rr]);
-            }
+            buf ^= 1;
         }
     }
-    if (p.dS0 != nullptr) {
+
+    if (!failed && p.dS0 != nullptr) {
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
+        for (int r = 0; r < R; ++r) {
             const int row = row0 + wrow + r;
             if (row < Dv) {
+                float *dst = p.dS0 + (head * Dv + row) * DK;
 #pragma unroll
-                for (int e = 0; e < E; ++e) p.dS0[(state_off + row) * DK + lane + 32 * e] = Sh[r][e];
+                for (int m = 0; m < P2; ++m) {
+                    dst[lane + 64 * m] = Sh[r][m].x;
+                    if (lane + 64 * m + 32 < DK) dst[lane + 64 * m + 32] = Sh[r][m].y;
+                }
             }
         }
     }
+    if (failed && tid == 0) report_status(p.status, kStatusTimeout);
+    // release tensor memory on every path
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(*tslot, 512);
 }
 
 // dq[b,t,hk,:] = sum over h in the kv head's group (ascending) of the sum over row splits
@@ -366,40 +597,41 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceParams p) {
     }
 }
 
-size_t bwd_smem_bytes(int DK, int nw, int C) {
-    const int RB = nw * kRowsPerWarp, SUB = kSub;
-    const size_t floats = (size_t)2 * C * RB + (size_t)(2 * SUB + 1) * DK + (size_t)3 * SUB * RB +
-                          (size_t)SUB * nw * 2 * DK + (size_t)SUB * nw + 4 * SUB;
-    return floats * sizeof(float);
+size_t bwd_smem_bytes(int Dk, int warps, int C, int F, int dtype) {
+    return BwdSmem(Dk, warps * kBwdRowsPerWarp, warps, dtype == 0 ? 4 : 2, C, F).total;
 }
 
 template <int E, typename TIn>
-static cudaError_t launch_bwd_t(const BwdParams &p, int warps, cudaStream_t s) {
-    const size_t smem = bwd_smem_bytes(32 * E, warps, p.C);
+static cudaError_t launch_bwd_t(const BwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk, int warps,
+                                cudaStream_t s) {
+    const size_t smem = bwd_smem_bytes(32 * E, warps, p.C, p.flush, IsF32B<TIn>::value ? 0 : 1);
     cudaError_t err = cudaFuncSetAttribute(bwd_kernel<E, TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid(p.nsplit, p.Hv, p.B);
-    bwd_kernel<E, TIn><<<grid, warps * 32, smem, s>>>(p);
+    bwd_kernel<E, TIn><<<grid, warps * 32, smem, s>>>(tq, tk, p);
     return cudaGetLastError();
 }
 
 template <typename TIn>
-static cudaError_t launch_bwd_dk(const BwdParams &p, int Dk, int warps, cudaStream_t s) {
+static cudaError_t launch_bwd_dk(const BwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk, int Dk,
+                                 int warps, cudaStream_t s) {
     switch (Dk) {
-        case 32: return launch_bwd_t<1, TIn>(p, warps, s);
-        case 64: return launch_bwd_t<2, TIn>(p, warps, s);
-        case 96: return launch_bwd_t<3, TIn>(p, warps, s);
-        case 128: return launch_bwd_t<4, TIn>(p, warps, s);
-        case 160: return launch_bwd_t<5, TIn>(p, warps, s);
-        case 192: return launch_bwd_t<6, TIn>(p, warps, s);
-        case 224: return launch_bwd_t<7, TIn>(p, warps, s);
-        case 256: return launch_bwd_t<8, TIn>(p, warps, s);
+        case 32: return launch_bwd_t<1, TIn>(p, tq, tk, warps, s);
+        case 64: return launch_bwd_t<2, TIn>(p, tq, tk, warps, s);
+        case 96: return launch_bwd_t<3, TIn>(p, tq, tk, warps, s);
+        case 128: return launch_bwd_t<4, TIn>(p, tq, tk, warps, s);
+        case 160: return launch_bwd_t<5, TIn>(p, tq, tk, warps, s);
+        case 192: return launch_bwd_t<6, TIn>(p, tq, tk, warps, s);
+        case 224: return launch_bwd_t<7, TIn>(p, tq, tk, warps, s);
+        case 256: return launch_bwd_t<8, TIn>(p, tq, tk, warps, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_bwd(const BwdParams &p, int Dk, int dtype, int warps, cudaStream_t s) {
-    return dtype == 0 ? launch_bwd_dk<float>(p, Dk, warps, s) : launch_bwd_dk<__nv_bfloat16>(p, Dk, warps, s);
+cudaError_t launch_bwd(const BwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k, int Dk, int dtype,
+                       int warps, cudaStream_t s) {
+    return dtype == 0 ? launch_bwd_dk<float>(p, tm_q, tm_k, Dk, warps, s)
+                      : launch_bwd_dk<__nv_bfloat16>(p, tm_q, tm_k, Dk, warps, s);
 }
 
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s) {

@@ -19,9 +19,6 @@ constexpr unsigned kFullMask = 0xffffffffu;
 constexpr int kRowsPerWarp = 8;
 // Steps per forward staging tile (a multiple of 16).
 constexpr int kFwdTile = 32;
-// Steps per backward sub-block: states inside a sub-block are re-computed and kept
-// so that the reverse sweep can read S_{t-1} for each step.
-constexpr int kSub = 8;
 constexpr int kMaxChunk = 128;
 constexpr int kMaxDv = 4096;
 
@@ -42,10 +39,22 @@ struct BwdParams {
     float *dS0;
     float *ws_dq, *ws_dk;   // [B, T, Hv, nsplit, Dk] per-CTA column partials
     float *ws_dg, *ws_db;   // [B, T, Hv, nsplit]
-    float *ws_state;        // per CTA: (nsub_max + kSub - 1) states of [RB, Dk]
+    float *ws_state;        // per CTA: nsub_max sub-block start states of RB x Dk (pair layout)
     void *dv;
-    int B, T, Hk, Hv, Dv, C, NC, nsplit, nsub_max;
+    int *status;            // device status word (bounded-wait timeouts), may be null
+    int B, T, Hk, Hv, Dv, C, NC, nsplit, nsub_max, flush;
 };
+
+// Backward geometry, shared by host and device. A lane holds Dk/32 columns of each of
+// its rows as bwd_pairs(Dk) column pairs (the last pair half-empty when Dk/32 is odd).
+// A sub-block of bwd_sub(Dk) steps keeps bwd_sub - 1 states in tensor memory (256
+// columns per thread: 8 rows x 2 x pairs columns per state) and one in registers.
+__host__ __device__ constexpr int bwd_pairs(int Dk) { return (Dk / 32 + 1) / 2; }
+__host__ __device__ constexpr int bwd_sub(int Dk) {
+    return 256 / (16 * bwd_pairs(Dk)) + 1 > 8 ? 8 : 256 / (16 * bwd_pairs(Dk)) + 1;
+}
+constexpr int kBwdRowsPerWarp = 8;
+constexpr int kBwdMaxWarps = 8;
 
 struct ReduceParams {
     const float *ws_dq, *ws_dk, *ws_dg, *ws_db;
@@ -168,6 +177,55 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Orders this thread's earlier generic-proxy global writes before later async-proxy
+// (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tensor memory
+// Allocation is warp-collective (one warp); the allocated base address is written to
+// shared memory. 32x32b accesses: warp w reaches TMEM lanes 32*(w%4) .. +31, one lane
+// per thread, N consecutive 32-bit columns per access.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float2 (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y), "f"(v[3].x), "f"(v[3].y),
+        "f"(v[4].x), "f"(v[4].y), "f"(v[5].x), "f"(v[5].y), "f"(v[6].x), "f"(v[6].y), "f"(v[7].x), "f"(v[7].y)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 (&v)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y), "=f"(v[3].x),
+          "=f"(v[3].y), "=f"(v[4].x), "=f"(v[4].y), "=f"(v[5].x), "=f"(v[5].y), "=f"(v[6].x), "=f"(v[6].y),
+          "=f"(v[7].x), "=f"(v[7].y)
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void report_status(int *status, int code) {
     if (status != nullptr) atomicExch(status, code);
 }
@@ -182,8 +240,12 @@ __device__ __forceinline__ float warp_sum(float x) {
 // tm_q / tm_k: 4-D tensor maps of q and k ([B, T, Hk, Dk], box {Dk, 1, kFwdTile, 1}).
 cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k, int Dk, int dtype,
                        int warps, cudaStream_t s);
-cudaError_t launch_bwd(const BwdParams &p, int Dk, int dtype, int warps, cudaStream_t s);
+// tm_q / tm_k: tensor maps with box {Dk, 1, bwd_sub(Dk) + 1, 1}.
+cudaError_t launch_bwd(const BwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k, int Dk, int dtype,
+                       int warps, cudaStream_t s);
+// Shared-memory bytes of bwd_kernel for a checkpoint interval C and flush interval F
+// (F steps of column partials kept before a reduction).
+size_t bwd_smem_bytes(int Dk, int warps, int C, int F, int dtype);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
-size_t bwd_smem_bytes(int DK, int nw, int C);
 
 }  // namespace gdn
