@@ -29,11 +29,13 @@
 //     core    runs the reverse steps, each reading S_{t-1} from TMEM one step ahead.
 //
 // Layout: a CTA owns RB = 8 * warps rows of one (b, h); a warp owns 8 rows; lane l holds
-// the column pairs (l + 64m, l + 32 + 64m) of each row, so row dot products are 32-lane
-// reductions and a warp's column sums are complete per lane. Column sums (dq, dk) and dg
-// are reduced over the warps in shared memory in ascending warp order and written per
-// (b, t, h, row split) to fp32 scratch; reduce_kernel adds the row splits (ascending) and
-// the value heads of each kv head (ascending). No atomics.
+// the column pairs (2l + 64m, 2l + 1 + 64m) of each row, so row dot products are 32-lane
+// reductions and a warp's column sums are complete per lane. Each warp folds the row
+// sums delta . dy and ddelta . (v - u) of its rows into its partials in the same pass;
+// column sums (dq, dk), dg and dbeta are then reduced over the warps in shared memory in
+// ascending warp order and written per (b, t, h, row split) to fp32 scratch;
+// reduce_kernel adds the row splits (ascending) and the value heads of each kv head
+// (ascending). No atomics.
 //
 // Staging: k and q tiles of SUB + 1 steps arrive by TMA (tiled tensor maps, one tile
 // ahead, two buffers); v or dy, g and beta are loaded one tile ahead into registers.
@@ -70,25 +72,23 @@ __host__ __device__ inline size_t align_upb(size_t x, size_t a) { return (x + a 
 
 // Shared-memory layout of bwd_kernel (byte offsets from a 128-byte aligned base).
 struct BwdSmem {
-    size_t raw, kf, qf, scb, dl, vm, xs, dd, cp, gp, gs, bs, kq, dd2, bar, tslot, total;
+    size_t raw, kf, scb, dl, vm, xs, dd, cp, gp, gs, bs, kq, bar, tslot, total;
     __host__ __device__ BwdSmem(int DK, int RB, int nw, int esize, int C, int F) {
         const int P2 = bwd_pairs(DK), SUB = bwd_sub(DK), TR = SUB + 1;
         size_t o = 0;
         raw = o; o += align_upb((size_t)2 * 2 * TR * DK * esize, 128);   // [buf][k|q][TR][DK], input type
-        kf = o; o += (size_t)TR * P2 * 64 * 4;                             // fp32, pair layout
-        qf = o; o += (size_t)TR * P2 * 64 * 4;
+        kf = o; if (esize != 4) o += (size_t)2 * TR * DK * 4;              // widened k rows then q rows
         o = align_upb(o, 128);
         scb = o; o += (size_t)RB * P2 * 64 * 4;                            // incoming sub-block start state
         dl = o; o += (size_t)C * RB * 4;
         vm = o; o += (size_t)C * RB * 4;
         xs = o; o += (size_t)SUB * RB * 4;                                  // v (pass A) or dy (reverse)
         dd = o; o += (size_t)SUB * RB * 4;
-        cp = o; o += (size_t)F * nw * 2 * P2 * 64 * 4;
-        gp = o; o += (size_t)F * nw * 4;
+        cp = o; o += (size_t)F * nw * 2 * DK * 4;                           // [F][warp][dk|dq][DK]
+        gp = o; o += (size_t)F * nw * 8;                                    // [F][warp] (dg, dbeta)
         gs = o; o += SUB * 4;
         bs = o; o += SUB * 4;
         kq = o; o += SUB * 4;
-        dd2 = o; o += SUB * 4;
         bar = align_upb(o, 8); o = bar + 3 * 8;
         tslot = o; o += 16;
         total = o + 128;
@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(256, 1)
     constexpr int NPAIR = R * P2;         // float2 pairs of one state per thread
     constexpr int SW = 2 * NPAIR;         // TMEM columns of one state per thread
     constexpr bool kConv = !IsF32B<TIn>::value;
+    constexpr bool kOdd = (DK % 64) != 0;   // the last pair exists only on lanes 0..15
     using QuadT = typename QuadB<TIn>::type;
     static_assert(NPAIR % 8 == 0, "state must be a whole number of 16-column TMEM chunks");
     static_assert((SUB - 1) * SW <= 256, "sub-block states exceed the TMEM share");
@@ -130,19 +131,17 @@ __global__ void __launch_bounds__(256, 1)
     unsigned char *base = reinterpret_cast<unsigned char *>(align_upb(reinterpret_cast<size_t>(smem_raw), 128));
     const BwdSmem L(DK, RB, nw, (int)sizeof(TIn), C, F);
     TIn *raw = reinterpret_cast<TIn *>(base + L.raw);
-    float *kf = reinterpret_cast<float *>(base + L.kf);
-    float *qf = reinterpret_cast<float *>(base + L.qf);
+    float *kfq = reinterpret_cast<float *>(base + L.kf);   // widened k rows then q rows (bf16 input)
     float *scb = reinterpret_cast<float *>(base + L.scb);
     float *dl_s = reinterpret_cast<float *>(base + L.dl);
     float *vm_s = reinterpret_cast<float *>(base + L.vm);
     float *xs = reinterpret_cast<float *>(base + L.xs);
     float *dd_s = reinterpret_cast<float *>(base + L.dd);
     float *cp_s = reinterpret_cast<float *>(base + L.cp);
-    float *gp_s = reinterpret_cast<float *>(base + L.gp);
+    float2 *gp_s = reinterpret_cast<float2 *>(base + L.gp);
     float *g_s = reinterpret_cast<float *>(base + L.gs);
     float *b_s = reinterpret_cast<float *>(base + L.bs);
     float *kq_s = reinterpret_cast<float *>(base + L.kq);
-    float *dd2_s = reinterpret_cast<float *>(base + L.dd2);
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);   // [0], [1]: tiles; [2]: sub-block state
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
@@ -158,6 +157,8 @@ __global__ void __launch_bounds__(256, 1)
     const size_t slot_floats = (size_t)RB * P2 * 64;
     float *scratch = p.ws_state + cta * (size_t)p.nsub_max * slot_floats;
     const int pair_off = wrow * P2 * 64 + 2 * lane;   // this thread's pair (r, m) is at + (r * P2 + m) * 64
+    const int pc = 2 * lane;                          // first column of this lane's pair 0
+    auto pvalid = [&](int m) { return !kOdd || m < P2 - 1 || lane < 16; };
 
     // ---- set-up: barriers, tensor memory
     if (tid == 0) {
@@ -228,16 +229,17 @@ __global__ void __launch_bounds__(256, 1)
         const bool ok = mbar_wait(&bar[buf], buf ? tile_phase1 : tile_phase0);
         if (buf) tile_phase1 ^= 1u;
         else tile_phase0 ^= 1u;
-        if (ok) {
-            const TIn *rk = raw + (size_t)buf * 2 * TR * DK;
-            const int nrows = t.kind == 1 ? 2 * TR : TR;   // k rows, then q rows
-            for (int i = tid; i < nrows * P2 * 64; i += nthreads) {
-                const int row = i / (P2 * 64), rem = i - row * (P2 * 64);
-                const int pr = rem >> 1, x = rem & 1, m = pr >> 5, l = pr & 31;
-                const int col = l + 32 * (2 * m + x);
-                const float val = col < DK ? to_f32(rk[row * DK + col]) : 0.f;
-                if (row < TR) kf[row * P2 * 64 + rem] = val;
-                else qf[(row - TR) * P2 * 64 + rem] = val;
+        if (ok && kConv) {
+            // widen 8 bf16 (16 bytes) at a time: k rows then q rows
+            const uint4 *src = reinterpret_cast<const uint4 *>(raw + (size_t)buf * 2 * TR * DK);
+            const int nchunks = (t.kind == 1 ? 2 * TR : TR) * DK / 8;
+            for (int i = tid; i < nchunks; i += nthreads) {
+                const uint4 w = src[i];
+                float4 *dst = reinterpret_cast<float4 *>(kfq + 8 * i);
+                dst[0] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+                dst[1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                                     __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
             }
         }
         if (__syncthreads_or(!ok)) return false;
@@ -245,8 +247,16 @@ __global__ void __launch_bounds__(256, 1)
         if (nt.kind >= 0) issue_tile(nt, buf ^ 1);
         return true;
     };
+    // row tiles of the current tile: k rows 0..TR-1 (row i = step s0 - 1 + i), q rows likewise
+    const float *kf = kfq, *qf = kfq + TR * DK;
+    auto set_tile_rows = [&](int buf) {
+        if (!kConv) {
+            kf = reinterpret_cast<const float *>(raw + (size_t)buf * 2 * TR * DK);
+            qf = kf + TR * DK;
+        }
+    };
     auto load_pair = [&](const float *rowbase, int m) {
-        return *reinterpret_cast<const float2 *>(rowbase + m * 64 + 2 * lane);
+        return pvalid(m) ? *reinterpret_cast<const float2 *>(rowbase + pc + 64 * m) : make_float2(0.f, 0.f);
     };
 
     // ---- adjoint state Sh from dS_T, and its first row dot with k_{T-1}
@@ -256,13 +266,9 @@ __global__ void __launch_bounds__(256, 1)
         const int row = row0 + wrow + r;
 #pragma unroll
         for (int m = 0; m < P2; ++m) {
-            float2 e = make_float2(0.f, 0.f);
-            if (p.dS_T != nullptr && row < Dv) {
-                const float *src = p.dS_T + (head * Dv + row) * DK;
-                e.x = src[lane + 64 * m];
-                if (lane + 64 * m + 32 < DK) e.y = src[lane + 64 * m + 32];
-            }
-            Sh[r][m] = e;
+            Sh[r][m] = (p.dS_T != nullptr && row < Dv && pvalid(m))
+                           ? *reinterpret_cast<const float2 *>(p.dS_T + (head * Dv + row) * DK + pc + 64 * m)
+                           : make_float2(0.f, 0.f);
         }
     }
     float p_own;   // Sh . k_t of row my_row, for the next reverse step t
@@ -272,8 +278,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int m = 0; m < P2; ++m) {
             const TIn *src = k + (((size_t)b * T + T - 1) * p.Hk + hk) * DK;
-            kk[m].x = to_f32(src[lane + 64 * m]);
-            kk[m].y = lane + 64 * m + 32 < DK ? to_f32(src[lane + 64 * m + 32]) : 0.f;
+            kk[m].x = pvalid(m) ? to_f32(src[pc + 64 * m]) : 0.f;
+            kk[m].y = pvalid(m) ? to_f32(src[pc + 64 * m + 1]) : 0.f;
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -302,18 +308,16 @@ __global__ void __launch_bounds__(256, 1)
                 const int row = row0 + wrow + r;
 #pragma unroll
                 for (int m = 0; m < P2; ++m) {
-                    float2 e = make_float2(0.f, 0.f);
-                    if (row < Dv) {
-                        e.x = ck[(size_t)row * DK + lane + 64 * m];
-                        if (lane + 64 * m + 32 < DK) e.y = ck[(size_t)row * DK + lane + 64 * m + 32];
-                    }
-                    S[r][m] = e;
+                    S[r][m] = (row < Dv && pvalid(m))
+                                  ? *reinterpret_cast<const float2 *>(ck + (size_t)row * DK + pc + 64 * m)
+                                  : make_float2(0.f, 0.f);
                 }
             }
         }
         for (int m = 0; m < nsub; ++m) {
             const int s0 = t0 + m * SUB, slen = min(SUB, t0 + len - s0);
             if (!begin_tile(TileRef{0, c, m}, buf)) { failed = true; break; }
+            set_tile_rows(buf);
             float *slot = scratch + (size_t)m * slot_floats + pair_off;
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int j = 0; j < slen; ++j) {
                 float2 kv[P2];
 #pragma unroll
-                for (int mm = 0; mm < P2; ++mm) kv[mm] = load_pair(kf + (j + 1) * P2 * 64, mm);
+                for (int mm = 0; mm < P2; ++mm) kv[mm] = load_pair(kf + (j + 1) * DK, mm);
                 float part[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
@@ -357,6 +361,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int m = nsub - 1; m >= 0; --m) {
             const int s0 = t0 + m * SUB, slen = min(SUB, t0 + len - s0);
             if (!begin_tile(TileRef{1, c, m}, buf)) { failed = true; break; }
+            set_tile_rows(buf);
             if (m == nsub - 1 && tid == 0) {
                 mbar_expect_tx(&bar[2], (unsigned)(slot_floats * 4));
                 bulk_load(scb, scratch + (size_t)m * slot_floats, (unsigned)(slot_floats * 4), &bar[2]);
@@ -364,7 +369,7 @@ __global__ void __launch_bounds__(256, 1)
             // per-step k_t . q_t
             for (int j = warp; j < slen; j += nw) {
                 float a = 0.f;
-                for (int i = lane; i < P2 * 64; i += 32) a = fmaf(kf[(j + 1) * P2 * 64 + i], qf[(j + 1) * P2 * 64 + i], a);
+                for (int i = lane; i < DK; i += 32) a = fmaf(kf[(j + 1) * DK + i], qf[(j + 1) * DK + i], a);
                 a = warp_sum(a);
                 if (lane == 0) kq_s[j] = a;
             }
@@ -397,7 +402,7 @@ __global__ void __launch_bounds__(256, 1)
                 const float2 gg = make_float2(gt, gt);
                 float2 kv[P2];
 #pragma unroll
-                for (int mm = 0; mm < P2; ++mm) kv[mm] = load_pair(kf + (j + 1) * P2 * 64, mm);
+                for (int mm = 0; mm < P2; ++mm) kv[mm] = load_pair(kf + (j + 1) * DK, mm);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const float d = dl_s[(s0 - t0 + j) * RB + wrow + r];
@@ -420,75 +425,89 @@ __global__ void __launch_bounds__(256, 1)
                     for (int i = 0; i < 8; ++i) dst[(q * 8 + i) / P2][(q * 8 + i) % P2] = chunk[i];
                 }
             };
-            auto flush = [&](int jlo, int jhi) {   // steps jlo .. jhi of this sub-block (jhi >= jlo)
+            // Reduce the warps' partials of steps jlo .. jhi (the batch's highest step, jhi, sits
+            // in partial slot 0; step j in slot jhi - j), write them out, and free the slots.
+            auto flush = [&](int jlo, int jhi) {
                 __syncthreads();
-                for (int j = jlo + warp; j <= jhi; j += nw) {
-                    const int t = s0 + j, tc = t - t0, jf = (slen - 1 - j) % F;
-                    float s1 = 0.f, s2 = 0.f;
-                    for (int rr = lane; rr < RB; rr += 32) {
-                        s1 = fmaf(dl_s[tc * RB + rr], xs[j * RB + rr], s1);
-                        s2 = fmaf(dd_s[j * RB + rr], vm_s[tc * RB + rr], s2);
+                const int nst = jhi - jlo + 1;
+                for (int i = tid; i < nst * (DK / 4); i += nthreads) {
+                    const int jj = i / (DK / 4), c4 = (i - jj * (DK / 4)) * 4;
+                    const int j = jhi - jj, t = s0 + j;
+                    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), q4 = a;
+#pragma unroll
+                    for (int w = 0; w < kBwdMaxWarps; ++w) {
+                        if (w < nw) {
+                            const float4 x = *reinterpret_cast<const float4 *>(cp_s + ((size_t)(jj * nw + w) * 2) * DK + c4);
+                            const float4 y = *reinterpret_cast<const float4 *>(cp_s + ((size_t)(jj * nw + w) * 2 + 1) * DK + c4);
+                            a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+                            q4.x += y.x; q4.y += y.y; q4.z += y.z; q4.w += y.w;
+                        }
                     }
-                    s1 = warp_sum(s1);
-                    s2 = warp_sum(s2);
-                    if (lane == 0) {
-                        float dgs = 0.f;
-                        for (int w = 0; w < nw; ++w) dgs += gp_s[jf * nw + w];
-                        const size_t o = (((size_t)b * T + t) * Hv + h) * nsplit + split;
-                        p.ws_dg[o] = dgs;
-                        p.ws_db[o] = s2;
-                        dd2_s[j] = s1;
-                    }
+                    const size_t o = ((((size_t)b * T + t) * Hv + h) * nsplit + split) * DK + c4;
+                    *reinterpret_cast<float4 *>(p.ws_dk + o) = a;
+                    *reinterpret_cast<float4 *>(p.ws_dq + o) = q4;
                 }
-                __syncthreads();
-                for (int i = tid; i < (jhi - jlo + 1) * DK; i += nthreads) {
-                    const int j = jlo + i / DK, col = i % DK, t = s0 + j, jf = (slen - 1 - j) % F;
-                    const int e = col >> 5, l = col & 31;
-                    const int pidx = ((e >> 1) * 32 + l) * 2 + (e & 1);   // pair-layout index of `col`
-                    float a = 0.f, bq2 = 0.f;
-                    for (int w = 0; w < nw; ++w) {
-                        a += cp_s[((size_t)(jf * nw + w) * 2) * P2 * 64 + pidx];
-                        bq2 += cp_s[((size_t)(jf * nw + w) * 2 + 1) * P2 * 64 + pidx];
+                if (tid < nst) {
+                    const int jj = tid, j = jhi - jj, t = s0 + j;
+                    float dgs = 0.f, dbs = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kBwdMaxWarps; ++w) {
+                        if (w < nw) {
+                            dgs += gp_s[jj * nw + w].x;
+                            dbs += gp_s[jj * nw + w].y;
+                        }
                     }
-                    bq2 = fmaf(kf[(j + 1) * P2 * 64 + pidx], dd2_s[j], bq2);
-                    const size_t o = ((((size_t)b * T + t) * Hv + h) * nsplit + split) * DK + col;
-                    p.ws_dk[o] = a;
-                    p.ws_dq[o] = bq2;
+                    const size_t o = (((size_t)b * T + t) * Hv + h) * nsplit + split;
+                    p.ws_dg[o] = dgs;
+                    p.ws_db[o] = dbs;
                 }
-                for (int i = tid; i < (jhi - jlo + 1) * RB; i += nthreads) {
-                    const int j = jlo + i / RB, rr = i % RB, row = row0 + rr;
+                for (int i = tid; i < nst * RB; i += nthreads) {
+                    const int jj = i / RB, rr = i - jj * RB, j = jhi - jj, row = row0 + rr;
                     if (row < Dv)
                         dv[(((size_t)b * T + s0 + j) * Hv + h) * Dv + row] = from_f32<TIn>(b_s[j] * dd_s[j * RB + rr]);
                 }
                 __syncthreads();
             };
+            int jf = 0;   // partial slot of the next core step
             auto core_step = [&](int j, const float2 (&Sp)[R][P2]) {
-                const int tc = s0 + j - t0, jf = (slen - 1 - j) % F;
+                const int tc = s0 + j - t0;
                 const float gt = g_s[j], bt = b_s[j];
-                const float dyo = xs[j * RB + wrow + my_row];
-                const float ddo = p_own + dyo * kq_s[j];
-                const float duo = -bt * ddo;
+                // owner lane: ddelta of its row; then every lane takes all 8 rows' values
+                const float ddo = p_own + xs[j * RB + wrow + my_row] * kq_s[j];
                 if ((lane & 3) == 0) dd_s[j * RB + wrow + my_row] = ddo;
+                float dyr[R], drr[R], vmr[R];
+#pragma unroll
+                for (int h4 = 0; h4 < R / 4; ++h4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(xs + j * RB + wrow + 4 * h4);
+                    const float4 d = *reinterpret_cast<const float4 *>(dl_s + tc * RB + wrow + 4 * h4);
+                    const float4 u = *reinterpret_cast<const float4 *>(vm_s + tc * RB + wrow + 4 * h4);
+                    dyr[4 * h4] = a.x; dyr[4 * h4 + 1] = a.y; dyr[4 * h4 + 2] = a.z; dyr[4 * h4 + 3] = a.w;
+                    drr[4 * h4] = d.x; drr[4 * h4 + 1] = d.y; drr[4 * h4 + 2] = d.z; drr[4 * h4 + 3] = d.w;
+                    vmr[4 * h4] = u.x; vmr[4 * h4 + 1] = u.y; vmr[4 * h4 + 2] = u.z; vmr[4 * h4 + 3] = u.w;
+                }
                 float2 kt[P2], qt[P2], kp[P2];
 #pragma unroll
                 for (int mm = 0; mm < P2; ++mm) {
-                    kt[mm] = load_pair(kf + (j + 1) * P2 * 64, mm);
-                    qt[mm] = load_pair(qf + (j + 1) * P2 * 64, mm);
-                    kp[mm] = load_pair(kf + j * P2 * 64, mm);
+                    kt[mm] = load_pair(kf + (j + 1) * DK, mm);
+                    qt[mm] = load_pair(qf + (j + 1) * DK, mm);
+                    kp[mm] = load_pair(kf + j * DK, mm);
                 }
                 float2 dkacc[P2], dqacc[P2];
 #pragma unroll
                 for (int mm = 0; mm < P2; ++mm) dkacc[mm] = dqacc[mm] = make_float2(0.f, 0.f);
                 float2 dg2 = make_float2(0.f, 0.f);
+                float s_dy = 0.f, s_db = 0.f;   // sum over the warp's rows of delta.dy and ddelta.(v - u)
                 float pn[R];
                 const float2 gg = make_float2(gt, gt);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float du = __shfl_sync(kFullMask, duo, 4 * r);
-                    const float dyr = xs[j * RB + wrow + r];
-                    const float dr = dl_s[tc * RB + wrow + r];
-                    const float2 du2 = make_float2(du, du), dy2 = make_float2(dyr, dyr), dr2 = make_float2(dr, dr);
-                    const float2 gdu2 = make_float2(gt * du, gt * du), gdy2 = make_float2(gt * dyr, gt * dyr);
+                    const float dd = __shfl_sync(kFullMask, ddo, 4 * r);
+                    const float du = -bt * dd;
+                    s_dy = fmaf(drr[r], dyr[r], s_dy);
+                    s_db = fmaf(dd, vmr[r], s_db);
+                    const float2 du2 = make_float2(du, du), dy2 = make_float2(dyr[r], dyr[r]);
+                    const float2 dr2 = make_float2(drr[r], drr[r]);
+                    const float2 gdu2 = make_float2(gt * du, gt * du), gdy2 = make_float2(gt * dyr[r], gt * dyr[r]);
                     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int mm = 0; mm < P2; ++mm) {
@@ -505,16 +524,25 @@ __global__ void __launch_bounds__(256, 1)
                     }
                     pn[r] = acc.x + acc.y;
                 }
-                float *cpw = cp_s + (size_t)(jf * nw + warp) * 2 * P2 * 64 + 2 * lane;
+                // dq_t also carries k_t (delta_t . dy_t) over the warp's rows
+                const float2 sdy2 = make_float2(s_dy, s_dy);
+                float *cpw = cp_s + (size_t)(jf * nw + warp) * 2 * DK + pc;
 #pragma unroll
                 for (int mm = 0; mm < P2; ++mm) {
-                    *reinterpret_cast<float2 *>(cpw + mm * 64) = dkacc[mm];
-                    *reinterpret_cast<float2 *>(cpw + P2 * 64 + mm * 64) = dqacc[mm];
+                    if (pvalid(mm)) {
+                        *reinterpret_cast<float2 *>(cpw + 64 * mm) = dkacc[mm];
+                        *reinterpret_cast<float2 *>(cpw + DK + 64 * mm) = __ffma2_rn(kt[mm], sdy2, dqacc[mm]);
+                    }
                 }
                 const float dgs = warp_sum(dg2.x + dg2.y);
-                if (lane == 0) gp_s[jf * nw + warp] = dgs;
+                if (lane == 0) gp_s[jf * nw + warp] = make_float2(dgs, s_db);
                 p_own = group_transpose_reduce<R, 32>(pn, lane);
-                if (jf == F - 1 || j == 0) flush(j, j + jf);
+                if (jf == F - 1 || j == 0) {
+                    flush(j, j + jf);
+                    jf = 0;
+                } else {
+                    ++jf;
+                }
             };
             // Sa holds S_{t-1} for the last step; the others come from TMEM one step ahead
             for (int j = slen - 1; j >= 0; j -= 2) {
@@ -538,10 +566,8 @@ __global__ void __launch_bounds__(256, 1)
             if (row < Dv) {
                 float *dst = p.dS0 + (head * Dv + row) * DK;
 #pragma unroll
-                for (int m = 0; m < P2; ++m) {
-                    dst[lane + 64 * m] = Sh[r][m].x;
-                    if (lane + 64 * m + 32 < DK) dst[lane + 64 * m + 32] = Sh[r][m].y;
-                }
+                for (int m = 0; m < P2; ++m)
+                    if (pvalid(m)) *reinterpret_cast<float2 *>(dst + pc + 64 * m) = Sh[r][m];
             }
         }
     }
