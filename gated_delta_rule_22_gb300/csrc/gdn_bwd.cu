@@ -26,7 +26,8 @@
 //             sub-block ahead) and re-builds the states inside it with the kept delta
 //             (S <- g S + delta k^T), writing them to tensor memory (TMEM); the last one
 //             stays in registers;
-//     core    runs the reverse steps, each reading S_{t-1} from TMEM one step ahead.
+//     core    runs the reverse steps, reading S_{t-1} from TMEM in two halves (rows 0-3,
+//             rows 4-7 of each warp) so that one half loads while the other is used.
 //
 // Layout: a CTA owns RB = 8 * warps rows of one (b, h); a warp owns 8 rows; lane l holds
 // the column pairs (2l + 64m, 2l + 1 + 64m) of each row, so row dot products are 32-lane
@@ -376,11 +377,15 @@ __global__ void __launch_bounds__(256, 1)
             // the sub-block's start state
             const bool ok = mbar_wait(&bar[2], scb_phase);
             scb_phase ^= 1u;
-            float2 Sa[R][P2];
+            // the state of the warp's rows 0-3 (X) and rows 4-7 (Y)
+            float2 X[R / 2][P2], Y[R / 2][P2];
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R / 2; ++r)
 #pragma unroll
-                for (int mm = 0; mm < P2; ++mm) Sa[r][mm] = *reinterpret_cast<const float2 *>(scb + pair_off + (r * P2 + mm) * 64);
+                for (int mm = 0; mm < P2; ++mm) {
+                    X[r][mm] = *reinterpret_cast<const float2 *>(scb + pair_off + (r * P2 + mm) * 64);
+                    Y[r][mm] = *reinterpret_cast<const float2 *>(scb + pair_off + ((r + R / 2) * P2 + mm) * 64);
+                }
             if (__syncthreads_or(!ok)) { failed = true; break; }
             if (m > 0 && tid == 0) {
                 fence_proxy_async();
@@ -388,14 +393,17 @@ __global__ void __launch_bounds__(256, 1)
                 bulk_load(scb, scratch + (size_t)(m - 1) * slot_floats, (unsigned)(slot_floats * 4), &bar[2]);
             }
 
-            // ---- pass B: states before steps s0 .. s0+slen-2 to TMEM; the last stays in Sa
+            // ---- pass B: states before steps s0 .. s0+slen-2 to TMEM; the last stays in X, Y
             for (int j = 0; j + 1 < slen; ++j) {
                 const uint32_t ts = tmem + (uint32_t)(j * SW);
 #pragma unroll
                 for (int q = 0; q < NPAIR / 8; ++q) {
                     float2 chunk[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) chunk[i] = Sa[(q * 8 + i) / P2][(q * 8 + i) % P2];
+                    for (int i = 0; i < 8; ++i) {
+                        const int f = q * 8 + i;   // pair index in the state: rows 0-3 then rows 4-7
+                        chunk[i] = f < NPAIR / 2 ? X[f / P2][f % P2] : Y[(f - NPAIR / 2) / P2][(f - NPAIR / 2) % P2];
+                    }
                     tmem_st16(ts + q * 16, chunk);
                 }
                 const float gt = g_s[j];
@@ -404,25 +412,29 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                 for (int mm = 0; mm < P2; ++mm) kv[mm] = load_pair(kf + (j + 1) * DK, mm);
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const float d = dl_s[(s0 - t0 + j) * RB + wrow + r];
-                    const float2 dd = make_float2(d, d);
+                for (int r = 0; r < R / 2; ++r) {
+                    const float d0 = dl_s[(s0 - t0 + j) * RB + wrow + r];
+                    const float d1 = dl_s[(s0 - t0 + j) * RB + wrow + r + R / 2];
+                    const float2 dd0 = make_float2(d0, d0), dd1 = make_float2(d1, d1);
 #pragma unroll
-                    for (int mm = 0; mm < P2; ++mm) Sa[r][mm] = __ffma2_rn(dd, kv[mm], __fmul2_rn(gg, Sa[r][mm]));
+                    for (int mm = 0; mm < P2; ++mm) {
+                        X[r][mm] = __ffma2_rn(dd0, kv[mm], __fmul2_rn(gg, X[r][mm]));
+                        Y[r][mm] = __ffma2_rn(dd1, kv[mm], __fmul2_rn(gg, Y[r][mm]));
+                    }
                 }
             }
             tmem_wait_st();
 
             // ---- core: reverse steps j = slen-1 .. 0, S_{t-1} in Sa / Sb alternately
-            float2 Sb[R][P2];
-            auto tmem_load_state = [&](int j, float2 (&dst)[R][P2]) {
-                const uint32_t ts = tmem + (uint32_t)(j * SW);
+            // half h (0: rows 0-3, 1: rows 4-7) of the state before step s0 + j, from TMEM
+            auto tmem_load_half = [&](int j, int hh, float2 (&dst)[R / 2][P2]) {
+                const uint32_t ts = tmem + (uint32_t)(j * SW + hh * (SW / 2));
 #pragma unroll
-                for (int q = 0; q < NPAIR / 8; ++q) {
-                    float2 chunk[8];
-                    tmem_ld16(ts + q * 16, chunk);
+                for (int q = 0; q < NPAIR / 8; ++q) {   // NPAIR / 2 pairs in chunks of 4
+                    float2 chunk[4];
+                    tmem_ld8(ts + q * 8, chunk);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) dst[(q * 8 + i) / P2][(q * 8 + i) % P2] = chunk[i];
+                    for (int i = 0; i < 4; ++i) dst[(q * 4 + i) / P2][(q * 4 + i) % P2] = chunk[i];
                 }
             };
             // Reduce the warps' partials of steps jlo .. jhi (the batch's highest step, jhi, sits
@@ -469,7 +481,7 @@ __global__ void __launch_bounds__(256, 1)
                 __syncthreads();
             };
             int jf = 0;   // partial slot of the next core step
-            auto core_step = [&](int j, const float2 (&Sp)[R][P2]) {
+            auto core_step = [&](int j) {
                 const int tc = s0 + j - t0;
                 const float gt = g_s[j], bt = b_s[j];
                 // owner lane: ddelta of its row; then every lane takes all 8 rows' values
@@ -499,8 +511,8 @@ __global__ void __launch_bounds__(256, 1)
                 float s_dy = 0.f, s_db = 0.f;   // sum over the warp's rows of delta.dy and ddelta.(v - u)
                 float pn[R];
                 const float2 gg = make_float2(gt, gt);
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
+                // one row of the fused reverse step, with that row's S_{t-1} in sprow
+                auto row_step = [&](int r, const float2 (&sprow)[P2]) {
                     const float dd = __shfl_sync(kFullMask, ddo, 4 * r);
                     const float du = -bt * dd;
                     s_dy = fmaf(drr[r], dyr[r], s_dy);
@@ -511,7 +523,7 @@ __global__ void __launch_bounds__(256, 1)
                     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int mm = 0; mm < P2; ++mm) {
-                        const float2 sp = Sp[r][mm];
+                        const float2 sp = sprow[mm];
                         const float2 sc = __ffma2_rn(dy2, qt[mm], Sh[r][mm]);
                         dkacc[mm] = __ffma2_rn(sc, dr2, dkacc[mm]);
                         const float2 dA = __ffma2_rn(du2, kt[mm], sc);
@@ -523,7 +535,18 @@ __global__ void __launch_bounds__(256, 1)
                         acc = __ffma2_rn(shn, kp[mm], acc);
                     }
                     pn[r] = acc.x + acc.y;
-                }
+                };
+                // rows 0-3 (X, already in registers) while rows 4-7 load; then the next step's
+                // rows 0-3 load while rows 4-7 (Y) are used
+                const bool first = j == slen - 1;   // X, Y come from pass B
+                if (!first) tmem_load_half(j, 1, Y);
+#pragma unroll
+                for (int r = 0; r < R / 2; ++r) row_step(r, X[r]);
+                if (!first) tmem_wait_ld();
+                if (j >= 1) tmem_load_half(j - 1, 0, X);
+#pragma unroll
+                for (int r = 0; r < R / 2; ++r) row_step(r + R / 2, Y[r]);
+                if (j >= 1) tmem_wait_ld();
                 // dq_t also carries k_t (delta_t . dy_t) over the warp's rows
                 const float2 sdy2 = make_float2(s_dy, s_dy);
                 float *cpw = cp_s + (size_t)(jf * nw + warp) * 2 * DK + pc;
@@ -544,17 +567,7 @@ __global__ void __launch_bounds__(256, 1)
                     ++jf;
                 }
             };
-            // Sa holds S_{t-1} for the last step; the others come from TMEM one step ahead
-            for (int j = slen - 1; j >= 0; j -= 2) {
-                if (j >= 1) tmem_load_state(j - 1, Sb);
-                core_step(j, Sa);
-                if (j >= 1) {
-                    tmem_wait_ld();
-                    if (j >= 2) tmem_load_state(j - 2, Sa);
-                    core_step(j - 1, Sb);
-                    if (j >= 2) tmem_wait_ld();
-                }
-            }
+            for (int j = slen - 1; j >= 0; --j) core_step(j);
             buf ^= 1;
         }
     }
