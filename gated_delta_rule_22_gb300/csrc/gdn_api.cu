@@ -16,12 +16,12 @@ thread_local char g_last_error[256] = "";
 
 struct Plan {
     int B, T, Hk, Hv, Dk, Dv, C, NC, dtype;
-    int warps;     // warps per CTA (both kernels)
-    int RB;        // rows of a state per CTA
-    int nsplit;    // CTAs per (b, h)
+    int warps;     // forward warps per CTA
+    int RB;        // backward: rows of a state per CTA
+    int nsplit;    // backward: CTAs per (b, h)
     int sub;       // backward sub-block length
     int nsub_max;  // sub-blocks per chunk
-    int flush;     // backward steps per column-partial reduction
+    int slots;     // backward partial-sum ring depth (steps)
 };
 
 constexpr size_t kMaxSmem = 232448;   // opt-in shared memory per block on sm_103
@@ -52,13 +52,12 @@ int make_plan(const gdn_shape *s, Plan *p) {
     int warps = (s->Dv + gdn::kRowsPerWarp - 1) / gdn::kRowsPerWarp;
     if (warps > 8) warps = 8;
     p->warps = warps;
-    p->RB = warps * gdn::kRowsPerWarp;
+    p->RB = gdn::kBwdRows;
     p->nsplit = (s->Dv + p->RB - 1) / p->RB;
     p->sub = gdn::bwd_sub(s->Dk);
     p->nsub_max = (C + p->sub - 1) / p->sub;
-    p->flush = p->sub;
-    if (gdn::bwd_smem_bytes(s->Dk, warps, C, p->flush, s->dtype) > kMaxSmem) p->flush = (p->sub + 1) / 2;
-    if (gdn::bwd_smem_bytes(s->Dk, warps, C, p->flush, s->dtype) > kMaxSmem) return GDN_ERR_UNSUPPORTED_SHAPE;
+    p->slots = gdn::bwd_slots(s->Dk, C, s->dtype, kMaxSmem);
+    if (p->slots == 0) return GDN_ERR_UNSUPPORTED_SHAPE;
     return GDN_OK;
 }
 
@@ -212,7 +211,7 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     bp.ws_db = reinterpret_cast<float *>(ws + w.db);
     bp.ws_state = reinterpret_cast<float *>(ws + w.state);
     bp.B = p.B; bp.T = p.T; bp.Hk = p.Hk; bp.Hv = p.Hv; bp.Dv = p.Dv; bp.C = p.C; bp.NC = p.NC;
-    bp.nsplit = p.nsplit; bp.nsub_max = p.nsub_max; bp.flush = p.flush;
+    bp.nsplit = p.nsplit; bp.nsub_max = p.nsub_max; bp.slots = p.slots;
 
     gdn::ReduceParams rp;
     rp.ws_dq = bp.ws_dq; rp.ws_dk = bp.ws_dk; rp.ws_dg = bp.ws_dg; rp.ws_db = bp.ws_db;
@@ -225,7 +224,7 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     CUtensorMap tm_q, tm_k;
     if ((rc = make_qk_map(&tm_q, q, p, p.sub + 1)) != GDN_OK) return rc;
     if ((rc = make_qk_map(&tm_k, k, p, p.sub + 1)) != GDN_OK) return rc;
-    rc = cuda_status(gdn::launch_bwd(bp, tm_q, tm_k, p.Dk, p.dtype, p.warps, (cudaStream_t)stream));
+    rc = cuda_status(gdn::launch_bwd(bp, tm_q, tm_k, p.Dk, p.dtype, (cudaStream_t)stream));
     if (rc != GDN_OK) return rc;
     return cuda_status(gdn::launch_reduce(rp, p.dtype, (cudaStream_t)stream));
 }

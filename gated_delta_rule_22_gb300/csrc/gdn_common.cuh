@@ -42,19 +42,32 @@ struct BwdParams {
     float *ws_state;        // per CTA: nsub_max sub-block start states of RB x Dk (pair layout)
     void *dv;
     int *status;            // device status word (bounded-wait timeouts), may be null
-    int B, T, Hk, Hv, Dv, C, NC, nsplit, nsub_max, flush;
+    int B, T, Hk, Hv, Dv, C, NC, nsplit, nsub_max;
+    int slots;              // depth of the per-step partial-sum ring (2..4)
 };
 
 // Backward geometry, shared by host and device. A lane holds Dk/32 columns of each of
-// its rows as bwd_pairs(Dk) column pairs (the last pair half-empty when Dk/32 is odd).
-// A sub-block of bwd_sub(Dk) steps keeps bwd_sub - 1 states in tensor memory (256
-// columns per thread: 8 rows x 2 x pairs columns per state) and one in registers.
+// its rows as bwd_pairs(Dk) column pairs (the last pair only on lanes 0..15 when Dk/32
+// is odd). A sub-block of bwd_sub(Dk) steps keeps bwd_sub - 1 states in tensor memory
+// (256 columns per thread: 8 rows x 2 x pairs columns per state) and one in registers.
 __host__ __device__ constexpr int bwd_pairs(int Dk) { return (Dk / 32 + 1) / 2; }
 __host__ __device__ constexpr int bwd_sub(int Dk) {
     return 256 / (16 * bwd_pairs(Dk)) + 1 > 8 ? 8 : 256 / (16 * bwd_pairs(Dk)) + 1;
 }
 constexpr int kBwdRowsPerWarp = 8;
-constexpr int kBwdMaxWarps = 8;
+// The backward CTA: two warpgroups of compute warps (8 rows each, 64 rows per CTA) and one
+// service warpgroup. Registers are rebalanced with setmaxnreg after launch: the launch
+// gives every thread kBwdLaunchRegs; the compute warpgroups raise theirs to
+// kBwdComputeRegs and the service warpgroup lowers its to kBwdServiceRegs, and the two
+// shares add up to no more than the launch's total.
+constexpr int kBwdComputeWarps = 8;
+constexpr int kBwdThreads = (kBwdComputeWarps + 4) * 32;
+constexpr int kBwdRows = kBwdComputeWarps * kBwdRowsPerWarp;
+constexpr int kBwdLaunchRegs = 168;
+constexpr int kBwdComputeRegs = 216;
+constexpr int kBwdServiceRegs = 72;
+static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <= kBwdThreads * kBwdLaunchRegs,
+              "register split exceeds the launch's registers");
 
 struct ReduceParams {
     const float *ws_dq, *ws_dk, *ws_dg, *ws_db;
@@ -146,6 +159,10 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, unsigned bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
@@ -233,6 +250,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 (&v)[8]) {
         : "memory");
 }
 
+// Per-thread register limit of the executing warpgroup (all four warps execute it).
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+
 __device__ __forceinline__ void report_status(int *status, int code) {
     if (status != nullptr) atomicExch(status, code);
 }
@@ -248,11 +271,15 @@ __device__ __forceinline__ float warp_sum(float x) {
 cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k, int Dk, int dtype,
                        int warps, cudaStream_t s);
 // tm_q / tm_k: tensor maps with box {Dk, 1, bwd_sub(Dk) + 1, 1}.
+// Fails with cudaErrorInvalidConfiguration if the compiled kernel was given fewer
+// registers per thread than the register split assumes.
 cudaError_t launch_bwd(const BwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k, int Dk, int dtype,
-                       int warps, cudaStream_t s);
-// Shared-memory bytes of bwd_kernel for a checkpoint interval C and flush interval F
-// (F steps of column partials kept before a reduction).
-size_t bwd_smem_bytes(int Dk, int warps, int C, int F, int dtype);
+                       cudaStream_t s);
+// Depth of the backward's partial-sum ring for checkpoint interval C: the deepest (4, 3
+// or 2 steps) whose shared-memory layout fits `limit` bytes, 0 if none does; and the
+// shared-memory bytes of that layout.
+int bwd_slots(int Dk, int C, int dtype, size_t limit);
+size_t bwd_smem_bytes(int Dk, int C, int dtype, int slots);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
 
 }  // namespace gdn
