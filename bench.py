@@ -221,7 +221,7 @@ def run_ours(args, w):
     NC = -(-T // w.chunk)
     y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
     S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
-    ckpt = torch.empty((B, Hv, NC, Dv, Dk), dtype=torch.float32, device=dev)
+    ckpt = gdn.new_ckpt(t["q"], t["v"], w.chunk)
     grads = {"dq": torch.empty_like(t["q"]), "dk": torch.empty_like(t["k"]), "dv": torch.empty_like(t["v"]),
              "dg": torch.empty_like(t["g"]), "dbeta": torch.empty_like(t["beta"]),
              "dS0": torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)}

@@ -121,6 +121,36 @@ def gdn_bwd_workspace_bytes(shape: GdnShape) -> int:
     return load_library().gdn_bwd_workspace_bytes(ctypes.byref(shape))
 
 
+def _room(t) -> int:
+    """Bytes of t's storage from its first element on."""
+    return t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
+
+
+def new_ckpt(q, v, chunk=64):
+    """The saved-for-backward buffer of gdn_fwd for inputs shaped like q and v: one fp32
+    allocation of gdn_ckpt_bytes bytes, returned as its leading [B, Hv, NC, Dv, Dk] view of
+    chunk-start states (the per-step residuals v - u follow in the same storage)."""
+    torch = _torch()
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    NC = -(-T // (chunk or 64))
+    need = gdn_ckpt_bytes(_shape_of(q, v, chunk))
+    buf = torch.empty(-(-need // 4), dtype=torch.float32, device=q.device)
+    return buf[: B * Hv * NC * Dv * Dk].view(B, Hv, NC, Dv, Dk)
+
+
+def _check_ckpt(ckpt, q, v, chunk):
+    torch = _torch()
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    NC = -(-T // (chunk or 64))
+    _check("ckpt", ckpt, (B, Hv, NC, Dv, Dk), torch.float32, q.device)
+    need = gdn_ckpt_bytes(_shape_of(q, v, chunk))
+    if _room(ckpt) < need:
+        raise ValueError(f"ckpt: its storage holds {_room(ckpt)} bytes from the first state on, "
+                         f"gdn_ckpt_bytes = {need} (allocate it with new_ckpt)")
+
+
 def _shape_of(q, v, chunk):
     B, T, Hk, Dk = q.shape
     Hv, Dv = v.shape[2], v.shape[3]
@@ -129,7 +159,8 @@ def _shape_of(q, v, chunk):
 
 def gdn_fwd(q, k, v, g, beta, S0=None, chunk=64, *, y=None, S_T=None, ckpt=None, want_S_T=True,
             stream=None):
-    """y, S_T, ckpt = gdn_fwd(q, k, v, g, beta[, S0]) on CUDA tensors (see include/gdn.h)."""
+    """y, S_T, ckpt = gdn_fwd(q, k, v, g, beta[, S0]) on CUDA tensors (see include/gdn.h).
+    ckpt is the [B, Hv, NC, Dv, Dk] view of the saved-for-backward buffer (new_ckpt)."""
     torch = _torch()
     lib = load_library()
     shape = _shape_of(q, v, chunk)
@@ -147,7 +178,8 @@ def gdn_fwd(q, k, v, g, beta, S0=None, chunk=64, *, y=None, S_T=None, ckpt=None,
     if S_T is None and want_S_T:
         S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
     if ckpt is None:
-        ckpt = torch.empty((B, Hv, NC, Dv, Dk), dtype=torch.float32, device=dev)
+        ckpt = new_ckpt(q, v, chunk)
+    _check_ckpt(ckpt, q, v, chunk)
     rc = lib.gdn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0),
                      _ptr(y), _ptr(S_T), _ptr(ckpt), _stream(stream))
     if rc != GDN_OK:
@@ -167,8 +199,7 @@ def gdn_bwd(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, workspace=None, 
     for name, t, shp in (("q", q, q.shape), ("k", k, q.shape), ("v", v, (B, T, Hv, Dv)),
                          ("g", g, (B, T, Hv)), ("beta", beta, (B, T, Hv)), ("dy", dy, (B, T, Hv, Dv))):
         _check(name, t, shp, dt, dev)
-    NC = -(-T // (chunk or 64))
-    _check("ckpt", ckpt, (B, Hv, NC, Dv, Dk), torch.float32, dev)
+    _check_ckpt(ckpt, q, v, chunk)
     if dS_T is not None:
         _check("dS_T", dS_T, (B, Hv, Dv, Dk), torch.float32, dev)
     if out is None:

@@ -61,6 +61,11 @@ int make_plan(const gdn_shape *s, Plan *p) {
     return GDN_OK;
 }
 
+// The saved-for-backward buffer `ckpt`: the chunk-start states [B,Hv,NC,Dv,Dk], then (from a
+// 256-byte boundary) the residuals v_t - u_t [B,T,Hv,Dv], all fp32.
+size_t ckpt_state_bytes(const Plan &p) { return round_up((size_t)p.B * p.Hv * p.NC * p.Dv * p.Dk * sizeof(float)); }
+size_t ckpt_resid_bytes(const Plan &p) { return (size_t)p.B * p.T * p.Hv * p.Dv * sizeof(float); }
+
 struct Workspace {
     size_t dq, dk, dg, db, state, total;  // byte offsets and total
 };
@@ -155,7 +160,7 @@ extern "C" {
 size_t gdn_ckpt_bytes(const gdn_shape *shape) {
     Plan p;
     if (make_plan(shape, &p) != GDN_OK) return 0;
-    return (size_t)p.B * p.Hv * p.NC * p.Dv * p.Dk * sizeof(float);
+    return ckpt_state_bytes(p) + ckpt_resid_bytes(p);
 }
 
 size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
@@ -177,6 +182,7 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     gdn::FwdParams fp;
     fp.q = q; fp.k = k; fp.v = v; fp.g = g; fp.beta = beta; fp.S0 = S0;
     fp.y = y; fp.S_T = S_T; fp.ckpt = ckpt;
+    fp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
     fp.B = p.B; fp.T = p.T; fp.Hk = p.Hk; fp.Hv = p.Hv; fp.Dv = p.Dv; fp.C = p.C; fp.NC = p.NC;
     rc = device_status_address(&fp.status);
     if (rc != GDN_OK) return rc;
@@ -204,6 +210,7 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
 
     gdn::BwdParams bp;
     bp.q = q; bp.k = k; bp.v = v; bp.g = g; bp.beta = beta; bp.ckpt = ckpt; bp.dy = dy;
+    bp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
     bp.dS_T = dS_T; bp.dS0 = dS0; bp.dv = dv;
     bp.ws_dq = reinterpret_cast<float *>(ws + w.dq);
     bp.ws_dk = reinterpret_cast<float *>(ws + w.dk);

@@ -18,8 +18,10 @@
 //
 // Checkpointing (mlx-lm PR #1217, "What this PR adds": forward-with-save, then a reverse
 // sweep in the same chunked layout). Per chunk, going backwards:
-//   pass A  re-runs the chunk from its checkpoint, keeping delta_t and v_t - u_t per row
-//           and step in shared memory and the state at the start of every sub-block of
+//   pass A  re-runs the chunk from its checkpoint with the forward's own residuals
+//           v_t - u_t (delta_t = beta_t (v_t - u_t), so no prediction dot: the states are
+//           the forward's, bit for bit), keeping delta_t and v_t - u_t per row and step in
+//           shared memory and the state at the start of every sub-block of
 //           SUB = bwd_sub(Dk) steps in an L2-resident scratch;
 //   per sub-block, going backwards:
 //     pass B  takes the sub-block's start state (1-D TMA bulk copy, issued one sub-block
@@ -36,7 +38,7 @@
 // are complete per lane. What a compute warp keeps between steps (delta, v - u, its rows
 // of the states) is its own, so compute warps never wait for one another.
 //   stager warp   stages every tile one tile ahead into a double buffer (k and q rows by
-//                 TMA, widened to fp32; v or dy, g, beta and k . q per step, the global
+//                 TMA, widened to fp32; v - u or dy, g, beta and k . q per step, the global
 //                 loads issued a tile earlier still) and issues the start-state copies;
 //   reducer warp  sums the compute warps' per-step partials (columns of dq and dk, dg,
 //                 dbeta) in ascending warp order out of a ring of slots into fp32
@@ -96,7 +98,7 @@ struct BwdSmem {
         size_t o = 0;
         raw = o; o += align_upb((size_t)2 * 2 * TR * DK * esize, 128);   // [buf][k|q][TR][DK], input type
         kfq = o; o += (size_t)2 * 2 * TR * DK * 4;                        // [buf][k|q][TR][DK], fp32
-        xrow = o; o += (size_t)2 * SUB * RB * 4;                           // [buf][SUB][RB]: v or dy
+        xrow = o; o += (size_t)2 * SUB * RB * 4;                           // [buf][SUB][RB]: v - u or dy
         gsc = o; o += (size_t)2 * 4 * SUB * 4;                             // [buf][g | beta | k.q | -][SUB]
         dl = o; o += (size_t)C * RB * 4;                                   // delta per step and row
         vm = o; o += (size_t)C * RB * 4;                                   // v - u per step and row
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     regs_dec<kBwdServiceRegs>();
     if (warp == kStager) {
         // =============================== stager warp ===============================
-        const TIn *v = static_cast<const TIn *>(p.v);
+        const float *resid = p.resid;
         const TIn *dy = static_cast<const TIn *>(p.dy);
         const TIn *g = static_cast<const TIn *>(p.g);
         const TIn *beta = static_cast<const TIn *>(p.beta);
@@ -228,20 +230,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (t.kind == 1) tma_load_4d(dst + TR * DK, &tm_q, &bar[kBarRaw + rb], 0, hk, s0 - 1, b);
             ++raw_issued[rb];
         };
-        // per-step inputs of a tile, loaded into registers one tile before they are staged
-        QuadT xq[kQ];
+        // per-step inputs of a tile, loaded into registers one tile before they are staged:
+        // dy (input type) for reverse tiles, v - u (fp32) for pass-A tiles
+        constexpr bool kWide = IsF32B<TIn>::value;   // dy quads are 16 bytes (else 8)
+        uint4 xq[kQ];                               // raw bits of 4 consecutive rows
         float gq = 1.f, bq = 0.f;
         auto fetch = [&](TileRef t) {
             int s0, slen;
             slice_of(t, s0, slen);
-            const TIn *x_in = t.kind == 1 ? dy : v;
             constexpr int nq = RB / 4;
 #pragma unroll
             for (int i = 0; i < kQ; ++i) {
                 const int e = lane + 32 * i, j = e / nq, r4 = (e - j * nq) * 4;
-                xq[i] = QuadB<TIn>::zero();
-                if (j < slen && row0 + r4 < Dv)
-                    xq[i] = *reinterpret_cast<const QuadT *>(x_in + (((size_t)b * T + s0 + j) * Hv + h) * Dv + row0 + r4);
+                const size_t o = (((size_t)b * T + s0 + j) * Hv + h) * Dv + row0 + r4;
+                const bool in = j < slen && row0 + r4 < Dv;
+                if (t.kind == 1 && !kWide) {
+                    const uint2 u = in ? *reinterpret_cast<const uint2 *>(dy + o) : make_uint2(0u, 0u);
+                    xq[i] = make_uint4(u.x, u.y, 0u, 0u);
+                } else {
+                    const void *src = t.kind == 1 ? static_cast<const void *>(dy + o) : static_cast<const void *>(resid + o);
+                    xq[i] = in ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             gq = lane < slen ? to_f32(g[((size_t)b * T + s0 + lane) * Hv + h]) : 1.f;
             bq = lane < slen ? to_f32(beta[((size_t)b * T + s0 + lane) * Hv + h]) : 0.f;
@@ -259,7 +268,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int i = 0; i < kQ; ++i) {
                 const int e = lane + 32 * i;
-                if (e < SUB * nq) *reinterpret_cast<float4 *>(xr + 4 * e) = QuadB<TIn>::unpack(xq[i]);
+                if (e < SUB * nq) {
+                    const uint4 u = xq[i];
+                    *reinterpret_cast<float4 *>(xr + 4 * e) =
+                        (t.kind == 1 && !kWide)
+                            ? make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                                          __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u))
+                            : make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                          __uint_as_float(u.w));
+                }
             }
             if (lane < SUB) {
                 gs[lane] = gq;
@@ -480,26 +497,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         float2 kv[P2];
 #pragma unroll
                         for (int m = 0; m < P2; ++m) kv[m] = load_pair(kf + (j + 1) * DK, m);
-                        float part[R];
-#pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                            for (int m = 0; m < P2; ++m) acc = __ffma2_rn(S[r][m], kv[m], acc);
-                            part[r] = acc.x + acc.y;
-                        }
-                        const float a = group_transpose_reduce<R, 32>(part, lane);
                         const float gt = gs[j], bt = gs[SUB + j];
-                        const float vmv = xr[j * RB + wrow + my_row] - gt * a;
-                        const float dlv = bt * vmv;
-                        if ((lane & 3) == 0) {
-                            dl_s[(s0 - t0 + j) * RB + wrow + my_row] = dlv;
-                            vm_s[(s0 - t0 + j) * RB + wrow + my_row] = vmv;
+                        // v - u of the warp's rows (the forward's residuals); delta = beta (v - u)
+                        const float *xw = xr + j * RB + wrow;
+                        if (lane < R) {
+                            const float x = xw[lane];
+                            dl_s[(s0 - t0 + j) * RB + wrow + lane] = bt * x;
+                            vm_s[(s0 - t0 + j) * RB + wrow + lane] = x;
                         }
+                        const float4 x0 = *reinterpret_cast<const float4 *>(xw);
+                        const float4 x1 = *reinterpret_cast<const float4 *>(xw + 4);
+                        const float xv[R] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
                         const float2 gg = make_float2(gt, gt);
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
-                            const float d = __shfl_sync(kFullMask, dlv, 4 * r);
+                            const float d = bt * xv[r];
                             const float2 dd = make_float2(d, d);
 #pragma unroll
                             for (int m = 0; m < P2; ++m) S[r][m] = __ffma2_rn(dd, kv[m], __fmul2_rn(gg, S[r][m]));

@@ -27,6 +27,7 @@ struct FwdParams {
     const float *S0;
     void *y;
     float *S_T, *ckpt;
+    float *resid;           // [B, T, Hv, Dv] v_t - u_t, kept for the backward; may be null
     int *status;            // device status word (bounded-wait timeouts), may be null
     int B, T, Hk, Hv, Dv, C, NC;
 };
@@ -34,6 +35,7 @@ struct FwdParams {
 struct BwdParams {
     const void *q, *k, *v, *g, *beta;
     const float *ckpt;
+    const float *resid;     // [B, T, Hv, Dv] v_t - u_t as written by the forward
     const void *dy;
     const float *dS_T;
     float *dS0;

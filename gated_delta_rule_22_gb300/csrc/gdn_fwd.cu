@@ -17,6 +17,10 @@
 // reduction; the lane that ends up with row r's `an` computes
 // delta_{t+1} = beta_{t+1} (v_{t+1} - g_{t+1} an) and shares it with a shuffle.
 //
+// Residuals: v_t - u_t of every step and row is kept (fp32, staged per tile like y) for the
+// backward, whose re-computation then applies the same delta_t = beta_t (v_t - u_t) as the
+// forward instead of forming the prediction dot again.
+//
 // Staging: k and q arrive by TMA (tiled 4-D tensor maps, one tile of kFwdTile steps
 // ahead, two buffers, mbarrier completion); v, g and beta are loaded one tile ahead into
 // registers. Each tile starts with a prediction dot against its first k, so no tile
@@ -60,7 +64,7 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 
 // Shared-memory layout of fwd_kernel (byte offsets from a 128-byte aligned base).
 struct FwdSmem {
-    size_t raw, fk, fq, fv, fy, fg, fb, bar, total;
+    size_t raw, fk, fq, fv, fy, fr, fg, fb, bar, total;
     __host__ __device__ FwdSmem(int DK, int RB, int esize, bool conv) {
         const int TS = kFwdTile;
         size_t o = 0;
@@ -69,6 +73,7 @@ struct FwdSmem {
         fq = o; if (conv) o += (size_t)TS * DK * 4;                        // fp32 q rows
         fv = o; o += (size_t)TS * RB * 4;
         fy = o; o += (size_t)TS * RB * 4;
+        fr = o; o += (size_t)TS * RB * 4;                                  // v - u per step and row
         fg = o; o += TS * 4;
         fb = o; o += TS * 4;
         bar = align_up(o, 8); o = bar + 2 * 8;
@@ -102,6 +107,7 @@ __global__ void __launch_bounds__(256, 1)
     float *fq = reinterpret_cast<float *>(base + L.fq);
     float *fv = reinterpret_cast<float *>(base + L.fv);
     float *fy = reinterpret_cast<float *>(base + L.fy);
+    float *fr = reinterpret_cast<float *>(base + L.fr);
     float *fg = reinterpret_cast<float *>(base + L.fg);
     float *fb = reinterpret_cast<float *>(base + L.fb);
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
@@ -215,7 +221,9 @@ __global__ void __launch_bounds__(256, 1)
                 part[r] = acc.x + acc.y;
             }
             const float a = group_transpose_reduce<R, G>(part, lane);      // row lrow + (gl >> 2)
-            const float d0 = fb[0] * (fv[own_row] - fg[0] * a);
+            const float r0 = fv[own_row] - fg[0] * a;
+            const float d0 = fb[0] * r0;
+            if ((gl & 3) == 0) fr[own_row] = r0;
 #pragma unroll
             for (int r = 0; r < R; ++r) delta[r] = __shfl_sync(kFullMask, d0, (lane & 16) + 4 * r);
         }
@@ -265,7 +273,9 @@ __global__ void __launch_bounds__(256, 1)
             const float tot = group_transpose_reduce<2 * R, G>(red, lane);
             if ((gl & 3) == 0) fy[tt * RB + own_row] = tot;
             if (tt + 1 < tl) {
-                const float dn = fb[tt + 1] * (fv[(tt + 1) * RB + own_row] - fg[tt + 1] * tot);
+                const float rn = fv[(tt + 1) * RB + own_row] - fg[tt + 1] * tot;
+                const float dn = fb[tt + 1] * rn;
+                if ((gl & 3) == 2) fr[(tt + 1) * RB + own_row] = rn;
 #pragma unroll
                 for (int r = 0; r < R; ++r) delta[r] = __shfl_sync(kFullMask, dn, (lane & 16) + 4 * r + 2);
             }
@@ -273,7 +283,11 @@ __global__ void __launch_bounds__(256, 1)
         __syncthreads();
         for (int e = tid; e < tl * RB; e += nthreads) {
             const int tt = e / RB, rr = e - tt * RB, row = row0 + rr;
-            if (row < Dv) y[(((size_t)b * T + t0 + tt) * Hv + h) * Dv + row] = from_f32<TIn>(fy[e]);
+            if (row < Dv) {
+                const size_t o = (((size_t)b * T + t0 + tt) * Hv + h) * Dv + row;
+                y[o] = from_f32<TIn>(fy[e]);
+                if (p.resid != nullptr) p.resid[o] = fr[e];
+            }
         }
     }
     if (p.S_T != nullptr) {

@@ -82,7 +82,9 @@ enum {
                                        GDN_BWD_NOALLOC_SCRATCH_BYTES */
 };
 
-/* Bytes of the checkpoint buffer gdn_fwd writes: B*Hv*NC*Dv*Dk*4. 0 for an invalid shape. */
+/* Bytes of the saved-for-backward buffer `ckpt` that gdn_fwd writes: the chunk-start states
+ * (B*Hv*NC*Dv*Dk*4 bytes, rounded up to a multiple of 256) followed by the per-step
+ * residuals v_t - u_t (B*T*Hv*Dv*4 bytes). 0 for an invalid shape. */
 GDN_API size_t gdn_ckpt_bytes(const gdn_shape *shape);
 
 /* Bytes of device scratch gdn_bwd needs (fp32 partial sums for the fixed-order
@@ -95,8 +97,11 @@ GDN_API size_t gdn_bwd_workspace_bytes(const gdn_shape *shape);
  *        S0                          (float32, may be NULL: zeros)
  *   out: y                           (dtype)
  *        S_T                         (float32, may be NULL: not written)
- *        ckpt                        (float32, gdn_ckpt_bytes(shape) bytes):
- *                                    ckpt[b, h, c] = state before step c*C
+ *        ckpt                        (float32, gdn_ckpt_bytes(shape) bytes, 16-byte aligned):
+ *                                    ckpt[b, h, c] = state before step c*C, [B,Hv,NC,Dv,Dk];
+ *                                    then, from the next 256-byte boundary, the residuals
+ *                                    r[b, t, h, :] = v_t - u_t, u_t = g_t S_{t-1} k_t,
+ *                                    [B,T,Hv,Dv] (what the backward re-computes from)
  * Returns GDN_OK or an error code.
  */
 GDN_API int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
@@ -108,8 +113,8 @@ GDN_API int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const 
  * beta and S0, for the forward defined by the same inputs. The pages print no backward
  * formula; this is the chain rule applied to the recurrence above, in reverse time.
  *   in : q, k, v, g, beta, dy        (dtype)
- *        ckpt                        (float32) as written by gdn_fwd for the same inputs,
- *                                    shape and S0
+ *        ckpt                        (float32, gdn_ckpt_bytes(shape) bytes) as written by
+ *                                    gdn_fwd for the same inputs, shape and S0
  *        dS_T                        (float32, may be NULL: zeros)
  *   out: dq, dk                      (dtype) summed over the value heads of each kv head,
  *                                    in ascending value-head order

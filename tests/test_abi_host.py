@@ -60,7 +60,9 @@ def test_checkpoint_bytes(lib):
     for T, C in ((16, 0), (37, 16), (1, 1), (128, 128), (2048, 64)):
         s = shape(T=T, chunk=C, Hv=6, Hk=3, Dk=96, Dv=20)
         nc = -(-T // (C or 64))
-        assert lib.gdn_ckpt_bytes(ctypes.byref(s)) == 1 * 6 * nc * 20 * 96 * 4
+        states = -(-(1 * 6 * nc * 20 * 96 * 4) // 256) * 256   # chunk-start states, 256-byte rounded
+        resid = 1 * T * 6 * 20 * 4                              # v - u per step and row
+        assert lib.gdn_ckpt_bytes(ctypes.byref(s)) == states + resid
     assert lib.gdn_ckpt_bytes(ctypes.byref(shape(Hv=3))) == 0
     assert lib.gdn_ckpt_bytes(None) == 0
 
