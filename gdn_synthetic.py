@@ -19,6 +19,18 @@ stream, drawn in the order
 (normal(mean, std), as numpy takes it). The "half" decay mode gives value heads
 h < Hv/2 the strong mean and the rest the weak one, the same for every batch row.
 
+Gate inputs (make_gate_inputs). No page gives a recipe for the layer's raw gate inputs;
+the reading taken draws, from its own stream, in the order
+
+    a       ~ N(mu_a, 0.5)                       [B, T, Hv]   mu_a = +8 strong, -2 weak
+    b       ~ N(0, 1)                            [B, T, Hv]   (the beta logits above)
+    A_log   ~ N(0, 0.5)                          [Hv]
+    dt_bias ~ N(0, 0.5)                          [Hv]
+    dg      ~ N(0, 1), dbeta ~ N(0, 1)           [B, T, Hv]   (cotangents)
+
+so that through the layer's gate map the mean log g lands near the strong (-8.4) and weak
+(-0.15) profiles of the accuracy table. The "half" mode splits the heads as above.
+
 Every array is returned as float32 holding exactly the value the kernels receive:
 for bf16 workloads q, k, v, g, beta and dy are rounded to bf16 (round to nearest
 even) and kept as float32 (an exact embedding). Widening to float64 for the oracle
@@ -110,3 +122,29 @@ def make_inputs(w: Workload | None = None, **kw) -> dict:
         raise ValueError(f"unknown dtype {w.dtype!r}")
     return {"workload": w, "q": q, "k": k, "v": v, "g": g, "beta": beta, "dy": dy,
             "S0": S0, "dS_T": dS_T, "mean_log_g": float(log_g.mean())}
+
+
+def make_gate_inputs(w: Workload) -> dict:
+    """Draw the raw gate inputs of a workload (see the module docstring). a, b, dg, dbeta
+    are rounded to bf16 for bf16 workloads; A_log and dt_bias are float32 parameters."""
+    rng = np.random.default_rng(w.seed + 1)
+    B, T, Hv = w.B, w.T, w.Hv
+    if w.decay == "strong":
+        mu = 8.0
+    elif w.decay == "weak":
+        mu = -2.0
+    elif w.decay == "half":
+        mu = np.where(np.arange(Hv) < Hv // 2, 8.0, -2.0)[None, None, :]
+    else:
+        raise ValueError(f"unknown decay mode {w.decay!r}")
+    a = rng.normal(mu, 0.5, (B, T, Hv)).astype(np.float32)
+    b = rng.standard_normal((B, T, Hv)).astype(np.float32)
+    A_log = rng.normal(0.0, 0.5, Hv).astype(np.float32)
+    dt_bias = rng.normal(0.0, 0.5, Hv).astype(np.float32)
+    dg = rng.standard_normal((B, T, Hv)).astype(np.float32)
+    dbeta = rng.standard_normal((B, T, Hv)).astype(np.float32)
+    if w.dtype == "bf16":
+        a, b, dg, dbeta = (round_to_bf16(x) for x in (a, b, dg, dbeta))
+    elif w.dtype != "f32":
+        raise ValueError(f"unknown dtype {w.dtype!r}")
+    return {"workload": w, "a": a, "b": b, "A_log": A_log, "dt_bias": dt_bias, "dg": dg, "dbeta": dbeta}

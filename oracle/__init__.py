@@ -10,8 +10,10 @@ Functions
 fwd(q, k, v, g, beta, S0=None, chunk=64)  -> dict(y, S_T, ckpt)
 bwd(q, k, v, g, beta, dy, S0=None, dS_T=None, chunk=64)
                                           -> dict(dq, dk, dv, dg, dbeta, dS0)
-Layouts: q, k [B,T,Hk,Dk]; v, dy [B,T,Hv,Dv]; g, beta [B,T,Hv]; states [B,Hv,Dv,Dk];
-ckpt [B,Hv,NC,Dv,Dk] with ckpt[:, :, c] the state before step c*chunk.
+gates_fwd(a, b, A_log, dt_bias)           -> dict(g, beta)
+gates_bwd(a, b, A_log, dt_bias, dg, dbeta) -> dict(da, db, dA_log, ddt_bias)
+Layouts: q, k [B,T,Hk,Dk]; v, dy [B,T,Hv,Dv]; g, beta, a, b [B,T,Hv]; A_log, dt_bias [Hv];
+states [B,Hv,Dv,Dk]; ckpt [B,Hv,NC,Dv,Dk] with ckpt[:, :, c] the state before step c*chunk.
 """
 from __future__ import annotations
 
@@ -62,6 +64,10 @@ def load(path: str | None = None):
     lib.oracle_n_chunks.restype = ctypes.c_int
     lib.oracle_n_chunks.argtypes = [ctypes.POINTER(OracleShape)]
     lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_gates_fwd.restype = ctypes.c_int
+    lib.oracle_gates_fwd.argtypes = [ctypes.c_int, ctypes.c_int] + [_P] * 6
+    lib.oracle_gates_bwd.restype = ctypes.c_int
+    lib.oracle_gates_bwd.argtypes = [ctypes.c_int, ctypes.c_int] + [_P] * 10
     return lib
 
 
@@ -124,6 +130,35 @@ def bwd(q, k, v, g, beta, dy, S0=None, dS_T=None, chunk=64, nthreads=0, lib=None
     if rc != 0:
         raise RuntimeError(f"oracle_bwd failed with code {rc}")
     return {"dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": dbeta, "dS0": dS0}
+
+
+def gates_fwd(a, b, A_log, dt_bias, lib=None):
+    lib = lib or _lib()
+    a, b, A_log, dt_bias = (_f64(x) for x in (a, b, A_log, dt_bias))
+    Hv = a.shape[-1]
+    BT = a.size // Hv
+    g = np.empty(a.shape)
+    beta = np.empty(a.shape)
+    rc = lib.oracle_gates_fwd(BT, Hv, _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(g), _ptr(beta))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gates_fwd failed with code {rc}")
+    return {"g": g, "beta": beta}
+
+
+def gates_bwd(a, b, A_log, dt_bias, dg, dbeta, lib=None):
+    lib = lib or _lib()
+    a, b, A_log, dt_bias, dg, dbeta = (_f64(x) for x in (a, b, A_log, dt_bias, dg, dbeta))
+    Hv = a.shape[-1]
+    BT = a.size // Hv
+    da = np.empty(a.shape)
+    db = np.empty(a.shape)
+    dA_log = np.empty(Hv)
+    ddt_bias = np.empty(Hv)
+    rc = lib.oracle_gates_bwd(BT, Hv, _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(dg), _ptr(dbeta),
+                              _ptr(da), _ptr(db), _ptr(dA_log), _ptr(ddt_bias))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gates_bwd failed with code {rc}")
+    return {"da": da, "db": db, "dA_log": dA_log, "ddt_bias": ddt_bias}
 
 
 def loss(out_fwd, dy, dS_T=None) -> float:

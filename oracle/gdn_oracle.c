@@ -40,9 +40,20 @@
  * operations on the same stored state reproduces the same values bit for bit, so
  * this changes memory use only, not the result.
  *
+ * Gates (oracle_gates_fwd / oracle_gates_bwd): the decay and write strength computed
+ *   from the layer's trainable gate inputs. mlx-lm PR #1217 ("Correctness") checks the
+ *   gradients of eight trainable inputs, q, k, v, a, b, A_log, dt_bias and the state,
+ *   but no page prints how g and beta follow from a, b, A_log and dt_bias. The reading
+ *   taken is the public mlx-lm Qwen3-Next / Qwen3.5 linear-attention layer's:
+ *       log g[b,t,h] = -exp(A_log[h]) * softplus(a[b,t,h] + dt_bias[h]),  g = exp(log g)
+ *       beta[b,t,h]  = sigmoid(b[b,t,h])
+ *   and its VJP goes through log g (mlx issue #4614 warns that the g-gradient is what a
+ *   log_g parameterisation trains through): d(log g) = g * dg, never dg / something.
+ *
  * Build: plain C99, no fused multiply-add contraction (-ffp-contract=off), optional
  * OpenMP over independent (batch row, value head) pairs.
  */
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 #include <stddef.h>
@@ -311,4 +322,54 @@ int oracle_max_threads(void) {
 #else
     return 1;
 #endif
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Gates. a, b, g, beta, da, db, dg, dbeta are [BT, Hv] (BT = B*T rows); A_log, dt_bias,  */
+/* dA_log, ddt_bias are [Hv]. The parameter gradients are sums over the BT rows, added in */
+/* ascending row order.                                                                   */
+
+static double softplus_d(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
+
+static double sigmoid_d(double x) {
+    if (x >= 0.0) return 1.0 / (1.0 + exp(-x));
+    const double e = exp(x);
+    return e / (1.0 + e);
+}
+
+int oracle_gates_fwd(int BT, int Hv, const double *a, const double *b, const double *A_log,
+                     const double *dt_bias, double *g, double *beta) {
+    if (BT <= 0 || Hv <= 0 || !a || !b || !A_log || !dt_bias || !g || !beta) return ORACLE_EINVAL;
+    for (int i = 0; i < BT; ++i)
+        for (int h = 0; h < Hv; ++h) {
+            const size_t o = (size_t)i * Hv + h;
+            const double log_g = -exp(A_log[h]) * softplus_d(a[o] + dt_bias[h]);
+            g[o] = exp(log_g);
+            beta[o] = sigmoid_d(b[o]);
+        }
+    return ORACLE_OK;
+}
+
+int oracle_gates_bwd(int BT, int Hv, const double *a, const double *b, const double *A_log,
+                     const double *dt_bias, const double *dg, const double *dbeta, double *da,
+                     double *db, double *dA_log, double *ddt_bias) {
+    if (BT <= 0 || Hv <= 0 || !a || !b || !A_log || !dt_bias || !dg || !dbeta || !da || !db ||
+        !dA_log || !ddt_bias)
+        return ORACLE_EINVAL;
+    for (int h = 0; h < Hv; ++h) { dA_log[h] = 0.0; ddt_bias[h] = 0.0; }
+    for (int i = 0; i < BT; ++i)
+        for (int h = 0; h < Hv; ++h) {
+            const size_t o = (size_t)i * Hv + h;
+            const double A = exp(A_log[h]);
+            const double x = a[o] + dt_bias[h];
+            const double log_g = -A * softplus_d(x);
+            const double dlog_g = exp(log_g) * dg[o];        /* d(log g) = g dg */
+            const double dx = dlog_g * (-A) * sigmoid_d(x);   /* softplus' = sigmoid */
+            da[o] = dx;
+            ddt_bias[h] += dx;
+            dA_log[h] += dlog_g * log_g;                      /* d(log g)/d(A_log) = log g */
+            const double bt = sigmoid_d(b[o]);
+            db[o] = dbeta[o] * bt * (1.0 - bt);
+        }
+    return ORACLE_OK;
 }
