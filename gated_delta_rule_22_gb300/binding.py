@@ -54,6 +54,10 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_bwd.argtypes = [SP] + [_VP] * 15 + [ctypes.c_size_t, _VP]
     lib.gdn_bwd_noalloc.restype = ctypes.c_int
     lib.gdn_bwd_noalloc.argtypes = [SP] + [_VP] * 15
+    lib.gdn_gates_fwd.restype = ctypes.c_int
+    lib.gdn_gates_fwd.argtypes = [SP] + [_VP] * 7
+    lib.gdn_gates_bwd.restype = ctypes.c_int
+    lib.gdn_gates_bwd.argtypes = [SP] + [_VP] * 11
     lib.gdn_strerror.restype = ctypes.c_char_p
     lib.gdn_strerror.argtypes = [ctypes.c_int]
     lib.gdn_last_error.restype = ctypes.c_char_p
@@ -158,9 +162,10 @@ def _shape_of(q, v, chunk):
 
 
 def gdn_fwd(q, k, v, g, beta, S0=None, chunk=64, *, y=None, S_T=None, ckpt=None, want_S_T=True,
-            stream=None):
+            want_ckpt=True, stream=None):
     """y, S_T, ckpt = gdn_fwd(q, k, v, g, beta[, S0]) on CUDA tensors (see include/gdn.h).
-    ckpt is the [B, Hv, NC, Dv, Dk] view of the saved-for-backward buffer (new_ckpt)."""
+    ckpt is the [B, Hv, NC, Dv, Dk] view of the saved-for-backward buffer (new_ckpt), or None
+    with want_ckpt=False (inference / decode: nothing is saved)."""
     torch = _torch()
     lib = load_library()
     shape = _shape_of(q, v, chunk)
@@ -177,9 +182,10 @@ def gdn_fwd(q, k, v, g, beta, S0=None, chunk=64, *, y=None, S_T=None, ckpt=None,
         y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
     if S_T is None and want_S_T:
         S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
-    if ckpt is None:
+    if ckpt is None and want_ckpt:
         ckpt = new_ckpt(q, v, chunk)
-    _check_ckpt(ckpt, q, v, chunk)
+    if ckpt is not None:
+        _check_ckpt(ckpt, q, v, chunk)
     rc = lib.gdn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0),
                      _ptr(y), _ptr(S_T), _ptr(ckpt), _stream(stream))
     if rc != GDN_OK:
@@ -215,4 +221,50 @@ def gdn_bwd(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, workspace=None, 
                      workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != GDN_OK:
         raise GdnError("gdn_bwd", rc, lib)
+    return out
+
+
+def _gate_shape(a, Hk, Dk, Dv):
+    B, T, Hv = a.shape
+    return make_shape(B, T, Hk, Hv, Dk, Dv, 64, _dtype_code(a))
+
+
+def gdn_gates_fwd(a, b, A_log, dt_bias, *, Hk=None, Dk=32, Dv=4, stream=None):
+    """g, beta = gdn_gates_fwd(a, b, A_log, dt_bias) on CUDA tensors (see include/gdn.h).
+    a, b [B, T, Hv] (float32 or bfloat16); A_log, dt_bias [Hv] float32. Hk, Dk, Dv only
+    complete the layer shape the library checks (defaults: Hk = Hv, Dk = 32, Dv = 4)."""
+    torch = _torch()
+    lib = load_library()
+    B, T, Hv = a.shape
+    _check("a", a, (B, T, Hv), a.dtype, a.device)
+    _check("b", b, (B, T, Hv), a.dtype, a.device)
+    _check("A_log", A_log, (Hv,), torch.float32, a.device)
+    _check("dt_bias", dt_bias, (Hv,), torch.float32, a.device)
+    shape = _gate_shape(a, Hk or Hv, Dk, Dv)
+    g = torch.empty_like(a)
+    beta = torch.empty_like(a)
+    rc = lib.gdn_gates_fwd(ctypes.byref(shape), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(g),
+                           _ptr(beta), _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError("gdn_gates_fwd", rc, lib)
+    return g, beta
+
+
+def gdn_gates_bwd(a, b, A_log, dt_bias, dg, dbeta, *, Hk=None, Dk=32, Dv=4, stream=None):
+    """dict(da, db, dA_log, ddt_bias) = gdn_gates_bwd(...) on CUDA tensors (see include/gdn.h)."""
+    torch = _torch()
+    lib = load_library()
+    B, T, Hv = a.shape
+    for name, t in (("a", a), ("b", b), ("dg", dg), ("dbeta", dbeta)):
+        _check(name, t, (B, T, Hv), a.dtype, a.device)
+    _check("A_log", A_log, (Hv,), torch.float32, a.device)
+    _check("dt_bias", dt_bias, (Hv,), torch.float32, a.device)
+    shape = _gate_shape(a, Hk or Hv, Dk, Dv)
+    out = {"da": torch.empty_like(a), "db": torch.empty_like(a),
+           "dA_log": torch.empty_like(A_log), "ddt_bias": torch.empty_like(dt_bias)}
+    rc = lib.gdn_gates_bwd(ctypes.byref(shape), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(dg),
+                           _ptr(dbeta), _ptr(out["da"]), _ptr(out["db"]), _ptr(out["dA_log"]),
+                           _ptr(out["ddt_bias"]), _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError("gdn_gates_bwd", rc, lib)
     return out

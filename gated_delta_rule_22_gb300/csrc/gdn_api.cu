@@ -174,7 +174,7 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     Plan p;
     int rc = make_plan(shape, &p);
     if (rc != GDN_OK) return rc;
-    if (!q || !k || !v || !g || !beta || !y || !ckpt) return GDN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !g || !beta || !y) return GDN_ERR_INVALID_ARG;
     const void *all[] = {q, k, v, g, beta, S0, y, S_T, ckpt};
     for (const void *ptr : all)
         if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
@@ -182,7 +182,7 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     gdn::FwdParams fp;
     fp.q = q; fp.k = k; fp.v = v; fp.g = g; fp.beta = beta; fp.S0 = S0;
     fp.y = y; fp.S_T = S_T; fp.ckpt = ckpt;
-    fp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
+    fp.resid = ckpt != nullptr ? ckpt + ckpt_state_bytes(p) / sizeof(float) : nullptr;
     fp.B = p.B; fp.T = p.T; fp.Hk = p.Hk; fp.Hv = p.Hv; fp.Dv = p.Dv; fp.C = p.C; fp.NC = p.NC;
     rc = device_status_address(&fp.status);
     if (rc != GDN_OK) return rc;
@@ -234,6 +234,43 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     rc = cuda_status(gdn::launch_bwd(bp, tm_q, tm_k, p.Dk, p.dtype, (cudaStream_t)stream));
     if (rc != GDN_OK) return rc;
     return cuda_status(gdn::launch_reduce(rp, p.dtype, (cudaStream_t)stream));
+}
+
+int gdn_gates_fwd(const gdn_shape *shape, const void *a, const void *b, const float *A_log,
+                  const float *dt_bias, void *g, void *beta, void *stream) {
+    Plan p;
+    int rc = make_plan(shape, &p);
+    if (rc != GDN_OK) return rc;
+    if ((long long)p.B * p.T > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!a || !b || !A_log || !dt_bias || !g || !beta) return GDN_ERR_INVALID_ARG;
+    const void *all[] = {a, b, A_log, dt_bias, g, beta};
+    for (const void *ptr : all)
+        if (!aligned(ptr)) return GDN_ERR_MISALIGNED;
+    g_last_error[0] = '\0';
+    gdn::GatesParams gp = {};
+    gp.a = a; gp.b = b; gp.A_log = A_log; gp.dt_bias = dt_bias; gp.g = g; gp.beta = beta;
+    gp.rows = p.B * p.T; gp.Hv = p.Hv;
+    return cuda_status(gdn::launch_gates_fwd(gp, p.dtype, (cudaStream_t)stream));
+}
+
+int gdn_gates_bwd(const gdn_shape *shape, const void *a, const void *b, const float *A_log,
+                  const float *dt_bias, const void *dg, const void *dbeta, void *da, void *db,
+                  float *dA_log, float *ddt_bias, void *stream) {
+    Plan p;
+    int rc = make_plan(shape, &p);
+    if (rc != GDN_OK) return rc;
+    if ((long long)p.B * p.T > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!a || !b || !A_log || !dt_bias || !dg || !dbeta || !da || !db || !dA_log || !ddt_bias)
+        return GDN_ERR_INVALID_ARG;
+    const void *all[] = {a, b, A_log, dt_bias, dg, dbeta, da, db, dA_log, ddt_bias};
+    for (const void *ptr : all)
+        if (!aligned(ptr)) return GDN_ERR_MISALIGNED;
+    g_last_error[0] = '\0';
+    gdn::GatesParams gp = {};
+    gp.a = a; gp.b = b; gp.A_log = A_log; gp.dt_bias = dt_bias; gp.dg = dg; gp.dbeta = dbeta;
+    gp.da = da; gp.db = db; gp.dA_log = dA_log; gp.ddt_bias = ddt_bias;
+    gp.rows = p.B * p.T; gp.Hv = p.Hv;
+    return cuda_status(gdn::launch_gates_bwd(gp, p.dtype, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -26,7 +26,7 @@ struct FwdParams {
     const void *q, *k, *v, *g, *beta;
     const float *S0;
     void *y;
-    float *S_T, *ckpt;
+    float *S_T, *ckpt;      // ckpt may be null (no backward follows: nothing is saved)
     float *resid;           // [B, T, Hv, Dv] v_t - u_t, kept for the backward; may be null
     int *status;            // device status word (bounded-wait timeouts), may be null
     int B, T, Hk, Hv, Dv, C, NC;
@@ -70,6 +70,18 @@ constexpr int kBwdComputeRegs = 216;
 constexpr int kBwdServiceRegs = 72;
 static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <= kBwdThreads * kBwdLaunchRegs,
               "register split exceeds the launch's registers");
+
+// Gate map (a, b, A_log, dt_bias -> g, beta) and its VJP; a, b, g, beta, dg, dbeta, da, db
+// are [rows = B*T, Hv] in the input type, the per-head parameters fp32.
+struct GatesParams {
+    const void *a, *b;
+    const float *A_log, *dt_bias;
+    void *g, *beta;
+    const void *dg, *dbeta;
+    void *da, *db;
+    float *dA_log, *ddt_bias;
+    int rows, Hv;
+};
 
 struct ReduceParams {
     const float *ws_dq, *ws_dk, *ws_dg, *ws_db;
@@ -283,5 +295,7 @@ cudaError_t launch_bwd(const BwdParams &p, const CUtensorMap &tm_q, const CUtens
 int bwd_slots(int Dk, int C, int dtype, size_t limit);
 size_t bwd_smem_bytes(int Dk, int C, int dtype, int slots);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s);
 
 }  // namespace gdn

@@ -231,16 +231,18 @@ __global__ void __launch_bounds__(256, 1)
         for (int tt = 0; tt < tl; ++tt) {
             const int t = t0 + tt;
             if (to_ckpt == 0) {
-                // checkpoint: the state before step t
+                // checkpoint: the state before step t (none without a saved-for-backward buffer)
                 to_ckpt = p.C;
-                float *ck = p.ckpt + (head * p.NC + t / p.C) * (size_t)Dv * DK;
+                if (p.ckpt != nullptr) {
+                    float *ck = p.ckpt + (head * p.NC + t / p.C) * (size_t)Dv * DK;
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int row = row0 + lrow + r;
-                    if (row < Dv) {
+                    for (int r = 0; r < R; ++r) {
+                        const int row = row0 + lrow + r;
+                        if (row < Dv) {
 #pragma unroll
-                        for (int m = 0; m < P; ++m)
-                            *reinterpret_cast<float2 *>(ck + (size_t)row * DK + col + 32 * m) = S[r][m];
+                            for (int m = 0; m < P; ++m)
+                                *reinterpret_cast<float2 *>(ck + (size_t)row * DK + col + 32 * m) = S[r][m];
+                        }
                     }
                 }
             }
@@ -281,12 +283,23 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
         __syncthreads();
-        for (int e = tid; e < tl * RB; e += nthreads) {
-            const int tt = e / RB, rr = e - tt * RB, row = row0 + rr;
+        // y and the residuals of the tile, four consecutive rows per access (Dv % 4 == 0)
+        for (int e = tid; e < tl * (RB / 4); e += nthreads) {
+            const int tt = e / (RB / 4), rr = (e - tt * (RB / 4)) * 4, row = row0 + rr;
             if (row < Dv) {
                 const size_t o = (((size_t)b * T + t0 + tt) * Hv + h) * Dv + row;
-                y[o] = from_f32<TIn>(fy[e]);
-                if (p.resid != nullptr) p.resid[o] = fr[e];
+                const float4 yv = *reinterpret_cast<const float4 *>(fy + tt * RB + rr);
+                if (kConv) {
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(yv.x, yv.y), hi = __floats2bfloat162_rn(yv.z, yv.w);
+                    uint2 u;
+                    u.x = *reinterpret_cast<const uint32_t *>(&lo);
+                    u.y = *reinterpret_cast<const uint32_t *>(&hi);
+                    *reinterpret_cast<uint2 *>(y + o) = u;
+                } else {
+                    *reinterpret_cast<float4 *>(y + o) = yv;
+                }
+                if (p.resid != nullptr)
+                    *reinterpret_cast<float4 *>(p.resid + o) = *reinterpret_cast<const float4 *>(fr + tt * RB + rr);
             }
         }
     }

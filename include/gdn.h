@@ -92,12 +92,15 @@ GDN_API size_t gdn_ckpt_bytes(const gdn_shape *shape);
 GDN_API size_t gdn_bwd_workspace_bytes(const gdn_shape *shape);
 
 /*
- * Forward with checkpoints.
+ * Forward with checkpoints (or, with ckpt = NULL, without: inference and decode, where no
+ * backward follows; a decode step is T = 1 with the carried state passed as S0 and read
+ * back from S_T).
  *   in : q, k, v, g, beta            (dtype)
  *        S0                          (float32, may be NULL: zeros)
  *   out: y                           (dtype)
  *        S_T                         (float32, may be NULL: not written)
- *        ckpt                        (float32, gdn_ckpt_bytes(shape) bytes, 16-byte aligned):
+ *        ckpt                        (float32, gdn_ckpt_bytes(shape) bytes, 16-byte aligned;
+ *                                    may be NULL: nothing saved):
  *                                    ckpt[b, h, c] = state before step c*C, [B,Hv,NC,Dv,Dk];
  *                                    then, from the next 256-byte boundary, the residuals
  *                                    r[b, t, h, :] = v_t - u_t, u_t = g_t S_{t-1} k_t,
@@ -159,6 +162,28 @@ GDN_API int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k
                             const void *g, const void *beta, const float *ckpt, const void *dy,
                             const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta,
                             float *dS0, void *stream);
+
+/*
+ * Gates of the layer: the decay g and write strength beta from its raw gate inputs, and the
+ * VJP back to them (mlx-lm PR #1217, "Correctness", trains through q, k, v, a, b, A_log,
+ * dt_bias and the state; no page prints the gate map, and the one taken is the public
+ * mlx-lm Qwen3-Next / Qwen3.5 linear-attention layer's). For every b, t and value head h:
+ *     log g = -exp(A_log[h]) * softplus(a[b,t,h] + dt_bias[h]),  g = exp(log g)
+ *     beta  = sigmoid(b[b,t,h])
+ * The VJP goes through log g (d log g = g dg), with da, db elementwise and dA_log[h],
+ * ddt_bias[h] summed over all b, t in a fixed order (deterministic).
+ *   a, b, g, beta, dg, dbeta, da, db   [B, T, Hv]  (dtype)
+ *   A_log, dt_bias, dA_log, ddt_bias   [Hv]        (float32)
+ * The shape is the layer's (the same as for gdn_fwd; Hk, Dk, Dv are checked but unused).
+ * All pointers are device pointers, 16-byte aligned, owned by the caller. The arithmetic is
+ * fp32 (the parameter sums fp64). Returns GDN_OK or an error code (checks as for gdn_fwd;
+ * B*T above 2^31-1 is GDN_ERR_UNSUPPORTED_SHAPE).
+ */
+GDN_API int gdn_gates_fwd(const gdn_shape *shape, const void *a, const void *b, const float *A_log,
+                          const float *dt_bias, void *g, void *beta, void *stream);
+GDN_API int gdn_gates_bwd(const gdn_shape *shape, const void *a, const void *b, const float *A_log,
+                          const float *dt_bias, const void *dg, const void *dbeta, void *da,
+                          void *db, float *dA_log, float *ddt_bias, void *stream);
 
 /* Static description of a return code. */
 GDN_API const char *gdn_strerror(int code);

@@ -90,8 +90,11 @@ def test_null_shape_and_pointers(lib):
     assert fwd(lib, None) == INVALID
     assert bwd(lib, None, ws_bytes=0) == INVALID
     s = shape()
-    for n in ("q", "k", "v", "g", "beta", "y", "ckpt"):
+    for n in ("q", "k", "v", "g", "beta", "y"):
         assert fwd(lib, s, **{n: None}) == INVALID, n
+    # the forward may run without a saved-for-backward buffer (inference / decode): a null
+    # ckpt passes the argument checks (shown here by the next check, alignment, firing)
+    assert fwd(lib, s, ckpt=None, q=FAKE + 4) == MISALIGNED
     for n in ("q", "k", "v", "g", "beta", "ckpt", "dy", "dq", "dk", "dv", "dg", "dbeta", "ws"):
         assert bwd(lib, s, **{n: None}) == INVALID, n
 
@@ -109,6 +112,29 @@ def test_workspace_too_small(lib):
     need = lib.gdn_bwd_workspace_bytes(ctypes.byref(s))
     assert bwd(lib, s, ws_bytes=need - 1) == WS_SMALL
     assert bwd(lib, s, ws_bytes=0) == WS_SMALL
+
+
+GATE_FWD = ("a", "b", "A_log", "dt_bias", "g", "beta")
+GATE_BWD = ("a", "b", "A_log", "dt_bias", "dg", "dbeta", "da", "db", "dA_log", "ddt_bias")
+
+
+def gates(lib, s, names, **ptrs):
+    p = {n: FAKE for n in names}
+    p.update(ptrs)
+    args = [ctypes.c_void_p(p[n]) if p[n] is not None else None for n in names]
+    f = lib.gdn_gates_fwd if names == GATE_FWD else lib.gdn_gates_bwd
+    return f(ctypes.byref(s) if s is not None else None, *args, None)
+
+
+def test_gate_argument_checks(lib):
+    s = shape()
+    for names in (GATE_FWD, GATE_BWD):
+        assert gates(lib, None, names) == INVALID
+        assert gates(lib, shape(Hv=3), names) == UNSUPPORTED        # Hv % Hk
+        assert gates(lib, shape(B=65535, T=40000), names) == UNSUPPORTED   # B*T >= 2^31
+        for n in names:
+            assert gates(lib, s, names, **{n: None}) == INVALID, n
+            assert gates(lib, s, names, **{n: FAKE + 4}) == MISALIGNED, n
 
 
 def test_error_strings(lib):
