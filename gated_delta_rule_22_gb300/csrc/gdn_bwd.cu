@@ -46,6 +46,8 @@
 // reduce_kernel then adds the row splits (ascending) and the value heads of each kv head
 // (ascending). Every hand-off is an mbarrier with a bounded wait; there are no atomics and
 // no block-wide barriers between set-up and tear-down.
+#include <type_traits>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -285,31 +287,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const TileRef nt = tile_after(t);
             if (nt.kind >= 0) fetch(nt);
             if (!mbar_wait(&bar[kBarRaw + bx], fx & 1)) return false;
-            // widen the k (and q) rows to fp32
-            const int rows = t.kind == 1 ? 2 * TR : TR;
+            // widen the k (and q) rows to fp32: 16 bytes of input per access, the loads of a
+            // batch issued back to back (trip counts are compile-time per tile kind)
             float *dstf = kfq + (size_t)bx * 2 * TR * DK;
             const TIn *src = raw + (size_t)bx * 2 * TR * DK;
-            if (IsF32B<TIn>::value) {
-                for (int i = lane; i < rows * DK / 4; i += 32)
-                    reinterpret_cast<float4 *>(dstf)[i] = reinterpret_cast<const float4 *>(src)[i];
-            } else {
-                for (int i = lane; i < rows * DK / 8; i += 32) {
-                    const uint4 w = reinterpret_cast<const uint4 *>(src)[i];
-                    float4 *d = reinterpret_cast<float4 *>(dstf + 8 * i);
-                    d[0] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-                    d[1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
-                                       __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+            auto widen = [&](auto rows_c) {
+                constexpr int ROWS = decltype(rows_c)::value;
+                constexpr int EPC = IsF32B<TIn>::value ? 4 : 8;   // elements per 16 bytes
+                constexpr int NCH = ROWS * DK / EPC;
+                constexpr int PER = (NCH + 31) / 32;
+                constexpr int BATCH = 4;
+#pragma unroll
+                for (int i0 = 0; i0 < PER; i0 += BATCH) {
+                    uint4 w[BATCH];
+#pragma unroll
+                    for (int u = 0; u < BATCH; ++u) {
+                        const int i = lane + 32 * (i0 + u);
+                        if (i0 + u < PER && i < NCH) w[u] = reinterpret_cast<const uint4 *>(src)[i];
+                    }
+#pragma unroll
+                    for (int u = 0; u < BATCH; ++u) {
+                        const int i = lane + 32 * (i0 + u);
+                        if (i0 + u < PER && i < NCH) {
+                            if (IsF32B<TIn>::value) {
+                                reinterpret_cast<uint4 *>(dstf)[i] = w[u];
+                            } else {
+                                float4 *d = reinterpret_cast<float4 *>(dstf + 8 * i);
+                                d[0] = make_float4(__uint_as_float(w[u].x << 16), __uint_as_float(w[u].x & 0xffff0000u),
+                                                   __uint_as_float(w[u].y << 16), __uint_as_float(w[u].y & 0xffff0000u));
+                                d[1] = make_float4(__uint_as_float(w[u].z << 16), __uint_as_float(w[u].z & 0xffff0000u),
+                                                   __uint_as_float(w[u].w << 16), __uint_as_float(w[u].w & 0xffff0000u));
+                            }
+                        }
+                    }
                 }
-            }
+            };
+            if (t.kind == 1) widen(std::integral_constant<int, 2 * TR>{});
+            else widen(std::integral_constant<int, TR>{});
             __syncwarp();
             if (t.kind == 1) {
-                // k_t . q_t for the tile's steps: 8 lane partials, one transpose reduction
+                // k_t . q_t for the tile's steps (all SUB rows; those past the tile's end are
+                // never used): lane partials, one transpose reduction
                 float part[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     float a = 0.f;
-                    if (j < slen) {
+                    if (j < SUB) {
 #pragma unroll
                         for (int e = 0; e < E; ++e)
                             a = fmaf(dstf[(j + 1) * DK + lane + 32 * e], dstf[(TR + j + 1) * DK + lane + 32 * e], a);

@@ -66,8 +66,8 @@ constexpr int kBwdComputeWarps = 8;
 constexpr int kBwdThreads = (kBwdComputeWarps + 4) * 32;
 constexpr int kBwdRows = kBwdComputeWarps * kBwdRowsPerWarp;
 constexpr int kBwdLaunchRegs = 168;
-constexpr int kBwdComputeRegs = 216;
-constexpr int kBwdServiceRegs = 72;
+constexpr int kBwdComputeRegs = 208;
+constexpr int kBwdServiceRegs = 88;
 static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <= kBwdThreads * kBwdLaunchRegs,
               "register split exceeds the launch's registers");
 

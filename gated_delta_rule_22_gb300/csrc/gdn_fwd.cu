@@ -228,6 +228,9 @@ __global__ void __launch_bounds__(256, 1)
             for (int r = 0; r < R; ++r) delta[r] = __shfl_sync(kFullMask, d0, (lane & 16) + 4 * r);
         }
 
+        float2 kc[P];
+#pragma unroll
+        for (int m = 0; m < P; ++m) kc[m] = *reinterpret_cast<const float2 *>(kt + col + 32 * m);
         for (int tt = 0; tt < tl; ++tt) {
             const int t = t0 + tt;
             if (to_ckpt == 0) {
@@ -247,10 +250,9 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
             --to_ckpt;
-            float2 kc[P], qv[P], kn[P];
+            float2 qv[P], kn[P];
 #pragma unroll
             for (int m = 0; m < P; ++m) {
-                kc[m] = *reinterpret_cast<const float2 *>(kt + tt * DK + col + 32 * m);
                 qv[m] = *reinterpret_cast<const float2 *>(qt + tt * DK + col + 32 * m);
                 kn[m] = *reinterpret_cast<const float2 *>(kt + (tt + 1) * DK + col + 32 * m);
             }
@@ -271,6 +273,8 @@ __global__ void __launch_bounds__(256, 1)
                 red[2 * r] = ya.x + ya.y;
                 red[2 * r + 1] = an.x + an.y;
             }
+#pragma unroll
+            for (int m = 0; m < P; ++m) kc[m] = kn[m];   // k_{t+1} is the next step's k_t
             // lane holds value (gl >> 1) = 2 * (row offset) + kind; kind 1 = prediction
             const float tot = group_transpose_reduce<2 * R, G>(red, lane);
             if ((gl & 3) == 0) fy[tt * RB + own_row] = tot;
