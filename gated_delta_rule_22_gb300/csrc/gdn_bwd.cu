@@ -193,6 +193,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     bool failed = false;
     int raw_issued[2] = {0, 0}, scb_loads = 0;   // stager: copies issued (for the drain)
+    // Streamed data (checkpoints, residuals, dy, partial sums) is evicted first from L2; the
+    // sub-block start states, written and read back within a chunk, are kept.
+    const uint64_t pol_stream = l2_policy_evict_first();
+    const uint64_t pol_keep = l2_policy_evict_last();
 
     // Each role's code sits under its own setmaxnreg, so that it is compiled for that
     // role's register limit.
@@ -247,11 +251,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const size_t o = (((size_t)b * T + s0 + j) * Hv + h) * Dv + row0 + r4;
                 const bool in = j < slen && row0 + r4 < Dv;
                 if (t.kind == 1 && !kWide) {
-                    const uint2 u = in ? *reinterpret_cast<const uint2 *>(dy + o) : make_uint2(0u, 0u);
+                    const uint2 u = in ? ld_hint(reinterpret_cast<const uint2 *>(dy + o), pol_stream) : make_uint2(0u, 0u);
                     xq[i] = make_uint4(u.x, u.y, 0u, 0u);
                 } else {
                     const void *src = t.kind == 1 ? static_cast<const void *>(dy + o) : static_cast<const void *>(resid + o);
-                    xq[i] = in ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0u, 0u, 0u, 0u);
+                    xq[i] = in ? ld_hint(reinterpret_cast<const uint4 *>(src), pol_stream) : make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             gq = lane < slen ? to_f32(g[((size_t)b * T + s0 + lane) * Hv + h]) : 1.f;
@@ -379,7 +383,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         fence_proxy_async_global();
                         fence_proxy_async();
                         mbar_expect_tx(&bar[kBarScb], (unsigned)(slot_floats * 4));
-                        bulk_load(scb, scratch + (size_t)nt.m * slot_floats, (unsigned)(slot_floats * 4), &bar[kBarScb]);
+                        bulk_load_hint(scb, scratch + (size_t)nt.m * slot_floats, (unsigned)(slot_floats * 4), &bar[kBarScb],
+                                       pol_keep);
                     }
                     ++scb_loads;
                     __syncwarp();
@@ -412,8 +417,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             a.x += x1.x; a.y += x1.y;
                             q2.x += x2.x; q2.y += x2.y;
                         }
-                        *reinterpret_cast<float2 *>(p.ws_dk + og * DK + col) = a;
-                        *reinterpret_cast<float2 *>(p.ws_dq + og * DK + col) = q2;
+                        st_hint(reinterpret_cast<float2 *>(p.ws_dk + og * DK + col), a, pol_stream);
+                        st_hint(reinterpret_cast<float2 *>(p.ws_dq + og * DK + col), q2, pol_stream);
                     }
                 }
                 if (lane == 0) {
@@ -423,8 +428,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         dgs += gp[w].x;
                         dbs += gp[w].y;
                     }
-                    p.ws_dg[og] = dgs;
-                    p.ws_db[og] = dbs;
+                    st_hint(p.ws_dg + og, dgs, pol_stream);
+                    st_hint(p.ws_db + og, dbs, pol_stream);
                 }
 #pragma unroll
                 for (int i = 0; i < RB / 32; ++i) {
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int m = 0; m < P2; ++m)
                         S[r][m] = (row < Dv && pvalid(m))
-                                      ? *reinterpret_cast<const float2 *>(ck + (size_t)row * DK + pc + 64 * m)
+                                      ? ld_hint(reinterpret_cast<const float2 *>(ck + (size_t)row * DK + pc + 64 * m), pol_stream)
                                       : make_float2(0.f, 0.f);
                 }
                 for (int sm = 0; sm < nsub; ++sm, ++x) {
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int r = 0; r < R; ++r)
 #pragma unroll
-                        for (int m = 0; m < P2; ++m) *reinterpret_cast<float2 *>(slot + (r * P2 + m) * 64) = S[r][m];
+                        for (int m = 0; m < P2; ++m) st_hint(reinterpret_cast<float2 *>(slot + (r * P2 + m) * 64), S[r][m], pol_keep);
                     if (sm == nsub - 1) {
                         // the reverse sweep starts from this state: hand it to the bulk copy
                         fence_proxy_async_global();
