@@ -22,6 +22,7 @@ struct Plan {
     int sub;       // backward sub-block length
     int nsub_max;  // sub-blocks per chunk
     int slots;     // backward partial-sum ring depth (steps)
+    bool tc;       // forward in the chunkwise tensor-core form (bf16, C = 64, supported sizes)
 };
 
 constexpr size_t kMaxSmem = 232448;   // opt-in shared memory per block on sm_103
@@ -58,6 +59,9 @@ int make_plan(const gdn_shape *s, Plan *p) {
     p->nsub_max = (C + p->sub - 1) / p->sub;
     p->slots = gdn::bwd_slots(s->Dk, C, s->dtype, kMaxSmem);
     if (p->slots == 0) return GDN_ERR_UNSUPPORTED_SHAPE;
+    p->tc = s->dtype == GDN_BF16 && C == 64 && (s->Dk == 64 || s->Dk == 128 || s->Dk == 192) &&
+            s->Dv % 64 == 0 && s->Dv <= 256 && gdn::chunk_prep_smem(s->Dk, s->Dv) <= kMaxSmem &&
+            gdn::chunk_sweep_smem(s->Dk) <= kMaxSmem;
     return GDN_OK;
 }
 
@@ -65,6 +69,25 @@ int make_plan(const gdn_shape *s, Plan *p) {
 // 256-byte boundary) the residuals v_t - u_t [B,T,Hv,Dv], all fp32.
 size_t ckpt_state_bytes(const Plan &p) { return round_up((size_t)p.B * p.Hv * p.NC * p.Dv * p.Dk * sizeof(float)); }
 size_t ckpt_resid_bytes(const Plan &p) { return (size_t)p.B * p.T * p.Hv * p.Dv * sizeof(float); }
+
+// With the chunkwise forward the buffer continues (each part from a 256-byte boundary) with
+// the per-chunk matrices of every (b, h, chunk): Lam [64] fp32, (Q K^T) o E and (K K^T) o E
+// [64][64] bf16, W [64][Dk] bf16, U [64][Dv] fp32.
+struct ChunkLayout {
+    size_t lam, pm, kkm, wm, um, end;
+};
+ChunkLayout chunk_layout(const Plan &p) {
+    const size_t n = (size_t)p.B * p.Hv * p.NC * 64;   // chunk rows
+    ChunkLayout c;
+    size_t o = ckpt_state_bytes(p) + round_up(ckpt_resid_bytes(p));
+    c.lam = o; o += round_up(n * 4);
+    c.pm = o; o += round_up(n * 64 * 2);
+    c.kkm = o; o += round_up(n * 64 * 2);
+    c.wm = o; o += round_up(n * p.Dk * 2);
+    c.um = o; o += round_up(n * p.Dv * 4);
+    c.end = o;
+    return c;
+}
 
 struct Workspace {
     size_t dq, dk, dg, db, state, total;  // byte offsets and total
@@ -160,7 +183,7 @@ extern "C" {
 size_t gdn_ckpt_bytes(const gdn_shape *shape) {
     Plan p;
     if (make_plan(shape, &p) != GDN_OK) return 0;
-    return ckpt_state_bytes(p) + ckpt_resid_bytes(p);
+    return p.tc ? chunk_layout(p).end : ckpt_state_bytes(p) + ckpt_resid_bytes(p);
 }
 
 size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
@@ -186,6 +209,22 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     fp.B = p.B; fp.T = p.T; fp.Hk = p.Hk; fp.Hv = p.Hv; fp.Dv = p.Dv; fp.C = p.C; fp.NC = p.NC;
     rc = device_status_address(&fp.status);
     if (rc != GDN_OK) return rc;
+    if (p.tc && ckpt != nullptr) {
+        // chunkwise form on the tensor cores
+        const ChunkLayout cl = chunk_layout(p);
+        char *sb = reinterpret_cast<char *>(ckpt);
+        gdn::ChunkParams cp;
+        cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.S0 = S0; cp.y = y; cp.S_T = S_T;
+        cp.ckpt = ckpt; cp.resid = fp.resid;
+        cp.lam = reinterpret_cast<float *>(sb + cl.lam);
+        cp.pm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.pm);
+        cp.kkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.kkm);
+        cp.wm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.wm);
+        cp.um = reinterpret_cast<float *>(sb + cl.um);
+        cp.status = fp.status;
+        cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
+        return cuda_status(gdn::launch_chunk_fwd(cp, p.Dk, (cudaStream_t)stream));
+    }
     CUtensorMap tm_q, tm_k;
     if ((rc = make_qk_map(&tm_q, q, p, gdn::kFwdTile)) != GDN_OK) return rc;
     if ((rc = make_qk_map(&tm_k, k, p, gdn::kFwdTile)) != GDN_OK) return rc;

@@ -1,0 +1,704 @@
+// gdn_chunk.cu -- the forward of the gated delta rule in its chunkwise (dense) form on the
+// 5th-generation tensor cores, for bf16 inputs and chunks of 64 steps.
+//
+// The recurrence is that of mlx issue #4614 ("Recurrence used for the references"); the
+// chunkwise form is derived from it (the pages do not give it). Per value head and chunk of
+// L = 64 steps with start state S0 [Dv, Dk] (lam_t = log g_t, Lam its in-chunk prefix sum,
+// E(s, i) = exp(Lam_s - Lam_i) <= 1, never a division by a decay):
+//     A[t, i] = beta_t (k_t . k_i) E(t, i)  (i < t),   T = (I + A)^-1
+//     W = T diag(beta exp Lam) K,   U = T diag(beta) V,   Delta = U - W S0^T
+//     y = diag(exp Lam) Q S0^T + ((Q K^T) o E_incl) Delta
+//     u = diag(exp Lam) K S0^T + ((K K^T) o E_strict) Delta      (u_t = g_t S_{t-1} k_t)
+//     S_L = exp(Lam_L) S0 + (diag(E(L, .)) Delta)^T K
+// chunk_prep_kernel computes what does not depend on the state, for all chunks at once;
+// chunk_sweep_kernel carries the state through the chunks of one head. Products run on the
+// tensor cores with bf16 operands and fp32 accumulators in tensor memory; T is formed in
+// fp32 on the CUDA cores. The outputs (y, the chunk-start states, v - u) are those of the
+// sequential forward, so the backward consumes them unchanged.
+#include "gdn_umma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kL = 64;           // chunk length of the tensor-core forward
+constexpr int kPad = kL + 1;     // padded row of the fp32 64 x 64 work matrices
+
+__host__ __device__ inline size_t al(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct PrepSmem {
+    size_t kc, qc, kk, qk, am, ts, xs, tcm, bw, bu, vr, kr, lam, bar, tslot, total;
+    __host__ __device__ PrepSmem(int DK, int Dv) {
+        size_t o = 0;
+        kc = o; o += (size_t)kL * DK * 2;           // K of the chunk, bf16 operand [64][DK]
+        qc = o; o += (size_t)kL * DK * 2;           // Q of the chunk
+        kk = o; o += (size_t)kL * kPad * 4;         // K K^T, fp32
+        qk = o; o += (size_t)kL * kPad * 4;         // Q K^T, fp32
+        am = o; o += (size_t)kL * kPad * 4;         // A
+        ts = o; o += (size_t)kL * kPad * 4;         // T = (I + A)^-1
+        xs = o; o += (size_t)3 * 16 * 17 * 4;       // block products of the inversion
+        tcm = o; o += (size_t)kL * kL * 2;          // T, bf16 operand [64][64]
+        bw = o; o += (size_t)DK * kL * 2;           // (diag(beta exp Lam) K)^T, bf16 operand [DK][64]
+        bu = o; o += (size_t)Dv * kL * 2;           // (diag(beta) V)^T, bf16 operand [Dv][64]
+        vr = o; o += (size_t)kL * Dv * 2;           // V of the chunk, row-major bf16
+        kr = o; o += (size_t)kL * DK * 2;           // K of the chunk, row-major bf16
+        lam = o; o += 4 * kL * 4;                   // log g, Lam, exp Lam, beta
+        bar = al(o, 8); o = bar + 8;
+        tslot = o; o += 16;
+        total = o + 1024;
+    }
+};
+
+__device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
+    uint4 u;
+    __nv_bfloat162 h;
+    h = __floats2bfloat162_rn(x[0], x[1]); u.x = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2bfloat162_rn(x[2], x[3]); u.y = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2bfloat162_rn(x[4], x[5]); u.z = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2bfloat162_rn(x[6], x[7]); u.w = *reinterpret_cast<uint32_t *>(&h);
+    return u;
+}
+
+__device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&x)[8]) {
+    x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
+    x[4] = __uint_as_float(u.z << 16); x[5] = __uint_as_float(u.z & 0xffff0000u);
+    x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+// T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kPad), by 16 x 16 blocks:
+// the four diagonal blocks by forward substitution (a column per thread), then the blocks
+// below the diagonal, one block diagonal at a time,
+//     T_ij = -T_ii (A_ij T_jj + A_i,j+1 T_j+1,j + ... + A_i,i-1 T_i-1,j).
+// Called by all 256 threads of the CTA.
+__device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid) {
+    for (int e = tid; e < kL * kL; e += 256) {              // blocks above the diagonal are zero
+        const int t = e >> 6, j = e & (kL - 1);
+        if ((t >> 4) < (j >> 4)) ts[t * kPad + j] = 0.f;
+    }
+    if (tid < kL) {
+        const int b0 = 16 * (tid >> 4), c = tid & 15;
+        float col[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float x = r == c ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 0; i < r; ++i) x = fmaf(-am[(b0 + r) * kPad + b0 + i], col[i], x);
+            col[r] = r < c ? 0.f : x;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) ts[(b0 + r) * kPad + b0 + c] = col[r];
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {
+        const int nb = 4 - d;                               // blocks (j + d, j), j < nb
+        for (int e = tid; e < nb * 256; e += 256) {
+            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i0 = 16 * (j + d);
+            float x = 0.f;
+            for (int kb = j; kb < j + d; ++kb)
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    x = fmaf(am[(i0 + r) * kPad + 16 * kb + i], ts[(16 * kb + i) * kPad + 16 * j + c], x);
+            xs[(j * 16 + r) * 17 + c] = x;
+        }
+        __syncthreads();
+        for (int e = tid; e < nb * 256; e += 256) {
+            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i0 = 16 * (j + d);
+            float x = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x = fmaf(ts[(i0 + r) * kPad + i0 + i], xs[(j * 16 + i) * 17 + c], x);
+            ts[(i0 + r) * kPad + 16 * j + c] = -x;
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+// One CTA per (chunk, kv head, batch row): K K^T and Q K^T once, then per value head of the
+// kv head the decay-weighted matrices, T, W and U.
+template <int E>
+__global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
+    constexpr int DK = 32 * E;
+    constexpr int NKQ = (kL * DK / 8 + 255) / 256;   // 16-byte pieces of K (or Q) per thread
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, Dv = p.Dv, Hv = p.Hv, rep = p.Hv / p.Hk;
+    const int t0 = c * kL, len = min(kL, T - t0);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 1024));
+    const PrepSmem L(DK, Dv);
+    unsigned char *kc = base + L.kc, *qc = base + L.qc, *tcm = base + L.tcm, *bw = base + L.bw, *bu = base + L.bu;
+    __nv_bfloat16 *vr = reinterpret_cast<__nv_bfloat16 *>(base + L.vr);
+    __nv_bfloat16 *kr = reinterpret_cast<__nv_bfloat16 *>(base + L.kr);
+    float *kk = reinterpret_cast<float *>(base + L.kk);
+    float *qk = reinterpret_cast<float *>(base + L.qk);
+    float *am = reinterpret_cast<float *>(base + L.am);
+    float *ts = reinterpret_cast<float *>(base + L.ts);
+    float *xs = reinterpret_cast<float *>(base + L.xs);
+    float *lg = reinterpret_cast<float *>(base + L.lam);     // log g
+    float *Lm = lg + kL;                                      // Lam (inclusive prefix)
+    float *gm = Lm + kL;                                      // exp(Lam)
+    float *bt = gm + kL;                                      // beta
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
+
+    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
+    const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(p.g);
+    const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    {
+        // K and Q of the chunk (rows past the end are zero): all loads, then the stores
+        uint4 kx[NKQ], qx[NKQ];
+#pragma unroll
+        for (int u = 0; u < NKQ; ++u) {
+            const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
+            kx[u] = qx[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (e < kL * (DK / 8) && r < len) {
+                const size_t o = (((size_t)b * T + t0 + r) * p.Hk + hk) * DK + 8 * ch;
+                kx[u] = *reinterpret_cast<const uint4 *>(k + o);
+                qx[u] = *reinterpret_cast<const uint4 *>(q + o);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NKQ; ++u) {
+            const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
+            if (e < kL * (DK / 8)) {
+                *reinterpret_cast<uint4 *>(kc + cm_off(r, 16 * ch, kL)) = kx[u];
+                *reinterpret_cast<uint4 *>(qc + cm_off(r, 16 * ch, kL)) = qx[u];
+                reinterpret_cast<uint4 *>(kr)[e] = kx[u];   // row-major: e = r * DK / 8 + ch
+            }
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    unsigned phase = 0;
+    bool ok = true;
+
+    // K K^T -> columns [0, 64), Q K^T -> [64, 128) (M = 64: row m in lane m % 16 + 32 (m / 16))
+    if (tid == 0) {
+        constexpr uint32_t id = umma_idesc(1, kL, kL);
+        umma_gemm_bf16(tmem, kc, kL, 0, kc, kL, 0, DK, id, false);
+        umma_gemm_bf16(tmem + kL, qc, kL, 0, kc, kL, 0, DK, id, false);
+        umma_commit(bar);
+    }
+    ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
+    ++phase;
+    tc_fence_after();
+    if (ok) {
+        // warps 0-3 read K K^T, warps 4-7 Q K^T; each warp its quarter's 16 valid lanes
+        const int quarter = warp & 3, row = 16 * quarter + lane;
+        float *dst = warp < 4 ? kk : qk;
+        const uint32_t col0 = warp < 4 ? 0u : (uint32_t)kL;
+#pragma unroll
+        for (int cc = 0; cc < kL; cc += 16) {
+            float x[16];
+            tmem_ld16f(tmem + ((uint32_t)(32 * quarter) << 16) + col0 + cc, x);
+            tmem_wait_ld();
+            if (lane < 16)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) dst[row * kPad + cc + i] = x[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    for (int hh = 0; hh < rep && ok; ++hh) {
+        const int h = hk * rep + hh;
+        const size_t chk = ((size_t)b * Hv + h) * p.NC + c;   // (b, h, c)
+        // V of the chunk (row-major), loads issued first
+        {
+            constexpr int kMaxV = kL * 256 / 8 / 256;          // Dv <= 256
+            uint4 vx[kMaxV];
+            const int nv = kL * Dv / 8;
+#pragma unroll
+            for (int u = 0; u < kMaxV; ++u) {
+                const int e = tid + 256 * u, r = e / (Dv / 8), ch = e - r * (Dv / 8);
+                vx[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (e < nv && r < len)
+                    vx[u] = *reinterpret_cast<const uint4 *>(v + (((size_t)b * T + t0 + r) * Hv + h) * Dv + 8 * ch);
+            }
+#pragma unroll
+            for (int u = 0; u < kMaxV; ++u) {
+                const int e = tid + 256 * u;
+                if (e < nv) reinterpret_cast<uint4 *>(vr)[e] = vx[u];
+            }
+        }
+        // log g, beta and the in-chunk prefix Lam (warp 0: two steps per lane, a shuffle scan)
+        if (warp == 0) {
+            float l2[2], b2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = 2 * lane + u;
+                const bool in = t < len;
+                const size_t o = ((size_t)b * T + t0 + t) * Hv + h;
+                l2[u] = in ? fmaxf(logf(__bfloat162float(g[o])), -1.0e4f) : 0.f;   // g = 0: exp(-1e4) = 0
+                b2[u] = in ? __bfloat162float(beta[o]) : 0.f;
+            }
+            float s = l2[0] + l2[1];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y2 = __shfl_up_sync(kFullMask, s, off);
+                if (lane >= off) s += y2;
+            }
+            const float e0 = s - l2[1];                       // inclusive prefix at step 2 lane
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = 2 * lane + u;
+                const float Lt = u == 0 ? e0 : s;
+                Lm[t] = Lt;
+                gm[t] = expf(Lt);
+                bt[t] = b2[u];
+                p.lam[chk * kL + t] = Lt;
+            }
+        }
+        __syncthreads();
+        // A, and the decay-weighted Q K^T (i <= t) and K K^T (i < t), bf16, row-major [64][64]
+        __nv_bfloat16 *P = p.pm + chk * kL * kL;
+        __nv_bfloat16 *KKm = p.kkm + chk * kL * kL;
+        for (int e = tid; e < kL * kL; e += 256) {
+            const int t = e >> 6, i = e & (kL - 1);
+            const float ex = i <= t ? expf(Lm[t] - Lm[i]) : 0.f;
+            const float kkv = kk[t * kPad + i];
+            am[t * kPad + i] = i < t ? bt[t] * kkv * ex : 0.f;
+            P[e] = __float2bfloat16_rn(qk[t * kPad + i] * ex);
+            KKm[e] = __float2bfloat16_rn(i < t ? kkv * ex : 0.f);
+        }
+        __syncthreads();
+        invert_unit_lower(am, ts, xs, tid);
+        // operands: T (A of both products), (diag(beta exp Lam) K)^T and (diag(beta) V)^T,
+        // eight consecutive K elements (16 bytes) per store
+        for (int e = tid; e < kL * 8; e += 256) {
+            const int t = e >> 3, ch = e & 7;
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = ts[t * kPad + 8 * ch + i];
+            *reinterpret_cast<uint4 *>(tcm + cm_off(t, 16 * ch, kL)) = pack8_bf16(x);
+        }
+        for (int e = tid; e < DK * 8; e += 256) {
+            const int ch = e / DK, n = e - ch * DK;   // consecutive threads: consecutive columns
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 8 * ch + i;
+                x[i] = bt[r] * gm[r] * __bfloat162float(kr[r * DK + n]);
+            }
+            *reinterpret_cast<uint4 *>(bw + cm_off(n, 16 * ch, DK)) = pack8_bf16(x);
+        }
+        for (int e = tid; e < Dv * 8; e += 256) {
+            const int ch = e / Dv, n = e - ch * Dv;
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 8 * ch + i;
+                x[i] = bt[r] * __bfloat162float(vr[r * Dv + n]);
+            }
+            *reinterpret_cast<uint4 *>(bu + cm_off(n, 16 * ch, Dv)) = pack8_bf16(x);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // W -> columns [256, 256 + DK), U -> [0, Dv)
+        if (tid == 0) {
+            umma_gemm_bf16(tmem + 256, tcm, kL, 0, bw, DK, 0, kL, umma_idesc(1, kL, DK), false);
+            umma_gemm_bf16(tmem, tcm, kL, 0, bu, Dv, 0, kL, umma_idesc(1, kL, Dv), false);
+            umma_commit(bar);
+        }
+        ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
+        ++phase;
+        tc_fence_after();
+        if (ok) {
+            const int quarter = warp & 3, row = 16 * quarter + lane;
+            const uint32_t lo = (uint32_t)(32 * quarter) << 16;
+            if (warp < 4) {
+                __nv_bfloat16 *W = p.wm + chk * kL * DK;
+                for (int cc = 0; cc < DK; cc += 16) {
+                    float x[16];
+                    tmem_ld16f(tmem + lo + 256 + cc, x);
+                    tmem_wait_ld();
+                    if (lane < 16) {
+                        float a[8], bb[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) { a[i] = x[i]; bb[i] = x[8 + i]; }
+                        *reinterpret_cast<uint4 *>(W + row * DK + cc) = pack8_bf16(a);
+                        *reinterpret_cast<uint4 *>(W + row * DK + cc + 8) = pack8_bf16(bb);
+                    }
+                }
+            } else {
+                float *U = p.um + chk * kL * Dv;
+                for (int cc = 0; cc < Dv; cc += 16) {
+                    float x[16];
+                    tmem_ld16f(tmem + lo + cc, x);
+                    tmem_wait_ld();
+                    if (lane < 16)
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4 *>(U + row * Dv + cc + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (!ok && tid == 0) report_status(p.status, kStatusTimeout);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace gdn
+
+namespace gdn {
+
+namespace {
+
+struct SweepSmem {
+    size_t wc, qs, ks, kt, pc, kkc, sop, dt, de, dtile, kraw, vec, bar, tslot, total;
+    __host__ __device__ SweepSmem(int DK) {
+        size_t o = 0;
+        wc = o; o += (size_t)kL * DK * 2;     // W of the chunk        A [64][DK]
+        qs = o; o += (size_t)kL * DK * 2;     // diag(exp Lam) Q       A [64][DK]
+        ks = o; o += (size_t)kL * DK * 2;     // diag(exp Lam) K       A [64][DK]
+        kt = o; o += (size_t)DK * kL * 2;     // K^T                   B [DK][64]
+        pc = o; o += (size_t)kL * kL * 2;     // (Q K^T) o E_incl      A [64][64]
+        kkc = o; o += (size_t)kL * kL * 2;    // (K K^T) o E_strict    A [64][64]
+        sop = o; o += (size_t)kL * DK * 2;    // S (64 value rows)     B [64][DK]
+        dt = o; o += (size_t)kL * kL * 2;     // Delta^T               B [64][64]
+        de = o; o += (size_t)kL * kL * 2;     // (diag(E_L) Delta)^T   A [64][64]
+        dtile = o; o += (size_t)kL * kPad * 4; // Delta, fp32 [64][65]
+        kraw = o; o += (size_t)kL * DK * 2;   // K of the chunk, row-major bf16
+        vec = o; o += 3 * kL * 4;             // Lam, exp Lam, E(L, .)
+        bar = al(o, 8); o = bar + 8;
+        tslot = o; o += 16;
+        total = o + 1024;
+    }
+};
+
+}  // namespace
+
+// One CTA per (64-row block of the state, value head, batch row), carrying that block of the
+// state through the chunks. Tensor memory (fp32 accumulators, M = 64 layout):
+//   [0, DK)             the state S (value row r in lane r % 16 + 32 (r / 16))
+//   [DK, DK + 64)       y of the chunk (chunk row t in the lane of t)
+//   [DK + 64, DK + 128) the prediction u of the chunk
+//   [DK + 128, 2 DK + 128)  the state update (diag(E_L) Delta)^T K, whose first 64 columns
+//                       first hold W S^T (read before the update is issued)
+template <int E>
+__global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
+    constexpr int DK = 32 * E;
+    constexpr int NKQ = (kL * DK / 8 + 255) / 256;   // 16-byte pieces of a [64][DK] bf16 matrix per thread
+    static_assert(2 * DK + 128 <= 512, "tensor memory holds the state, y, u and the update");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, Dv = p.Dv, Hv = p.Hv, hk = h / (p.Hv / p.Hk), r0 = split * kL;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int lrow = 16 * quarter + lane;                   // M = 64 row of this lane (lanes 0-15)
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 1024));
+    const SweepSmem L(DK);
+    unsigned char *wc = base + L.wc, *qs = base + L.qs, *ks = base + L.ks, *kt = base + L.kt;
+    unsigned char *pc = base + L.pc, *kkc = base + L.kkc, *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
+    float *dtile = reinterpret_cast<float *>(base + L.dtile);
+    __nv_bfloat16 *kraw = reinterpret_cast<__nv_bfloat16 *>(base + L.kraw);
+    float *Lm = reinterpret_cast<float *>(base + L.vec), *gm = Lm + kL, *eL = gm + kL;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
+
+    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
+    __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
+    const size_t head = (size_t)b * Hv + h;
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tS = tmem, tY = tmem + DK, tU = tmem + DK + 64, tD = tmem + DK + 128;
+    constexpr int SC = DK / 2;                              // state columns per warp half
+
+    // the start state into tensor memory
+    {
+        float x[16];
+        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                x[i] = (p.S0 != nullptr && lane < 16 && r0 + lrow < Dv)
+                           ? p.S0[(head * Dv + r0 + lrow) * DK + cc + i] : 0.f;
+            tmem_st16f(tS + lane_off + cc, x);
+        }
+        tmem_wait_st();
+    }
+    unsigned phase = 0;
+    bool ok = true;
+    for (int c = 0; c < p.NC && ok; ++c) {
+        const int t0 = c * kL, len = min(kL, T - t0);
+        const size_t chk = head * p.NC + c;
+        // ---- the chunk's operands: all global loads first, then the shared-memory stores
+        {
+            uint4 kx[NKQ], qx[NKQ], wx[NKQ], px[2], kkx[2];
+            const __nv_bfloat16 *Wg = p.wm + chk * kL * DK;
+            const __nv_bfloat16 *Pg = p.pm + chk * kL * kL, *KKg = p.kkm + chk * kL * kL;
+#pragma unroll
+            for (int u = 0; u < NKQ; ++u) {
+                const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
+                kx[u] = qx[u] = wx[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (e < kL * (DK / 8)) {
+                    wx[u] = *reinterpret_cast<const uint4 *>(Wg + r * DK + 8 * ch);
+                    if (r < len) {
+                        const size_t o = (((size_t)b * T + t0 + r) * p.Hk + hk) * DK + 8 * ch;
+                        kx[u] = *reinterpret_cast<const uint4 *>(k + o);
+                        qx[u] = *reinterpret_cast<const uint4 *>(q + o);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + 256 * u;
+                px[u] = reinterpret_cast<const uint4 *>(Pg)[e];
+                kkx[u] = reinterpret_cast<const uint4 *>(KKg)[e];
+            }
+            if (tid < kL) {
+                const float lt = p.lam[chk * kL + tid];
+                Lm[tid] = lt;
+                gm[tid] = expf(lt);
+            }
+            __syncthreads();
+            if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
+#pragma unroll
+            for (int u = 0; u < NKQ; ++u) {
+                const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
+                if (e < kL * (DK / 8)) {
+                    *reinterpret_cast<uint4 *>(wc + cm_off(r, 16 * ch, kL)) = wx[u];
+                    float kf[8], qf[8], a[8], bq[8];
+                    unpack8_bf16(kx[u], kf);
+                    unpack8_bf16(qx[u], qf);
+                    const float gr = gm[r];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        a[i] = gr * kf[i];
+                        bq[i] = gr * qf[i];
+                    }
+                    *reinterpret_cast<uint4 *>(ks + cm_off(r, 16 * ch, kL)) = pack8_bf16(a);
+                    *reinterpret_cast<uint4 *>(qs + cm_off(r, 16 * ch, kL)) = pack8_bf16(bq);
+                    reinterpret_cast<uint4 *>(kraw)[e] = kx[u];   // row-major: e = r * DK / 8 + ch
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + 256 * u, r = e >> 3, ch = e & 7;
+                *reinterpret_cast<uint4 *>(pc + cm_off(r, 16 * ch, kL)) = px[u];
+                *reinterpret_cast<uint4 *>(kkc + cm_off(r, 16 * ch, kL)) = kkx[u];
+            }
+            __syncthreads();
+            // K^T: key column n, eight chunk rows per 16-byte store; consecutive threads take
+            // consecutive columns (conflict-free reads and stores)
+            for (int e = tid; e < DK * 8; e += 256) {
+                const int ch = e / DK, n = e - ch * DK;
+                float x[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = __bfloat162float(kraw[(8 * ch + i) * DK + n]);
+                *reinterpret_cast<uint4 *>(kt + cm_off(n, 16 * ch, DK)) = pack8_bf16(x);
+            }
+        }
+        // ---- the state as an operand, and the chunk-start checkpoint
+        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+            float x[16];
+            tmem_ld16f(tS + lane_off + cc, x);
+            tmem_wait_ld();
+            if (lane < 16) {
+                float a[8], bb[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) { a[i] = x[i]; bb[i] = x[8 + i]; }
+                *reinterpret_cast<uint4 *>(sop + cm_off(lrow, 2 * cc, kL)) = pack8_bf16(a);
+                *reinterpret_cast<uint4 *>(sop + cm_off(lrow, 2 * cc + 16, kL)) = pack8_bf16(bb);
+                if (p.ckpt != nullptr && r0 + lrow < Dv) {
+                    float *ck = p.ckpt + (chk * Dv + r0 + lrow) * DK + cc;
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4)
+                        *reinterpret_cast<float4 *>(ck + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+                }
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- W S^T
+        if (tid == 0) {
+            umma_gemm_bf16(tD, wc, kL, 0, sop, kL, 0, DK, umma_idesc(1, kL, kL), false);
+            umma_commit(bar);
+        }
+        {
+            // U of the chunk (this lane's row, this warp's 32 columns), loaded while the MMA runs
+            float4 ux[8];
+            const float *Ug = p.um + chk * kL * Dv + (size_t)lrow * Dv + r0 + half * 32;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ux[i] = lane < 16 ? reinterpret_cast<const float4 *>(Ug)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
+            ++phase;
+            tc_fence_after();
+            if (!ok) break;
+            // Delta = U - W S^T into an fp32 tile
+            float x[32];
+            tmem_ld16f(tD + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(x));
+            tmem_ld16f(tD + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(x + 16));
+            tmem_wait_ld();
+            if (lane < 16) {
+                const float *uf = reinterpret_cast<const float *>(ux);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dtile[lrow * kPad + half * 32 + i] = uf[i] - x[i];
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // Delta^T and (diag(E_L) Delta)^T as operands: value column n, eight chunk rows per store
+        for (int e = tid; e < kL * 8; e += 256) {
+            const int n = e >> 3, ch = e & 7;
+            float a[8], bb[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = 8 * ch + i;
+                a[i] = dtile[t * kPad + n];
+                bb[i] = eL[t] * a[i];
+            }
+            *reinterpret_cast<uint4 *>(dt + cm_off(n, 16 * ch, kL)) = pack8_bf16(a);
+            *reinterpret_cast<uint4 *>(de + cm_off(n, 16 * ch, kL)) = pack8_bf16(bb);
+        }
+        fence_proxy_async();
+        __syncthreads();
+        tc_fence_after();
+        // ---- y = Qs S^T + P Delta;  u = Ks S^T + KKm Delta;  update = (E_L Delta)^T K
+        if (tid == 0) {
+            constexpr uint32_t id64 = umma_idesc(1, kL, kL);
+            umma_gemm_bf16(tY, qs, kL, 0, sop, kL, 0, DK, id64, false);
+            umma_gemm_bf16(tY, pc, kL, 0, dt, kL, 0, kL, id64, true);
+            umma_gemm_bf16(tU, ks, kL, 0, sop, kL, 0, DK, id64, false);
+            umma_gemm_bf16(tU, kkc, kL, 0, dt, kL, 0, kL, id64, true);
+            umma_gemm_bf16(tD, de, kL, 0, kt, DK, 0, kL, umma_idesc(1, kL, DK), false);
+            umma_commit(bar);
+        }
+        {
+            // v of the chunk (this lane's row, 32 columns), loaded while the MMAs run
+            uint4 vx[4];
+            const size_t o = (((size_t)b * T + t0 + lrow) * Hv + h) * Dv + r0 + half * 32;
+            const bool mine = lane < 16 && lrow < len;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vx[i] = mine ? reinterpret_cast<const uint4 *>(v + o)[i] : make_uint4(0u, 0u, 0u, 0u);
+            ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
+            ++phase;
+            tc_fence_after();
+            if (!ok) break;
+            // ---- y and v - u of the chunk
+            float x[16];
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                const int cc = half * 32 + 16 * hc;
+                tmem_ld16f(tY + lane_off + cc, x);
+                tmem_wait_ld();
+                if (mine) {
+                    float a[8], bb[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) { a[i] = x[i]; bb[i] = x[8 + i]; }
+                    *reinterpret_cast<uint4 *>(y + o + 16 * hc) = pack8_bf16(a);
+                    *reinterpret_cast<uint4 *>(y + o + 16 * hc + 8) = pack8_bf16(bb);
+                }
+                tmem_ld16f(tU + lane_off + cc, x);
+                tmem_wait_ld();
+                if (mine && p.resid != nullptr) {
+                    float va[8], vb[8];
+                    unpack8_bf16(vx[2 * hc], va);
+                    unpack8_bf16(vx[2 * hc + 1], vb);
+                    float *rr = p.resid + o + 16 * hc;
+#pragma unroll
+                    for (int i = 0; i < 8; i += 4) {
+                        *reinterpret_cast<float4 *>(rr + i) = make_float4(va[i] - x[i], va[i + 1] - x[i + 1], va[i + 2] - x[i + 2], va[i + 3] - x[i + 3]);
+                        *reinterpret_cast<float4 *>(rr + 8 + i) = make_float4(vb[i] - x[8 + i], vb[i + 1] - x[9 + i], vb[i + 2] - x[10 + i], vb[i + 3] - x[11 + i]);
+                    }
+                }
+            }
+            // ---- the state after the chunk
+            const float decay = gm[kL - 1];
+            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+                float s[16], d[16];
+                tmem_ld16f(tS + lane_off + cc, s);
+                tmem_ld16f(tD + lane_off + cc, d);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) s[i] = fmaf(decay, s[i], d[i]);
+                tmem_st16f(tS + lane_off + cc, s);
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (ok && p.S_T != nullptr) {
+        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+            float x[16];
+            tmem_ld16f(tS + lane_off + cc, x);
+            tmem_wait_ld();
+            if (lane < 16 && r0 + lrow < Dv)
+#pragma unroll
+                for (int i = 0; i < 16; i += 4)
+                    *reinterpret_cast<float4 *>(p.S_T + (head * Dv + r0 + lrow) * DK + cc + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+        }
+    }
+    if (!ok && tid == 0) report_status(p.status, kStatusTimeout);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+size_t chunk_prep_smem(int Dk, int Dv) { return PrepSmem(Dk, Dv).total; }
+size_t chunk_sweep_smem(int Dk) { return SweepSmem(Dk).total; }
+
+template <int E>
+static cudaError_t launch_chunk_t(const ChunkParams &p, cudaStream_t s) {
+    constexpr int DK = 32 * E;
+    const size_t sp = PrepSmem(DK, p.Dv).total, ss = SweepSmem(DK).total;
+    cudaError_t err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(chunk_sweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+    if (err != cudaSuccess) return err;
+    chunk_prep_kernel<E><<<dim3(p.NC, p.Hk, p.B), 256, sp, s>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    chunk_sweep_kernel<E><<<dim3(p.Dv / kL, p.Hv, p.B), 256, ss, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_fwd(const ChunkParams &p, int Dk, cudaStream_t s) {
+    switch (Dk) {
+        case 64: return launch_chunk_t<2>(p, s);
+        case 128: return launch_chunk_t<4>(p, s);
+        case 192: return launch_chunk_t<6>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gdn

@@ -71,6 +71,21 @@ constexpr int kBwdServiceRegs = 88;
 static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <= kBwdThreads * kBwdLaunchRegs,
               "register split exceeds the launch's registers");
 
+// Chunkwise tensor-core forward (bf16 inputs, chunks of 64 steps). lam, pm, kkm, wm, um are
+// per (b, h, chunk): the in-chunk log-decay prefix [64], the decay-weighted Q K^T and K K^T
+// [64][64] (bf16), W [64][Dk] (bf16) and U [64][Dv] (fp32); they live in the saved buffer.
+struct ChunkParams {
+    const void *q, *k, *v, *g, *beta;
+    const float *S0;
+    void *y;
+    float *S_T, *ckpt, *resid;
+    float *lam;
+    __nv_bfloat16 *pm, *kkm, *wm;
+    float *um;
+    int *status;
+    int B, T, Hk, Hv, Dv, NC;
+};
+
 // Gate map (a, b, A_log, dt_bias -> g, beta) and its VJP; a, b, g, beta, dg, dbeta, da, db
 // are [rows = B*T, Hv] in the input type, the per-head parameters fp32.
 struct GatesParams {
@@ -343,6 +358,10 @@ int bwd_slots(int Dk, int C, int dtype, size_t limit);
 size_t bwd_smem_bytes(int Dk, int C, int dtype, int slots);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
+// Chunkwise forward: Dk in {64, 128, 192}, Dv a multiple of 64 up to 256, bf16, C = 64.
+cudaError_t launch_chunk_fwd(const ChunkParams &p, int Dk, cudaStream_t s);
+size_t chunk_prep_smem(int Dk, int Dv);
+size_t chunk_sweep_smem(int Dk);
 cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s);
 
 }  // namespace gdn

@@ -1,0 +1,96 @@
+// gdn_umma.cuh -- 5th-generation tensor-core (tcgen05) helpers for the chunkwise kernels
+// (internal; not part of the C ABI).
+//
+// Operands live in shared memory in the canonical no-swizzle K-major layout: "core
+// matrices" of 8 rows x 16 bytes (128 contiguous bytes, rows of 16 bytes), stored K-chunk
+// major: the core matrix of row group i and 16-byte K chunk j sits at (j * RG + i) * 128,
+// RG = rows / 8. In a matrix descriptor the leading byte offset is then the distance
+// between K-adjacent core matrices (RG * 128) and the stride byte offset the distance
+// between row-adjacent ones (128). One MMA consumes 32 bytes of K (16 bf16 or 8 tf32
+// elements): two core matrices; the next one starts 2 * RG * 128 bytes further.
+//
+// Accumulators live in tensor memory (fp32). For M = 128 row m is lane m; for M = 64
+// row m is lane (m % 16) + 32 * (m / 16), i.e. lanes 0-15 of each warp quarter.
+#pragma once
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+// Byte offset of element (r, kb) (kb = byte offset along K) of a K-major operand with
+// `rows` rows (a multiple of 8), in the layout above.
+__host__ __device__ __forceinline__ uint32_t cm_off(int r, int kb, int rows) {
+    return (uint32_t)(((kb >> 4) * (rows >> 3) + (r >> 3)) * 128 + (r & 7) * 16 + (kb & 15));
+}
+
+// Shared-memory matrix descriptor (no swizzle) of a K-major operand with `rows` rows whose
+// K range starts at byte `kb0` (a multiple of 32).
+__device__ __forceinline__ uint64_t umma_desc(const void *base, int rows, int kb0) {
+    const uint32_t start = smem_addr(base) + (uint32_t)((kb0 >> 4) * (rows >> 3) * 128);
+    const uint32_t lbo = (uint32_t)((rows >> 3) * 128), sbo = 128;
+    uint64_t d = 0;
+    d |= (uint64_t)((start >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version of this generation
+    return d;                 // base offset 0, no swizzle
+}
+
+// Instruction descriptor: fp32 accumulator, A and B of format `fmt` (1 = bf16 with
+// kind::f16, 2 = tf32 with kind::tf32), both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc(int fmt, int M, int N) {
+    return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// D (tensor memory) = A B (+ D if accumulate), bf16 operands, issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
+// Completion of this thread's earlier MMAs arrives once on `bar`.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+// All K steps of one bf16 GEMM: D[M x N] (+)= A[M x K] B[N x K]^T, K in elements (a multiple
+// of 16), operands at their K offsets (bytes) ka0 / kb0.
+__device__ __forceinline__ void umma_gemm_bf16(uint32_t d_tmem, const void *A, int arows, int ka0, const void *B,
+                                               int brows, int kb0, int K, uint32_t idesc, bool accumulate) {
+    for (int k = 0; k < K; k += 16) {
+        umma_bf16(d_tmem, umma_desc(A, arows, ka0 + 2 * k), umma_desc(B, brows, kb0 + 2 * k), idesc,
+                  accumulate || k > 0);
+    }
+}
+
+// 32x32b tensor-memory load of 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]),
+          "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+        "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15])
+        : "memory");
+}
+
+// Store bf16 value x at element (r, k) of a K-major bf16 operand with `rows` rows.
+__device__ __forceinline__ void cm_put_bf16(unsigned char *base, int r, int k, int rows, float x) {
+    *reinterpret_cast<__nv_bfloat16 *>(base + cm_off(r, 2 * k, rows)) = __float2bfloat16_rn(x);
+}
+
+}  // namespace gdn
