@@ -71,10 +71,11 @@ size_t ckpt_state_bytes(const Plan &p) { return round_up((size_t)p.B * p.Hv * p.
 size_t ckpt_resid_bytes(const Plan &p) { return (size_t)p.B * p.T * p.Hv * p.Dv * sizeof(float); }
 
 // With the chunkwise forward the buffer continues (each part from a 256-byte boundary) with
-// the per-chunk matrices of every (b, h, chunk): Lam [64] fp32, (Q K^T) o E and (K K^T) o E
-// [64][64] bf16, W [64][Dk] bf16, U [64][Dv] fp32.
+// the per-chunk data of every (b, h, chunk): Lam [64] fp32, the sweep's bf16 operands in their
+// core-matrix layout ((Q K^T) o E and (K K^T) o E [64][64], W, diag(exp Lam) Q,
+// diag(exp Lam) K [64][Dk], K^T [Dk][64]) and U [64][Dv] fp32.
 struct ChunkLayout {
-    size_t lam, pm, kkm, wm, um, end;
+    size_t lam, pm, kkm, wm, qsm, ksm, ktm, um, end;
 };
 ChunkLayout chunk_layout(const Plan &p) {
     const size_t n = (size_t)p.B * p.Hv * p.NC * 64;   // chunk rows
@@ -84,6 +85,9 @@ ChunkLayout chunk_layout(const Plan &p) {
     c.pm = o; o += round_up(n * 64 * 2);
     c.kkm = o; o += round_up(n * 64 * 2);
     c.wm = o; o += round_up(n * p.Dk * 2);
+    c.qsm = o; o += round_up(n * p.Dk * 2);
+    c.ksm = o; o += round_up(n * p.Dk * 2);
+    c.ktm = o; o += round_up(n * p.Dk * 2);
     c.um = o; o += round_up(n * p.Dv * 4);
     c.end = o;
     return c;
@@ -220,6 +224,9 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.pm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.pm);
         cp.kkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.kkm);
         cp.wm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.wm);
+        cp.qsm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qsm);
+        cp.ksm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.ksm);
+        cp.ktm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.ktm);
         cp.um = reinterpret_cast<float *>(sb + cl.um);
         cp.status = fp.status;
         cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;

@@ -265,16 +265,49 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
             }
         }
         __syncthreads();
-        // A, and the decay-weighted Q K^T (i <= t) and K K^T (i < t), bf16, row-major [64][64]
+        // A, and the decay-weighted Q K^T (i <= t) and K K^T (i < t) as bf16 operands in their
+        // core-matrix layout: 16-byte chunk e holds row e % 64, columns 8 (e / 64) .. + 7
         __nv_bfloat16 *P = p.pm + chk * kL * kL;
         __nv_bfloat16 *KKm = p.kkm + chk * kL * kL;
-        for (int e = tid; e < kL * kL; e += 256) {
-            const int t = e >> 6, i = e & (kL - 1);
-            const float ex = i <= t ? expf(Lm[t] - Lm[i]) : 0.f;
-            const float kkv = kk[t * kPad + i];
-            am[t * kPad + i] = i < t ? bt[t] * kkv * ex : 0.f;
-            P[e] = __float2bfloat16_rn(qk[t * kPad + i] * ex);
-            KKm[e] = __float2bfloat16_rn(i < t ? kkv * ex : 0.f);
+        for (int e = tid; e < kL * 8; e += 256) {
+            const int t = e & (kL - 1), i0 = 8 * (e >> 6);
+            float pv[8], kv8[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j;
+                const float ex = i <= t ? expf(Lm[t] - Lm[i]) : 0.f;
+                const float kkv = kk[t * kPad + i];
+                am[t * kPad + i] = i < t ? bt[t] * kkv * ex : 0.f;
+                pv[j] = qk[t * kPad + i] * ex;
+                kv8[j] = i < t ? kkv * ex : 0.f;
+            }
+            reinterpret_cast<uint4 *>(P)[e] = pack8_bf16(pv);
+            reinterpret_cast<uint4 *>(KKm)[e] = pack8_bf16(kv8);
+        }
+        // diag(exp Lam) Q and diag(exp Lam) K (row scaling of the staged operands), and K^T
+        {
+            uint4 *Qg = reinterpret_cast<uint4 *>(p.qsm + chk * kL * DK);
+            uint4 *Kg = reinterpret_cast<uint4 *>(p.ksm + chk * kL * DK);
+            for (int e = tid; e < kL * DK / 8; e += 256) {
+                const float gr = gm[e & (kL - 1)];
+                float a[8];
+                unpack8_bf16(reinterpret_cast<const uint4 *>(qc)[e], a);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) a[j] *= gr;
+                Qg[e] = pack8_bf16(a);
+                unpack8_bf16(reinterpret_cast<const uint4 *>(kc)[e], a);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) a[j] *= gr;
+                Kg[e] = pack8_bf16(a);
+            }
+            unsigned char *Ktg = reinterpret_cast<unsigned char *>(p.ktm + chk * kL * DK);
+            for (int e = tid; e < DK * 8; e += 256) {
+                const int ch = e / DK, n = e - ch * DK;
+                float x[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = __bfloat162float(kr[(8 * ch + i) * DK + n]);
+                *reinterpret_cast<uint4 *>(Ktg + cm_off(n, 16 * ch, DK)) = pack8_bf16(x);
+            }
         }
         __syncthreads();
         invert_unit_lower(am, ts, xs, tid);
@@ -324,7 +357,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
             const int quarter = warp & 3, row = 16 * quarter + lane;
             const uint32_t lo = (uint32_t)(32 * quarter) << 16;
             if (warp < 4) {
-                __nv_bfloat16 *W = p.wm + chk * kL * DK;
+                unsigned char *W = reinterpret_cast<unsigned char *>(p.wm + chk * kL * DK);   // core-matrix layout
                 for (int cc = 0; cc < DK; cc += 16) {
                     float x[16];
                     tmem_ld16f(tmem + lo + 256 + cc, x);
@@ -333,8 +366,8 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
                         float a[8], bb[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) { a[i] = x[i]; bb[i] = x[8 + i]; }
-                        *reinterpret_cast<uint4 *>(W + row * DK + cc) = pack8_bf16(a);
-                        *reinterpret_cast<uint4 *>(W + row * DK + cc + 8) = pack8_bf16(bb);
+                        *reinterpret_cast<uint4 *>(W + cm_off(row, 2 * cc, kL)) = pack8_bf16(a);
+                        *reinterpret_cast<uint4 *>(W + cm_off(row, 2 * cc + 16, kL)) = pack8_bf16(bb);
                     }
                 }
             } else {
@@ -368,7 +401,7 @@ namespace gdn {
 namespace {
 
 struct SweepSmem {
-    size_t wc, qs, ks, kt, pc, kkc, sop, dt, de, dtile, kraw, vec, bar, tslot, total;
+    size_t wc, qs, ks, kt, pc, kkc, sop, dt, de, dtile, vec, bar, tslot, total;
     __host__ __device__ SweepSmem(int DK) {
         size_t o = 0;
         wc = o; o += (size_t)kL * DK * 2;     // W of the chunk        A [64][DK]
@@ -381,9 +414,8 @@ struct SweepSmem {
         dt = o; o += (size_t)kL * kL * 2;     // Delta^T               B [64][64]
         de = o; o += (size_t)kL * kL * 2;     // (diag(E_L) Delta)^T   A [64][64]
         dtile = o; o += (size_t)kL * kPad * 4; // Delta, fp32 [64][65]
-        kraw = o; o += (size_t)kL * DK * 2;   // K of the chunk, row-major bf16
         vec = o; o += 3 * kL * 4;             // Lam, exp Lam, E(L, .)
-        bar = al(o, 8); o = bar + 8;
+        bar = al(o, 8); o = bar + 16;         // MMA completion, operand copies
         tslot = o; o += 16;
         total = o + 1024;
     }
@@ -401,11 +433,10 @@ struct SweepSmem {
 template <int E>
 __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
     constexpr int DK = 32 * E;
-    constexpr int NKQ = (kL * DK / 8 + 255) / 256;   // 16-byte pieces of a [64][DK] bf16 matrix per thread
     static_assert(2 * DK + 128 <= 512, "tensor memory holds the state, y, u and the update");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, Dv = p.Dv, Hv = p.Hv, hk = h / (p.Hv / p.Hk), r0 = split * kL;
+    const int T = p.T, Dv = p.Dv, Hv = p.Hv, r0 = split * kL;
     const int quarter = warp & 3, half = warp >> 2;
     const int lrow = 16 * quarter + lane;                   // M = 64 row of this lane (lanes 0-15)
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
@@ -416,19 +447,31 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
     unsigned char *wc = base + L.wc, *qs = base + L.qs, *ks = base + L.ks, *kt = base + L.kt;
     unsigned char *pc = base + L.pc, *kkc = base + L.kkc, *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
     float *dtile = reinterpret_cast<float *>(base + L.dtile);
-    __nv_bfloat16 *kraw = reinterpret_cast<__nv_bfloat16 *>(base + L.kraw);
     float *Lm = reinterpret_cast<float *>(base + L.vec), *gm = Lm + kL, *eL = gm + kL;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
     const size_t head = (size_t)b * Hv + h;
+    // the six operand matrices of chunk cc, prepared in their shared-memory layout (thread 0)
+    int copies = 0;
+    auto issue_copies = [&](int cc) {
+        const size_t ck = head * p.NC + cc;
+        constexpr unsigned big = kL * DK * 2, small = kL * kL * 2;
+        mbar_expect_tx(cbar, 4 * big + 2 * small);
+        bulk_load(wc, p.wm + ck * kL * DK, big, cbar);
+        bulk_load(qs, p.qsm + ck * kL * DK, big, cbar);
+        bulk_load(ks, p.ksm + ck * kL * DK, big, cbar);
+        bulk_load(kt, p.ktm + ck * kL * DK, big, cbar);
+        bulk_load(pc, p.pm + ck * kL * kL, small, cbar);
+        bulk_load(kkc, p.kkm + ck * kL * kL, small, cbar);
+        ++copies;
+    };
 
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(cbar, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, 512);
@@ -451,78 +494,22 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
         }
         tmem_wait_st();
     }
-    unsigned phase = 0;
+    unsigned phase = 0, cph = 0;
     bool ok = true;
+    if (tid == 0) issue_copies(0);
     for (int c = 0; c < p.NC && ok; ++c) {
         const int t0 = c * kL, len = min(kL, T - t0);
         const size_t chk = head * p.NC + c;
-        // ---- the chunk's operands: all global loads first, then the shared-memory stores
-        {
-            uint4 kx[NKQ], qx[NKQ], wx[NKQ], px[2], kkx[2];
-            const __nv_bfloat16 *Wg = p.wm + chk * kL * DK;
-            const __nv_bfloat16 *Pg = p.pm + chk * kL * kL, *KKg = p.kkm + chk * kL * kL;
-#pragma unroll
-            for (int u = 0; u < NKQ; ++u) {
-                const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
-                kx[u] = qx[u] = wx[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (e < kL * (DK / 8)) {
-                    wx[u] = *reinterpret_cast<const uint4 *>(Wg + r * DK + 8 * ch);
-                    if (r < len) {
-                        const size_t o = (((size_t)b * T + t0 + r) * p.Hk + hk) * DK + 8 * ch;
-                        kx[u] = *reinterpret_cast<const uint4 *>(k + o);
-                        qx[u] = *reinterpret_cast<const uint4 *>(q + o);
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + 256 * u;
-                px[u] = reinterpret_cast<const uint4 *>(Pg)[e];
-                kkx[u] = reinterpret_cast<const uint4 *>(KKg)[e];
-            }
-            if (tid < kL) {
-                const float lt = p.lam[chk * kL + tid];
-                Lm[tid] = lt;
-                gm[tid] = expf(lt);
-            }
-            __syncthreads();
-            if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
-#pragma unroll
-            for (int u = 0; u < NKQ; ++u) {
-                const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
-                if (e < kL * (DK / 8)) {
-                    *reinterpret_cast<uint4 *>(wc + cm_off(r, 16 * ch, kL)) = wx[u];
-                    float kf[8], qf[8], a[8], bq[8];
-                    unpack8_bf16(kx[u], kf);
-                    unpack8_bf16(qx[u], qf);
-                    const float gr = gm[r];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        a[i] = gr * kf[i];
-                        bq[i] = gr * qf[i];
-                    }
-                    *reinterpret_cast<uint4 *>(ks + cm_off(r, 16 * ch, kL)) = pack8_bf16(a);
-                    *reinterpret_cast<uint4 *>(qs + cm_off(r, 16 * ch, kL)) = pack8_bf16(bq);
-                    reinterpret_cast<uint4 *>(kraw)[e] = kx[u];   // row-major: e = r * DK / 8 + ch
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + 256 * u, r = e >> 3, ch = e & 7;
-                *reinterpret_cast<uint4 *>(pc + cm_off(r, 16 * ch, kL)) = px[u];
-                *reinterpret_cast<uint4 *>(kkc + cm_off(r, 16 * ch, kL)) = kkx[u];
-            }
-            __syncthreads();
-            // K^T: key column n, eight chunk rows per 16-byte store; consecutive threads take
-            // consecutive columns (conflict-free reads and stores)
-            for (int e = tid; e < DK * 8; e += 256) {
-                const int ch = e / DK, n = e - ch * DK;
-                float x[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = __bfloat162float(kraw[(8 * ch + i) * DK + n]);
-                *reinterpret_cast<uint4 *>(kt + cm_off(n, 16 * ch, DK)) = pack8_bf16(x);
-            }
+        // ---- the chunk's operands (bulk copies issued one chunk ahead) and its decays
+        if (tid < kL) {
+            const float lt = p.lam[chk * kL + tid];
+            Lm[tid] = lt;
+            gm[tid] = expf(lt);
         }
+        ok = !__syncthreads_or(!mbar_wait(cbar, cph & 1));
+        ++cph;
+        if (!ok) break;
+        if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
         // ---- the state as an operand, and the chunk-start checkpoint
         for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
             float x[16];
@@ -611,6 +598,8 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
             ++phase;
             tc_fence_after();
             if (!ok) break;
+            // the operand buffers are free again: bring in the next chunk's
+            if (tid == 0 && c + 1 < p.NC) issue_copies(c + 1);
             // ---- y and v - u of the chunk
             float x[16];
 #pragma unroll
@@ -667,7 +656,10 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
                     *reinterpret_cast<float4 *>(p.S_T + (head * Dv + r0 + lrow) * DK + cc + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
         }
     }
-    if (!ok && tid == 0) report_status(p.status, kStatusTimeout);
+    if (!ok && tid == 0) {
+        report_status(p.status, kStatusTimeout);
+        if (copies > (int)cph) mbar_wait(cbar, (copies - 1) & 1);   // copies still in flight
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -71,16 +71,18 @@ constexpr int kBwdServiceRegs = 88;
 static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <= kBwdThreads * kBwdLaunchRegs,
               "register split exceeds the launch's registers");
 
-// Chunkwise tensor-core forward (bf16 inputs, chunks of 64 steps). lam, pm, kkm, wm, um are
-// per (b, h, chunk): the in-chunk log-decay prefix [64], the decay-weighted Q K^T and K K^T
-// [64][64] (bf16), W [64][Dk] (bf16) and U [64][Dv] (fp32); they live in the saved buffer.
+// Chunkwise tensor-core forward (bf16 inputs, chunks of 64 steps). Per (b, h, chunk), in the
+// saved buffer: lam, the in-chunk log-decay prefix [64]; um, U [64][Dv] fp32; and the sweep's
+// tensor-core operands, bf16 in their shared-memory (core-matrix) layout: wm W [64][Dk],
+// qsm diag(exp Lam) Q [64][Dk], ksm diag(exp Lam) K [64][Dk], ktm K^T [Dk][64],
+// pm (Q K^T) o E_incl [64][64], kkm (K K^T) o E_strict [64][64].
 struct ChunkParams {
     const void *q, *k, *v, *g, *beta;
     const float *S0;
     void *y;
     float *S_T, *ckpt, *resid;
     float *lam;
-    __nv_bfloat16 *pm, *kkm, *wm;
+    __nv_bfloat16 *pm, *kkm, *wm, *qsm, *ksm, *ktm;
     float *um;
     int *status;
     int B, T, Hk, Hv, Dv, NC;
