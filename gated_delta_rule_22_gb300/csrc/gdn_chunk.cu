@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
                 const int t = 2 * lane + u;
                 const bool in = t < len;
                 const size_t o = ((size_t)b * T + t0 + t) * Hv + h;
-                l2[u] = in ? fmaxf(logf(__bfloat162float(g[o])), -1.0e4f) : 0.f;   // g = 0: exp(-1e4) = 0
+                l2[u] = in ? fmaxf(logf(__bfloat162float(g[o])), -200.f) : 0.f;   // g = 0: exp(-200) = 0 in fp32; a nonzero bf16 g has log g > -93
                 b2[u] = in ? __bfloat162float(beta[o]) : 0.f;
             }
             float s = l2[0] + l2[1];
