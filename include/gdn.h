@@ -84,7 +84,11 @@ enum {
 
 /* Bytes of the saved-for-backward buffer `ckpt` that gdn_fwd writes: the chunk-start states
  * (B*Hv*NC*Dv*Dk*4 bytes, rounded up to a multiple of 256) followed by the per-step
- * residuals v_t - u_t (B*T*Hv*Dv*4 bytes). 0 for an invalid shape. */
+ * residuals v_t - u_t (B*T*Hv*Dv*4 bytes). For bf16 inputs with chunk 64, Dk in
+ * {64, 128, 192} and Dv a multiple of 64 (up to 256, shared memory permitting) the forward
+ * runs in its chunkwise form on the tensor cores, and the buffer continues with that form's
+ * per-chunk matrices ((4 Dk + 2 Dv + 130) * 128 bytes per chunk and value head; their
+ * layout is internal). 0 for an invalid shape. */
 GDN_API size_t gdn_ckpt_bytes(const gdn_shape *shape);
 
 /* Bytes of device scratch gdn_bwd needs (fp32 partial sums for the fixed-order
