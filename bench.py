@@ -45,8 +45,8 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 # gdn_bwd call = bwd_kernel + reduce_kernel, captured with
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:"bwd_kernel|reduce_kernel" -s 6 -c 2 python bench.py --steps 2 --warmup 3 --no-cpu-baseline
-# bwd_kernel 338.9 MB read + 967.6 MB written, reduce_kernel 404.8 MB + 20.3 MB.
-TRAFFIC = {"9fc9ab2ba9b899f8": 338896640 + 967572992 + 404771840 + 20280832}
+# bwd_kernel 338.0 MB read + 944.2 MB written, reduce_kernel 404.8 MB + 20.1 MB.
+TRAFFIC = {"21be09ecae3f7db3": 337952000 + 944215552 + 404779008 + 20103168}
 
 
 def load_peaks():
