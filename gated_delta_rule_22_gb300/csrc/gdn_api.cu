@@ -23,6 +23,7 @@ struct Plan {
     int nsub_max;  // sub-blocks per chunk
     int slots;     // backward partial-sum ring depth (steps)
     bool tc;       // forward in the chunkwise tensor-core form (bf16, C = 64, supported sizes)
+    bool tcb;      // backward in the chunkwise form too (its shared memory fits)
 };
 
 constexpr size_t kMaxSmem = 232448;   // opt-in shared memory per block on sm_103
@@ -62,6 +63,7 @@ int make_plan(const gdn_shape *s, Plan *p) {
     p->tc = s->dtype == GDN_BF16 && C == 64 && (s->Dk == 64 || s->Dk == 128 || s->Dk == 192) &&
             s->Dv % 64 == 0 && s->Dv <= 256 && gdn::chunk_prep_smem(s->Dk, s->Dv) <= kMaxSmem &&
             gdn::chunk_sweep_smem(s->Dk) <= kMaxSmem;
+    p->tcb = p->tc && gdn::chunk_dsweep_smem(s->Dk) <= kMaxSmem && gdn::chunk_grad_smem(s->Dk, s->Dv) <= kMaxSmem;
     return GDN_OK;
 }
 
@@ -75,7 +77,7 @@ size_t ckpt_resid_bytes(const Plan &p) { return (size_t)p.B * p.T * p.Hv * p.Dv 
 // core-matrix layout ((Q K^T) o E and (K K^T) o E [64][64], W, diag(exp Lam) Q,
 // diag(exp Lam) K [64][Dk], K^T [Dk][64]) and U [64][Dv] fp32.
 struct ChunkLayout {
-    size_t lam, pm, kkm, wm, qsm, ksm, ktm, um, end;
+    size_t lam, pm, kkm, wm, qsm, ksm, ktm, um, tm, end;
 };
 ChunkLayout chunk_layout(const Plan &p) {
     const size_t n = (size_t)p.B * p.Hv * p.NC * 64;   // chunk rows
@@ -89,6 +91,7 @@ ChunkLayout chunk_layout(const Plan &p) {
     c.ksm = o; o += round_up(n * p.Dk * 2);
     c.ktm = o; o += round_up(n * p.Dk * 2);
     c.um = o; o += round_up(n * p.Dv * 4);
+    c.tm = o; o += round_up(n * 64 * 2);
     c.end = o;
     return c;
 }
@@ -111,6 +114,31 @@ Workspace workspace_layout(const Plan &p) {
     w.total = off;
     return w;
 }
+
+// Scratch of the chunkwise backward: dq, dk per value head [B,T,Hv,Dk] fp32; dbeta and f
+// partials per block of 64 value rows [B,T,Hv,nsplit] fp32; dU [B,Hv,NC,nsplit][64 x 64] and
+// dS at each chunk end [B,Hv,NC,nsplit][64 x Dk], bf16 in their operand layout.
+struct TcWorkspace {
+    size_t dq, dk, db, f, du, dsl, total;
+};
+
+TcWorkspace tc_workspace_layout(const Plan &p) {
+    TcWorkspace w;
+    const size_t nqk = (size_t)p.B * p.T * p.Hv * p.Dk;
+    const size_t ngate = (size_t)p.B * p.T * p.Hv * p.nsplit;
+    const size_t nblk = (size_t)p.B * p.Hv * p.NC * p.nsplit;
+    size_t off = 0;
+    w.dq = off; off += round_up(nqk * 4);
+    w.dk = off; off += round_up(nqk * 4);
+    w.db = off; off += round_up(ngate * 4);
+    w.f = off; off += round_up(ngate * 4);
+    w.du = off; off += round_up(nblk * 64 * 64 * 2);
+    w.dsl = off; off += round_up(nblk * 64 * p.Dk * 2);
+    w.total = off;
+    return w;
+}
+
+size_t bwd_workspace_total(const Plan &p) { return p.tcb ? tc_workspace_layout(p).total : workspace_layout(p).total; }
 
 bool aligned(const void *ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
@@ -193,7 +221,7 @@ size_t gdn_ckpt_bytes(const gdn_shape *shape) {
 size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
     Plan p;
     if (make_plan(shape, &p) != GDN_OK) return 0;
-    return workspace_layout(p).total;
+    return bwd_workspace_total(p);
 }
 
 int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
@@ -228,6 +256,7 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.ksm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.ksm);
         cp.ktm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.ktm);
         cp.um = reinterpret_cast<float *>(sb + cl.um);
+        cp.tm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tm);
         cp.status = fp.status;
         cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
         return cuda_status(gdn::launch_chunk_fwd(cp, p.Dk, (cudaStream_t)stream));
@@ -250,9 +279,38 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     const void *all[] = {q, k, v, g, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace};
     for (const void *ptr : all)
         if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
-    const Workspace w = workspace_layout(p);
-    if (workspace_bytes < w.total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace_bytes < bwd_workspace_total(p)) return GDN_ERR_WORKSPACE_TOO_SMALL;
     char *ws = static_cast<char *>(workspace);
+    if (p.tcb) {
+        // chunkwise form on the tensor cores, reading the chunkwise forward's saved buffer
+        const ChunkLayout cl = chunk_layout(p);
+        const TcWorkspace tw = tc_workspace_layout(p);
+        const char *sb = reinterpret_cast<const char *>(ckpt);
+        gdn::ChunkBwdParams cp;
+        cp.q = q; cp.k = k; cp.dy = dy; cp.beta = beta;
+        cp.ckpt = ckpt;
+        cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
+        cp.lam = reinterpret_cast<const float *>(sb + cl.lam);
+        cp.tm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.tm);
+        cp.pm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.pm);
+        cp.qsm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qsm);
+        cp.ksm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.ksm);
+        cp.ktm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.ktm);
+        cp.dS_T = dS_T; cp.dS0 = dS0;
+        cp.dv = dv; cp.dg = dg; cp.dq = dq; cp.dk = dk; cp.dbeta = dbeta;
+        cp.ws_dq = reinterpret_cast<float *>(ws + tw.dq);
+        cp.ws_dk = reinterpret_cast<float *>(ws + tw.dk);
+        cp.ws_db = reinterpret_cast<float *>(ws + tw.db);
+        cp.ws_f = reinterpret_cast<float *>(ws + tw.f);
+        cp.ws_du = reinterpret_cast<__nv_bfloat16 *>(ws + tw.du);
+        cp.ws_dsl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dsl);
+        cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC; cp.nsplit = p.nsplit;
+        g_last_error[0] = '\0';
+        rc = device_status_address(&cp.status);
+        if (rc != GDN_OK) return rc;
+        return cuda_status(gdn::launch_chunk_bwd(cp, p.Dk, (cudaStream_t)stream));
+    }
+    const Workspace w = workspace_layout(p);
 
     gdn::BwdParams bp;
     bp.q = q; bp.k = k; bp.v = v; bp.g = g; bp.beta = beta; bp.ckpt = ckpt; bp.dy = dy;
@@ -363,7 +421,7 @@ int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k, const 
     Plan p;
     int rc = make_plan(shape, &p);
     if (rc != GDN_OK) return rc;
-    const size_t need = workspace_layout(p).total;
+    const size_t need = bwd_workspace_total(p);
     if (need > GDN_BWD_NOALLOC_SCRATCH_BYTES) return GDN_ERR_SCRATCH_LIMIT;
     if (!q || !k || !v || !g || !beta || !ckpt || !dy || !dq || !dk || !dv || !dg || !dbeta)
         return GDN_ERR_INVALID_ARG;

@@ -23,6 +23,9 @@ namespace {
 
 constexpr int kL = 64;           // chunk length of the tensor-core forward
 constexpr int kPad = kL + 1;     // padded row of the fp32 64 x 64 work matrices
+// Both kernels hold all 512 tensor-memory columns, so each must be alone on its SM: they ask
+// for more than half of the shared memory.
+constexpr size_t kOneCtaSmem = 120 * 1024;
 
 __host__ __device__ inline size_t al(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -46,6 +49,7 @@ struct PrepSmem {
         bar = al(o, 8); o = bar + 8;
         tslot = o; o += 16;
         total = o + 1024;
+        if (total < kOneCtaSmem) total = kOneCtaSmem;
     }
 };
 
@@ -344,6 +348,11 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        if (p.tm != nullptr) {
+            // T in its operand layout, for the backward
+            uint4 *Tg = reinterpret_cast<uint4 *>(p.tm + chk * kL * kL);
+            for (int e = tid; e < kL * kL / 8; e += 256) Tg[e] = reinterpret_cast<const uint4 *>(tcm)[e];
+        }
         // W -> columns [256, 256 + DK), U -> [0, Dv)
         if (tid == 0) {
             umma_gemm_bf16(tmem + 256, tcm, kL, 0, bw, DK, 0, kL, umma_idesc(1, kL, DK), false);
@@ -418,6 +427,7 @@ struct SweepSmem {
         bar = al(o, 8); o = bar + 16;         // MMA completion, operand copies
         tslot = o; o += 16;
         total = o + 1024;
+        if (total < kOneCtaSmem) total = kOneCtaSmem;
     }
 };
 

@@ -1,0 +1,824 @@
+// gdn_chunk_bwd.cu -- the backward (VJP) of the gated delta rule in its chunkwise form on the
+// 5th-generation tensor cores, for bf16 inputs and chunks of 64 steps. It consumes the
+// saved buffer of the chunkwise forward (gdn_chunk.cu).
+//
+// The recurrence is that of mlx issue #4614 ("Recurrence used for the references"); the
+// chunkwise VJP is derived from it (the pages give neither form). Per value head and chunk of
+// L = 64 steps, with the forward's quantities (Lam, E, T, P = (Q K^T) o E_incl, the chunk-start
+// state S0, Delta = diag(beta) (v - u)) and the adjoint dS_L of the chunk-end state:
+//     dD  = T^T (diag(E(L, .)) K dS_L^T + P^T dY)          (row t: ddelta_t = Sc_t k_t)
+//     dv  = diag(beta) dD,  dU = -diag(beta) dD,  dbeta_t = ddelta_t . (v_t - u_t)
+//     dS0 = exp(Lam_L) dS_L + dY^T diag(exp Lam) Q + dU^T diag(exp Lam) K
+//     G = dY Delta^T,  H = dU Delta^T
+//     dQ = diag(exp Lam) dY S0 + (G o E_incl) K
+//     dK = diag(E(L, .)) Delta dS_L + (G o E_incl)^T Q + (H o E_strict)^T K
+//          + diag(exp Lam) dU S0 + (H o E_strict) K
+//     dg_t = <dA_t, S_{t-1}>, expanded over the chunk without any division by a decay:
+//          E(L,t) e^{Lam_{t-1}} c0 + E(L,t) sum_{i<t} E(t-1,i) f_i
+//          + sum_{s>=t} e^{Lam_{t-1}} E(s,t) (a_s + b_s) + sum_{s>=t} E(s,t) Z[s,t]
+//       with c0 = <dS_L, S0>, f_i = delta_i . (dS_L k_i), a_s = dy_s . S0 q_s,
+//       b_s = du_s . S0 k_s, Z = (G o (Q K^T) + H o (K K^T)) M, M[i,t] = E(t-1,i) [i < t].
+//
+// Three kernels:
+//   chunk_dsweep_kernel  the reverse sweep over the chunks of one (b, h, block of 64 value
+//                        rows), carrying dS (fp32, tensor memory): dD, dv, dbeta and f
+//                        (partials over the value rows), dU and dS_L for the next kernel, dS0.
+//                        K dS_L^T takes dS as a bf16 high part plus a bf16 low part (exact to
+//                        about 2^-16): with dS rounded once to bf16, dg under strong decay
+//                        misses the bf16 parity bound.
+//   chunk_grad_kernel    per (b, h, chunk), fully parallel: everything else (dq, dk per value
+//                        head, dg).
+//   chunk_reduce_kernel  dq, dk summed over the value heads of each kv head (ascending), dbeta
+//                        over the value-row blocks (ascending).
+// Operands are bf16 in the core-matrix layout of gdn_umma.cuh, read K-major or MN-major (one
+// stored copy serves a matrix and its transpose); accumulators fp32 in tensor memory; Z is a
+// tf32 product. No atomics: every sum has a fixed order.
+#include "gdn_umma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kL = 64;           // chunk length
+constexpr int kPad = kL + 1;
+
+__host__ __device__ inline size_t alb(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    uint4 u;
+    __nv_bfloat162 h;
+    h = __floats2bfloat162_rn(x[0], x[1]); u.x = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2bfloat162_rn(x[2], x[3]); u.y = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2bfloat162_rn(x[4], x[5]); u.z = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2bfloat162_rn(x[6], x[7]); u.w = *reinterpret_cast<uint32_t *>(&h);
+    return u;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float *x) {
+    x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
+    x[4] = __uint_as_float(u.z << 16); x[5] = __uint_as_float(u.z & 0xffff0000u);
+    x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+// A kernel holding all 512 tensor-memory columns must be alone on its SM: it asks for more
+// than half of the shared memory.
+constexpr size_t kOneCtaSmem = 120 * 1024;
+
+// ------------------------------------------------------------------ reverse sweep (dS)
+struct DSweepSmem {
+    size_t kt, qs, ks, tm, pm, dys, shi, slo, rhs, du, vec, red, bar, tslot, total;
+    __host__ __device__ DSweepSmem(int DK) {
+        size_t o = 0;
+        kt = o; o += (size_t)DK * kL * 2;    // K^T [DK][64] (read MN-major as K)
+        qs = o; o += (size_t)kL * DK * 2;    // diag(exp Lam) Q [64][DK] (read MN-major)
+        ks = o; o += (size_t)kL * DK * 2;    // diag(exp Lam) K [64][DK] (read MN-major)
+        tm = o; o += (size_t)kL * kL * 2;    // T [64][64] (read MN-major as T^T)
+        pm = o; o += (size_t)kL * kL * 2;    // P = (Q K^T) o E_incl [64][64] (read MN-major)
+        dys = o; o += (size_t)kL * kL * 2;   // dY block [64 t][64 v]
+        shi = o; o += (size_t)kL * DK * 2;   // dS, bf16 high part [64 v][DK]
+        slo = o; o += (size_t)kL * DK * 2;   // dS - high part, bf16
+        rhs = o; o += (size_t)kL * kL * 2;   // diag(E_L) K dS^T + P^T dY [64 t][64 v]
+        du = o; o += (size_t)kL * kL * 2;    // dU block [64 t][64 v]
+        vec = o; o += 4 * kL * 4;            // Lam, E(L, .), beta, -
+        red = o; o += 2 * 2 * kL * 4;        // [f | dbeta][half][64]
+        bar = alb(o, 8); o = bar + 4 * 8;    // MMA, copies of (K^T, P, Qs), of T, of Ks
+        tslot = o; o += 16;
+        total = o + 1024;
+        if (total < kOneCtaSmem) total = kOneCtaSmem;
+    }
+};
+
+}  // namespace
+
+// One CTA per (block of 64 value rows, value head, batch row), over the chunks in reverse.
+// Tensor memory (M = 64 layout: row r in lane r % 16 + 32 (r / 16)):
+//   [0, DK)            dS (value rows of this block)
+//   [DK, DK + 64)      K dS^T, then dD (chunk row t, value column of this block)
+//   [DK + 64, DK + 128) P^T dY
+template <int E>
+__global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) {
+    constexpr int DK = 32 * E;
+    static_assert(DK + 128 <= 512, "tensor memory");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, Dv = p.Dv, Hv = p.Hv, r0 = split * kL, nsplit = p.nsplit;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int lrow = 16 * quarter + lane;                   // M = 64 row of this lane (lanes 0-15)
+    const bool rowlane = lane < 16;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
+    const DSweepSmem L(DK);
+    unsigned char *kt = base + L.kt, *qs = base + L.qs, *ks = base + L.ks, *tmm = base + L.tm, *pmm = base + L.pm;
+    unsigned char *dys = base + L.dys, *shi = base + L.shi, *slo = base + L.slo, *rhs = base + L.rhs, *dus = base + L.du;
+    float *Lm = reinterpret_cast<float *>(base + L.vec), *eL = Lm + kL, *bt = eL + kL;
+    float *red = reinterpret_cast<float *>(base + L.red);   // [2][2][64]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
+    uint64_t *cbA = bar + 1, *cbT = bar + 2, *cbK = bar + 3;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
+
+    const __nv_bfloat16 *dy = static_cast<const __nv_bfloat16 *>(p.dy);
+    const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
+    __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(p.dv);
+    const size_t head = (size_t)b * Hv + h;
+
+    // bulk copies of chunk cc's operands, three groups (each freed at a different point)
+    int nA = 0, nT = 0, nK = 0;
+    auto copy_A = [&](int cc) {
+        const size_t ck = head * p.NC + cc;
+        mbar_expect_tx(cbA, 2 * kL * DK * 2 + kL * kL * 2);
+        bulk_load(kt, p.ktm + ck * kL * DK, kL * DK * 2, cbA);
+        bulk_load(qs, p.qsm + ck * kL * DK, kL * DK * 2, cbA);
+        bulk_load(pmm, p.pm + ck * kL * kL, kL * kL * 2, cbA);
+        ++nA;
+    };
+    auto copy_T = [&](int cc) {
+        const size_t ck = head * p.NC + cc;
+        mbar_expect_tx(cbT, kL * kL * 2);
+        bulk_load(tmm, p.tm + ck * kL * kL, kL * kL * 2, cbT);
+        ++nT;
+    };
+    auto copy_K = [&](int cc) {
+        const size_t ck = head * p.NC + cc;
+        mbar_expect_tx(cbK, kL * DK * 2);
+        bulk_load(ks, p.ksm + ck * kL * DK, kL * DK * 2, cbK);
+        ++nK;
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(bar + i, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tS = tmem, tX = tmem + DK, tP = tmem + DK + 64;
+    constexpr int SC = DK / 2;                              // state columns per warp half
+
+    // dS_T into tensor memory
+    {
+        float x[16];
+        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                x[i] = (p.dS_T != nullptr && rowlane && r0 + lrow < Dv)
+                           ? p.dS_T[(head * Dv + r0 + lrow) * DK + cc + i] : 0.f;
+            tmem_st16f(tS + lane_off + cc, x);
+        }
+        tmem_wait_st();
+    }
+    unsigned ph = 0, cph = 0;
+    bool ok = true;
+    if (tid == 0) { copy_A(p.NC - 1); copy_T(p.NC - 1); copy_K(p.NC - 1); }
+    for (int c = p.NC - 1; c >= 0 && ok; --c) {
+        const int t0 = c * kL, len = min(kL, T - t0);
+        const size_t chk = head * p.NC + c;
+        const size_t rowbase = (size_t)b * T + t0;          // (b, t0) row of [B, T, ...]
+        // ---- this chunk's dY block into its operand layout, decays, beta, and this lane's
+        // v - u (row lrow, 32 value columns)
+        {
+            uint4 yx[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + 256 * u, t = e >> 3, j = e & 7;
+                yx[u] = t < len ? *reinterpret_cast<const uint4 *>(dy + ((rowbase + t) * Hv + h) * Dv + r0 + 8 * j)
+                                : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + 256 * u, t = e >> 3, j = e & 7;
+                *reinterpret_cast<uint4 *>(dys + cm_off(t, 16 * j, kL)) = yx[u];
+            }
+        }
+        if (tid < kL) {
+            Lm[tid] = p.lam[chk * kL + tid];
+            bt[tid] = tid < len ? __bfloat162float(beta[(rowbase + tid) * Hv + h]) : 0.f;
+        }
+        float rs[32];
+        {
+            const bool mine = rowlane && lrow < len;
+            const float4 *rg = reinterpret_cast<const float4 *>(p.resid + ((rowbase + lrow) * Hv + h) * Dv + r0 + half * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 f4 = mine ? rg[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                rs[4 * i] = f4.x; rs[4 * i + 1] = f4.y; rs[4 * i + 2] = f4.z; rs[4 * i + 3] = f4.w;
+            }
+        }
+        __syncthreads();
+        if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
+        const float decay = expf(Lm[kL - 1]);
+        // ---- dS (the adjoint of the chunk-end state) as operands (high and low bf16 parts),
+        // stored for the gradient kernel; then dS <- exp(Lam_L) dS in place
+        {
+            unsigned char *gdsl = reinterpret_cast<unsigned char *>(p.ws_dsl + (chk * nsplit + split) * kL * DK);
+            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+                float x[16];
+                tmem_ld16f(tS + lane_off + cc, x);
+                tmem_wait_ld();
+                if (rowlane) {
+                    float hi[16], lo[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        hi[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
+                        lo[i] = x[i] - hi[i];
+                    }
+                    const uint4 h0 = pack8(hi), h1 = pack8(hi + 8);
+                    const uint32_t o0 = cm_off(lrow, 2 * cc, kL), o1 = cm_off(lrow, 2 * cc + 16, kL);
+                    *reinterpret_cast<uint4 *>(shi + o0) = h0;
+                    *reinterpret_cast<uint4 *>(shi + o1) = h1;
+                    *reinterpret_cast<uint4 *>(slo + o0) = pack8(lo);
+                    *reinterpret_cast<uint4 *>(slo + o1) = pack8(lo + 8);
+                    *reinterpret_cast<uint4 *>(gdsl + o0) = h0;
+                    *reinterpret_cast<uint4 *>(gdsl + o1) = h1;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] *= decay;
+                tmem_st16f(tS + lane_off + cc, x);
+            }
+            tmem_wait_st();
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbA, cph & 1));
+        if (!ok) break;
+        // ---- K dS^T (high + low), P^T dY, dS += dY^T diag(exp Lam) Q
+        if (tid == 0) {
+            constexpr uint32_t idX = umma_idesc_t(1, kL, kL, true, false);
+            constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
+            constexpr uint32_t idS = umma_idesc_t(1, kL, DK, true, true);
+            umma_gemm(tX, CmOp{kt, DK, 0, 0, true}, CmOp{shi, kL, 0, 0, false}, DK, idX, false);
+            umma_gemm(tX, CmOp{kt, DK, 0, 0, true}, CmOp{slo, kL, 0, 0, false}, DK, idX, true);
+            umma_gemm(tP, CmOp{pmm, kL, 0, 0, true}, CmOp{dys, kL, 0, 0, true}, kL, idP, false);
+            umma_gemm(tS, CmOp{dys, kL, 0, 0, true}, CmOp{qs, kL, 0, 0, true}, kL, idS, true);
+            umma_commit(bar);
+        }
+        ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
+        ++ph;
+        tc_fence_after();
+        if (!ok) break;
+        // ---- rhs = diag(E_L) K dS^T + P^T dY as an operand; f partial = beta_t (v_t - u_t) . (dS k_t)
+        {
+            float x[32], y2[32];
+            tmem_ld16f(tX + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(x));
+            tmem_ld16f(tX + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(x + 16));
+            tmem_ld16f(tP + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(y2));
+            tmem_ld16f(tP + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(y2 + 16));
+            tmem_wait_ld();
+            if (rowlane) {
+                const float el = eL[lrow];
+                float fs = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    fs = fmaf(rs[i], x[i], fs);
+                    y2[i] = fmaf(el, x[i], y2[i]);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(rhs + cm_off(lrow, 2 * (half * 32 + 8 * j), kL)) = pack8(y2 + 8 * j);
+                red[half * kL + lrow] = bt[lrow] * fs;
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // the buffers of K^T, P and Qs are free: the previous chunk's copies go out now
+        if (tid == 0 && c > 0) copy_A(c - 1);
+        if (tid < kL && tid < len) p.ws_f[((rowbase + tid) * Hv + h) * nsplit + split] = red[tid] + red[kL + tid];
+        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbT, cph & 1));
+        if (!ok) break;
+        // ---- dD = T^T rhs
+        if (tid == 0) {
+            umma_gemm(tX, CmOp{tmm, kL, 0, 0, true}, CmOp{rhs, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, kL, true, true),
+                      false);
+            umma_commit(bar);
+        }
+        ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
+        ++ph;
+        tc_fence_after();
+        if (!ok) break;
+        if (tid == 0 && c > 0) copy_T(c - 1);
+        // ---- dv = beta dD, dbeta partial, dU = -beta dD (operand, and stored for the gradient kernel)
+        {
+            float x[32];
+            tmem_ld16f(tX + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(x));
+            tmem_ld16f(tX + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(x + 16));
+            tmem_wait_ld();
+            if (rowlane) {
+                const float bb = bt[lrow];
+                float ds = 0.f, dvv[32], duu[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    ds = fmaf(x[i], rs[i], ds);
+                    dvv[i] = bb * x[i];
+                    duu[i] = -dvv[i];
+                }
+                unsigned char *gdu = reinterpret_cast<unsigned char *>(p.ws_du + (chk * nsplit + split) * kL * kL);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t o = cm_off(lrow, 2 * (half * 32 + 8 * j), kL);
+                    const uint4 u = pack8(duu + 8 * j);
+                    *reinterpret_cast<uint4 *>(dus + o) = u;
+                    *reinterpret_cast<uint4 *>(gdu + o) = u;
+                }
+                if (lrow < len) {
+                    uint4 *dvg = reinterpret_cast<uint4 *>(dv + ((rowbase + lrow) * Hv + h) * Dv + r0 + half * 32);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) dvg[j] = pack8(dvv + 8 * j);
+                }
+                red[2 * kL + half * kL + lrow] = ds;
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid < kL && tid < len)
+            p.ws_db[((rowbase + tid) * Hv + h) * nsplit + split] = red[2 * kL + tid] + red[3 * kL + tid];
+        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbK, cph & 1));
+        if (!ok) break;
+        // ---- dS += dU^T diag(exp Lam) K
+        if (tid == 0) {
+            umma_gemm(tS, CmOp{dus, kL, 0, 0, true}, CmOp{ks, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, true, true),
+                      true);
+            umma_commit(bar);
+        }
+        ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
+        ++ph;
+        tc_fence_after();
+        if (!ok) break;
+        if (tid == 0 && c > 0) copy_K(c - 1);
+        ++cph;
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (ok && p.dS0 != nullptr) {
+        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+            float x[16];
+            tmem_ld16f(tS + lane_off + cc, x);
+            tmem_wait_ld();
+            if (rowlane && r0 + lrow < Dv)
+#pragma unroll
+                for (int i = 0; i < 16; i += 4)
+                    *reinterpret_cast<float4 *>(p.dS0 + (head * Dv + r0 + lrow) * DK + cc + i) =
+                        make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+        }
+    }
+    if (!ok && tid == 0) {
+        report_status(p.status, kStatusTimeout);
+        // copies still in flight land before the CTA exits (each wait bounded)
+        if (nA > (int)cph) mbar_wait(cbA, (nA - 1) & 1);
+        if (nT > (int)cph) mbar_wait(cbT, (nT - 1) & 1);
+        if (nK > (int)cph) mbar_wait(cbK, (nK - 1) & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+namespace {
+
+// ------------------------------------------------------------------ per-chunk gradients
+struct GradSmem {
+    size_t qk, yu, dl, s0, dsl, vec, bar, tslot, total;
+    size_t gehe, wt, mt;      // in the s0 region once the first products are done
+    __host__ __device__ GradSmem(int DK, int Dv) {
+        size_t o = 0;
+        qk = o; o += (size_t)2 * kL * DK * 2;                      // [Q; K] [128][DK]
+        yu = o; o += alb((size_t)2 * kL * Dv * 2 > (size_t)kL * kPad * 4 ? (size_t)2 * kL * Dv * 2 : (size_t)kL * kPad * 4, 1024);   // [dY; dU] [128][Dv], later Z weighted [64][65] fp32
+        dl = o; o += (size_t)kL * Dv * 2;                          // Delta [64][Dv]
+        s0 = o;
+        {
+            const size_t a = (size_t)Dv * DK * 2, b2 = (size_t)3 * kL * kL * 4;
+            o += a > b2 ? a : b2;                                  // S0 [Dv][DK], later GE|HE, W, M
+        }
+        gehe = s0; wt = s0 + (size_t)2 * kL * kL * 2; mt = wt + (size_t)kL * kL * 4;
+        dsl = o;
+        {
+            const size_t a = (size_t)Dv * DK * 2, b2 = (size_t)kL * DK * 4;
+            o += a > b2 ? a : b2;                                  // dS_L [Dv / 64][64][DK], later dK part fp32 [64][DK]
+        }
+        vec = o; o += (6 * kL + 2 * 2 * kL + 16) * 4;             // Lam, Lam_{t-1}, exp Lam, E(L,.), beta, f; ab [2][128]; c0 parts
+        bar = alb(o, 8); o = bar + 2 * 8;
+        tslot = o; o += 16;
+        total = o + 1024;
+        if (total < kOneCtaSmem) total = kOneCtaSmem;
+    }
+};
+
+// fp32 [64][DK] tile with its float4 slots permuted within each 32-column group by row
+// (conflict-free stores of 16 consecutive rows)
+__device__ __forceinline__ int swz(int m, int c) { return c ^ ((m & 7) << 2); }
+
+}  // namespace
+
+// One CTA per (chunk, value head, batch row). Tensor memory:
+//   [0, DK)             R1, M = 128: rows 0-63 dQ, rows 64-127 the dK terms with B = S0 or K
+//   [DK, 2 DK)          R2, M = 64: the dK terms diag(E_L) Delta dS_L + GE^T Q + HE^T K
+//   [2 DK, 2 DK + 64)   [Q; K] K^T (M = 128), later Z (M = 64)
+//   [2 DK + 64, + 128)  [dY; dU] Delta^T = [G; H] (M = 128)
+template <int E>
+__global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
+    constexpr int DK = 32 * E;
+    static_assert(2 * DK + 128 <= 512, "tensor memory");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, Dv = p.Dv, Hv = p.Hv, Hk = p.Hk, nsplit = p.nsplit;
+    const int hk = h / (Hv / Hk);
+    const int t0 = c * kL, len = min(kL, T - t0);
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const size_t head = (size_t)b * Hv + h, chk = head * p.NC + c;
+    const size_t rowbase = (size_t)b * T + t0;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
+    const GradSmem L(DK, Dv);
+    unsigned char *qk = base + L.qk, *yu = base + L.yu, *dl = base + L.dl, *s0 = base + L.s0, *dsl = base + L.dsl;
+    unsigned char *gehe = base + L.gehe;
+    float *wt = reinterpret_cast<float *>(base + L.wt), *mt = reinterpret_cast<float *>(base + L.mt);
+    float *zt = reinterpret_cast<float *>(yu);
+    float *dkb = reinterpret_cast<float *>(dsl);
+    float *Lm = reinterpret_cast<float *>(base + L.vec), *LmP = Lm + kL, *gm = LmP + kL, *eL = gm + kL;
+    float *bt = eL + kL, *fv = bt + kL, *abp = fv + kL, *c0p = abp + 4 * kL;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
+
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
+    const __nv_bfloat16 *dy = static_cast<const __nv_bfloat16 *>(p.dy);
+    const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init(cbar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tR1 = tmem, tR2 = tmem + DK, tS1 = tmem + 2 * DK, tS2 = tmem + 2 * DK + 64;
+
+    // ---- dS_L (all value-row blocks) and dU (into rows 64-127 of [dY; dU]) by bulk copy
+    if (tid == 0) {
+        mbar_expect_tx(cbar, (unsigned)(nsplit * kL * DK * 2 + Dv * kL * 2));
+        for (int s = 0; s < nsplit; ++s) {
+            bulk_load(dsl + (size_t)s * kL * DK * 2, p.ws_dsl + (chk * nsplit + s) * kL * DK, kL * DK * 2, cbar);
+            const unsigned char *du = reinterpret_cast<const unsigned char *>(p.ws_du + (chk * nsplit + s) * kL * kL);
+            for (int j = 0; j < 8; ++j)
+                bulk_load(yu + (size_t)((8 * s + j) * 16 + 8) * 128, du + j * 1024, 1024, cbar);
+        }
+    }
+    // ---- decays, beta, f
+    if (tid < kL) {
+        const float lt = p.lam[chk * kL + tid];
+        Lm[tid] = lt;
+        gm[tid] = expf(lt);
+        const bool in = tid < len;
+        bt[tid] = in ? __bfloat162float(beta[(rowbase + tid) * Hv + h]) : 0.f;
+        float f = 0.f;
+        if (in)
+            for (int s = 0; s < nsplit; ++s) f += p.ws_f[((rowbase + tid) * Hv + h) * nsplit + s];
+        fv[tid] = f;
+    }
+    // ---- [Q; K] rows of the chunk (kv head), dY rows
+    {
+        constexpr int NQ = 2 * kL * DK / 8;
+        for (int e = tid; e < NQ; e += 256) {
+            const int r = e / (DK / 8), ch = e - r * (DK / 8), t = r & (kL - 1);
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (t < len) x = *reinterpret_cast<const uint4 *>((r < kL ? q : k) + ((rowbase + t) * Hk + hk) * DK + 8 * ch);
+            *reinterpret_cast<uint4 *>(qk + cm_off(r, 16 * ch, 2 * kL)) = x;
+        }
+        const int nv8 = Dv / 8;
+        for (int e = tid; e < kL * nv8; e += 256) {
+            const int t = e / nv8, ch = e - t * nv8;
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (t < len) x = *reinterpret_cast<const uint4 *>(dy + ((rowbase + t) * Hv + h) * Dv + 8 * ch);
+            *reinterpret_cast<uint4 *>(yu + cm_off(t, 16 * ch, 2 * kL)) = x;
+        }
+    }
+    __syncthreads();
+    if (tid < kL) {
+        LmP[tid] = tid > 0 ? Lm[tid - 1] : 0.f;
+        eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
+    }
+    // ---- Delta = diag(beta) (v - u)
+    {
+        const int nv8 = Dv / 8;
+        for (int e = tid; e < kL * nv8; e += 256) {
+            const int t = e / nv8, ch = e - t * nv8;
+            float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (t < len) {
+                const float4 *rg = reinterpret_cast<const float4 *>(p.resid + ((rowbase + t) * Hv + h) * Dv + 8 * ch);
+                const float4 a = rg[0], a2 = rg[1];
+                const float bb = bt[t];
+                x[0] = bb * a.x; x[1] = bb * a.y; x[2] = bb * a.z; x[3] = bb * a.w;
+                x[4] = bb * a2.x; x[5] = bb * a2.y; x[6] = bb * a2.z; x[7] = bb * a2.w;
+            }
+            *reinterpret_cast<uint4 *>(dl + cm_off(t, 16 * ch, kL)) = pack8(x);
+        }
+    }
+    bool ok = !__syncthreads_or(!mbar_wait(cbar, 0));   // every thread reads dS_L below
+    // ---- S0 (the chunk-start state) as a bf16 operand; c0 = <dS_L, S0> with S0 in fp32
+    float c0s = 0.f;
+    if (ok) {
+        const float *S0g = p.ckpt + chk * (size_t)Dv * DK;
+        const int n8 = Dv * DK / 8;
+#pragma unroll 2
+        for (int e = tid; e < n8; e += 256) {
+            const int v = e / (DK / 8), ch = e - v * (DK / 8);
+            const float4 a = reinterpret_cast<const float4 *>(S0g)[2 * e];
+            const float4 a2 = reinterpret_cast<const float4 *>(S0g)[2 * e + 1];
+            const float x[8] = {a.x, a.y, a.z, a.w, a2.x, a2.y, a2.z, a2.w};
+            *reinterpret_cast<uint4 *>(s0 + cm_off(v, 16 * ch, Dv)) = pack8(x);
+            float d[8];
+            unpack8(*reinterpret_cast<const uint4 *>(dsl + (size_t)(v >> 6) * kL * DK * 2 + cm_off(v & (kL - 1), 16 * ch, kL)), d);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c0s = fmaf(x[i], d[i], c0s);
+        }
+    }
+    c0s = warp_sum(c0s);
+    if (lane == 0) c0p[warp] = c0s;
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- first products: [Q; K] K^T, [dY; dU] Delta^T, [dY; dU] S0, Delta dS_L
+    if (ok && tid == 0) {
+        umma_gemm(tS1, CmOp{qk, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, kL, 0, false}, DK,
+                  umma_idesc_t(1, 2 * kL, kL, false, false), false);
+        umma_gemm(tS2, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{dl, kL, 0, 0, false}, Dv,
+                  umma_idesc_t(1, 2 * kL, kL, false, false), false);
+        umma_gemm(tR1, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{s0, Dv, 0, 0, true}, Dv,
+                  umma_idesc_t(1, 2 * kL, DK, false, true), false);
+        for (int s = 0; s < nsplit; ++s)
+            umma_gemm(tR2, CmOp{dl, kL, 0, kL * s, false}, CmOp{dsl + (size_t)s * kL * DK * 2, kL, 0, 0, true}, kL,
+                      umma_idesc_t(1, kL, DK, false, true), s > 0);
+        umma_commit(bar);
+    }
+    if (ok) ok = !__syncthreads_or(!mbar_wait(bar, 0));
+    tc_fence_after();
+    if (ok) {
+        // ---- G o E_incl, H o E_strict (operands), W = G o (Q K^T) + H o (K K^T) (tf32 operand)
+        const int r = 32 * quarter + lane, s = r & (kL - 1);
+        const bool upper = r >= kL;
+        float wv[32];
+        {
+            float a[32], g2[32];
+            tmem_ld16f(tS1 + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(a));
+            tmem_ld16f(tS1 + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(a + 16));
+            tmem_ld16f(tS2 + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(g2));
+            tmem_ld16f(tS2 + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(g2 + 16));
+            tmem_wait_ld();
+            const float ls = Lm[s];
+            float ge[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int col = half * 32 + i;
+                const bool keep = upper ? col < s : col <= s;
+                ge[i] = keep ? g2[i] * expf(ls - Lm[col]) : 0.f;
+                wv[i] = g2[i] * a[i];
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4 *>(gehe + cm_off(r, 2 * (half * 32 + 8 * j), 2 * kL)) = pack8(ge + 8 * j);
+            if (!upper)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(wt) + cm_off(s, 4 * (half * 32 + 4 * j), kL)) =
+                        make_float4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+        }
+        // ---- R1: a_s = (dY S0)_s . q_s, b_s = (dU S0)_s . k_s; then the rows scaled by exp(Lam_s)
+        {
+            constexpr int SC = DK / 2;
+            const float gs = gm[s];
+            float ab = 0.f;
+            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+                float x[16], qv[16];
+                tmem_ld16f(tR1 + lane_off + cc, x);
+                unpack8(*reinterpret_cast<const uint4 *>(qk + cm_off(r, 2 * cc, 2 * kL)), qv);
+                unpack8(*reinterpret_cast<const uint4 *>(qk + cm_off(r, 2 * cc + 16, 2 * kL)), qv + 8);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    ab = fmaf(x[i], qv[i], ab);
+                    x[i] *= gs;
+                }
+                tmem_st16f(tR1 + lane_off + cc, x);
+            }
+            abp[half * 2 * kL + r] = ab;
+        }
+        // ---- R2: rows scaled by E(L, t)
+        {
+            constexpr int SC = DK / 2;
+            const int m = 16 * quarter + lane;
+            const float sc = lane < 16 ? eL[m] : 1.f;
+            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+                float x[16];
+                tmem_ld16f(tR2 + lane_off + cc, x);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] *= sc;
+                tmem_st16f(tR2 + lane_off + cc, x);
+            }
+        }
+        tmem_wait_st();
+        __syncthreads();
+        if (upper)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float4 *w4 = reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(wt) + cm_off(s, 4 * (half * 32 + 4 * j), kL));
+                float4 w = *w4;
+                w.x += wv[4 * j]; w.y += wv[4 * j + 1]; w.z += wv[4 * j + 2]; w.w += wv[4 * j + 3];
+                *w4 = w;
+            }
+        // M[i, t] = E(t-1, i) for i < t, as the tf32 operand M^T [t][i]
+        for (int e = tid; e < kL * kL / 4; e += 256) {
+            const int t = e & (kL - 1), i0 = 4 * (e >> 6);
+            float m4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m4[j] = i0 + j < t ? expf(LmP[t] - Lm[i0 + j]) : 0.f;
+            *reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(mt) + cm_off(t, 4 * i0, kL)) =
+                make_float4(m4[0], m4[1], m4[2], m4[3]);
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- second products: R1 += [GE; HE] K, R2 += GE^T Q + HE^T K, Z = W M (tf32)
+    if (ok && tid == 0) {
+        umma_gemm(tR1, CmOp{gehe, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
+                  umma_idesc_t(1, 2 * kL, DK, false, true), true);
+        umma_gemm(tR2, CmOp{gehe, 2 * kL, 0, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, kL,
+                  umma_idesc_t(1, kL, DK, true, true), true);
+        umma_gemm(tR2, CmOp{gehe, 2 * kL, 0, kL, true}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
+                  umma_idesc_t(1, kL, DK, true, true), true);
+        for (int kk = 0; kk < kL; kk += 8)
+            umma_tf32(tS1, cm_kmajor(wt, kL, 0, 4 * kk), cm_kmajor(mt, kL, 0, 4 * kk), umma_idesc(2, kL, kL), kk > 0);
+        umma_commit(bar);
+    }
+    if (ok) ok = !__syncthreads_or(!mbar_wait(bar, 1));
+    tc_fence_after();
+    if (ok) {
+        const int m = 16 * quarter + lane;
+        // ---- Z weighted by E(s, t) (s >= t) into [64][65]; R2 (the dK part in M = 64 rows) to shared memory
+        {
+            float z[32];
+            tmem_ld16f(tS1 + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(z));
+            tmem_ld16f(tS1 + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(z + 16));
+            tmem_wait_ld();
+            if (lane < 16) {
+                const float ls = Lm[m];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = half * 32 + i;
+                    zt[m * kPad + t] = m >= t ? z[i] * expf(ls - Lm[t]) : 0.f;
+                }
+            }
+        }
+        {
+            constexpr int SC = DK / 2;
+            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+                float x[16];
+                tmem_ld16f(tR2 + lane_off + cc, x);
+                tmem_wait_ld();
+                if (lane < 16)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<float4 *>(dkb + m * DK + swz(m, cc + 4 * j)) =
+                            make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+            }
+        }
+    }
+    __syncthreads();
+    if (ok && tid < kL && tid < len) {
+        // ---- dg_t
+        const int t = tid;
+        float c0 = 0.f;
+        for (int w = 0; w < 8; ++w) c0 += c0p[w];
+        const float lt = Lm[t], lp = LmP[t], lL = Lm[kL - 1];
+        float s2 = 0.f, s3 = 0.f, s4 = 0.f;
+        for (int i = 0; i < t; ++i) s2 = fmaf(expf(lp - Lm[i]), fv[i], s2);
+        for (int s = t; s < kL; ++s) {
+            const float ab = abp[s] + abp[2 * kL + s] + abp[kL + s] + abp[3 * kL + s];
+            s3 = fmaf(expf(lp + Lm[s] - lt), ab, s3);
+        }
+        for (int s = 0; s < kL; ++s) s4 += zt[s * kPad + t];
+        const float dgv = expf(lL - lt + lp) * c0 + expf(lL - lt) * s2 + s3 + s4;
+        static_cast<__nv_bfloat16 *>(p.dg)[(rowbase + t) * Hv + h] = __float2bfloat16_rn(dgv);
+    }
+    if (ok) {
+        // ---- dq and dk of this value head
+        constexpr int SC = DK / 2;
+        const int r = 32 * quarter + lane, s = r & (kL - 1);
+        const bool upper = r >= kL;
+        float *dst = (upper ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + h) * DK;
+        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+            float x[16];
+            tmem_ld16f(tR1 + lane_off + cc, x);
+            tmem_wait_ld();
+            if (upper)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 a = *reinterpret_cast<const float4 *>(dkb + s * DK + swz(s, cc + 4 * j));
+                    x[4 * j] += a.x; x[4 * j + 1] += a.y; x[4 * j + 2] += a.z; x[4 * j + 3] += a.w;
+                }
+            if (s < len)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<float4 *>(dst + cc + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+        }
+    }
+    if (!ok && tid == 0) {
+        report_status(p.status, kStatusTimeout);
+        mbar_wait(cbar, 0);   // the copies land before the CTA exits (bounded)
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// dq, dk: the value heads of each kv head in ascending order; dbeta: the value-row blocks.
+__global__ void __launch_bounds__(256) chunk_reduce_kernel(ChunkBwdParams p, int Dk) {
+    const size_t nqk = (size_t)p.B * p.T * p.Hk * Dk;
+    const size_t ngate = (size_t)p.B * p.T * p.Hv;
+    const int rep = p.Hv / p.Hk;
+    __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.dq);
+    __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(p.dk);
+    __nv_bfloat16 *db = static_cast<__nv_bfloat16 *>(p.dbeta);
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nqk / 4 + ngate;
+         i += (size_t)gridDim.x * blockDim.x) {
+        if (i < nqk / 4) {
+            const size_t e = 4 * i;
+            const int j = (int)(e % Dk);
+            const size_t bthk = e / Dk;
+            const int hk = (int)(bthk % p.Hk);
+            const size_t bt = bthk / p.Hk;
+            float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
+            for (int h = hk * rep; h < (hk + 1) * rep; ++h) {
+                const size_t o = (bt * p.Hv + h) * Dk + j;
+                const float4 a = *reinterpret_cast<const float4 *>(p.ws_dq + o);
+                const float4 b2 = *reinterpret_cast<const float4 *>(p.ws_dk + o);
+                sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
+                sk.x += b2.x; sk.y += b2.y; sk.z += b2.z; sk.w += b2.w;
+            }
+            __nv_bfloat162 *q2 = reinterpret_cast<__nv_bfloat162 *>(dq + e);
+            __nv_bfloat162 *k2 = reinterpret_cast<__nv_bfloat162 *>(dk + e);
+            q2[0] = __floats2bfloat162_rn(sq.x, sq.y); q2[1] = __floats2bfloat162_rn(sq.z, sq.w);
+            k2[0] = __floats2bfloat162_rn(sk.x, sk.y); k2[1] = __floats2bfloat162_rn(sk.z, sk.w);
+        } else {
+            const size_t gi = i - nqk / 4;
+            float sb = 0.f;
+            for (int s = 0; s < p.nsplit; ++s) sb += p.ws_db[gi * p.nsplit + s];
+            db[gi] = __float2bfloat16_rn(sb);
+        }
+    }
+}
+
+size_t chunk_dsweep_smem(int Dk) { return DSweepSmem(Dk).total; }
+size_t chunk_grad_smem(int Dk, int Dv) { return GradSmem(Dk, Dv).total; }
+
+template <int E>
+static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, cudaStream_t s) {
+    constexpr int DK = 32 * E;
+    const size_t sd = DSweepSmem(DK).total, sg = GradSmem(DK, p.Dv).total;
+    cudaError_t err = cudaFuncSetAttribute(chunk_dsweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(chunk_grad_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
+    if (err != cudaSuccess) return err;
+    chunk_dsweep_kernel<E><<<dim3(p.nsplit, p.Hv, p.B), 256, sd, s>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    chunk_grad_kernel<E><<<dim3(p.NC, p.Hv, p.B), 256, sg, s>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const size_t n = (size_t)p.B * p.T * p.Hk * DK / 4 + (size_t)p.B * p.T * p.Hv;
+    size_t blocks = (n + 255) / 256;
+    if (blocks > 8 * 152) blocks = 8 * 152;
+    chunk_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, DK);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, int Dk, cudaStream_t s) {
+    switch (Dk) {
+        case 64: return launch_chunk_bwd_t<2>(p, s);
+        case 128: return launch_chunk_bwd_t<4>(p, s);
+        case 192: return launch_chunk_bwd_t<6>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gdn

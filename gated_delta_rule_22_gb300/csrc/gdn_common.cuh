@@ -75,17 +75,34 @@ static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <=
 // saved buffer: lam, the in-chunk log-decay prefix [64]; um, U [64][Dv] fp32; and the sweep's
 // tensor-core operands, bf16 in their shared-memory (core-matrix) layout: wm W [64][Dk],
 // qsm diag(exp Lam) Q [64][Dk], ksm diag(exp Lam) K [64][Dk], ktm K^T [Dk][64],
-// pm (Q K^T) o E_incl [64][64], kkm (K K^T) o E_strict [64][64].
+// pm (Q K^T) o E_incl [64][64], kkm (K K^T) o E_strict [64][64], tm T = (I + A)^-1 [64][64].
 struct ChunkParams {
     const void *q, *k, *v, *g, *beta;
     const float *S0;
     void *y;
     float *S_T, *ckpt, *resid;
     float *lam;
-    __nv_bfloat16 *pm, *kkm, *wm, *qsm, *ksm, *ktm;
+    __nv_bfloat16 *pm, *kkm, *wm, *qsm, *ksm, *ktm, *tm;
     float *um;
     int *status;
     int B, T, Hk, Hv, Dv, NC;
+};
+
+// Chunkwise tensor-core backward (same sizes as the chunkwise forward; consumes its saved
+// buffer). nsplit = Dv / 64 blocks of value rows.
+struct ChunkBwdParams {
+    const void *q, *k, *dy, *beta;
+    const float *ckpt, *resid, *lam;
+    const __nv_bfloat16 *tm, *pm, *qsm, *ksm, *ktm;
+    const float *dS_T;
+    float *dS0;
+    void *dv, *dg, *dq, *dk, *dbeta;
+    float *ws_dq, *ws_dk;      // [B, T, Hv, Dk]: per value head
+    float *ws_db, *ws_f;       // [B, T, Hv, nsplit]: per block of 64 value rows
+    __nv_bfloat16 *ws_du;      // [B, Hv, NC, nsplit][64 x 64]: -beta o ddelta, operand layout
+    __nv_bfloat16 *ws_dsl;     // [B, Hv, NC, nsplit][64 x Dk]: dS at each chunk end, operand layout
+    int *status;
+    int B, T, Hk, Hv, Dv, NC, nsplit;
 };
 
 // Gate map (a, b, A_log, dt_bias -> g, beta) and its VJP; a, b, g, beta, dg, dbeta, da, db
@@ -364,6 +381,11 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_chunk_fwd(const ChunkParams &p, int Dk, cudaStream_t s);
 size_t chunk_prep_smem(int Dk, int Dv);
 size_t chunk_sweep_smem(int Dk);
+// Chunkwise backward: the reverse sweep over chunks (dS), the per-chunk gradient products
+// and the fixed-order sums over value heads and row blocks.
+cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, int Dk, cudaStream_t s);
+size_t chunk_dsweep_smem(int Dk);
+size_t chunk_grad_smem(int Dk, int Dv);
 cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s);
 
 }  // namespace gdn

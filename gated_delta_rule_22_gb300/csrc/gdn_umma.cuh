@@ -9,6 +9,13 @@
 // between row-adjacent ones (128). One MMA consumes 32 bytes of K (16 bf16 or 8 tf32
 // elements): two core matrices; the next one starts 2 * RG * 128 bytes further.
 //
+// The same bytes also serve as the transposed operand: read "MN-major", the array's rows
+// become the operand's K index and its K index the operand's M (or N) index. A core
+// matrix is then 8 K rows x 16 bytes of M/N, and the descriptor's leading byte offset is
+// still the distance between K-adjacent core matrices (here the row-group stride, 128)
+// and the stride byte offset the distance between M/N-adjacent ones (RG * 128); the
+// instruction descriptor marks the operand as transposed (bit 15 for A, 16 for B).
+//
 // Accumulators live in tensor memory (fp32). For M = 128 row m is lane m; for M = 64
 // row m is lane (m % 16) + 32 * (m / 16), i.e. lanes 0-15 of each warp quarter.
 #pragma once
@@ -36,11 +43,39 @@ __device__ __forceinline__ uint64_t umma_desc(const void *base, int rows, int kb
     return d;                 // base offset 0, no swizzle
 }
 
+// Descriptor from a shared-memory byte address and the two strides (no swizzle).
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t start, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((start >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// K-major view of an array with R rows: operand rows from array row r0, K from byte kb0.
+__device__ __forceinline__ uint64_t cm_kmajor(const void *base, int R, int r0, int kb0) {
+    return umma_sdesc(smem_addr(base) + (uint32_t)(((kb0 >> 4) * (R >> 3) + (r0 >> 3)) * 128), (uint32_t)(R * 16),
+                      128u);
+}
+
+// MN-major view of a bf16 array with R rows: operand K index = array row (from k0, a
+// multiple of 8), operand M/N index = array column (from mn0, a multiple of 8).
+__device__ __forceinline__ uint64_t cm_mnmajor(const void *base, int R, int k0, int mn0) {
+    return umma_sdesc(smem_addr(base) + (uint32_t)(((mn0 >> 3) * (R >> 3) + (k0 >> 3)) * 128), 128u,
+                      (uint32_t)(R * 16));
+}
+
 // Instruction descriptor: fp32 accumulator, A and B of format `fmt` (1 = bf16 with
 // kind::f16, 2 = tf32 with kind::tf32), both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t umma_idesc(int fmt, int M, int N) {
     return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
+}
+
+// The same with either operand transposed (read MN-major).
+__host__ __device__ constexpr uint32_t umma_idesc_t(int fmt, int M, int N, bool a_mn, bool b_mn) {
+    return umma_idesc(fmt, M, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
 }
 
 // D (tensor memory) = A B (+ D if accumulate), bf16 operands, issued by one thread.
@@ -49,6 +84,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
+// The same with tf32 operands (fp32 in shared memory, mantissa cut to 10 bits).
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
         : "memory");
 }
@@ -68,6 +113,25 @@ __device__ __forceinline__ void umma_gemm_bf16(uint32_t d_tmem, const void *A, i
         umma_bf16(d_tmem, umma_desc(A, arows, ka0 + 2 * k), umma_desc(B, brows, kb0 + 2 * k), idesc,
                   accumulate || k > 0);
     }
+}
+
+// One bf16 operand of a GEMM: an array in the layout above with R rows, read K-major
+// (operand rows = array rows from `mn0`, K = array columns from `k0`) or MN-major (operand
+// rows = array columns from `mn0`, K = array rows from `k0`). Offsets in elements.
+struct CmOp {
+    const void *base;
+    int R, mn0, k0;
+    bool mn;
+    __device__ __forceinline__ uint64_t desc(int k) const {
+        return mn ? cm_mnmajor(base, R, k0 + k, mn0) : cm_kmajor(base, R, mn0, 2 * (k0 + k));
+    }
+};
+
+// D[M x N] (+)= A B over K elements (a multiple of 16), bf16 operands in either orientation;
+// the instruction descriptor must carry the same orientations.
+__device__ __forceinline__ void umma_gemm(uint32_t d_tmem, const CmOp &A, const CmOp &B, int K, uint32_t idesc,
+                                          bool accumulate) {
+    for (int k = 0; k < K; k += 16) umma_bf16(d_tmem, A.desc(k), B.desc(k), idesc, accumulate || k > 0);
 }
 
 // 32x32b tensor-memory load of 16 consecutive columns.
