@@ -77,7 +77,7 @@ size_t ckpt_resid_bytes(const Plan &p) { return (size_t)p.B * p.T * p.Hv * p.Dv 
 // core-matrix layout ((Q K^T) o E and (K K^T) o E [64][64], W, diag(exp Lam) Q,
 // diag(exp Lam) K [64][Dk], K^T [Dk][64]) and U [64][Dv] fp32.
 struct ChunkLayout {
-    size_t lam, pm, kkm, wm, qsm, ksm, ktm, um, tm, end;
+    size_t lam, pm, kkm, wm, qsm, ksm, ktm, um, tm, s0m, qkm, end;
 };
 ChunkLayout chunk_layout(const Plan &p) {
     const size_t n = (size_t)p.B * p.Hv * p.NC * 64;   // chunk rows
@@ -92,6 +92,8 @@ ChunkLayout chunk_layout(const Plan &p) {
     c.ktm = o; o += round_up(n * p.Dk * 2);
     c.um = o; o += round_up(n * p.Dv * 4);
     c.tm = o; o += round_up(n * 64 * 2);
+    c.s0m = o; o += round_up((size_t)p.B * p.Hv * p.NC * p.Dv * p.Dk * 2);
+    c.qkm = o; o += round_up((size_t)p.B * p.Hk * p.NC * 128 * p.Dk * 2);
     c.end = o;
     return c;
 }
@@ -116,10 +118,11 @@ Workspace workspace_layout(const Plan &p) {
 }
 
 // Scratch of the chunkwise backward: dq, dk per value head [B,T,Hv,Dk] fp32; dbeta and f
-// partials per block of 64 value rows [B,T,Hv,nsplit] fp32; dU [B,Hv,NC,nsplit][64 x 64] and
-// dS at each chunk end [B,Hv,NC,nsplit][64 x Dk], bf16 in their operand layout.
+// partials per block of 64 value rows [B,T,Hv,nsplit] fp32; [dY; dU] [B,Hv,NC,nsplit][128 x 64],
+// Delta [B,Hv,NC,nsplit][64 x 64] and dS at each chunk end [B,Hv,NC,nsplit][64 x Dk], bf16 in
+// their operand layout.
 struct TcWorkspace {
-    size_t dq, dk, db, f, du, dsl, total;
+    size_t dq, dk, db, f, yu, dl, dsl, total;
 };
 
 TcWorkspace tc_workspace_layout(const Plan &p) {
@@ -132,7 +135,8 @@ TcWorkspace tc_workspace_layout(const Plan &p) {
     w.dk = off; off += round_up(nqk * 4);
     w.db = off; off += round_up(ngate * 4);
     w.f = off; off += round_up(ngate * 4);
-    w.du = off; off += round_up(nblk * 64 * 64 * 2);
+    w.yu = off; off += round_up(nblk * 128 * 64 * 2);
+    w.dl = off; off += round_up(nblk * 64 * 64 * 2);
     w.dsl = off; off += round_up(nblk * 64 * p.Dk * 2);
     w.total = off;
     return w;
@@ -257,6 +261,8 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.ktm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.ktm);
         cp.um = reinterpret_cast<float *>(sb + cl.um);
         cp.tm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tm);
+        cp.s0m = reinterpret_cast<__nv_bfloat16 *>(sb + cl.s0m);
+        cp.qkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qkm);
         cp.status = fp.status;
         cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
         return cuda_status(gdn::launch_chunk_fwd(cp, p.Dk, (cudaStream_t)stream));
@@ -287,8 +293,7 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         const TcWorkspace tw = tc_workspace_layout(p);
         const char *sb = reinterpret_cast<const char *>(ckpt);
         gdn::ChunkBwdParams cp;
-        cp.q = q; cp.k = k; cp.dy = dy; cp.beta = beta;
-        cp.ckpt = ckpt;
+        cp.dy = dy; cp.beta = beta;
         cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
         cp.lam = reinterpret_cast<const float *>(sb + cl.lam);
         cp.tm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.tm);
@@ -296,13 +301,16 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.qsm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qsm);
         cp.ksm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.ksm);
         cp.ktm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.ktm);
+        cp.s0m = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.s0m);
+        cp.qkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qkm);
         cp.dS_T = dS_T; cp.dS0 = dS0;
         cp.dv = dv; cp.dg = dg; cp.dq = dq; cp.dk = dk; cp.dbeta = dbeta;
         cp.ws_dq = reinterpret_cast<float *>(ws + tw.dq);
         cp.ws_dk = reinterpret_cast<float *>(ws + tw.dk);
         cp.ws_db = reinterpret_cast<float *>(ws + tw.db);
         cp.ws_f = reinterpret_cast<float *>(ws + tw.f);
-        cp.ws_du = reinterpret_cast<__nv_bfloat16 *>(ws + tw.du);
+        cp.ws_yu = reinterpret_cast<__nv_bfloat16 *>(ws + tw.yu);
+        cp.ws_dl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dl);
         cp.ws_dsl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dsl);
         cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC; cp.nsplit = p.nsplit;
         g_last_error[0] = '\0';

@@ -189,6 +189,16 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
     const uint32_t tmem = *tslot;
     unsigned phase = 0;
     bool ok = true;
+    if (p.qkm != nullptr) {
+        // [Q; K] in the backward's operand layout (128 rows): 16-byte piece j * 128 + r is
+        // row r of K chunk j, from Q (r < 64) or K
+        uint4 *QKg = reinterpret_cast<uint4 *>(p.qkm + (((size_t)b * p.Hk + hk) * p.NC + c) * 2 * kL * DK);
+        const uint4 *q4 = reinterpret_cast<const uint4 *>(qc), *k4 = reinterpret_cast<const uint4 *>(kc);
+        for (int e = tid; e < 2 * kL * DK / 8; e += 256) {
+            const int j = e >> 7, r = e & 127;
+            QKg[e] = r < kL ? q4[j * kL + r] : k4[j * kL + r - kL];
+        }
+    }
 
     // K K^T -> columns [0, 64), Q K^T -> [64, 128) (M = 64: row m in lane m % 16 + 32 (m / 16))
     if (tid == 0) {
@@ -529,8 +539,16 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
                 float a[8], bb[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) { a[i] = x[i]; bb[i] = x[8 + i]; }
-                *reinterpret_cast<uint4 *>(sop + cm_off(lrow, 2 * cc, kL)) = pack8_bf16(a);
-                *reinterpret_cast<uint4 *>(sop + cm_off(lrow, 2 * cc + 16, kL)) = pack8_bf16(bb);
+                const uint4 ua = pack8_bf16(a), ub = pack8_bf16(bb);
+                const uint32_t oa = cm_off(lrow, 2 * cc, kL), ob = cm_off(lrow, 2 * cc + 16, kL);
+                *reinterpret_cast<uint4 *>(sop + oa) = ua;
+                *reinterpret_cast<uint4 *>(sop + ob) = ub;
+                if (p.s0m != nullptr) {
+                    // the same operand for the backward
+                    unsigned char *sg = reinterpret_cast<unsigned char *>(p.s0m + (chk * gridDim.x + split) * kL * DK);
+                    *reinterpret_cast<uint4 *>(sg + oa) = ua;
+                    *reinterpret_cast<uint4 *>(sg + ob) = ub;
+                }
                 if (p.ckpt != nullptr && r0 + lrow < Dv) {
                     float *ck = p.ckpt + (chk * Dv + r0 + lrow) * DK + cc;
 #pragma unroll

@@ -188,10 +188,14 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
                 yx[u] = t < len ? *reinterpret_cast<const uint4 *>(dy + ((rowbase + t) * Hv + h) * Dv + r0 + 8 * j)
                                 : make_uint4(0u, 0u, 0u, 0u);
             }
+            // [dY; dU] of this block for the gradient kernel: value group j at j * 2048, dY rows
+            // then dU rows, 16 bytes per row
+            unsigned char *gyu = reinterpret_cast<unsigned char *>(p.ws_yu + (chk * nsplit + split) * 2 * kL * kL);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int e = tid + 256 * u, t = e >> 3, j = e & 7;
                 *reinterpret_cast<uint4 *>(dys + cm_off(t, 16 * j, kL)) = yx[u];
+                *reinterpret_cast<uint4 *>(gyu + j * 2048 + 16 * t) = yx[u];
             }
         }
         if (tid < kL) {
@@ -278,10 +282,18 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
                     fs = fmaf(rs[i], x[i], fs);
                     y2[i] = fmaf(el, x[i], y2[i]);
                 }
+                const float bb = bt[lrow];
+                unsigned char *gdl = reinterpret_cast<unsigned char *>(p.ws_dl + (chk * nsplit + split) * kL * kL);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(rhs + cm_off(lrow, 2 * (half * 32 + 8 * j), kL)) = pack8(y2 + 8 * j);
-                red[half * kL + lrow] = bt[lrow] * fs;
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t o = cm_off(lrow, 2 * (half * 32 + 8 * j), kL);
+                    *reinterpret_cast<uint4 *>(rhs + o) = pack8(y2 + 8 * j);
+                    float dl8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) dl8[i] = bb * rs[8 * j + i];
+                    *reinterpret_cast<uint4 *>(gdl + o) = pack8(dl8);   // Delta for the gradient kernel
+                }
+                red[half * kL + lrow] = bb * fs;
             }
         }
         fence_proxy_async();
@@ -319,13 +331,13 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
                     dvv[i] = bb * x[i];
                     duu[i] = -dvv[i];
                 }
-                unsigned char *gdu = reinterpret_cast<unsigned char *>(p.ws_du + (chk * nsplit + split) * kL * kL);
+                unsigned char *gyu = reinterpret_cast<unsigned char *>(p.ws_yu + (chk * nsplit + split) * 2 * kL * kL);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t o = cm_off(lrow, 2 * (half * 32 + 8 * j), kL);
+                    const int grp = half * 4 + j;
                     const uint4 u = pack8(duu + 8 * j);
-                    *reinterpret_cast<uint4 *>(dus + o) = u;
-                    *reinterpret_cast<uint4 *>(gdu + o) = u;
+                    *reinterpret_cast<uint4 *>(dus + cm_off(lrow, 16 * grp, kL)) = u;
+                    *reinterpret_cast<uint4 *>(gyu + grp * 2048 + 1024 + 16 * lrow) = u;
                 }
                 if (lrow < len) {
                     uint4 *dvg = reinterpret_cast<uint4 *>(dv + ((rowbase + lrow) * Hv + h) * Dv + r0 + half * 32);
@@ -398,7 +410,7 @@ struct GradSmem {
         s0 = o;
         {
             const size_t a = (size_t)Dv * DK * 2, b2 = (size_t)3 * kL * kL * 4;
-            o += a > b2 ? a : b2;                                  // S0 [Dv][DK], later GE|HE, W, M
+            o += a > b2 ? a : b2;                                  // S0 [Dv / 64][64][DK], later GE|HE, W, M
         }
         gehe = s0; wt = s0 + (size_t)2 * kL * kL * 2; mt = wt + (size_t)kL * kL * 4;
         dsl = o;
@@ -452,9 +464,6 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
-    const __nv_bfloat16 *dy = static_cast<const __nv_bfloat16 *>(p.dy);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
 
     if (tid == 0) {
@@ -469,14 +478,19 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
     const uint32_t tmem = *tslot;
     const uint32_t tR1 = tmem, tR2 = tmem + DK, tS1 = tmem + 2 * DK, tS2 = tmem + 2 * DK + 64;
 
-    // ---- dS_L (all value-row blocks) and dU (into rows 64-127 of [dY; dU]) by bulk copy
+    // ---- every operand by bulk copy, in its layout: [Q; K] (written by the forward), [dY; dU]
+    // and Delta (by the reverse sweep, per block of value rows), S0 (by the forward sweep) and
+    // dS_L (by the reverse sweep)
     if (tid == 0) {
-        mbar_expect_tx(cbar, (unsigned)(nsplit * kL * DK * 2 + Dv * kL * 2));
+        const unsigned qkb = 2 * kL * DK * 2, yub = 2 * kL * kL * 2, dlb = kL * kL * 2, sb = kL * DK * 2;
+        mbar_expect_tx(cbar, qkb + (unsigned)nsplit * (yub + dlb + 2 * sb));
+        bulk_load(qk, p.qkm + (((size_t)b * Hk + hk) * p.NC + c) * 2 * kL * DK, qkb, cbar);
         for (int s = 0; s < nsplit; ++s) {
-            bulk_load(dsl + (size_t)s * kL * DK * 2, p.ws_dsl + (chk * nsplit + s) * kL * DK, kL * DK * 2, cbar);
-            const unsigned char *du = reinterpret_cast<const unsigned char *>(p.ws_du + (chk * nsplit + s) * kL * kL);
-            for (int j = 0; j < 8; ++j)
-                bulk_load(yu + (size_t)((8 * s + j) * 16 + 8) * 128, du + j * 1024, 1024, cbar);
+            const size_t blk = chk * nsplit + s;
+            bulk_load(yu + (size_t)s * yub, p.ws_yu + blk * 2 * kL * kL, yub, cbar);
+            bulk_load(dl + (size_t)s * dlb, p.ws_dl + blk * kL * kL, dlb, cbar);
+            bulk_load(s0 + (size_t)s * sb, p.s0m + blk * kL * DK, sb, cbar);
+            bulk_load(dsl + (size_t)s * sb, p.ws_dsl + blk * kL * DK, sb, cbar);
         }
     }
     // ---- decays, beta, f
@@ -491,66 +505,28 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
             for (int s = 0; s < nsplit; ++s) f += p.ws_f[((rowbase + tid) * Hv + h) * nsplit + s];
         fv[tid] = f;
     }
-    // ---- [Q; K] rows of the chunk (kv head), dY rows
-    {
-        constexpr int NQ = 2 * kL * DK / 8;
-        for (int e = tid; e < NQ; e += 256) {
-            const int r = e / (DK / 8), ch = e - r * (DK / 8), t = r & (kL - 1);
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (t < len) x = *reinterpret_cast<const uint4 *>((r < kL ? q : k) + ((rowbase + t) * Hk + hk) * DK + 8 * ch);
-            *reinterpret_cast<uint4 *>(qk + cm_off(r, 16 * ch, 2 * kL)) = x;
-        }
-        const int nv8 = Dv / 8;
-        for (int e = tid; e < kL * nv8; e += 256) {
-            const int t = e / nv8, ch = e - t * nv8;
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (t < len) x = *reinterpret_cast<const uint4 *>(dy + ((rowbase + t) * Hv + h) * Dv + 8 * ch);
-            *reinterpret_cast<uint4 *>(yu + cm_off(t, 16 * ch, 2 * kL)) = x;
-        }
-    }
     __syncthreads();
     if (tid < kL) {
         LmP[tid] = tid > 0 ? Lm[tid - 1] : 0.f;
         eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
     }
-    // ---- Delta = diag(beta) (v - u)
-    {
-        const int nv8 = Dv / 8;
-        for (int e = tid; e < kL * nv8; e += 256) {
-            const int t = e / nv8, ch = e - t * nv8;
-            float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (t < len) {
-                const float4 *rg = reinterpret_cast<const float4 *>(p.resid + ((rowbase + t) * Hv + h) * Dv + 8 * ch);
-                const float4 a = rg[0], a2 = rg[1];
-                const float bb = bt[t];
-                x[0] = bb * a.x; x[1] = bb * a.y; x[2] = bb * a.z; x[3] = bb * a.w;
-                x[4] = bb * a2.x; x[5] = bb * a2.y; x[6] = bb * a2.z; x[7] = bb * a2.w;
-            }
-            *reinterpret_cast<uint4 *>(dl + cm_off(t, 16 * ch, kL)) = pack8(x);
-        }
-    }
-    bool ok = !__syncthreads_or(!mbar_wait(cbar, 0));   // every thread reads dS_L below
-    // ---- S0 (the chunk-start state) as a bf16 operand; c0 = <dS_L, S0> with S0 in fp32
+    bool ok = !__syncthreads_or(!mbar_wait(cbar, 0));   // every thread reads S0 and dS_L below
+    // ---- c0 = <dS_L, S0> (both in the same layout)
     float c0s = 0.f;
     if (ok) {
-        const float *S0g = p.ckpt + chk * (size_t)Dv * DK;
+        const uint4 *a4 = reinterpret_cast<const uint4 *>(s0), *d4 = reinterpret_cast<const uint4 *>(dsl);
         const int n8 = Dv * DK / 8;
-#pragma unroll 2
+#pragma unroll 4
         for (int e = tid; e < n8; e += 256) {
-            const int v = e / (DK / 8), ch = e - v * (DK / 8);
-            const float4 a = reinterpret_cast<const float4 *>(S0g)[2 * e];
-            const float4 a2 = reinterpret_cast<const float4 *>(S0g)[2 * e + 1];
-            const float x[8] = {a.x, a.y, a.z, a.w, a2.x, a2.y, a2.z, a2.w};
-            *reinterpret_cast<uint4 *>(s0 + cm_off(v, 16 * ch, Dv)) = pack8(x);
-            float d[8];
-            unpack8(*reinterpret_cast<const uint4 *>(dsl + (size_t)(v >> 6) * kL * DK * 2 + cm_off(v & (kL - 1), 16 * ch, kL)), d);
+            float x[8], d[8];
+            unpack8(a4[e], x);
+            unpack8(d4[e], d);
 #pragma unroll
             for (int i = 0; i < 8; ++i) c0s = fmaf(x[i], d[i], c0s);
         }
     }
     c0s = warp_sum(c0s);
     if (lane == 0) c0p[warp] = c0s;
-    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -560,11 +536,12 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
                   umma_idesc_t(1, 2 * kL, kL, false, false), false);
         umma_gemm(tS2, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{dl, kL, 0, 0, false}, Dv,
                   umma_idesc_t(1, 2 * kL, kL, false, false), false);
-        umma_gemm(tR1, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{s0, Dv, 0, 0, true}, Dv,
-                  umma_idesc_t(1, 2 * kL, DK, false, true), false);
-        for (int s = 0; s < nsplit; ++s)
+        for (int s = 0; s < nsplit; ++s) {
+            umma_gemm(tR1, CmOp{yu, 2 * kL, 0, kL * s, false}, CmOp{s0 + (size_t)s * kL * DK * 2, kL, 0, 0, true}, kL,
+                      umma_idesc_t(1, 2 * kL, DK, false, true), s > 0);
             umma_gemm(tR2, CmOp{dl, kL, 0, kL * s, false}, CmOp{dsl + (size_t)s * kL * DK * 2, kL, 0, 0, true}, kL,
                       umma_idesc_t(1, kL, DK, false, true), s > 0);
+        }
         umma_commit(bar);
     }
     if (ok) ok = !__syncthreads_or(!mbar_wait(bar, 0));

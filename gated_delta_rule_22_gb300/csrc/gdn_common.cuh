@@ -75,14 +75,16 @@ static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <=
 // saved buffer: lam, the in-chunk log-decay prefix [64]; um, U [64][Dv] fp32; and the sweep's
 // tensor-core operands, bf16 in their shared-memory (core-matrix) layout: wm W [64][Dk],
 // qsm diag(exp Lam) Q [64][Dk], ksm diag(exp Lam) K [64][Dk], ktm K^T [Dk][64],
-// pm (Q K^T) o E_incl [64][64], kkm (K K^T) o E_strict [64][64], tm T = (I + A)^-1 [64][64].
+// pm (Q K^T) o E_incl [64][64], kkm (K K^T) o E_strict [64][64], tm T = (I + A)^-1 [64][64];
+// per (b, h, chunk, block of 64 value rows) s0m, the chunk-start state in bf16 [64][Dk]; and
+// per (b, kv head, chunk) qkm, [Q; K] of the chunk [128][Dk].
 struct ChunkParams {
     const void *q, *k, *v, *g, *beta;
     const float *S0;
     void *y;
     float *S_T, *ckpt, *resid;
     float *lam;
-    __nv_bfloat16 *pm, *kkm, *wm, *qsm, *ksm, *ktm, *tm;
+    __nv_bfloat16 *pm, *kkm, *wm, *qsm, *ksm, *ktm, *tm, *s0m, *qkm;
     float *um;
     int *status;
     int B, T, Hk, Hv, Dv, NC;
@@ -91,15 +93,16 @@ struct ChunkParams {
 // Chunkwise tensor-core backward (same sizes as the chunkwise forward; consumes its saved
 // buffer). nsplit = Dv / 64 blocks of value rows.
 struct ChunkBwdParams {
-    const void *q, *k, *dy, *beta;
-    const float *ckpt, *resid, *lam;
-    const __nv_bfloat16 *tm, *pm, *qsm, *ksm, *ktm;
+    const void *dy, *beta;
+    const float *resid, *lam;
+    const __nv_bfloat16 *tm, *pm, *qsm, *ksm, *ktm, *s0m, *qkm;
     const float *dS_T;
     float *dS0;
     void *dv, *dg, *dq, *dk, *dbeta;
     float *ws_dq, *ws_dk;      // [B, T, Hv, Dk]: per value head
     float *ws_db, *ws_f;       // [B, T, Hv, nsplit]: per block of 64 value rows
-    __nv_bfloat16 *ws_du;      // [B, Hv, NC, nsplit][64 x 64]: -beta o ddelta, operand layout
+    __nv_bfloat16 *ws_yu;      // [B, Hv, NC, nsplit][128 x 64]: [dY; dU] of the block, operand layout
+    __nv_bfloat16 *ws_dl;      // [B, Hv, NC, nsplit][64 x 64]: Delta = diag(beta) (v - u), operand layout
     __nv_bfloat16 *ws_dsl;     // [B, Hv, NC, nsplit][64 x Dk]: dS at each chunk end, operand layout
     int *status;
     int B, T, Hk, Hv, Dv, NC, nsplit;
