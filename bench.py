@@ -39,28 +39,38 @@ FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # Apple-silicon Metal VJP, fwd+bwd at this exact shape (149.8 ms for T=2048, mlx-lm
 # PR #1217 performance table): another machine's number, quoted as context.
 PAGES_TOKENS_PER_S = 2048 / 0.1498
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant call from one
-# ncu capture, keyed by a hash of the kernel sources it was taken on (None: not measured
-# for the current sources).
-# gdn_bwd call = bwd_kernel + reduce_kernel, captured with
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of a kernel, from one ncu capture,
+# keyed by (hash of the kernel sources it was taken on, kernel family); absent: not measured
+# for the current sources.
+# Capture (bench workload, 5 chunk kernels of one step after 3 warm-up steps):
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
-#       -k regex:"bwd_kernel|reduce_kernel" -s 6 -c 2 python bench.py --steps 2 --warmup 3 --no-cpu-baseline
-# bwd_kernel 338.0 MB read + 944.2 MB written, reduce_kernel 404.8 MB + 20.1 MB.
-TRAFFIC = {"21be09ecae3f7db3": 337952000 + 944215552 + 404779008 + 20103168}
+#       -k regex:chunk_ -s 15 -c 5 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
+TRAFFIC = {
+    ("f286727a52b987e7", "chunk_prep"): 59350272 + 284655360,
+    ("f286727a52b987e7", "chunk_sweep"): 336266240 + 353604608,
+    ("f286727a52b987e7", "chunk_dsweep"): 286054400 + 196773120,
+    ("f286727a52b987e7", "chunk_grad"): 329587456 + 158589184,
+    ("f286727a52b987e7", "chunk_reduce"): 202411520 + 13944320,
+}
 
 
 def load_peaks():
+    """HBM GB/s and dense bf16 TFLOP/s (sustained: the kernels run inside a long step)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs"
-    return 6800.0, "fallback 6.8 TB/s"
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "MEASURED_PEAKS.json (hbm_gbs, bf16_tflops_sustained): of measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1700.0, "source": "fallback 6.8 TB/s, 1.7 PFLOP/s sustained: of fallback"}
 
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gdn_common.cuh", "gdn_fwd.cu", "gdn_bwd.cu", "gdn_api.cu"):
-        h.update(open(os.path.join(ROOT, "gated_delta_rule_22_gb300", "csrc", f), "rb").read())
+    csrc = os.path.join(ROOT, "gated_delta_rule_22_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -84,6 +94,60 @@ def bytes_per_step(w):
     fwd = 2 * qk + vv + 2 * gate + vv + (st if w.with_S0 else 0) + st + ck
     bwd = 2 * qk + vv + 2 * gate + ck + vv + (st if w.with_dST else 0) + 2 * qk + vv + 2 * gate + st
     return float(fwd + bwd)
+
+
+def kernel_model(w):
+    """Per kernel family: (algorithmic HBM bytes, tensor-core flops, FP32 flops) of one launch.
+    Bytes count every tensor a kernel must read or write once (re-reads served by L2 are
+    not counted); tensor flops are the issued MMA products of the chunkwise form (2 per
+    multiply-add); FP32 flops apply to the sequential kernels (fp32 inputs)."""
+    B, T, Hk, Hv, Dk, Dv, L = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv, w.chunk
+    NC = -(-T // L)
+    ch, ck = B * Hv * NC, B * Hk * NC               # (chunk, value head), (chunk, kv head)
+    e = 2 if w.dtype == "bf16" else 4
+    st = B * Hv * Dv * Dk * 4
+    rows = B * T * Hv
+    nsplit = max(1, Dv // 64)
+    m = {}
+    m["chunk_prep"] = (
+        ck * 2 * L * Dk * 2 + ch * L * Dv * 2 + 2 * rows * 2
+        + ch * (L * 4 + 3 * L * L * 2 + 4 * L * Dk * 2 + L * Dv * 4) + ck * 2 * L * Dk * 2,
+        ck * 2 * (2 * L * L * Dk) + ch * (2 * L * Dk * L + 2 * L * Dv * L), 0.0)
+    m["chunk_sweep"] = (
+        ch * (L * 4 + 4 * L * Dk * 2 + 2 * L * L * 2 + L * Dv * 4 + L * Dv * 2)
+        + ch * (L * Dv * 2 + L * Dv * 4 + Dv * Dk * 4 + Dv * Dk * 2) + (st if w.with_S0 else 0) + st,
+        ch * (2 * L * Dv * Dk * 3 + 2 * L * Dv * L * 2 + 2 * Dv * Dk * L), 0.0)
+    m["chunk_dsweep"] = (
+        ch * (L * 4 + 3 * L * Dk * 2 + 2 * L * L * 2 + L * Dv * 2 + L * Dv * 4)
+        + ch * (L * Dv * 2 + Dv * Dk * 2 + 2 * L * Dv * 2 + L * Dv * 2) + 2 * rows * nsplit * 4
+        + rows * 2 + (st if w.with_dST else 0) + st,
+        ch * (2 * 2 * L * Dv * Dk + 2 * L * Dv * L * 2 + 2 * Dv * Dk * L * 2), 0.0)
+    m["chunk_grad"] = (
+        ck * 2 * L * Dk * 2 + ch * (2 * L * Dv * 2 + L * Dv * 2 + 2 * Dv * Dk * 2 + L * 4)
+        + rows * (2 + nsplit * 4) + 2 * rows * Dk * 4 + rows * 2,
+        ch * 2 * (2 * L * L * Dk + 2 * L * L * Dv + 2 * L * Dk * Dv + L * Dk * Dv + 2 * L * Dk * L
+                  + 2 * L * Dk * L + L * L * L), 0.0)
+    m["chunk_reduce"] = (2 * rows * Dk * 4 + rows * nsplit * 4 + 2 * B * T * Hk * Dk * 2 + rows * 2, 0.0, 0.0)
+    qk, vv, gate, ckb = B * T * Hk * Dk * e, B * T * Hv * Dv * e, rows * e, ch * Dv * Dk * 4
+    m["seq_fwd"] = (2 * qk + 2 * vv + 2 * gate + ckb + st + rows * Dv * 4, 0.0, 7.0 * rows * Dv * Dk)
+    m["seq_bwd"] = (2 * qk + 2 * vv + 2 * gate + ckb + rows * Dv * 4 + 2 * rows * nsplit * Dk * 4 + st,
+                    0.0, 21.0 * rows * Dv * Dk)
+    m["seq_reduce"] = (2 * rows * nsplit * Dk * 4 + 2 * qk + 4 * rows * nsplit + 2 * gate, 0.0, 0.0)
+    return m
+
+
+def kernel_roofline(name, ms, model, peaks):
+    """The bound of one kernel launch taking `ms`: HBM bytes, tensor flops or FP32 flops,
+    whichever needs the most time at its peak; achieved is that quantity over `ms`."""
+    nbytes, tflops, fflops = model
+    hbm, bf16 = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    cands = [("hbm", nbytes / (hbm * 1e9), nbytes / (ms * 1e-3) / 1e9, hbm, "GB/s", nbytes),
+             ("tensor", tflops / (bf16 * 1e12), tflops / (ms * 1e-3) / 1e12, bf16, "TFLOP/s", tflops),
+             ("alu", fflops / (FP32_PEAK_TFLOPS * 1e12), fflops / (ms * 1e-3) / 1e12, FP32_PEAK_TFLOPS,
+              "TFLOP/s", fflops)]
+    bound, t_min, achieved, peak, unit, amount = max(cands, key=lambda c: c[1])
+    return {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "ms_per_launch": ms, "roofline_ms": t_min * 1e3, "per_launch": amount}
 
 
 # --------------------------------------------------------------------------- clocks
@@ -269,6 +333,17 @@ def run_ours(args, w):
         step_ms, fwd_ms, bwd_ms = (float(x) for x in m.tolist())
     clocks = clk.summary()
 
+    # per-kernel device times: the same steps again with the library's event timing on
+    gdn.gdn_timing_read()
+    gdn.gdn_timing_enable(True)
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    ktimes = gdn.gdn_timing_read()
+    gdn.gdn_timing_enable(False)
+    launches_per_step = sum(n for n, _ in ktimes.values()) / K
+
     # end to end through the public API: pinned host inputs in, host results out
     host_in = {n: torch.from_numpy(inp[n]).to(dt).pin_memory() for n in names}
     host_out = {n: torch.empty(x.shape, dtype=x.dtype).pin_memory() for n, x in
@@ -305,38 +380,53 @@ def run_ours(args, w):
 
     tokens = w.B * w.T * world
     value = tokens / (step_ms * 1e-3)
-    hbm_gbs, hbm_src = load_peaks()
+    peaks = load_peaks()
+    hbm_gbs = peaks["hbm_gbs"]
     f28, f22 = flops_per_step(w, 28), flops_per_step(w, 22)
-    bwd_flops = flops_per_step(w, 21)   # backward 15 + one re-computation 6
     nbytes = bytes_per_step(w)
     t_roof = max(nbytes / (hbm_gbs * 1e9), f28 / (FP32_PEAK_TFLOPS * 1e12))
     src_hash = kernel_source_hash()
+    model = kernel_model(w)
+    kernels = {}
+    for name, (n, ms) in ktimes.items():
+        kernels[name] = kernel_roofline(name, ms / n, model.get(name, (0.0, 0.0, 0.0)), peaks)
+        kernels[name]["launches_per_step"] = n / K
+        kernels[name]["share"] = ms / sum(t for _, t in ktimes.values())
+        kernels[name]["traffic"] = TRAFFIC.get((src_hash, name))
+    dominant = max(kernels.values(), key=lambda k: k["share"])
+    roof = {"bound": dominant["bound"], "achieved": dominant["achieved"], "peak": dominant["peak"],
+            "unit": dominant["unit"], "frac": dominant["frac"], "traffic": TRAFFIC.get((src_hash, dominant["kernel"])),
+            "kernel": dominant["kernel"], "ms_per_launch": dominant["ms_per_launch"],
+            "per_launch": dominant["per_launch"], "peak_source": peaks["source"] if dominant["bound"] != "alu"
+            else "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"}
+    mma = sum(model[k][1] for k in kernels if k in model)
+    chunk_t = max(nbytes / (hbm_gbs * 1e9), mma / (peaks["bf16_tflops"] * 1e12))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": value / PAGES_TOKENS_PER_S if w.name == "linattn-T2048" else None,
         "vs_baseline_note": "ratio to the Apple-silicon Metal VJP figure on the pages (another machine; context)",
-        "dtype": "f32", "data": "synthetic",
+        "dtype": "bf16 tensor-core operands, f32 state and accumulation" if mma > 0 else "f32",
+        "data": "synthetic",
         "config": config_of(w, l2="flushed between steps by an untimed 256 MiB write"),
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-        "roofline": {
-            "bound": "alu", "kernel": "gdn_bwd (bwd_kernel + reduce_kernel)",
-            "achieved": bwd_flops / (bwd_ms * 1e-3) / 1e12, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-            "frac": bwd_flops / (bwd_ms * 1e-3) / 1e12 / FP32_PEAK_TFLOPS,
-            "traffic": TRAFFIC.get(src_hash),
-            "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz",
-            "flops_per_launch": bwd_flops,
-        },
+        "roofline": roof,
         "roofline_step": {
             "bound": "alu", "flops_28": f28, "flops_22": f22, "bytes": nbytes,
             "roofline_ms": t_roof * 1e3, "frac": t_roof * 1e3 / step_ms,
             "achieved_tflops": f28 / (step_ms * 1e-3) / 1e12,
             "frac_22": f22 / (step_ms * 1e-3) / 1e12 / FP32_PEAK_TFLOPS,
-            "achieved_gbs": nbytes / (step_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm_gbs, "hbm_peak_source": hbm_src,
+            "achieved_gbs": nbytes / (step_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm_gbs,
+            "note": "sequential-form FP32 flops (28 per token, value head, Dv Dk) at the FP32 peak",
         },
+        "roofline_chunkwise": {
+            "bytes": nbytes, "mma_flops": mma, "roofline_ms": chunk_t * 1e3, "frac": chunk_t * 1e3 / step_ms,
+            "note": "max(algorithmic bytes / HBM, issued MMA flops / bf16 sustained peak) of the chunkwise form",
+        } if mma > 0 else None,
+        "kernels": kernels,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * K,
+        "gpu_launches": int(round(launches_per_step * K)),
         "clocks": clocks,
         "kernel_sources": src_hash,
     }

@@ -5,6 +5,6 @@ The compute lives in libgdn.so, a C-ABI library of hand-written CUDA kernels
 """
 from .binding import (  # noqa: F401
     GDN_BF16, GDN_F32, GdnError, GdnShape, gdn_bwd, gdn_bwd_workspace_bytes, gdn_ckpt_bytes, gdn_fwd,
-    gdn_gates_bwd, gdn_gates_fwd,
+    gdn_gates_bwd, gdn_gates_fwd, gdn_timing_enable, gdn_timing_read,
     header_functions, load_library, make_shape, new_ckpt,
 )

@@ -23,6 +23,10 @@ class GdnShape(ctypes.Structure):
                 ("Dk", ctypes.c_int), ("Dv", ctypes.c_int), ("chunk", ctypes.c_int), ("dtype", ctypes.c_int)]
 
 
+class GdnKernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("ms", ctypes.c_double)]
+
+
 class GdnError(RuntimeError):
     def __init__(self, fn, code, lib):
         self.code = code
@@ -66,6 +70,10 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_device_status.argtypes = []
     lib.gdn_version.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
+    lib.gdn_timing_enable.restype = ctypes.c_int
+    lib.gdn_timing_enable.argtypes = [ctypes.c_int]
+    lib.gdn_timing_read.restype = ctypes.c_int
+    lib.gdn_timing_read.argtypes = [ctypes.POINTER(GdnKernelTime), ctypes.c_int]
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -115,6 +123,21 @@ def _stream(stream):
     torch = _torch()
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def gdn_timing_enable(on: bool = True) -> None:
+    """Per-kernel device timing of the library's own launches (a diagnostic)."""
+    load_library().gdn_timing_enable(1 if on else 0)
+
+
+def gdn_timing_read() -> dict:
+    """{kernel family: (launches, summed ms)} since the last read; clears the record."""
+    lib = load_library()
+    buf = (GdnKernelTime * 32)()
+    n = lib.gdn_timing_read(buf, 32)
+    if n < 0:
+        raise GdnError("gdn_timing_read", n, lib)
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].ms) for i in range(min(n, 32))}
 
 
 def gdn_ckpt_bytes(shape: GdnShape) -> int:

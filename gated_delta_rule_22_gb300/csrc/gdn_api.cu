@@ -5,7 +5,9 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
+#include <vector>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
@@ -212,9 +214,98 @@ int make_qk_map(CUtensorMap *map, const void *ptr, const Plan &p, int box_t) {
     return GDN_OK;
 }
 
+// ---- per-kernel timing (gdn_timing_enable / gdn_timing_read)
+struct TimedLaunch {
+    const char *name;
+    cudaEvent_t start, stop;
+};
+std::atomic<bool> g_timing_on{false};
+std::mutex g_timing_mutex;
+std::vector<TimedLaunch> g_timed;          // launches recorded since the last read
+std::vector<cudaEvent_t> g_event_pool;     // events free for reuse
+
+cudaEvent_t pooled_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+void release_timed() {
+    for (const TimedLaunch &t : g_timed) {
+        if (t.start) g_event_pool.push_back(t.start);
+        if (t.stop) g_event_pool.push_back(t.stop);
+    }
+    g_timed.clear();
+}
+
 }  // namespace
 
+namespace gdn {
+void timing_mark(const char *kernel, int phase, cudaStream_t s) {
+    if (!g_timing_on.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    if (phase == 0) {
+        TimedLaunch t{kernel, pooled_event(), nullptr};
+        if (t.start == nullptr) return;
+        cudaEventRecord(t.start, s);
+        g_timed.push_back(t);
+    } else {
+        for (size_t i = g_timed.size(); i-- > 0;) {
+            TimedLaunch &t = g_timed[i];
+            if (t.stop == nullptr && strcmp(t.name, kernel) == 0) {
+                t.stop = pooled_event();
+                if (t.stop != nullptr) cudaEventRecord(t.stop, s);
+                break;
+            }
+        }
+    }
+}
+}  // namespace gdn
+
 extern "C" {
+
+int gdn_timing_enable(int on) {
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    g_timing_on.store(on != 0);
+    if (!on) release_timed();
+    return GDN_OK;
+}
+
+int gdn_timing_read(gdn_kernel_time *out, int max_entries) {
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    std::vector<gdn_kernel_time> agg;
+    int rc = GDN_OK;
+    for (const TimedLaunch &t : g_timed) {
+        if (t.stop == nullptr) continue;
+        float ms = 0.f;
+        cudaError_t e = cudaEventSynchronize(t.stop);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.start, t.stop);
+        if (e != cudaSuccess) {
+            rc = cuda_status(e);
+            break;
+        }
+        size_t j = 0;
+        while (j < agg.size() && strcmp(agg[j].name, t.name) != 0) ++j;
+        if (j == agg.size()) {
+            gdn_kernel_time k;
+            memset(&k, 0, sizeof k);
+            snprintf(k.name, sizeof k.name, "%s", t.name);
+            agg.push_back(k);
+        }
+        agg[j].launches += 1;
+        agg[j].ms += ms;
+    }
+    release_timed();
+    if (rc != GDN_OK) return rc;
+    for (int i = 0; i < (int)agg.size() && i < max_entries; ++i)
+        if (out != nullptr) out[i] = agg[(size_t)i];
+    return (int)agg.size();
+}
 
 size_t gdn_ckpt_bytes(const gdn_shape *shape) {
     Plan p;

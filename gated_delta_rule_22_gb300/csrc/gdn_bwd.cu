@@ -802,7 +802,9 @@ static cudaError_t launch_bwd_t(const BwdParams &p, const CUtensorMap &tq, const
     err = cudaFuncSetAttribute(bwd_kernel<E, TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid(p.nsplit, p.Hv, p.B);
+    timing_mark("seq_bwd", 0, s);
     bwd_kernel<E, TIn><<<grid, kBwdThreads, smem, s>>>(tq, tk, p);
+    timing_mark("seq_bwd", 1, s);
     return cudaGetLastError();
 }
 
@@ -833,8 +835,10 @@ cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s) {
     const int threads = 256;
     const size_t want = (n + threads - 1) / threads;
     const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
+    timing_mark("seq_reduce", 0, s);
     if (dtype == 0) reduce_kernel<float><<<blocks, threads, 0, s>>>(p);
     else reduce_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(p);
+    timing_mark("seq_reduce", 1, s);
     return cudaGetLastError();
 }
 

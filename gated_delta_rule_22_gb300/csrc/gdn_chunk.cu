@@ -705,10 +705,14 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(chunk_sweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
     if (err != cudaSuccess) return err;
+    timing_mark("chunk_prep", 0, s);
     chunk_prep_kernel<E><<<dim3(p.NC, p.Hk, p.B), 256, sp, s>>>(p);
+    timing_mark("chunk_prep", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    timing_mark("chunk_sweep", 0, s);
     chunk_sweep_kernel<E><<<dim3(p.Dv / kL, p.Hv, p.B), 256, ss, s>>>(p);
+    timing_mark("chunk_sweep", 1, s);
     return cudaGetLastError();
 }
 

@@ -776,16 +776,22 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(chunk_grad_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
     if (err != cudaSuccess) return err;
+    timing_mark("chunk_dsweep", 0, s);
     chunk_dsweep_kernel<E><<<dim3(p.nsplit, p.Hv, p.B), 256, sd, s>>>(p);
+    timing_mark("chunk_dsweep", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    timing_mark("chunk_grad", 0, s);
     chunk_grad_kernel<E><<<dim3(p.NC, p.Hv, p.B), 256, sg, s>>>(p);
+    timing_mark("chunk_grad", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const size_t n = (size_t)p.B * p.T * p.Hk * DK / 4 + (size_t)p.B * p.T * p.Hv;
     size_t blocks = (n + 255) / 256;
     if (blocks > 8 * 152) blocks = 8 * 152;
+    timing_mark("chunk_reduce", 0, s);
     chunk_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, DK);
+    timing_mark("chunk_reduce", 1, s);
     return cudaGetLastError();
 }
 

@@ -364,6 +364,11 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+// Per-kernel timing (gdn_timing_enable): every launcher calls timing_mark(name, 0, s) just
+// before and timing_mark(name, 1, s) just after each kernel launch; a no-op while timing is
+// off. Defined with the C ABI.
+void timing_mark(const char *kernel, int phase, cudaStream_t s);
+
 // Launchers (one per kernel family); each returns the cudaError_t of its launch.
 // tm_q / tm_k: 4-D tensor maps of q and k ([B, T, Hk, Dk], box {Dk, 1, kFwdTile, 1}).
 cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k, int Dk, int dtype,

@@ -329,7 +329,9 @@ static cudaError_t launch_fwd_t(const FwdParams &p, const CUtensorMap &tq, const
         cudaFuncSetAttribute(fwd_kernel<P, TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
     if (err != cudaSuccess) return err;
     dim3 grid((p.Dv + RB - 1) / RB, p.Hv, p.B);
+    timing_mark("seq_fwd", 0, s);
     fwd_kernel<P, TIn><<<grid, warps * 32, L.total, s>>>(tq, tk, p);
+    timing_mark("seq_fwd", 1, s);
     return cudaGetLastError();
 }
 

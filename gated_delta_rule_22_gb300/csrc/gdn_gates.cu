@@ -93,15 +93,19 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s) {
     const size_t n = (size_t)p.rows * p.Hv;
     const size_t want = (n + 255) / 256;
     const int blocks = (int)(want < 152 * 8 ? want : 152 * 8);
+    timing_mark("gates_fwd", 0, s);
     if (dtype == 0) gates_fwd_kernel<float><<<blocks, 256, 0, s>>>(p);
     else gates_fwd_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+    timing_mark("gates_fwd", 1, s);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s) {
     const int blocks = (p.Hv + 31) / 32;
+    timing_mark("gates_bwd", 0, s);
     if (dtype == 0) gates_bwd_kernel<float><<<blocks, 1024, 0, s>>>(p);
     else gates_bwd_kernel<__nv_bfloat16><<<blocks, 1024, 0, s>>>(p);
+    timing_mark("gates_bwd", 1, s);
     return cudaGetLastError();
 }
 

@@ -206,6 +206,25 @@ GDN_API int gdn_device_status(void);
 /* GDN_VERSION of the library that was loaded. */
 GDN_API int gdn_version(void);
 
+/* Per-kernel timing, a diagnostic (off by default). While it is on, every kernel that
+ * gdn_fwd, gdn_bwd and the gate calls launch is bracketed by two CUDA events recorded on
+ * the caller's stream, so the times are device times of each kernel on that stream. */
+typedef struct gdn_kernel_time {
+    char name[48];   /* kernel family, e.g. "chunk_grad" */
+    int launches;    /* launches recorded since the last read */
+    double ms;       /* their summed device time in milliseconds */
+} gdn_kernel_time;
+
+/* Turns per-kernel timing on (on != 0) or off; turning it off drops what was recorded.
+ * Returns GDN_OK. */
+GDN_API int gdn_timing_enable(int on);
+
+/* Waits for the recorded events (host-side wait), writes up to max_entries entries (one
+ * per kernel family, in order of first launch) to out, and clears the record. Returns the
+ * number of families recorded (which may exceed max_entries; out may then be NULL with
+ * max_entries 0), or GDN_ERR_CUDA. */
+GDN_API int gdn_timing_read(gdn_kernel_time *out, int max_entries);
+
 #ifdef __cplusplus
 }
 #endif
