@@ -91,7 +91,7 @@ ChunkLayout chunk_layout(const Plan &p) {
     c.wm = o; o += round_up(n * p.Dk * 2);
     c.qsm = o; o += round_up(n * p.Dk * 2);
     c.ksm = o; o += round_up(n * p.Dk * 2);
-    c.ktm = o; o += round_up(n * p.Dk * 2);
+    c.ktm = o; o += round_up((size_t)p.B * p.Hk * p.NC * 64 * p.Dk * 2);   // per kv head
     c.um = o; o += round_up(n * p.Dv * 4);
     c.tm = o; o += round_up(n * 64 * 2);
     c.s0m = o; o += round_up((size_t)p.B * p.Hv * p.NC * p.Dv * p.Dk * 2);

@@ -43,7 +43,7 @@ struct PrepSmem {
         tcm = o; o += (size_t)kL * kL * 2;          // T, bf16 operand [64][64]
         bw = o; o += (size_t)DK * kL * 2;           // (diag(beta exp Lam) K)^T, bf16 operand [DK][64]
         bu = o; o += (size_t)Dv * kL * 2;           // (diag(beta) V)^T, bf16 operand [Dv][64]
-        vr = o; o += (size_t)kL * Dv * 2;           // V of the chunk, row-major bf16
+        vr = o; o += (size_t)2 * kL * Dv * 2;       // V of the chunk, row-major bf16, two buffers (heads alternate)
         kr = o; o += (size_t)kL * DK * 2;           // K of the chunk, row-major bf16
         lam = o; o += 4 * kL * 4;                   // log g, Lam, exp Lam, beta
         bar = al(o, 8); o = bar + 8;
@@ -69,6 +69,15 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&x)[8]) {
     x[4] = __uint_as_float(u.z << 16); x[5] = __uint_as_float(u.z & 0xffff0000u);
     x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
 }
+
+// 16-byte asynchronous copy global -> shared; the bytes past src_bytes (0 or 16) are zero.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kPad), by 16 x 16 blocks:
 // the four diagonal blocks by forward substitution (a column per thread), then the blocks
@@ -229,26 +238,52 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
     __syncthreads();
     tc_fence_after();
 
+    // K^T of the chunk in its operand layout, once per kv head
+    {
+        unsigned char *Ktg = reinterpret_cast<unsigned char *>(p.ktm + (((size_t)b * p.Hk + hk) * p.NC + c) * kL * DK);
+        for (int e = tid; e < DK * 8; e += 256) {
+            const int ch = e / DK, n = e - ch * DK;
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = __bfloat162float(kr[(8 * ch + i) * DK + n]);
+            *reinterpret_cast<uint4 *>(Ktg + cm_off(n, 16 * ch, DK)) = pack8_bf16(x);
+        }
+    }
+    // V of a value head's chunk into buffer `buf` by asynchronous copies (rows past the end: zeros)
+    auto fetch_v = [&](int h, int buf) {
+        const int nv = kL * Dv / 8;
+        uint4 *dst = reinterpret_cast<uint4 *>(vr) + (size_t)buf * nv;
+        for (int e = tid; e < nv; e += 256) {
+            const int r = e / (Dv / 8), ch = e - r * (Dv / 8);
+            const int rr = r < len ? r : 0;
+            cp_async16(dst + e, v + (((size_t)b * T + t0 + rr) * Hv + h) * Dv + 8 * ch, r < len ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    // log g and beta of a value head (warp 0, two steps per lane), raw
+    __nv_bfloat16 graw[2], braw[2];
+    auto fetch_gb = [&](int h) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int t = 2 * lane + u;
+            const size_t o = ((size_t)b * T + t0 + (t < len ? t : 0)) * Hv + h;
+            graw[u] = g[o];
+            braw[u] = beta[o];
+        }
+    };
+    fetch_v(hk * rep, 0);
+    if (warp == 0) fetch_gb(hk * rep);
+
     for (int hh = 0; hh < rep && ok; ++hh) {
         const int h = hk * rep + hh;
         const size_t chk = ((size_t)b * Hv + h) * p.NC + c;   // (b, h, c)
-        // V of the chunk (row-major), loads issued first
-        {
-            constexpr int kMaxV = kL * 256 / 8 / 256;          // Dv <= 256
-            uint4 vx[kMaxV];
-            const int nv = kL * Dv / 8;
-#pragma unroll
-            for (int u = 0; u < kMaxV; ++u) {
-                const int e = tid + 256 * u, r = e / (Dv / 8), ch = e - r * (Dv / 8);
-                vx[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (e < nv && r < len)
-                    vx[u] = *reinterpret_cast<const uint4 *>(v + (((size_t)b * T + t0 + r) * Hv + h) * Dv + 8 * ch);
-            }
-#pragma unroll
-            for (int u = 0; u < kMaxV; ++u) {
-                const int e = tid + 256 * u;
-                if (e < nv) reinterpret_cast<uint4 *>(vr)[e] = vx[u];
-            }
+        __nv_bfloat16 *vrh = vr + (size_t)(hh & 1) * kL * Dv;
+        // the next head's V goes out now; this head's has landed once the older group is done
+        if (hh + 1 < rep) {
+            fetch_v(h + 1, (hh + 1) & 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
         // log g, beta and the in-chunk prefix Lam (warp 0: two steps per lane, a shuffle scan)
         if (warp == 0) {
@@ -257,10 +292,10 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
             for (int u = 0; u < 2; ++u) {
                 const int t = 2 * lane + u;
                 const bool in = t < len;
-                const size_t o = ((size_t)b * T + t0 + t) * Hv + h;
-                l2[u] = in ? fmaxf(logf(__bfloat162float(g[o])), -200.f) : 0.f;   // g = 0: exp(-200) = 0 in fp32; a nonzero bf16 g has log g > -93
-                b2[u] = in ? __bfloat162float(beta[o]) : 0.f;
+                l2[u] = in ? fmaxf(logf(__bfloat162float(graw[u])), -200.f) : 0.f;   // g = 0: exp(-200) = 0 in fp32; a nonzero bf16 g has log g > -93
+                b2[u] = in ? __bfloat162float(braw[u]) : 0.f;
             }
+            if (hh + 1 < rep) fetch_gb(h + 1);   // used one head later
             float s = l2[0] + l2[1];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -298,7 +333,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
             reinterpret_cast<uint4 *>(P)[e] = pack8_bf16(pv);
             reinterpret_cast<uint4 *>(KKm)[e] = pack8_bf16(kv8);
         }
-        // diag(exp Lam) Q and diag(exp Lam) K (row scaling of the staged operands), and K^T
+        // diag(exp Lam) Q and diag(exp Lam) K (row scaling of the staged operands)
         {
             uint4 *Qg = reinterpret_cast<uint4 *>(p.qsm + chk * kL * DK);
             uint4 *Kg = reinterpret_cast<uint4 *>(p.ksm + chk * kL * DK);
@@ -313,14 +348,6 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) a[j] *= gr;
                 Kg[e] = pack8_bf16(a);
-            }
-            unsigned char *Ktg = reinterpret_cast<unsigned char *>(p.ktm + chk * kL * DK);
-            for (int e = tid; e < DK * 8; e += 256) {
-                const int ch = e / DK, n = e - ch * DK;
-                float x[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = __bfloat162float(kr[(8 * ch + i) * DK + n]);
-                *reinterpret_cast<uint4 *>(Ktg + cm_off(n, 16 * ch, DK)) = pack8_bf16(x);
             }
         }
         __syncthreads();
@@ -350,7 +377,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int r = 8 * ch + i;
-                x[i] = bt[r] * __bfloat162float(vr[r * Dv + n]);
+                x[i] = bt[r] * __bfloat162float(vrh[r * Dv + n]);
             }
             *reinterpret_cast<uint4 *>(bu + cm_off(n, 16 * ch, Dv)) = pack8_bf16(x);
         }
@@ -434,7 +461,7 @@ struct SweepSmem {
         de = o; o += (size_t)kL * kL * 2;     // (diag(E_L) Delta)^T   A [64][64]
         dtile = o; o += (size_t)kL * kPad * 4; // Delta, fp32 [64][65]
         vec = o; o += 3 * kL * 4;             // Lam, exp Lam, E(L, .)
-        bar = al(o, 8); o = bar + 16;         // MMA completion, operand copies
+        bar = al(o, 8); o = bar + 24;         // MMA completion, the two groups of operand copies
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -468,30 +495,37 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
     unsigned char *pc = base + L.pc, *kkc = base + L.kkc, *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
     float *dtile = reinterpret_cast<float *>(base + L.dtile);
     float *Lm = reinterpret_cast<float *>(base + L.vec), *gm = Lm + kL, *eL = gm + kL;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1, *rbar = bar + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
     const size_t head = (size_t)b * Hv + h;
-    // the six operand matrices of chunk cc, prepared in their shared-memory layout (thread 0)
-    int copies = 0;
-    auto issue_copies = [&](int cc) {
+    // the six operand matrices of chunk cc, prepared in their shared-memory layout, by bulk
+    // copies in two groups (thread 0): W, read by the first product of a chunk, goes out as
+    // soon as that product is done; the rest, read by the second group, after that group
+    constexpr unsigned kBig = kL * DK * 2, kSmall = kL * kL * 2;
+    int ncw = 0, ncr = 0;
+    auto issue_w = [&](int cc) {
+        mbar_expect_tx(cbar, kBig);
+        bulk_load(wc, p.wm + (head * p.NC + cc) * kL * DK, kBig, cbar);
+        ++ncw;
+    };
+    auto issue_r = [&](int cc) {
         const size_t ck = head * p.NC + cc;
-        constexpr unsigned big = kL * DK * 2, small = kL * kL * 2;
-        mbar_expect_tx(cbar, 4 * big + 2 * small);
-        bulk_load(wc, p.wm + ck * kL * DK, big, cbar);
-        bulk_load(qs, p.qsm + ck * kL * DK, big, cbar);
-        bulk_load(ks, p.ksm + ck * kL * DK, big, cbar);
-        bulk_load(kt, p.ktm + ck * kL * DK, big, cbar);
-        bulk_load(pc, p.pm + ck * kL * kL, small, cbar);
-        bulk_load(kkc, p.kkm + ck * kL * kL, small, cbar);
-        ++copies;
+        mbar_expect_tx(rbar, 3 * kBig + 2 * kSmall);
+        bulk_load(qs, p.qsm + ck * kL * DK, kBig, rbar);
+        bulk_load(ks, p.ksm + ck * kL * DK, kBig, rbar);
+        bulk_load(kt, p.ktm + (((size_t)b * p.Hk + h / (Hv / p.Hk)) * p.NC + cc) * kL * DK, kBig, rbar);
+        bulk_load(pc, p.pm + ck * kL * kL, kSmall, rbar);
+        bulk_load(kkc, p.kkm + ck * kL * kL, kSmall, rbar);
+        ++ncr;
     };
 
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(cbar, 1);
+        mbar_init(rbar, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, 512);
@@ -516,66 +550,113 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
     }
     unsigned phase = 0, cph = 0;
     bool ok = true;
-    if (tid == 0) issue_copies(0);
-    for (int c = 0; c < p.NC && ok; ++c) {
-        const int t0 = c * kL, len = min(kL, T - t0);
-        const size_t chk = head * p.NC + c;
-        // ---- the chunk's operands (bulk copies issued one chunk ahead) and its decays
-        if (tid < kL) {
-            const float lt = p.lam[chk * kL + tid];
-            Lm[tid] = lt;
-            gm[tid] = expf(lt);
-        }
-        ok = !__syncthreads_or(!mbar_wait(cbar, cph & 1));
-        ++cph;
-        if (!ok) break;
-        if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
-        // ---- the state as an operand, and the chunk-start checkpoint
-        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
-            float x[16];
-            tmem_ld16f(tS + lane_off + cc, x);
+    float4 ux[8];        // U of the current chunk: this lane's row, this warp's 32 columns
+    uint4 vx[4];         // v of the chunk whose epilogue is pending
+    float lamn = 0.f;    // Lam of the next chunk (threads < 64)
+    auto load_u = [&](int cc) {
+        const float *Ug = p.um + (head * p.NC + cc) * kL * Dv + (size_t)lrow * Dv + r0 + half * 32;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            ux[i] = lane < 16 ? reinterpret_cast<const float4 *>(Ug)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto load_v = [&](int cc) {
+        const int tt0 = cc * kL, ln = min(kL, T - tt0);
+        const size_t o = (((size_t)b * T + tt0 + lrow) * Hv + h) * Dv + r0 + half * 32;
+        const bool mine = lane < 16 && lrow < ln;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vx[i] = mine ? reinterpret_cast<const uint4 *>(v + o)[i] : make_uint4(0u, 0u, 0u, 0u);
+    };
+    // y and v - u of chunk cc, from tensor memory (their columns are rewritten only by the
+    // next chunk's second group of products)
+    auto epilogue = [&](int cc) {
+        const int tt0 = cc * kL, ln = min(kL, T - tt0);
+        const size_t o = (((size_t)b * T + tt0 + lrow) * Hv + h) * Dv + r0 + half * 32;
+        const bool mine = lane < 16 && lrow < ln;
+        float x[16];
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+            const int cc2 = half * 32 + 16 * hc;
+            tmem_ld16f(tY + lane_off + cc2, x);
             tmem_wait_ld();
-            if (lane < 16) {
+            if (mine) {
                 float a[8], bb[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) { a[i] = x[i]; bb[i] = x[8 + i]; }
-                const uint4 ua = pack8_bf16(a), ub = pack8_bf16(bb);
-                const uint32_t oa = cm_off(lrow, 2 * cc, kL), ob = cm_off(lrow, 2 * cc + 16, kL);
-                *reinterpret_cast<uint4 *>(sop + oa) = ua;
-                *reinterpret_cast<uint4 *>(sop + ob) = ub;
-                if (p.s0m != nullptr) {
-                    // the same operand for the backward
-                    unsigned char *sg = reinterpret_cast<unsigned char *>(p.s0m + (chk * gridDim.x + split) * kL * DK);
-                    *reinterpret_cast<uint4 *>(sg + oa) = ua;
-                    *reinterpret_cast<uint4 *>(sg + ob) = ub;
-                }
-                if (p.ckpt != nullptr && r0 + lrow < Dv) {
-                    float *ck = p.ckpt + (chk * Dv + r0 + lrow) * DK + cc;
+                *reinterpret_cast<uint4 *>(y + o + 16 * hc) = pack8_bf16(a);
+                *reinterpret_cast<uint4 *>(y + o + 16 * hc + 8) = pack8_bf16(bb);
+            }
+            tmem_ld16f(tU + lane_off + cc2, x);
+            tmem_wait_ld();
+            if (mine && p.resid != nullptr) {
+                float va[8], vb[8];
+                unpack8_bf16(vx[2 * hc], va);
+                unpack8_bf16(vx[2 * hc + 1], vb);
+                float *rr = p.resid + o + 16 * hc;
 #pragma unroll
-                    for (int i = 0; i < 16; i += 4)
-                        *reinterpret_cast<float4 *>(ck + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+                for (int i = 0; i < 8; i += 4) {
+                    *reinterpret_cast<float4 *>(rr + i) = make_float4(va[i] - x[i], va[i + 1] - x[i + 1], va[i + 2] - x[i + 2], va[i + 3] - x[i + 3]);
+                    *reinterpret_cast<float4 *>(rr + 8 + i) = make_float4(vb[i] - x[8 + i], vb[i + 1] - x[9 + i], vb[i + 2] - x[10 + i], vb[i + 3] - x[11 + i]);
                 }
+            }
+        }
+    };
+    if (tid == 0) { issue_w(0); issue_r(0); }
+    if (tid < kL) lamn = p.lam[head * p.NC * kL + tid];
+    load_u(0);
+    for (int c = 0; c < p.NC && ok; ++c) {
+        const size_t chk = head * p.NC + c;
+        // ---- decays of the chunk (Lam loaded one chunk ahead)
+        if (tid < kL) {
+            Lm[tid] = lamn;
+            gm[tid] = expf(lamn);
+            if (c + 1 < p.NC) lamn = p.lam[(chk + 1) * kL + tid];
+        }
+        __syncthreads();
+        if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
+        // ---- the state as an operand, and the chunk-start checkpoint (all of this thread's
+        // columns loaded from tensor memory before one wait)
+        {
+            float xs[SC];
+#pragma unroll
+            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tS + lane_off + half * SC + 32 * j, xs + 32 * j);
+            tmem_wait_ld();
+            if (lane < 16) {
+                unsigned char *sg = p.s0m != nullptr
+                    ? reinterpret_cast<unsigned char *>(p.s0m + (chk * gridDim.x + split) * kL * DK) : nullptr;
+                float *ck = p.ckpt != nullptr ? p.ckpt + (chk * Dv + r0 + lrow) * DK + half * SC : nullptr;
+#pragma unroll
+                for (int j = 0; j < SC / 8; ++j) {
+                    const uint4 u = pack8_bf16(*reinterpret_cast<const float (*)[8]>(xs + 8 * j));
+                    const uint32_t o = cm_off(lrow, 2 * (half * SC + 8 * j), kL);
+                    *reinterpret_cast<uint4 *>(sop + o) = u;
+                    if (sg != nullptr) *reinterpret_cast<uint4 *>(sg + o) = u;   // the same operand for the backward
+                }
+                if (ck != nullptr)
+#pragma unroll
+                    for (int i = 0; i < SC; i += 4)
+                        *reinterpret_cast<float4 *>(ck + i) = make_float4(xs[i], xs[i + 1], xs[i + 2], xs[i + 3]);
             }
         }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        // W of the chunk (copied half a chunk ahead; only the MMAs read it)
+        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbar, cph & 1));
         tc_fence_after();
+        if (!ok) break;
         // ---- W S^T
         if (tid == 0) {
             umma_gemm_bf16(tD, wc, kL, 0, sop, kL, 0, DK, umma_idesc(1, kL, kL), false);
             umma_commit(bar);
         }
+        // the previous chunk's y and v - u while the product runs
+        if (c > 0) epilogue(c - 1);
+        tc_fence_before();
+        ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
+        ++phase;
+        tc_fence_after();
+        if (!ok) break;
+        if (tid == 0 && c + 1 < p.NC) issue_w(c + 1);      // W's buffer is free again
         {
-            // U of the chunk (this lane's row, this warp's 32 columns), loaded while the MMA runs
-            float4 ux[8];
-            const float *Ug = p.um + chk * kL * Dv + (size_t)lrow * Dv + r0 + half * 32;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ux[i] = lane < 16 ? reinterpret_cast<const float4 *>(Ug)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-            ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
-            ++phase;
-            tc_fence_after();
-            if (!ok) break;
             // Delta = U - W S^T into an fp32 tile
             float x[32];
             tmem_ld16f(tD + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(x));
@@ -587,11 +668,12 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
                 for (int i = 0; i < 32; ++i) dtile[lrow * kPad + half * 32 + i] = uf[i] - x[i];
             }
         }
+        if (c + 1 < p.NC) load_u(c + 1);                   // the next chunk's U, used one chunk later
         tc_fence_before();
         __syncthreads();
         // Delta^T and (diag(E_L) Delta)^T as operands: value column n, eight chunk rows per store
         for (int e = tid; e < kL * 8; e += 256) {
-            const int n = e >> 3, ch = e & 7;
+            const int n = e & (kL - 1), ch = e >> 6;        // consecutive threads: consecutive columns
             float a[8], bb[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -603,8 +685,11 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
             *reinterpret_cast<uint4 *>(de + cm_off(n, 16 * ch, kL)) = pack8_bf16(bb);
         }
         fence_proxy_async();
-        __syncthreads();
+        // the rest of the chunk's operands (copied a chunk ahead)
+        ok = !__syncthreads_or(tid == 0 && !mbar_wait(rbar, cph & 1));
+        ++cph;
         tc_fence_after();
+        if (!ok) break;
         // ---- y = Qs S^T + P Delta;  u = Ks S^T + KKm Delta;  update = (E_L Delta)^T K
         if (tid == 0) {
             constexpr uint32_t id64 = umma_idesc(1, kL, kL);
@@ -615,57 +700,25 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
             umma_gemm_bf16(tD, de, kL, 0, kt, DK, 0, kL, umma_idesc(1, kL, DK), false);
             umma_commit(bar);
         }
+        load_v(c);                                          // for this chunk's epilogue, one chunk later
+        ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
+        ++phase;
+        tc_fence_after();
+        if (!ok) break;
+        // the other operand buffers are free again: bring in the next chunk's
+        if (tid == 0 && c + 1 < p.NC) issue_r(c + 1);
+        // ---- the state after the chunk, 32 columns at a time
         {
-            // v of the chunk (this lane's row, 32 columns), loaded while the MMAs run
-            uint4 vx[4];
-            const size_t o = (((size_t)b * T + t0 + lrow) * Hv + h) * Dv + r0 + half * 32;
-            const bool mine = lane < 16 && lrow < len;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) vx[i] = mine ? reinterpret_cast<const uint4 *>(v + o)[i] : make_uint4(0u, 0u, 0u, 0u);
-            ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
-            ++phase;
-            tc_fence_after();
-            if (!ok) break;
-            // the operand buffers are free again: bring in the next chunk's
-            if (tid == 0 && c + 1 < p.NC) issue_copies(c + 1);
-            // ---- y and v - u of the chunk
-            float x[16];
-#pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {
-                const int cc = half * 32 + 16 * hc;
-                tmem_ld16f(tY + lane_off + cc, x);
-                tmem_wait_ld();
-                if (mine) {
-                    float a[8], bb[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) { a[i] = x[i]; bb[i] = x[8 + i]; }
-                    *reinterpret_cast<uint4 *>(y + o + 16 * hc) = pack8_bf16(a);
-                    *reinterpret_cast<uint4 *>(y + o + 16 * hc + 8) = pack8_bf16(bb);
-                }
-                tmem_ld16f(tU + lane_off + cc, x);
-                tmem_wait_ld();
-                if (mine && p.resid != nullptr) {
-                    float va[8], vb[8];
-                    unpack8_bf16(vx[2 * hc], va);
-                    unpack8_bf16(vx[2 * hc + 1], vb);
-                    float *rr = p.resid + o + 16 * hc;
-#pragma unroll
-                    for (int i = 0; i < 8; i += 4) {
-                        *reinterpret_cast<float4 *>(rr + i) = make_float4(va[i] - x[i], va[i + 1] - x[i + 1], va[i + 2] - x[i + 2], va[i + 3] - x[i + 3]);
-                        *reinterpret_cast<float4 *>(rr + 8 + i) = make_float4(vb[i] - x[8 + i], vb[i + 1] - x[9 + i], vb[i + 2] - x[10 + i], vb[i + 3] - x[11 + i]);
-                    }
-                }
-            }
-            // ---- the state after the chunk
             const float decay = gm[kL - 1];
-            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
-                float s[16], d[16];
-                tmem_ld16f(tS + lane_off + cc, s);
-                tmem_ld16f(tD + lane_off + cc, d);
+#pragma unroll
+            for (int j = 0; j < SC / 32; ++j) {
+                float s2[32], d[32];
+                tmem_ld32f(tS + lane_off + half * SC + 32 * j, s2);
+                tmem_ld32f(tD + lane_off + half * SC + 32 * j, d);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) s[i] = fmaf(decay, s[i], d[i]);
-                tmem_st16f(tS + lane_off + cc, s);
+                for (int i = 0; i < 32; ++i) s2[i] = fmaf(decay, s2[i], d[i]);
+                tmem_st32f(tS + lane_off + half * SC + 32 * j, s2);
             }
             tmem_wait_st();
         }
@@ -673,6 +726,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
         __syncthreads();
         tc_fence_after();
     }
+    if (ok) epilogue(p.NC - 1);
     if (ok && p.S_T != nullptr) {
         for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
             float x[16];
@@ -686,7 +740,9 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
     }
     if (!ok && tid == 0) {
         report_status(p.status, kStatusTimeout);
-        if (copies > (int)cph) mbar_wait(cbar, (copies - 1) & 1);   // copies still in flight
+        // copies still in flight land before the CTA exits (each wait bounded)
+        if (ncw > 0) mbar_wait(cbar, (ncw - 1) & 1);
+        if (ncr > 0) mbar_wait(rbar, (ncr - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
     auto copy_A = [&](int cc) {
         const size_t ck = head * p.NC + cc;
         mbar_expect_tx(cbA, 2 * kL * DK * 2 + kL * kL * 2);
-        bulk_load(kt, p.ktm + ck * kL * DK, kL * DK * 2, cbA);
+        bulk_load(kt, p.ktm + (((size_t)b * p.Hk + h / (Hv / p.Hk)) * p.NC + cc) * kL * DK, kL * DK * 2, cbA);
         bulk_load(qs, p.qsm + ck * kL * DK, kL * DK * 2, cbA);
         bulk_load(pmm, p.pm + ck * kL * kL, kL * kL * 2, cbA);
         ++nA;
@@ -173,23 +173,41 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
     }
     unsigned ph = 0, cph = 0;
     bool ok = true;
+    // a chunk's dY block (two 16-byte pieces per thread), its v - u (this lane's row, 32
+    // columns), Lam and beta (threads < 64): loaded one chunk ahead
+    uint4 yx[2];
+    float rs[32];
+    float lamn = 0.f, btn = 0.f;
+    auto load_chunk = [&](int cc) {
+        const int tt0 = cc * kL, ln = min(kL, T - tt0);
+        const size_t rb = (size_t)b * T + tt0;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + 256 * u, t = e >> 3, j = e & 7;
+            yx[u] = t < ln ? *reinterpret_cast<const uint4 *>(dy + ((rb + t) * Hv + h) * Dv + r0 + 8 * j)
+                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const bool mine = rowlane && lrow < ln;
+        const float4 *rg = reinterpret_cast<const float4 *>(p.resid + ((rb + (mine ? lrow : 0)) * Hv + h) * Dv + r0 + half * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 f4 = mine ? rg[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            rs[4 * i] = f4.x; rs[4 * i + 1] = f4.y; rs[4 * i + 2] = f4.z; rs[4 * i + 3] = f4.w;
+        }
+        if (tid < kL) {
+            lamn = p.lam[(head * p.NC + cc) * kL + tid];
+            btn = tid < ln ? __bfloat162float(beta[(rb + tid) * Hv + h]) : 0.f;
+        }
+    };
     if (tid == 0) { copy_A(p.NC - 1); copy_T(p.NC - 1); copy_K(p.NC - 1); }
+    load_chunk(p.NC - 1);
     for (int c = p.NC - 1; c >= 0 && ok; --c) {
         const int t0 = c * kL, len = min(kL, T - t0);
         const size_t chk = head * p.NC + c;
         const size_t rowbase = (size_t)b * T + t0;          // (b, t0) row of [B, T, ...]
-        // ---- this chunk's dY block into its operand layout, decays, beta, and this lane's
-        // v - u (row lrow, 32 value columns)
+        // ---- this chunk's dY block into its operand layout (and, with dU below, [dY; dU] for
+        // the gradient kernel: value group j at j * 2048, dY rows then dU rows, 16 bytes per row)
         {
-            uint4 yx[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + 256 * u, t = e >> 3, j = e & 7;
-                yx[u] = t < len ? *reinterpret_cast<const uint4 *>(dy + ((rowbase + t) * Hv + h) * Dv + r0 + 8 * j)
-                                : make_uint4(0u, 0u, 0u, 0u);
-            }
-            // [dY; dU] of this block for the gradient kernel: value group j at j * 2048, dY rows
-            // then dU rows, 16 bytes per row
             unsigned char *gyu = reinterpret_cast<unsigned char *>(p.ws_yu + (chk * nsplit + split) * 2 * kL * kL);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -199,18 +217,8 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
             }
         }
         if (tid < kL) {
-            Lm[tid] = p.lam[chk * kL + tid];
-            bt[tid] = tid < len ? __bfloat162float(beta[(rowbase + tid) * Hv + h]) : 0.f;
-        }
-        float rs[32];
-        {
-            const bool mine = rowlane && lrow < len;
-            const float4 *rg = reinterpret_cast<const float4 *>(p.resid + ((rowbase + lrow) * Hv + h) * Dv + r0 + half * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 f4 = mine ? rg[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-                rs[4 * i] = f4.x; rs[4 * i + 1] = f4.y; rs[4 * i + 2] = f4.z; rs[4 * i + 3] = f4.w;
-            }
+            Lm[tid] = lamn;
+            bt[tid] = btn;
         }
         __syncthreads();
         if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
@@ -218,31 +226,32 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
         // ---- dS (the adjoint of the chunk-end state) as operands (high and low bf16 parts),
         // stored for the gradient kernel; then dS <- exp(Lam_L) dS in place
         {
-            unsigned char *gdsl = reinterpret_cast<unsigned char *>(p.ws_dsl + (chk * nsplit + split) * kL * DK);
-            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
-                float x[16];
-                tmem_ld16f(tS + lane_off + cc, x);
-                tmem_wait_ld();
-                if (rowlane) {
-                    float hi[16], lo[16];
+            // all of this thread's columns loaded from tensor memory before one wait
+            float xs[SC];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        hi[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
-                        lo[i] = x[i] - hi[i];
+            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tS + lane_off + half * SC + 32 * j, xs + 32 * j);
+            tmem_wait_ld();
+            if (rowlane) {
+                unsigned char *gdsl = reinterpret_cast<unsigned char *>(p.ws_dsl + (chk * nsplit + split) * kL * DK);
+#pragma unroll
+                for (int j = 0; j < SC / 8; ++j) {
+                    float hi[8], lo[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        hi[i] = __bfloat162float(__float2bfloat16_rn(xs[8 * j + i]));
+                        lo[i] = xs[8 * j + i] - hi[i];
                     }
-                    const uint4 h0 = pack8(hi), h1 = pack8(hi + 8);
-                    const uint32_t o0 = cm_off(lrow, 2 * cc, kL), o1 = cm_off(lrow, 2 * cc + 16, kL);
-                    *reinterpret_cast<uint4 *>(shi + o0) = h0;
-                    *reinterpret_cast<uint4 *>(shi + o1) = h1;
-                    *reinterpret_cast<uint4 *>(slo + o0) = pack8(lo);
-                    *reinterpret_cast<uint4 *>(slo + o1) = pack8(lo + 8);
-                    *reinterpret_cast<uint4 *>(gdsl + o0) = h0;
-                    *reinterpret_cast<uint4 *>(gdsl + o1) = h1;
+                    const uint4 hu = pack8(hi);
+                    const uint32_t o = cm_off(lrow, 2 * (half * SC + 8 * j), kL);
+                    *reinterpret_cast<uint4 *>(shi + o) = hu;
+                    *reinterpret_cast<uint4 *>(slo + o) = pack8(lo);
+                    *reinterpret_cast<uint4 *>(gdsl + o) = hu;
                 }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] *= decay;
-                tmem_st16f(tS + lane_off + cc, x);
             }
+#pragma unroll
+            for (int i = 0; i < SC; ++i) xs[i] *= decay;
+#pragma unroll
+            for (int j = 0; j < SC / 32; ++j) tmem_st32f(tS + lane_off + half * SC + 32 * j, xs + 32 * j);
             tmem_wait_st();
         }
         fence_proxy_async();
@@ -353,6 +362,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
         tc_fence_after();
         if (tid < kL && tid < len)
             p.ws_db[((rowbase + tid) * Hv + h) * nsplit + split] = red[2 * kL + tid] + red[3 * kL + tid];
+        if (c > 0) load_chunk(c - 1);                       // this chunk's are used up
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbK, cph & 1));
         if (!ok) break;
         // ---- dS += dU^T diag(exp Lam) K
@@ -418,7 +428,7 @@ struct GradSmem {
             const size_t a = (size_t)Dv * DK * 2, b2 = (size_t)kL * DK * 4;
             o += a > b2 ? a : b2;                                  // dS_L [Dv / 64][64][DK], later dK part fp32 [64][DK]
         }
-        vec = o; o += (6 * kL + 2 * 2 * kL + 16) * 4;             // Lam, Lam_{t-1}, exp Lam, E(L,.), beta, f; ab [2][128]; c0 parts
+        vec = o; o += (6 * kL + 2 * 2 * kL + 16 + 12 * kL) * 4;   // Lam, Lam_{t-1}, exp Lam, E(L,.), beta, f; ab [2][128]; c0 parts; dg parts [4][3][64]
         bar = alb(o, 8); o = bar + 2 * 8;
         tslot = o; o += 16;
         total = o + 1024;
@@ -460,7 +470,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
     float *zt = reinterpret_cast<float *>(yu);
     float *dkb = reinterpret_cast<float *>(dsl);
     float *Lm = reinterpret_cast<float *>(base + L.vec), *LmP = Lm + kL, *gm = LmP + kL, *eL = gm + kL;
-    float *bt = eL + kL, *fv = bt + kL, *abp = fv + kL, *c0p = abp + 4 * kL;
+    float *bt = eL + kL, *fv = bt + kL, *abp = fv + kL, *c0p = abp + 4 * kL, *dgp = c0p + 16;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
@@ -581,19 +591,22 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
             constexpr int SC = DK / 2;
             const float gs = gm[s];
             float ab = 0.f;
-            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
-                float x[16], qv[16];
-                tmem_ld16f(tR1 + lane_off + cc, x);
-                unpack8(*reinterpret_cast<const uint4 *>(qk + cm_off(r, 2 * cc, 2 * kL)), qv);
-                unpack8(*reinterpret_cast<const uint4 *>(qk + cm_off(r, 2 * cc + 16, 2 * kL)), qv + 8);
-                tmem_wait_ld();
+            float x[SC];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    ab = fmaf(x[i], qv[i], ab);
-                    x[i] *= gs;
+            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < SC / 8; ++j) {
+                float qv[8];
+                unpack8(*reinterpret_cast<const uint4 *>(qk + cm_off(r, 2 * (half * SC + 8 * j), 2 * kL)), qv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    ab = fmaf(x[8 * j + i], qv[i], ab);
+                    x[8 * j + i] *= gs;
                 }
-                tmem_st16f(tR1 + lane_off + cc, x);
             }
+#pragma unroll
+            for (int j = 0; j < SC / 32; ++j) tmem_st32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
             abp[half * 2 * kL + r] = ab;
         }
         // ---- R2: rows scaled by E(L, t)
@@ -601,14 +614,14 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
             constexpr int SC = DK / 2;
             const int m = 16 * quarter + lane;
             const float sc = lane < 16 ? eL[m] : 1.f;
-            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
-                float x[16];
-                tmem_ld16f(tR2 + lane_off + cc, x);
-                tmem_wait_ld();
+            float x[SC];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] *= sc;
-                tmem_st16f(tR2 + lane_off + cc, x);
-            }
+            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < SC; ++i) x[i] *= sc;
+#pragma unroll
+            for (int j = 0; j < SC / 32; ++j) tmem_st32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
         }
         tmem_wait_st();
         __syncthreads();
@@ -667,32 +680,48 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
         }
         {
             constexpr int SC = DK / 2;
-            for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
-                float x[16];
-                tmem_ld16f(tR2 + lane_off + cc, x);
-                tmem_wait_ld();
-                if (lane < 16)
+            float x[SC];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<float4 *>(dkb + m * DK + swz(m, cc + 4 * j)) =
-                            make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-            }
+            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
+            tmem_wait_ld();
+            if (lane < 16)
+#pragma unroll
+                for (int j = 0; j < SC / 4; ++j)
+                    *reinterpret_cast<float4 *>(dkb + m * DK + swz(m, half * SC + 4 * j)) =
+                        make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
         }
     }
     __syncthreads();
+    if (ok) {
+        // ---- dg_t: the three sums over the chunk's steps, a quarter of the steps per thread
+        const int t = tid & (kL - 1), part = tid >> 6;
+        const float lt = Lm[t], lp = LmP[t];
+        float s2 = 0.f, s3 = 0.f, s4 = 0.f;
+        for (int j = 16 * part; j < 16 * part + 16; ++j) {
+            if (j < t) {
+                s2 = fmaf(expf(lp - Lm[j]), fv[j], s2);
+            } else {
+                const float ab = abp[j] + abp[2 * kL + j] + abp[kL + j] + abp[3 * kL + j];
+                s3 = fmaf(expf(lp + Lm[j] - lt), ab, s3);
+            }
+            s4 += zt[j * kPad + t];
+        }
+        dgp[(3 * part + 0) * kL + t] = s2;
+        dgp[(3 * part + 1) * kL + t] = s3;
+        dgp[(3 * part + 2) * kL + t] = s4;
+    }
+    __syncthreads();
     if (ok && tid < kL && tid < len) {
-        // ---- dg_t
         const int t = tid;
         float c0 = 0.f;
         for (int w = 0; w < 8; ++w) c0 += c0p[w];
-        const float lt = Lm[t], lp = LmP[t], lL = Lm[kL - 1];
         float s2 = 0.f, s3 = 0.f, s4 = 0.f;
-        for (int i = 0; i < t; ++i) s2 = fmaf(expf(lp - Lm[i]), fv[i], s2);
-        for (int s = t; s < kL; ++s) {
-            const float ab = abp[s] + abp[2 * kL + s] + abp[kL + s] + abp[3 * kL + s];
-            s3 = fmaf(expf(lp + Lm[s] - lt), ab, s3);
+        for (int part = 0; part < 4; ++part) {
+            s2 += dgp[(3 * part + 0) * kL + t];
+            s3 += dgp[(3 * part + 1) * kL + t];
+            s4 += dgp[(3 * part + 2) * kL + t];
         }
-        for (int s = 0; s < kL; ++s) s4 += zt[s * kPad + t];
+        const float lt = Lm[t], lp = LmP[t], lL = Lm[kL - 1];
         const float dgv = expf(lL - lt + lp) * c0 + expf(lL - lt) * s2 + s3 + s4;
         static_cast<__nv_bfloat16 *>(p.dg)[(rowbase + t) * Hv + h] = __float2bfloat16_rn(dgv);
     }
@@ -701,22 +730,21 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
         constexpr int SC = DK / 2;
         const int r = 32 * quarter + lane, s = r & (kL - 1);
         const bool upper = r >= kL;
-        float *dst = (upper ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + h) * DK;
-        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
-            float x[16];
-            tmem_ld16f(tR1 + lane_off + cc, x);
-            tmem_wait_ld();
-            if (upper)
+        float *dst = (upper ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + h) * DK + half * SC;
+        float x[SC];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 a = *reinterpret_cast<const float4 *>(dkb + s * DK + swz(s, cc + 4 * j));
-                    x[4 * j] += a.x; x[4 * j + 1] += a.y; x[4 * j + 2] += a.z; x[4 * j + 3] += a.w;
-                }
-            if (s < len)
+        for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
+        tmem_wait_ld();
+        if (upper)
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<float4 *>(dst + cc + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-        }
+            for (int j = 0; j < SC / 4; ++j) {
+                const float4 a = *reinterpret_cast<const float4 *>(dkb + s * DK + swz(s, half * SC + 4 * j));
+                x[4 * j] += a.x; x[4 * j + 1] += a.y; x[4 * j + 2] += a.z; x[4 * j + 3] += a.w;
+            }
+        if (s < len)
+#pragma unroll
+            for (int j = 0; j < SC / 4; ++j)
+                *reinterpret_cast<float4 *>(dst + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
     }
     if (!ok && tid == 0) {
         report_status(p.status, kStatusTimeout);
