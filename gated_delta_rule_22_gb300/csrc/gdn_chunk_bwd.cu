@@ -40,7 +40,6 @@ namespace gdn {
 namespace {
 
 constexpr int kL = 64;           // chunk length
-constexpr int kPad = kL + 1;
 
 __host__ __device__ inline size_t alb(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -410,75 +409,123 @@ namespace {
 
 // ------------------------------------------------------------------ per-chunk gradients
 struct GradSmem {
-    size_t qk, yu, dl, s0, dsl, vec, bar, tslot, total;
-    size_t gehe, wt, mt;      // in the s0 region once the first products are done
+    size_t qk, yu, dl, s0, dsl, vec, stg, bar, tslot, total;
+    size_t gehe, wst, mt;     // in the S0 region once the first products are done
     __host__ __device__ GradSmem(int DK, int Dv) {
         size_t o = 0;
         qk = o; o += (size_t)2 * kL * DK * 2;                      // [Q; K] [128][DK]
-        yu = o; o += alb((size_t)2 * kL * Dv * 2 > (size_t)kL * kPad * 4 ? (size_t)2 * kL * Dv * 2 : (size_t)kL * kPad * 4, 1024);   // [dY; dU] [128][Dv], later Z weighted [64][65] fp32
+        yu = o; o += (size_t)2 * kL * Dv * 2;                      // [dY; dU] [128][Dv]
         dl = o; o += (size_t)kL * Dv * 2;                          // Delta [64][Dv]
         s0 = o;
         {
-            const size_t a = (size_t)Dv * DK * 2, b2 = (size_t)3 * kL * kL * 4;
-            o += a > b2 ? a : b2;                                  // S0 [Dv / 64][64][DK], later GE|HE, W, M
+            const size_t a = (size_t)Dv * DK * 2, b2 = (size_t)5 * kL * kL * 2;
+            o += a > b2 ? a : b2;                                  // S0 [Dv / 64][64][DK]; later GE|HE, W1|W2 [128][64], M^T [64][64]
         }
-        gehe = s0; wt = s0 + (size_t)2 * kL * kL * 2; mt = wt + (size_t)kL * kL * 4;
-        dsl = o;
-        {
-            const size_t a = (size_t)Dv * DK * 2, b2 = (size_t)kL * DK * 4;
-            o += a > b2 ? a : b2;                                  // dS_L [Dv / 64][64][DK], later dK part fp32 [64][DK]
-        }
-        vec = o; o += (6 * kL + 2 * 2 * kL + 16 + 12 * kL) * 4;   // Lam, Lam_{t-1}, exp Lam, E(L,.), beta, f; ab [2][128]; c0 parts; dg parts [4][3][64]
-        bar = alb(o, 8); o = bar + 2 * 8;
+        gehe = s0; wst = s0 + (size_t)2 * kL * kL * 2; mt = wst + (size_t)2 * kL * kL * 2;
+        dsl = o; o += (size_t)Dv * DK * 2;                         // dS_L [Dv / 64][64][DK]
+        vec = o; o += (6 * kL + 4 * kL + 16 + 12 * kL + 4 * kL) * 4;   // Lam, Lam_{t-1}, exp Lam, E(L,.), beta, f; ab [2][128]; c0 parts; dg parts [4][3][64]; Z column sums [4][64]
+        stg = o; o += (size_t)32 * (DK + 4) * 4;                   // 32 output rows (fp32, padded) for coalesced stores
+        bar = alb(o, 8); o = bar + 4 * 8;                          // MMA; copies of (dY;dU, Delta, dS_L), of S0, of [Q; K]
         tslot = o; o += 16;
-        total = o + 1024;
+        total = o + 128;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
     }
 };
 
-// fp32 [64][DK] tile with its float4 slots permuted within each 32-column group by row
-// (conflict-free stores of 16 consecutive rows)
-__device__ __forceinline__ int swz(int m, int c) { return c ^ ((m & 7) << 2); }
-
 }  // namespace
 
-// One CTA per (chunk, value head, batch row). Tensor memory:
+// Persistent: one CTA per SM, each over a contiguous range of units (b, chunk, value head),
+// value head fastest, so that consecutive units share [Q; K]. Every operand arrives by bulk
+// copy, the next unit's as soon as its buffers are free: [dY; dU], Delta and dS_L after the
+// first products, S0 (whose region then holds the scratch operands) after the second, [Q; K]
+// (when the kv head or chunk changes) after the second.
+// Tensor memory:
 //   [0, DK)             R1, M = 128: rows 0-63 dQ, rows 64-127 the dK terms with B = S0 or K
-//   [DK, 2 DK)          R2, M = 64: the dK terms diag(E_L) Delta dS_L + GE^T Q + HE^T K
-//   [2 DK, 2 DK + 64)   [Q; K] K^T (M = 128), later Z (M = 64)
+//   [DK, 2 DK)          R2, M = 128: rows 64-127 the dK terms diag(E_L) Delta dS_L + GE^T Q +
+//                       HE^T K (the A operands are read from 64 rows before the real ones, so
+//                       that row t lands in the lane of R1's dK row t; rows 0-63 are not used)
+//   [2 DK, 2 DK + 64)   [Q; K] K^T (M = 128), later [W1; W2] M (M = 128)
 //   [2 DK + 64, + 128)  [dY; dU] Delta^T = [G; H] (M = 128)
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
+__global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, int units) {
     constexpr int DK = 32 * E;
+    constexpr int SC = DK / 2;
     static_assert(2 * DK + 128 <= 512, "tensor memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, Dv = p.Dv, Hv = p.Hv, Hk = p.Hk, nsplit = p.nsplit;
-    const int hk = h / (Hv / Hk);
-    const int t0 = c * kL, len = min(kL, T - t0);
+    const int T = p.T, Dv = p.Dv, Hv = p.Hv, Hk = p.Hk, nsplit = p.nsplit, NC = p.NC, rep = Hv / Hk;
     const int quarter = warp & 3, half = warp >> 2;
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    const size_t head = (size_t)b * Hv + h, chk = head * p.NC + c;
-    const size_t rowbase = (size_t)b * T + t0;
+    const int u_begin = (int)((long long)blockIdx.x * units / gridDim.x);
+    const int u_end = (int)((long long)(blockIdx.x + 1) * units / gridDim.x);
 
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
+    unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 128));
     const GradSmem L(DK, Dv);
     unsigned char *qk = base + L.qk, *yu = base + L.yu, *dl = base + L.dl, *s0 = base + L.s0, *dsl = base + L.dsl;
-    unsigned char *gehe = base + L.gehe;
-    float *wt = reinterpret_cast<float *>(base + L.wt), *mt = reinterpret_cast<float *>(base + L.mt);
-    float *zt = reinterpret_cast<float *>(yu);
-    float *dkb = reinterpret_cast<float *>(dsl);
+    unsigned char *gehe = base + L.gehe, *wst = base + L.wst, *mt = base + L.mt;
+    float *stg = reinterpret_cast<float *>(base + L.stg);
     float *Lm = reinterpret_cast<float *>(base + L.vec), *LmP = Lm + kL, *gm = LmP + kL, *eL = gm + kL;
-    float *bt = eL + kL, *fv = bt + kL, *abp = fv + kL, *c0p = abp + 4 * kL, *dgp = c0p + 16;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1;
+    float *bt = eL + kL, *fv = bt + kL, *abp = fv + kL, *c0p = abp + 4 * kL, *dgp = c0p + 16, *zq = dgp + 12 * kL;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbA = bar + 1, *cbS = bar + 2, *cbQ = bar + 3;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
-
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
 
+    // unit u = ((b * NC + c) * Hv + h)
+    auto chunk_of = [&](int u, int &b, int &c, int &h) {
+        h = u % Hv;
+        const int bc = u / Hv;
+        c = bc % NC;
+        b = bc / NC;
+    };
+    constexpr unsigned kSb = kL * DK * 2, kYub = 2 * kL * kL * 2, kDlb = kL * kL * 2, kQkb = 2 * kL * DK * 2;
+    int nA = 0, nS = 0, nQ = 0, wA = 0, wS = 0, wQ = 0;
+    auto copy_a = [&](int u) {            // [dY; dU], Delta and dS_L of unit u
+        int b, c, h;
+        chunk_of(u, b, c, h);
+        const size_t chk = ((size_t)b * Hv + h) * NC + c;
+        mbar_expect_tx(cbA, (unsigned)nsplit * (kYub + kDlb + kSb));
+        for (int s = 0; s < nsplit; ++s) {
+            const size_t blk = chk * nsplit + s;
+            bulk_load(yu + (size_t)s * kYub, p.ws_yu + blk * 2 * kL * kL, kYub, cbA);
+            bulk_load(dl + (size_t)s * kDlb, p.ws_dl + blk * kL * kL, kDlb, cbA);
+            bulk_load(dsl + (size_t)s * kSb, p.ws_dsl + blk * kL * DK, kSb, cbA);
+        }
+        ++nA;
+    };
+    auto copy_s = [&](int u) {            // S0 of unit u
+        int b, c, h;
+        chunk_of(u, b, c, h);
+        const size_t chk = ((size_t)b * Hv + h) * NC + c;
+        mbar_expect_tx(cbS, (unsigned)nsplit * kSb);
+        for (int s = 0; s < nsplit; ++s) bulk_load(s0 + (size_t)s * kSb, p.s0m + (chk * nsplit + s) * kL * DK, kSb, cbS);
+        ++nS;
+    };
+    auto copy_q = [&](int u) {            // [Q; K] of unit u's chunk and kv head
+        int b, c, h;
+        chunk_of(u, b, c, h);
+        mbar_expect_tx(cbQ, kQkb);
+        bulk_load(qk, p.qkm + (((size_t)b * Hk + h / rep) * NC + c) * 2 * kL * DK, kQkb, cbQ);
+        ++nQ;
+    };
+    auto same_qk = [&](int u1, int u2) { return u1 / rep == u2 / rep; };   // same (b, chunk, kv head)
+    // decays, beta and f of a unit (threads < 64), loaded one unit ahead
+    float vlam = 0.f, vbt = 0.f, vf = 0.f;
+    auto load_vec = [&](int u) {
+        if (tid >= kL) return;
+        int b, c, h;
+        chunk_of(u, b, c, h);
+        const size_t chk = ((size_t)b * Hv + h) * NC + c;
+        const int t0 = c * kL, len = min(kL, T - t0);
+        const size_t row = ((size_t)b * T + t0 + tid) * Hv + h;
+        vlam = p.lam[chk * kL + tid];
+        vbt = tid < len ? __bfloat162float(beta[row]) : 0.f;
+        vf = 0.f;
+        if (tid < len)
+            for (int s = 0; s < nsplit; ++s) vf += p.ws_f[row * nsplit + s];
+    };
+
     if (tid == 0) {
-        mbar_init(bar, 1);
-        mbar_init(cbar, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, 512);
@@ -488,267 +535,270 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p) {
     const uint32_t tmem = *tslot;
     const uint32_t tR1 = tmem, tR2 = tmem + DK, tS1 = tmem + 2 * DK, tS2 = tmem + 2 * DK + 64;
 
-    // ---- every operand by bulk copy, in its layout: [Q; K] (written by the forward), [dY; dU]
-    // and Delta (by the reverse sweep, per block of value rows), S0 (by the forward sweep) and
-    // dS_L (by the reverse sweep)
-    if (tid == 0) {
-        const unsigned qkb = 2 * kL * DK * 2, yub = 2 * kL * kL * 2, dlb = kL * kL * 2, sb = kL * DK * 2;
-        mbar_expect_tx(cbar, qkb + (unsigned)nsplit * (yub + dlb + 2 * sb));
-        bulk_load(qk, p.qkm + (((size_t)b * Hk + hk) * p.NC + c) * 2 * kL * DK, qkb, cbar);
-        for (int s = 0; s < nsplit; ++s) {
-            const size_t blk = chk * nsplit + s;
-            bulk_load(yu + (size_t)s * yub, p.ws_yu + blk * 2 * kL * kL, yub, cbar);
-            bulk_load(dl + (size_t)s * dlb, p.ws_dl + blk * kL * kL, dlb, cbar);
-            bulk_load(s0 + (size_t)s * sb, p.s0m + blk * kL * DK, sb, cbar);
-            bulk_load(dsl + (size_t)s * sb, p.ws_dsl + blk * kL * DK, sb, cbar);
+    if (tid == 0 && u_begin < u_end) {
+        copy_q(u_begin);
+        copy_a(u_begin);
+        copy_s(u_begin);
+    }
+    if (u_begin < u_end) load_vec(u_begin);
+    unsigned ph = 0;
+    bool ok = true;
+    for (int u = u_begin; u < u_end && ok; ++u) {
+        int b, c, h;
+        chunk_of(u, b, c, h);
+        const int t0 = c * kL, len = min(kL, T - t0);
+        const size_t rowbase = (size_t)b * T + t0;
+        const bool newq = u == u_begin || !same_qk(u - 1, u);
+        // ---- decays, beta, f
+        if (tid < kL) {
+            Lm[tid] = vlam;
+            gm[tid] = expf(vlam);
+            bt[tid] = vbt;
+            fv[tid] = vf;
         }
-    }
-    // ---- decays, beta, f
-    if (tid < kL) {
-        const float lt = p.lam[chk * kL + tid];
-        Lm[tid] = lt;
-        gm[tid] = expf(lt);
-        const bool in = tid < len;
-        bt[tid] = in ? __bfloat162float(beta[(rowbase + tid) * Hv + h]) : 0.f;
-        float f = 0.f;
-        if (in)
-            for (int s = 0; s < nsplit; ++s) f += p.ws_f[((rowbase + tid) * Hv + h) * nsplit + s];
-        fv[tid] = f;
-    }
-    __syncthreads();
-    if (tid < kL) {
-        LmP[tid] = tid > 0 ? Lm[tid - 1] : 0.f;
-        eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
-    }
-    bool ok = !__syncthreads_or(!mbar_wait(cbar, 0));   // every thread reads S0 and dS_L below
-    // ---- c0 = <dS_L, S0> (both in the same layout)
-    float c0s = 0.f;
-    if (ok) {
-        const uint4 *a4 = reinterpret_cast<const uint4 *>(s0), *d4 = reinterpret_cast<const uint4 *>(dsl);
-        const int n8 = Dv * DK / 8;
-#pragma unroll 4
-        for (int e = tid; e < n8; e += 256) {
-            float x[8], d[8];
-            unpack8(a4[e], x);
-            unpack8(d4[e], d);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) c0s = fmaf(x[i], d[i], c0s);
+        __syncthreads();
+        if (tid < kL) {
+            LmP[tid] = tid > 0 ? Lm[tid - 1] : 0.f;
+            eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
         }
-    }
-    c0s = warp_sum(c0s);
-    if (lane == 0) c0p[warp] = c0s;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // ---- first products: [Q; K] K^T, [dY; dU] Delta^T, [dY; dU] S0, Delta dS_L
-    if (ok && tid == 0) {
-        umma_gemm(tS1, CmOp{qk, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, kL, 0, false}, DK,
-                  umma_idesc_t(1, 2 * kL, kL, false, false), false);
-        umma_gemm(tS2, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{dl, kL, 0, 0, false}, Dv,
-                  umma_idesc_t(1, 2 * kL, kL, false, false), false);
-        for (int s = 0; s < nsplit; ++s) {
-            umma_gemm(tR1, CmOp{yu, 2 * kL, 0, kL * s, false}, CmOp{s0 + (size_t)s * kL * DK * 2, kL, 0, 0, true}, kL,
-                      umma_idesc_t(1, 2 * kL, DK, false, true), s > 0);
-            umma_gemm(tR2, CmOp{dl, kL, 0, kL * s, false}, CmOp{dsl + (size_t)s * kL * DK * 2, kL, 0, 0, true}, kL,
-                      umma_idesc_t(1, kL, DK, false, true), s > 0);
-        }
-        umma_commit(bar);
-    }
-    if (ok) ok = !__syncthreads_or(!mbar_wait(bar, 0));
-    tc_fence_after();
-    if (ok) {
-        // ---- G o E_incl, H o E_strict (operands), W = G o (Q K^T) + H o (K K^T) (tf32 operand)
-        const int r = 32 * quarter + lane, s = r & (kL - 1);
-        const bool upper = r >= kL;
-        float wv[32];
+        // ---- this unit's operands (every thread reads S0 and dS_L, and [Q; K] rows in pass 1)
         {
-            float a[32], g2[32];
-            tmem_ld16f(tS1 + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(a));
-            tmem_ld16f(tS1 + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(a + 16));
-            tmem_ld16f(tS2 + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(g2));
-            tmem_ld16f(tS2 + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(g2 + 16));
+            bool w = mbar_wait(cbA, wA & 1) && mbar_wait(cbS, wS & 1);
+            if (newq) w = w && mbar_wait(cbQ, wQ & 1);
+            ok = !__syncthreads_or(!w);
+            ++wA;
+            ++wS;
+            if (newq) ++wQ;
+        }
+        tc_fence_after();
+        if (!ok) break;
+        // ---- first products: [Q; K] K^T, [dY; dU] Delta^T, [dY; dU] S0, Delta dS_L
+        if (tid == 0) {
+            umma_gemm(tS1, CmOp{qk, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, kL, 0, false}, DK,
+                      umma_idesc_t(1, 2 * kL, kL, false, false), false);
+            umma_gemm(tS2, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{dl, kL, 0, 0, false}, Dv,
+                      umma_idesc_t(1, 2 * kL, kL, false, false), false);
+            for (int s = 0; s < nsplit; ++s) {
+                umma_gemm(tR1, CmOp{yu, 2 * kL, 0, kL * s, false}, CmOp{s0 + (size_t)s * kSb, kL, 0, 0, true}, kL,
+                          umma_idesc_t(1, 2 * kL, DK, false, true), s > 0);
+                umma_gemm(tR2, CmOp{dl, kL, -kL, kL * s, false}, CmOp{dsl + (size_t)s * kSb, kL, 0, 0, true}, kL,
+                          umma_idesc_t(1, 2 * kL, DK, false, true), s > 0);
+            }
+            umma_commit(bar);
+        }
+        // ---- c0 = <dS_L, S0> (both in the same layout) while the products run
+        {
+            float c0s = 0.f;
+            const uint4 *a4 = reinterpret_cast<const uint4 *>(s0), *d4 = reinterpret_cast<const uint4 *>(dsl);
+            const int n8 = Dv * DK / 8;
+#pragma unroll 4
+            for (int e = tid; e < n8; e += 256) {
+                float x[8], d[8];
+                unpack8(a4[e], x);
+                unpack8(d4[e], d);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) c0s = fmaf(x[i], d[i], c0s);
+            }
+            c0s = warp_sum(c0s);
+            if (lane == 0) c0p[warp] = c0s;
+        }
+        tc_fence_before();
+        ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
+        ++ph;
+        tc_fence_after();
+        if (!ok) break;
+        // [dY; dU], Delta and dS_L are used up: the next unit's go out now
+        if (tid == 0 && u + 1 < u_end) copy_a(u + 1);
+        if (u + 1 < u_end) load_vec(u + 1);                // used at the next unit's start
+        {
+            // ---- G o E_incl, H o E_strict and [W1; W2] = [G o QK^T; H o KK^T] as operands
+            const int r = 32 * quarter + lane, s = r & (kL - 1);
+            const bool upper = r >= kL;
+            {
+                float a[32], g2[32];
+                tmem_ld32f(tS1 + lane_off + half * 32, a);
+                tmem_ld32f(tS2 + lane_off + half * 32, g2);
+                tmem_wait_ld();
+                const float ls = Lm[s];
+                float ge[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = half * 32 + i;
+                    const bool keep = upper ? col < s : col <= s;
+                    ge[i] = keep ? g2[i] * expf(ls - Lm[col]) : 0.f;
+                    a[i] *= g2[i];
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t o = cm_off(r, 2 * (half * 32 + 8 * j), 2 * kL);
+                    *reinterpret_cast<uint4 *>(gehe + o) = pack8(ge + 8 * j);
+                    *reinterpret_cast<uint4 *>(wst + o) = pack8(a + 8 * j);
+                }
+            }
+            // ---- R1: a_s = (dY S0)_s . q_s, b_s = (dU S0)_s . k_s; then the rows scaled by exp(Lam_s)
+            {
+                const float gs = gm[s];
+                float ab = 0.f;
+                float x[SC];
+#pragma unroll
+                for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < SC / 8; ++j) {
+                    float qv[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(qk + cm_off(r, 2 * (half * SC + 8 * j), 2 * kL)), qv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        ab = fmaf(x[8 * j + i], qv[i], ab);
+                        x[8 * j + i] *= gs;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < SC / 32; ++j) tmem_st32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
+                abp[half * 2 * kL + r] = ab;
+            }
+            // ---- R2 (rows 64-127): scaled by E(L, t)
+            if (upper) {
+                const float sc = eL[s];
+                float x[SC];
+#pragma unroll
+                for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < SC; ++i) x[i] *= sc;
+#pragma unroll
+                for (int j = 0; j < SC / 32; ++j) tmem_st32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
+            }
+            // ---- M^T [t][i] = E(t-1, i) for i < t, bf16 operand
+            for (int e = tid; e < kL * kL / 8; e += 256) {
+                const int t = e & (kL - 1), i0 = 8 * (e >> 6);
+                float m8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) m8[j] = i0 + j < t ? expf(LmP[t] - Lm[i0 + j]) : 0.f;
+                *reinterpret_cast<uint4 *>(mt + cm_off(t, 2 * i0, kL)) = pack8(m8);
+            }
+        }
+        tmem_wait_st();
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- second products: R1 += [GE; HE] K, R2 += GE^T Q + HE^T K, Z = [W1; W2] M
+        if (tid == 0) {
+            umma_gemm(tR1, CmOp{gehe, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
+                      umma_idesc_t(1, 2 * kL, DK, false, true), true);
+            umma_gemm(tR2, CmOp{gehe, 2 * kL, -kL, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, kL,
+                      umma_idesc_t(1, 2 * kL, DK, true, true), true);
+            umma_gemm(tR2, CmOp{gehe, 2 * kL, -kL, kL, true}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
+                      umma_idesc_t(1, 2 * kL, DK, true, true), true);
+            umma_gemm(tS1, CmOp{wst, 2 * kL, 0, 0, false}, CmOp{mt, kL, 0, 0, false}, kL,
+                      umma_idesc_t(1, 2 * kL, kL, false, false), false);
+            umma_commit(bar);
+        }
+        ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
+        ++ph;
+        tc_fence_after();
+        if (!ok) break;
+        // the S0 region (scratch) and, when the next unit needs another [Q; K], its buffer are free
+        if (tid == 0 && u + 1 < u_end) {
+            copy_s(u + 1);
+            if (!same_qk(u, u + 1)) copy_q(u + 1);
+        }
+        {
+            // ---- Z weighted by E(s, t) (s >= t), summed over the rows of both halves: a
+            // transpose reduction over the warp's 32 rows, then the four row quarters
+            const int r = 32 * quarter + lane, s = r & (kL - 1);
+            float z[32];
+            tmem_ld32f(tS1 + lane_off + half * 32, z);
             tmem_wait_ld();
             const float ls = Lm[s];
-            float ge[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const int col = half * 32 + i;
-                const bool keep = upper ? col < s : col <= s;
-                ge[i] = keep ? g2[i] * expf(ls - Lm[col]) : 0.f;
-                wv[i] = g2[i] * a[i];
+                const int t = half * 32 + i;
+                z[i] = s >= t ? z[i] * expf(ls - Lm[t]) : 0.f;
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4 *>(gehe + cm_off(r, 2 * (half * 32 + 8 * j), 2 * kL)) = pack8(ge + 8 * j);
-            if (!upper)
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(wt) + cm_off(s, 4 * (half * 32 + 4 * j), kL)) =
-                        make_float4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+            zq[quarter * kL + half * 32 + lane] = transpose_reduce<32>(z, lane);
         }
-        // ---- R1: a_s = (dY S0)_s . q_s, b_s = (dU S0)_s . k_s; then the rows scaled by exp(Lam_s)
         {
-            constexpr int SC = DK / 2;
-            const float gs = gm[s];
-            float ab = 0.f;
+            // ---- dg_t: the sums over the chunk's steps, a quarter of the steps per thread
+            const int t = tid & (kL - 1), part = tid >> 6;
+            const float lt = Lm[t], lp = LmP[t];
+            float s2 = 0.f, s3 = 0.f;
+            for (int j = 16 * part; j < 16 * part + 16; ++j) {
+                if (j < t) {
+                    s2 = fmaf(expf(lp - Lm[j]), fv[j], s2);
+                } else {
+                    const float ab = abp[j] + abp[2 * kL + j] + abp[kL + j] + abp[3 * kL + j];
+                    s3 = fmaf(expf(lp + Lm[j] - lt), ab, s3);
+                }
+            }
+            dgp[(2 * part + 0) * kL + t] = s2;
+            dgp[(2 * part + 1) * kL + t] = s3;
+        }
+        __syncthreads();
+        if (tid < kL && tid < len) {
+            const int t = tid;
+            float c0 = 0.f;
+            for (int w = 0; w < 8; ++w) c0 += c0p[w];
+            float s2 = 0.f, s3 = 0.f, s4 = 0.f;
+            for (int part = 0; part < 4; ++part) {
+                s2 += dgp[(2 * part + 0) * kL + t];
+                s3 += dgp[(2 * part + 1) * kL + t];
+                s4 += zq[part * kL + t];
+            }
+            const float lt = Lm[t], lp = LmP[t], lL = Lm[kL - 1];
+            const float dgv = expf(lL - lt + lp) * c0 + expf(lL - lt) * s2 + s3 + s4;
+            static_cast<__nv_bfloat16 *>(p.dg)[(rowbase + t) * Hv + h] = __float2bfloat16_rn(dgv);
+        }
+        {
+            // ---- dq (rows 0-63 of R1) and dk (rows 64-127 of R1 plus R2) of this value head, a
+            // row quarter at a time through shared memory to bulk stores, which write HBM while
+            // the next unit computes
+            const int r = 32 * quarter + lane;
+            const bool upper = r >= kL;
             float x[SC];
 #pragma unroll
             for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
-            tmem_wait_ld();
+            if (upper) {
+                float x2[SC];
 #pragma unroll
-            for (int j = 0; j < SC / 8; ++j) {
-                float qv[8];
-                unpack8(*reinterpret_cast<const uint4 *>(qk + cm_off(r, 2 * (half * SC + 8 * j), 2 * kL)), qv);
+                for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR2 + lane_off + half * SC + 32 * j, x2 + 32 * j);
+                tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    ab = fmaf(x[8 * j + i], qv[i], ab);
-                    x[8 * j + i] *= gs;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < SC / 32; ++j) tmem_st32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
-            abp[half * 2 * kL + r] = ab;
-        }
-        // ---- R2: rows scaled by E(L, t)
-        {
-            constexpr int SC = DK / 2;
-            const int m = 16 * quarter + lane;
-            const float sc = lane < 16 ? eL[m] : 1.f;
-            float x[SC];
-#pragma unroll
-            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < SC; ++i) x[i] *= sc;
-#pragma unroll
-            for (int j = 0; j < SC / 32; ++j) tmem_st32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
-        }
-        tmem_wait_st();
-        __syncthreads();
-        if (upper)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float4 *w4 = reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(wt) + cm_off(s, 4 * (half * 32 + 4 * j), kL));
-                float4 w = *w4;
-                w.x += wv[4 * j]; w.y += wv[4 * j + 1]; w.z += wv[4 * j + 2]; w.w += wv[4 * j + 3];
-                *w4 = w;
-            }
-        // M[i, t] = E(t-1, i) for i < t, as the tf32 operand M^T [t][i]
-        for (int e = tid; e < kL * kL / 4; e += 256) {
-            const int t = e & (kL - 1), i0 = 4 * (e >> 6);
-            float m4[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) m4[j] = i0 + j < t ? expf(LmP[t] - Lm[i0 + j]) : 0.f;
-            *reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(mt) + cm_off(t, 4 * i0, kL)) =
-                make_float4(m4[0], m4[1], m4[2], m4[3]);
-        }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // ---- second products: R1 += [GE; HE] K, R2 += GE^T Q + HE^T K, Z = W M (tf32)
-    if (ok && tid == 0) {
-        umma_gemm(tR1, CmOp{gehe, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
-                  umma_idesc_t(1, 2 * kL, DK, false, true), true);
-        umma_gemm(tR2, CmOp{gehe, 2 * kL, 0, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, kL,
-                  umma_idesc_t(1, kL, DK, true, true), true);
-        umma_gemm(tR2, CmOp{gehe, 2 * kL, 0, kL, true}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
-                  umma_idesc_t(1, kL, DK, true, true), true);
-        for (int kk = 0; kk < kL; kk += 8)
-            umma_tf32(tS1, cm_kmajor(wt, kL, 0, 4 * kk), cm_kmajor(mt, kL, 0, 4 * kk), umma_idesc(2, kL, kL), kk > 0);
-        umma_commit(bar);
-    }
-    if (ok) ok = !__syncthreads_or(!mbar_wait(bar, 1));
-    tc_fence_after();
-    if (ok) {
-        const int m = 16 * quarter + lane;
-        // ---- Z weighted by E(s, t) (s >= t) into [64][65]; R2 (the dK part in M = 64 rows) to shared memory
-        {
-            float z[32];
-            tmem_ld16f(tS1 + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(z));
-            tmem_ld16f(tS1 + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(z + 16));
-            tmem_wait_ld();
-            if (lane < 16) {
-                const float ls = Lm[m];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int t = half * 32 + i;
-                    zt[m * kPad + t] = m >= t ? z[i] * expf(ls - Lm[t]) : 0.f;
-                }
-            }
-        }
-        {
-            constexpr int SC = DK / 2;
-            float x[SC];
-#pragma unroll
-            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
-            tmem_wait_ld();
-            if (lane < 16)
-#pragma unroll
-                for (int j = 0; j < SC / 4; ++j)
-                    *reinterpret_cast<float4 *>(dkb + m * DK + swz(m, half * SC + 4 * j)) =
-                        make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-        }
-    }
-    __syncthreads();
-    if (ok) {
-        // ---- dg_t: the three sums over the chunk's steps, a quarter of the steps per thread
-        const int t = tid & (kL - 1), part = tid >> 6;
-        const float lt = Lm[t], lp = LmP[t];
-        float s2 = 0.f, s3 = 0.f, s4 = 0.f;
-        for (int j = 16 * part; j < 16 * part + 16; ++j) {
-            if (j < t) {
-                s2 = fmaf(expf(lp - Lm[j]), fv[j], s2);
+                for (int i = 0; i < SC; ++i) x[i] += x2[i];
             } else {
-                const float ab = abp[j] + abp[2 * kL + j] + abp[kL + j] + abp[3 * kL + j];
-                s3 = fmaf(expf(lp + Lm[j] - lt), ab, s3);
+                tmem_wait_ld();
             }
-            s4 += zt[j * kPad + t];
-        }
-        dgp[(3 * part + 0) * kL + t] = s2;
-        dgp[(3 * part + 1) * kL + t] = s3;
-        dgp[(3 * part + 2) * kL + t] = s4;
-    }
-    __syncthreads();
-    if (ok && tid < kL && tid < len) {
-        const int t = tid;
-        float c0 = 0.f;
-        for (int w = 0; w < 8; ++w) c0 += c0p[w];
-        float s2 = 0.f, s3 = 0.f, s4 = 0.f;
-        for (int part = 0; part < 4; ++part) {
-            s2 += dgp[(3 * part + 0) * kL + t];
-            s3 += dgp[(3 * part + 1) * kL + t];
-            s4 += dgp[(3 * part + 2) * kL + t];
-        }
-        const float lt = Lm[t], lp = LmP[t], lL = Lm[kL - 1];
-        const float dgv = expf(lL - lt + lp) * c0 + expf(lL - lt) * s2 + s3 + s4;
-        static_cast<__nv_bfloat16 *>(p.dg)[(rowbase + t) * Hv + h] = __float2bfloat16_rn(dgv);
-    }
-    if (ok) {
-        // ---- dq and dk of this value head
-        constexpr int SC = DK / 2;
-        const int r = 32 * quarter + lane, s = r & (kL - 1);
-        const bool upper = r >= kL;
-        float *dst = (upper ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + h) * DK + half * SC;
-        float x[SC];
+            // rows pass through a padded shared-memory tile so that each warp store covers 512
+            // contiguous bytes of one row
+            constexpr int RS = DK + 4;                      // padded row stride (floats)
+            for (int q = 0; q < 4; ++q) {
+                if (quarter == q) {
+                    float *row = stg + lane * RS + half * SC;
 #pragma unroll
-        for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
-        tmem_wait_ld();
-        if (upper)
-#pragma unroll
-            for (int j = 0; j < SC / 4; ++j) {
-                const float4 a = *reinterpret_cast<const float4 *>(dkb + s * DK + swz(s, half * SC + 4 * j));
-                x[4 * j] += a.x; x[4 * j + 1] += a.y; x[4 * j + 2] += a.z; x[4 * j + 3] += a.w;
+                    for (int j = 0; j < SC / 4; ++j)
+                        *reinterpret_cast<float4 *>(row + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                }
+                __syncthreads();
+                for (int e = tid; e < 32 * DK / 4; e += 256) {
+                    const int rr = e / (DK / 4), c4 = e - rr * (DK / 4), r2 = 32 * q + rr, s = r2 & (kL - 1);
+                    if (s < len)
+                        *reinterpret_cast<float4 *>((r2 >= kL ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + h) * DK + 4 * c4) =
+                            *reinterpret_cast<const float4 *>(stg + rr * RS + 4 * c4);
+                }
+                __syncthreads();
             }
-        if (s < len)
-#pragma unroll
-            for (int j = 0; j < SC / 4; ++j)
-                *reinterpret_cast<float4 *>(dst + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     }
     if (!ok && tid == 0) {
         report_status(p.status, kStatusTimeout);
-        mbar_wait(cbar, 0);   // the copies land before the CTA exits (bounded)
+        // copies still in flight land before the CTA exits (each wait bounded)
+        if (nA > wA) mbar_wait(cbA, (nA - 1) & 1);
+        if (nS > wS) mbar_wait(cbS, (nS - 1) & 1);
+        if (nQ > wQ) mbar_wait(cbQ, (nQ - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -810,7 +860,14 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, cudaStream_t s) {
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     timing_mark("chunk_grad", 0, s);
-    chunk_grad_kernel<E><<<dim3(p.NC, p.Hv, p.B), 256, sg, s>>>(p);
+    const int units = p.NC * p.Hv * p.B;
+    int dev = 0, sms = 0;
+    err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    const int grid = units < sms ? units : sms;             // persistent: one CTA per SM
+    chunk_grad_kernel<E><<<grid, 256, sg, s>>>(p, units);
     timing_mark("chunk_grad", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;

@@ -300,6 +300,19 @@ __device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, unsig
         : "memory");
 }
 
+// 1-D bulk copy shared -> global (16-byte aligned addresses, size a multiple of 16), in the
+// issuing thread's current bulk async-group.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, unsigned bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk stores have read their shared-memory source (the buffer may be
+// reused), or have completed entirely.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Orders this thread's earlier generic-proxy global writes before later async-proxy
 // (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_global() {
