@@ -22,7 +22,8 @@ namespace gdn {
 namespace {
 
 constexpr int kL = 64;           // chunk length of the tensor-core forward
-constexpr int kPad = kL + 1;     // padded row of the fp32 64 x 64 work matrices
+constexpr int kP = 68;           // row of prep's fp32 64 x 64 work matrices (16-byte aligned, conflict-free float4 columns)
+constexpr int kPad = kL + 1;     // row of the sweep's fp32 64 x 64 tile
 // Both kernels hold all 512 tensor-memory columns, so each must be alone on its SM: they ask
 // for more than half of the shared memory.
 constexpr size_t kOneCtaSmem = 120 * 1024;
@@ -30,25 +31,23 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 __host__ __device__ inline size_t al(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct PrepSmem {
-    size_t kc, qc, kk, qk, am, ts, xs, tcm, bw, bu, vr, kr, lam, bar, tslot, total;
+    size_t kc, qc, kk, qk, am, ts, xs, tcw, tcu, vc, lam, bar, tslot, total;
     __host__ __device__ PrepSmem(int DK, int Dv) {
         size_t o = 0;
         kc = o; o += (size_t)kL * DK * 2;           // K of the chunk, bf16 operand [64][DK]
         qc = o; o += (size_t)kL * DK * 2;           // Q of the chunk
-        kk = o; o += (size_t)kL * kPad * 4;         // K K^T, fp32
-        qk = o; o += (size_t)kL * kPad * 4;         // Q K^T, fp32
-        am = o; o += (size_t)kL * kPad * 4;         // A
-        ts = o; o += (size_t)kL * kPad * 4;         // T = (I + A)^-1
-        xs = o; o += (size_t)3 * 16 * 17 * 4;       // block products of the inversion
-        tcm = o; o += (size_t)kL * kL * 2;          // T, bf16 operand [64][64]
-        bw = o; o += (size_t)DK * kL * 2;           // (diag(beta exp Lam) K)^T, bf16 operand [DK][64]
-        bu = o; o += (size_t)Dv * kL * 2;           // (diag(beta) V)^T, bf16 operand [Dv][64]
-        vr = o; o += (size_t)2 * kL * Dv * 2;       // V of the chunk, row-major bf16, two buffers (heads alternate)
-        kr = o; o += (size_t)kL * DK * 2;           // K of the chunk, row-major bf16
+        kk = o; o += (size_t)kL * kP * 4;           // K K^T, fp32
+        qk = o; o += (size_t)kL * kP * 4;           // Q K^T, fp32
+        am = o; o += (size_t)kL * kP * 4;           // A
+        ts = o; o += (size_t)kL * kP * 4;           // T = (I + A)^-1 (blocks above the diagonal not written)
+        xs = o; o += (size_t)3 * 16 * 16 * 4;       // block products of the inversion
+        tcw = o; o += (size_t)kL * kL * 2;          // T diag(beta exp Lam), bf16 operand [64][64]
+        tcu = o; o += (size_t)kL * kL * 2;          // T diag(beta), bf16 operand [64][64]
+        vc = o; o += (size_t)2 * kL * Dv * 2;       // V of the chunk, bf16 operand [64][Dv], two buffers (heads alternate)
         lam = o; o += 4 * kL * 4;                   // log g, Lam, exp Lam, beta
         bar = al(o, 8); o = bar + 8;
         tslot = o; o += 16;
-        total = o + 1024;
+        total = o + 128;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
     }
 };
@@ -79,16 +78,13 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kPad), by 16 x 16 blocks:
-// the four diagonal blocks by forward substitution (a column per thread), then the blocks
-// below the diagonal, one block diagonal at a time,
-//     T_ij = -T_ii (A_ij T_jj + A_i,j+1 T_j+1,j + ... + A_i,i-1 T_i-1,j).
-// Called by all 256 threads of the CTA.
+// T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kP), by 16 x 16 blocks: the
+// four diagonal blocks by forward substitution (a column per thread), then the blocks below
+// the diagonal, one block diagonal d at a time,
+//     X = A_{j+d,j} T_jj + ... + A_{j+d,j+d-1} T_{j+d-1,j},   T_{j+d,j} = -T_{j+d,j+d} X,
+// each thread four consecutive columns of one row of a block (a scalar and a float4 load per
+// four multiply-adds). Blocks above the diagonal are not written. Called by all 256 threads.
 __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid) {
-    for (int e = tid; e < kL * kL; e += 256) {              // blocks above the diagonal are zero
-        const int t = e >> 6, j = e & (kL - 1);
-        if ((t >> 4) < (j >> 4)) ts[t * kPad + j] = 0.f;
-    }
     if (tid < kL) {
         const int b0 = 16 * (tid >> 4), c = tid & 15;
         float col[16];
@@ -96,31 +92,45 @@ __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid
         for (int r = 0; r < 16; ++r) {
             float x = r == c ? 1.f : 0.f;
 #pragma unroll
-            for (int i = 0; i < r; ++i) x = fmaf(-am[(b0 + r) * kPad + b0 + i], col[i], x);
+            for (int i = 0; i < r; ++i) x = fmaf(-am[(b0 + r) * kP + b0 + i], col[i], x);
             col[r] = r < c ? 0.f : x;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) ts[(b0 + r) * kPad + b0 + c] = col[r];
+        for (int r = 0; r < 16; ++r) ts[(b0 + r) * kP + b0 + c] = col[r];
     }
     __syncthreads();
-    for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d;                               // blocks (j + d, j), j < nb
-        for (int e = tid; e < nb * 256; e += 256) {
-            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i0 = 16 * (j + d);
-            float x = 0.f;
-            for (int kb = j; kb < j + d; ++kb)
+    const int j = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    x = fmaf(am[(i0 + r) * kPad + 16 * kb + i], ts[(16 * kb + i) * kPad + 16 * j + c], x);
-            xs[(j * 16 + r) * 17 + c] = x;
+    for (int d = 1; d < 4; ++d) {
+        const int nb = 4 - d, i0 = 16 * (j + d);
+        if (j < nb) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int kb = 0; kb < d; ++kb)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a = am[(i0 + r) * kP + 16 * (j + kb) + i];
+                    const float4 t4 = *reinterpret_cast<const float4 *>(ts + (16 * (j + kb) + i) * kP + 16 * j + c4);
+                    acc.x = fmaf(a, t4.x, acc.x);
+                    acc.y = fmaf(a, t4.y, acc.y);
+                    acc.z = fmaf(a, t4.z, acc.z);
+                    acc.w = fmaf(a, t4.w, acc.w);
+                }
+            *reinterpret_cast<float4 *>(xs + (j * 16 + r) * 16 + c4) = acc;
         }
         __syncthreads();
-        for (int e = tid; e < nb * 256; e += 256) {
-            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i0 = 16 * (j + d);
-            float x = 0.f;
+        if (j < nb) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x = fmaf(ts[(i0 + r) * kPad + i0 + i], xs[(j * 16 + i) * 17 + c], x);
-            ts[(i0 + r) * kPad + 16 * j + c] = -x;
+            for (int i = 0; i < 16; ++i) {
+                const float a = ts[(i0 + r) * kP + i0 + i];
+                const float4 x4 = *reinterpret_cast<const float4 *>(xs + (j * 16 + i) * 16 + c4);
+                acc.x = fmaf(a, x4.x, acc.x);
+                acc.y = fmaf(a, x4.y, acc.y);
+                acc.z = fmaf(a, x4.z, acc.z);
+                acc.w = fmaf(a, x4.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(ts + (i0 + r) * kP + 16 * j + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
     }
@@ -129,7 +139,8 @@ __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid
 }  // namespace
 
 // One CTA per (chunk, kv head, batch row): K K^T and Q K^T once, then per value head of the
-// kv head the decay-weighted matrices, T, W and U.
+// kv head the decay-weighted matrices, T, W = (T diag(beta exp Lam)) K and U = (T diag(beta)) V
+// (the row scalings folded into T's columns, K and V read as MN-major operands).
 template <int E>
 __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
     constexpr int DK = 32 * E;
@@ -140,11 +151,9 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
     const int t0 = c * kL, len = min(kL, T - t0);
 
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 1024));
+    unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 128));
     const PrepSmem L(DK, Dv);
-    unsigned char *kc = base + L.kc, *qc = base + L.qc, *tcm = base + L.tcm, *bw = base + L.bw, *bu = base + L.bu;
-    __nv_bfloat16 *vr = reinterpret_cast<__nv_bfloat16 *>(base + L.vr);
-    __nv_bfloat16 *kr = reinterpret_cast<__nv_bfloat16 *>(base + L.kr);
+    unsigned char *kc = base + L.kc, *qc = base + L.qc, *tcw = base + L.tcw, *tcu = base + L.tcu, *vc = base + L.vc;
     float *kk = reinterpret_cast<float *>(base + L.kk);
     float *qk = reinterpret_cast<float *>(base + L.qk);
     float *am = reinterpret_cast<float *>(base + L.am);
@@ -187,7 +196,6 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
             if (e < kL * (DK / 8)) {
                 *reinterpret_cast<uint4 *>(kc + cm_off(r, 16 * ch, kL)) = kx[u];
                 *reinterpret_cast<uint4 *>(qc + cm_off(r, 16 * ch, kL)) = qx[u];
-                reinterpret_cast<uint4 *>(kr)[e] = kx[u];   // row-major: e = r * DK / 8 + ch
             }
         }
     }
@@ -198,23 +206,28 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
     const uint32_t tmem = *tslot;
     unsigned phase = 0;
     bool ok = true;
-    if (p.qkm != nullptr) {
-        // [Q; K] in the backward's operand layout (128 rows): 16-byte piece j * 128 + r is
-        // row r of K chunk j, from Q (r < 64) or K
-        uint4 *QKg = reinterpret_cast<uint4 *>(p.qkm + (((size_t)b * p.Hk + hk) * p.NC + c) * 2 * kL * DK);
-        const uint4 *q4 = reinterpret_cast<const uint4 *>(qc), *k4 = reinterpret_cast<const uint4 *>(kc);
-        for (int e = tid; e < 2 * kL * DK / 8; e += 256) {
-            const int j = e >> 7, r = e & 127;
-            QKg[e] = r < kL ? q4[j * kL + r] : k4[j * kL + r - kL];
-        }
-    }
-
     // K K^T -> columns [0, 64), Q K^T -> [64, 128) (M = 64: row m in lane m % 16 + 32 (m / 16))
     if (tid == 0) {
         constexpr uint32_t id = umma_idesc(1, kL, kL);
         umma_gemm_bf16(tmem, kc, kL, 0, kc, kL, 0, DK, id, false);
         umma_gemm_bf16(tmem + kL, qc, kL, 0, kc, kL, 0, DK, id, false);
         umma_commit(bar);
+    }
+    {
+        // while the products run: K (its operand layout, for both sweeps) once per kv head, and
+        // [Q; K] in the gradient kernel's 128-row layout (16-byte piece j * 128 + r is row r of
+        // K chunk j, from Q (r < 64) or K)
+        const size_t ckv = ((size_t)b * p.Hk + hk) * p.NC + c;
+        const uint4 *q4 = reinterpret_cast<const uint4 *>(qc), *k4 = reinterpret_cast<const uint4 *>(kc);
+        uint4 *Kg = reinterpret_cast<uint4 *>(p.ktm + ckv * kL * DK);
+        for (int e = tid; e < kL * DK / 8; e += 256) Kg[e] = k4[e];
+        if (p.qkm != nullptr) {
+            uint4 *QKg = reinterpret_cast<uint4 *>(p.qkm + ckv * 2 * kL * DK);
+            for (int e = tid; e < 2 * kL * DK / 8; e += 256) {
+                const int j = e >> 7, r = e & 127;
+                QKg[e] = r < kL ? q4[j * kL + r] : k4[j * kL + r - kL];
+            }
+        }
     }
     ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
     ++phase;
@@ -224,39 +237,29 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
         const int quarter = warp & 3, row = 16 * quarter + lane;
         float *dst = warp < 4 ? kk : qk;
         const uint32_t col0 = warp < 4 ? 0u : (uint32_t)kL;
+        float x[64];
+        tmem_ld32f(tmem + ((uint32_t)(32 * quarter) << 16) + col0, x);
+        tmem_ld32f(tmem + ((uint32_t)(32 * quarter) << 16) + col0 + 32, x + 32);
+        tmem_wait_ld();
+        if (lane < 16)
 #pragma unroll
-        for (int cc = 0; cc < kL; cc += 16) {
-            float x[16];
-            tmem_ld16f(tmem + ((uint32_t)(32 * quarter) << 16) + col0 + cc, x);
-            tmem_wait_ld();
-            if (lane < 16)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) dst[row * kPad + cc + i] = x[i];
-        }
+            for (int i = 0; i < 64; i += 4)
+                *reinterpret_cast<float4 *>(dst + row * kP + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // K^T of the chunk in its operand layout, once per kv head
-    {
-        unsigned char *Ktg = reinterpret_cast<unsigned char *>(p.ktm + (((size_t)b * p.Hk + hk) * p.NC + c) * kL * DK);
-        for (int e = tid; e < DK * 8; e += 256) {
-            const int ch = e / DK, n = e - ch * DK;
-            float x[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = __bfloat162float(kr[(8 * ch + i) * DK + n]);
-            *reinterpret_cast<uint4 *>(Ktg + cm_off(n, 16 * ch, DK)) = pack8_bf16(x);
-        }
-    }
-    // V of a value head's chunk into buffer `buf` by asynchronous copies (rows past the end: zeros)
+    // V of a value head's chunk into buffer `buf`, in its operand layout, by asynchronous
+    // copies (rows past the end: zeros)
     auto fetch_v = [&](int h, int buf) {
-        const int nv = kL * Dv / 8;
-        uint4 *dst = reinterpret_cast<uint4 *>(vr) + (size_t)buf * nv;
-        for (int e = tid; e < nv; e += 256) {
-            const int r = e / (Dv / 8), ch = e - r * (Dv / 8);
+        const int nv8 = Dv / 8;
+        unsigned char *dst = vc + (size_t)buf * kL * Dv * 2;
+        for (int e = tid; e < kL * nv8; e += 256) {
+            const int r = e / nv8, ch = e - r * nv8;
             const int rr = r < len ? r : 0;
-            cp_async16(dst + e, v + (((size_t)b * T + t0 + rr) * Hv + h) * Dv + 8 * ch, r < len ? 16 : 0);
+            cp_async16(dst + cm_off(r, 16 * ch, kL), v + (((size_t)b * T + t0 + rr) * Hv + h) * Dv + 8 * ch,
+                       r < len ? 16 : 0);
         }
         cp_async_commit();
     };
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
     for (int hh = 0; hh < rep && ok; ++hh) {
         const int h = hk * rep + hh;
         const size_t chk = ((size_t)b * Hv + h) * p.NC + c;   // (b, h, c)
-        __nv_bfloat16 *vrh = vr + (size_t)(hh & 1) * kL * Dv;
+        unsigned char *vch = vc + (size_t)(hh & 1) * kL * Dv * 2;
         // the next head's V goes out now; this head's has landed once the older group is done
         if (hh + 1 < rep) {
             fetch_v(h + 1, (hh + 1) & 1);
@@ -325,9 +328,9 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
             for (int j = 0; j < 8; ++j) {
                 const int i = i0 + j;
                 const float ex = i <= t ? expf(Lm[t] - Lm[i]) : 0.f;
-                const float kkv = kk[t * kPad + i];
-                am[t * kPad + i] = i < t ? bt[t] * kkv * ex : 0.f;
-                pv[j] = qk[t * kPad + i] * ex;
+                const float kkv = kk[t * kP + i];
+                am[t * kP + i] = i < t ? bt[t] * kkv * ex : 0.f;
+                pv[j] = qk[t * kP + i] * ex;
                 kv8[j] = i < t ? kkv * ex : 0.f;
             }
             reinterpret_cast<uint4 *>(P)[e] = pack8_bf16(pv);
@@ -352,48 +355,43 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
         }
         __syncthreads();
         invert_unit_lower(am, ts, xs, tid);
-        // operands: T (A of both products), (diag(beta exp Lam) K)^T and (diag(beta) V)^T,
-        // eight consecutive K elements (16 bytes) per store
-        for (int e = tid; e < kL * 8; e += 256) {
-            const int t = e >> 3, ch = e & 7;
-            float x[8];
+        // T (for the backward), T diag(beta exp Lam) and T diag(beta) as bf16 operands; the
+        // blocks of T above the diagonal are zero
+        {
+            unsigned char *Tg = reinterpret_cast<unsigned char *>(p.tm != nullptr ? p.tm + chk * kL * kL : nullptr);
+            for (int e = tid; e < kL * 8; e += 256) {
+                const int t = e & (kL - 1), ch = e >> 6;
+                float x[8], w8[8], u8[8];
+                if ((8 * ch) >> 4 <= t >> 4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(ts + t * kP + 8 * ch);
+                    const float4 a2 = *reinterpret_cast<const float4 *>(ts + t * kP + 8 * ch + 4);
+                    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = a2.x; x[5] = a2.y; x[6] = a2.z; x[7] = a2.w;
+                } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = ts[t * kPad + 8 * ch + i];
-            *reinterpret_cast<uint4 *>(tcm + cm_off(t, 16 * ch, kL)) = pack8_bf16(x);
-        }
-        for (int e = tid; e < DK * 8; e += 256) {
-            const int ch = e / DK, n = e - ch * DK;   // consecutive threads: consecutive columns
-            float x[8];
+                    for (int i = 0; i < 8; ++i) x[i] = 0.f;
+                }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = 8 * ch + i;
-                x[i] = bt[r] * gm[r] * __bfloat162float(kr[r * DK + n]);
+                for (int i = 0; i < 8; ++i) {
+                    const int col = 8 * ch + i;
+                    u8[i] = x[i] * bt[col];
+                    w8[i] = u8[i] * gm[col];
+                }
+                const uint32_t o = cm_off(t, 16 * ch, kL);
+                *reinterpret_cast<uint4 *>(tcw + o) = pack8_bf16(w8);
+                *reinterpret_cast<uint4 *>(tcu + o) = pack8_bf16(u8);
+                if (Tg != nullptr) *reinterpret_cast<uint4 *>(Tg + o) = pack8_bf16(x);
             }
-            *reinterpret_cast<uint4 *>(bw + cm_off(n, 16 * ch, DK)) = pack8_bf16(x);
-        }
-        for (int e = tid; e < Dv * 8; e += 256) {
-            const int ch = e / Dv, n = e - ch * Dv;
-            float x[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = 8 * ch + i;
-                x[i] = bt[r] * __bfloat162float(vrh[r * Dv + n]);
-            }
-            *reinterpret_cast<uint4 *>(bu + cm_off(n, 16 * ch, Dv)) = pack8_bf16(x);
         }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (p.tm != nullptr) {
-            // T in its operand layout, for the backward
-            uint4 *Tg = reinterpret_cast<uint4 *>(p.tm + chk * kL * kL);
-            for (int e = tid; e < kL * kL / 8; e += 256) Tg[e] = reinterpret_cast<const uint4 *>(tcm)[e];
-        }
         // W -> columns [256, 256 + DK), U -> [0, Dv)
         if (tid == 0) {
-            umma_gemm_bf16(tmem + 256, tcm, kL, 0, bw, DK, 0, kL, umma_idesc(1, kL, DK), false);
-            umma_gemm_bf16(tmem, tcm, kL, 0, bu, Dv, 0, kL, umma_idesc(1, kL, Dv), false);
+            umma_gemm(tmem + 256, CmOp{tcw, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, true}, kL,
+                      umma_idesc_t(1, kL, DK, false, true), false);
+            umma_gemm(tmem, CmOp{tcu, kL, 0, 0, false}, CmOp{vch, kL, 0, 0, true}, kL,
+                      umma_idesc_t(1, kL, Dv, false, true), false);
             umma_commit(bar);
         }
         ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
@@ -403,29 +401,37 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
             const int quarter = warp & 3, row = 16 * quarter + lane;
             const uint32_t lo = (uint32_t)(32 * quarter) << 16;
             if (warp < 4) {
-                unsigned char *W = reinterpret_cast<unsigned char *>(p.wm + chk * kL * DK);   // core-matrix layout
-                for (int cc = 0; cc < DK; cc += 16) {
-                    float x[16];
-                    tmem_ld16f(tmem + lo + 256 + cc, x);
-                    tmem_wait_ld();
-                    if (lane < 16) {
-                        float a[8], bb[8];
+                // W in its operand layout, 96 columns per tensor-memory wait
+                unsigned char *W = reinterpret_cast<unsigned char *>(p.wm + chk * kL * DK);
+                for (int c0 = 0; c0 < DK; c0 += 96) {
+                    const int n = DK - c0 < 96 ? DK - c0 : 96;
+                    float x[96];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) { a[i] = x[i]; bb[i] = x[8 + i]; }
-                        *reinterpret_cast<uint4 *>(W + cm_off(row, 2 * cc, kL)) = pack8_bf16(a);
-                        *reinterpret_cast<uint4 *>(W + cm_off(row, 2 * cc + 16, kL)) = pack8_bf16(bb);
-                    }
-                }
-            } else {
-                float *U = p.um + chk * kL * Dv;
-                for (int cc = 0; cc < Dv; cc += 16) {
-                    float x[16];
-                    tmem_ld16f(tmem + lo + cc, x);
+                    for (int j = 0; j < 3; ++j)
+                        if (32 * j < n) tmem_ld32f(tmem + lo + 256 + c0 + 32 * j, x + 32 * j);
                     tmem_wait_ld();
                     if (lane < 16)
 #pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *reinterpret_cast<float4 *>(U + row * Dv + cc + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+                        for (int j = 0; j < 12; ++j)
+                            if (8 * j < n)
+                                *reinterpret_cast<uint4 *>(W + cm_off(row, 2 * (c0 + 8 * j), kL)) =
+                                    pack8_bf16(*reinterpret_cast<const float (*)[8]>(x + 8 * j));
+                }
+            } else {
+                float *U = p.um + chk * kL * Dv;
+                for (int c0 = 0; c0 < Dv; c0 += 96) {
+                    const int n = Dv - c0 < 96 ? Dv - c0 : 96;
+                    float x[96];
+#pragma unroll
+                    for (int j = 0; j < 3; ++j)
+                        if (32 * j < n) tmem_ld32f(tmem + lo + c0 + 32 * j, x + 32 * j);
+                    tmem_wait_ld();
+                    if (lane < 16)
+#pragma unroll
+                        for (int j = 0; j < 24; ++j)
+                            if (4 * j < n)
+                                *reinterpret_cast<float4 *>(U + row * Dv + c0 + 4 * j) =
+                                    make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
                 }
             }
         }
@@ -434,6 +440,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
         tc_fence_after();
     }
     if (!ok && tid == 0) report_status(p.status, kStatusTimeout);
+    cp_async_wait<0>();   // no copy still writes shared memory when the CTA exits
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -453,7 +460,7 @@ struct SweepSmem {
         wc = o; o += (size_t)kL * DK * 2;     // W of the chunk        A [64][DK]
         qs = o; o += (size_t)kL * DK * 2;     // diag(exp Lam) Q       A [64][DK]
         ks = o; o += (size_t)kL * DK * 2;     // diag(exp Lam) K       A [64][DK]
-        kt = o; o += (size_t)DK * kL * 2;     // K^T                   B [DK][64]
+        kt = o; o += (size_t)kL * DK * 2;     // K (read MN-major)     B [64][DK]
         pc = o; o += (size_t)kL * kL * 2;     // (Q K^T) o E_incl      A [64][64]
         kkc = o; o += (size_t)kL * kL * 2;    // (K K^T) o E_strict    A [64][64]
         sop = o; o += (size_t)kL * DK * 2;    // S (64 value rows)     B [64][DK]
@@ -697,7 +704,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
             umma_gemm_bf16(tY, pc, kL, 0, dt, kL, 0, kL, id64, true);
             umma_gemm_bf16(tU, ks, kL, 0, sop, kL, 0, DK, id64, false);
             umma_gemm_bf16(tU, kkc, kL, 0, dt, kL, 0, kL, id64, true);
-            umma_gemm_bf16(tD, de, kL, 0, kt, DK, 0, kL, umma_idesc(1, kL, DK), false);
+            umma_gemm(tD, CmOp{de, kL, 0, 0, false}, CmOp{kt, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, false, true), false);
             umma_commit(bar);
         }
         load_v(c);                                          // for this chunk's epilogue, one chunk later

@@ -69,7 +69,7 @@ struct DSweepSmem {
     size_t kt, qs, ks, tm, pm, dys, shi, slo, rhs, du, vec, red, bar, tslot, total;
     __host__ __device__ DSweepSmem(int DK) {
         size_t o = 0;
-        kt = o; o += (size_t)DK * kL * 2;    // K^T [DK][64] (read MN-major as K)
+        kt = o; o += (size_t)kL * DK * 2;    // K [64][DK]
         qs = o; o += (size_t)kL * DK * 2;    // diag(exp Lam) Q [64][DK] (read MN-major)
         ks = o; o += (size_t)kL * DK * 2;    // diag(exp Lam) K [64][DK] (read MN-major)
         tm = o; o += (size_t)kL * kL * 2;    // T [64][64] (read MN-major as T^T)
@@ -261,11 +261,11 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
         if (!ok) break;
         // ---- K dS^T (high + low), P^T dY, dS += dY^T diag(exp Lam) Q
         if (tid == 0) {
-            constexpr uint32_t idX = umma_idesc_t(1, kL, kL, true, false);
+            constexpr uint32_t idX = umma_idesc_t(1, kL, kL, false, false);
             constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
             constexpr uint32_t idS = umma_idesc_t(1, kL, DK, true, true);
-            umma_gemm(tX, CmOp{kt, DK, 0, 0, true}, CmOp{shi, kL, 0, 0, false}, DK, idX, false);
-            umma_gemm(tX, CmOp{kt, DK, 0, 0, true}, CmOp{slo, kL, 0, 0, false}, DK, idX, true);
+            umma_gemm(tX, CmOp{kt, kL, 0, 0, false}, CmOp{shi, kL, 0, 0, false}, DK, idX, false);
+            umma_gemm(tX, CmOp{kt, kL, 0, 0, false}, CmOp{slo, kL, 0, 0, false}, DK, idX, true);
             umma_gemm(tP, CmOp{pmm, kL, 0, 0, true}, CmOp{dys, kL, 0, 0, true}, kL, idP, false);
             umma_gemm(tS, CmOp{dys, kL, 0, 0, true}, CmOp{qs, kL, 0, 0, true}, kL, idS, true);
             umma_commit(bar);
