@@ -243,6 +243,27 @@ void release_timed() {
     g_timed.clear();
 }
 
+// 2-D fp32 tensor map [rows][cols] (row-major), box {box_c, box_r}, 128-byte swizzle.
+int make_f32_map_2d(CUtensorMap *map, void *ptr, size_t rows, size_t cols, int box_c, int box_r) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available from the driver");
+        return GDN_ERR_CUDA;
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)box_c, (cuuint32_t)box_r};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 }  // namespace
 
 namespace gdn {
@@ -356,7 +377,10 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.qkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qkm);
         cp.status = fp.status;
         cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
-        return cuda_status(gdn::launch_chunk_fwd(cp, p.Dk, (cudaStream_t)stream));
+        CUtensorMap tm_ck;
+        rc = make_f32_map_2d(&tm_ck, ckpt, (size_t)p.B * p.Hv * p.NC * p.Dv, (size_t)p.Dk, 32, 64);
+        if (rc != GDN_OK) return rc;
+        return cuda_status(gdn::launch_chunk_fwd(cp, tm_ck, p.Dk, (cudaStream_t)stream));
     }
     CUtensorMap tm_q, tm_k;
     if ((rc = make_qk_map(&tm_q, q, p, gdn::kFwdTile)) != GDN_OK) return rc;

@@ -454,7 +454,7 @@ namespace gdn {
 namespace {
 
 struct SweepSmem {
-    size_t wc, qs, ks, kt, pc, kkc, sop, dt, de, dtile, vec, bar, tslot, total;
+    size_t wc, qs, ks, kt, pc, kkc, sop, dt, de, dtile, ckst, vec, bar, tslot, total;
     __host__ __device__ SweepSmem(int DK) {
         size_t o = 0;
         wc = o; o += (size_t)kL * DK * 2;     // W of the chunk        A [64][DK]
@@ -467,6 +467,7 @@ struct SweepSmem {
         dt = o; o += (size_t)kL * kL * 2;     // Delta^T               B [64][64]
         de = o; o += (size_t)kL * kL * 2;     // (diag(E_L) Delta)^T   A [64][64]
         dtile = o; o += (size_t)kL * kPad * 4; // Delta, fp32 [64][65]
+        ckst = al(o, 1024); o = ckst + (size_t)kL * DK * 4;   // chunk-start state, fp32, boxes of [64][32] in the 128-byte swizzle
         vec = o; o += 3 * kL * 4;             // Lam, exp Lam, E(L, .)
         bar = al(o, 8); o = bar + 24;         // MMA completion, the two groups of operand copies
         tslot = o; o += 16;
@@ -485,7 +486,7 @@ struct SweepSmem {
 //   [DK + 128, 2 DK + 128)  the state update (diag(E_L) Delta)^T K, whose first 64 columns
 //                       first hold W S^T (read before the update is issued)
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
+__global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ CUtensorMap tm_ck) {
     constexpr int DK = 32 * E;
     static_assert(2 * DK + 128 <= 512, "tensor memory holds the state, y, u and the update");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -501,6 +502,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
     unsigned char *wc = base + L.wc, *qs = base + L.qs, *ks = base + L.ks, *kt = base + L.kt;
     unsigned char *pc = base + L.pc, *kkc = base + L.kkc, *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
     float *dtile = reinterpret_cast<float *>(base + L.dtile);
+    unsigned char *ckst = base + L.ckst;
     float *Lm = reinterpret_cast<float *>(base + L.vec), *gm = Lm + kL, *eL = gm + kL;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1, *rbar = bar + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
@@ -618,30 +620,31 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
             gm[tid] = expf(lamn);
             if (c + 1 < p.NC) lamn = p.lam[(chk + 1) * kL + tid];
         }
+        if (tid == 0) bulk_wait_read();                     // the previous chunk's stores have read sop and ckst
         __syncthreads();
         if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
-        // ---- the state as an operand, and the chunk-start checkpoint (all of this thread's
-        // columns loaded from tensor memory before one wait)
+        // ---- the state as an operand, and the chunk-start checkpoint staged for TMA stores (all
+        // of this thread's columns loaded from tensor memory before one wait). The stores of the
+        // previous chunk have read both buffers (thread 0 waited before the barrier above).
         {
             float xs[SC];
 #pragma unroll
             for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tS + lane_off + half * SC + 32 * j, xs + 32 * j);
             tmem_wait_ld();
             if (lane < 16) {
-                unsigned char *sg = p.s0m != nullptr
-                    ? reinterpret_cast<unsigned char *>(p.s0m + (chk * gridDim.x + split) * kL * DK) : nullptr;
-                float *ck = p.ckpt != nullptr ? p.ckpt + (chk * Dv + r0 + lrow) * DK + half * SC : nullptr;
 #pragma unroll
                 for (int j = 0; j < SC / 8; ++j) {
-                    const uint4 u = pack8_bf16(*reinterpret_cast<const float (*)[8]>(xs + 8 * j));
                     const uint32_t o = cm_off(lrow, 2 * (half * SC + 8 * j), kL);
-                    *reinterpret_cast<uint4 *>(sop + o) = u;
-                    if (sg != nullptr) *reinterpret_cast<uint4 *>(sg + o) = u;   // the same operand for the backward
+                    *reinterpret_cast<uint4 *>(sop + o) = pack8_bf16(*reinterpret_cast<const float (*)[8]>(xs + 8 * j));
                 }
-                if (ck != nullptr)
+                // box bx holds columns 32 bx .. + 31: row r at r * 128 bytes, its 16-byte chunk q
+                // at chunk q ^ (r % 8) (the 128-byte swizzle)
 #pragma unroll
-                    for (int i = 0; i < SC; i += 4)
-                        *reinterpret_cast<float4 *>(ck + i) = make_float4(xs[i], xs[i + 1], xs[i + 2], xs[i + 3]);
+                for (int j = 0; j < SC / 4; ++j) {
+                    const int col = half * SC + 4 * j, bx = col >> 5, q = (col & 31) >> 2;
+                    *reinterpret_cast<float4 *>(ckst + bx * (kL * 128) + lrow * 128 + ((q ^ (lrow & 7)) << 4)) =
+                        make_float4(xs[4 * j], xs[4 * j + 1], xs[4 * j + 2], xs[4 * j + 3]);
+                }
             }
         }
         fence_proxy_async();
@@ -650,6 +653,14 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbar, cph & 1));
         tc_fence_after();
         if (!ok) break;
+        if (tid == 0) {
+            // the bf16 state (the backward's operand) and the fp32 checkpoint leave by bulk stores
+            if (p.s0m != nullptr) bulk_store(p.s0m + (chk * gridDim.x + split) * kL * DK, sop, kL * DK * 2);
+            if (p.ckpt != nullptr)
+#pragma unroll
+                for (int bx = 0; bx < DK / 32; ++bx) tma_store_2d(&tm_ck, ckst + bx * (kL * 128), 32 * bx, (int)(chk * Dv + r0));
+            bulk_commit();
+        }
         // ---- W S^T
         if (tid == 0) {
             umma_gemm_bf16(tD, wc, kL, 0, sop, kL, 0, DK, umma_idesc(1, kL, kL), false);
@@ -734,6 +745,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p) {
         tc_fence_after();
     }
     if (ok) epilogue(p.NC - 1);
+    if (tid == 0) bulk_wait_all();                          // the state stores are complete
     if (ok && p.S_T != nullptr) {
         for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
             float x[16];
@@ -761,7 +773,7 @@ size_t chunk_prep_smem(int Dk, int Dv) { return PrepSmem(Dk, Dv).total; }
 size_t chunk_sweep_smem(int Dk) { return SweepSmem(Dk).total; }
 
 template <int E>
-static cudaError_t launch_chunk_t(const ChunkParams &p, cudaStream_t s) {
+static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck, cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sp = PrepSmem(DK, p.Dv).total, ss = SweepSmem(DK).total;
     cudaError_t err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
@@ -774,16 +786,16 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, cudaStream_t s) {
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     timing_mark("chunk_sweep", 0, s);
-    chunk_sweep_kernel<E><<<dim3(p.Dv / kL, p.Hv, p.B), 256, ss, s>>>(p);
+    chunk_sweep_kernel<E><<<dim3(p.Dv / kL, p.Hv, p.B), 256, ss, s>>>(p, tm_ck);
     timing_mark("chunk_sweep", 1, s);
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_fwd(const ChunkParams &p, int Dk, cudaStream_t s) {
+cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, int Dk, cudaStream_t s) {
     switch (Dk) {
-        case 64: return launch_chunk_t<2>(p, s);
-        case 128: return launch_chunk_t<4>(p, s);
-        case 192: return launch_chunk_t<6>(p, s);
+        case 64: return launch_chunk_t<2>(p, tm_ck, s);
+        case 128: return launch_chunk_t<4>(p, tm_ck, s);
+        case 192: return launch_chunk_t<6>(p, tm_ck, s);
         default: return cudaErrorInvalidValue;
     }
 }

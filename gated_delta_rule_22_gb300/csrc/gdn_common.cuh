@@ -313,6 +313,15 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// 2-D tiled TMA store of one box from shared memory (the box's layout as the tensor map's
+// swizzle mode describes), in the issuing thread's current bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(smem_addr(src))
+                 : "memory");
+}
+
 // Orders this thread's earlier generic-proxy global writes before later async-proxy
 // (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -399,7 +408,9 @@ size_t bwd_smem_bytes(int Dk, int C, int dtype, int slots);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // Chunkwise forward: Dk in {64, 128, 192}, Dv a multiple of 64 up to 256, bf16, C = 64.
-cudaError_t launch_chunk_fwd(const ChunkParams &p, int Dk, cudaStream_t s);
+// tm_ck: 2-D tensor map of the fp32 checkpoints as [B*Hv*NC*Dv rows][Dk], box {32, 64},
+// 128-byte swizzle (written by TMA stores).
+cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, int Dk, cudaStream_t s);
 size_t chunk_prep_smem(int Dk, int Dv);
 size_t chunk_sweep_smem(int Dk);
 // Chunkwise backward: the reverse sweep over chunks (dS), the per-chunk gradient products
