@@ -69,14 +69,6 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&x)[8]) {
     x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
 }
 
-// 16-byte asynchronous copy global -> shared; the bytes past src_bytes (0 or 16) are zero.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kP), by 16 x 16 blocks: the
 // four diagonal blocks by forward substitution (a column per thread), then the blocks below

@@ -66,7 +66,7 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 
 // ------------------------------------------------------------------ reverse sweep (dS)
 struct DSweepSmem {
-    size_t kt, qs, ks, tm, pm, dys, shi, slo, rhs, du, vec, red, bar, tslot, total;
+    size_t kt, qs, ks, tm, pm, ydu, rsm, lms, shi, slo, rhs, dls, vec, red, bar, tslot, total;
     __host__ __device__ DSweepSmem(int DK) {
         size_t o = 0;
         kt = o; o += (size_t)kL * DK * 2;    // K [64][DK]
@@ -74,11 +74,13 @@ struct DSweepSmem {
         ks = o; o += (size_t)kL * DK * 2;    // diag(exp Lam) K [64][DK] (read MN-major)
         tm = o; o += (size_t)kL * kL * 2;    // T [64][64] (read MN-major as T^T)
         pm = o; o += (size_t)kL * kL * 2;    // P = (Q K^T) o E_incl [64][64] (read MN-major)
-        dys = o; o += (size_t)kL * kL * 2;   // dY block [64 t][64 v]
+        ydu = o; o += (size_t)2 * 2 * kL * kL * 2;   // [dY; dU] block [128][64 v] (rows 0-63 dY, 64-127 dU), two buffers
+        rsm = o; o += (size_t)kL * 68 * 4;       // v - u block [64 t][64 v], fp32, row stride 68
+        lms = o; o += (size_t)2 * kL * 4;        // Lam, two buffers
         shi = o; o += (size_t)kL * DK * 2;   // dS, bf16 high part [64 v][DK]
         slo = o; o += (size_t)kL * DK * 2;   // dS - high part, bf16
         rhs = o; o += (size_t)kL * kL * 2;   // diag(E_L) K dS^T + P^T dY [64 t][64 v]
-        du = o; o += (size_t)kL * kL * 2;    // dU block [64 t][64 v]
+        dls = o; o += (size_t)kL * kL * 2;   // Delta block [64 t][64 v], for the gradient kernel
         vec = o; o += 4 * kL * 4;            // Lam, E(L, .), beta, -
         red = o; o += 2 * 2 * kL * 4;        // [f | dbeta][half][64]
         bar = alb(o, 8); o = bar + 4 * 8;    // MMA, copies of (K^T, P, Qs), of T, of Ks
@@ -111,7 +113,8 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
     unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
     const DSweepSmem L(DK);
     unsigned char *kt = base + L.kt, *qs = base + L.qs, *ks = base + L.ks, *tmm = base + L.tm, *pmm = base + L.pm;
-    unsigned char *dys = base + L.dys, *shi = base + L.shi, *slo = base + L.slo, *rhs = base + L.rhs, *dus = base + L.du;
+    unsigned char *ydu2 = base + L.ydu, *shi = base + L.shi, *slo = base + L.slo, *rhs = base + L.rhs, *dls = base + L.dls;
+    float *rsm = reinterpret_cast<float *>(base + L.rsm), *lms = reinterpret_cast<float *>(base + L.lms);
     float *Lm = reinterpret_cast<float *>(base + L.vec), *eL = Lm + kL, *bt = eL + kL;
     float *red = reinterpret_cast<float *>(base + L.red);   // [2][2][64]
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
@@ -172,52 +175,46 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
     }
     unsigned ph = 0, cph = 0;
     bool ok = true;
-    // a chunk's dY block (two 16-byte pieces per thread), its v - u (this lane's row, 32
-    // columns), Lam and beta (threads < 64): loaded one chunk ahead
-    uint4 yx[2];
-    float rs[32];
-    float lamn = 0.f, btn = 0.f;
-    auto load_chunk = [&](int cc) {
+    // a chunk's dY block (into the dY rows of a [dY; dU] buffer), its v - u and Lam arrive by
+    // asynchronous copies one chunk ahead; beta (threads < 64) by a load one chunk ahead
+    float btn = 0.f;
+    auto fetch_chunk = [&](int cc, int buf) {
         const int tt0 = cc * kL, ln = min(kL, T - tt0);
         const size_t rb = (size_t)b * T + tt0;
+        unsigned char *yb = ydu2 + (size_t)buf * 2 * kL * kL * 2;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const int e = tid + 256 * u, t = e >> 3, j = e & 7;
-            yx[u] = t < ln ? *reinterpret_cast<const uint4 *>(dy + ((rb + t) * Hv + h) * Dv + r0 + 8 * j)
-                           : make_uint4(0u, 0u, 0u, 0u);
+            const int e = tid + 256 * u, t = e >> 3, j = e & 7, tt = t < ln ? t : 0;
+            cp_async16(yb + cm_off(t, 16 * j, 2 * kL), dy + ((rb + tt) * Hv + h) * Dv + r0 + 8 * j, t < ln ? 16 : 0);
         }
-        const bool mine = rowlane && lrow < ln;
-        const float4 *rg = reinterpret_cast<const float4 *>(p.resid + ((rb + (mine ? lrow : 0)) * Hv + h) * Dv + r0 + half * 32);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 f4 = mine ? rg[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-            rs[4 * i] = f4.x; rs[4 * i + 1] = f4.y; rs[4 * i + 2] = f4.z; rs[4 * i + 3] = f4.w;
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + 256 * u, t = e >> 4, j = e & 15, tt = t < ln ? t : 0;
+            cp_async16(rsm + t * 68 + 4 * j, p.resid + ((rb + tt) * Hv + h) * Dv + r0 + 4 * j, t < ln ? 16 : 0);
         }
-        if (tid < kL) {
-            lamn = p.lam[(head * p.NC + cc) * kL + tid];
-            btn = tid < ln ? __bfloat162float(beta[(rb + tid) * Hv + h]) : 0.f;
-        }
+        if (tid < 16) cp_async16(lms + buf * kL + 4 * tid, p.lam + (head * p.NC + cc) * kL + 4 * tid, 16);
+        cp_async_commit();
+        if (tid < kL) btn = tid < ln ? __bfloat162float(beta[(rb + tid) * Hv + h]) : 0.f;
     };
     if (tid == 0) { copy_A(p.NC - 1); copy_T(p.NC - 1); copy_K(p.NC - 1); }
-    load_chunk(p.NC - 1);
+    fetch_chunk(p.NC - 1, 0);
     for (int c = p.NC - 1; c >= 0 && ok; --c) {
         const int t0 = c * kL, len = min(kL, T - t0);
         const size_t chk = head * p.NC + c;
         const size_t rowbase = (size_t)b * T + t0;          // (b, t0) row of [B, T, ...]
-        // ---- this chunk's dY block into its operand layout (and, with dU below, [dY; dU] for
-        // the gradient kernel: value group j at j * 2048, dY rows then dU rows, 16 bytes per row)
-        {
-            unsigned char *gyu = reinterpret_cast<unsigned char *>(p.ws_yu + (chk * nsplit + split) * 2 * kL * kL);
+        const int buf = (p.NC - 1 - c) & 1;
+        unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;   // [dY; dU] of this chunk
+        cp_async_wait<0>();                                 // this chunk's dY, v - u and Lam have landed
+        if (tid < kL) bt[tid] = btn;
+        __syncthreads();
+        if (tid < kL) Lm[tid] = lms[buf * kL + tid];
+        // this lane's v - u (row lrow, 32 value columns)
+        float rs[32];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + 256 * u, t = e >> 3, j = e & 7;
-                *reinterpret_cast<uint4 *>(dys + cm_off(t, 16 * j, kL)) = yx[u];
-                *reinterpret_cast<uint4 *>(gyu + j * 2048 + 16 * t) = yx[u];
-            }
-        }
-        if (tid < kL) {
-            Lm[tid] = lamn;
-            bt[tid] = btn;
+        for (int i = 0; i < 8; ++i) {
+            const float4 f4 = rowlane ? *reinterpret_cast<const float4 *>(rsm + lrow * 68 + half * 32 + 4 * i)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            rs[4 * i] = f4.x; rs[4 * i + 1] = f4.y; rs[4 * i + 2] = f4.z; rs[4 * i + 3] = f4.w;
         }
         __syncthreads();
         if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
@@ -231,7 +228,6 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
             for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tS + lane_off + half * SC + 32 * j, xs + 32 * j);
             tmem_wait_ld();
             if (rowlane) {
-                unsigned char *gdsl = reinterpret_cast<unsigned char *>(p.ws_dsl + (chk * nsplit + split) * kL * DK);
 #pragma unroll
                 for (int j = 0; j < SC / 8; ++j) {
                     float hi[8], lo[8];
@@ -244,7 +240,6 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
                     const uint32_t o = cm_off(lrow, 2 * (half * SC + 8 * j), kL);
                     *reinterpret_cast<uint4 *>(shi + o) = hu;
                     *reinterpret_cast<uint4 *>(slo + o) = pack8(lo);
-                    *reinterpret_cast<uint4 *>(gdsl + o) = hu;
                 }
             }
 #pragma unroll
@@ -257,6 +252,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbA, cph & 1));
         if (!ok) break;
         // ---- K dS^T (high + low), P^T dY, dS += dY^T diag(exp Lam) Q
@@ -266,8 +262,11 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
             constexpr uint32_t idS = umma_idesc_t(1, kL, DK, true, true);
             umma_gemm(tX, CmOp{kt, kL, 0, 0, false}, CmOp{shi, kL, 0, 0, false}, DK, idX, false);
             umma_gemm(tX, CmOp{kt, kL, 0, 0, false}, CmOp{slo, kL, 0, 0, false}, DK, idX, true);
-            umma_gemm(tP, CmOp{pmm, kL, 0, 0, true}, CmOp{dys, kL, 0, 0, true}, kL, idP, false);
-            umma_gemm(tS, CmOp{dys, kL, 0, 0, true}, CmOp{qs, kL, 0, 0, true}, kL, idS, true);
+            umma_gemm(tP, CmOp{pmm, kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false);
+            umma_gemm(tS, CmOp{ydu, 2 * kL, 0, 0, true}, CmOp{qs, kL, 0, 0, true}, kL, idS, true);
+            // dS at the chunk end (its bf16 high part) for the gradient kernel
+            bulk_store(p.ws_dsl + (chk * nsplit + split) * kL * DK, shi, kL * DK * 2);
+            bulk_commit();
             umma_commit(bar);
         }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
@@ -291,7 +290,6 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
                     y2[i] = fmaf(el, x[i], y2[i]);
                 }
                 const float bb = bt[lrow];
-                unsigned char *gdl = reinterpret_cast<unsigned char *>(p.ws_dl + (chk * nsplit + split) * kL * kL);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t o = cm_off(lrow, 2 * (half * 32 + 8 * j), kL);
@@ -299,7 +297,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
                     float dl8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) dl8[i] = bb * rs[8 * j + i];
-                    *reinterpret_cast<uint4 *>(gdl + o) = pack8(dl8);   // Delta for the gradient kernel
+                    *reinterpret_cast<uint4 *>(dls + o) = pack8(dl8);   // Delta for the gradient kernel
                 }
                 red[half * kL + lrow] = bb * fs;
             }
@@ -339,14 +337,9 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
                     dvv[i] = bb * x[i];
                     duu[i] = -dvv[i];
                 }
-                unsigned char *gyu = reinterpret_cast<unsigned char *>(p.ws_yu + (chk * nsplit + split) * 2 * kL * kL);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int grp = half * 4 + j;
-                    const uint4 u = pack8(duu + 8 * j);
-                    *reinterpret_cast<uint4 *>(dus + cm_off(lrow, 16 * grp, kL)) = u;
-                    *reinterpret_cast<uint4 *>(gyu + grp * 2048 + 1024 + 16 * lrow) = u;
-                }
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(ydu + cm_off(kL + lrow, 16 * (half * 4 + j), 2 * kL)) = pack8(duu + 8 * j);
                 if (lrow < len) {
                     uint4 *dvg = reinterpret_cast<uint4 *>(dv + ((rowbase + lrow) * Hv + h) * Dv + r0 + half * 32);
 #pragma unroll
@@ -361,13 +354,17 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
         tc_fence_after();
         if (tid < kL && tid < len)
             p.ws_db[((rowbase + tid) * Hv + h) * nsplit + split] = red[2 * kL + tid] + red[3 * kL + tid];
-        if (c > 0) load_chunk(c - 1);                       // this chunk's are used up
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbK, cph & 1));
         if (!ok) break;
         // ---- dS += dU^T diag(exp Lam) K
         if (tid == 0) {
-            umma_gemm(tS, CmOp{dus, kL, 0, 0, true}, CmOp{ks, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, true, true),
+            umma_gemm(tS, CmOp{ydu, 2 * kL, 0, kL, true}, CmOp{ks, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, true, true),
                       true);
+            // [dY; dU] and Delta of the block for the gradient kernel
+            const size_t blk = chk * nsplit + split;
+            bulk_store(p.ws_yu + blk * 2 * kL * kL, ydu, 2 * kL * kL * 2);
+            bulk_store(p.ws_dl + blk * kL * kL, dls, kL * kL * 2);
+            bulk_commit();
             umma_commit(bar);
         }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
@@ -376,10 +373,13 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
         if (!ok) break;
         if (tid == 0 && c > 0) copy_K(c - 1);
         ++cph;
+        if (tid == 0) bulk_wait_read();                     // the stores have read the block's buffers
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
     }
+    if (tid == 0) bulk_wait_all();                          // the block outputs are complete
+    cp_async_wait<0>();                                     // no copy still writes shared memory
     if (ok && p.dS0 != nullptr) {
         for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
             float x[16];

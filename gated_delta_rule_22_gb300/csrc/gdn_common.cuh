@@ -300,6 +300,15 @@ __device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, unsig
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared; the bytes past src_bytes (0 or 16) are zero.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // 1-D bulk copy shared -> global (16-byte aligned addresses, size a multiple of 16), in the
 // issuing thread's current bulk async-group.
 __device__ __forceinline__ void bulk_store(void *dst, const void *src, unsigned bytes) {
