@@ -46,11 +46,11 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:chunk_ -s 15 -c 5 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("f286727a52b987e7", "chunk_prep"): 59350272 + 284655360,
-    ("f286727a52b987e7", "chunk_sweep"): 336266240 + 353604608,
-    ("f286727a52b987e7", "chunk_dsweep"): 286054400 + 196773120,
-    ("f286727a52b987e7", "chunk_grad"): 329587456 + 158589184,
-    ("f286727a52b987e7", "chunk_reduce"): 202411520 + 13944320,
+    ("06d41ac009d06140", "chunk_prep"): 59418112 + 246302976,
+    ("06d41ac009d06140", "chunk_sweep"): 298400256 + 352946944,
+    ("06d41ac009d06140", "chunk_dsweep"): 248325632 + 192136192,
+    ("06d41ac009d06140", "chunk_grad"): 335119616 + 153087488,
+    ("06d41ac009d06140", "chunk_reduce"): 202403072 + 14012416,
 }
 
 
