@@ -56,6 +56,31 @@ def test_exports_every_header_function(lib):
     assert lib.gdn_version() == 1
 
 
+def test_buffer_sizes_follow_the_plan(lib):
+    """bf16 with chunk 64 and a supported Dk, Dv: the chunkwise form's saved buffer (larger than
+    states + residuals) and workspace (per value head dq, dk: no row-split factor). When the
+    chunked backward does not fit shared memory (Dk 128, Dv 256) the workspace is the
+    sequential backward's (row-split partials), while the saved buffer stays chunkwise."""
+    def sizes(**kw):
+        s = shape(dtype=1, chunk=64, **kw)
+        return lib.gdn_ckpt_bytes(ctypes.byref(s)), lib.gdn_bwd_workspace_bytes(ctypes.byref(s))
+    for Dk, Dv, chunked_bwd in ((128, 128, True), (192, 128, True), (64, 64, True), (128, 256, False)):
+        T, Hv = 150, 2
+        ck, ws = sizes(T=T, Hk=1, Hv=Hv, Dk=Dk, Dv=Dv)
+        NC = -(-T // 64)
+        states, resid = Hv * NC * Dv * Dk * 4, T * Hv * Dv * 4
+        assert ck > states + resid + 256, (Dk, Dv)
+        per_head = 2 * T * Hv * Dk * 4
+        row_split = 2 * T * Hv * (Dv // 64) * Dk * 4
+        if chunked_bwd:
+            assert per_head <= ws < per_head + row_split // 2 + (8 << 20), (Dk, Dv, ws)
+        else:
+            assert ws >= row_split, (Dk, Dv, ws)
+    # fp32 or another chunk size: the sequential layout, states + residuals exactly
+    s = shape(dtype=1, chunk=32, T=150, Hk=1, Hv=2, Dk=128, Dv=128)
+    assert lib.gdn_ckpt_bytes(ctypes.byref(s)) == (2 * 5 * 128 * 128 * 4 + 255) // 256 * 256 + 150 * 2 * 128 * 4
+
+
 def test_checkpoint_bytes(lib):
     for T, C in ((16, 0), (37, 16), (1, 1), (128, 128), (2048, 64)):
         s = shape(T=T, chunk=C, Hv=6, Hk=3, Dk=96, Dv=20)

@@ -31,6 +31,12 @@ CASES = [
     gs.Workload("tc-Dk128-Dv192-gqa3", 1, 200, 2, 6, 128, 192, "bf16", "weak", True, True, 64),
     gs.Workload("tc-Dk192-Dv64-half", 2, 64, 1, 2, 192, 64, "bf16", "half", False, True, 64),
     gs.Workload("tc-Dk192-short", 1, 5, 1, 2, 192, 128, "bf16", "weak", True, False, 64),
+    # three batch rows with a ragged last chunk each and no GQA: the persistent gradient
+    # kernel's unit ranges cross batch rows and kv heads
+    gs.Workload("tc-B3-ragged-noGQA", 3, 190, 3, 3, 128, 128, "bf16", "strong", True, True, 64),
+    # the chunked backward does not fit shared memory here: the sequential backward consumes
+    # the chunkwise forward's saved buffer
+    gs.Workload("tc-fwd-seq-bwd-Dv256", 1, 150, 1, 2, 128, 256, "bf16", "half", True, True, 64),
 ]
 
 
