@@ -169,6 +169,33 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, 512);
+    // V of a value head's chunk into buffer `buf`, in its operand layout, by asynchronous
+    // copies (rows past the end: zeros)
+    auto fetch_v = [&](int h, int buf) {
+        const int nv8 = Dv / 8;
+        unsigned char *dst = vc + (size_t)buf * kL * Dv * 2;
+        for (int e = tid; e < kL * nv8; e += 256) {
+            const int r = e / nv8, ch = e - r * nv8;
+            const int rr = r < len ? r : 0;
+            cp_async16(dst + cm_off(r, 16 * ch, kL), v + (((size_t)b * T + t0 + rr) * Hv + h) * Dv + 8 * ch,
+                       r < len ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    // log g and beta of a value head (warp 0, two steps per lane), raw
+    __nv_bfloat16 graw[2], braw[2];
+    auto fetch_gb = [&](int h) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int t = 2 * lane + u;
+            const size_t o = ((size_t)b * T + t0 + (t < len ? t : 0)) * Hv + h;
+            graw[u] = g[o];
+            braw[u] = beta[o];
+        }
+    };
+    // the first value head's V, g and beta go out before anything else
+    fetch_v(hk * rep, 0);
+    if (warp == 0) fetch_gb(hk * rep);
     {
         // K and Q of the chunk (rows past the end are zero): all loads, then the stores
         uint4 kx[NKQ], qx[NKQ];
@@ -242,32 +269,6 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
     __syncthreads();
     tc_fence_after();
 
-    // V of a value head's chunk into buffer `buf`, in its operand layout, by asynchronous
-    // copies (rows past the end: zeros)
-    auto fetch_v = [&](int h, int buf) {
-        const int nv8 = Dv / 8;
-        unsigned char *dst = vc + (size_t)buf * kL * Dv * 2;
-        for (int e = tid; e < kL * nv8; e += 256) {
-            const int r = e / nv8, ch = e - r * nv8;
-            const int rr = r < len ? r : 0;
-            cp_async16(dst + cm_off(r, 16 * ch, kL), v + (((size_t)b * T + t0 + rr) * Hv + h) * Dv + 8 * ch,
-                       r < len ? 16 : 0);
-        }
-        cp_async_commit();
-    };
-    // log g and beta of a value head (warp 0, two steps per lane), raw
-    __nv_bfloat16 graw[2], braw[2];
-    auto fetch_gb = [&](int h) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int t = 2 * lane + u;
-            const size_t o = ((size_t)b * T + t0 + (t < len ? t : 0)) * Hv + h;
-            graw[u] = g[o];
-            braw[u] = beta[o];
-        }
-    };
-    fetch_v(hk * rep, 0);
-    if (warp == 0) fetch_gb(hk * rep);
 
     for (int hh = 0; hh < rep && ok; ++hh) {
         const int h = hk * rep + hh;
@@ -315,16 +316,22 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
         __nv_bfloat16 *KKm = p.kkm + chk * kL * kL;
         for (int e = tid; e < kL * 8; e += 256) {
             const int t = e & (kL - 1), i0 = 8 * (e >> 6);
-            float pv[8], kv8[8];
+            float kk8[8], qk8[8], a8[8], pv[8], kv8[8];
+            *reinterpret_cast<float4 *>(kk8) = *reinterpret_cast<const float4 *>(kk + t * kP + i0);
+            *reinterpret_cast<float4 *>(kk8 + 4) = *reinterpret_cast<const float4 *>(kk + t * kP + i0 + 4);
+            *reinterpret_cast<float4 *>(qk8) = *reinterpret_cast<const float4 *>(qk + t * kP + i0);
+            *reinterpret_cast<float4 *>(qk8 + 4) = *reinterpret_cast<const float4 *>(qk + t * kP + i0 + 4);
+            const float lt = Lm[t], bb = bt[t];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = i0 + j;
-                const float ex = i <= t ? expf(Lm[t] - Lm[i]) : 0.f;
-                const float kkv = kk[t * kP + i];
-                am[t * kP + i] = i < t ? bt[t] * kkv * ex : 0.f;
-                pv[j] = qk[t * kP + i] * ex;
-                kv8[j] = i < t ? kkv * ex : 0.f;
+                const float ex = i <= t ? expf(lt - Lm[i]) : 0.f;
+                a8[j] = i < t ? bb * kk8[j] * ex : 0.f;
+                pv[j] = qk8[j] * ex;
+                kv8[j] = i < t ? kk8[j] * ex : 0.f;
             }
+            *reinterpret_cast<float4 *>(am + t * kP + i0) = *reinterpret_cast<const float4 *>(a8);
+            *reinterpret_cast<float4 *>(am + t * kP + i0 + 4) = *reinterpret_cast<const float4 *>(a8 + 4);
             reinterpret_cast<uint4 *>(P)[e] = pack8_bf16(pv);
             reinterpret_cast<uint4 *>(KKm)[e] = pack8_bf16(kv8);
         }
@@ -410,6 +417,8 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
                                     pack8_bf16(*reinterpret_cast<const float (*)[8]>(x + 8 * j));
                 }
             } else {
+                // U in blocks of 32 columns, [Dv / 32][64][32]: a lane's 32 columns of a row are
+                // 128 contiguous bytes, and consecutive rows follow each other
                 float *U = p.um + chk * kL * Dv;
                 for (int c0 = 0; c0 < Dv; c0 += 96) {
                     const int n = Dv - c0 < 96 ? Dv - c0 : 96;
@@ -421,9 +430,11 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
                     if (lane < 16)
 #pragma unroll
                         for (int j = 0; j < 24; ++j)
-                            if (4 * j < n)
-                                *reinterpret_cast<float4 *>(U + row * Dv + c0 + 4 * j) =
+                            if (4 * j < n) {
+                                const int col = c0 + 4 * j;
+                                *reinterpret_cast<float4 *>(U + ((col >> 5) * kL + row) * 32 + (col & 31)) =
                                     make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                            }
                 }
             }
         }
@@ -555,7 +566,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     uint4 vx[4];         // v of the chunk whose epilogue is pending
     float lamn = 0.f;    // Lam of the next chunk (threads < 64)
     auto load_u = [&](int cc) {
-        const float *Ug = p.um + (head * p.NC + cc) * kL * Dv + (size_t)lrow * Dv + r0 + half * 32;
+        const float *Ug = p.um + (head * p.NC + cc) * kL * Dv + ((size_t)((r0 + half * 32) >> 5) * kL + lrow) * 32;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             ux[i] = lane < 16 ? reinterpret_cast<const float4 *>(Ug)[i] : make_float4(0.f, 0.f, 0.f, 0.f);

@@ -72,7 +72,8 @@ static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <=
               "register split exceeds the launch's registers");
 
 // Chunkwise tensor-core forward (bf16 inputs, chunks of 64 steps). Per (b, h, chunk), in the
-// saved buffer: lam, the in-chunk log-decay prefix [64]; um, U [64][Dv] fp32; and the sweep's
+// saved buffer: lam, the in-chunk log-decay prefix [64]; um, U fp32 in column blocks
+// [Dv / 32][64][32]; and the sweep's
 // tensor-core operands, bf16 in their shared-memory (core-matrix) layout: wm W [64][Dk],
 // qsm diag(exp Lam) Q [64][Dk], ksm diag(exp Lam) K [64][Dk], ktm K [64][Dk] (per kv head),
 // pm (Q K^T) o E_incl [64][64], kkm (K K^T) o E_strict [64][64], tm T = (I + A)^-1 [64][64];
