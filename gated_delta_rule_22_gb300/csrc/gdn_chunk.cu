@@ -483,15 +483,16 @@ struct SweepSmem {
 
 // One CTA per (64-row block of the state, value head, batch row), carrying that block of the
 // state through the chunks. Tensor memory (fp32 accumulators, M = 64 layout):
-//   [0, DK)             the state S (value row r in lane r % 16 + 32 (r / 16))
+//   [0, DK)             the state S (value row r in lane r % 16 + 32 (r / 16)); per chunk it is
+//                       scaled by exp(Lam_L) in place and the update (diag(E_L) Delta)^T K is
+//                       accumulated onto it by MMA
 //   [DK, DK + 64)       y of the chunk (chunk row t in the lane of t)
 //   [DK + 64, DK + 128) the prediction u of the chunk
-//   [DK + 128, 2 DK + 128)  the state update (diag(E_L) Delta)^T K, whose first 64 columns
-//                       first hold W S^T (read before the update is issued)
+//   [DK + 128, DK + 192) W S^T
 template <int E>
 __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ CUtensorMap tm_ck) {
     constexpr int DK = 32 * E;
-    static_assert(2 * DK + 128 <= 512, "tensor memory holds the state, y, u and the update");
+    static_assert(DK + 192 <= 512, "tensor memory holds the state, y, u and W S^T");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, r0 = split * kL;
@@ -649,6 +650,14 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
                         make_float4(xs[4 * j], xs[4 * j + 1], xs[4 * j + 2], xs[4 * j + 3]);
                 }
             }
+            // S <- exp(Lam_L) S in place: the chunk's update (diag(E_L) Delta)^T K is accumulated
+            // onto it by the second group of products
+            const float decay = gm[kL - 1];
+#pragma unroll
+            for (int i = 0; i < SC; ++i) xs[i] *= decay;
+#pragma unroll
+            for (int j = 0; j < SC / 32; ++j) tmem_st32f(tS + lane_off + half * SC + 32 * j, xs + 32 * j);
+            tmem_wait_st();
         }
         fence_proxy_async();
         tc_fence_before();
@@ -718,7 +727,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
             umma_gemm_bf16(tY, pc, kL, 0, dt, kL, 0, kL, id64, true);
             umma_gemm_bf16(tU, ks, kL, 0, sop, kL, 0, DK, id64, false);
             umma_gemm_bf16(tU, kkc, kL, 0, dt, kL, 0, kL, id64, true);
-            umma_gemm(tD, CmOp{de, kL, 0, 0, false}, CmOp{kt, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, false, true), false);
+            umma_gemm(tS, CmOp{de, kL, 0, 0, false}, CmOp{kt, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, false, true), true);
             umma_commit(bar);
         }
         load_v(c);                                          // for this chunk's epilogue, one chunk later
@@ -728,21 +737,6 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         if (!ok) break;
         // the other operand buffers are free again: bring in the next chunk's
         if (tid == 0 && c + 1 < p.NC) issue_r(c + 1);
-        // ---- the state after the chunk, 32 columns at a time
-        {
-            const float decay = gm[kL - 1];
-#pragma unroll
-            for (int j = 0; j < SC / 32; ++j) {
-                float s2[32], d[32];
-                tmem_ld32f(tS + lane_off + half * SC + 32 * j, s2);
-                tmem_ld32f(tD + lane_off + half * SC + 32 * j, d);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s2[i] = fmaf(decay, s2[i], d[i]);
-                tmem_st32f(tS + lane_off + half * SC + 32 * j, s2);
-            }
-            tmem_wait_st();
-        }
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
