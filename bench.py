@@ -150,6 +150,26 @@ def kernel_roofline(name, ms, model, peaks):
             "frac": achieved / peak, "ms_per_launch": ms, "roofline_ms": t_min * 1e3, "per_launch": amount}
 
 
+# ------------------------------------------------------------------ multi-rank helpers
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of `values` (floats) over all ranks of the default process group
+    (any backend: NCCL with a CUDA device, gloo with the CPU); the values themselves when
+    world == 1. The slowest rank sets every timing of a weak-scaling run."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    m = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    return [float(x) for x in m.tolist()]
+
+
+def job_throughput(tokens_per_rank, world, ms_per_step):
+    """Whole-job tokens/s of a weak-scaling run: every rank processes its own full workload
+    (independent (batch row, kv head) groups, no data exchange) in the slowest rank's time."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
@@ -327,10 +347,7 @@ def run_ours(args, w):
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     step_ms = fwd_ms + bwd_ms
-    if world > 1:
-        m = torch.tensor([step_ms, fwd_ms, bwd_ms], device=dev)
-        dist.all_reduce(m, op=dist.ReduceOp.MAX)
-        step_ms, fwd_ms, bwd_ms = (float(x) for x in m.tolist())
+    step_ms, fwd_ms, bwd_ms = max_over_ranks([step_ms, fwd_ms, bwd_ms], dev, world)
     clocks = clk.summary()
 
     # per-kernel device times: the same steps again with the library's event timing on
@@ -407,13 +424,10 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     e2e_ms = run_e2e(K, True)
     e2e_serial_ms = run_e2e(K, False)
-    if world > 1:
-        m = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
-        dist.all_reduce(m, op=dist.ReduceOp.MAX)
-        e2e_ms, e2e_serial_ms = (float(x) for x in m.tolist())
+    e2e_ms, e2e_serial_ms = max_over_ranks([e2e_ms, e2e_serial_ms], dev, world)
 
     tokens = w.B * w.T * world
-    value = tokens / (step_ms * 1e-3)
+    value = job_throughput(w.B * w.T, world, step_ms)
     peaks = load_peaks()
     hbm_gbs = peaks["hbm_gbs"]
     f28, f22 = flops_per_step(w, 28), flops_per_step(w, 22)
@@ -458,12 +472,12 @@ def run_ours(args, w):
             "note": "max(algorithmic bytes / HBM, issued MMA flops / bf16 sustained peak) of the chunkwise form",
         } if mma > 0 else None,
         "kernels": kernels,
-        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(w.B * w.T, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "mode": "each step uploads its inputs from pinned host memory and downloads all results; "
                         "uploads and downloads on a second stream with two buffer sets overlap the kernels "
                         "of the neighbouring steps",
-                "serial": {"value": tokens / (e2e_serial_ms * 1e-3), "ms_per_step": e2e_serial_ms,
+                "serial": {"value": job_throughput(w.B * w.T, world, e2e_serial_ms), "ms_per_step": e2e_serial_ms,
                            "mode": "one stream: upload, kernels, download in sequence"}},
         "gpu_launches": int(round(launches_per_step * K)),
         "clocks": clocks,
