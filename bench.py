@@ -370,11 +370,13 @@ def run_ours(args, w):
     def run_e2e(K, pipelined):
         """K steps; each copies its inputs from pinned host memory to the device, runs gdn_fwd
         and gdn_bwd, and copies every result back to pinned host memory. Serial: one stream.
-        Pipelined: the copies run on a second stream with two sets of device buffers, so that
-        step i+1's upload and step i-1's download overlap step i's kernels."""
+        Pipelined: uploads and downloads run on two more streams with two sets of device
+        buffers, so that step i+1's upload and step i's download overlap each other and the
+        neighbouring steps' kernels."""
         nslot = 2 if pipelined else 1
         comp = torch.cuda.current_stream()
-        copy = torch.cuda.Stream() if pipelined else comp
+        copy = torch.cuda.Stream() if pipelined else comp        # uploads
+        down = torch.cuda.Stream() if pipelined else comp        # downloads (the other direction of the link)
         slots = []
         for _ in range(nslot):
             d_in = {n: torch.empty(host_in[n].shape, dtype=dt, device=dev) for n in names}
@@ -409,11 +411,12 @@ def run_ours(args, w):
             sl["done"].record(comp)
             if i + 1 < K:
                 upload(i + 1)
-            with torch.cuda.stream(copy):
-                copy.wait_event(sl["done"])
+            with torch.cuda.stream(down):
+                down.wait_event(sl["done"])
                 for n in o:
                     sl["h_out"][n].copy_(o[n], non_blocking=True)
-                sl["down"].record(copy)
+                sl["down"].record(down)
+        copy.wait_stream(down)
         end.record(copy)
         torch.cuda.synchronize()
         return start.elapsed_time(end) / K
@@ -475,8 +478,8 @@ def run_ours(args, w):
         "e2e": {"value": job_throughput(w.B * w.T, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "mode": "each step uploads its inputs from pinned host memory and downloads all results; "
-                        "uploads and downloads on a second stream with two buffer sets overlap the kernels "
-                        "of the neighbouring steps",
+                        "uploads and downloads on two more streams with two buffer sets overlap the kernels "
+                        "of the neighbouring steps and each other",
                 "serial": {"value": job_throughput(w.B * w.T, world, e2e_serial_ms), "ms_per_step": e2e_serial_ms,
                            "mode": "one stream: upload, kernels, download in sequence"}},
         "gpu_launches": int(round(launches_per_step * K)),
