@@ -46,11 +46,11 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:chunk_ -s 15 -c 5 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("06d41ac009d06140", "chunk_prep"): 59418112 + 246302976,
-    ("06d41ac009d06140", "chunk_sweep"): 298400256 + 352946944,
-    ("06d41ac009d06140", "chunk_dsweep"): 248325632 + 192136192,
-    ("06d41ac009d06140", "chunk_grad"): 335119616 + 153087488,
-    ("06d41ac009d06140", "chunk_reduce"): 202403072 + 14012416,
+    ("502483ca0f0adcc3", "chunk_prep"): 59356672 + 246289152,
+    ("502483ca0f0adcc3", "chunk_sweep"): 298427136 + 352934400,
+    ("502483ca0f0adcc3", "chunk_dsweep"): 248486656 + 192163072,
+    ("502483ca0f0adcc3", "chunk_grad"): 334970112 + 153178880,
+    ("502483ca0f0adcc3", "chunk_reduce"): 202402816 + 14045184,
 }
 
 
