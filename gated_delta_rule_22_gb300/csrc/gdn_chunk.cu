@@ -40,7 +40,7 @@ struct PrepSmem {
         qk = o; o += (size_t)kL * kP * 4;           // Q K^T, fp32
         am = o; o += (size_t)kL * kP * 4;           // A
         ts = o; o += (size_t)kL * kP * 4;           // T = (I + A)^-1 (blocks above the diagonal not written)
-        xs = o; o += (size_t)3 * 16 * 16 * 4;       // block products of the inversion
+        xs = o; o += (size_t)32 * 32 * 4;           // block products of the inversion
         tcw = o; o += (size_t)kL * kL * 2;          // T diag(beta exp Lam), bf16 operand [64][64]
         tcu = o; o += (size_t)kL * kL * 2;          // T diag(beta), bf16 operand [64][64]
         vc = o; o += (size_t)2 * kL * Dv * 2;       // V of the chunk, bf16 operand [64][Dv], two buffers (heads alternate)
@@ -70,12 +70,13 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&x)[8]) {
 }
 
 
-// T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kP), by 16 x 16 blocks: the
-// four diagonal blocks by forward substitution (a column per thread), then the blocks below
-// the diagonal, one block diagonal d at a time,
-//     X = A_{j+d,j} T_jj + ... + A_{j+d,j+d-1} T_{j+d-1,j},   T_{j+d,j} = -T_{j+d,j+d} X,
-// each thread four consecutive columns of one row of a block (a scalar and a float4 load per
-// four multiply-adds). Blocks above the diagonal are not written. Called by all 256 threads.
+// T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kP), in two levels of 2 x 2
+// block recursion: the four diagonal 16 x 16 blocks by forward substitution (a column per
+// thread); then the two 32 x 32 diagonal blocks, and then the 64 x 64, each by
+//     T_21 = -T_22 (A_21 T_11)
+// as two dependent products with four consecutive columns of one row per thread (a scalar
+// and a float4 load per four multiply-adds). Blocks of T above the diagonal are not written,
+// and the products skip them. Called by all 256 threads; xs holds 32 x 32 floats.
 __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid) {
     if (tid < kL) {
         const int b0 = 16 * (tid >> 4), c = tid & 15;
@@ -91,39 +92,57 @@ __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid
         for (int r = 0; r < 16; ++r) ts[(b0 + r) * kP + b0 + c] = col[r];
     }
     __syncthreads();
-    const int j = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
-#pragma unroll
-    for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d, i0 = 16 * (j + d);
-        if (j < nb) {
+    // ---- level 1: the 32 x 32 diagonal blocks b = 0, 1 (threads 0-127)
+    {
+        const int b = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3), o = 32 * b;
+        if (tid < 128) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int kb = 0; kb < d; ++kb)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float a = am[(i0 + r) * kP + 16 * (j + kb) + i];
-                    const float4 t4 = *reinterpret_cast<const float4 *>(ts + (16 * (j + kb) + i) * kP + 16 * j + c4);
-                    acc.x = fmaf(a, t4.x, acc.x);
-                    acc.y = fmaf(a, t4.y, acc.y);
-                    acc.z = fmaf(a, t4.z, acc.z);
-                    acc.w = fmaf(a, t4.w, acc.w);
-                }
-            *reinterpret_cast<float4 *>(xs + (j * 16 + r) * 16 + c4) = acc;
+            for (int k = 0; k < 16; ++k) {
+                const float a = am[(o + 16 + r) * kP + o + k];
+                const float4 t4 = *reinterpret_cast<const float4 *>(ts + (o + k) * kP + o + c4);
+                acc.x = fmaf(a, t4.x, acc.x); acc.y = fmaf(a, t4.y, acc.y);
+                acc.z = fmaf(a, t4.z, acc.z); acc.w = fmaf(a, t4.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(xs + (b * 16 + r) * 16 + c4) = acc;
         }
         __syncthreads();
-        if (j < nb) {
+        if (tid < 128) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float a = ts[(i0 + r) * kP + i0 + i];
-                const float4 x4 = *reinterpret_cast<const float4 *>(xs + (j * 16 + i) * 16 + c4);
-                acc.x = fmaf(a, x4.x, acc.x);
-                acc.y = fmaf(a, x4.y, acc.y);
-                acc.z = fmaf(a, x4.z, acc.z);
-                acc.w = fmaf(a, x4.w, acc.w);
+            for (int k = 0; k < 16; ++k) {
+                const float a = ts[(o + 16 + r) * kP + o + 16 + k];
+                const float4 x4 = *reinterpret_cast<const float4 *>(xs + (b * 16 + k) * 16 + c4);
+                acc.x = fmaf(a, x4.x, acc.x); acc.y = fmaf(a, x4.y, acc.y);
+                acc.z = fmaf(a, x4.z, acc.z); acc.w = fmaf(a, x4.w, acc.w);
             }
-            *reinterpret_cast<float4 *>(ts + (i0 + r) * kP + 16 * j + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            *reinterpret_cast<float4 *>(ts + (o + 16 + r) * kP + o + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
+        __syncthreads();
+    }
+    // ---- level 2: rows 32-63, columns 0-31 (all threads: row r, columns c4 .. c4 + 3)
+    {
+        const int r = tid >> 3, c4 = 4 * (tid & 7);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // X = A_21 T_11: T_11[k][c] = 0 for k in a 16-block above c's
+        for (int k = 16 * (c4 >> 4); k < 32; ++k) {
+            const float a = am[(32 + r) * kP + k];
+            const float4 t4 = *reinterpret_cast<const float4 *>(ts + k * kP + c4);
+            acc.x = fmaf(a, t4.x, acc.x); acc.y = fmaf(a, t4.y, acc.y);
+            acc.z = fmaf(a, t4.z, acc.z); acc.w = fmaf(a, t4.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(xs + r * 32 + c4) = acc;
+        __syncthreads();
+        // T_21 = -T_22 X: T_22[r][k] = 0 for k in a 16-block right of r's
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int kend = 16 * ((r >> 4) + 1);
+        for (int k = 0; k < kend; ++k) {
+            const float a = ts[(32 + r) * kP + 32 + k];
+            const float4 x4 = *reinterpret_cast<const float4 *>(xs + k * 32 + c4);
+            acc.x = fmaf(a, x4.x, acc.x); acc.y = fmaf(a, x4.y, acc.y);
+            acc.z = fmaf(a, x4.z, acc.z); acc.w = fmaf(a, x4.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(ts + (32 + r) * kP + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         __syncthreads();
     }
 }
