@@ -149,17 +149,20 @@ __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid
 
 }  // namespace
 
-// One CTA per (chunk, kv head, batch row): K K^T and Q K^T once, then per value head of the
-// kv head the decay-weighted matrices, T, W = (T diag(beta exp Lam)) K and U = (T diag(beta)) V
-// (the row scalings folded into T's columns, K and V read as MN-major operands).
+// Persistent: one CTA per SM over a contiguous range of units (batch row, chunk, kv head,
+// value head), value head fastest. When a unit starts a new (batch row, chunk, kv head) group
+// the CTA stages K and Q and forms K K^T and Q K^T; per unit (value head) it forms the
+// decay-weighted matrices, T, W = (T diag(beta exp Lam)) K and U = (T diag(beta)) V (the row
+// scalings folded into T's columns, K and V read as MN-major operands). The next unit's V, g
+// and beta are fetched while the current one computes.
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
+__global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int units) {
     constexpr int DK = 32 * E;
     constexpr int NKQ = (kL * DK / 8 + 255) / 256;   // 16-byte pieces of K (or Q) per thread
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, Dv = p.Dv, Hv = p.Hv, rep = p.Hv / p.Hk;
-    const int t0 = c * kL, len = min(kL, T - t0);
+    const int T = p.T, Dv = p.Dv, Hv = p.Hv, Hk = p.Hk, NC = p.NC, rep = p.Hv / p.Hk;
+    const int u_begin = (int)((long long)blockIdx.x * units / gridDim.x);
+    const int u_end = (int)((long long)(blockIdx.x + 1) * units / gridDim.x);
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 128));
@@ -183,119 +186,148 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
     const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(p.g);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
 
+    // unit u = ((b * NC + c) * Hk + hk) * rep + hh, value head h = hk * rep + hh
+    struct Unit { int b, c, hk, h, t0, len; };
+    auto unit_of = [&](int u) {
+        Unit x;
+        const int hh = u % rep, grp = u / rep;
+        x.hk = grp % Hk;
+        const int bc = grp / Hk;
+        x.c = bc % NC;
+        x.b = bc / NC;
+        x.h = x.hk * rep + hh;
+        x.t0 = x.c * kL;
+        x.len = min(kL, T - x.t0);
+        return x;
+    };
+
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, 512);
-    // V of a value head's chunk into buffer `buf`, in its operand layout, by asynchronous
-    // copies (rows past the end: zeros)
-    auto fetch_v = [&](int h, int buf) {
+    // V of a unit's chunk into buffer `buf`, in its operand layout, by asynchronous copies
+    // (rows past the end: zeros)
+    auto fetch_v = [&](const Unit &x, int buf) {
         const int nv8 = Dv / 8;
         unsigned char *dst = vc + (size_t)buf * kL * Dv * 2;
         for (int e = tid; e < kL * nv8; e += 256) {
             const int r = e / nv8, ch = e - r * nv8;
-            const int rr = r < len ? r : 0;
-            cp_async16(dst + cm_off(r, 16 * ch, kL), v + (((size_t)b * T + t0 + rr) * Hv + h) * Dv + 8 * ch,
-                       r < len ? 16 : 0);
+            const int rr = r < x.len ? r : 0;
+            cp_async16(dst + cm_off(r, 16 * ch, kL), v + (((size_t)x.b * T + x.t0 + rr) * Hv + x.h) * Dv + 8 * ch,
+                       r < x.len ? 16 : 0);
         }
         cp_async_commit();
     };
-    // log g and beta of a value head (warp 0, two steps per lane), raw
+    // log g and beta of a unit (warp 0, two steps per lane), raw
     __nv_bfloat16 graw[2], braw[2];
-    auto fetch_gb = [&](int h) {
+    auto fetch_gb = [&](const Unit &x) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int t = 2 * lane + u;
-            const size_t o = ((size_t)b * T + t0 + (t < len ? t : 0)) * Hv + h;
+            const size_t o = ((size_t)x.b * T + x.t0 + (t < x.len ? t : 0)) * Hv + x.h;
             graw[u] = g[o];
             braw[u] = beta[o];
         }
     };
-    // the first value head's V, g and beta go out before anything else
-    fetch_v(hk * rep, 0);
-    if (warp == 0) fetch_gb(hk * rep);
-    {
-        // K and Q of the chunk (rows past the end are zero): all loads, then the stores
-        uint4 kx[NKQ], qx[NKQ];
-#pragma unroll
-        for (int u = 0; u < NKQ; ++u) {
-            const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
-            kx[u] = qx[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (e < kL * (DK / 8) && r < len) {
-                const size_t o = (((size_t)b * T + t0 + r) * p.Hk + hk) * DK + 8 * ch;
-                kx[u] = *reinterpret_cast<const uint4 *>(k + o);
-                qx[u] = *reinterpret_cast<const uint4 *>(q + o);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < NKQ; ++u) {
-            const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
-            if (e < kL * (DK / 8)) {
-                *reinterpret_cast<uint4 *>(kc + cm_off(r, 16 * ch, kL)) = kx[u];
-                *reinterpret_cast<uint4 *>(qc + cm_off(r, 16 * ch, kL)) = qx[u];
-            }
-        }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
     unsigned phase = 0;
     bool ok = true;
-    // K K^T -> columns [0, 64), Q K^T -> [64, 128) (M = 64: row m in lane m % 16 + 32 (m / 16))
-    if (tid == 0) {
-        constexpr uint32_t id = umma_idesc(1, kL, kL);
-        umma_gemm_bf16(tmem, kc, kL, 0, kc, kL, 0, DK, id, false);
-        umma_gemm_bf16(tmem + kL, qc, kL, 0, kc, kL, 0, DK, id, false);
-        umma_commit(bar);
-    }
-    {
-        // while the products run: K (its operand layout, for both sweeps) once per kv head, and
-        // [Q; K] in the gradient kernel's 128-row layout (16-byte piece j * 128 + r is row r of
-        // K chunk j, from Q (r < 64) or K)
-        const size_t ckv = ((size_t)b * p.Hk + hk) * p.NC + c;
-        const uint4 *q4 = reinterpret_cast<const uint4 *>(qc), *k4 = reinterpret_cast<const uint4 *>(kc);
-        uint4 *Kg = reinterpret_cast<uint4 *>(p.ktm + ckv * kL * DK);
-        for (int e = tid; e < kL * DK / 8; e += 256) Kg[e] = k4[e];
-        if (p.qkm != nullptr) {
-            uint4 *QKg = reinterpret_cast<uint4 *>(p.qkm + ckv * 2 * kL * DK);
-            for (int e = tid; e < 2 * kL * DK / 8; e += 256) {
-                const int j = e >> 7, r = e & 127;
-                QKg[e] = r < kL ? q4[j * kL + r] : k4[j * kL + r - kL];
+    uint32_t tmem = 0;
+    // K and Q of a (batch row, chunk, kv head), K K^T and Q K^T into kk and qk, and K and
+    // [Q; K] in the layouts of the sweeps and the gradient kernel
+    auto stage_group = [&](const Unit &x) {
+        {
+            uint4 kx[NKQ], qx[NKQ];
+#pragma unroll
+            for (int u = 0; u < NKQ; ++u) {
+                const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
+                kx[u] = qx[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (e < kL * (DK / 8) && r < x.len) {
+                    const size_t o = (((size_t)x.b * T + x.t0 + r) * Hk + x.hk) * DK + 8 * ch;
+                    kx[u] = *reinterpret_cast<const uint4 *>(k + o);
+                    qx[u] = *reinterpret_cast<const uint4 *>(q + o);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < NKQ; ++u) {
+                const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
+                if (e < kL * (DK / 8)) {
+                    *reinterpret_cast<uint4 *>(kc + cm_off(r, 16 * ch, kL)) = kx[u];
+                    *reinterpret_cast<uint4 *>(qc + cm_off(r, 16 * ch, kL)) = qx[u];
+                }
             }
         }
-    }
-    ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
-    ++phase;
-    tc_fence_after();
-    if (ok) {
-        // warps 0-3 read K K^T, warps 4-7 Q K^T; each warp its quarter's 16 valid lanes
-        const int quarter = warp & 3, row = 16 * quarter + lane;
-        float *dst = warp < 4 ? kk : qk;
-        const uint32_t col0 = warp < 4 ? 0u : (uint32_t)kL;
-        float x[64];
-        tmem_ld32f(tmem + ((uint32_t)(32 * quarter) << 16) + col0, x);
-        tmem_ld32f(tmem + ((uint32_t)(32 * quarter) << 16) + col0 + 32, x + 32);
-        tmem_wait_ld();
-        if (lane < 16)
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // K K^T -> columns [0, 64), Q K^T -> [64, 128) (M = 64: row m in lane m % 16 + 32 (m / 16))
+        if (tid == 0) {
+            constexpr uint32_t id = umma_idesc(1, kL, kL);
+            umma_gemm_bf16(tmem, kc, kL, 0, kc, kL, 0, DK, id, false);
+            umma_gemm_bf16(tmem + kL, qc, kL, 0, kc, kL, 0, DK, id, false);
+            umma_commit(bar);
+        }
+        {
+            // while the products run: K (its operand layout, for both sweeps), and [Q; K] in the
+            // gradient kernel's 128-row layout (16-byte piece j * 128 + r is row r of K chunk j,
+            // from Q (r < 64) or K). A group split between two CTAs is written by both, alike.
+            const size_t ckv = ((size_t)x.b * Hk + x.hk) * NC + x.c;
+            const uint4 *q4 = reinterpret_cast<const uint4 *>(qc), *k4 = reinterpret_cast<const uint4 *>(kc);
+            uint4 *Kg = reinterpret_cast<uint4 *>(p.ktm + ckv * kL * DK);
+            for (int e = tid; e < kL * DK / 8; e += 256) Kg[e] = k4[e];
+            if (p.qkm != nullptr) {
+                uint4 *QKg = reinterpret_cast<uint4 *>(p.qkm + ckv * 2 * kL * DK);
+                for (int e = tid; e < 2 * kL * DK / 8; e += 256) {
+                    const int j = e >> 7, r = e & 127;
+                    QKg[e] = r < kL ? q4[j * kL + r] : k4[j * kL + r - kL];
+                }
+            }
+        }
+        ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
+        ++phase;
+        tc_fence_after();
+        if (ok) {
+            // warps 0-3 read K K^T, warps 4-7 Q K^T; each warp its quarter's 16 valid lanes
+            const int quarter = warp & 3, row = 16 * quarter + lane;
+            float *dst = warp < 4 ? kk : qk;
+            const uint32_t col0 = warp < 4 ? 0u : (uint32_t)kL;
+            float xv[64];
+            tmem_ld32f(tmem + ((uint32_t)(32 * quarter) << 16) + col0, xv);
+            tmem_ld32f(tmem + ((uint32_t)(32 * quarter) << 16) + col0 + 32, xv + 32);
+            tmem_wait_ld();
+            if (lane < 16)
 #pragma unroll
-            for (int i = 0; i < 64; i += 4)
-                *reinterpret_cast<float4 *>(dst + row * kP + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+                for (int i = 0; i < 64; i += 4)
+                    *reinterpret_cast<float4 *>(dst + row * kP + i) = make_float4(xv[i], xv[i + 1], xv[i + 2], xv[i + 3]);
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+    // the first unit's V, g and beta go out before anything else
+    if (u_begin < u_end) {
+        const Unit x0 = unit_of(u_begin);
+        fetch_v(x0, 0);
+        if (warp == 0) fetch_gb(x0);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    tmem = *tslot;
 
-
-    for (int hh = 0; hh < rep && ok; ++hh) {
-        const int h = hk * rep + hh;
-        const size_t chk = ((size_t)b * Hv + h) * p.NC + c;   // (b, h, c)
-        unsigned char *vch = vc + (size_t)(hh & 1) * kL * Dv * 2;
-        // the next head's V goes out now; this head's has landed once the older group is done
-        if (hh + 1 < rep) {
-            fetch_v(h + 1, (hh + 1) & 1);
+    for (int u = u_begin, i = 0; u < u_end && ok; ++u, ++i) {
+        const Unit x = unit_of(u);
+        const int b = x.b, c = x.c, h = x.h, len = x.len;
+        if (i == 0 || (u - 1) / rep != u / rep) {
+            stage_group(x);
+            if (!ok) break;
+        }
+        const size_t chk = ((size_t)b * Hv + h) * NC + c;   // (b, h, c)
+        unsigned char *vch = vc + (size_t)(i & 1) * kL * Dv * 2;
+        // the next unit's V goes out now; this unit's has landed once the older group is done
+        if (u + 1 < u_end) {
+            fetch_v(unit_of(u + 1), (i + 1) & 1);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
@@ -304,13 +336,13 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
         if (warp == 0) {
             float l2[2], b2[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int t = 2 * lane + u;
+            for (int j = 0; j < 2; ++j) {
+                const int t = 2 * lane + j;
                 const bool in = t < len;
-                l2[u] = in ? fmaxf(logf(__bfloat162float(graw[u])), -200.f) : 0.f;   // g = 0: exp(-200) = 0 in fp32; a nonzero bf16 g has log g > -93
-                b2[u] = in ? __bfloat162float(braw[u]) : 0.f;
+                l2[j] = in ? fmaxf(logf(__bfloat162float(graw[j])), -200.f) : 0.f;   // g = 0: exp(-200) = 0 in fp32; a nonzero bf16 g has log g > -93
+                b2[j] = in ? __bfloat162float(braw[j]) : 0.f;
             }
-            if (hh + 1 < rep) fetch_gb(h + 1);   // used one head later
+            if (u + 1 < u_end) fetch_gb(unit_of(u + 1));   // used one unit later
             float s = l2[0] + l2[1];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -319,12 +351,12 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p) {
             }
             const float e0 = s - l2[1];                       // inclusive prefix at step 2 lane
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int t = 2 * lane + u;
-                const float Lt = u == 0 ? e0 : s;
+            for (int j = 0; j < 2; ++j) {
+                const int t = 2 * lane + j;
+                const float Lt = j == 0 ? e0 : s;
                 Lm[t] = Lt;
                 gm[t] = expf(Lt);
-                bt[t] = b2[u];
+                bt[t] = b2[j];
                 p.lam[chk * kL + t] = Lt;
             }
         }
@@ -797,7 +829,13 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck
     err = cudaFuncSetAttribute(chunk_sweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_prep", 0, s);
-    chunk_prep_kernel<E><<<dim3(p.NC, p.Hk, p.B), 256, sp, s>>>(p);
+    const int units = p.NC * p.Hv * p.B;
+    int dev = 0, sms = 0;
+    err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    chunk_prep_kernel<E><<<units < sms ? units : sms, 256, sp, s>>>(p, units);   // persistent: one CTA per SM
     timing_mark("chunk_prep", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
