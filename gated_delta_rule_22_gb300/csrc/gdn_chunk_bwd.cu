@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
     bool ok = true;
     // a chunk's dY block (into the dY rows of a [dY; dU] buffer), its v - u and Lam arrive by
     // asynchronous copies one chunk ahead; beta (threads < 64) by a load one chunk ahead
-    float btn = 0.f;
+    __nv_bfloat16 btn = __float2bfloat16_rn(0.f);   // raw: converted where it is used, so that the load does not stall here
     auto fetch_chunk = [&](int cc, int buf) {
         const int tt0 = cc * kL, ln = min(kL, T - tt0);
         const size_t rb = (size_t)b * T + tt0;
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
         }
         if (tid < 16) cp_async16(lms + buf * kL + 4 * tid, p.lam + (head * p.NC + cc) * kL + 4 * tid, 16);
         cp_async_commit();
-        if (tid < kL) btn = tid < ln ? __bfloat162float(beta[(rb + tid) * Hv + h]) : 0.f;
+        if (tid < kL) btn = beta[(rb + (tid < ln ? tid : 0)) * Hv + h];
     };
     if (tid == 0) { copy_A(p.NC - 1); copy_T(p.NC - 1); copy_K(p.NC - 1); }
     fetch_chunk(p.NC - 1, 0);
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
         const int buf = (p.NC - 1 - c) & 1;
         unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;   // [dY; dU] of this chunk
         cp_async_wait<0>();                                 // this chunk's dY, v - u and Lam have landed
-        if (tid < kL) bt[tid] = btn;
+        if (tid < kL) bt[tid] = tid < len ? __bfloat162float(btn) : 0.f;
         __syncthreads();
         if (tid < kL) Lm[tid] = lms[buf * kL + tid];
         // this lane's v - u (row lrow, 32 value columns)
@@ -508,20 +508,22 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         ++nQ;
     };
     auto same_qk = [&](int u1, int u2) { return u1 / rep == u2 / rep; };   // same (b, chunk, kv head)
-    // decays, beta and f of a unit (threads < 64), loaded one unit ahead
-    float vlam = 0.f, vbt = 0.f, vf = 0.f;
+    // decays, beta and the f partials of a unit (threads < 64), loaded one unit ahead and kept
+    // raw (converted and summed where they are used, so that the loads do not stall here)
+    constexpr int kMaxSplit = 4;                            // Dv <= 256
+    float vlam = 0.f, vfp[kMaxSplit] = {0.f, 0.f, 0.f, 0.f};
+    __nv_bfloat16 vbt = __float2bfloat16_rn(0.f);
     auto load_vec = [&](int u) {
         if (tid >= kL) return;
         int b, c, h;
         chunk_of(u, b, c, h);
         const size_t chk = ((size_t)b * Hv + h) * NC + c;
         const int t0 = c * kL, len = min(kL, T - t0);
-        const size_t row = ((size_t)b * T + t0 + tid) * Hv + h;
+        const size_t row = ((size_t)b * T + t0 + (tid < len ? tid : 0)) * Hv + h;
         vlam = p.lam[chk * kL + tid];
-        vbt = tid < len ? __bfloat162float(beta[row]) : 0.f;
-        vf = 0.f;
-        if (tid < len)
-            for (int s = 0; s < nsplit; ++s) vf += p.ws_f[row * nsplit + s];
+        vbt = beta[row];
+#pragma unroll
+        for (int s = 0; s < kMaxSplit; ++s) vfp[s] = s < nsplit ? p.ws_f[row * nsplit + s] : 0.f;
     };
 
     if (tid == 0) {
@@ -553,8 +555,12 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         if (tid < kL) {
             Lm[tid] = vlam;
             gm[tid] = expf(vlam);
-            bt[tid] = vbt;
-            fv[tid] = vf;
+            const bool in = tid < len;
+            bt[tid] = in ? __bfloat162float(vbt) : 0.f;
+            float f = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxSplit; ++s) f += s < nsplit ? vfp[s] : 0.f;   // splits in ascending order
+            fv[tid] = in ? f : 0.f;
         }
         __syncthreads();
         if (tid < kL) {
