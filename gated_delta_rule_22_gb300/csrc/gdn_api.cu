@@ -264,6 +264,29 @@ int make_f32_map_2d(CUtensorMap *map, void *ptr, size_t rows, size_t cols, int b
     return GDN_OK;
 }
 
+// 4-D tensor map of a row-major [B][T][H][D] tensor (bf16 or fp32), box {box_d, 1, box_t, 1},
+// 128-byte swizzle (box_d * element size must be 128 bytes).
+int make_btd_map(CUtensorMap *map, void *ptr, bool bf16, int B, int T, int H, int D, int box_d, int box_t) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available from the driver");
+        return GDN_ERR_CUDA;
+    }
+    const cuuint64_t e = bf16 ? 2 : 4;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {D * e, (cuuint64_t)H * D * e, (cuuint64_t)T * H * D * e};
+    const cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)box_t, 1};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr,
+                           dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 }  // namespace
 
 namespace gdn {
@@ -377,10 +400,14 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.qkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qkm);
         cp.status = fp.status;
         cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
-        CUtensorMap tm_ck;
+        CUtensorMap tm_ck, tm_y, tm_r;
         rc = make_f32_map_2d(&tm_ck, ckpt, (size_t)p.B * p.Hv * p.NC * p.Dv, (size_t)p.Dk, 32, 64);
         if (rc != GDN_OK) return rc;
-        return cuda_status(gdn::launch_chunk_fwd(cp, tm_ck, p.Dk, (cudaStream_t)stream));
+        rc = make_btd_map(&tm_y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64);
+        if (rc != GDN_OK) return rc;
+        rc = make_btd_map(&tm_r, fp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64);
+        if (rc != GDN_OK) return rc;
+        return cuda_status(gdn::launch_chunk_fwd(cp, tm_ck, tm_y, tm_r, p.Dk, (cudaStream_t)stream));
     }
     CUtensorMap tm_q, tm_k;
     if ((rc = make_qk_map(&tm_q, q, p, gdn::kFwdTile)) != GDN_OK) return rc;

@@ -508,7 +508,7 @@ namespace gdn {
 namespace {
 
 struct SweepSmem {
-    size_t wc, qs, ks, kt, pc, kkc, sop, dt, de, dtile, ckst, vec, bar, tslot, total;
+    size_t wc, qs, ks, kt, pc, kkc, sop, dt, de, dtile, ckst, ysg, vec, bar, tslot, total;
     __host__ __device__ SweepSmem(int DK) {
         size_t o = 0;
         wc = o; o += (size_t)kL * DK * 2;     // W of the chunk        A [64][DK]
@@ -522,6 +522,7 @@ struct SweepSmem {
         de = o; o += (size_t)kL * kL * 2;     // (diag(E_L) Delta)^T   A [64][64]
         dtile = o; o += (size_t)kL * kPad * 4; // Delta, fp32 [64][65]
         ckst = al(o, 1024); o = ckst + (size_t)kL * DK * 4;   // chunk-start state, fp32, boxes of [64][32] in the 128-byte swizzle
+        ysg = al(o, 1024); o = ysg + (size_t)kL * 128;       // y of a chunk, bf16 [64][64] in the 128-byte swizzle
         vec = o; o += 3 * kL * 4;             // Lam, exp Lam, E(L, .)
         bar = al(o, 8); o = bar + 24;         // MMA completion, the two groups of operand copies
         tslot = o; o += 16;
@@ -541,7 +542,9 @@ struct SweepSmem {
 //   [DK + 64, DK + 128) the prediction u of the chunk
 //   [DK + 128, DK + 192) W S^T
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ CUtensorMap tm_ck) {
+__global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ CUtensorMap tm_ck,
+                                                             const __grid_constant__ CUtensorMap tm_y,
+                                                             const __grid_constant__ CUtensorMap tm_r) {
     constexpr int DK = 32 * E;
     static_assert(DK + 192 <= 512, "tensor memory holds the state, y, u and W S^T");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -557,13 +560,13 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     unsigned char *wc = base + L.wc, *qs = base + L.qs, *ks = base + L.ks, *kt = base + L.kt;
     unsigned char *pc = base + L.pc, *kkc = base + L.kkc, *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
     float *dtile = reinterpret_cast<float *>(base + L.dtile);
-    unsigned char *ckst = base + L.ckst;
+    unsigned char *ckst = base + L.ckst, *ysg = base + L.ysg;
+    unsigned char *rsg = dt;                                // v - u of a chunk, fp32 [2][64][32] in the 128-byte swizzle (dt, de)
     float *Lm = reinterpret_cast<float *>(base + L.vec), *gm = Lm + kL, *eL = gm + kL;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1, *rbar = bar + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
-    __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
     const size_t head = (size_t)b * Hv + h;
     // the six operand matrices of chunk cc, prepared in their shared-memory layout, by bulk
     // copies in two groups (thread 0): W, read by the first product of a chunk, goes out as
@@ -630,38 +633,41 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
 #pragma unroll
         for (int i = 0; i < 4; ++i) vx[i] = mine ? reinterpret_cast<const uint4 *>(v + o)[i] : make_uint4(0u, 0u, 0u, 0u);
     };
-    // y and v - u of chunk cc, from tensor memory (their columns are rewritten only by the
-    // next chunk's second group of products)
+    // y and v - u of chunk cc, from tensor memory (their columns are rewritten only by the next
+    // chunk's second group of products), staged in the 128-byte swizzle for TMA stores: y in its
+    // own tile, v - u in the Delta^T operand buffers (free until this chunk's operands are
+    // built; thread 0 waits for the stores' reads before that). Rows past T are clipped by the
+    // stores.
     auto epilogue = [&](int cc) {
-        const int tt0 = cc * kL, ln = min(kL, T - tt0);
-        const size_t o = (((size_t)b * T + tt0 + lrow) * Hv + h) * Dv + r0 + half * 32;
-        const bool mine = lane < 16 && lrow < ln;
-        float x[16];
+        float yv[32], uv[32];
+        tmem_ld32f(tY + lane_off + half * 32, yv);
+        tmem_ld32f(tU + lane_off + half * 32, uv);
+        tmem_wait_ld();
+        if (lane < 16) {
+            const int t = lrow, sw = t & 7;
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-            const int cc2 = half * 32 + 16 * hc;
-            tmem_ld16f(tY + lane_off + cc2, x);
-            tmem_wait_ld();
-            if (mine) {
-                float a[8], bb[8];
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4 *>(ysg + t * 128 + (((half * 4 + j) ^ sw) << 4)) =
+                    pack8_bf16(*reinterpret_cast<const float (*)[8]>(yv + 8 * j));
+            float va[32];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) { a[i] = x[i]; bb[i] = x[8 + i]; }
-                *reinterpret_cast<uint4 *>(y + o + 16 * hc) = pack8_bf16(a);
-                *reinterpret_cast<uint4 *>(y + o + 16 * hc + 8) = pack8_bf16(bb);
+            for (int j = 0; j < 4; ++j) unpack8_bf16(vx[j], *reinterpret_cast<float (*)[8]>(va + 8 * j));
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4 *>(rsg + half * (kL * 128) + t * 128 + ((j ^ sw) << 4)) =
+                    make_float4(va[4 * j] - uv[4 * j], va[4 * j + 1] - uv[4 * j + 1], va[4 * j + 2] - uv[4 * j + 2],
+                                va[4 * j + 3] - uv[4 * j + 3]);
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            const int tt0 = cc * kL;
+            tma_store_4d(&tm_y, ysg, r0, h, tt0, b);
+            if (p.resid != nullptr) {
+                tma_store_4d(&tm_r, rsg, r0, h, tt0, b);
+                tma_store_4d(&tm_r, rsg + kL * 128, r0 + 32, h, tt0, b);
             }
-            tmem_ld16f(tU + lane_off + cc2, x);
-            tmem_wait_ld();
-            if (mine && p.resid != nullptr) {
-                float va[8], vb[8];
-                unpack8_bf16(vx[2 * hc], va);
-                unpack8_bf16(vx[2 * hc + 1], vb);
-                float *rr = p.resid + o + 16 * hc;
-#pragma unroll
-                for (int i = 0; i < 8; i += 4) {
-                    *reinterpret_cast<float4 *>(rr + i) = make_float4(va[i] - x[i], va[i + 1] - x[i + 1], va[i + 2] - x[i + 2], va[i + 3] - x[i + 3]);
-                    *reinterpret_cast<float4 *>(rr + 8 + i) = make_float4(vb[i] - x[8 + i], vb[i + 1] - x[9 + i], vb[i + 2] - x[10 + i], vb[i + 3] - x[11 + i]);
-                }
-            }
+            bulk_commit();
         }
     };
     if (tid == 0) { issue_w(0); issue_r(0); }
@@ -750,6 +756,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
             }
         }
         if (c + 1 < p.NC) load_u(c + 1);                   // the next chunk's U, used one chunk later
+        if (tid == 0) bulk_wait_read();                     // the y and v - u stores have read dt, de and ysg
         tc_fence_before();
         __syncthreads();
         // Delta^T and (diag(E_L) Delta)^T as operands: value column n, eight chunk rows per store
@@ -821,7 +828,8 @@ size_t chunk_prep_smem(int Dk, int Dv) { return PrepSmem(Dk, Dv).total; }
 size_t chunk_sweep_smem(int Dk) { return SweepSmem(Dk).total; }
 
 template <int E>
-static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck, cudaStream_t s) {
+static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck, const CUtensorMap &tm_y,
+                                  const CUtensorMap &tm_r, cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sp = PrepSmem(DK, p.Dv).total, ss = SweepSmem(DK).total;
     cudaError_t err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
@@ -840,16 +848,17 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     timing_mark("chunk_sweep", 0, s);
-    chunk_sweep_kernel<E><<<dim3(p.Dv / kL, p.Hv, p.B), 256, ss, s>>>(p, tm_ck);
+    chunk_sweep_kernel<E><<<dim3(p.Dv / kL, p.Hv, p.B), 256, ss, s>>>(p, tm_ck, tm_y, tm_r);
     timing_mark("chunk_sweep", 1, s);
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, int Dk, cudaStream_t s) {
+cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, const CUtensorMap &tm_y,
+                             const CUtensorMap &tm_r, int Dk, cudaStream_t s) {
     switch (Dk) {
-        case 64: return launch_chunk_t<2>(p, tm_ck, s);
-        case 128: return launch_chunk_t<4>(p, tm_ck, s);
-        case 192: return launch_chunk_t<6>(p, tm_ck, s);
+        case 64: return launch_chunk_t<2>(p, tm_ck, tm_y, tm_r, s);
+        case 128: return launch_chunk_t<4>(p, tm_ck, tm_y, tm_r, s);
+        case 192: return launch_chunk_t<6>(p, tm_ck, tm_y, tm_r, s);
         default: return cudaErrorInvalidValue;
     }
 }

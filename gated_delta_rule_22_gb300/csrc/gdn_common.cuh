@@ -332,6 +332,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
                  : "memory");
 }
 
+// 4-D tiled TMA store of one box from shared memory, in the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int c0, int c1, int c2,
+                                             int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(src))
+        : "memory");
+}
+
 // Orders this thread's earlier generic-proxy global writes before later async-proxy
 // (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -418,9 +428,11 @@ size_t bwd_smem_bytes(int Dk, int C, int dtype, int slots);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // Chunkwise forward: Dk in {64, 128, 192}, Dv a multiple of 64 up to 256, bf16, C = 64.
-// tm_ck: 2-D tensor map of the fp32 checkpoints as [B*Hv*NC*Dv rows][Dk], box {32, 64},
-// 128-byte swizzle (written by TMA stores).
-cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, int Dk, cudaStream_t s);
+// Tensor maps (all written by TMA stores, 128-byte swizzle): tm_ck the fp32 checkpoints as
+// [B*Hv*NC*Dv rows][Dk], box {32, 64}; tm_y y as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1};
+// tm_r v - u as [B][T][Hv][Dv] fp32, box {32, 1, 64, 1}.
+cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, const CUtensorMap &tm_y,
+                             const CUtensorMap &tm_r, int Dk, cudaStream_t s);
 size_t chunk_prep_smem(int Dk, int Dv);
 size_t chunk_sweep_smem(int Dk);
 // Chunkwise backward: the reverse sweep over chunks (dS), the per-chunk gradient products
