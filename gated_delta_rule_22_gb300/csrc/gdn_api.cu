@@ -458,7 +458,10 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         g_last_error[0] = '\0';
         rc = device_status_address(&cp.status);
         if (rc != GDN_OK) return rc;
-        return cuda_status(gdn::launch_chunk_bwd(cp, p.Dk, (cudaStream_t)stream));
+        CUtensorMap tm_dv;
+        rc = make_btd_map(&tm_dv, dv, true, p.B, p.T, p.Hv, p.Dv, 64, 64);
+        if (rc != GDN_OK) return rc;
+        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, p.Dk, (cudaStream_t)stream));
     }
     const Workspace w = workspace_layout(p);
 

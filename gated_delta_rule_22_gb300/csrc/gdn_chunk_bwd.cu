@@ -66,7 +66,7 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 
 // ------------------------------------------------------------------ reverse sweep (dS)
 struct DSweepSmem {
-    size_t kt, qs, ks, tm, pm, ydu, rsm, lms, shi, slo, rhs, dls, vec, red, bar, tslot, total;
+    size_t kt, qs, ks, tm, pm, ydu, rsm, lms, shi, slo, rhs, dls, dvs, vec, red, bar, tslot, total;
     __host__ __device__ DSweepSmem(int DK) {
         size_t o = 0;
         kt = o; o += (size_t)kL * DK * 2;    // K [64][DK]
@@ -81,6 +81,7 @@ struct DSweepSmem {
         slo = o; o += (size_t)kL * DK * 2;   // dS - high part, bf16
         rhs = o; o += (size_t)kL * kL * 2;   // diag(E_L) K dS^T + P^T dY [64 t][64 v]
         dls = o; o += (size_t)kL * kL * 2;   // Delta block [64 t][64 v], for the gradient kernel
+        dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
         vec = o; o += 4 * kL * 4;            // Lam, E(L, .), beta, -
         red = o; o += 2 * 2 * kL * 4;        // [f | dbeta][half][64]
         bar = alb(o, 8); o = bar + 4 * 8;    // MMA, copies of (K^T, P, Qs), of T, of Ks
@@ -98,7 +99,7 @@ struct DSweepSmem {
 //   [DK, DK + 64)      K dS^T, then dD (chunk row t, value column of this block)
 //   [DK + 64, DK + 128) P^T dY
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) {
+__global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, const __grid_constant__ CUtensorMap tm_dv) {
     constexpr int DK = 32 * E;
     static_assert(DK + 128 <= 512, "tensor memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
     const DSweepSmem L(DK);
     unsigned char *kt = base + L.kt, *qs = base + L.qs, *ks = base + L.ks, *tmm = base + L.tm, *pmm = base + L.pm;
     unsigned char *ydu2 = base + L.ydu, *shi = base + L.shi, *slo = base + L.slo, *rhs = base + L.rhs, *dls = base + L.dls;
+    unsigned char *dvs = base + L.dvs;
     float *rsm = reinterpret_cast<float *>(base + L.rsm), *lms = reinterpret_cast<float *>(base + L.lms);
     float *Lm = reinterpret_cast<float *>(base + L.vec), *eL = Lm + kL, *bt = eL + kL;
     float *red = reinterpret_cast<float *>(base + L.red);   // [2][2][64]
@@ -123,7 +125,6 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
 
     const __nv_bfloat16 *dy = static_cast<const __nv_bfloat16 *>(p.dy);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
-    __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(p.dv);
     const size_t head = (size_t)b * Hv + h;
 
     // bulk copies of chunk cc's operands, three groups (each freed at a different point)
@@ -340,11 +341,10 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     *reinterpret_cast<uint4 *>(ydu + cm_off(kL + lrow, 16 * (half * 4 + j), 2 * kL)) = pack8(duu + 8 * j);
-                if (lrow < len) {
-                    uint4 *dvg = reinterpret_cast<uint4 *>(dv + ((rowbase + lrow) * Hv + h) * Dv + r0 + half * 32);
+                // dv staged in the 128-byte swizzle for a TMA store (rows past T are clipped by it)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) dvg[j] = pack8(dvv + 8 * j);
-                }
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(dvs + lrow * 128 + (((half * 4 + j) ^ (lrow & 7)) << 4)) = pack8(dvv + 8 * j);
                 red[2 * kL + half * kL + lrow] = ds;
             }
         }
@@ -360,10 +360,11 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p) 
         if (tid == 0) {
             umma_gemm(tS, CmOp{ydu, 2 * kL, 0, kL, true}, CmOp{ks, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, true, true),
                       true);
-            // [dY; dU] and Delta of the block for the gradient kernel
+            // [dY; dU] and Delta of the block for the gradient kernel, and dv
             const size_t blk = chk * nsplit + split;
             bulk_store(p.ws_yu + blk * 2 * kL * kL, ydu, 2 * kL * kL * 2);
             bulk_store(p.ws_dl + blk * kL * kL, dls, kL * kL * 2);
+            tma_store_4d(&tm_dv, dvs, r0, h, t0, b);
             bulk_commit();
             umma_commit(bar);
         }
@@ -853,7 +854,7 @@ size_t chunk_dsweep_smem(int Dk) { return DSweepSmem(Dk).total; }
 size_t chunk_grad_smem(int Dk, int Dv) { return GradSmem(Dk, Dv).total; }
 
 template <int E>
-static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, cudaStream_t s) {
+static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap &tm_dv, cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sd = DSweepSmem(DK).total, sg = GradSmem(DK, p.Dv).total;
     cudaError_t err = cudaFuncSetAttribute(chunk_dsweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd);
@@ -861,7 +862,7 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, cudaStream_t s) {
     err = cudaFuncSetAttribute(chunk_grad_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_dsweep", 0, s);
-    chunk_dsweep_kernel<E><<<dim3(p.nsplit, p.Hv, p.B), 256, sd, s>>>(p);
+    chunk_dsweep_kernel<E><<<dim3(p.nsplit, p.Hv, p.B), 256, sd, s>>>(p, tm_dv);
     timing_mark("chunk_dsweep", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
@@ -886,11 +887,11 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, int Dk, cudaStream_t s) {
+cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, int Dk, cudaStream_t s) {
     switch (Dk) {
-        case 64: return launch_chunk_bwd_t<2>(p, s);
-        case 128: return launch_chunk_bwd_t<4>(p, s);
-        case 192: return launch_chunk_bwd_t<6>(p, s);
+        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, s);
+        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, s);
+        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, s);
         default: return cudaErrorInvalidValue;
     }
 }

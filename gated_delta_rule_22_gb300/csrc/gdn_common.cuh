@@ -437,7 +437,8 @@ size_t chunk_prep_smem(int Dk, int Dv);
 size_t chunk_sweep_smem(int Dk);
 // Chunkwise backward: the reverse sweep over chunks (dS), the per-chunk gradient products
 // and the fixed-order sums over value heads and row blocks.
-cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, int Dk, cudaStream_t s);
+// tm_dv: 4-D tensor map of dv as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1}, 128-byte swizzle.
+cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, int Dk, cudaStream_t s);
 size_t chunk_dsweep_smem(int Dk);
 size_t chunk_grad_smem(int Dk, int Dv);
 cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s);
