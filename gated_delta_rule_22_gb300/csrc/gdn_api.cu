@@ -77,7 +77,7 @@ size_t ckpt_resid_bytes(const Plan &p) { return (size_t)p.B * p.T * p.Hv * p.Dv 
 // With the chunkwise forward the buffer continues (each part from a 256-byte boundary) with
 // the per-chunk data of every (b, h, chunk): Lam [64] fp32, the sweep's bf16 operands in their
 // core-matrix layout ((Q K^T) o E and (K K^T) o E [64][64], W, diag(exp Lam) Q,
-// diag(exp Lam) K [64][Dk], K^T [Dk][64]) and U [64][Dv] fp32.
+// diag(exp Lam) K [64][Dk]; K [64][Dk] per kv head) and U fp32 in [Dv/32][64][32] blocks.
 struct ChunkLayout {
     size_t lam, pm, kkm, wm, qsm, ksm, ktm, um, tm, s0m, qkm, end;
 };
@@ -407,7 +407,10 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         if (rc != GDN_OK) return rc;
         rc = make_btd_map(&tm_r, fp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64);
         if (rc != GDN_OK) return rc;
-        return cuda_status(gdn::launch_chunk_fwd(cp, tm_ck, tm_y, tm_r, p.Dk, (cudaStream_t)stream));
+        CUtensorMap tm_u;
+        rc = make_f32_map_2d(&tm_u, cp.um, (size_t)p.B * p.Hv * p.NC * 2 * p.Dv, 32, 32, 64);
+        if (rc != GDN_OK) return rc;
+        return cuda_status(gdn::launch_chunk_fwd(cp, tm_ck, tm_y, tm_r, tm_u, p.Dk, (cudaStream_t)stream));
     }
     CUtensorMap tm_q, tm_k;
     if ((rc = make_qk_map(&tm_q, q, p, gdn::kFwdTile)) != GDN_OK) return rc;

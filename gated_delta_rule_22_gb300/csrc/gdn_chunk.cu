@@ -30,8 +30,14 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 
 __host__ __device__ inline size_t al(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// U leaves prep by TMA stores of [64][32] fp32 boxes staged in the 128-byte swizzle, in
+// kUSlots slots of 8 KB that reuse T, the inversion scratch and the T operands (slots 0-3;
+// the next unit writes them from its inversion on) and A (slots 4-5; written from the next
+// unit's start): all are dead once the products W and U are done.
+constexpr int kUSlots = 6;
+
 struct PrepSmem {
-    size_t kc, qc, kk, qk, am, ts, xs, tcw, tcu, vc, lam, bar, tslot, total;
+    size_t kc, qc, kk, qk, am, ts, xs, tcw, tcu, vc, lam, bar, tslot, ustg, ustg2, total;
     __host__ __device__ PrepSmem(int DK, int Dv) {
         size_t o = 0;
         kc = o; o += (size_t)kL * DK * 2;           // K of the chunk, bf16 operand [64][DK]
@@ -43,11 +49,13 @@ struct PrepSmem {
         xs = o; o += (size_t)32 * 32 * 4;           // block products of the inversion
         tcw = o; o += (size_t)kL * kL * 2;          // T diag(beta exp Lam), bf16 operand [64][64]
         tcu = o; o += (size_t)kL * kL * 2;          // T diag(beta), bf16 operand [64][64]
+        ustg = al(ts, 1024);                        // U staging slots 0-3 (base 1024-aligned), up to the end of tcu
+        ustg2 = al(am, 1024);                       // slots 4-5
         vc = o; o += (size_t)2 * kL * Dv * 2;       // V of the chunk, bf16 operand [64][Dv], two buffers (heads alternate)
         lam = o; o += 4 * kL * 4;                   // log g, Lam, exp Lam, beta
         bar = al(o, 8); o = bar + 8;
         tslot = o; o += 16;
-        total = o + 128;
+        total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
     }
 };
@@ -156,16 +164,16 @@ __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid
 // scalings folded into T's columns, K and V read as MN-major operands). The next unit's V, g
 // and beta are fetched while the current one computes.
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int units) {
+__global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int units,
+                                                            const __grid_constant__ CUtensorMap tm_u) {
     constexpr int DK = 32 * E;
-    constexpr int NKQ = (kL * DK / 8 + 255) / 256;   // 16-byte pieces of K (or Q) per thread
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, Hk = p.Hk, NC = p.NC, rep = p.Hv / p.Hk;
     const int u_begin = (int)((long long)blockIdx.x * units / gridDim.x);
     const int u_end = (int)((long long)(blockIdx.x + 1) * units / gridDim.x);
 
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 128));
+    unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 1024));
     const PrepSmem L(DK, Dv);
     unsigned char *kc = base + L.kc, *qc = base + L.qc, *tcw = base + L.tcw, *tcu = base + L.tcu, *vc = base + L.vc;
     float *kk = reinterpret_cast<float *>(base + L.kk);
@@ -230,33 +238,26 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
             braw[u] = beta[o];
         }
     };
+    // K and Q of a (batch row, chunk, kv head) into kc and qc in their operand layout, by
+    // asynchronous copies (rows past the end: zeros)
+    auto fetch_kq = [&](const Unit &x) {
+        for (int e = tid; e < kL * (DK / 8); e += 256) {
+            const int r = e / (DK / 8), ch = e - r * (DK / 8);
+            const size_t o = (((size_t)x.b * T + x.t0 + (r < x.len ? r : 0)) * Hk + x.hk) * DK + 8 * ch;
+            cp_async16(kc + cm_off(r, 16 * ch, kL), k + o, r < x.len ? 16 : 0);
+            cp_async16(qc + cm_off(r, 16 * ch, kL), q + o, r < x.len ? 16 : 0);
+        }
+        cp_async_commit();
+    };
     unsigned phase = 0;
     bool ok = true;
     uint32_t tmem = 0;
-    // K and Q of a (batch row, chunk, kv head), K K^T and Q K^T into kk and qk, and K and
-    // [Q; K] in the layouts of the sweeps and the gradient kernel
+    // A (batch row, chunk, kv head) group whose K and Q were fetched into kc and qc: K K^T and
+    // Q K^T into kk and qk, and K and [Q; K] in the layouts of the sweeps and the gradient
+    // kernel (bulk stores by thread 32, which waits for their reads before kc and qc are
+    // refilled)
     auto stage_group = [&](const Unit &x) {
-        {
-            uint4 kx[NKQ], qx[NKQ];
-#pragma unroll
-            for (int u = 0; u < NKQ; ++u) {
-                const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
-                kx[u] = qx[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (e < kL * (DK / 8) && r < x.len) {
-                    const size_t o = (((size_t)x.b * T + x.t0 + r) * Hk + x.hk) * DK + 8 * ch;
-                    kx[u] = *reinterpret_cast<const uint4 *>(k + o);
-                    qx[u] = *reinterpret_cast<const uint4 *>(q + o);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < NKQ; ++u) {
-                const int e = tid + 256 * u, r = e / (DK / 8), ch = e - r * (DK / 8);
-                if (e < kL * (DK / 8)) {
-                    *reinterpret_cast<uint4 *>(kc + cm_off(r, 16 * ch, kL)) = kx[u];
-                    *reinterpret_cast<uint4 *>(qc + cm_off(r, 16 * ch, kL)) = qx[u];
-                }
-            }
-        }
+        cp_async_wait<0>();
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
@@ -268,21 +269,20 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
             umma_gemm_bf16(tmem + kL, qc, kL, 0, kc, kL, 0, DK, id, false);
             umma_commit(bar);
         }
-        {
-            // while the products run: K (its operand layout, for both sweeps), and [Q; K] in the
-            // gradient kernel's 128-row layout (16-byte piece j * 128 + r is row r of K chunk j,
-            // from Q (r < 64) or K). A group split between two CTAs is written by both, alike.
+        if (tid == 32) {
+            // K in its operand layout (for both sweeps), and [Q; K] in the gradient kernel's
+            // 128-row layout (K chunk j: the 64 rows of Q, then the 64 rows of K). A group split
+            // between two CTAs is written by both, alike.
             const size_t ckv = ((size_t)x.b * Hk + x.hk) * NC + x.c;
-            const uint4 *q4 = reinterpret_cast<const uint4 *>(qc), *k4 = reinterpret_cast<const uint4 *>(kc);
-            uint4 *Kg = reinterpret_cast<uint4 *>(p.ktm + ckv * kL * DK);
-            for (int e = tid; e < kL * DK / 8; e += 256) Kg[e] = k4[e];
+            bulk_store(p.ktm + ckv * kL * DK, kc, kL * DK * 2);
             if (p.qkm != nullptr) {
-                uint4 *QKg = reinterpret_cast<uint4 *>(p.qkm + ckv * 2 * kL * DK);
-                for (int e = tid; e < 2 * kL * DK / 8; e += 256) {
-                    const int j = e >> 7, r = e & 127;
-                    QKg[e] = r < kL ? q4[j * kL + r] : k4[j * kL + r - kL];
+                __nv_bfloat16 *QKg = p.qkm + ckv * 2 * kL * DK;
+                for (int j = 0; j < DK / 8; ++j) {
+                    bulk_store(QKg + (size_t)j * 2 * kL * 8, qc + j * kL * 16, kL * 16);
+                    bulk_store(QKg + (size_t)j * 2 * kL * 8 + kL * 8, kc + j * kL * 16, kL * 16);
                 }
             }
+            bulk_commit();
         }
         ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
         ++phase;
@@ -305,10 +305,11 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         __syncthreads();
         tc_fence_after();
     };
-    // the first unit's V, g and beta go out before anything else
+    // the first unit's V, K, Q, g and beta go out before anything else
     if (u_begin < u_end) {
         const Unit x0 = unit_of(u_begin);
         fetch_v(x0, 0);
+        fetch_kq(x0);
         if (warp == 0) fetch_gb(x0);
     }
     tc_fence_before();
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
                 p.lam[chk * kL + t] = Lt;
             }
         }
+        if (tid == 128 && Dv > 128) bulk_wait_read();   // the last unit's U boxes have left A
         __syncthreads();
         // A, and the decay-weighted Q K^T (i <= t) and K K^T (i < t) as bf16 operands in their
         // core-matrix layout: 16-byte chunk e holds row e % 64, columns 8 (e / 64) .. + 7
@@ -403,6 +405,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
                 Kg[e] = pack8_bf16(a);
             }
         }
+        if (tid == 128) bulk_wait_read();   // the last unit's U boxes have left T and the T operands
         __syncthreads();
         invert_unit_lower(am, ts, xs, tid);
         // T (for the backward), T diag(beta exp Lam) and T diag(beta) as bf16 operands; the
@@ -444,9 +447,14 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
                       umma_idesc_t(1, kL, Dv, false, true), false);
             umma_commit(bar);
         }
+        // when the next unit starts another group, its K and Q are fetched into kc and qc
+        // (free once these products are done) while this unit's results are read back
+        const bool kq_next = u + 1 < u_end && (u + 1) / rep != u / rep;
+        if (tid == 32 && kq_next) bulk_wait_read();   // the stores of K and [Q; K] have read kc, qc
         ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
         ++phase;
         tc_fence_after();
+        if (ok && kq_next) fetch_kq(unit_of(u + 1));
         if (ok) {
             const int quarter = warp & 3, row = 16 * quarter + lane;
             const uint32_t lo = (uint32_t)(32 * quarter) << 16;
@@ -468,24 +476,44 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
                                     pack8_bf16(*reinterpret_cast<const float (*)[8]>(x + 8 * j));
                 }
             } else {
-                // U in blocks of 32 columns, [Dv / 32][64][32]: a lane's 32 columns of a row are
-                // 128 contiguous bytes, and consecutive rows follow each other
-                float *U = p.um + chk * kL * Dv;
-                for (int c0 = 0; c0 < Dv; c0 += 96) {
+                // U in blocks of 32 columns, [Dv / 32][64][32] (a row's 32 columns are 128
+                // contiguous bytes): each block staged as a 128-byte-swizzled box (row r's
+                // 16-byte piece j at r * 128 + ((j ^ (r & 7)) << 4)) and written by a TMA store
+                // from thread 128; up to three boxes per pass, kUSlots slots in a ring
+                const int nb = Dv / 32;
+                auto slot = [&](int i) { return base + (i < 4 ? L.ustg + (size_t)i * 8192 : L.ustg2 + (size_t)(i - 4) * 8192); };
+                for (int c0 = 0, pass = 0; c0 < Dv; c0 += 96, ++pass) {
                     const int n = Dv - c0 < 96 ? Dv - c0 : 96;
                     float x[96];
 #pragma unroll
                     for (int j = 0; j < 3; ++j)
                         if (32 * j < n) tmem_ld32f(tmem + lo + c0 + 32 * j, x + 32 * j);
                     tmem_wait_ld();
+                    if (3 * (pass + 1) > kUSlots) {
+                        // the slots of two passes ago: their stores must have read them
+                        if (tid == 128) bulk_wait_read_but<1>();
+                        named_bar_sync(1, 128);
+                    }
                     if (lane < 16)
 #pragma unroll
-                        for (int j = 0; j < 24; ++j)
-                            if (4 * j < n) {
-                                const int col = c0 + 4 * j;
-                                *reinterpret_cast<float4 *>(U + ((col >> 5) * kL + row) * 32 + (col & 31)) =
-                                    make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                        for (int j = 0; j < 3; ++j)
+                            if (32 * j < n) {
+                                unsigned char *box = slot((c0 / 32 + j) % kUSlots) + row * 128;
+#pragma unroll
+                                for (int q4 = 0; q4 < 8; ++q4)
+                                    *reinterpret_cast<float4 *>(box + ((q4 ^ (row & 7)) << 4)) =
+                                        make_float4(x[32 * j + 4 * q4], x[32 * j + 4 * q4 + 1], x[32 * j + 4 * q4 + 2],
+                                                    x[32 * j + 4 * q4 + 3]);
                             }
+                    fence_proxy_async();
+                    named_bar_sync(1, 128);
+                    if (tid == 128) {
+                        for (int j = 0; j < 3 && 32 * j < n; ++j) {
+                            const int blk = c0 / 32 + j;
+                            tma_store_2d(&tm_u, slot(blk % kUSlots), 0, (int)((chk * nb + blk) * kL));
+                        }
+                        bulk_commit();
+                    }
                 }
             }
         }
@@ -495,6 +523,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
     }
     if (!ok && tid == 0) report_status(p.status, kStatusTimeout);
     cp_async_wait<0>();   // no copy still writes shared memory when the CTA exits
+    if (tid == 32 || tid == 128) bulk_wait_all();   // nor reads it
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -824,12 +853,18 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-size_t chunk_prep_smem(int Dk, int Dv) { return PrepSmem(Dk, Dv).total; }
+size_t chunk_prep_smem(int Dk, int Dv) {
+    const PrepSmem L(Dk, Dv);
+    // the U staging slots must lie inside the regions they reuse
+    const bool fits = L.ustg + (size_t)4 * 8192 <= L.tcu + (size_t)kL * kL * 2 &&
+                      L.ustg2 + (size_t)(kUSlots - 4) * 8192 <= L.ts;
+    return fits ? L.total : ~(size_t)0;
+}
 size_t chunk_sweep_smem(int Dk) { return SweepSmem(Dk).total; }
 
 template <int E>
 static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck, const CUtensorMap &tm_y,
-                                  const CUtensorMap &tm_r, cudaStream_t s) {
+                                  const CUtensorMap &tm_r, const CUtensorMap &tm_u, cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sp = PrepSmem(DK, p.Dv).total, ss = SweepSmem(DK).total;
     cudaError_t err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
@@ -843,7 +878,7 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    chunk_prep_kernel<E><<<units < sms ? units : sms, 256, sp, s>>>(p, units);   // persistent: one CTA per SM
+    chunk_prep_kernel<E><<<units < sms ? units : sms, 256, sp, s>>>(p, units, tm_u);   // persistent: one CTA per SM
     timing_mark("chunk_prep", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
@@ -854,11 +889,11 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck
 }
 
 cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, const CUtensorMap &tm_y,
-                             const CUtensorMap &tm_r, int Dk, cudaStream_t s) {
+                             const CUtensorMap &tm_r, const CUtensorMap &tm_u, int Dk, cudaStream_t s) {
     switch (Dk) {
-        case 64: return launch_chunk_t<2>(p, tm_ck, tm_y, tm_r, s);
-        case 128: return launch_chunk_t<4>(p, tm_ck, tm_y, tm_r, s);
-        case 192: return launch_chunk_t<6>(p, tm_ck, tm_y, tm_r, s);
+        case 64: return launch_chunk_t<2>(p, tm_ck, tm_y, tm_r, tm_u, s);
+        case 128: return launch_chunk_t<4>(p, tm_ck, tm_y, tm_r, tm_u, s);
+        case 192: return launch_chunk_t<6>(p, tm_ck, tm_y, tm_r, tm_u, s);
         default: return cudaErrorInvalidValue;
     }
 }

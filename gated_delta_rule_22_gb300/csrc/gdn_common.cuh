@@ -207,6 +207,11 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Barrier `id` (1-15; 0 is __syncthreads) among the `n` threads (whole warps) that reach it.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -321,6 +326,9 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Wait until this thread's bulk stores have read their shared-memory source (the buffer may be
 // reused), or have completed entirely.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// The same, leaving this thread's N most recent bulk groups possibly still reading.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_but() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // 2-D tiled TMA store of one box from shared memory (the box's layout as the tensor map's
@@ -430,9 +438,10 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // Chunkwise forward: Dk in {64, 128, 192}, Dv a multiple of 64 up to 256, bf16, C = 64.
 // Tensor maps (all written by TMA stores, 128-byte swizzle): tm_ck the fp32 checkpoints as
 // [B*Hv*NC*Dv rows][Dk], box {32, 64}; tm_y y as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1};
-// tm_r v - u as [B][T][Hv][Dv] fp32, box {32, 1, 64, 1}.
+// tm_r v - u as [B][T][Hv][Dv] fp32, box {32, 1, 64, 1}; tm_u U as rows of 32 fp32
+// ([B*Hv*NC*Dv*2 rows][32], each chunk's [Dv/32][64][32] blocks in order), box {32, 64}.
 cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, const CUtensorMap &tm_y,
-                             const CUtensorMap &tm_r, int Dk, cudaStream_t s);
+                             const CUtensorMap &tm_r, const CUtensorMap &tm_u, int Dk, cudaStream_t s);
 size_t chunk_prep_smem(int Dk, int Dv);
 size_t chunk_sweep_smem(int Dk);
 // Chunkwise backward: the reverse sweep over chunks (dS), the per-chunk gradient products
