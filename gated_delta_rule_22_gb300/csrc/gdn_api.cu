@@ -265,8 +265,9 @@ int make_f32_map_2d(CUtensorMap *map, void *ptr, size_t rows, size_t cols, int b
 }
 
 // 4-D tensor map of a row-major [B][T][H][D] tensor (bf16 or fp32), box {box_d, 1, box_t, 1},
-// 128-byte swizzle (box_d * element size must be 128 bytes).
-int make_btd_map(CUtensorMap *map, void *ptr, bool bf16, int B, int T, int H, int D, int box_d, int box_t) {
+// 128-byte swizzle (box_d * element size must then be 128 bytes) or none.
+int make_btd_map(CUtensorMap *map, const void *ptr, bool bf16, int B, int T, int H, int D, int box_d, int box_t,
+                 bool swizzle = true) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) {
         snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available from the driver");
@@ -277,8 +278,38 @@ int make_btd_map(CUtensorMap *map, void *ptr, bool bf16, int B, int T, int H, in
     const cuuint64_t strides[3] = {D * e, (cuuint64_t)H * D * e, (cuuint64_t)T * H * D * e};
     const cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)box_t, 1};
     const cuuint32_t estride[4] = {1, 1, 1, 1};
-    const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr,
-                           dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                           const_cast<void *>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
+// 5-D tensor map of a row-major [B][T][H][D] tensor (bf16 or fp32) whose box lands in shared
+// memory column block by column block: dimensions {inner, T, D / inner, H, B}, box
+// {inner, box_t, box_c, 1, 1}, so that one box holds box_c blocks of `inner` columns, each
+// box_t rows x inner columns contiguous. With bf16 and inner = 8 (no swizzle) that is the
+// core-matrix operand layout of box_t rows; with fp32 and inner = 32 (128-byte swizzle), box_c
+// swizzled [box_t][32] tiles.
+int make_colblock_map(CUtensorMap *map, const void *ptr, bool bf16, int B, int T, int H, int D, int inner, int box_t,
+                      int box_c, bool swizzle) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available from the driver");
+        return GDN_ERR_CUDA;
+    }
+    const cuuint64_t e = bf16 ? 2 : 4;
+    const cuuint64_t dims[5] = {(cuuint64_t)inner, (cuuint64_t)T, (cuuint64_t)(D / inner), (cuuint64_t)H, (cuuint64_t)B};
+    const cuuint64_t strides[4] = {(cuuint64_t)H * D * e, inner * e, D * e, (cuuint64_t)T * H * D * e};
+    const cuuint32_t box[5] = {(cuuint32_t)inner, (cuuint32_t)box_t, (cuuint32_t)box_c, 1, 1};
+    const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5,
+                           const_cast<void *>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
@@ -400,17 +431,16 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.qkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qkm);
         cp.status = fp.status;
         cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
-        CUtensorMap tm_ck, tm_y, tm_r;
-        rc = make_f32_map_2d(&tm_ck, ckpt, (size_t)p.B * p.Hv * p.NC * p.Dv, (size_t)p.Dk, 32, 64);
-        if (rc != GDN_OK) return rc;
-        rc = make_btd_map(&tm_y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64);
-        if (rc != GDN_OK) return rc;
-        rc = make_btd_map(&tm_r, fp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64);
-        if (rc != GDN_OK) return rc;
-        CUtensorMap tm_u;
-        rc = make_f32_map_2d(&tm_u, cp.um, (size_t)p.B * p.Hv * p.NC * 2 * p.Dv, 32, 32, 64);
-        if (rc != GDN_OK) return rc;
-        return cuda_status(gdn::launch_chunk_fwd(cp, tm_ck, tm_y, tm_r, tm_u, p.Dk, (cudaStream_t)stream));
+        gdn::ChunkFwdMaps maps;
+        if ((rc = make_f32_map_2d(&maps.ck, ckpt, (size_t)p.B * p.Hv * p.NC * p.Dv, (size_t)p.Dk, 32, 64)) != GDN_OK ||
+            (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
+            (rc = make_btd_map(&maps.r, fp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64)) != GDN_OK ||
+            (rc = make_f32_map_2d(&maps.u, cp.um, (size_t)p.B * p.Hv * p.NC * 2 * p.Dv, 32, 32, 64)) != GDN_OK ||
+            (rc = make_colblock_map(&maps.v, v, true, p.B, p.T, p.Hv, p.Dv, 8, 64, p.Dv / 8, false)) != GDN_OK ||
+            (rc = make_colblock_map(&maps.k, k, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
+            (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK)
+            return rc;
+        return cuda_status(gdn::launch_chunk_fwd(cp, maps, p.Dk, (cudaStream_t)stream));
     }
     CUtensorMap tm_q, tm_k;
     if ((rc = make_qk_map(&tm_q, q, p, gdn::kFwdTile)) != GDN_OK) return rc;
@@ -464,7 +494,12 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         CUtensorMap tm_dv;
         rc = make_btd_map(&tm_dv, dv, true, p.B, p.T, p.Hv, p.Dv, 64, 64);
         if (rc != GDN_OK) return rc;
-        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, p.Dk, (cudaStream_t)stream));
+        CUtensorMap tm_dy, tm_rs;
+        rc = make_btd_map(&tm_dy, dy, true, p.B, p.T, p.Hv, p.Dv, 8, 64, false);
+        if (rc != GDN_OK) return rc;
+        rc = make_colblock_map(&tm_rs, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true);
+        if (rc != GDN_OK) return rc;
+        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_rs, p.Dk, (cudaStream_t)stream));
     }
     const Workspace w = workspace_layout(p);
 

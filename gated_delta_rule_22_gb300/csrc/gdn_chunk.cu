@@ -53,7 +53,7 @@ struct PrepSmem {
         ustg2 = al(am, 1024);                       // slots 4-5
         vc = o; o += (size_t)2 * kL * Dv * 2;       // V of the chunk, bf16 operand [64][Dv], two buffers (heads alternate)
         lam = o; o += 4 * kL * 4;                   // log g, Lam, exp Lam, beta
-        bar = al(o, 8); o = bar + 8;
+        bar = al(o, 8); o = bar + 3 * 8;            // MMA, copies of V, of K and Q
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -165,7 +165,7 @@ __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid
 // and beta are fetched while the current one computes.
 template <int E>
 __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int units,
-                                                            const __grid_constant__ CUtensorMap tm_u) {
+                                                            const __grid_constant__ ChunkFwdMaps maps) {
     constexpr int DK = 32 * E;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, Hk = p.Hk, NC = p.NC, rep = p.Hv / p.Hk;
@@ -185,12 +185,9 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
     float *Lm = lg + kL;                                      // Lam (inclusive prefix)
     float *gm = Lm + kL;                                      // exp(Lam)
     float *bt = gm + kL;                                      // beta
-    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbV = bar + 1, *cbKQ = bar + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(p.g);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
 
@@ -210,22 +207,23 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
     };
 
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int j = 0; j < 3; ++j) mbar_init(bar + j, 1);
         fence_mbar_init();
+        tma_prefetch_map(&maps.v);
+        tma_prefetch_map(&maps.u);
+    }
+    if (tid == 32) {
+        tma_prefetch_map(&maps.k);
+        tma_prefetch_map(&maps.q);
     }
     if (warp == 0) tmem_alloc(tslot, 512);
-    // V of a unit's chunk into buffer `buf`, in its operand layout, by asynchronous copies
-    // (rows past the end: zeros)
+    // V of a unit's chunk into buffer `buf` in its operand layout, as one TMA box of 1 KB
+    // core-matrix columns (rows past T are zeros). Thread 0 issues it and waits for it.
+    int nV = 0, wV = 0, nKQ = 0, wKQ = 0;
     auto fetch_v = [&](const Unit &x, int buf) {
-        const int nv8 = Dv / 8;
-        unsigned char *dst = vc + (size_t)buf * kL * Dv * 2;
-        for (int e = tid; e < kL * nv8; e += 256) {
-            const int r = e / nv8, ch = e - r * nv8;
-            const int rr = r < x.len ? r : 0;
-            cp_async16(dst + cm_off(r, 16 * ch, kL), v + (((size_t)x.b * T + x.t0 + rr) * Hv + x.h) * Dv + 8 * ch,
-                       r < x.len ? 16 : 0);
-        }
-        cp_async_commit();
+        mbar_expect_tx(cbV, kL * Dv * 2);
+        tma_load_5d(vc + (size_t)buf * kL * Dv * 2, &maps.v, cbV, 0, x.t0, 0, x.h, x.b);
+        ++nV;
     };
     // log g and beta of a unit (warp 0, two steps per lane), raw
     __nv_bfloat16 graw[2], braw[2];
@@ -238,16 +236,15 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
             braw[u] = beta[o];
         }
     };
-    // K and Q of a (batch row, chunk, kv head) into kc and qc in their operand layout, by
-    // asynchronous copies (rows past the end: zeros)
+    // K and Q of a (batch row, chunk, kv head) into kc and qc in their operand layout, a TMA
+    // box each as for V, issued by thread 32 (called by all threads, which all wait for it)
     auto fetch_kq = [&](const Unit &x) {
-        for (int e = tid; e < kL * (DK / 8); e += 256) {
-            const int r = e / (DK / 8), ch = e - r * (DK / 8);
-            const size_t o = (((size_t)x.b * T + x.t0 + (r < x.len ? r : 0)) * Hk + x.hk) * DK + 8 * ch;
-            cp_async16(kc + cm_off(r, 16 * ch, kL), k + o, r < x.len ? 16 : 0);
-            cp_async16(qc + cm_off(r, 16 * ch, kL), q + o, r < x.len ? 16 : 0);
+        if (tid == 32) {
+            mbar_expect_tx(cbKQ, 2 * kL * DK * 2);
+            tma_load_5d(kc, &maps.k, cbKQ, 0, x.t0, 0, x.hk, x.b);
+            tma_load_5d(qc, &maps.q, cbKQ, 0, x.t0, 0, x.hk, x.b);
         }
-        cp_async_commit();
+        ++nKQ;
     };
     unsigned phase = 0;
     bool ok = true;
@@ -257,11 +254,14 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
     // kernel (bulk stores by thread 32, which waits for their reads before kc and qc are
     // refilled)
     auto stage_group = [&](const Unit &x) {
-        cp_async_wait<0>();
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        {
+            const bool w = mbar_wait(cbKQ, wKQ & 1);
+            ++wKQ;
+            tc_fence_before();
+            ok = !__syncthreads_or(!w);
+            tc_fence_after();
+            if (!ok) return;
+        }
         // K K^T -> columns [0, 64), Q K^T -> [64, 128) (M = 64: row m in lane m % 16 + 32 (m / 16))
         if (tid == 0) {
             constexpr uint32_t id = umma_idesc(1, kL, kL);
@@ -305,17 +305,18 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         __syncthreads();
         tc_fence_after();
     };
-    // the first unit's V, K, Q, g and beta go out before anything else
-    if (u_begin < u_end) {
-        const Unit x0 = unit_of(u_begin);
-        fetch_v(x0, 0);
-        fetch_kq(x0);
-        if (warp == 0) fetch_gb(x0);
-    }
+    // the first unit's g and beta go out before anything else, its V, K and Q once the
+    // barriers are initialised
+    if (u_begin < u_end && warp == 0) fetch_gb(unit_of(u_begin));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     tmem = *tslot;
+    if (u_begin < u_end) {
+        const Unit x0 = unit_of(u_begin);
+        if (tid == 0) fetch_v(x0, 0);
+        fetch_kq(x0);
+    }
 
     for (int u = u_begin, i = 0; u < u_end && ok; ++u, ++i) {
         const Unit x = unit_of(u);
@@ -326,13 +327,6 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         }
         const size_t chk = ((size_t)b * Hv + h) * NC + c;   // (b, h, c)
         unsigned char *vch = vc + (size_t)(i & 1) * kL * Dv * 2;
-        // the next unit's V goes out now; this unit's has landed once the older group is done
-        if (u + 1 < u_end) {
-            fetch_v(unit_of(u + 1), (i + 1) & 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
         // log g, beta and the in-chunk prefix Lam (warp 0: two steps per lane, a shuffle scan)
         if (warp == 0) {
             float l2[2], b2[2];
@@ -439,19 +433,26 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // W -> columns [256, 256 + DK), U -> [0, Dv)
+        // W -> columns [256, 256 + DK), U -> [0, Dv) (once this unit's V has landed); then the
+        // next unit's V goes out into the other buffer
+        bool vok = true;
         if (tid == 0) {
-            umma_gemm(tmem + 256, CmOp{tcw, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, true}, kL,
-                      umma_idesc_t(1, kL, DK, false, true), false);
-            umma_gemm(tmem, CmOp{tcu, kL, 0, 0, false}, CmOp{vch, kL, 0, 0, true}, kL,
-                      umma_idesc_t(1, kL, Dv, false, true), false);
-            umma_commit(bar);
+            vok = mbar_wait(cbV, wV & 1);
+            ++wV;
+            if (vok) {
+                umma_gemm(tmem + 256, CmOp{tcw, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, true}, kL,
+                          umma_idesc_t(1, kL, DK, false, true), false);
+                umma_gemm(tmem, CmOp{tcu, kL, 0, 0, false}, CmOp{vch, kL, 0, 0, true}, kL,
+                          umma_idesc_t(1, kL, Dv, false, true), false);
+                umma_commit(bar);
+                if (u + 1 < u_end) fetch_v(unit_of(u + 1), (i + 1) & 1);
+            }
         }
         // when the next unit starts another group, its K and Q are fetched into kc and qc
         // (free once these products are done) while this unit's results are read back
         const bool kq_next = u + 1 < u_end && (u + 1) / rep != u / rep;
         if (tid == 32 && kq_next) bulk_wait_read();   // the stores of K and [Q; K] have read kc, qc
-        ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
+        ok = !__syncthreads_or(!vok || !mbar_wait(bar, phase & 1));
         ++phase;
         tc_fence_after();
         if (ok && kq_next) fetch_kq(unit_of(u + 1));
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
                     if (tid == 128) {
                         for (int j = 0; j < 3 && 32 * j < n; ++j) {
                             const int blk = c0 / 32 + j;
-                            tma_store_2d(&tm_u, slot(blk % kUSlots), 0, (int)((chk * nb + blk) * kL));
+                            tma_store_2d(&maps.u, slot(blk % kUSlots), 0, (int)((chk * nb + blk) * kL));
                         }
                         bulk_commit();
                     }
@@ -521,9 +522,13 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         __syncthreads();
         tc_fence_after();
     }
-    if (!ok && tid == 0) report_status(p.status, kStatusTimeout);
-    cp_async_wait<0>();   // no copy still writes shared memory when the CTA exits
-    if (tid == 32 || tid == 128) bulk_wait_all();   // nor reads it
+    if (!ok && tid == 0) {
+        report_status(p.status, kStatusTimeout);
+        // copies still in flight land before the CTA exits (each wait bounded)
+        if (nV > wV) mbar_wait(cbV, (nV - 1) & 1);
+        if (nKQ > wKQ) mbar_wait(cbKQ, (nKQ - 1) & 1);
+    }
+    if (tid == 32 || tid == 128) bulk_wait_all();   // no store still reads shared memory when the CTA exits
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -623,6 +628,9 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         mbar_init(cbar, 1);
         mbar_init(rbar, 1);
         fence_mbar_init();
+        tma_prefetch_map(&tm_ck);
+        tma_prefetch_map(&tm_y);
+        tma_prefetch_map(&tm_r);
     }
     if (warp == 0) tmem_alloc(tslot, 512);
     tc_fence_before();
@@ -863,8 +871,7 @@ size_t chunk_prep_smem(int Dk, int Dv) {
 size_t chunk_sweep_smem(int Dk) { return SweepSmem(Dk).total; }
 
 template <int E>
-static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck, const CUtensorMap &tm_y,
-                                  const CUtensorMap &tm_r, const CUtensorMap &tm_u, cudaStream_t s) {
+static cudaError_t launch_chunk_t(const ChunkParams &p, const ChunkFwdMaps &maps, cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sp = PrepSmem(DK, p.Dv).total, ss = SweepSmem(DK).total;
     cudaError_t err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
@@ -878,22 +885,21 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tm_ck
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    chunk_prep_kernel<E><<<units < sms ? units : sms, 256, sp, s>>>(p, units, tm_u);   // persistent: one CTA per SM
+    chunk_prep_kernel<E><<<units < sms ? units : sms, 256, sp, s>>>(p, units, maps);   // persistent: one CTA per SM
     timing_mark("chunk_prep", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     timing_mark("chunk_sweep", 0, s);
-    chunk_sweep_kernel<E><<<dim3(p.Dv / kL, p.Hv, p.B), 256, ss, s>>>(p, tm_ck, tm_y, tm_r);
+    chunk_sweep_kernel<E><<<dim3(p.Dv / kL, p.Hv, p.B), 256, ss, s>>>(p, maps.ck, maps.y, maps.r);
     timing_mark("chunk_sweep", 1, s);
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, const CUtensorMap &tm_y,
-                             const CUtensorMap &tm_r, const CUtensorMap &tm_u, int Dk, cudaStream_t s) {
+cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s) {
     switch (Dk) {
-        case 64: return launch_chunk_t<2>(p, tm_ck, tm_y, tm_r, tm_u, s);
-        case 128: return launch_chunk_t<4>(p, tm_ck, tm_y, tm_r, tm_u, s);
-        case 192: return launch_chunk_t<6>(p, tm_ck, tm_y, tm_r, tm_u, s);
+        case 64: return launch_chunk_t<2>(p, maps, s);
+        case 128: return launch_chunk_t<4>(p, maps, s);
+        case 192: return launch_chunk_t<6>(p, maps, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -75,7 +75,7 @@ struct DSweepSmem {
         tm = o; o += (size_t)kL * kL * 2;    // T [64][64] (read MN-major as T^T)
         pm = o; o += (size_t)kL * kL * 2;    // P = (Q K^T) o E_incl [64][64] (read MN-major)
         ydu = o; o += (size_t)2 * 2 * kL * kL * 2;   // [dY; dU] block [128][64 v] (rows 0-63 dY, 64-127 dU), two buffers
-        rsm = o; o += (size_t)kL * 68 * 4;       // v - u block [64 t][64 v], fp32, row stride 68
+        rsm = alb(o, 1024); o = rsm + (size_t)2 * kL * 128;   // v - u block, fp32: two [64 t][32 v] boxes in the 128-byte swizzle
         lms = o; o += (size_t)2 * kL * 4;        // Lam, two buffers
         shi = o; o += (size_t)kL * DK * 2;   // dS, bf16 high part [64 v][DK]
         slo = o; o += (size_t)kL * DK * 2;   // dS - high part, bf16
@@ -84,7 +84,7 @@ struct DSweepSmem {
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
         vec = o; o += 4 * kL * 4;            // Lam, E(L, .), beta, -
         red = o; o += 2 * 2 * kL * 4;        // [f | dbeta][half][64]
-        bar = alb(o, 8); o = bar + 4 * 8;    // MMA, copies of (K^T, P, Qs), of T, of Ks
+        bar = alb(o, 8); o = bar + 5 * 8;    // MMA, copies of (K^T, P, Qs), of T, of Ks, of (dY, v - u, Lam)
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -99,7 +99,9 @@ struct DSweepSmem {
 //   [DK, DK + 64)      K dS^T, then dD (chunk row t, value column of this block)
 //   [DK + 64, DK + 128) P^T dY
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, const __grid_constant__ CUtensorMap tm_dv) {
+__global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, const __grid_constant__ CUtensorMap tm_dv,
+                                                              const __grid_constant__ CUtensorMap tm_dy,
+                                                              const __grid_constant__ CUtensorMap tm_rs) {
     constexpr int DK = 32 * E;
     static_assert(DK + 128 <= 512, "tensor memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -120,10 +122,9 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     float *Lm = reinterpret_cast<float *>(base + L.vec), *eL = Lm + kL, *bt = eL + kL;
     float *red = reinterpret_cast<float *>(base + L.red);   // [2][2][64]
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
-    uint64_t *cbA = bar + 1, *cbT = bar + 2, *cbK = bar + 3;
+    uint64_t *cbA = bar + 1, *cbT = bar + 2, *cbK = bar + 3, *cbY = bar + 4;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
-    const __nv_bfloat16 *dy = static_cast<const __nv_bfloat16 *>(p.dy);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t head = (size_t)b * Hv + h;
 
@@ -151,8 +152,11 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     };
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(bar + i, 1);
+        for (int i = 0; i < 5; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
+        tma_prefetch_map(&tm_dy);
+        tma_prefetch_map(&tm_rs);
+        tma_prefetch_map(&tm_dv);
     }
     if (warp == 0) tmem_alloc(tslot, 512);
     tc_fence_before();
@@ -176,26 +180,25 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     }
     unsigned ph = 0, cph = 0;
     bool ok = true;
-    // a chunk's dY block (into the dY rows of a [dY; dU] buffer), its v - u and Lam arrive by
-    // asynchronous copies one chunk ahead; beta (threads < 64) by a load one chunk ahead
+    // a chunk's dY block (into the dY rows of a [dY; dU] buffer: one TMA box per 8 value
+    // columns, a 1 KB core-matrix column), its v - u (one TMA box of two 128-byte-swizzled
+    // [64][32] tiles) and Lam (a bulk copy) arrive one chunk ahead, issued by thread 0 (rows
+    // past T: zeros); beta
+    // (threads < 64) by a load one chunk ahead
     __nv_bfloat16 btn = __float2bfloat16_rn(0.f);   // raw: converted where it is used, so that the load does not stall here
+    int nY = 0, wY = 0;
     auto fetch_chunk = [&](int cc, int buf) {
         const int tt0 = cc * kL, ln = min(kL, T - tt0);
-        const size_t rb = (size_t)b * T + tt0;
-        unsigned char *yb = ydu2 + (size_t)buf * 2 * kL * kL * 2;
+        if (tid == 0) {
+            unsigned char *yb = ydu2 + (size_t)buf * 2 * kL * kL * 2;
+            mbar_expect_tx(cbY, kL * kL * 2 + kL * kL * 4 + kL * 4);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int e = tid + 256 * u, t = e >> 3, j = e & 7, tt = t < ln ? t : 0;
-            cp_async16(yb + cm_off(t, 16 * j, 2 * kL), dy + ((rb + tt) * Hv + h) * Dv + r0 + 8 * j, t < ln ? 16 : 0);
+            for (int j = 0; j < 8; ++j) tma_load_4d(yb + j * 2 * kL * 16, &tm_dy, cbY, r0 + 8 * j, h, tt0, b);
+            tma_load_5d(rsm, &tm_rs, cbY, 0, tt0, r0 / 32, h, b);
+            bulk_load(lms + buf * kL, p.lam + (head * p.NC + cc) * kL, kL * 4, cbY);
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = tid + 256 * u, t = e >> 4, j = e & 15, tt = t < ln ? t : 0;
-            cp_async16(rsm + t * 68 + 4 * j, p.resid + ((rb + tt) * Hv + h) * Dv + r0 + 4 * j, t < ln ? 16 : 0);
-        }
-        if (tid < 16) cp_async16(lms + buf * kL + 4 * tid, p.lam + (head * p.NC + cc) * kL + 4 * tid, 16);
-        cp_async_commit();
-        if (tid < kL) btn = beta[(rb + (tid < ln ? tid : 0)) * Hv + h];
+        ++nY;
+        if (tid < kL) btn = beta[((size_t)b * T + tt0 + (tid < ln ? tid : 0)) * Hv + h];
     };
     if (tid == 0) { copy_A(p.NC - 1); copy_T(p.NC - 1); copy_K(p.NC - 1); }
     fetch_chunk(p.NC - 1, 0);
@@ -205,15 +208,22 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         const size_t rowbase = (size_t)b * T + t0;          // (b, t0) row of [B, T, ...]
         const int buf = (p.NC - 1 - c) & 1;
         unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;   // [dY; dU] of this chunk
-        cp_async_wait<0>();                                 // this chunk's dY, v - u and Lam have landed
-        if (tid < kL) bt[tid] = tid < len ? __bfloat162float(btn) : 0.f;
-        __syncthreads();
+        {
+            // this chunk's dY, v - u and Lam have landed (every thread reads them)
+            const bool w = mbar_wait(cbY, wY & 1);
+            ++wY;
+            if (tid < kL) bt[tid] = tid < len ? __bfloat162float(btn) : 0.f;
+            ok = !__syncthreads_or(!w);
+            if (!ok) break;
+        }
         if (tid < kL) Lm[tid] = lms[buf * kL + tid];
-        // this lane's v - u (row lrow, 32 value columns)
+        // this lane's v - u (row lrow, 32 value columns: box `half`, 16-byte piece i of the row
+        // at ((i ^ (row & 7)) << 4))
         float rs[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float4 f4 = rowlane ? *reinterpret_cast<const float4 *>(rsm + lrow * 68 + half * 32 + 4 * i)
+            const float4 f4 = rowlane ? *reinterpret_cast<const float4 *>(reinterpret_cast<const unsigned char *>(rsm) +
+                                                                          half * kL * 128 + lrow * 128 + ((i ^ (lrow & 7)) << 4))
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
             rs[4 * i] = f4.x; rs[4 * i + 1] = f4.y; rs[4 * i + 2] = f4.z; rs[4 * i + 3] = f4.w;
         }
@@ -399,6 +409,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         if (nA > (int)cph) mbar_wait(cbA, (nA - 1) & 1);
         if (nT > (int)cph) mbar_wait(cbT, (nT - 1) & 1);
         if (nK > (int)cph) mbar_wait(cbK, (nK - 1) & 1);
+        if (nY > wY) mbar_wait(cbY, (nY - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -854,7 +865,8 @@ size_t chunk_dsweep_smem(int Dk) { return DSweepSmem(Dk).total; }
 size_t chunk_grad_smem(int Dk, int Dv) { return GradSmem(Dk, Dv).total; }
 
 template <int E>
-static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap &tm_dv, cudaStream_t s) {
+static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
+                                      const CUtensorMap &tm_rs, cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sd = DSweepSmem(DK).total, sg = GradSmem(DK, p.Dv).total;
     cudaError_t err = cudaFuncSetAttribute(chunk_dsweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd);
@@ -862,7 +874,7 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     err = cudaFuncSetAttribute(chunk_grad_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_dsweep", 0, s);
-    chunk_dsweep_kernel<E><<<dim3(p.nsplit, p.Hv, p.B), 256, sd, s>>>(p, tm_dv);
+    chunk_dsweep_kernel<E><<<dim3(p.nsplit, p.Hv, p.B), 256, sd, s>>>(p, tm_dv, tm_dy, tm_rs);
     timing_mark("chunk_dsweep", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
@@ -887,11 +899,12 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, int Dk, cudaStream_t s) {
+cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
+                             const CUtensorMap &tm_rs, int Dk, cudaStream_t s) {
     switch (Dk) {
-        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, s);
-        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, s);
-        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, s);
+        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, tm_dy, tm_rs, s);
+        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, tm_dy, tm_rs, s);
+        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_rs, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -251,6 +251,21 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// 5-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
+                                            int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], "
+        "[%7];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Fetch a tensor map (a kernel parameter) into the descriptor cache ahead of its first use.
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -436,18 +451,25 @@ size_t bwd_smem_bytes(int Dk, int C, int dtype, int slots);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // Chunkwise forward: Dk in {64, 128, 192}, Dv a multiple of 64 up to 256, bf16, C = 64.
-// Tensor maps (all written by TMA stores, 128-byte swizzle): tm_ck the fp32 checkpoints as
-// [B*Hv*NC*Dv rows][Dk], box {32, 64}; tm_y y as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1};
-// tm_r v - u as [B][T][Hv][Dv] fp32, box {32, 1, 64, 1}; tm_u U as rows of 32 fp32
-// ([B*Hv*NC*Dv*2 rows][32], each chunk's [Dv/32][64][32] blocks in order), box {32, 64}.
-cudaError_t launch_chunk_fwd(const ChunkParams &p, const CUtensorMap &tm_ck, const CUtensorMap &tm_y,
-                             const CUtensorMap &tm_r, const CUtensorMap &tm_u, int Dk, cudaStream_t s);
+// Tensor maps. Written by TMA stores, 128-byte swizzle: ck the fp32 checkpoints as
+// [B*Hv*NC*Dv rows][Dk], box {32, 64}; y as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1}; r (v - u)
+// as [B][T][Hv][Dv] fp32, box {32, 1, 64, 1}; u (U) as rows of 32 fp32 ([B*Hv*NC*Dv*2
+// rows][32], each chunk's [Dv/32][64][32] blocks in order), box {32, 64}. Read by TMA loads,
+// no swizzle, box {8, 1, 64, 1} (one 1 KB core-matrix column of 64 rows): v as
+// [B][T][Hv][Dv], k and q as [B][T][Hk][Dk], bf16.
+struct ChunkFwdMaps {
+    CUtensorMap ck, y, r, u, v, k, q;
+};
+cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s);
 size_t chunk_prep_smem(int Dk, int Dv);
 size_t chunk_sweep_smem(int Dk);
 // Chunkwise backward: the reverse sweep over chunks (dS), the per-chunk gradient products
 // and the fixed-order sums over value heads and row blocks.
-// tm_dv: 4-D tensor map of dv as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1}, 128-byte swizzle.
-cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, int Dk, cudaStream_t s);
+// 4-D tensor maps of [B][T][Hv][Dv] tensors: tm_dv dv (bf16, box {64, 1, 64, 1}, 128-byte
+// swizzle); tm_dy dy (bf16, box {8, 1, 64, 1}, no swizzle); tm_rs v - u (fp32, box
+// {32, 1, 64, 1}, 128-byte swizzle).
+cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
+                             const CUtensorMap &tm_rs, int Dk, cudaStream_t s);
 size_t chunk_dsweep_smem(int Dk);
 size_t chunk_grad_smem(int Dk, int Dv);
 cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s);
