@@ -66,7 +66,7 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 
 // ------------------------------------------------------------------ reverse sweep (dS)
 struct DSweepSmem {
-    size_t kt, qs, ks, tm, pm, ydu, rsm, lms, shi, slo, rhs, dls, dvs, vec, red, bar, tslot, total;
+    size_t kt, qs, ks, tm, pm, ydu, rsm, lms, shl, rhs, dls, dvs, vec, red, bar, tslot, total;
     __host__ __device__ DSweepSmem(int DK) {
         size_t o = 0;
         kt = o; o += (size_t)kL * DK * 2;    // K [64][DK]
@@ -77,8 +77,7 @@ struct DSweepSmem {
         ydu = o; o += (size_t)2 * 2 * kL * kL * 2;   // [dY; dU] block [128][64 v] (rows 0-63 dY, 64-127 dU), two buffers
         rsm = alb(o, 1024); o = rsm + (size_t)2 * kL * 128;   // v - u block, fp32: two [64 t][32 v] boxes in the 128-byte swizzle
         lms = o; o += (size_t)2 * kL * 4;        // Lam, two buffers
-        shi = o; o += (size_t)kL * DK * 2;   // dS, bf16 high part [64 v][DK]
-        slo = o; o += (size_t)kL * DK * 2;   // dS - high part, bf16
+        shl = o; o += (size_t)2 * kL * DK * 2;   // dS as [high; low] bf16 parts [128][DK] (rows 0-63 high, 64-127 dS - high)
         rhs = o; o += (size_t)kL * kL * 2;   // diag(E_L) K dS^T + P^T dY [64 t][64 v]
         dls = o; o += (size_t)kL * kL * 2;   // Delta block [64 t][64 v], for the gradient kernel
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
@@ -95,15 +94,16 @@ struct DSweepSmem {
 
 // One CTA per (block of 64 value rows, value head, batch row), over the chunks in reverse.
 // Tensor memory (M = 64 layout: row r in lane r % 16 + 32 (r / 16)):
-//   [0, DK)            dS (value rows of this block)
-//   [DK, DK + 64)      K dS^T, then dD (chunk row t, value column of this block)
-//   [DK + 64, DK + 128) P^T dY
+//   [0, DK)              dS (value rows of this block)
+//   [DK, DK + 128)       K [dS_high; dS_low]^T (one N = 128 product: chunk row t, value column
+//                        of the high part, then of the low part); then dD in the first 64
+//   [DK + 128, DK + 192) P^T dY
 template <int E>
 __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, const __grid_constant__ CUtensorMap tm_dv,
                                                               const __grid_constant__ CUtensorMap tm_dy,
                                                               const __grid_constant__ CUtensorMap tm_rs) {
     constexpr int DK = 32 * E;
-    static_assert(DK + 128 <= 512, "tensor memory");
+    static_assert(DK + 192 <= 512, "tensor memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, r0 = split * kL, nsplit = p.nsplit;
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
     const DSweepSmem L(DK);
     unsigned char *kt = base + L.kt, *qs = base + L.qs, *ks = base + L.ks, *tmm = base + L.tm, *pmm = base + L.pm;
-    unsigned char *ydu2 = base + L.ydu, *shi = base + L.shi, *slo = base + L.slo, *rhs = base + L.rhs, *dls = base + L.dls;
+    unsigned char *ydu2 = base + L.ydu, *shl = base + L.shl, *rhs = base + L.rhs, *dls = base + L.dls;
     unsigned char *dvs = base + L.dvs;
     float *rsm = reinterpret_cast<float *>(base + L.rsm), *lms = reinterpret_cast<float *>(base + L.lms);
     float *Lm = reinterpret_cast<float *>(base + L.vec), *eL = Lm + kL, *bt = eL + kL;
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tS = tmem, tX = tmem + DK, tP = tmem + DK + 64;
+    const uint32_t tS = tmem, tX = tmem + DK, tP = tmem + DK + 128;
     constexpr int SC = DK / 2;                              // state columns per warp half
 
     // dS_T into tensor memory
@@ -231,8 +231,10 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
         const float decay = expf(Lm[kL - 1]);
         // ---- dS (the adjoint of the chunk-end state) as operands (high and low bf16 parts),
-        // stored for the gradient kernel; then dS <- exp(Lam_L) dS in place
+        // the high part also stored for the gradient kernel ([64][DK] operand layout: a warp's
+        // 16 rows of one K chunk are 256 contiguous bytes); then dS <- exp(Lam_L) dS in place
         {
+            unsigned char *dsl_g = reinterpret_cast<unsigned char *>(p.ws_dsl + (chk * nsplit + split) * kL * DK);
             // all of this thread's columns loaded from tensor memory before one wait
             float xs[SC];
 #pragma unroll
@@ -248,9 +250,10 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
                         lo[i] = xs[8 * j + i] - hi[i];
                     }
                     const uint4 hu = pack8(hi);
-                    const uint32_t o = cm_off(lrow, 2 * (half * SC + 8 * j), kL);
-                    *reinterpret_cast<uint4 *>(shi + o) = hu;
-                    *reinterpret_cast<uint4 *>(slo + o) = pack8(lo);
+                    const int kb = 2 * (half * SC + 8 * j);
+                    *reinterpret_cast<uint4 *>(shl + cm_off(lrow, kb, 2 * kL)) = hu;
+                    *reinterpret_cast<uint4 *>(shl + cm_off(kL + lrow, kb, 2 * kL)) = pack8(lo);
+                    *reinterpret_cast<uint4 *>(dsl_g + cm_off(lrow, kb, kL)) = hu;
                 }
             }
 #pragma unroll
@@ -266,18 +269,14 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbA, cph & 1));
         if (!ok) break;
-        // ---- K dS^T (high + low), P^T dY, dS += dY^T diag(exp Lam) Q
+        // ---- K [dS_high; dS_low]^T (N = 128), P^T dY, dS += dY^T diag(exp Lam) Q
         if (tid == 0) {
-            constexpr uint32_t idX = umma_idesc_t(1, kL, kL, false, false);
+            constexpr uint32_t idX = umma_idesc_t(1, kL, 2 * kL, false, false);
             constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
             constexpr uint32_t idS = umma_idesc_t(1, kL, DK, true, true);
-            umma_gemm(tX, CmOp{kt, kL, 0, 0, false}, CmOp{shi, kL, 0, 0, false}, DK, idX, false);
-            umma_gemm(tX, CmOp{kt, kL, 0, 0, false}, CmOp{slo, kL, 0, 0, false}, DK, idX, true);
+            umma_gemm(tX, CmOp{kt, kL, 0, 0, false}, CmOp{shl, 2 * kL, 0, 0, false}, DK, idX, false);
             umma_gemm(tP, CmOp{pmm, kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false);
             umma_gemm(tS, CmOp{ydu, 2 * kL, 0, 0, true}, CmOp{qs, kL, 0, 0, true}, kL, idS, true);
-            // dS at the chunk end (its bf16 high part) for the gradient kernel
-            bulk_store(p.ws_dsl + (chk * nsplit + split) * kL * DK, shi, kL * DK * 2);
-            bulk_commit();
             umma_commit(bar);
         }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
@@ -286,12 +285,13 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         if (!ok) break;
         // ---- rhs = diag(E_L) K dS^T + P^T dY as an operand; f partial = beta_t (v_t - u_t) . (dS k_t)
         {
-            float x[32], y2[32];
-            tmem_ld16f(tX + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(x));
-            tmem_ld16f(tX + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(x + 16));
-            tmem_ld16f(tP + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(y2));
-            tmem_ld16f(tP + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(y2 + 16));
+            float x[32], xl[32], y2[32];
+            tmem_ld32f(tX + lane_off + half * 32, x);
+            tmem_ld32f(tX + lane_off + kL + half * 32, xl);
+            tmem_ld32f(tP + lane_off + half * 32, y2);
             tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] += xl[i];           // K dS^T = K dS_high^T + K dS_low^T
             if (rowlane) {
                 const float el = eL[lrow];
                 float fs = 0.f;

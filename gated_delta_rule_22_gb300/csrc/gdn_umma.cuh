@@ -109,9 +109,14 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
 // of 16), operands at their K offsets (bytes) ka0 / kb0.
 __device__ __forceinline__ void umma_gemm_bf16(uint32_t d_tmem, const void *A, int arows, int ka0, const void *B,
                                                int brows, int kb0, int K, uint32_t idesc, bool accumulate) {
+    // each step of 16 columns moves a descriptor's start address by two K chunks (rows * 32
+    // bytes; the start field counts 16-byte units): the descriptors are built once and advanced
+    uint64_t a = umma_desc(A, arows, ka0), b = umma_desc(B, brows, kb0);
+    const uint64_t da = (uint64_t)(2 * arows), db = (uint64_t)(2 * brows);
     for (int k = 0; k < K; k += 16) {
-        umma_bf16(d_tmem, umma_desc(A, arows, ka0 + 2 * k), umma_desc(B, brows, kb0 + 2 * k), idesc,
-                  accumulate || k > 0);
+        umma_bf16(d_tmem, a, b, idesc, accumulate || k > 0);
+        a += da;
+        b += db;
     }
 }
 
@@ -131,7 +136,15 @@ struct CmOp {
 // the instruction descriptor must carry the same orientations.
 __device__ __forceinline__ void umma_gemm(uint32_t d_tmem, const CmOp &A, const CmOp &B, int K, uint32_t idesc,
                                           bool accumulate) {
-    for (int k = 0; k < K; k += 16) umma_bf16(d_tmem, A.desc(k), B.desc(k), idesc, accumulate || k > 0);
+    // a step of 16 along K advances a K-major operand by two K chunks (R * 32 bytes) and an
+    // MN-major one by two row groups (256 bytes); in the 16-byte units of the start field
+    uint64_t a = A.desc(0), b = B.desc(0);
+    const uint64_t da = A.mn ? 16u : (uint64_t)(2 * A.R), db = B.mn ? 16u : (uint64_t)(2 * B.R);
+    for (int k = 0; k < K; k += 16) {
+        umma_bf16(d_tmem, a, b, idesc, accumulate || k > 0);
+        a += da;
+        b += db;
+    }
 }
 
 // 32x32b tensor-memory load of 16 consecutive columns.
