@@ -76,21 +76,19 @@ size_t ckpt_resid_bytes(const Plan &p) { return (size_t)p.B * p.T * p.Hv * p.Dv 
 
 // With the chunkwise forward the buffer continues (each part from a 256-byte boundary) with
 // the per-chunk data of every (b, h, chunk): Lam [64] fp32, the sweep's bf16 operands in their
-// core-matrix layout ((Q K^T) o E and (K K^T) o E [64][64], W, diag(exp Lam) Q,
-// diag(exp Lam) K [64][Dk]; K [64][Dk] per kv head) and U fp32 in [Dv/32][64][32] blocks.
+// core-matrix layout ([(Q K^T) o E; (K K^T) o E] [128][64], W [64][Dk], [diag(exp Lam) Q;
+// diag(exp Lam) K] [128][Dk]; K [64][Dk] per kv head) and U fp32 in [Dv/32][64][32] blocks.
 struct ChunkLayout {
-    size_t lam, pm, kkm, wm, qsm, ksm, ktm, um, tm, s0m, qkm, end;
+    size_t lam, pkm, wm, qksm, ktm, um, tm, s0m, qkm, end;
 };
 ChunkLayout chunk_layout(const Plan &p) {
     const size_t n = (size_t)p.B * p.Hv * p.NC * 64;   // chunk rows
     ChunkLayout c;
     size_t o = ckpt_state_bytes(p) + round_up(ckpt_resid_bytes(p));
     c.lam = o; o += round_up(n * 4);
-    c.pm = o; o += round_up(n * 64 * 2);
-    c.kkm = o; o += round_up(n * 64 * 2);
+    c.pkm = o; o += round_up(n * 2 * 64 * 2);
     c.wm = o; o += round_up(n * p.Dk * 2);
-    c.qsm = o; o += round_up(n * p.Dk * 2);
-    c.ksm = o; o += round_up(n * p.Dk * 2);
+    c.qksm = o; o += round_up(n * 2 * p.Dk * 2);
     c.ktm = o; o += round_up((size_t)p.B * p.Hk * p.NC * 64 * p.Dk * 2);   // per kv head
     c.um = o; o += round_up(n * p.Dv * 4);
     c.tm = o; o += round_up(n * 64 * 2);
@@ -419,11 +417,9 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.S0 = S0; cp.y = y; cp.S_T = S_T;
         cp.ckpt = ckpt; cp.resid = fp.resid;
         cp.lam = reinterpret_cast<float *>(sb + cl.lam);
-        cp.pm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.pm);
-        cp.kkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.kkm);
+        cp.pkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.pkm);
         cp.wm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.wm);
-        cp.qsm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qsm);
-        cp.ksm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.ksm);
+        cp.qksm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qksm);
         cp.ktm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.ktm);
         cp.um = reinterpret_cast<float *>(sb + cl.um);
         cp.tm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tm);
@@ -472,9 +468,8 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
         cp.lam = reinterpret_cast<const float *>(sb + cl.lam);
         cp.tm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.tm);
-        cp.pm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.pm);
-        cp.qsm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qsm);
-        cp.ksm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.ksm);
+        cp.pkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.pkm);
+        cp.qksm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qksm);
         cp.ktm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.ktm);
         cp.s0m = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.s0m);
         cp.qkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qkm);

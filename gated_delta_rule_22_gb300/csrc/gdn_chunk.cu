@@ -357,10 +357,10 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         }
         if (tid == 128 && Dv > 128) bulk_wait_read();   // the last unit's U boxes have left A
         __syncthreads();
-        // A, and the decay-weighted Q K^T (i <= t) and K K^T (i < t) as bf16 operands in their
-        // core-matrix layout: 16-byte chunk e holds row e % 64, columns 8 (e / 64) .. + 7
-        __nv_bfloat16 *P = p.pm + chk * kL * kL;
-        __nv_bfloat16 *KKm = p.kkm + chk * kL * kL;
+        // A, and the decay-weighted Q K^T (i <= t) and K K^T (i < t) as bf16 operands stacked
+        // in one 128-row core-matrix layout: columns 8 j .. + 7 of row t are 16-byte piece
+        // 128 j + t (P) and 128 j + 64 + t (KKm)
+        uint4 *PK = reinterpret_cast<uint4 *>(p.pkm + chk * 2 * kL * kL);
         for (int e = tid; e < kL * 8; e += 256) {
             const int t = e & (kL - 1), i0 = 8 * (e >> 6);
             float kk8[8], qk8[8], a8[8], pv[8], kv8[8];
@@ -379,24 +379,26 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
             }
             *reinterpret_cast<float4 *>(am + t * kP + i0) = *reinterpret_cast<const float4 *>(a8);
             *reinterpret_cast<float4 *>(am + t * kP + i0 + 4) = *reinterpret_cast<const float4 *>(a8 + 4);
-            reinterpret_cast<uint4 *>(P)[e] = pack8_bf16(pv);
-            reinterpret_cast<uint4 *>(KKm)[e] = pack8_bf16(kv8);
+            PK[(e >> 6) * 2 * kL + t] = pack8_bf16(pv);
+            PK[(e >> 6) * 2 * kL + kL + t] = pack8_bf16(kv8);
         }
-        // diag(exp Lam) Q and diag(exp Lam) K (row scaling of the staged operands)
+        // [diag(exp Lam) Q; diag(exp Lam) K] (row scaling of the staged operands), one 128-row
+        // operand: piece e of Q (K chunk e / 64, row e % 64) goes to 128 (e / 64) + e % 64,
+        // that of K 64 pieces later
         {
-            uint4 *Qg = reinterpret_cast<uint4 *>(p.qsm + chk * kL * DK);
-            uint4 *Kg = reinterpret_cast<uint4 *>(p.ksm + chk * kL * DK);
+            uint4 *QK = reinterpret_cast<uint4 *>(p.qksm + chk * 2 * kL * DK);
             for (int e = tid; e < kL * DK / 8; e += 256) {
+                const int o = (e >> 6) * 2 * kL + (e & (kL - 1));
                 const float gr = gm[e & (kL - 1)];
                 float a[8];
                 unpack8_bf16(reinterpret_cast<const uint4 *>(qc)[e], a);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) a[j] *= gr;
-                Qg[e] = pack8_bf16(a);
+                QK[o] = pack8_bf16(a);
                 unpack8_bf16(reinterpret_cast<const uint4 *>(kc)[e], a);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) a[j] *= gr;
-                Kg[e] = pack8_bf16(a);
+                QK[o + kL] = pack8_bf16(a);
             }
         }
         if (tid == 128) bulk_wait_read();   // the last unit's U boxes have left T and the T operands
@@ -542,15 +544,13 @@ namespace gdn {
 namespace {
 
 struct SweepSmem {
-    size_t wc, qs, ks, kt, pc, kkc, sop, dt, de, dtile, ckst, ysg, vec, bar, tslot, total;
+    size_t wc, qks, kt, pkc, sop, dt, de, dtile, ckst, ysg, vec, bar, tslot, total;
     __host__ __device__ SweepSmem(int DK) {
         size_t o = 0;
         wc = o; o += (size_t)kL * DK * 2;     // W of the chunk        A [64][DK]
-        qs = o; o += (size_t)kL * DK * 2;     // diag(exp Lam) Q       A [64][DK]
-        ks = o; o += (size_t)kL * DK * 2;     // diag(exp Lam) K       A [64][DK]
+        qks = o; o += (size_t)2 * kL * DK * 2;   // [diag(exp Lam) Q; diag(exp Lam) K]   A [128][DK]
         kt = o; o += (size_t)kL * DK * 2;     // K (read MN-major)     B [64][DK]
-        pc = o; o += (size_t)kL * kL * 2;     // (Q K^T) o E_incl      A [64][64]
-        kkc = o; o += (size_t)kL * kL * 2;    // (K K^T) o E_strict    A [64][64]
+        pkc = o; o += (size_t)2 * kL * kL * 2;   // [(Q K^T) o E_incl; (K K^T) o E_strict]   A [128][64]
         sop = o; o += (size_t)kL * DK * 2;    // S (64 value rows)     B [64][DK]
         dt = o; o += (size_t)kL * kL * 2;     // Delta^T               B [64][64]
         de = o; o += (size_t)kL * kL * 2;     // (diag(E_L) Delta)^T   A [64][64]
@@ -568,19 +568,19 @@ struct SweepSmem {
 }  // namespace
 
 // One CTA per (64-row block of the state, value head, batch row), carrying that block of the
-// state through the chunks. Tensor memory (fp32 accumulators, M = 64 layout):
-//   [0, DK)             the state S (value row r in lane r % 16 + 32 (r / 16)); per chunk it is
-//                       scaled by exp(Lam_L) in place and the update (diag(E_L) Delta)^T K is
-//                       accumulated onto it by MMA
-//   [DK, DK + 64)       y of the chunk (chunk row t in the lane of t)
-//   [DK + 64, DK + 128) the prediction u of the chunk
-//   [DK + 128, DK + 192) W S^T
+// state through the chunks. Tensor memory (fp32 accumulators):
+//   [0, DK)             the state S (M = 64: value row r in lane r % 16 + 32 (r / 16)); per
+//                       chunk it is scaled by exp(Lam_L) in place and the update
+//                       (diag(E_L) Delta)^T K is accumulated onto it by MMA
+//   [DK, DK + 64)       [y; u] of the chunk, one M = 128 product of the stacked operands: chunk
+//                       row t of y in lane t, of the prediction u in lane 64 + t
+//   [DK + 64, DK + 128) W S^T (M = 64)
 template <int E>
 __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ CUtensorMap tm_ck,
                                                              const __grid_constant__ CUtensorMap tm_y,
                                                              const __grid_constant__ CUtensorMap tm_r) {
     constexpr int DK = 32 * E;
-    static_assert(DK + 192 <= 512, "tensor memory holds the state, y, u and W S^T");
+    static_assert(DK + 128 <= 512, "tensor memory holds the state, [y; u] and W S^T");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, r0 = split * kL;
@@ -591,8 +591,8 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 1024));
     const SweepSmem L(DK);
-    unsigned char *wc = base + L.wc, *qs = base + L.qs, *ks = base + L.ks, *kt = base + L.kt;
-    unsigned char *pc = base + L.pc, *kkc = base + L.kkc, *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
+    unsigned char *wc = base + L.wc, *qks = base + L.qks, *kt = base + L.kt, *pkc = base + L.pkc;
+    unsigned char *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
     float *dtile = reinterpret_cast<float *>(base + L.dtile);
     unsigned char *ckst = base + L.ckst, *ysg = base + L.ysg;
     unsigned char *rsg = dt;                                // v - u of a chunk, fp32 [2][64][32] in the 128-byte swizzle (dt, de)
@@ -615,11 +615,9 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     auto issue_r = [&](int cc) {
         const size_t ck = head * p.NC + cc;
         mbar_expect_tx(rbar, 3 * kBig + 2 * kSmall);
-        bulk_load(qs, p.qsm + ck * kL * DK, kBig, rbar);
-        bulk_load(ks, p.ksm + ck * kL * DK, kBig, rbar);
+        bulk_load(qks, p.qksm + ck * 2 * kL * DK, 2 * kBig, rbar);
         bulk_load(kt, p.ktm + (((size_t)b * p.Hk + h / (Hv / p.Hk)) * p.NC + cc) * kL * DK, kBig, rbar);
-        bulk_load(pc, p.pm + ck * kL * kL, kSmall, rbar);
-        bulk_load(kkc, p.kkm + ck * kL * kL, kSmall, rbar);
+        bulk_load(pkc, p.pkm + ck * 2 * kL * kL, 2 * kSmall, rbar);
         ++ncr;
     };
 
@@ -637,7 +635,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tS = tmem, tY = tmem + DK, tU = tmem + DK + 64, tD = tmem + DK + 128;
+    const uint32_t tS = tmem, tYU = tmem + DK, tD = tmem + DK + 64;
     constexpr int SC = DK / 2;                              // state columns per warp half
 
     // the start state into tensor memory
@@ -663,37 +661,39 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         for (int i = 0; i < 8; ++i)
             ux[i] = lane < 16 ? reinterpret_cast<const float4 *>(Ug)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     };
+    // v for the threads that form v - u (warps of row quarters 2 and 3: chunk row
+    // 32 (quarter - 2) + lane, this half's 32 value columns)
     auto load_v = [&](int cc) {
-        const int tt0 = cc * kL, ln = min(kL, T - tt0);
-        const size_t o = (((size_t)b * T + tt0 + lrow) * Hv + h) * Dv + r0 + half * 32;
-        const bool mine = lane < 16 && lrow < ln;
+        const int tt0 = cc * kL, ln = min(kL, T - tt0), t = 32 * (quarter & 1) + lane;
+        const size_t o = (((size_t)b * T + tt0 + t) * Hv + h) * Dv + r0 + half * 32;
+        const bool mine = quarter >= 2 && t < ln;
 #pragma unroll
         for (int i = 0; i < 4; ++i) vx[i] = mine ? reinterpret_cast<const uint4 *>(v + o)[i] : make_uint4(0u, 0u, 0u, 0u);
     };
-    // y and v - u of chunk cc, from tensor memory (their columns are rewritten only by the next
-    // chunk's second group of products), staged in the 128-byte swizzle for TMA stores: y in its
-    // own tile, v - u in the Delta^T operand buffers (free until this chunk's operands are
-    // built; thread 0 waits for the stores' reads before that). Rows past T are clipped by the
-    // stores.
+    // y and v - u of chunk cc, from tensor memory (its columns are rewritten only by the next
+    // chunk's second group of products), staged in the 128-byte swizzle for TMA stores: y (row
+    // quarters 0-1 of [y; u]) in its own tile, v - u (quarters 2-3) in the Delta^T operand
+    // buffers (free until this chunk's operands are built; thread 0 waits for the stores' reads
+    // before that). Rows past T are clipped by the stores.
     auto epilogue = [&](int cc) {
-        float yv[32], uv[32];
-        tmem_ld32f(tY + lane_off + half * 32, yv);
-        tmem_ld32f(tU + lane_off + half * 32, uv);
+        float x[32];
+        tmem_ld32f(tYU + lane_off + half * 32, x);
         tmem_wait_ld();
-        if (lane < 16) {
-            const int t = lrow, sw = t & 7;
+        const int t = 32 * (quarter & 1) + lane, sw = t & 7;
+        if (quarter < 2) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 *reinterpret_cast<uint4 *>(ysg + t * 128 + (((half * 4 + j) ^ sw) << 4)) =
-                    pack8_bf16(*reinterpret_cast<const float (*)[8]>(yv + 8 * j));
+                    pack8_bf16(*reinterpret_cast<const float (*)[8]>(x + 8 * j));
+        } else {
             float va[32];
 #pragma unroll
             for (int j = 0; j < 4; ++j) unpack8_bf16(vx[j], *reinterpret_cast<float (*)[8]>(va + 8 * j));
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 *reinterpret_cast<float4 *>(rsg + half * (kL * 128) + t * 128 + ((j ^ sw) << 4)) =
-                    make_float4(va[4 * j] - uv[4 * j], va[4 * j + 1] - uv[4 * j + 1], va[4 * j + 2] - uv[4 * j + 2],
-                                va[4 * j + 3] - uv[4 * j + 3]);
+                    make_float4(va[4 * j] - x[4 * j], va[4 * j + 1] - x[4 * j + 1], va[4 * j + 2] - x[4 * j + 2],
+                                va[4 * j + 3] - x[4 * j + 3]);
         }
         fence_proxy_async();
         __syncthreads();
@@ -815,13 +815,11 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         ++cph;
         tc_fence_after();
         if (!ok) break;
-        // ---- y = Qs S^T + P Delta;  u = Ks S^T + KKm Delta;  update = (E_L Delta)^T K
+        // ---- [y; u] = [Qs; Ks] S^T + [P; KKm] Delta (M = 128);  update = (E_L Delta)^T K
         if (tid == 0) {
-            constexpr uint32_t id64 = umma_idesc(1, kL, kL);
-            umma_gemm_bf16(tY, qs, kL, 0, sop, kL, 0, DK, id64, false);
-            umma_gemm_bf16(tY, pc, kL, 0, dt, kL, 0, kL, id64, true);
-            umma_gemm_bf16(tU, ks, kL, 0, sop, kL, 0, DK, id64, false);
-            umma_gemm_bf16(tU, kkc, kL, 0, dt, kL, 0, kL, id64, true);
+            constexpr uint32_t id128 = umma_idesc(1, 2 * kL, kL);
+            umma_gemm(tYU, CmOp{qks, 2 * kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id128, false);
+            umma_gemm(tYU, CmOp{pkc, 2 * kL, 0, 0, false}, CmOp{dt, kL, 0, 0, false}, kL, id128, true);
             umma_gemm(tS, CmOp{de, kL, 0, 0, false}, CmOp{kt, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, false, true), true);
             umma_commit(bar);
         }

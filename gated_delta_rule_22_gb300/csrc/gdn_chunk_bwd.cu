@@ -66,14 +66,13 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 
 // ------------------------------------------------------------------ reverse sweep (dS)
 struct DSweepSmem {
-    size_t kt, qs, ks, tm, pm, ydu, rsm, lms, shl, rhs, dls, dvs, vec, red, bar, tslot, total;
+    size_t kt, qks, tm, pkm, ydu, rsm, lms, shl, rhs, dls, dvs, vec, red, bar, tslot, total;
     __host__ __device__ DSweepSmem(int DK) {
         size_t o = 0;
         kt = o; o += (size_t)kL * DK * 2;    // K [64][DK]
-        qs = o; o += (size_t)kL * DK * 2;    // diag(exp Lam) Q [64][DK] (read MN-major)
-        ks = o; o += (size_t)kL * DK * 2;    // diag(exp Lam) K [64][DK] (read MN-major)
+        qks = o; o += (size_t)2 * kL * DK * 2;   // [diag(exp Lam) Q; diag(exp Lam) K] [128][DK] (read MN-major)
         tm = o; o += (size_t)kL * kL * 2;    // T [64][64] (read MN-major as T^T)
-        pm = o; o += (size_t)kL * kL * 2;    // P = (Q K^T) o E_incl [64][64] (read MN-major)
+        pkm = o; o += (size_t)2 * kL * kL * 2;   // [P; KKm] [128][64], P = (Q K^T) o E_incl (read MN-major)
         ydu = o; o += (size_t)2 * 2 * kL * kL * 2;   // [dY; dU] block [128][64 v] (rows 0-63 dY, 64-127 dU), two buffers
         rsm = alb(o, 1024); o = rsm + (size_t)2 * kL * 128;   // v - u block, fp32: two [64 t][32 v] boxes in the 128-byte swizzle
         lms = o; o += (size_t)2 * kL * 4;        // Lam, two buffers
@@ -83,7 +82,7 @@ struct DSweepSmem {
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
         vec = o; o += 4 * kL * 4;            // Lam, E(L, .), beta, -
         red = o; o += 2 * 2 * kL * 4;        // [f | dbeta][half][64]
-        bar = alb(o, 8); o = bar + 5 * 8;    // MMA, copies of (K^T, P, Qs), of T, of Ks, of (dY, v - u, Lam)
+        bar = alb(o, 8); o = bar + 5 * 8;    // MMA, copies of (K, P), of T, of [Qs; Ks], of (dY, v - u, Lam)
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -115,7 +114,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
     const DSweepSmem L(DK);
-    unsigned char *kt = base + L.kt, *qs = base + L.qs, *ks = base + L.ks, *tmm = base + L.tm, *pmm = base + L.pm;
+    unsigned char *kt = base + L.kt, *qks = base + L.qks, *tmm = base + L.tm, *pmm = base + L.pkm;
     unsigned char *ydu2 = base + L.ydu, *shl = base + L.shl, *rhs = base + L.rhs, *dls = base + L.dls;
     unsigned char *dvs = base + L.dvs;
     float *rsm = reinterpret_cast<float *>(base + L.rsm), *lms = reinterpret_cast<float *>(base + L.lms);
@@ -132,10 +131,9 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     int nA = 0, nT = 0, nK = 0;
     auto copy_A = [&](int cc) {
         const size_t ck = head * p.NC + cc;
-        mbar_expect_tx(cbA, 2 * kL * DK * 2 + kL * kL * 2);
+        mbar_expect_tx(cbA, kL * DK * 2 + 2 * kL * kL * 2);
         bulk_load(kt, p.ktm + (((size_t)b * p.Hk + h / (Hv / p.Hk)) * p.NC + cc) * kL * DK, kL * DK * 2, cbA);
-        bulk_load(qs, p.qsm + ck * kL * DK, kL * DK * 2, cbA);
-        bulk_load(pmm, p.pm + ck * kL * kL, kL * kL * 2, cbA);
+        bulk_load(pmm, p.pkm + ck * 2 * kL * kL, 2 * kL * kL * 2, cbA);
         ++nA;
     };
     auto copy_T = [&](int cc) {
@@ -146,8 +144,8 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     };
     auto copy_K = [&](int cc) {
         const size_t ck = head * p.NC + cc;
-        mbar_expect_tx(cbK, kL * DK * 2);
-        bulk_load(ks, p.ksm + ck * kL * DK, kL * DK * 2, cbK);
+        mbar_expect_tx(cbK, 2 * kL * DK * 2);
+        bulk_load(qks, p.qksm + ck * 2 * kL * DK, 2 * kL * DK * 2, cbK);
         ++nK;
     };
 
@@ -269,14 +267,12 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbA, cph & 1));
         if (!ok) break;
-        // ---- K [dS_high; dS_low]^T (N = 128), P^T dY, dS += dY^T diag(exp Lam) Q
+        // ---- K [dS_high; dS_low]^T (N = 128), P^T dY (P: rows 0-63 of [P; KKm])
         if (tid == 0) {
             constexpr uint32_t idX = umma_idesc_t(1, kL, 2 * kL, false, false);
             constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
-            constexpr uint32_t idS = umma_idesc_t(1, kL, DK, true, true);
             umma_gemm(tX, CmOp{kt, kL, 0, 0, false}, CmOp{shl, 2 * kL, 0, 0, false}, DK, idX, false);
-            umma_gemm(tP, CmOp{pmm, kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false);
-            umma_gemm(tS, CmOp{ydu, 2 * kL, 0, 0, true}, CmOp{qs, kL, 0, 0, true}, kL, idS, true);
+            umma_gemm(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false);
             umma_commit(bar);
         }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
@@ -317,7 +313,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // the buffers of K^T, P and Qs are free: the previous chunk's copies go out now
+        // the buffers of K and [P; KKm] are free: the previous chunk's copies go out now
         if (tid == 0 && c > 0) copy_A(c - 1);
         if (tid < kL && tid < len) p.ws_f[((rowbase + tid) * Hv + h) * nsplit + split] = red[tid] + red[kL + tid];
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbT, cph & 1));
@@ -366,10 +362,10 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
             p.ws_db[((rowbase + tid) * Hv + h) * nsplit + split] = red[2 * kL + tid] + red[3 * kL + tid];
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbK, cph & 1));
         if (!ok) break;
-        // ---- dS += dU^T diag(exp Lam) K
+        // ---- dS += [dY; dU]^T [diag(exp Lam) Q; diag(exp Lam) K] (K = 128)
         if (tid == 0) {
-            umma_gemm(tS, CmOp{ydu, 2 * kL, 0, kL, true}, CmOp{ks, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, true, true),
-                      true);
+            umma_gemm(tS, CmOp{ydu, 2 * kL, 0, 0, true}, CmOp{qks, 2 * kL, 0, 0, true}, 2 * kL,
+                      umma_idesc_t(1, kL, DK, true, true), true);
             // [dY; dU] and Delta of the block for the gradient kernel, and dv
             const size_t blk = chk * nsplit + split;
             bulk_store(p.ws_yu + blk * 2 * kL * kL, ydu, 2 * kL * kL * 2);

@@ -75,8 +75,8 @@ static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <=
 // saved buffer: lam, the in-chunk log-decay prefix [64]; um, U fp32 in column blocks
 // [Dv / 32][64][32]; and the sweep's
 // tensor-core operands, bf16 in their shared-memory (core-matrix) layout: wm W [64][Dk],
-// qsm diag(exp Lam) Q [64][Dk], ksm diag(exp Lam) K [64][Dk], ktm K [64][Dk] (per kv head),
-// pm (Q K^T) o E_incl [64][64], kkm (K K^T) o E_strict [64][64], tm T = (I + A)^-1 [64][64];
+// qksm [diag(exp Lam) Q; diag(exp Lam) K] [128][Dk], ktm K [64][Dk] (per kv head),
+// pkm [(Q K^T) o E_incl; (K K^T) o E_strict] [128][64], tm T = (I + A)^-1 [64][64];
 // per (b, h, chunk, block of 64 value rows) s0m, the chunk-start state in bf16 [64][Dk]; and
 // per (b, kv head, chunk) qkm, [Q; K] of the chunk [128][Dk].
 struct ChunkParams {
@@ -85,7 +85,7 @@ struct ChunkParams {
     void *y;
     float *S_T, *ckpt, *resid;
     float *lam;
-    __nv_bfloat16 *pm, *kkm, *wm, *qsm, *ksm, *ktm, *tm, *s0m, *qkm;
+    __nv_bfloat16 *pkm, *wm, *qksm, *ktm, *tm, *s0m, *qkm;
     float *um;
     int *status;
     int B, T, Hk, Hv, Dv, NC;
@@ -96,7 +96,7 @@ struct ChunkParams {
 struct ChunkBwdParams {
     const void *dy, *beta;
     const float *resid, *lam;
-    const __nv_bfloat16 *tm, *pm, *qsm, *ksm, *ktm, *s0m, *qkm;
+    const __nv_bfloat16 *tm, *pkm, *qksm, *ktm, *s0m, *qkm;
     const float *dS_T;
     float *dS0;
     void *dv, *dg, *dq, *dk, *dbeta;
