@@ -23,7 +23,6 @@ namespace {
 
 constexpr int kL = 64;           // chunk length of the tensor-core forward
 constexpr int kP = 68;           // row of prep's fp32 64 x 64 work matrices (16-byte aligned, conflict-free float4 columns)
-constexpr int kPad = kL + 1;     // row of the sweep's fp32 64 x 64 tile
 // Both kernels hold all 512 tensor-memory columns, so each must be alone on its SM: they ask
 // for more than half of the shared memory.
 constexpr size_t kOneCtaSmem = 120 * 1024;
@@ -544,7 +543,7 @@ namespace gdn {
 namespace {
 
 struct SweepSmem {
-    size_t wc, qks, kt, pkc, sop, dt, de, dtile, ckst, ysg, vec, bar, tslot, total;
+    size_t wc, qks, kt, pkc, sop, dt, de, ckst, ysg, rsg, vec, bar, tslot, total;
     __host__ __device__ SweepSmem(int DK) {
         size_t o = 0;
         wc = o; o += (size_t)kL * DK * 2;     // W of the chunk        A [64][DK]
@@ -552,11 +551,11 @@ struct SweepSmem {
         kt = o; o += (size_t)kL * DK * 2;     // K (read MN-major)     B [64][DK]
         pkc = o; o += (size_t)2 * kL * kL * 2;   // [(Q K^T) o E_incl; (K K^T) o E_strict]   A [128][64]
         sop = o; o += (size_t)kL * DK * 2;    // S (64 value rows)     B [64][DK]
-        dt = o; o += (size_t)kL * kL * 2;     // Delta^T               B [64][64]
-        de = o; o += (size_t)kL * kL * 2;     // (diag(E_L) Delta)^T   A [64][64]
-        dtile = o; o += (size_t)kL * kPad * 4; // Delta, fp32 [64][65]
+        dt = o; o += (size_t)kL * kL * 2;     // Delta [64 t][64 v], read MN-major (B)
+        de = o; o += (size_t)kL * kL * 2;     // diag(E_L) Delta [64 t][64 v], read MN-major (A, transposed)
         ckst = al(o, 1024); o = ckst + (size_t)kL * DK * 4;   // chunk-start state, fp32, boxes of [64][32] in the 128-byte swizzle
         ysg = al(o, 1024); o = ysg + (size_t)kL * 128;       // y of a chunk, bf16 [64][64] in the 128-byte swizzle
+        rsg = al(o, 1024); o = rsg + (size_t)2 * kL * 128;   // v - u of a chunk, fp32 [2][64][32] in the 128-byte swizzle
         vec = o; o += 3 * kL * 4;             // Lam, exp Lam, E(L, .)
         bar = al(o, 8); o = bar + 24;         // MMA completion, the two groups of operand copies
         tslot = o; o += 16;
@@ -593,9 +592,8 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     const SweepSmem L(DK);
     unsigned char *wc = base + L.wc, *qks = base + L.qks, *kt = base + L.kt, *pkc = base + L.pkc;
     unsigned char *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
-    float *dtile = reinterpret_cast<float *>(base + L.dtile);
     unsigned char *ckst = base + L.ckst, *ysg = base + L.ysg;
-    unsigned char *rsg = dt;                                // v - u of a chunk, fp32 [2][64][32] in the 128-byte swizzle (dt, de)
+    unsigned char *rsg = base + L.rsg;
     float *Lm = reinterpret_cast<float *>(base + L.vec), *gm = Lm + kL, *eL = gm + kL;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbar = bar + 1, *rbar = bar + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
@@ -672,9 +670,8 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     };
     // y and v - u of chunk cc, from tensor memory (its columns are rewritten only by the next
     // chunk's second group of products), staged in the 128-byte swizzle for TMA stores: y (row
-    // quarters 0-1 of [y; u]) in its own tile, v - u (quarters 2-3) in the Delta^T operand
-    // buffers (free until this chunk's operands are built; thread 0 waits for the stores' reads
-    // before that). Rows past T are clipped by the stores.
+    // quarters 0-1 of [y; u]) and v - u (quarters 2-3), each in its own tile (thread 0 waits
+    // for the stores' reads at the next chunk's start). Rows past T are clipped by the stores.
     auto epilogue = [&](int cc) {
         float x[32];
         tmem_ld32f(tYU + lane_off + half * 32, x);
@@ -718,7 +715,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
             gm[tid] = expf(lamn);
             if (c + 1 < p.NC) lamn = p.lam[(chk + 1) * kL + tid];
         }
-        if (tid == 0) bulk_wait_read();                     // the previous chunk's stores have read sop and ckst
+        if (tid == 0) bulk_wait_read();                     // the earlier stores have read sop, ckst, ysg and rsg
         __syncthreads();
         if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
         // ---- the state as an operand, and the chunk-start checkpoint staged for TMA stores (all
@@ -781,34 +778,30 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         if (!ok) break;
         if (tid == 0 && c + 1 < p.NC) issue_w(c + 1);      // W's buffer is free again
         {
-            // Delta = U - W S^T into an fp32 tile
+            // Delta = U - W S^T, straight into the operands Delta and diag(E_L) Delta, stored as
+            // [t][v] (row t of the lane, 8 value columns per 16-byte piece) and read MN-major:
+            // Delta as the B of [P; KKm] Delta, diag(E_L) Delta as the (transposed) A of the update
             float x[32];
-            tmem_ld16f(tD + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(x));
-            tmem_ld16f(tD + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(x + 16));
+            tmem_ld32f(tD + lane_off + half * 32, x);
             tmem_wait_ld();
             if (lane < 16) {
                 const float *uf = reinterpret_cast<const float *>(ux);
+                const float el = eL[lrow];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) dtile[lrow * kPad + half * 32 + i] = uf[i] - x[i];
+                for (int j = 0; j < 4; ++j) {
+                    float a[8], bb[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        a[i] = uf[8 * j + i] - x[8 * j + i];
+                        bb[i] = el * a[i];
+                    }
+                    const uint32_t o = cm_off(lrow, 2 * (half * 32 + 8 * j), kL);
+                    *reinterpret_cast<uint4 *>(dt + o) = pack8_bf16(a);
+                    *reinterpret_cast<uint4 *>(de + o) = pack8_bf16(bb);
+                }
             }
         }
         if (c + 1 < p.NC) load_u(c + 1);                   // the next chunk's U, used one chunk later
-        if (tid == 0) bulk_wait_read();                     // the y and v - u stores have read dt, de and ysg
-        tc_fence_before();
-        __syncthreads();
-        // Delta^T and (diag(E_L) Delta)^T as operands: value column n, eight chunk rows per store
-        for (int e = tid; e < kL * 8; e += 256) {
-            const int n = e & (kL - 1), ch = e >> 6;        // consecutive threads: consecutive columns
-            float a[8], bb[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = 8 * ch + i;
-                a[i] = dtile[t * kPad + n];
-                bb[i] = eL[t] * a[i];
-            }
-            *reinterpret_cast<uint4 *>(dt + cm_off(n, 16 * ch, kL)) = pack8_bf16(a);
-            *reinterpret_cast<uint4 *>(de + cm_off(n, 16 * ch, kL)) = pack8_bf16(bb);
-        }
         fence_proxy_async();
         // the rest of the chunk's operands (copied a chunk ahead)
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(rbar, cph & 1));
@@ -819,8 +812,9 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         if (tid == 0) {
             constexpr uint32_t id128 = umma_idesc(1, 2 * kL, kL);
             umma_gemm(tYU, CmOp{qks, 2 * kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id128, false);
-            umma_gemm(tYU, CmOp{pkc, 2 * kL, 0, 0, false}, CmOp{dt, kL, 0, 0, false}, kL, id128, true);
-            umma_gemm(tS, CmOp{de, kL, 0, 0, false}, CmOp{kt, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, false, true), true);
+            umma_gemm(tYU, CmOp{pkc, 2 * kL, 0, 0, false}, CmOp{dt, kL, 0, 0, true}, kL,
+                      umma_idesc_t(1, 2 * kL, kL, false, true), true);
+            umma_gemm(tS, CmOp{de, kL, 0, 0, true}, CmOp{kt, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, true, true), true);
             umma_commit(bar);
         }
         load_v(c);                                          // for this chunk's epilogue, one chunk later
