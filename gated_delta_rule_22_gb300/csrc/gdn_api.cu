@@ -316,6 +316,30 @@ int make_colblock_map(CUtensorMap *map, const void *ptr, bool bf16, int B, int T
     return GDN_OK;
 }
 
+// 5-D tensor map of the [Q; K] buffer of the chunkwise forward (nblk blocks of [128][Dk] bf16
+// in the core-matrix layout: K chunk j holds 64 rows of Q, then 64 rows of K): dimensions
+// {8, 64 rows, Dk / 8 chunks, 2 halves, nblk}, box {8, 64, Dk / 8, 1, 1}, so that one box is a
+// [64][Dk] operand tile of Q or of K.
+int make_qkm_map(CUtensorMap *map, void *ptr, size_t nblk, int Dk) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available from the driver");
+        return GDN_ERR_CUDA;
+    }
+    const cuuint64_t dims[5] = {8, 64, (cuuint64_t)(Dk / 8), 2, (cuuint64_t)nblk};
+    const cuuint64_t strides[4] = {16, 128 * 16, 64 * 16, (cuuint64_t)128 * Dk * 2};
+    const cuuint32_t box[5] = {8, 64, (cuuint32_t)(Dk / 8), 1, 1};
+    const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, ptr, dims, strides, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 }  // namespace
 
 namespace gdn {
@@ -434,7 +458,8 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
             (rc = make_f32_map_2d(&maps.u, cp.um, (size_t)p.B * p.Hv * p.NC * 2 * p.Dv, 32, 32, 64)) != GDN_OK ||
             (rc = make_colblock_map(&maps.v, v, true, p.B, p.T, p.Hv, p.Dv, 8, 64, p.Dv / 8, false)) != GDN_OK ||
             (rc = make_colblock_map(&maps.k, k, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
-            (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK)
+            (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
+            (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK)
             return rc;
         return cuda_status(gdn::launch_chunk_fwd(cp, maps, p.Dk, (cudaStream_t)stream));
     }
@@ -490,7 +515,7 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         rc = make_btd_map(&tm_dv, dv, true, p.B, p.T, p.Hv, p.Dv, 64, 64);
         if (rc != GDN_OK) return rc;
         CUtensorMap tm_dy, tm_rs;
-        rc = make_btd_map(&tm_dy, dy, true, p.B, p.T, p.Hv, p.Dv, 8, 64, false);
+        rc = make_colblock_map(&tm_dy, dy, true, p.B, p.T, p.Hv, p.Dv, 8, 128, 8, false);
         if (rc != GDN_OK) return rc;
         rc = make_colblock_map(&tm_rs, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true);
         if (rc != GDN_OK) return rc;

@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
     if (tid == 32) {
         tma_prefetch_map(&maps.k);
         tma_prefetch_map(&maps.q);
+        tma_prefetch_map(&maps.qk);
     }
     if (warp == 0) tmem_alloc(tslot, 512);
     // V of a unit's chunk into buffer `buf` in its operand layout, as one TMA box of 1 KB
@@ -270,17 +271,12 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         }
         if (tid == 32) {
             // K in its operand layout (for both sweeps), and [Q; K] in the gradient kernel's
-            // 128-row layout (K chunk j: the 64 rows of Q, then the 64 rows of K). A group split
-            // between two CTAs is written by both, alike.
+            // 128-row layout (K chunk j: the 64 rows of Q, then the 64 rows of K; a TMA store of
+            // each half). A group split between two CTAs is written by both, alike.
             const size_t ckv = ((size_t)x.b * Hk + x.hk) * NC + x.c;
             bulk_store(p.ktm + ckv * kL * DK, kc, kL * DK * 2);
-            if (p.qkm != nullptr) {
-                __nv_bfloat16 *QKg = p.qkm + ckv * 2 * kL * DK;
-                for (int j = 0; j < DK / 8; ++j) {
-                    bulk_store(QKg + (size_t)j * 2 * kL * 8, qc + j * kL * 16, kL * 16);
-                    bulk_store(QKg + (size_t)j * 2 * kL * 8 + kL * 8, kc + j * kL * 16, kL * 16);
-                }
-            }
+            tma_store_5d(&maps.qk, qc, 0, 0, 0, 0, (int)ckv);
+            tma_store_5d(&maps.qk, kc, 0, 0, 0, 1, (int)ckv);
             bulk_commit();
         }
         ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));

@@ -178,10 +178,8 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     }
     unsigned ph = 0, cph = 0;
     bool ok = true;
-    // a chunk's dY block (into the dY rows of a [dY; dU] buffer: one TMA box per 8 value
-    // columns, a 1 KB core-matrix column), its v - u (one TMA box of two 128-byte-swizzled
-    // [64][32] tiles) and Lam (a bulk copy) arrive one chunk ahead, issued by thread 0 (rows
-    // past T: zeros); beta
+    // a chunk's dY block, its v - u (one TMA box of two 128-byte-swizzled [64][32] tiles) and
+    // Lam (a bulk copy) arrive one chunk ahead, issued by thread 0 (rows past T: zeros); beta
     // (threads < 64) by a load one chunk ahead
     __nv_bfloat16 btn = __float2bfloat16_rn(0.f);   // raw: converted where it is used, so that the load does not stall here
     int nY = 0, wY = 0;
@@ -189,9 +187,11 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         const int tt0 = cc * kL, ln = min(kL, T - tt0);
         if (tid == 0) {
             unsigned char *yb = ydu2 + (size_t)buf * 2 * kL * kL * 2;
-            mbar_expect_tx(cbY, kL * kL * 2 + kL * kL * 4 + kL * 4);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) tma_load_4d(yb + j * 2 * kL * 16, &tm_dy, cbY, r0 + 8 * j, h, tt0, b);
+            // dY: one box of 128 rows in the [dY; dU] operand layout (8 core-matrix columns of
+            // 128 rows); rows 64-127 (the following steps) land in the dU rows, which the chunk
+            // rewrites before reading them
+            mbar_expect_tx(cbY, 2 * kL * kL * 2 + kL * kL * 4 + kL * 4);
+            tma_load_5d(yb, &tm_dy, cbY, 0, tt0, r0 / 8, h, b);
             tma_load_5d(rsm, &tm_rs, cbY, 0, tt0, r0 / 32, h, b);
             bulk_load(lms + buf * kL, p.lam + (head * p.NC + cc) * kL, kL * 4, cbY);
         }
@@ -491,13 +491,12 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         int b, c, h;
         chunk_of(u, b, c, h);
         const size_t chk = ((size_t)b * Hv + h) * NC + c;
+        // the row blocks of a unit are adjacent in the workspace and in shared memory
         mbar_expect_tx(cbA, (unsigned)nsplit * (kYub + kDlb + kSb));
-        for (int s = 0; s < nsplit; ++s) {
-            const size_t blk = chk * nsplit + s;
-            bulk_load(yu + (size_t)s * kYub, p.ws_yu + blk * 2 * kL * kL, kYub, cbA);
-            bulk_load(dl + (size_t)s * kDlb, p.ws_dl + blk * kL * kL, kDlb, cbA);
-            bulk_load(dsl + (size_t)s * kSb, p.ws_dsl + blk * kL * DK, kSb, cbA);
-        }
+        const size_t blk = chk * nsplit;
+        bulk_load(yu, p.ws_yu + blk * 2 * kL * kL, (unsigned)nsplit * kYub, cbA);
+        bulk_load(dl, p.ws_dl + blk * kL * kL, (unsigned)nsplit * kDlb, cbA);
+        bulk_load(dsl, p.ws_dsl + blk * kL * DK, (unsigned)nsplit * kSb, cbA);
         ++nA;
     };
     auto copy_s = [&](int u) {            // S0 of unit u
@@ -505,7 +504,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         chunk_of(u, b, c, h);
         const size_t chk = ((size_t)b * Hv + h) * NC + c;
         mbar_expect_tx(cbS, (unsigned)nsplit * kSb);
-        for (int s = 0; s < nsplit; ++s) bulk_load(s0 + (size_t)s * kSb, p.s0m + (chk * nsplit + s) * kL * DK, kSb, cbS);
+        bulk_load(s0, p.s0m + chk * nsplit * kL * DK, (unsigned)nsplit * kSb, cbS);
         ++nS;
     };
     auto copy_q = [&](int u) {            // [Q; K] of unit u's chunk and kv head

@@ -355,6 +355,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
                  : "memory");
 }
 
+// 5-D tiled TMA store of one box from shared memory, in the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, const void *src, int c0, int c1, int c2, int c3,
+                                             int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_addr(src))
+        : "memory");
+}
+
 // 4-D tiled TMA store of one box from shared memory, in the issuing thread's bulk async-group.
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int c0, int c1, int c2,
                                              int c3) {
@@ -456,18 +466,21 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // as [B][T][Hv][Dv] fp32, box {32, 1, 64, 1}; u (U) as rows of 32 fp32 ([B*Hv*NC*Dv*2
 // rows][32], each chunk's [Dv/32][64][32] blocks in order), box {32, 64}. Read by TMA loads,
 // no swizzle, box {8, 1, 64, 1} (one 1 KB core-matrix column of 64 rows): v as
-// [B][T][Hv][Dv], k and q as [B][T][Hk][Dk], bf16.
+// [B][T][Hv][Dv], k and q as [B][T][Hk][Dk], bf16. Written by TMA stores from an operand
+// tile of 64 rows: qk, the [Q; K] buffer as {8, 64 rows, Dk / 8 chunks, 2 halves (Q, K),
+// B*Hk*NC blocks}, box {8, 64, Dk / 8, 1, 1}.
 struct ChunkFwdMaps {
-    CUtensorMap ck, y, r, u, v, k, q;
+    CUtensorMap ck, y, r, u, v, k, q, qk;
 };
 cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s);
 size_t chunk_prep_smem(int Dk, int Dv);
 size_t chunk_sweep_smem(int Dk);
 // Chunkwise backward: the reverse sweep over chunks (dS), the per-chunk gradient products
 // and the fixed-order sums over value heads and row blocks.
-// 4-D tensor maps of [B][T][Hv][Dv] tensors: tm_dv dv (bf16, box {64, 1, 64, 1}, 128-byte
-// swizzle); tm_dy dy (bf16, box {8, 1, 64, 1}, no swizzle); tm_rs v - u (fp32, box
-// {32, 1, 64, 1}, 128-byte swizzle).
+// Tensor maps of [B][T][Hv][Dv] tensors: tm_dv dv (bf16, 4-D, box {64, 1, 64, 1}, 128-byte
+// swizzle); tm_dy dy (bf16, 5-D column blocks {8, T, Dv / 8, Hv, B}, box {8, 128, 8, 1, 1}, no
+// swizzle); tm_rs v - u (fp32, 5-D column blocks {32, T, Dv / 32, Hv, B}, box
+// {32, 64, 2, 1, 1}, 128-byte swizzle).
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
                              const CUtensorMap &tm_rs, int Dk, cudaStream_t s);
 size_t chunk_dsweep_smem(int Dk);
