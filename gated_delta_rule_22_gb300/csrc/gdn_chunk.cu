@@ -694,8 +694,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
             const int tt0 = cc * kL;
             tma_store_4d(&tm_y, ysg, r0, h, tt0, b);
             if (p.resid != nullptr) {
-                tma_store_4d(&tm_r, rsg, r0, h, tt0, b);
-                tma_store_4d(&tm_r, rsg + kL * 128, r0 + 32, h, tt0, b);
+                tma_store_5d(&tm_r, rsg, 0, tt0, r0 / 32, h, b);
             }
             bulk_commit();
         }
@@ -757,7 +756,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
             if (p.s0m != nullptr) bulk_store(p.s0m + (chk * gridDim.x + split) * kL * DK, sop, kL * DK * 2);
             if (p.ckpt != nullptr)
 #pragma unroll
-                for (int bx = 0; bx < DK / 32; ++bx) tma_store_2d(&tm_ck, ckst + bx * (kL * 128), 32 * bx, (int)(chk * Dv + r0));
+                tma_store_5d(&tm_ck, ckst, 0, (int)(chk * Dv + r0), 0, 0, 0);
             bulk_commit();
         }
         // ---- W S^T

@@ -461,10 +461,12 @@ size_t bwd_smem_bytes(int Dk, int C, int dtype, int slots);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // Chunkwise forward: Dk in {64, 128, 192}, Dv a multiple of 64 up to 256, bf16, C = 64.
-// Tensor maps. Written by TMA stores, 128-byte swizzle: ck the fp32 checkpoints as
-// [B*Hv*NC*Dv rows][Dk], box {32, 64}; y as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1}; r (v - u)
-// as [B][T][Hv][Dv] fp32, box {32, 1, 64, 1}; u (U) as rows of 32 fp32 ([B*Hv*NC*Dv*2
-// rows][32], each chunk's [Dv/32][64][32] blocks in order), box {32, 64}. Read by TMA loads,
+// Tensor maps. Written by TMA stores, 128-byte swizzle: ck the fp32 checkpoints as 5-D column
+// blocks {32, B*Hv*NC*Dv rows, Dk / 32, 1, 1}, box {32, 64, Dk / 32, 1, 1} (a 64-row block of
+// one chunk-start state); y as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1}; r (v - u) as 5-D
+// column blocks of [B][T][Hv][Dv] fp32 {32, T, Dv / 32, Hv, B}, box {32, 64, 2, 1, 1}; u (U)
+// as rows of 32 fp32 ([B*Hv*NC*Dv*2 rows][32], each chunk's [Dv/32][64][32] blocks in
+// order), box {32, 64}. Read by TMA loads,
 // no swizzle, box {8, 1, 64, 1} (one 1 KB core-matrix column of 64 rows): v as
 // [B][T][Hv][Dv], k and q as [B][T][Hk][Dk], bf16. Written by TMA stores from an operand
 // tile of 64 rows: qk, the [Q; K] buffer as {8, 64 rows, Dk / 8 chunks, 2 halves (Q, K),
