@@ -122,12 +122,16 @@ def kernel_model(w):
         + ch * (L * Dv * 2 + Dv * Dk * 2 + 2 * L * Dv * 2 + L * Dv * 2) + 2 * rows * nsplit * 4
         + rows * 2 + (st if w.with_dST else 0) + st,
         ch * (2 * 2 * L * Dv * Dk + 2 * L * Dv * L * 2 + 2 * Dv * Dk * L * 2), 0.0)
+    # value-head groups split between gradient CTAs (one CTA per SM, at most one per unit):
+    # at most one per CTA boundary; their per-head fp32 partials go through chunk_reduce
+    n_split = min(ch, 152) - 1
+    split_bytes = n_split * (Hv // Hk) * 2 * L * Dk * 4
     m["chunk_grad"] = (
         ck * 2 * L * Dk * 2 + ch * (2 * L * Dv * 2 + L * Dv * 2 + 2 * Dv * Dk * 2 + L * 4)
-        + rows * (2 + nsplit * 4) + 2 * rows * Dk * 4 + rows * 2,
+        + rows * (2 + 2 * nsplit * 4) + 2 * rows * 2 + 2 * B * T * Hk * Dk * 2 + split_bytes,
         ch * 2 * (2 * L * L * Dk + 2 * L * L * Dv + 2 * L * Dk * Dv + L * Dk * Dv + 2 * L * Dk * L
                   + 2 * L * Dk * L + L * L * L), 0.0)
-    m["chunk_reduce"] = (2 * rows * Dk * 4 + rows * nsplit * 4 + 2 * B * T * Hk * Dk * 2 + rows * 2, 0.0, 0.0)
+    m["chunk_reduce"] = (split_bytes + n_split * 2 * L * Dk * 2, 0.0, 0.0)
     qk, vv, gate, ckb = B * T * Hk * Dk * e, B * T * Hv * Dv * e, rows * e, ch * Dv * Dk * 4
     m["seq_fwd"] = (2 * qk + 2 * vv + 2 * gate + ckb + st + rows * Dv * 4, 0.0, 7.0 * rows * Dv * Dk)
     m["seq_bwd"] = (2 * qk + 2 * vv + 2 * gate + ckb + rows * Dv * 4 + 2 * rows * nsplit * Dk * 4 + st,

@@ -26,13 +26,15 @@
 //                        K dS_L^T takes dS as a bf16 high part plus a bf16 low part (exact to
 //                        about 2^-16): with dS rounded once to bf16, dg under strong decay
 //                        misses the bf16 parity bound.
-//   chunk_grad_kernel    per (b, h, chunk), fully parallel: everything else (dq, dk per value
-//                        head, dg).
-//   chunk_reduce_kernel  dq, dk summed over the value heads of each kv head (ascending), dbeta
-//                        over the value-row blocks (ascending).
+//   chunk_grad_kernel    per (b, h, chunk), persistent over consecutive units: everything
+//                        else. dq, dk summed over the value heads of each kv head (ascending)
+//                        in a per-CTA fp32 scratch, written as bf16; dbeta summed over the
+//                        value-row blocks (ascending); dg.
+//   chunk_reduce_kernel  dq, dk of the few groups of value heads split between two gradient
+//                        CTAs, from their per-head partials (the same ascending order).
 // Operands are bf16 in the core-matrix layout of gdn_umma.cuh, read K-major or MN-major (one
-// stored copy serves a matrix and its transpose); accumulators fp32 in tensor memory; Z is a
-// tf32 product. No atomics: every sum has a fixed order.
+// stored copy serves a matrix and its transpose); accumulators fp32 in tensor memory. No
+// atomics: every sum has a fixed order, the same however the units fall on CTAs.
 #include "gdn_umma.cuh"
 
 namespace gdn {
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     // decays, beta and the f partials of a unit (threads < 64), loaded one unit ahead and kept
     // raw (converted and summed where they are used, so that the loads do not stall here)
     constexpr int kMaxSplit = 4;                            // Dv <= 256
-    float vlam = 0.f, vfp[kMaxSplit] = {0.f, 0.f, 0.f, 0.f};
+    float vlam = 0.f, vfp[kMaxSplit] = {0.f, 0.f, 0.f, 0.f}, vdb[kMaxSplit] = {0.f, 0.f, 0.f, 0.f};
     __nv_bfloat16 vbt = __float2bfloat16_rn(0.f);
     auto load_vec = [&](int u) {
         if (tid >= kL) return;
@@ -530,7 +532,10 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         vlam = p.lam[chk * kL + tid];
         vbt = beta[row];
 #pragma unroll
-        for (int s = 0; s < kMaxSplit; ++s) vfp[s] = s < nsplit ? p.ws_f[row * nsplit + s] : 0.f;
+        for (int s = 0; s < kMaxSplit; ++s) {
+            vfp[s] = s < nsplit ? p.ws_f[row * nsplit + s] : 0.f;
+            vdb[s] = s < nsplit ? p.ws_db[row * nsplit + s] : 0.f;
+        }
     };
 
     if (tid == 0) {
@@ -568,6 +573,11 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
 #pragma unroll
             for (int s = 0; s < kMaxSplit; ++s) f += s < nsplit ? vfp[s] : 0.f;   // splits in ascending order
             fv[tid] = in ? f : 0.f;
+            // dbeta of the row: its value-row block partials, in ascending order
+            float db = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxSplit; ++s) db += s < nsplit ? vdb[s] : 0.f;
+            if (in) static_cast<__nv_bfloat16 *>(p.dbeta)[(rowbase + tid) * Hv + h] = __float2bfloat16_rn(db);
         }
         __syncthreads();
         if (tid < kL) {
@@ -764,9 +774,33 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             static_cast<__nv_bfloat16 *>(p.dg)[(rowbase + t) * Hv + h] = __float2bfloat16_rn(dgv);
         }
         {
-            // ---- dq (rows 0-63 of R1) and dk (rows 64-127 of R1 plus R2) of this value head, a
-            // row quarter at a time through shared memory to bulk stores, which write HBM while
-            // the next unit computes
+            // ---- dq (rows 0-63 of R1) and dk (rows 64-127 of R1 plus R2) of this value head,
+            // summed over the value heads of the kv head in ascending order. A group of value
+            // heads that lies in this CTA's range accumulates in the CTA's fp32 scratch (it stays
+            // in L2) and leaves as bf16 with its last head; the heads of a group split between
+            // two CTAs leave fp32 partials, which chunk_reduce_kernel sums in the same order.
+            // A row quarter at a time passes through a padded shared-memory tile, so that each
+            // warp access covers 512 contiguous bytes of one row.
+            const int hh = h % rep, g0 = u - hh;
+            const bool whole = g0 >= u_begin && g0 + rep <= u_end;      // the group lies in this CTA's range
+            const bool addp = whole && hh > 0, fin = whole && hh == rep - 1;
+            float *acc = p.ws_acc + (size_t)blockIdx.x * 2 * kL * DK;
+            __nv_bfloat16 *outq = static_cast<__nv_bfloat16 *>(p.dq), *outk = static_cast<__nv_bfloat16 *>(p.dk);
+            const size_t hk = (size_t)(h / rep);
+            constexpr int NE = DK / 32;                     // float4 of a row quarter per thread
+            // the running sum of the first row quarter, loaded ahead; each later quarter's is
+            // loaded during the previous quarter's stores
+            float4 pre[NE];
+            auto load_pre = [&](int q) {
+                if (addp) {
+#pragma unroll
+                    for (int i = 0; i < NE; ++i) {
+                        const int e = tid + 256 * i, rr = e / (DK / 4), c4 = e - rr * (DK / 4);
+                        pre[i] = *reinterpret_cast<const float4 *>(acc + (32 * q + rr) * DK + 4 * c4);
+                    }
+                }
+            };
+            load_pre(0);
             const int r = 32 * quarter + lane;
             const bool upper = r >= kL;
             float x[SC];
@@ -782,8 +816,6 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             } else {
                 tmem_wait_ld();
             }
-            // rows pass through a padded shared-memory tile so that each warp store covers 512
-            // contiguous bytes of one row
             constexpr int RS = DK + 4;                      // padded row stride (floats)
             for (int q = 0; q < 4; ++q) {
                 if (quarter == q) {
@@ -793,12 +825,25 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                         *reinterpret_cast<float4 *>(row + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
                 }
                 __syncthreads();
-                for (int e = tid; e < 32 * DK / 4; e += 256) {
-                    const int rr = e / (DK / 4), c4 = e - rr * (DK / 4), r2 = 32 * q + rr, s = r2 & (kL - 1);
-                    if (s < len)
-                        *reinterpret_cast<float4 *>((r2 >= kL ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + h) * DK + 4 * c4) =
-                            *reinterpret_cast<const float4 *>(stg + rr * RS + 4 * c4);
+#pragma unroll
+                for (int i = 0; i < NE; ++i) {
+                    const int e = tid + 256 * i, rr = e / (DK / 4), c4 = e - rr * (DK / 4), r2 = 32 * q + rr, s = r2 & (kL - 1);
+                    float4 v4 = *reinterpret_cast<const float4 *>(stg + rr * RS + 4 * c4);
+                    if (addp) {
+                        v4.x = pre[i].x + v4.x; v4.y = pre[i].y + v4.y; v4.z = pre[i].z + v4.z; v4.w = pre[i].w + v4.w;
+                    }
+                    if (!whole) {
+                        if (s < len)
+                            *reinterpret_cast<float4 *>((r2 >= kL ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + h) * DK + 4 * c4) = v4;
+                    } else if (!fin) {
+                        *reinterpret_cast<float4 *>(acc + r2 * DK + 4 * c4) = v4;
+                    } else if (s < len) {
+                        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>((r2 >= kL ? outk : outq) + ((rowbase + s) * Hk + hk) * DK + 4 * c4);
+                        o2[0] = __floats2bfloat162_rn(v4.x, v4.y);
+                        o2[1] = __floats2bfloat162_rn(v4.z, v4.w);
+                    }
                 }
+                if (q < 3) load_pre(q + 1);
                 __syncthreads();
             }
         }
@@ -819,40 +864,38 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// dq, dk: the value heads of each kv head in ascending order; dbeta: the value-row blocks.
-__global__ void __launch_bounds__(256) chunk_reduce_kernel(ChunkBwdParams p, int Dk) {
-    const size_t nqk = (size_t)p.B * p.T * p.Hk * Dk;
-    const size_t ngate = (size_t)p.B * p.T * p.Hv;
+// dq, dk of the groups of value heads (one kv head, one chunk) that the gradient kernel's unit
+// ranges split between two or more CTAs: their per-head fp32 partials summed in ascending
+// head order (the order of the in-CTA sums), to bf16. Four blocks of 16 rows per boundary
+// between consecutive CTA ranges; the first boundary inside a group handles it.
+__global__ void __launch_bounds__(256) chunk_reduce_kernel(ChunkBwdParams p, int Dk, int units, int ctas) {
+    const int i = blockIdx.x / 4 + 1, rq = blockIdx.x % 4;
     const int rep = p.Hv / p.Hk;
+    const int ub = (int)((long long)i * units / ctas);
+    if (i >= ctas || ub % rep == 0) return;                  // no boundary, or one between groups
+    const int g = ub / rep;
+    if ((int)((long long)(i - 1) * units / ctas) > g * rep) return;   // an earlier boundary handles it
+    const int hk = g % p.Hk, bc = g / p.Hk, c = bc % p.NC, b = bc / p.NC;
+    const int t0 = c * 64, len = min(64, p.T - t0);
     __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.dq);
     __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(p.dk);
-    __nv_bfloat16 *db = static_cast<__nv_bfloat16 *>(p.dbeta);
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nqk / 4 + ngate;
-         i += (size_t)gridDim.x * blockDim.x) {
-        if (i < nqk / 4) {
-            const size_t e = 4 * i;
-            const int j = (int)(e % Dk);
-            const size_t bthk = e / Dk;
-            const int hk = (int)(bthk % p.Hk);
-            const size_t bt = bthk / p.Hk;
-            float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
-            for (int h = hk * rep; h < (hk + 1) * rep; ++h) {
-                const size_t o = (bt * p.Hv + h) * Dk + j;
-                const float4 a = *reinterpret_cast<const float4 *>(p.ws_dq + o);
-                const float4 b2 = *reinterpret_cast<const float4 *>(p.ws_dk + o);
-                sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
-                sk.x += b2.x; sk.y += b2.y; sk.z += b2.z; sk.w += b2.w;
-            }
-            __nv_bfloat162 *q2 = reinterpret_cast<__nv_bfloat162 *>(dq + e);
-            __nv_bfloat162 *k2 = reinterpret_cast<__nv_bfloat162 *>(dk + e);
-            q2[0] = __floats2bfloat162_rn(sq.x, sq.y); q2[1] = __floats2bfloat162_rn(sq.z, sq.w);
-            k2[0] = __floats2bfloat162_rn(sk.x, sk.y); k2[1] = __floats2bfloat162_rn(sk.z, sk.w);
-        } else {
-            const size_t gi = i - nqk / 4;
-            float sb = 0.f;
-            for (int s = 0; s < p.nsplit; ++s) sb += p.ws_db[gi * p.nsplit + s];
-            db[gi] = __float2bfloat16_rn(sb);
+    for (int e = threadIdx.x; e < 16 * Dk / 4; e += blockDim.x) {
+        const int s = 16 * rq + e / (Dk / 4), j = 4 * (e % (Dk / 4));
+        if (s >= len) break;
+        const size_t bt = (size_t)b * p.T + t0 + s;
+        float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
+        for (int h = hk * rep; h < (hk + 1) * rep; ++h) {
+            const size_t o = (bt * p.Hv + h) * Dk + j;
+            const float4 a = *reinterpret_cast<const float4 *>(p.ws_dq + o);
+            const float4 b2 = *reinterpret_cast<const float4 *>(p.ws_dk + o);
+            sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
+            sk.x += b2.x; sk.y += b2.y; sk.z += b2.z; sk.w += b2.w;
         }
+        const size_t oo = (bt * p.Hk + hk) * Dk + j;
+        __nv_bfloat162 *q2 = reinterpret_cast<__nv_bfloat162 *>(dq + oo);
+        __nv_bfloat162 *k2 = reinterpret_cast<__nv_bfloat162 *>(dk + oo);
+        q2[0] = __floats2bfloat162_rn(sq.x, sq.y); q2[1] = __floats2bfloat162_rn(sq.z, sq.w);
+        k2[0] = __floats2bfloat162_rn(sk.x, sk.y); k2[1] = __floats2bfloat162_rn(sk.z, sk.w);
     }
 }
 
@@ -880,16 +923,16 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    const int grid = units < sms ? units : sms;             // persistent: one CTA per SM
+    // persistent: one CTA per SM, within the scratch's room
+    int grid = units < sms ? units : sms;
+    if (grid > p.acc_ctas) grid = p.acc_ctas;
+    if (grid < 1) return cudaErrorInvalidValue;
     chunk_grad_kernel<E><<<grid, 256, sg, s>>>(p, units);
     timing_mark("chunk_grad", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const size_t n = (size_t)p.B * p.T * p.Hk * DK / 4 + (size_t)p.B * p.T * p.Hv;
-    size_t blocks = (n + 255) / 256;
-    if (blocks > 8 * 152) blocks = 8 * 152;
     timing_mark("chunk_reduce", 0, s);
-    chunk_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, DK);
+    chunk_reduce_kernel<<<4 * (grid > 1 ? grid - 1 : 1), 256, 0, s>>>(p, DK, units, grid);
     timing_mark("chunk_reduce", 1, s);
     return cudaGetLastError();
 }
