@@ -46,11 +46,11 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:chunk_ -s 15 -c 5 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("502483ca0f0adcc3", "chunk_prep"): 59356672 + 246289152,
-    ("502483ca0f0adcc3", "chunk_sweep"): 298427136 + 352934400,
-    ("502483ca0f0adcc3", "chunk_dsweep"): 248486656 + 192163072,
-    ("502483ca0f0adcc3", "chunk_grad"): 334970112 + 153178880,
-    ("502483ca0f0adcc3", "chunk_reduce"): 202402816 + 14045184,
+    ("93086040dee42621", "chunk_prep"): 64827904 + 254290432,
+    ("93086040dee42621", "chunk_sweep"): 298390016 + 352435200,
+    ("93086040dee42621", "chunk_dsweep"): 265136128 + 194604288,
+    ("93086040dee42621", "chunk_grad"): 335918080 + 41734400,
+    ("93086040dee42621", "chunk_reduce"): 44054272 + 1024,
 }
 
 
