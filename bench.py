@@ -123,9 +123,10 @@ def kernel_model(w):
         + rows * 2 + (st if w.with_dST else 0) + st,
         ch * (2 * 2 * L * Dv * Dk + 2 * L * Dv * L * 2 + 2 * Dv * Dk * L * 2), 0.0)
     # value-head groups split between gradient CTAs (one CTA per SM, at most one per unit):
-    # at most one per CTA boundary; their per-head fp32 partials go through chunk_reduce
+    # at most one per CTA boundary; each CTA's part leaves an fp32 [dq; dk] partial, which
+    # chunk_reduce adds (two parts per split group when a CTA holds more units than a group)
     n_split = min(ch, 152) - 1
-    split_bytes = n_split * (Hv // Hk) * 2 * L * Dk * 4
+    split_bytes = n_split * 2 * 2 * L * Dk * 4
     m["chunk_grad"] = (
         ck * 2 * L * Dk * 2 + ch * (2 * L * Dv * 2 + L * Dv * 2 + 2 * Dv * Dk * 2 + L * 4)
         + rows * (2 + 2 * nsplit * 4) + 2 * rows * 2 + 2 * B * T * Hk * Dk * 2 + split_bytes,

@@ -122,22 +122,8 @@ Workspace workspace_layout(const Plan &p) {
 // Delta [B,Hv,NC,nsplit][64 x 64] and dS at each chunk end [B,Hv,NC,nsplit][64 x Dk], bf16 in
 // their operand layout.
 struct TcWorkspace {
-    size_t dq, dk, db, f, yu, dl, dsl, acc, total;
+    size_t dq, dk, db, f, yu, dl, dsl, total;
 };
-
-// The gradient kernel runs one CTA per SM (at most one per unit); each CTA sums [dq; dk] over the
-// value heads of a kv head in a [128][Dk] fp32 scratch of its own. Without a device the count
-// is an upper bound.
-constexpr int kMaxGradCtas = 256;
-int grad_ctas(const Plan &p) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0)
-        sms = kMaxGradCtas;
-    (void)cudaGetLastError();
-    const long long units = (long long)p.B * p.Hv * p.NC;
-    return (int)(units < sms ? units : sms);
-}
 
 TcWorkspace tc_workspace_layout(const Plan &p) {
     TcWorkspace w;
@@ -152,7 +138,6 @@ TcWorkspace tc_workspace_layout(const Plan &p) {
     w.yu = off; off += round_up(nblk * 128 * 64 * 2);
     w.dl = off; off += round_up(nblk * 64 * 64 * 2);
     w.dsl = off; off += round_up(nblk * 64 * p.Dk * 2);
-    w.acc = off; off += round_up((size_t)grad_ctas(p) * 128 * p.Dk * 4);
     w.total = off;
     return w;
 }
@@ -523,8 +508,6 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.ws_yu = reinterpret_cast<__nv_bfloat16 *>(ws + tw.yu);
         cp.ws_dl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dl);
         cp.ws_dsl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dsl);
-        cp.ws_acc = reinterpret_cast<float *>(ws + tw.acc);
-        cp.acc_ctas = (int)((tw.total - tw.acc) / ((size_t)128 * p.Dk * 4));
         cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC; cp.nsplit = p.nsplit;
         g_last_error[0] = '\0';
         rc = device_status_address(&cp.status);

@@ -450,10 +450,13 @@ struct GradSmem {
 // first products, S0 (whose region then holds the scratch operands) after the second, [Q; K]
 // (when the kv head or chunk changes) after the second.
 // Tensor memory:
-//   [0, DK)             R1, M = 128: rows 0-63 dQ, rows 64-127 the dK terms with B = S0 or K
-//   [DK, 2 DK)          R2, M = 128: rows 64-127 the dK terms diag(E_L) Delta dS_L + GE^T Q +
-//                       HE^T K (the A operands are read from 64 rows before the real ones, so
-//                       that row t lands in the lane of R1's dK row t; rows 0-63 are not used)
+//   [0, DK)             R1, M = 128, per unit: first [dY; dU] S0 (rows 0-63 for dQ, 64-127 for
+//                       dK), then (diag(E_L) Delta) dS_L + GE^T Q + HE^T K, whose A operands are
+//                       read from 64 rows before the real ones, so that row t lands in the lane
+//                       of dK row t (rows 0-63 are not used)
+//   [DK, 2 DK)          RS, M = 128: [dQ; dK] summed over the value heads of this CTA's part of
+//                       the kv head's group: per unit += diag(e^Lam) [dY; dU] S0 (from R1, on the
+//                       CUDA cores), += [GE; HE] K (MMA), rows 64-127 += R1's second terms
 //   [2 DK, 2 DK + 64)   [Q; K] K^T (M = 128), later [W1; W2] M (M = 128)
 //   [2 DK + 64, + 128)  [dY; dU] Delta^T = [G; H] (M = 128)
 template <int E>
@@ -547,7 +550,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tR1 = tmem, tR2 = tmem + DK, tS1 = tmem + 2 * DK, tS2 = tmem + 2 * DK + 64;
+    const uint32_t tR1 = tmem, tRS = tmem + DK, tS1 = tmem + 2 * DK, tS2 = tmem + 2 * DK + 64;
 
     if (tid == 0 && u_begin < u_end) {
         copy_q(u_begin);
@@ -595,18 +598,20 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         }
         tc_fence_after();
         if (!ok) break;
-        // ---- first products: [Q; K] K^T, [dY; dU] Delta^T, [dY; dU] S0, Delta dS_L
+        // this unit's place in its group of value heads (one kv head, one chunk): the first and
+        // last of the group's heads in this CTA's range, and whether the whole group is in it
+        const int hh = h % rep, g0 = u - hh;
+        const bool gfirst = hh == 0 || u == u_begin, glast = hh == rep - 1 || u + 1 == u_end;
+        const bool whole = g0 >= u_begin && g0 + rep <= u_end;
+        // ---- first products: [Q; K] K^T, [dY; dU] Delta^T, [dY; dU] S0
         if (tid == 0) {
             umma_gemm(tS1, CmOp{qk, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, kL, 0, false}, DK,
                       umma_idesc_t(1, 2 * kL, kL, false, false), false);
             umma_gemm(tS2, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{dl, kL, 0, 0, false}, Dv,
                       umma_idesc_t(1, 2 * kL, kL, false, false), false);
-            for (int s = 0; s < nsplit; ++s) {
+            for (int s = 0; s < nsplit; ++s)
                 umma_gemm(tR1, CmOp{yu, 2 * kL, 0, kL * s, false}, CmOp{s0 + (size_t)s * kSb, kL, 0, 0, true}, kL,
                           umma_idesc_t(1, 2 * kL, DK, false, true), s > 0);
-                umma_gemm(tR2, CmOp{dl, kL, -kL, kL * s, false}, CmOp{dsl + (size_t)s * kSb, kL, 0, 0, true}, kL,
-                          umma_idesc_t(1, 2 * kL, DK, false, true), s > 0);
-            }
             umma_commit(bar);
         }
         // ---- c0 = <dS_L, S0> (both in the same layout) while the products run
@@ -630,8 +635,6 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         ++ph;
         tc_fence_after();
         if (!ok) break;
-        // [dY; dU], Delta and dS_L are used up: the next unit's go out now
-        if (tid == 0 && u + 1 < u_end) copy_a(u + 1);
         if (u + 1 < u_end) load_vec(u + 1);                // used at the next unit's start
         {
             // ---- G o E_incl, H o E_strict and [W1; W2] = [G o QK^T; H o KK^T] as operands
@@ -658,7 +661,8 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                     *reinterpret_cast<uint4 *>(wst + o) = pack8(a + 8 * j);
                 }
             }
-            // ---- R1: a_s = (dY S0)_s . q_s, b_s = (dU S0)_s . k_s; then the rows scaled by exp(Lam_s)
+            // ---- R1: a_s = (dY S0)_s . q_s, b_s = (dU S0)_s . k_s; the rows scaled by exp(Lam_s)
+            // into the running sum
             {
                 const float gs = gm[s];
                 float ab = 0.f;
@@ -676,21 +680,30 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                         x[8 * j + i] *= gs;
                     }
                 }
-#pragma unroll
-                for (int j = 0; j < SC / 32; ++j) tmem_st32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
                 abp[half * 2 * kL + r] = ab;
+                // 32 columns at a time (registers)
+#pragma unroll
+                for (int j = 0; j < SC / 32; ++j) {
+                    if (!gfirst) {
+                        float y[32];
+                        tmem_ld32f(tRS + lane_off + half * SC + 32 * j, y);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[32 * j + i] = y[i] + x[32 * j + i];
+                    }
+                    tmem_st32f(tRS + lane_off + half * SC + 32 * j, x + 32 * j);
+                }
             }
-            // ---- R2 (rows 64-127): scaled by E(L, t)
-            if (upper) {
-                const float sc = eL[s];
-                float x[SC];
+            // ---- diag(E_L) Delta in place (G and H are formed): rows t scaled by E(L, t)
+            for (int e = tid; e < kL * Dv / 8; e += 256) {
+                const int t = e & (kL - 1);
+                uint4 *p4 = reinterpret_cast<uint4 *>(dl) + e;    // piece e: row e % 64 of K chunk e / 64
+                float d8[8];
+                unpack8(*p4, d8);
+                const float sc = eL[t];
 #pragma unroll
-                for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < SC; ++i) x[i] *= sc;
-#pragma unroll
-                for (int j = 0; j < SC / 32; ++j) tmem_st32f(tR2 + lane_off + half * SC + 32 * j, x + 32 * j);
+                for (int i = 0; i < 8; ++i) d8[i] *= sc;
+                *p4 = pack8(d8);
             }
             // ---- M^T [t][i] = E(t-1, i) for i < t, bf16 operand
             for (int e = tid; e < kL * kL / 8; e += 256) {
@@ -706,13 +719,17 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // ---- second products: R1 += [GE; HE] K, R2 += GE^T Q + HE^T K, Z = [W1; W2] M
+        // ---- second products: RS += [GE; HE] K; R1 = (diag(E_L) Delta) dS_L + GE^T Q + HE^T K;
+        // Z = [W1; W2] M
         if (tid == 0) {
-            umma_gemm(tR1, CmOp{gehe, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
+            umma_gemm(tRS, CmOp{gehe, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
                       umma_idesc_t(1, 2 * kL, DK, false, true), true);
-            umma_gemm(tR2, CmOp{gehe, 2 * kL, -kL, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, kL,
+            for (int s = 0; s < nsplit; ++s)
+                umma_gemm(tR1, CmOp{dl, kL, -kL, kL * s, false}, CmOp{dsl + (size_t)s * kSb, kL, 0, 0, true}, kL,
+                          umma_idesc_t(1, 2 * kL, DK, false, true), s > 0);
+            umma_gemm(tR1, CmOp{gehe, 2 * kL, -kL, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, kL,
                       umma_idesc_t(1, 2 * kL, DK, true, true), true);
-            umma_gemm(tR2, CmOp{gehe, 2 * kL, -kL, kL, true}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
+            umma_gemm(tR1, CmOp{gehe, 2 * kL, -kL, kL, true}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
                       umma_idesc_t(1, 2 * kL, DK, true, true), true);
             umma_gemm(tS1, CmOp{wst, 2 * kL, 0, 0, false}, CmOp{mt, kL, 0, 0, false}, kL,
                       umma_idesc_t(1, 2 * kL, kL, false, false), false);
@@ -722,8 +739,10 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         ++ph;
         tc_fence_after();
         if (!ok) break;
-        // the S0 region (scratch) and, when the next unit needs another [Q; K], its buffer are free
+        // [dY; dU], Delta, dS_L, the S0 region (scratch) and, when the next unit needs another
+        // [Q; K], its buffer are free: the next unit's go out now
         if (tid == 0 && u + 1 < u_end) {
+            copy_a(u + 1);
             copy_s(u + 1);
             if (!same_qk(u, u + 1)) copy_q(u + 1);
         }
@@ -774,52 +793,43 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             static_cast<__nv_bfloat16 *>(p.dg)[(rowbase + t) * Hv + h] = __float2bfloat16_rn(dgv);
         }
         {
-            // ---- dq (rows 0-63 of R1) and dk (rows 64-127 of R1 plus R2) of this value head,
-            // summed over the value heads of the kv head in ascending order. A group of value
-            // heads that lies in this CTA's range accumulates in the CTA's fp32 scratch (it stays
-            // in L2) and leaves as bf16 with its last head; the heads of a group split between
-            // two CTAs leave fp32 partials, which chunk_reduce_kernel sums in the same order.
-            // A row quarter at a time passes through a padded shared-memory tile, so that each
-            // warp access covers 512 contiguous bytes of one row.
-            const int hh = h % rep, g0 = u - hh;
-            const bool whole = g0 >= u_begin && g0 + rep <= u_end;      // the group lies in this CTA's range
-            const bool addp = whole && hh > 0, fin = whole && hh == rep - 1;
-            float *acc = p.ws_acc + (size_t)blockIdx.x * 2 * kL * DK;
+            // ---- rows 64-127 of R1 (the second dK terms) into the running sum
+            const int r = 32 * quarter + lane;
+            if (r >= kL) {
+#pragma unroll
+                for (int j = 0; j < SC / 32; ++j) {
+                    float x[32], y[32];
+                    tmem_ld32f(tR1 + lane_off + half * SC + 32 * j, x);
+                    tmem_ld32f(tRS + lane_off + half * SC + 32 * j, y);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = y[i] + x[i];
+                    tmem_st32f(tRS + lane_off + half * SC + 32 * j, x);
+                }
+                tmem_wait_st();
+            }
+        }
+        if (glast) {
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            // ---- dq (rows 0-63) and dk (rows 64-127) of the group's value heads in this CTA's
+            // range, from RS: bf16 when the whole group lies in the range; otherwise an fp32
+            // partial under the head that starts this CTA's part, for chunk_reduce_kernel. A row
+            // quarter at a time passes through a padded shared-memory tile, so that each warp
+            // access covers 512 contiguous bytes of one row.
+            const int hs = h - (u - max(g0, u_begin));
             __nv_bfloat16 *outq = static_cast<__nv_bfloat16 *>(p.dq), *outk = static_cast<__nv_bfloat16 *>(p.dk);
             const size_t hk = (size_t)(h / rep);
             constexpr int NE = DK / 32;                     // float4 of a row quarter per thread
-            // the running sum of the first row quarter, loaded ahead; each later quarter's is
-            // loaded during the previous quarter's stores
-            float4 pre[NE];
-            auto load_pre = [&](int q) {
-                if (addp) {
-#pragma unroll
-                    for (int i = 0; i < NE; ++i) {
-                        const int e = tid + 256 * i, rr = e / (DK / 4), c4 = e - rr * (DK / 4);
-                        pre[i] = *reinterpret_cast<const float4 *>(acc + (32 * q + rr) * DK + 4 * c4);
-                    }
-                }
-            };
-            load_pre(0);
-            const int r = 32 * quarter + lane;
-            const bool upper = r >= kL;
             float x[SC];
 #pragma unroll
-            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR1 + lane_off + half * SC + 32 * j, x + 32 * j);
-            if (upper) {
-                float x2[SC];
-#pragma unroll
-                for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tR2 + lane_off + half * SC + 32 * j, x2 + 32 * j);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < SC; ++i) x[i] += x2[i];
-            } else {
-                tmem_wait_ld();
-            }
-            constexpr int RS = DK + 4;                      // padded row stride (floats)
+            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tRS + lane_off + half * SC + 32 * j, x + 32 * j);
+            tmem_wait_ld();
+            constexpr int RSt = DK + 4;                     // padded row stride (floats)
             for (int q = 0; q < 4; ++q) {
                 if (quarter == q) {
-                    float *row = stg + lane * RS + half * SC;
+                    float *row = stg + lane * RSt + half * SC;
 #pragma unroll
                     for (int j = 0; j < SC / 4; ++j)
                         *reinterpret_cast<float4 *>(row + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
@@ -828,22 +838,16 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
 #pragma unroll
                 for (int i = 0; i < NE; ++i) {
                     const int e = tid + 256 * i, rr = e / (DK / 4), c4 = e - rr * (DK / 4), r2 = 32 * q + rr, s = r2 & (kL - 1);
-                    float4 v4 = *reinterpret_cast<const float4 *>(stg + rr * RS + 4 * c4);
-                    if (addp) {
-                        v4.x = pre[i].x + v4.x; v4.y = pre[i].y + v4.y; v4.z = pre[i].z + v4.z; v4.w = pre[i].w + v4.w;
-                    }
+                    if (s >= len) continue;
+                    const float4 v4 = *reinterpret_cast<const float4 *>(stg + rr * RSt + 4 * c4);
                     if (!whole) {
-                        if (s < len)
-                            *reinterpret_cast<float4 *>((r2 >= kL ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + h) * DK + 4 * c4) = v4;
-                    } else if (!fin) {
-                        *reinterpret_cast<float4 *>(acc + r2 * DK + 4 * c4) = v4;
-                    } else if (s < len) {
+                        *reinterpret_cast<float4 *>((r2 >= kL ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + hs) * DK + 4 * c4) = v4;
+                    } else {
                         __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>((r2 >= kL ? outk : outq) + ((rowbase + s) * Hk + hk) * DK + 4 * c4);
                         o2[0] = __floats2bfloat162_rn(v4.x, v4.y);
                         o2[1] = __floats2bfloat162_rn(v4.z, v4.w);
                     }
                 }
-                if (q < 3) load_pre(q + 1);
                 __syncthreads();
             }
         }
@@ -865,9 +869,10 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
 }
 
 // dq, dk of the groups of value heads (one kv head, one chunk) that the gradient kernel's unit
-// ranges split between two or more CTAs: their per-head fp32 partials summed in ascending
-// head order (the order of the in-CTA sums), to bf16. Four blocks of 16 rows per boundary
-// between consecutive CTA ranges; the first boundary inside a group handles it.
+// ranges split between two or more CTAs: each CTA left the sum over its part of the group as
+// an fp32 partial under the part's first head; the parts are added in ascending order, to
+// bf16. Four blocks of 16 rows per boundary between consecutive CTA ranges; the first
+// boundary inside a group handles it.
 __global__ void __launch_bounds__(256) chunk_reduce_kernel(ChunkBwdParams p, int Dk, int units, int ctas) {
     const int i = blockIdx.x / 4 + 1, rq = blockIdx.x % 4;
     const int rep = p.Hv / p.Hk;
@@ -877,6 +882,14 @@ __global__ void __launch_bounds__(256) chunk_reduce_kernel(ChunkBwdParams p, int
     if ((int)((long long)(i - 1) * units / ctas) > g * rep) return;   // an earlier boundary handles it
     const int hk = g % p.Hk, bc = g / p.Hk, c = bc % p.NC, b = bc / p.NC;
     const int t0 = c * 64, len = min(64, p.T - t0);
+    // the parts' first heads: the group's first, then each CTA boundary inside the group
+    int starts[16], np = 0;
+    starts[np++] = (g * rep) % p.Hv;
+    for (int j = i; j < ctas && np < 16; ++j) {
+        const int uj = (int)((long long)j * units / ctas);
+        if (uj >= (g + 1) * rep) break;
+        starts[np++] = uj % p.Hv;
+    }
     __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.dq);
     __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(p.dk);
     for (int e = threadIdx.x; e < 16 * Dk / 4; e += blockDim.x) {
@@ -884,8 +897,8 @@ __global__ void __launch_bounds__(256) chunk_reduce_kernel(ChunkBwdParams p, int
         if (s >= len) break;
         const size_t bt = (size_t)b * p.T + t0 + s;
         float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
-        for (int h = hk * rep; h < (hk + 1) * rep; ++h) {
-            const size_t o = (bt * p.Hv + h) * Dk + j;
+        for (int k = 0; k < np; ++k) {
+            const size_t o = (bt * p.Hv + starts[k]) * Dk + j;
             const float4 a = *reinterpret_cast<const float4 *>(p.ws_dq + o);
             const float4 b2 = *reinterpret_cast<const float4 *>(p.ws_dk + o);
             sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
@@ -923,10 +936,7 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    // persistent: one CTA per SM, within the scratch's room
-    int grid = units < sms ? units : sms;
-    if (grid > p.acc_ctas) grid = p.acc_ctas;
-    if (grid < 1) return cudaErrorInvalidValue;
+    const int grid = units < sms ? units : sms;             // persistent: one CTA per SM
     chunk_grad_kernel<E><<<grid, 256, sg, s>>>(p, units);
     timing_mark("chunk_grad", 1, s);
     err = cudaGetLastError();

@@ -100,15 +100,14 @@ struct ChunkBwdParams {
     const float *dS_T;
     float *dS0;
     void *dv, *dg, *dq, *dk, *dbeta;
-    float *ws_dq, *ws_dk;      // [B, T, Hv, Dk]: per value head (groups of value heads split between gradient CTAs)
-    float *ws_acc;             // [acc_ctas][128 x Dk]: each gradient CTA's running sum of [dq; dk] over value heads
+    float *ws_dq, *ws_dk;      // [B, T, Hv, Dk]: a gradient CTA's part of a group of value heads split between CTAs,
+                               // under the part's first head
     float *ws_db, *ws_f;       // [B, T, Hv, nsplit]: per block of 64 value rows
     __nv_bfloat16 *ws_yu;      // [B, Hv, NC, nsplit][128 x 64]: [dY; dU] of the block, operand layout
     __nv_bfloat16 *ws_dl;      // [B, Hv, NC, nsplit][64 x 64]: Delta = diag(beta) (v - u), operand layout
     __nv_bfloat16 *ws_dsl;     // [B, Hv, NC, nsplit][64 x Dk]: dS at each chunk end, operand layout
     int *status;
     int B, T, Hk, Hv, Dv, NC, nsplit;
-    int acc_ctas;              // gradient CTAs the scratch has room for
 };
 
 // Gate map (a, b, A_log, dt_bias -> g, beta) and its VJP; a, b, g, beta, dg, dbeta, da, db
