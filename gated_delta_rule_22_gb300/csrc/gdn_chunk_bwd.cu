@@ -457,8 +457,8 @@ struct GradSmem {
 //   [DK, 2 DK)          RS, M = 128: [dQ; dK] summed over the value heads of this CTA's part of
 //                       the kv head's group: per unit += diag(e^Lam) [dY; dU] S0 (from R1, on the
 //                       CUDA cores), += [GE; HE] K (MMA), rows 64-127 += R1's second terms
-//   [2 DK, 2 DK + 64)   [Q; K] K^T (M = 128), later [W1; W2] M (M = 128)
-//   [2 DK + 64, + 128)  [dY; dU] Delta^T = [G; H] (M = 128)
+//   [2 DK, 2 DK + 64)   [Q; K] K^T (M = 128), formed once per (b, chunk, kv head)
+//   [2 DK + 64, + 128)  [dY; dU] Delta^T = [G; H] (M = 128), later [W1; W2] M (M = 128)
 template <int E>
 __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, int units) {
     constexpr int DK = 32 * E;
@@ -603,10 +603,12 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         const int hh = h % rep, g0 = u - hh;
         const bool gfirst = hh == 0 || u == u_begin, glast = hh == rep - 1 || u + 1 == u_end;
         const bool whole = g0 >= u_begin && g0 + rep <= u_end;
-        // ---- first products: [Q; K] K^T, [dY; dU] Delta^T, [dY; dU] S0
+        // ---- first products: [Q; K] K^T (when the kv head or chunk changes), [dY; dU] Delta^T,
+        // [dY; dU] S0
         if (tid == 0) {
-            umma_gemm(tS1, CmOp{qk, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, kL, 0, false}, DK,
-                      umma_idesc_t(1, 2 * kL, kL, false, false), false);
+            if (newq)
+                umma_gemm(tS1, CmOp{qk, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, kL, 0, false}, DK,
+                          umma_idesc_t(1, 2 * kL, kL, false, false), false);
             umma_gemm(tS2, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{dl, kL, 0, 0, false}, Dv,
                       umma_idesc_t(1, 2 * kL, kL, false, false), false);
             for (int s = 0; s < nsplit; ++s)
@@ -731,7 +733,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                       umma_idesc_t(1, 2 * kL, DK, true, true), true);
             umma_gemm(tR1, CmOp{gehe, 2 * kL, -kL, kL, true}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
                       umma_idesc_t(1, 2 * kL, DK, true, true), true);
-            umma_gemm(tS1, CmOp{wst, 2 * kL, 0, 0, false}, CmOp{mt, kL, 0, 0, false}, kL,
+            umma_gemm(tS2, CmOp{wst, 2 * kL, 0, 0, false}, CmOp{mt, kL, 0, 0, false}, kL,
                       umma_idesc_t(1, 2 * kL, kL, false, false), false);
             umma_commit(bar);
         }
@@ -751,7 +753,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             // transpose reduction over the warp's 32 rows, then the four row quarters
             const int r = 32 * quarter + lane, s = r & (kL - 1);
             float z[32];
-            tmem_ld32f(tS1 + lane_off + half * 32, z);
+            tmem_ld32f(tS2 + lane_off + half * 32, z);
             tmem_wait_ld();
             const float ls = Lm[s];
 #pragma unroll
