@@ -667,7 +667,8 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     // y and v - u of chunk cc, from tensor memory (its columns are rewritten only by the next
     // chunk's second group of products), staged in the 128-byte swizzle for TMA stores: y (row
     // quarters 0-1 of [y; u]) and v - u (quarters 2-3), each in its own tile (thread 0 waits
-    // for the stores' reads at the next chunk's start). Rows past T are clipped by the stores.
+    // for the stores' reads before the next chunk's first product). Rows past T are clipped by
+    // the stores.
     auto epilogue = [&](int cc) {
         float x[32];
         tmem_ld32f(tYU + lane_off + half * 32, x);
@@ -710,7 +711,12 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
             gm[tid] = expf(lamn);
             if (c + 1 < p.NC) lamn = p.lam[(chk + 1) * kL + tid];
         }
-        if (tid == 0) bulk_wait_read();                     // the earlier stores have read sop, ckst, ysg and rsg
+        // the previous chunk's state stores have read sop and ckst (from the third chunk on, the
+        // y and v - u stores committed after them may still be reading ysg and rsg)
+        if (tid == 0) {
+            if (c >= 2) bulk_wait_read_but<1>();
+            else bulk_wait_read();
+        }
         __syncthreads();
         if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
         // ---- the state as an operand, and the chunk-start checkpoint staged for TMA stores (all
@@ -747,6 +753,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         }
         fence_proxy_async();
         tc_fence_before();
+        if (tid == 0) bulk_wait_read();                     // the y and v - u stores have read ysg and rsg
         // W of the chunk (copied half a chunk ahead; only the MMAs read it)
         ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbar, cph & 1));
         tc_fence_after();

@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         }
         fence_proxy_async();
         tc_fence_before();
+        if (tid == 0) bulk_wait_read();                     // the last chunk's stores have read [dY; dU], Delta and dv
         __syncthreads();
         tc_fence_after();
         if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
@@ -382,7 +383,6 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         if (!ok) break;
         if (tid == 0 && c > 0) copy_K(c - 1);
         ++cph;
-        if (tid == 0) bulk_wait_read();                     // the stores have read the block's buffers
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
