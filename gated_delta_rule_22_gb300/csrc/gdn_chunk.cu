@@ -83,8 +83,11 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&x)[8]) {
 //     T_21 = -T_22 (A_21 T_11)
 // as two dependent products with four consecutive columns of one row per thread (a scalar
 // and a float4 load per four multiply-adds). Blocks of T above the diagonal are not written,
-// and the products skip them. Called by all 256 threads; xs holds 32 x 32 floats.
-__device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid) {
+// and the products skip them. Called by all 256 threads; xs holds 32 x 32 floats. Threads
+// 64-255, idle during the diagonal blocks, run `other` meanwhile.
+template <class Other>
+__device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid, Other &&other) {
+    if (tid >= kL) other();
     if (tid < kL) {
         const int b0 = 16 * (tid >> 4), c = tid & 15;
         float col[16];
@@ -377,12 +380,15 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
             PK[(e >> 6) * 2 * kL + t] = pack8_bf16(pv);
             PK[(e >> 6) * 2 * kL + kL + t] = pack8_bf16(kv8);
         }
+        if (tid == 128) bulk_wait_read();   // the last unit's U boxes have left T and the T operands
+        __syncthreads();
+        // T = (I + A)^-1; while threads 0-63 form its diagonal blocks, the others write
         // [diag(exp Lam) Q; diag(exp Lam) K] (row scaling of the staged operands), one 128-row
         // operand: piece e of Q (K chunk e / 64, row e % 64) goes to 128 (e / 64) + e % 64,
         // that of K 64 pieces later
-        {
+        invert_unit_lower(am, ts, xs, tid, [&] {
             uint4 *QK = reinterpret_cast<uint4 *>(p.qksm + chk * 2 * kL * DK);
-            for (int e = tid; e < kL * DK / 8; e += 256) {
+            for (int e = tid - kL; e < kL * DK / 8; e += 256 - kL) {
                 const int o = (e >> 6) * 2 * kL + (e & (kL - 1));
                 const float gr = gm[e & (kL - 1)];
                 float a[8];
@@ -395,10 +401,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
                 for (int j = 0; j < 8; ++j) a[j] *= gr;
                 QK[o + kL] = pack8_bf16(a);
             }
-        }
-        if (tid == 128) bulk_wait_read();   // the last unit's U boxes have left T and the T operands
-        __syncthreads();
-        invert_unit_lower(am, ts, xs, tid);
+        });
         // T (for the backward), T diag(beta exp Lam) and T diag(beta) as bf16 operands; the
         // blocks of T above the diagonal are zero
         {
@@ -761,9 +764,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         if (tid == 0) {
             // the bf16 state (the backward's operand) and the fp32 checkpoint leave by bulk stores
             if (p.s0m != nullptr) bulk_store(p.s0m + (chk * gridDim.x + split) * kL * DK, sop, kL * DK * 2);
-            if (p.ckpt != nullptr)
-#pragma unroll
-                tma_store_5d(&tm_ck, ckst, 0, (int)(chk * Dv + r0), 0, 0, 0);
+            if (p.ckpt != nullptr) tma_store_5d(&tm_ck, ckst, 0, (int)(chk * Dv + r0), 0, 0, 0);
             bulk_commit();
         }
         // ---- W S^T
