@@ -46,11 +46,11 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:chunk_ -s 15 -c 5 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("93086040dee42621", "chunk_prep"): 64827904 + 254290432,
-    ("93086040dee42621", "chunk_sweep"): 298390016 + 352435200,
-    ("93086040dee42621", "chunk_dsweep"): 265136128 + 194604288,
-    ("93086040dee42621", "chunk_grad"): 335918080 + 41734400,
-    ("93086040dee42621", "chunk_reduce"): 44054272 + 1024,
+    ("eee4c341b36ba821", "chunk_prep"): 64835072 + 254700544,
+    ("eee4c341b36ba821", "chunk_sweep"): 298387200 + 352509184,
+    ("eee4c341b36ba821", "chunk_dsweep"): 265152256 + 194958592,
+    ("eee4c341b36ba821", "chunk_grad"): 335957248 + 22577664,
+    ("eee4c341b36ba821", "chunk_reduce"): 22038016 + 0,
 }
 
 
@@ -130,8 +130,9 @@ def kernel_model(w):
     m["chunk_grad"] = (
         ck * 2 * L * Dk * 2 + ch * (2 * L * Dv * 2 + L * Dv * 2 + 2 * Dv * Dk * 2 + L * 4)
         + rows * (2 + 2 * nsplit * 4) + 2 * rows * 2 + 2 * B * T * Hk * Dk * 2 + split_bytes,
-        ch * 2 * (2 * L * L * Dk + 2 * L * L * Dv + 2 * L * Dk * Dv + L * Dk * Dv + 2 * L * Dk * L
-                  + 2 * L * Dk * L + L * L * L), 0.0)
+        ck * 2 * (2 * L * L * Dk)     # [Q; K] K^T, once per (chunk, kv head)
+        + ch * 2 * (2 * L * L * Dv + 2 * L * Dk * Dv + L * Dk * Dv + 2 * L * Dk * L
+                    + 2 * L * Dk * L + L * L * L), 0.0)
     m["chunk_reduce"] = (split_bytes + n_split * 2 * L * Dk * 2, 0.0, 0.0)
     qk, vv, gate, ckb = B * T * Hk * Dk * e, B * T * Hv * Dv * e, rows * e, ch * Dv * Dk * 4
     m["seq_fwd"] = (2 * qk + 2 * vv + 2 * gate + ckb + st + rows * Dv * 4, 0.0, 7.0 * rows * Dv * Dk)
