@@ -82,7 +82,7 @@ struct DSweepSmem {
         rhs = o; o += (size_t)kL * kL * 2;   // diag(E_L) K dS^T + P^T dY [64 t][64 v]
         dls = o; o += (size_t)kL * kL * 2;   // Delta block [64 t][64 v], for the gradient kernel
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
-        vec = o; o += 4 * kL * 4;            // Lam, E(L, .), beta, -
+        vec = o; o += 4 * kL * 4;            // -, E(L, .), beta, -
         red = o; o += 2 * 2 * kL * 4;        // [f | dbeta][half][64]
         bar = alb(o, 8); o = bar + 5 * 8;    // MMA, copies of (K, P), of T, of [Qs; Ks], of (dY, v - u, Lam)
         tslot = o; o += 16;
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     unsigned char *ydu2 = base + L.ydu, *shl = base + L.shl, *rhs = base + L.rhs, *dls = base + L.dls;
     unsigned char *dvs = base + L.dvs;
     float *rsm = reinterpret_cast<float *>(base + L.rsm), *lms = reinterpret_cast<float *>(base + L.lms);
-    float *Lm = reinterpret_cast<float *>(base + L.vec), *eL = Lm + kL, *bt = eL + kL;
+    float *eL = reinterpret_cast<float *>(base + L.vec) + kL, *bt = eL + kL;
     float *red = reinterpret_cast<float *>(base + L.red);   // [2][2][64]
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
     uint64_t *cbA = bar + 1, *cbT = bar + 2, *cbK = bar + 3, *cbY = bar + 4;
@@ -208,15 +208,19 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         const size_t rowbase = (size_t)b * T + t0;          // (b, t0) row of [B, T, ...]
         const int buf = (p.NC - 1 - c) & 1;
         unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;   // [dY; dU] of this chunk
+        const float *lmb = lms + buf * kL;                 // Lam of this chunk
         {
-            // this chunk's dY, v - u and Lam have landed (every thread reads them)
+            // this chunk's dY, v - u and Lam have landed (every thread waits: every thread reads them)
             const bool w = mbar_wait(cbY, wY & 1);
             ++wY;
-            if (tid < kL) bt[tid] = tid < len ? __bfloat162float(btn) : 0.f;
+            if (tid < kL) {
+                bt[tid] = tid < len ? __bfloat162float(btn) : 0.f;
+                eL[tid] = expf(lmb[kL - 1] - lmb[tid]);
+            }
             ok = !__syncthreads_or(!w);
             if (!ok) break;
         }
-        if (tid < kL) Lm[tid] = lms[buf * kL + tid];
+        const float decay = expf(lmb[kL - 1]);
         // this lane's v - u (row lrow, 32 value columns: box `half`, 16-byte piece i of the row
         // at ((i ^ (row & 7)) << 4))
         float rs[32];
@@ -227,9 +231,6 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
             rs[4 * i] = f4.x; rs[4 * i + 1] = f4.y; rs[4 * i + 2] = f4.z; rs[4 * i + 3] = f4.w;
         }
-        __syncthreads();
-        if (tid < kL) eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
-        const float decay = expf(Lm[kL - 1]);
         // ---- dS (the adjoint of the chunk-end state) as operands (high and low bf16 parts),
         // the high part also stored for the gradient kernel ([64][DK] operand layout: a warp's
         // 16 rows of one K chunk are 256 contiguous bytes); then dS <- exp(Lam_L) dS in place
@@ -264,12 +265,18 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         }
         fence_proxy_async();
         tc_fence_before();
-        if (tid == 0) bulk_wait_read();                     // the last chunk's stores have read [dY; dU], Delta and dv
-        __syncthreads();
+        {
+            // the last chunk's stores have read [dY; dU], Delta and dv; K and [P; KKm] have landed
+            bool w = true;
+            if (tid == 0) {
+                bulk_wait_read();
+                w = mbar_wait(cbA, cph & 1);
+            }
+            ok = !__syncthreads_or(!w);
+        }
         tc_fence_after();
-        if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
-        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbA, cph & 1));
         if (!ok) break;
+        if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
         // ---- K [dS_high; dS_low]^T (N = 128), P^T dY (P: rows 0-63 of [P; KKm])
         if (tid == 0) {
             constexpr uint32_t idX = umma_idesc_t(1, kL, 2 * kL, false, false);
@@ -314,13 +321,12 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbT, cph & 1));   // and T has landed
         tc_fence_after();
+        if (!ok) break;
         // the buffers of K and [P; KKm] are free: the previous chunk's copies go out now
         if (tid == 0 && c > 0) copy_A(c - 1);
         if (tid < kL && tid < len) p.ws_f[((rowbase + tid) * Hv + h) * nsplit + split] = red[tid] + red[kL + tid];
-        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbT, cph & 1));
-        if (!ok) break;
         // ---- dD = T^T rhs
         if (tid == 0) {
             umma_gemm(tX, CmOp{tmm, kL, 0, 0, true}, CmOp{rhs, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, kL, true, true),
@@ -359,12 +365,11 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbK, cph & 1));   // and [Qs; Ks] has landed
         tc_fence_after();
+        if (!ok) break;
         if (tid < kL && tid < len)
             p.ws_db[((rowbase + tid) * Hv + h) * nsplit + split] = red[2 * kL + tid] + red[3 * kL + tid];
-        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbK, cph & 1));
-        if (!ok) break;
         // ---- dS += [dY; dU]^T [diag(exp Lam) Q; diag(exp Lam) K] (K = 128)
         if (tid == 0) {
             umma_gemm(tS, CmOp{ydu, 2 * kL, 0, 0, true}, CmOp{qks, 2 * kL, 0, 0, true}, 2 * kL,
