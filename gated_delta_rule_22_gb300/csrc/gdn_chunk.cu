@@ -825,11 +825,9 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         ++phase;
         tc_fence_after();
         if (!ok) break;
-        // the other operand buffers are free again: bring in the next chunk's
+        // the other operand buffers are free again: bring in the next chunk's (no block barrier
+        // before the next chunk: nothing after this point reads what its first section writes)
         if (tid == 0 && c + 1 < p.NC) issue_r(c + 1);
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
     if (ok) epilogue(p.NC - 1);
     if (tid == 0) bulk_wait_all();                          // the state stores are complete

@@ -388,9 +388,8 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         if (!ok) break;
         if (tid == 0 && c > 0) copy_K(c - 1);
         ++cph;
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        // no block barrier before the next chunk: nothing after this point reads what its first
+        // section writes
     }
     if (tid == 0) bulk_wait_all();                          // the block outputs are complete
     cp_async_wait<0>();                                     // no copy still writes shared memory
