@@ -46,11 +46,11 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:chunk_ -s 15 -c 5 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("eee4c341b36ba821", "chunk_prep"): 64835072 + 254700544,
-    ("eee4c341b36ba821", "chunk_sweep"): 298387200 + 352509184,
-    ("eee4c341b36ba821", "chunk_dsweep"): 265152256 + 194958592,
-    ("eee4c341b36ba821", "chunk_grad"): 335957248 + 22577664,
-    ("eee4c341b36ba821", "chunk_reduce"): 22038016 + 0,
+    ("d7da8e37539f6da5", "chunk_prep"): 64848896 + 254633472,
+    ("d7da8e37539f6da5", "chunk_sweep"): 298392832 + 352944128,
+    ("d7da8e37539f6da5", "chunk_dsweep"): 265221888 + 194624000,
+    ("d7da8e37539f6da5", "chunk_grad"): 335968000 + 22657536,
+    ("d7da8e37539f6da5", "chunk_reduce"): 22039296 + 0,
 }
 
 
