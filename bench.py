@@ -46,11 +46,11 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:chunk_ -s 15 -c 5 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("d7da8e37539f6da5", "chunk_prep"): 64848896 + 254633472,
-    ("d7da8e37539f6da5", "chunk_sweep"): 298392832 + 352944128,
-    ("d7da8e37539f6da5", "chunk_dsweep"): 265221888 + 194624000,
-    ("d7da8e37539f6da5", "chunk_grad"): 335968000 + 22657536,
-    ("d7da8e37539f6da5", "chunk_reduce"): 22039296 + 0,
+    ("775115084e9696ab", "chunk_prep"): 64839424 + 254659840,
+    ("775115084e9696ab", "chunk_sweep"): 298366464 + 352674816,
+    ("775115084e9696ab", "chunk_dsweep"): 265112832 + 194504448,
+    ("775115084e9696ab", "chunk_grad"): 335942400 + 22636288,
+    ("775115084e9696ab", "chunk_reduce"): 22031872 + 0,
 }
 
 

@@ -888,14 +888,6 @@ __global__ void __launch_bounds__(256) chunk_reduce_kernel(ChunkBwdParams p, int
     if ((int)((long long)(i - 1) * units / ctas) > g * rep) return;   // an earlier boundary handles it
     const int hk = g % p.Hk, bc = g / p.Hk, c = bc % p.NC, b = bc / p.NC;
     const int t0 = c * 64, len = min(64, p.T - t0);
-    // the parts' first heads: the group's first, then each CTA boundary inside the group
-    int starts[16], np = 0;
-    starts[np++] = (g * rep) % p.Hv;
-    for (int j = i; j < ctas && np < 16; ++j) {
-        const int uj = (int)((long long)j * units / ctas);
-        if (uj >= (g + 1) * rep) break;
-        starts[np++] = uj % p.Hv;
-    }
     __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.dq);
     __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(p.dk);
     for (int e = threadIdx.x; e < 16 * Dk / 4; e += blockDim.x) {
@@ -903,8 +895,11 @@ __global__ void __launch_bounds__(256) chunk_reduce_kernel(ChunkBwdParams p, int
         if (s >= len) break;
         const size_t bt = (size_t)b * p.T + t0 + s;
         float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
-        for (int k = 0; k < np; ++k) {
-            const size_t o = (bt * p.Hv + starts[k]) * Dk + j;
+        // the parts' first units: the group's first, then each CTA boundary inside the group
+        for (int k = i - 1; k < ctas; ++k) {
+            const int us = k == i - 1 ? g * rep : (int)((long long)k * units / ctas);
+            if (us >= (g + 1) * rep) break;
+            const size_t o = (bt * p.Hv + us % p.Hv) * Dk + j;
             const float4 a = *reinterpret_cast<const float4 *>(p.ws_dq + o);
             const float4 b2 = *reinterpret_cast<const float4 *>(p.ws_dk + o);
             sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
