@@ -40,17 +40,17 @@ FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # PR #1217 performance table): another machine's number, quoted as context.
 PAGES_TOKENS_PER_S = 2048 / 0.1498
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of a kernel, from one ncu capture,
-# keyed by (hash of the kernel sources it was taken on, kernel family); absent: not measured
-# for the current sources.
+# keyed by (hash of the kernel family's source files, KERNEL_FILES, when it was taken; kernel
+# family); absent: not measured for the current sources.
 # Capture (bench workload, 5 chunk kernels of one step after 3 warm-up steps):
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:chunk_ -s 15 -c 5 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("775115084e9696ab", "chunk_prep"): 64839424 + 254659840,
-    ("775115084e9696ab", "chunk_sweep"): 298366464 + 352674816,
-    ("775115084e9696ab", "chunk_dsweep"): 265112832 + 194504448,
-    ("775115084e9696ab", "chunk_grad"): 335942400 + 22636288,
-    ("775115084e9696ab", "chunk_reduce"): 22031872 + 0,
+    ("b83a5a3c7c922963", "chunk_prep"): 64839424 + 254659840,
+    ("b83a5a3c7c922963", "chunk_sweep"): 298366464 + 352674816,
+    ("b7b33f75f072d0ee", "chunk_dsweep"): 265112832 + 194504448,
+    ("b7b33f75f072d0ee", "chunk_grad"): 335942400 + 22636288,
+    ("b7b33f75f072d0ee", "chunk_reduce"): 22031872 + 0,
 }
 
 
@@ -64,14 +64,34 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1700.0, "source": "fallback 6.8 TB/s, 1.7 PFLOP/s sustained: of fallback"}
 
 
-def kernel_source_hash():
+# The source files a kernel family's code and launch depend on (its translation unit, the
+# shared headers, and the host code that builds its tensor maps): its traffic entry stays valid
+# while these are unchanged.
+KERNEL_FILES = {
+    "chunk_prep": ("gdn_chunk.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
+    "chunk_sweep": ("gdn_chunk.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
+    "chunk_dsweep": ("gdn_chunk_bwd.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
+    "chunk_grad": ("gdn_chunk_bwd.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
+    "chunk_reduce": ("gdn_chunk_bwd.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
+}
+
+
+def kernel_source_hash(files=None):
+    """Hash of the library's CUDA sources (all of them, or the named files)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_22_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
+        if f.endswith((".cu", ".cuh")) and (files is None or f in files):
             h.update(f.encode())
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def traffic_of(name):
+    """The DRAM traffic per launch measured for kernel family `name` on its current sources,
+    or None."""
+    files = KERNEL_FILES.get(name)
+    return None if files is None else TRAFFIC.get((kernel_source_hash(files), name))
 
 
 def flops_per_step(w, count=28):
@@ -449,10 +469,10 @@ def run_ours(args, w):
         kernels[name] = kernel_roofline(name, ms / n, model.get(name, (0.0, 0.0, 0.0)), peaks)
         kernels[name]["launches_per_step"] = n / K
         kernels[name]["share"] = ms / sum(t for _, t in ktimes.values())
-        kernels[name]["traffic"] = TRAFFIC.get((src_hash, name))
+        kernels[name]["traffic"] = traffic_of(name)
     dominant = max(kernels.values(), key=lambda k: k["share"])
     roof = {"bound": dominant["bound"], "achieved": dominant["achieved"], "peak": dominant["peak"],
-            "unit": dominant["unit"], "frac": dominant["frac"], "traffic": TRAFFIC.get((src_hash, dominant["kernel"])),
+            "unit": dominant["unit"], "frac": dominant["frac"], "traffic": traffic_of(dominant["kernel"]),
             "kernel": dominant["kernel"], "ms_per_launch": dominant["ms_per_launch"],
             "per_launch": dominant["per_launch"], "peak_source": peaks["source"] if dominant["bound"] != "alu"
             else "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"}
