@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -46,11 +47,11 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:chunk_ -s 15 -c 5 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("b83a5a3c7c922963", "chunk_prep"): 64839424 + 254659840,
-    ("b83a5a3c7c922963", "chunk_sweep"): 298366464 + 352674816,
-    ("b7b33f75f072d0ee", "chunk_dsweep"): 265112832 + 194504448,
-    ("b7b33f75f072d0ee", "chunk_grad"): 335942400 + 22636288,
-    ("b7b33f75f072d0ee", "chunk_reduce"): 22031872 + 0,
+    ("15a325b284f4ae2f", "chunk_prep"): 64839424 + 254659840,
+    ("15a325b284f4ae2f", "chunk_sweep"): 298366464 + 352674816,
+    ("ed60ecc2f47f718f", "chunk_dsweep"): 265112832 + 194504448,
+    ("ed60ecc2f47f718f", "chunk_grad"): 335942400 + 22636288,
+    ("ed60ecc2f47f718f", "chunk_reduce"): 22031872 + 0,
 }
 
 
@@ -76,14 +77,22 @@ KERNEL_FILES = {
 }
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace runs collapsed: what the compiler sees."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(files=None):
-    """Hash of the library's CUDA sources (all of them, or the named files)."""
+    """Hash of the code (comments and layout aside) of the library's CUDA sources: all of
+    them, or the named files."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_22_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh")) and (files is None or f in files):
             h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            h.update(_code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

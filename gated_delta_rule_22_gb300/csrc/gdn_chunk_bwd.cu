@@ -450,9 +450,9 @@ struct GradSmem {
 
 // Persistent: one CTA per SM, each over a contiguous range of units (b, chunk, value head),
 // value head fastest, so that consecutive units share [Q; K]. Every operand arrives by bulk
-// copy, the next unit's as soon as its buffers are free: [dY; dU], Delta and dS_L after the
-// first products, S0 (whose region then holds the scratch operands) after the second, [Q; K]
-// (when the kv head or chunk changes) after the second.
+// copy, the next unit's as soon as its buffers are free, all after the second products:
+// [dY; dU], Delta (scaled in place by E_L for the second products) and dS_L, S0 (whose region
+// then holds the scratch operands) and [Q; K] (when the kv head or chunk changes).
 // Tensor memory:
 //   [0, DK)             R1, M = 128, per unit: first [dY; dU] S0 (rows 0-63 for dQ, 64-127 for
 //                       dK), then (diag(E_L) Delta) dS_L + GE^T Q + HE^T K, whose A operands are
