@@ -161,10 +161,11 @@ __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid
 
 // Persistent: one CTA per SM over a contiguous range of units (batch row, chunk, kv head,
 // value head), value head fastest. When a unit starts a new (batch row, chunk, kv head) group
-// the CTA stages K and Q and forms K K^T and Q K^T; per unit (value head) it forms the
-// decay-weighted matrices, T, W = (T diag(beta exp Lam)) K and U = (T diag(beta)) V (the row
-// scalings folded into T's columns, K and V read as MN-major operands). The next unit's V, g
-// and beta are fetched while the current one computes.
+// the CTA forms K K^T and Q K^T from K and Q (fetched by TMA while the previous group's last
+// unit was read back); per unit (value head) it forms the decay-weighted matrices, T,
+// W = (T diag(beta exp Lam)) K and U = (T diag(beta)) V (the row scalings folded into T's
+// columns, K and V read as MN-major operands). The next unit's V, g and beta are fetched while
+// the current one computes.
 template <int E>
 __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int units,
                                                             const __grid_constant__ ChunkFwdMaps maps) {
@@ -599,9 +600,10 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
 
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const size_t head = (size_t)b * Hv + h;
-    // the six operand matrices of chunk cc, prepared in their shared-memory layout, by bulk
-    // copies in two groups (thread 0): W, read by the first product of a chunk, goes out as
-    // soon as that product is done; the rest, read by the second group, after that group
+    // the operand matrices of chunk cc (W, [Qs; Ks], K, [P; KKm]), prepared in their
+    // shared-memory layout, by bulk copies in two groups (thread 0): W, read by the first
+    // product of a chunk, goes out as soon as that product is done; the rest, read by the
+    // second group, after that group
     constexpr unsigned kBig = kL * DK * 2, kSmall = kL * kL * 2;
     int ncw = 0, ncr = 0;
     auto issue_w = [&](int cc) {
