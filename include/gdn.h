@@ -77,7 +77,7 @@ enum {
                                        B or Hv > 65535, or a tensor too large to index */
     GDN_ERR_WORKSPACE_TOO_SMALL = -4,
     GDN_ERR_CUDA = -5,              /* the CUDA runtime reported an error (see gdn_last_error) */
-    GDN_ERR_TIMEOUT = -6,           /* reserved for bounded device-side waits */
+    GDN_ERR_TIMEOUT = -6,           /* a bounded device-side wait ran out (gdn_device_status) */
     GDN_ERR_SCRATCH_LIMIT = -7      /* gdn_bwd_noalloc: the problem needs more scratch than
                                        GDN_BWD_NOALLOC_SCRATCH_BYTES */
 };
