@@ -28,13 +28,14 @@
 //                        misses the bf16 parity bound.
 //   chunk_grad_kernel    per (b, h, chunk), persistent over consecutive units: everything
 //                        else. dq, dk summed over the value heads of each kv head (ascending)
-//                        in a per-CTA fp32 scratch, written as bf16; dbeta summed over the
-//                        value-row blocks (ascending); dg.
-//   chunk_reduce_kernel  dq, dk of the few groups of value heads split between two gradient
-//                        CTAs, from their per-head partials (the same ascending order).
+//                        in tensor memory, written as bf16 once per group; dbeta summed over
+//                        the value-row blocks (ascending); dg.
+//   chunk_reduce_kernel  dq, dk of the few groups of value heads split between gradient CTAs,
+//                        from one fp32 partial per CTA part (the same ascending order).
 // Operands are bf16 in the core-matrix layout of gdn_umma.cuh, read K-major or MN-major (one
 // stored copy serves a matrix and its transpose); accumulators fp32 in tensor memory. No
-// atomics: every sum has a fixed order, the same however the units fall on CTAs.
+// atomics: every sum has a fixed order for a given grid (the gradient kernel's grid is the SM
+// count, capped by the number of units, so results are bitwise repeatable on one GPU model).
 #include "gdn_umma.cuh"
 
 namespace gdn {

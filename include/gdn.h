@@ -35,7 +35,9 @@
  *   - Every argument check runs on the host before anything is enqueued: a call
  *     that returns an error has launched nothing and written nothing.
  *   - Results are bitwise deterministic: no atomics; every reduction (over rows,
- *     over the value heads that share a kv head) runs in a fixed order.
+ *     over the value heads that share a kv head) runs in a fixed order. The bf16
+ *     tensor-core backward groups the sum over value heads by its grid, which is the
+ *     GPU's SM count, so repeat runs agree bit for bit on one GPU model.
  *   - There is no host fallback: if the GPU cannot run a kernel the call returns
  *     GDN_ERR_CUDA.
  */
