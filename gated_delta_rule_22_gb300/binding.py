@@ -115,13 +115,20 @@ def _check(name, t, shape, dtype, device):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _require_cuda(t):
+    """The library takes device pointers only: a host tensor here would reach the kernels as a
+    host address. The other tensors of a call are checked to be on t's device."""
+    if t.device.type != "cuda":
+        raise ValueError(f"tensors are on {t.device}; the library takes CUDA tensors")
+
+
 def make_shape(B, T, Hk, Hv, Dk, Dv, chunk=64, dtype=GDN_F32) -> GdnShape:
     return GdnShape(B, T, Hk, Hv, Dk, Dv, chunk, dtype)
 
 
-def _stream(stream):
+def _stream(stream, device=None):
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -200,27 +207,30 @@ def gdn_fwd(q, k, v, g, beta, S0=None, chunk=64, *, y=None, S_T=None, ckpt=None,
         _check(name, t, shp, dt, dev)
     if S0 is not None:
         _check("S0", S0, (B, Hv, Dv, Dk), torch.float32, dev)
-    NC = -(-T // (chunk or 64))
+    if y is not None:
+        _check("y", y, (B, T, Hv, Dv), dt, dev)
+    if S_T is not None:
+        _check("S_T", S_T, (B, Hv, Dv, Dk), torch.float32, dev)
+    if ckpt is not None:
+        _check_ckpt(ckpt, q, v, chunk)
+    _require_cuda(q)
     if y is None:
         y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
     if S_T is None and want_S_T:
         S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
     if ckpt is None and want_ckpt:
         ckpt = new_ckpt(q, v, chunk)
-    if ckpt is not None:
-        _check_ckpt(ckpt, q, v, chunk)
     rc = lib.gdn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0),
-                     _ptr(y), _ptr(S_T), _ptr(ckpt), _stream(stream))
+                     _ptr(y), _ptr(S_T), _ptr(ckpt), _stream(stream, dev))
     if rc != GDN_OK:
         raise GdnError("gdn_fwd", rc, lib)
     return y, S_T, ckpt
 
 
-def gdn_bwd(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, workspace=None, out=None,
-            want_dS0=True, stream=None):
-    """dict(dq, dk, dv, dg, dbeta, dS0) = gdn_bwd(...) on CUDA tensors (see include/gdn.h)."""
+def _bwd_prepare(q, k, v, g, beta, ckpt, dy, dS_T, chunk, out, want_dS0, workspace=None):
+    """Checks of a backward call's tensors (all before anything is allocated or launched), then
+    the output dict (the caller's, or new tensors). Returns (shape, out)."""
     torch = _torch()
-    lib = load_library()
     shape = _shape_of(q, v, chunk)
     B, T, Hk, Dk = q.shape
     Hv, Dv = v.shape[2], v.shape[3]
@@ -231,20 +241,77 @@ def gdn_bwd(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, workspace=None, 
     _check_ckpt(ckpt, q, v, chunk)
     if dS_T is not None:
         _check("dS_T", dS_T, (B, Hv, Dv, Dk), torch.float32, dev)
+    if out is not None:
+        for name, shp in (("dq", q.shape), ("dk", q.shape), ("dv", (B, T, Hv, Dv)), ("dg", (B, T, Hv)),
+                          ("dbeta", (B, T, Hv))):
+            if out.get(name) is None:
+                raise ValueError(f"out lacks {name}")
+            _check(name, out[name], shp, dt, dev)
+        if out.get("dS0") is not None:
+            _check("dS0", out["dS0"], (B, Hv, Dv, Dk), torch.float32, dev)
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError(f"workspace must be a contiguous tensor on {dev}")
+    _require_cuda(q)
     if out is None:
         out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
                "dg": torch.empty_like(g), "dbeta": torch.empty_like(beta),
                "dS0": torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev) if want_dS0 else None}
-    need = lib.gdn_bwd_workspace_bytes(ctypes.byref(shape))
+    return shape, out
+
+
+def gdn_bwd(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, workspace=None, out=None,
+            want_dS0=True, stream=None):
+    """dict(dq, dk, dv, dg, dbeta, dS0) = gdn_bwd(...) on CUDA tensors (see include/gdn.h).
+    workspace: a device tensor of at least gdn_bwd_workspace_bytes bytes, or None (allocated
+    here for this call)."""
+    torch = _torch()
+    lib = load_library()
+    shape, out = _bwd_prepare(q, k, v, g, beta, ckpt, dy, dS_T, chunk, out, want_dS0, workspace)
     if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        need = lib.gdn_bwd_workspace_bytes(ctypes.byref(shape))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     rc = lib.gdn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ckpt),
                      _ptr(dy), _ptr(dS_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
                      _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out.get("dS0")), _ptr(workspace),
-                     workspace.numel() * workspace.element_size(), _stream(stream))
+                     workspace.numel() * workspace.element_size(), _stream(stream, q.device))
     if rc != GDN_OK:
         raise GdnError("gdn_bwd", rc, lib)
     return out
+
+
+def gdn_bwd_noalloc(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, out=None, want_dS0=True,
+                    stream=None):
+    """gdn_bwd with the library's fixed device scratch instead of a workspace (see
+    include/gdn.h: calls that overlap on one GPU race on that scratch). Pass `out` to
+    allocate nothing here either."""
+    lib = load_library()
+    shape, out = _bwd_prepare(q, k, v, g, beta, ckpt, dy, dS_T, chunk, out, want_dS0)
+    rc = lib.gdn_bwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ckpt),
+                             _ptr(dy), _ptr(dS_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                             _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out.get("dS0")),
+                             _stream(stream, q.device))
+    if rc != GDN_OK:
+        raise GdnError("gdn_bwd_noalloc", rc, lib)
+    return out
+
+
+def gdn_device_status() -> int:
+    """Reads and clears the current device's status word: GDN_OK, or GDN_ERR_TIMEOUT when a
+    kernel's bounded wait ran out since the last read (synchronises with the device)."""
+    return load_library().gdn_device_status()
+
+
+def gdn_strerror(code: int) -> str:
+    return load_library().gdn_strerror(code).decode()
+
+
+def gdn_last_error() -> str:
+    return load_library().gdn_last_error().decode()
+
+
+def gdn_version() -> int:
+    return load_library().gdn_version()
 
 
 def _gate_shape(a, Hk, Dk, Dv):
@@ -263,11 +330,12 @@ def gdn_gates_fwd(a, b, A_log, dt_bias, *, Hk=None, Dk=32, Dv=4, stream=None):
     _check("b", b, (B, T, Hv), a.dtype, a.device)
     _check("A_log", A_log, (Hv,), torch.float32, a.device)
     _check("dt_bias", dt_bias, (Hv,), torch.float32, a.device)
+    _require_cuda(a)
     shape = _gate_shape(a, Hk or Hv, Dk, Dv)
     g = torch.empty_like(a)
     beta = torch.empty_like(a)
     rc = lib.gdn_gates_fwd(ctypes.byref(shape), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(g),
-                           _ptr(beta), _stream(stream))
+                           _ptr(beta), _stream(stream, a.device))
     if rc != GDN_OK:
         raise GdnError("gdn_gates_fwd", rc, lib)
     return g, beta
@@ -282,12 +350,13 @@ def gdn_gates_bwd(a, b, A_log, dt_bias, dg, dbeta, *, Hk=None, Dk=32, Dv=4, stre
         _check(name, t, (B, T, Hv), a.dtype, a.device)
     _check("A_log", A_log, (Hv,), torch.float32, a.device)
     _check("dt_bias", dt_bias, (Hv,), torch.float32, a.device)
+    _require_cuda(a)
     shape = _gate_shape(a, Hk or Hv, Dk, Dv)
     out = {"da": torch.empty_like(a), "db": torch.empty_like(a),
            "dA_log": torch.empty_like(A_log), "ddt_bias": torch.empty_like(dt_bias)}
     rc = lib.gdn_gates_bwd(ctypes.byref(shape), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(dg),
                            _ptr(dbeta), _ptr(out["da"]), _ptr(out["db"]), _ptr(out["dA_log"]),
-                           _ptr(out["ddt_bias"]), _stream(stream))
+                           _ptr(out["ddt_bias"]), _stream(stream, a.device))
     if rc != GDN_OK:
         raise GdnError("gdn_gates_bwd", rc, lib)
     return out

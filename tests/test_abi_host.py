@@ -172,3 +172,69 @@ def test_error_strings(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(ImportError):
         B.load_library(str(tmp_path / "libgdn.so"))
+
+
+def test_binding_has_every_header_function(lib):
+    import gated_delta_rule_22_gb300 as gdn
+    missing = [f for f in B.header_functions() if not callable(getattr(gdn, f, None))]
+    assert not missing, missing
+
+
+def _host_tensors(dtype=None):
+    import torch
+    import gdn_synthetic as gs
+    w = gs.WORKLOADS["tiny"]
+    inp = gs.make_inputs(w)
+    dt = dtype or torch.float32
+    return w, {n: torch.from_numpy(inp[n]).to(dt) for n in ("q", "k", "v", "g", "beta", "dy")}
+
+
+def test_binding_refuses_host_tensors(lib):
+    """The C ABI takes device pointers; the binding stops host tensors before the call."""
+    import gated_delta_rule_22_gb300 as gdn
+    _, t = _host_tensors()
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"])
+    ck = gdn.new_ckpt(t["q"], t["v"])
+    for fn in (gdn.gdn_bwd, gdn.gdn_bwd_noalloc):
+        with pytest.raises(ValueError, match="CUDA tensors"):
+            fn(t["q"], t["k"], t["v"], t["g"], t["beta"], ck, t["dy"])
+    import torch
+    Hv = t["g"].shape[2]
+    A_log, dt_bias = torch.zeros(Hv), torch.zeros(Hv)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        gdn.gdn_gates_fwd(t["g"], t["beta"], A_log, dt_bias)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        gdn.gdn_gates_bwd(t["g"], t["beta"], A_log, dt_bias, t["g"], t["beta"])
+
+
+def test_binding_checks_caller_outputs(lib):
+    """Output tensors a caller passes in are checked like the inputs (shape, dtype, layout),
+    so a wrong one cannot reach a kernel as a too-small buffer."""
+    import torch
+    import gated_delta_rule_22_gb300 as gdn
+    _, t = _host_tensors()
+    q, k, v, g, beta, dy = (t[n] for n in ("q", "k", "v", "g", "beta", "dy"))
+    with pytest.raises(ValueError, match="y has shape"):
+        gdn.gdn_fwd(q, k, v, g, beta, y=torch.empty(v.shape[0], v.shape[1] - 1, *v.shape[2:]))
+    with pytest.raises(ValueError, match="S_T has shape"):
+        gdn.gdn_fwd(q, k, v, g, beta, S_T=torch.empty(1))
+    with pytest.raises(ValueError, match="ckpt"):
+        gdn.gdn_fwd(q, k, v, g, beta, ckpt=torch.empty(1))
+    ck = gdn.new_ckpt(q, v)
+    good = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+            "dg": torch.empty_like(g), "dbeta": torch.empty_like(beta)}
+    with pytest.raises(ValueError, match="out lacks dv"):
+        gdn.gdn_bwd(q, k, v, g, beta, ck, dy, out={n: x for n, x in good.items() if n != "dv"})
+    with pytest.raises(TypeError, match="dq has dtype"):
+        gdn.gdn_bwd(q, k, v, g, beta, ck, dy, out=dict(good, dq=torch.empty_like(q, dtype=torch.float64)))
+    with pytest.raises(ValueError, match="dk must be contiguous"):
+        gdn.gdn_bwd(q, k, v, g, beta, ck, dy, out=dict(good, dk=torch.empty_like(k).transpose(2, 3)
+                                                       .contiguous().transpose(2, 3)))
+    with pytest.raises(ValueError, match="dS0 has shape"):
+        gdn.gdn_bwd_noalloc(q, k, v, g, beta, ck, dy, out=dict(good, dS0=torch.empty(3)))
+    with pytest.raises(ValueError, match="workspace must be"):
+        gdn.gdn_bwd(q, k, v, g, beta, ck, dy, workspace=torch.empty(64, dtype=torch.uint8)[::2])
+    # all of it well formed: only the device is wrong
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        gdn.gdn_bwd(q, k, v, g, beta, ck, dy, out=good, workspace=torch.empty(64, dtype=torch.uint8))
