@@ -117,7 +117,9 @@ Workspace workspace_layout(const Plan &p) {
     return w;
 }
 
-// Scratch of the chunkwise backward: dq, dk per value head [B,T,Hv,Dk] fp32; dbeta and f
+// Scratch of the chunkwise backward: dq, dk partials [B,T,Hv,Dk] fp32, written only for the
+// value-head groups that the gradient kernel's CTA ranges split (one partial per CTA part, under
+// the part's first head; every other group is summed in tensor memory); dbeta and f
 // partials per block of 64 value rows [B,T,Hv,nsplit] fp32; [dY; dU] [B,Hv,NC,nsplit][128 x 64],
 // Delta [B,Hv,NC,nsplit][64 x 64] and dS at each chunk end [B,Hv,NC,nsplit][64 x Dk], bf16 in
 // their operand layout.
