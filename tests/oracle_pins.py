@@ -180,6 +180,14 @@ def pin_dot_product(lib, seed=4, tol=1e-11, **shape):
     return True, "ok"
 
 
+def pin_strong_decay_dot_product(lib, seed=11, tol=1e-11):
+    """The dot-product test with every decay in [1e-4, 1e-3] (mean log g near -8, the strong
+    profile of the accuracy table in mlx issue #4614, where a chunked kernel's dg was off by
+    orders of magnitude): the forward-mode side never divides by g, so a gradient that loses
+    or inverts a decay factor fails here, however small the decays."""
+    return pin_dot_product(lib, seed=seed, tol=tol, g_range=(1e-4, 1e-3), T=17)
+
+
 # ----------------------------------------------------------------- closed forms
 def pin_identity_decay_no_write(lib, seed=5, tol=1e-12):
     """g = 1, beta = 0: the state never changes. Closed forms for every output."""
@@ -345,6 +353,7 @@ def _compare(checks, tol):
 
 ALL_PINS = [
     pin_finite_differences, pin_directional_fd, pin_forward_mode_jacobian, pin_dot_product,
+    pin_strong_decay_dot_product,
     pin_identity_decay_no_write, pin_zero_decay, pin_single_step, pin_orthonormal_keys,
     pin_fixed_unit_key, pin_exact_retrieval,
 ]

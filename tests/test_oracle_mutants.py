@@ -40,7 +40,11 @@ MUTANTS = [
 # quick pins first: a mutant is killed by the first pin that fails
 ORDER = [P.pin_single_step, P.pin_zero_decay, P.pin_identity_decay_no_write, P.pin_exact_retrieval,
          P.pin_fixed_unit_key, P.pin_orthonormal_keys, P.pin_dot_product, P.pin_directional_fd,
-         P.pin_forward_mode_jacobian, P.pin_finite_differences]
+         P.pin_forward_mode_jacobian, P.pin_finite_differences, P.pin_strong_decay_dot_product]
+
+# mistakes in how the decay enters; the strong-decay pin (g in [1e-4, 1e-3]) must catch each
+# on its own, so that the regime where chunked kernels have lost dg stays covered
+DECAY_MUTANTS = ["dg reads S_t", "A^T du misses g", "carry without decay", "prediction before decay"]
 
 
 @pytest.fixture(scope="module")
@@ -79,3 +83,14 @@ def test_unmutated_copy_passes(tmp_path, source):
         ok, detail = pin(lib)
         assert ok, f"{pin.__name__}: {detail}"
     assert os.path.exists(so)
+
+
+@pytest.mark.parametrize("name", DECAY_MUTANTS)
+def test_strong_decay_pin_alone_catches_decay_mistakes(tmp_path, source, name):
+    (old, new), = [(o, n) for m, o, n, _ in MUTANTS if m == name]
+    src = tmp_path / "mutant.c"
+    src.write_text(source.replace(old, new))
+    so = str(tmp_path / "libmutant.so")
+    oracle.build(str(src), so)
+    ok, detail = P.pin_strong_decay_dot_product(oracle.load(so))
+    assert not ok, f"mutant '{name}' passed the strong-decay pin"
