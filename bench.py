@@ -125,11 +125,12 @@ def bytes_per_step(w):
     return float(fwd + bwd)
 
 
-def kernel_model(w):
+def kernel_model(w, sms=152):
     """Per kernel family: (algorithmic HBM bytes, tensor-core flops, FP32 flops) of one launch.
     Bytes count every tensor a kernel must read or write once (re-reads served by L2 are
     not counted); tensor flops are the issued MMA products of the chunkwise form (2 per
-    multiply-add); FP32 flops apply to the sequential kernels (fp32 inputs)."""
+    multiply-add); FP32 flops apply to the sequential kernels (fp32 inputs). `sms` is the
+    GPU's SM count, which sets the persistent gradient kernel's grid."""
     B, T, Hk, Hv, Dk, Dv, L = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv, w.chunk
     NC = -(-T // L)
     ch, ck = B * Hv * NC, B * Hk * NC               # (chunk, value head), (chunk, kv head)
@@ -154,7 +155,7 @@ def kernel_model(w):
     # value-head groups split between gradient CTAs (one CTA per SM, at most one per unit):
     # at most one per CTA boundary; each CTA's part leaves an fp32 [dq; dk] partial, which
     # chunk_reduce adds (two parts per split group when a CTA holds more units than a group)
-    n_split = min(ch, 152) - 1
+    n_split = min(ch, sms) - 1
     split_bytes = n_split * 2 * 2 * L * Dk * 4
     m["chunk_grad"] = (
         ck * 2 * L * Dk * 2 + ch * (2 * L * Dv * 2 + L * Dv * 2 + 2 * Dv * Dk * 2 + L * 4)
@@ -472,7 +473,7 @@ def run_ours(args, w):
     nbytes = bytes_per_step(w)
     t_roof = max(nbytes / (hbm_gbs * 1e9), f28 / (FP32_PEAK_TFLOPS * 1e12))
     src_hash = kernel_source_hash()
-    model = kernel_model(w)
+    model = kernel_model(w, torch.cuda.get_device_properties(dev).multi_processor_count)
     kernels = {}
     for name, (n, ms) in ktimes.items():
         kernels[name] = kernel_roofline(name, ms / n, model.get(name, (0.0, 0.0, 0.0)), peaks)

@@ -57,7 +57,7 @@ def test_split_group_bytes_bound_the_kernels_cover(name):
     assert len(ranges(units, ctas)) == ctas
     parts, _ = written_parts(units, ctas, rep, w.Hv)
     n_groups = len({g for g, _ in parts})
-    m = bench.kernel_model(w)
+    m = bench.kernel_model(w, sms=152)
     part_bytes = 2 * L * Dk * 4                     # dq and dk partial of one part, fp32
     assert len(parts) * part_bytes <= m["chunk_reduce"][0] - n_groups * 2 * L * Dk * 2
     n_split = min(units, 152) - 1
