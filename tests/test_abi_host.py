@@ -60,11 +60,15 @@ def test_buffer_sizes_follow_the_plan(lib):
     """bf16 with chunk 64 and a supported Dk, Dv: the chunkwise form's saved buffer (larger than
     states + residuals) and workspace (per value head dq, dk: no row-split factor). When the
     chunked backward does not fit shared memory (Dk 128, Dv 256) the workspace is the
-    sequential backward's (row-split partials), while the saved buffer stays chunkwise."""
+    sequential backward's (row-split partials), while the saved buffer stays chunkwise. Dv above
+    256 takes the sequential kernels altogether."""
     def sizes(**kw):
         s = shape(dtype=1, chunk=64, **kw)
         return lib.gdn_ckpt_bytes(ctypes.byref(s)), lib.gdn_bwd_workspace_bytes(ctypes.byref(s))
-    for Dk, Dv, chunked_bwd in ((128, 128, True), (192, 128, True), (64, 64, True), (128, 256, False)):
+    # every supported (Dk, Dv) of the tensor-core forward, and whether its backward fits too
+    table = {64: (64, 128, 192, 256), 128: (64, 128, 192), 192: (64, 128)}
+    cases = [(Dk, Dv, Dv in table[Dk]) for Dk in (64, 128, 192) for Dv in (64, 128, 192, 256)]
+    for Dk, Dv, chunked_bwd in cases:
         T, Hv = 150, 2
         ck, ws = sizes(T=T, Hk=1, Hv=Hv, Dk=Dk, Dv=Dv)
         NC = -(-T // 64)
@@ -76,6 +80,9 @@ def test_buffer_sizes_follow_the_plan(lib):
             assert per_head <= ws < per_head + row_split // 2 + (8 << 20), (Dk, Dv, ws)
         else:
             assert ws >= row_split, (Dk, Dv, ws)
+    for Dk in (64, 128, 192):
+        ck, _ = sizes(T=150, Hk=1, Hv=2, Dk=Dk, Dv=320)
+        assert ck == (2 * 3 * 320 * Dk * 4 + 255) // 256 * 256 + 150 * 2 * 320 * 4
     # fp32 or another chunk size: the sequential layout, states + residuals exactly
     s = shape(dtype=1, chunk=32, T=150, Hk=1, Hv=2, Dk=128, Dv=128)
     assert lib.gdn_ckpt_bytes(ctypes.byref(s)) == (2 * 5 * 128 * 128 * 4 + 255) // 256 * 256 + 150 * 2 * 128 * 4
