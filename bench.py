@@ -493,7 +493,9 @@ def run_ours(args, w):
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": value / PAGES_TOKENS_PER_S if w.name == "linattn-T2048" else None,
         "vs_baseline_note": "ratio to the Apple-silicon Metal VJP figure on the pages (another machine; context)",
-        "dtype": "bf16 tensor-core operands, f32 state and accumulation" if mma > 0 else "f32",
+        "dtype": "bf16" if mma > 0 else "f32",
+        "dtype_note": ("bf16 tensor-core operands, f32 state and accumulation" if mma > 0
+                       else "f32 arithmetic on the sequential kernels"),
         "data": "synthetic",
         "config": config_of(w, l2="flushed between steps by an untimed 256 MiB write"),
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
