@@ -831,7 +831,13 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         // before the next chunk: nothing after this point reads what its first section writes)
         if (tid == 0 && c + 1 < p.NC) issue_r(c + 1);
     }
-    if (ok) epilogue(p.NC - 1);
+    if (ok) {
+        // the previous chunk's y and v - u stores were committed after this chunk's wait: they
+        // must have read ysg and rsg before the last epilogue rewrites them
+        if (tid == 0) bulk_wait_read();
+        __syncthreads();
+        epilogue(p.NC - 1);
+    }
     if (tid == 0) bulk_wait_all();                          // the state stores are complete
     if (ok && p.S_T != nullptr) {
         for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
