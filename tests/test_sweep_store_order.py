@@ -1,4 +1,4 @@
-"""Host-side check of the forward sweep's store order (chunk_sweep_kernel).
+"""Host-side check of the sweeps' store order (chunk_sweep_kernel, chunk_dsweep_kernel).
 
 Per chunk the sweep's thread 0 commits two groups of bulk stores: the chunk-start state (the
 bf16 operand `sop` and the fp32 checkpoint tile `ckst`), and, while the chunk's first product
@@ -48,3 +48,33 @@ def test_missing_wait_before_the_last_epilogue_is_caught(NC):
 
 def test_one_chunk_needs_no_final_wait():
     run_sweep(1, final_wait=False)
+
+
+def run_dsweep(NC, wait_each_chunk=True):
+    """chunk_dsweep_kernel, chunks in reverse: [dY; dU] double-buffered (dY of the next chunk is
+    loaded into the other buffer), one group per chunk storing [dY; dU], Delta and dv from their
+    tiles. Thread 0 waits for all groups once per chunk, before that load and the tile writes."""
+    ring = Ring()
+
+    def write(tiles, what):
+        assert not (ring.reading() & tiles), f"{what} rewritten while a store still reads it"
+
+    write({"ydu0"}, "dY buffer 0")
+    for k in range(NC):
+        buf = k & 1
+        if wait_each_chunk:
+            ring.wait_read_but(0)
+        if k + 1 < NC:
+            write({f"ydu{buf ^ 1}"}, f"dY buffer {buf ^ 1}")
+        write({"dls", "dvs", f"ydu{buf}"}, f"Delta, dv and dU tiles of chunk {k}")
+        ring.groups.append({f"ydu{buf}", "dls", "dvs"})
+
+
+@pytest.mark.parametrize("NC", [1, 2, 3, 32])
+def test_reverse_sweep_tiles_are_never_rewritten_in_flight(NC):
+    run_dsweep(NC)
+
+
+def test_reverse_sweep_without_its_wait_is_caught():
+    with pytest.raises(AssertionError, match="rewritten while a store still reads it"):
+        run_dsweep(3, wait_each_chunk=False)
