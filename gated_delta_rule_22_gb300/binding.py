@@ -53,11 +53,12 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_bwd_workspace_bytes.argtypes = [SP]
     lib.gdn_fwd.restype = ctypes.c_int
-    lib.gdn_fwd.argtypes = [SP] + [_VP] * 10
+    _SZ = ctypes.c_size_t
+    lib.gdn_fwd.argtypes = [SP] + [_VP] * 9 + [_SZ, _VP]
     lib.gdn_bwd.restype = ctypes.c_int
-    lib.gdn_bwd.argtypes = [SP] + [_VP] * 15 + [ctypes.c_size_t, _VP]
+    lib.gdn_bwd.argtypes = [SP] + [_VP] * 6 + [_SZ] + [_VP] * 9 + [_SZ, _VP]
     lib.gdn_bwd_noalloc.restype = ctypes.c_int
-    lib.gdn_bwd_noalloc.argtypes = [SP] + [_VP] * 15
+    lib.gdn_bwd_noalloc.argtypes = [SP] + [_VP] * 6 + [_SZ] + [_VP] * 9
     lib.gdn_gates_fwd.restype = ctypes.c_int
     lib.gdn_gates_fwd.argtypes = [SP] + [_VP] * 7
     lib.gdn_gates_bwd.restype = ctypes.c_int
@@ -74,6 +75,10 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_timing_enable.argtypes = [ctypes.c_int]
     lib.gdn_timing_read.restype = ctypes.c_int
     lib.gdn_timing_read.argtypes = [ctypes.POINTER(GdnKernelTime), ctypes.c_int]
+    lib.gdn_debug_wait_probe.restype = ctypes.c_int
+    lib.gdn_debug_wait_probe.argtypes = [ctypes.c_uint, _VP]
+    lib.gdn_diag_fma_tflops.restype = ctypes.c_int
+    lib.gdn_diag_fma_tflops.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -221,7 +226,7 @@ def gdn_fwd(q, k, v, g, beta, S0=None, chunk=64, *, y=None, S_T=None, ckpt=None,
     if ckpt is None and want_ckpt:
         ckpt = new_ckpt(q, v, chunk)
     rc = lib.gdn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0),
-                     _ptr(y), _ptr(S_T), _ptr(ckpt), _stream(stream, dev))
+                     _ptr(y), _ptr(S_T), _ptr(ckpt), 0 if ckpt is None else _room(ckpt), _stream(stream, dev))
     if rc != GDN_OK:
         raise GdnError("gdn_fwd", rc, lib)
     return y, S_T, ckpt
@@ -272,7 +277,7 @@ def gdn_bwd(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, workspace=None, 
         need = lib.gdn_bwd_workspace_bytes(ctypes.byref(shape))
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     rc = lib.gdn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ckpt),
-                     _ptr(dy), _ptr(dS_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                     _room(ckpt), _ptr(dy), _ptr(dS_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
                      _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out.get("dS0")), _ptr(workspace),
                      workspace.numel() * workspace.element_size(), _stream(stream, q.device))
     if rc != GDN_OK:
@@ -288,7 +293,7 @@ def gdn_bwd_noalloc(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, out=None
     lib = load_library()
     shape, out = _bwd_prepare(q, k, v, g, beta, ckpt, dy, dS_T, chunk, out, want_dS0)
     rc = lib.gdn_bwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ckpt),
-                             _ptr(dy), _ptr(dS_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                             _room(ckpt), _ptr(dy), _ptr(dS_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
                              _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out.get("dS0")),
                              _stream(stream, q.device))
     if rc != GDN_OK:
@@ -300,6 +305,25 @@ def gdn_device_status() -> int:
     """Reads and clears the current device's status word: GDN_OK, or GDN_ERR_TIMEOUT when a
     kernel's bounded wait ran out since the last read (synchronises with the device)."""
     return load_library().gdn_device_status()
+
+
+def gdn_debug_wait_probe(polls: int = 1000, stream=None) -> None:
+    """Enqueue the timeout-path probe (include/gdn.h): one CTA whose bounded wait runs out after
+    `polls` polls and records GDN_ERR_TIMEOUT in the device status word."""
+    lib = load_library()
+    rc = lib.gdn_debug_wait_probe(int(polls), _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError("gdn_debug_wait_probe", rc, lib)
+
+
+def gdn_diag_fma_tflops(packed: bool = False) -> float:
+    """Measured FP32 FMA rate of the current device in TFLOP/s (include/gdn.h)."""
+    lib = load_library()
+    out = ctypes.c_double(0.0)
+    rc = lib.gdn_diag_fma_tflops(1 if packed else 0, ctypes.byref(out))
+    if rc != GDN_OK:
+        raise GdnError("gdn_diag_fma_tflops", rc, lib)
+    return out.value
 
 
 def gdn_strerror(code: int) -> str:

@@ -117,24 +117,19 @@ Workspace workspace_layout(const Plan &p) {
     return w;
 }
 
-// Scratch of the chunkwise backward: dq, dk partials [B,T,Hv,Dk] fp32, written only for the
-// value-head groups that the gradient kernel's CTA ranges split (one partial per CTA part, under
-// the part's first head; every other group is summed in tensor memory); dbeta and f
-// partials per block of 64 value rows [B,T,Hv,nsplit] fp32; [dY; dU] [B,Hv,NC,nsplit][128 x 64],
-// Delta [B,Hv,NC,nsplit][64 x 64] and dS at each chunk end [B,Hv,NC,nsplit][64 x Dk], bf16 in
-// their operand layout.
+// Scratch of the chunkwise backward: dbeta and f partials per block of 64 value rows
+// [B,T,Hv,nsplit] fp32; [dY; dU] [B,Hv,NC,nsplit][128 x 64], Delta [B,Hv,NC,nsplit][64 x 64] and
+// dS at each chunk end [B,Hv,NC,nsplit][64 x Dk], bf16 in their operand layout. (dq, dk are
+// summed over value heads in the gradient kernel's tensor memory and need no scratch.)
 struct TcWorkspace {
-    size_t dq, dk, db, f, yu, dl, dsl, total;
+    size_t db, f, yu, dl, dsl, total;
 };
 
 TcWorkspace tc_workspace_layout(const Plan &p) {
     TcWorkspace w;
-    const size_t nqk = (size_t)p.B * p.T * p.Hv * p.Dk;
     const size_t ngate = (size_t)p.B * p.T * p.Hv * p.nsplit;
     const size_t nblk = (size_t)p.B * p.Hv * p.NC * p.nsplit;
     size_t off = 0;
-    w.dq = off; off += round_up(nqk * 4);
-    w.dk = off; off += round_up(nqk * 4);
     w.db = off; off += round_up(ngate * 4);
     w.f = off; off += round_up(ngate * 4);
     w.yu = off; off += round_up(nblk * 128 * 64 * 2);
@@ -143,6 +138,8 @@ TcWorkspace tc_workspace_layout(const Plan &p) {
     w.total = off;
     return w;
 }
+
+size_t ckpt_total(const Plan &p) { return p.tc ? chunk_layout(p).end : ckpt_state_bytes(p) + ckpt_resid_bytes(p); }
 
 size_t bwd_workspace_total(const Plan &p) { return p.tcb ? tc_workspace_layout(p).total : workspace_layout(p).total; }
 
@@ -409,7 +406,7 @@ int gdn_timing_read(gdn_kernel_time *out, int max_entries) {
 size_t gdn_ckpt_bytes(const gdn_shape *shape) {
     Plan p;
     if (make_plan(shape, &p) != GDN_OK) return 0;
-    return p.tc ? chunk_layout(p).end : ckpt_state_bytes(p) + ckpt_resid_bytes(p);
+    return ckpt_total(p);
 }
 
 size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
@@ -419,7 +416,8 @@ size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
 }
 
 int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
-            const void *beta, const float *S0, void *y, float *S_T, float *ckpt, void *stream) {
+            const void *beta, const float *S0, void *y, float *S_T, float *ckpt, size_t ckpt_bytes,
+            void *stream) {
     Plan p;
     int rc = make_plan(shape, &p);
     if (rc != GDN_OK) return rc;
@@ -427,6 +425,7 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     const void *all[] = {q, k, v, g, beta, S0, y, S_T, ckpt};
     for (const void *ptr : all)
         if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    if (ckpt != nullptr && ckpt_bytes < ckpt_total(p)) return GDN_ERR_BUFFER_TOO_SMALL;
     g_last_error[0] = '\0';
     gdn::FwdParams fp;
     fp.q = q; fp.k = k; fp.v = v; fp.g = g; fp.beta = beta; fp.S0 = S0;
@@ -473,8 +472,8 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
 }
 
 int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
-            const void *beta, const float *ckpt, const void *dy, const float *dS_T, void *dq,
-            void *dk, void *dv, void *dg, void *dbeta, float *dS0, void *workspace,
+            const void *beta, const float *ckpt, size_t ckpt_bytes, const void *dy, const float *dS_T,
+            void *dq, void *dk, void *dv, void *dg, void *dbeta, float *dS0, void *workspace,
             size_t workspace_bytes, void *stream) {
     Plan p;
     int rc = make_plan(shape, &p);
@@ -484,7 +483,7 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     const void *all[] = {q, k, v, g, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace};
     for (const void *ptr : all)
         if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
-    if (workspace_bytes < bwd_workspace_total(p)) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    if (ckpt_bytes < ckpt_total(p) || workspace_bytes < bwd_workspace_total(p)) return GDN_ERR_BUFFER_TOO_SMALL;
     char *ws = static_cast<char *>(workspace);
     if (p.tcb) {
         // chunkwise form on the tensor cores, reading the chunkwise forward's saved buffer
@@ -503,8 +502,6 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.qkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qkm);
         cp.dS_T = dS_T; cp.dS0 = dS0;
         cp.dv = dv; cp.dg = dg; cp.dq = dq; cp.dk = dk; cp.dbeta = dbeta;
-        cp.ws_dq = reinterpret_cast<float *>(ws + tw.dq);
-        cp.ws_dk = reinterpret_cast<float *>(ws + tw.dk);
         cp.ws_db = reinterpret_cast<float *>(ws + tw.db);
         cp.ws_f = reinterpret_cast<float *>(ws + tw.f);
         cp.ws_yu = reinterpret_cast<__nv_bfloat16 *>(ws + tw.yu);
@@ -629,9 +626,9 @@ int static_scratch_address(void **out) {
 extern "C" {
 
 int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k, const void *v,
-                    const void *g, const void *beta, const float *ckpt, const void *dy,
-                    const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta,
-                    float *dS0, void *stream) {
+                    const void *g, const void *beta, const float *ckpt, size_t ckpt_bytes,
+                    const void *dy, const float *dS_T, void *dq, void *dk, void *dv, void *dg,
+                    void *dbeta, float *dS0, void *stream) {
     Plan p;
     int rc = make_plan(shape, &p);
     if (rc != GDN_OK) return rc;
@@ -642,11 +639,12 @@ int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k, const 
     const void *all[] = {q, k, v, g, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0};
     for (const void *ptr : all)
         if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    if (ckpt_bytes < ckpt_total(p)) return GDN_ERR_BUFFER_TOO_SMALL;
     g_last_error[0] = '\0';
     void *scratch = nullptr;
     rc = static_scratch_address(&scratch);
     if (rc != GDN_OK) return rc;
-    return gdn_bwd(shape, q, k, v, g, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, scratch,
+    return gdn_bwd(shape, q, k, v, g, beta, ckpt, ckpt_bytes, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, scratch,
                    GDN_BWD_NOALLOC_SCRATCH_BYTES, stream);
 }
 
@@ -656,7 +654,9 @@ const char *gdn_strerror(int code) {
         case GDN_ERR_INVALID_ARG: return "invalid argument (NULL shape or required pointer, size <= 0, or bad dtype)";
         case GDN_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
         case GDN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (Hv % Hk, Dk, Dv, chunk or tensor size)";
-        case GDN_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than gdn_bwd_workspace_bytes()";
+        case GDN_ERR_BUFFER_TOO_SMALL:
+            return "a caller buffer is too small (ckpt_bytes < gdn_ckpt_bytes() or workspace_bytes < "
+                   "gdn_bwd_workspace_bytes())";
         case GDN_ERR_CUDA: return "CUDA runtime error (see gdn_last_error)";
         case GDN_ERR_TIMEOUT: return "a bounded device-side wait timed out";
         case GDN_ERR_SCRATCH_LIMIT:
@@ -681,5 +681,20 @@ int gdn_device_status(void) {
 }
 
 int gdn_version(void) { return GDN_VERSION; }
+
+int gdn_debug_wait_probe(unsigned polls, void *stream) {
+    if (polls < 1 || polls > gdn::kWaitLimit) return GDN_ERR_INVALID_ARG;
+    int *status = nullptr;
+    int rc = device_status_address(&status);
+    if (rc != GDN_OK) return rc;
+    g_last_error[0] = '\0';
+    return cuda_status(gdn::launch_wait_probe(status, polls, (cudaStream_t)stream));
+}
+
+int gdn_diag_fma_tflops(int packed, double *tflops) {
+    if (tflops == nullptr) return GDN_ERR_INVALID_ARG;
+    g_last_error[0] = '\0';
+    return cuda_status(gdn::measure_fma_rate(packed != 0, tflops));
+}
 
 }  // extern "C"

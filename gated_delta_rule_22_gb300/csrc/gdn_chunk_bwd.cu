@@ -26,16 +26,16 @@
 //                        K dS_L^T takes dS as a bf16 high part plus a bf16 low part (exact to
 //                        about 2^-16): with dS rounded once to bf16, dg under strong decay
 //                        misses the bf16 parity bound.
-//   chunk_grad_kernel    per (b, h, chunk), persistent over consecutive units: everything
-//                        else. dq, dk summed over the value heads of each kv head (ascending)
-//                        in tensor memory, written as bf16 once per group; dbeta summed over
-//                        the value-row blocks (ascending); dg.
-//   chunk_reduce_kernel  dq, dk of the few groups of value heads split between gradient CTAs,
-//                        from one fp32 partial per CTA part (the same ascending order).
+//   chunk_grad_kernel    per (b, h, chunk), persistent over whole groups of units (the value
+//                        heads of one kv head and chunk): everything else. dq, dk summed over
+//                        the value heads of each kv head (ascending) in tensor memory, written
+//                        as bf16 once per group; dbeta summed over the value-row blocks
+//                        (ascending); dg.
 // Operands are bf16 in the core-matrix layout of gdn_umma.cuh, read K-major or MN-major (one
 // stored copy serves a matrix and its transpose); accumulators fp32 in tensor memory. No
-// atomics: every sum has a fixed order for a given grid (the gradient kernel's grid is the SM
-// count, capped by the number of units, so results are bitwise repeatable on one GPU model).
+// atomics, and every sum has a fixed order that depends on nothing but the problem: a group of
+// value heads never straddles two gradient CTAs, so the grid (the SM count) and the batch size
+// leave every result bit unchanged (a batch row's results are those of that row alone).
 #include "gdn_umma.cuh"
 
 namespace gdn {
@@ -449,8 +449,9 @@ struct GradSmem {
 
 }  // namespace
 
-// Persistent: one CTA per SM, each over a contiguous range of units (b, chunk, value head),
-// value head fastest, so that consecutive units share [Q; K]. Every operand arrives by bulk
+// Persistent: one CTA per SM, each over a contiguous range of whole groups of units (b, chunk,
+// value head), value head fastest, so that consecutive units share [Q; K] and the value heads
+// of a kv head are summed by one CTA, in ascending order, whatever the grid. Every operand arrives by bulk
 // copy, the next unit's as soon as its buffers are free, all after the second products:
 // [dY; dU], Delta (scaled in place by E_L for the second products) and dS_L, S0 (whose region
 // then holds the scratch operands) and [Q; K] (when the kv head or chunk changes).
@@ -459,13 +460,13 @@ struct GradSmem {
 //                       dK), then (diag(E_L) Delta) dS_L + GE^T Q + HE^T K, whose A operands are
 //                       read from 64 rows before the real ones, so that row t lands in the lane
 //                       of dK row t (rows 0-63 are not used)
-//   [DK, 2 DK)          RS, M = 128: [dQ; dK] summed over the value heads of this CTA's part of
-//                       the kv head's group: per unit += diag(e^Lam) [dY; dU] S0 (from R1, on the
+//   [DK, 2 DK)          RS, M = 128: [dQ; dK] summed over the value heads of the kv head's
+//                       group: per unit += diag(e^Lam) [dY; dU] S0 (from R1, on the
 //                       CUDA cores), += [GE; HE] K (MMA), rows 64-127 += R1's second terms
 //   [2 DK, 2 DK + 64)   [Q; K] K^T (M = 128), formed once per (b, chunk, kv head)
 //   [2 DK + 64, + 128)  [dY; dU] Delta^T = [G; H] (M = 128), later [W1; W2] M (M = 128)
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, int units) {
+__global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, int groups) {
     constexpr int DK = 32 * E;
     constexpr int SC = DK / 2;
     static_assert(2 * DK + 128 <= 512, "tensor memory");
@@ -473,8 +474,9 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, Hk = p.Hk, nsplit = p.nsplit, NC = p.NC, rep = Hv / Hk;
     const int quarter = warp & 3, half = warp >> 2;
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    const int u_begin = (int)((long long)blockIdx.x * units / gridDim.x);
-    const int u_end = (int)((long long)(blockIdx.x + 1) * units / gridDim.x);
+    // unit u = ((b * NC + c) * Hk + hk) * rep + (h % rep): group u / rep
+    const int u_begin = (int)((long long)blockIdx.x * groups / gridDim.x) * rep;
+    const int u_end = (int)((long long)(blockIdx.x + 1) * groups / gridDim.x) * rep;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 128));
@@ -603,11 +605,10 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         }
         tc_fence_after();
         if (!ok) break;
-        // this unit's place in its group of value heads (one kv head, one chunk): the first and
-        // last of the group's heads in this CTA's range, and whether the whole group is in it
-        const int hh = h % rep, g0 = u - hh;
-        const bool gfirst = hh == 0 || u == u_begin, glast = hh == rep - 1 || u + 1 == u_end;
-        const bool whole = g0 >= u_begin && g0 + rep <= u_end;
+        // this unit's place in its group of value heads (one kv head, one chunk), which lies
+        // wholly in this CTA's range
+        const int hh = h % rep;
+        const bool gfirst = hh == 0, glast = hh == rep - 1;
         // ---- first products: [Q; K] K^T (when the kv head or chunk changes), [dY; dU] Delta^T,
         // [dY; dU] S0
         if (tid == 0) {
@@ -820,12 +821,9 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
-            // ---- dq (rows 0-63) and dk (rows 64-127) of the group's value heads in this CTA's
-            // range, from RS: bf16 when the whole group lies in the range; otherwise an fp32
-            // partial under the head that starts this CTA's part, for chunk_reduce_kernel. A row
+            // ---- dq (rows 0-63) and dk (rows 64-127) of the group, from RS, as bf16. A row
             // quarter at a time passes through a padded shared-memory tile, so that each warp
-            // access covers 512 contiguous bytes of one row.
-            const int hs = h - (u - max(g0, u_begin));
+            // access covers 256 contiguous bytes of one row.
             __nv_bfloat16 *outq = static_cast<__nv_bfloat16 *>(p.dq), *outk = static_cast<__nv_bfloat16 *>(p.dk);
             const size_t hk = (size_t)(h / rep);
             constexpr int NE = DK / 32;                     // float4 of a row quarter per thread
@@ -847,13 +845,9 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                     const int e = tid + 256 * i, rr = e / (DK / 4), c4 = e - rr * (DK / 4), r2 = 32 * q + rr, s = r2 & (kL - 1);
                     if (s >= len) continue;
                     const float4 v4 = *reinterpret_cast<const float4 *>(stg + rr * RSt + 4 * c4);
-                    if (!whole) {
-                        *reinterpret_cast<float4 *>((r2 >= kL ? p.ws_dk : p.ws_dq) + ((rowbase + s) * Hv + hs) * DK + 4 * c4) = v4;
-                    } else {
-                        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>((r2 >= kL ? outk : outq) + ((rowbase + s) * Hk + hk) * DK + 4 * c4);
-                        o2[0] = __floats2bfloat162_rn(v4.x, v4.y);
-                        o2[1] = __floats2bfloat162_rn(v4.z, v4.w);
-                    }
+                    __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>((r2 >= kL ? outk : outq) + ((rowbase + s) * Hk + hk) * DK + 4 * c4);
+                    o2[0] = __floats2bfloat162_rn(v4.x, v4.y);
+                    o2[1] = __floats2bfloat162_rn(v4.z, v4.w);
                 }
                 __syncthreads();
             }
@@ -875,45 +869,6 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// dq, dk of the groups of value heads (one kv head, one chunk) that the gradient kernel's unit
-// ranges split between two or more CTAs: each CTA left the sum over its part of the group as
-// an fp32 partial under the part's first head; the parts are added in ascending order, to
-// bf16. Four blocks of 16 rows per boundary between consecutive CTA ranges; the first
-// boundary inside a group handles it.
-__global__ void __launch_bounds__(256) chunk_reduce_kernel(ChunkBwdParams p, int Dk, int units, int ctas) {
-    const int i = blockIdx.x / 4 + 1, rq = blockIdx.x % 4;
-    const int rep = p.Hv / p.Hk;
-    const int ub = (int)((long long)i * units / ctas);
-    if (i >= ctas || ub % rep == 0) return;                  // no boundary, or one between groups
-    const int g = ub / rep;
-    if ((int)((long long)(i - 1) * units / ctas) > g * rep) return;   // an earlier boundary handles it
-    const int hk = g % p.Hk, bc = g / p.Hk, c = bc % p.NC, b = bc / p.NC;
-    const int t0 = c * 64, len = min(64, p.T - t0);
-    __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.dq);
-    __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(p.dk);
-    for (int e = threadIdx.x; e < 16 * Dk / 4; e += blockDim.x) {
-        const int s = 16 * rq + e / (Dk / 4), j = 4 * (e % (Dk / 4));
-        if (s >= len) break;
-        const size_t bt = (size_t)b * p.T + t0 + s;
-        float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
-        // the parts' first units: the group's first, then each CTA boundary inside the group
-        for (int k = i - 1; k < ctas; ++k) {
-            const int us = k == i - 1 ? g * rep : (int)((long long)k * units / ctas);
-            if (us >= (g + 1) * rep) break;
-            const size_t o = (bt * p.Hv + us % p.Hv) * Dk + j;
-            const float4 a = *reinterpret_cast<const float4 *>(p.ws_dq + o);
-            const float4 b2 = *reinterpret_cast<const float4 *>(p.ws_dk + o);
-            sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
-            sk.x += b2.x; sk.y += b2.y; sk.z += b2.z; sk.w += b2.w;
-        }
-        const size_t oo = (bt * p.Hk + hk) * Dk + j;
-        __nv_bfloat162 *q2 = reinterpret_cast<__nv_bfloat162 *>(dq + oo);
-        __nv_bfloat162 *k2 = reinterpret_cast<__nv_bfloat162 *>(dk + oo);
-        q2[0] = __floats2bfloat162_rn(sq.x, sq.y); q2[1] = __floats2bfloat162_rn(sq.z, sq.w);
-        k2[0] = __floats2bfloat162_rn(sk.x, sk.y); k2[1] = __floats2bfloat162_rn(sk.z, sk.w);
-    }
-}
-
 size_t chunk_dsweep_smem(int Dk) { return DSweepSmem(Dk).total; }
 size_t chunk_grad_smem(int Dk, int Dv) { return GradSmem(Dk, Dv).total; }
 
@@ -932,20 +887,15 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     timing_mark("chunk_grad", 0, s);
-    const int units = p.NC * p.Hv * p.B;
+    const int groups = p.NC * p.Hk * p.B;                   // (b, chunk, kv head)
     int dev = 0, sms = 0;
     err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    const int grid = units < sms ? units : sms;             // persistent: one CTA per SM
-    chunk_grad_kernel<E><<<grid, 256, sg, s>>>(p, units);
+    const int grid = groups < sms ? groups : sms;           // persistent: one CTA per SM
+    chunk_grad_kernel<E><<<grid, 256, sg, s>>>(p, groups);
     timing_mark("chunk_grad", 1, s);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    timing_mark("chunk_reduce", 0, s);
-    chunk_reduce_kernel<<<4 * (grid > 1 ? grid - 1 : 1), 256, 0, s>>>(p, DK, units, grid);
-    timing_mark("chunk_reduce", 1, s);
     return cudaGetLastError();
 }
 

@@ -100,8 +100,6 @@ struct ChunkBwdParams {
     const float *dS_T;
     float *dS0;
     void *dv, *dg, *dq, *dk, *dbeta;
-    float *ws_dq, *ws_dk;      // [B, T, Hv, Dk]: a gradient CTA's part of a group of value heads split between CTAs,
-                               // under the part's first head
     float *ws_db, *ws_f;       // [B, T, Hv, nsplit]: per block of 64 value rows
     __nv_bfloat16 *ws_yu;      // [B, Hv, NC, nsplit][128 x 64]: [dY; dU] of the block, operand layout
     __nv_bfloat16 *ws_dl;      // [B, Hv, NC, nsplit][64 x 64]: Delta = diag(beta) (v - u), operand layout
@@ -226,10 +224,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, unsigned bytes) {
                  : "memory");
 }
 
-// Bounded wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
+// Bounded wait for the phase with the given parity to complete (at most `limit` polls); false
+// on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned limit = kWaitLimit) {
     const uint32_t a = smem_addr(bar);
-    for (unsigned it = 0; it < kWaitLimit; ++it) {
+    for (unsigned it = 0; it < limit; ++it) {
         uint32_t done;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -489,5 +488,9 @@ cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, 
 size_t chunk_dsweep_smem(int Dk);
 size_t chunk_grad_smem(int Dk, int Dv);
 cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s);
+// Diagnostics (gdn_diag.cu): a CTA whose bounded wait cannot succeed (the timeout path), and
+// the FP32 FMA issue rate of the whole GPU.
+cudaError_t launch_wait_probe(int *status, unsigned polls, cudaStream_t s);
+cudaError_t measure_fma_rate(int packed, double *tflops);
 
 }  // namespace gdn

@@ -14,6 +14,10 @@
 // Arithmetic is fp32 (the parameter sums in fp64), elementwise and memory-bound.
 #include "gdn_common.cuh"
 
+#include <cooperative_groups.h>
+
+namespace cg = cooperative_groups;
+
 namespace gdn {
 
 namespace {
@@ -45,24 +49,31 @@ __global__ void __launch_bounds__(256) gates_fwd_kernel(GatesParams p) {
     }
 }
 
-// One CTA per group of 32 value heads (lane = head), its warps walking the rows in a fixed
-// interleaved order; the per-head parameter sums are added over the warps in ascending
-// order, so the result does not depend on scheduling.
+// A cluster of kGateSplit CTAs per group of 32 value heads (lane = head): CTA y of the cluster
+// and warp w walk rows y * 32 + w, then every kGateSplit * 32 rows further (a fixed interleaved
+// order). The per-head parameter sums are added over a CTA's warps in ascending order, then
+// over the cluster's CTAs in ascending order by its first CTA, which reads the others' partials
+// from their shared memory: the result does not depend on scheduling.
+constexpr int kGateSplit = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(1024) gates_bwd_kernel(GatesParams p) {
+__global__ void __cluster_dims__(1, kGateSplit, 1) __launch_bounds__(1024) gates_bwd_kernel(GatesParams p) {
     __shared__ double part[2][32][33];
+    __shared__ double cta_sum[2][32];
     const T *a = static_cast<const T *>(p.a);
     const T *b = static_cast<const T *>(p.b);
     const T *dg = static_cast<const T *>(p.dg);
     const T *dbeta = static_cast<const T *>(p.dbeta);
     T *da = static_cast<T *>(p.da);
     T *db = static_cast<T *>(p.db);
+    cg::cluster_group cluster = cg::this_cluster();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int h = blockIdx.x * 32 + lane;
+    const size_t stride = (size_t)gridDim.y * nw;
     double sA = 0.0, sdt = 0.0;
     if (h < p.Hv) {
         const float A = expf(p.A_log[h]), dt = p.dt_bias[h];
-        for (size_t r = warp; r < (size_t)p.rows; r += nw) {
+        for (size_t r = (size_t)blockIdx.y * nw + warp; r < (size_t)p.rows; r += stride) {
             const size_t i = r * p.Hv + h;
             const float x = to_f32(a[i]) + dt;
             const float log_g = -A * softplus_f(x);
@@ -78,15 +89,27 @@ __global__ void __launch_bounds__(1024) gates_bwd_kernel(GatesParams p) {
     part[0][warp][lane] = sA;
     part[1][warp][lane] = sdt;
     __syncthreads();
-    if (warp == 0 && h < p.Hv) {
+    if (warp == 0) {
         double tA = 0.0, tdt = 0.0;
         for (int w = 0; w < nw; ++w) {
             tA += part[0][w][lane];
             tdt += part[1][w][lane];
         }
+        cta_sum[0][lane] = tA;
+        cta_sum[1][lane] = tdt;
+    }
+    cluster.sync();                      // every CTA's sums are in its shared memory
+    if (cluster.block_rank() == 0 && warp == 0 && h < p.Hv) {
+        double tA = 0.0, tdt = 0.0;
+        for (unsigned r = 0; r < cluster.num_blocks(); ++r) {
+            const double *o = cluster.map_shared_rank(&cta_sum[0][0], r);
+            tA += o[lane];
+            tdt += o[32 + lane];
+        }
         p.dA_log[h] = (float)tA;
         p.ddt_bias[h] = (float)tdt;
     }
+    cluster.sync();                      // no CTA leaves while the first still reads its sums
 }
 
 cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s) {
@@ -101,10 +124,10 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s) {
 }
 
 cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s) {
-    const int blocks = (p.Hv + 31) / 32;
+    const dim3 grid((p.Hv + 31) / 32, kGateSplit);          // one cluster per 32 value heads
     timing_mark("gates_bwd", 0, s);
-    if (dtype == 0) gates_bwd_kernel<float><<<blocks, 1024, 0, s>>>(p);
-    else gates_bwd_kernel<__nv_bfloat16><<<blocks, 1024, 0, s>>>(p);
+    if (dtype == 0) gates_bwd_kernel<float><<<grid, 1024, 0, s>>>(p);
+    else gates_bwd_kernel<__nv_bfloat16><<<grid, 1024, 0, s>>>(p);
     timing_mark("gates_bwd", 1, s);
     return cudaGetLastError();
 }

@@ -35,9 +35,10 @@
  *   - Every argument check runs on the host before anything is enqueued: a call
  *     that returns an error has launched nothing and written nothing.
  *   - Results are bitwise deterministic: no atomics; every reduction (over rows,
- *     over the value heads that share a kv head) runs in a fixed order. The bf16
- *     tensor-core backward groups the sum over value heads by its grid, which is the
- *     GPU's SM count, so repeat runs agree bit for bit on one GPU model.
+ *     over the value heads that share a kv head) runs in a fixed order that depends
+ *     only on the problem, not on the grid or the GPU's SM count, and a batch row's
+ *     results do not depend on the other rows (B = 8 gives, bit for bit, what eight
+ *     B = 1 calls give).
  *   - There is no host fallback: if the GPU cannot run a kernel the call returns
  *     GDN_ERR_CUDA.
  */
@@ -50,7 +51,7 @@
 extern "C" {
 #endif
 
-#define GDN_VERSION 1
+#define GDN_VERSION 2
 
 #if defined(__GNUC__)
 #define GDN_API __attribute__((visibility("default")))
@@ -77,7 +78,9 @@ enum {
     GDN_ERR_UNSUPPORTED_SHAPE = -3, /* Hv % Hk != 0, Dk not in {32,64,96,128,160,192,224,256},
                                        Dv % 4 != 0 or Dv > 4096, chunk outside 1..128,
                                        B or Hv > 65535, or a tensor too large to index */
-    GDN_ERR_WORKSPACE_TOO_SMALL = -4,
+    GDN_ERR_BUFFER_TOO_SMALL = -4,  /* ckpt_bytes < gdn_ckpt_bytes(shape), or workspace_bytes <
+                                       gdn_bwd_workspace_bytes(shape) */
+    GDN_ERR_WORKSPACE_TOO_SMALL = GDN_ERR_BUFFER_TOO_SMALL,
     GDN_ERR_CUDA = -5,              /* the CUDA runtime reported an error (see gdn_last_error) */
     GDN_ERR_TIMEOUT = -6,           /* a bounded device-side wait ran out (gdn_device_status) */
     GDN_ERR_SCRATCH_LIMIT = -7      /* gdn_bwd_noalloc: the problem needs more scratch than
@@ -107,8 +110,11 @@ GDN_API size_t gdn_bwd_workspace_bytes(const gdn_shape *shape);
  *        S0                          (float32, may be NULL: zeros)
  *   out: y                           (dtype)
  *        S_T                         (float32, may be NULL: not written)
- *        ckpt                        (float32, gdn_ckpt_bytes(shape) bytes, 16-byte aligned;
- *                                    may be NULL: nothing saved):
+ *        ckpt, ckpt_bytes            (float32; ckpt_bytes is the size of the buffer that ckpt
+ *                                    points to, at least gdn_ckpt_bytes(shape), else the call
+ *                                    returns GDN_ERR_BUFFER_TOO_SMALL before anything is
+ *                                    enqueued; 16-byte aligned; ckpt may be NULL: nothing
+ *                                    saved, ckpt_bytes ignored):
  *                                    ckpt[b, h, c] = state before step c*C, [B,Hv,NC,Dv,Dk];
  *                                    then, from the next 256-byte boundary, the residuals
  *                                    r[b, t, h, :] = v_t - u_t, u_t = g_t S_{t-1} k_t,
@@ -117,15 +123,16 @@ GDN_API size_t gdn_bwd_workspace_bytes(const gdn_shape *shape);
  */
 GDN_API int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
                     const void *g, const void *beta, const float *S0, void *y, float *S_T,
-                    float *ckpt, void *stream);
+                    float *ckpt, size_t ckpt_bytes, void *stream);
 
 /*
  * Reverse-time VJP. Gradients of L = <dy, y> + <dS_T, S_T> with respect to q, k, v, g,
  * beta and S0, for the forward defined by the same inputs. The pages print no backward
  * formula; this is the chain rule applied to the recurrence above, in reverse time.
  *   in : q, k, v, g, beta, dy        (dtype)
- *        ckpt                        (float32, gdn_ckpt_bytes(shape) bytes) as written by
- *                                    gdn_fwd for the same inputs, shape and S0
+ *        ckpt, ckpt_bytes            (float32) as written by gdn_fwd for the same inputs,
+ *                                    shape and S0; ckpt_bytes is the buffer's size, at least
+ *                                    gdn_ckpt_bytes(shape) (else GDN_ERR_BUFFER_TOO_SMALL)
  *        dS_T                        (float32, may be NULL: zeros)
  *   out: dq, dk                      (dtype) summed over the value heads of each kv head,
  *                                    in ascending value-head order
@@ -137,9 +144,10 @@ GDN_API int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const 
  * Returns GDN_OK or an error code.
  */
 GDN_API int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
-                    const void *g, const void *beta, const float *ckpt, const void *dy,
-                    const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta,
-                    float *dS0, void *workspace, size_t workspace_bytes, void *stream);
+                    const void *g, const void *beta, const float *ckpt, size_t ckpt_bytes,
+                    const void *dy, const float *dS_T, void *dq, void *dk, void *dv, void *dg,
+                    void *dbeta, float *dS0, void *workspace, size_t workspace_bytes,
+                    void *stream);
 
 /*
  * Backward without any allocation (no counterpart on the pages: it is a convenience of this
@@ -167,9 +175,9 @@ GDN_API int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const 
  */
 #define GDN_BWD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 GDN_API int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k, const void *v,
-                            const void *g, const void *beta, const float *ckpt, const void *dy,
-                            const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta,
-                            float *dS0, void *stream);
+                            const void *g, const void *beta, const float *ckpt, size_t ckpt_bytes,
+                            const void *dy, const float *dS_T, void *dq, void *dk, void *dv,
+                            void *dg, void *dbeta, float *dS0, void *stream);
 
 /*
  * Gates of the layer: the decay g and write strength beta from its raw gate inputs, and the
@@ -226,6 +234,24 @@ GDN_API int gdn_timing_enable(int on);
  * number of families recorded (which may exceed max_entries; out may then be NULL with
  * max_entries 0), or GDN_ERR_CUDA. */
 GDN_API int gdn_timing_read(gdn_kernel_time *out, int max_entries);
+
+/* ---- Diagnostics (no counterpart on the pages). */
+
+/* Exercises the timeout path of the library's bounded device-side waits without faulting or
+ * hanging anything: enqueues on `stream` one CTA that allocates tensor memory, arms an mbarrier
+ * for bytes that no copy will ever deliver (so nothing is in flight), polls it `polls` times
+ * (1 .. 2^24), records GDN_ERR_TIMEOUT in the device status word (gdn_device_status), frees its
+ * tensor memory and exits, exactly as a kernel of the library does when a wait runs out. The
+ * GPU context stays usable. Returns GDN_OK (launched), GDN_ERR_INVALID_ARG (polls out of range)
+ * or GDN_ERR_CUDA. */
+GDN_API int gdn_debug_wait_probe(unsigned polls, void *stream);
+
+/* Measured FP32 fused multiply-add rate of the current device in TFLOP/s (2 flops per FMA and
+ * lane): scalar FFMA (packed = 0) or the packed two-lane f32x2 form (packed = 1) that the
+ * sequential kernels use, from independent chains whose only distinct register operand is
+ * the accumulator, on 8 CTAs of 256 threads per SM, best of three timed launches on a
+ * private stream. Synchronises with that stream. Returns GDN_OK or GDN_ERR_CUDA. */
+GDN_API int gdn_diag_fma_tflops(int packed, double *tflops);
 
 #ifdef __cplusplus
 }

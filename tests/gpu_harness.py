@@ -53,6 +53,17 @@ def errors(got: dict, ref: dict) -> dict:
     return {n: oracle.rel_l2(got[n], ref[n]) for n in ref if n in got}
 
 
+def log_errors(label: str, errs: dict) -> None:
+    """Append one JSON line {label, errors} to the file named by $GDN_PARITY_LOG, if set (a
+    record of the per-output errors of a parity run)."""
+    import json
+    import os
+    path = os.environ.get("GDN_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": label, "rel_l2": errs}) + "\n")
+
+
 def group_outputs(out: dict, w, b: int, hk: int) -> dict:
     """The outputs of one (batch row, kv head) group, as numpy float64, laid out like a
     B=1, Hk=1 problem (matches oracle.group_slice)."""

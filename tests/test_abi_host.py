@@ -28,15 +28,21 @@ def shape(**kw):
     return B.GdnShape(**base)
 
 
-def fwd(lib, s, **ptrs):
+def _ck_bytes(lib, s, ck_bytes):
+    if ck_bytes is None:
+        ck_bytes = lib.gdn_ckpt_bytes(ctypes.byref(s)) if s is not None else 0
+    return ck_bytes
+
+
+def fwd(lib, s, ck_bytes=None, **ptrs):
     p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, S0=None, y=FAKE, S_T=None, ckpt=FAKE)
     p.update(ptrs)
     args = [ctypes.c_void_p(p[n]) if p[n] is not None else None for n in
             ("q", "k", "v", "g", "beta", "S0", "y", "S_T", "ckpt")]
-    return lib.gdn_fwd(ctypes.byref(s) if s is not None else None, *args, None)
+    return lib.gdn_fwd(ctypes.byref(s) if s is not None else None, *args, _ck_bytes(lib, s, ck_bytes), None)
 
 
-def bwd(lib, s, ws_bytes=None, **ptrs):
+def bwd(lib, s, ws_bytes=None, ck_bytes=None, **ptrs):
     p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, ckpt=FAKE, dy=FAKE, dS_T=None, dq=FAKE, dk=FAKE,
              dv=FAKE, dg=FAKE, dbeta=FAKE, dS0=None, ws=FAKE)
     p.update(ptrs)
@@ -44,7 +50,8 @@ def bwd(lib, s, ws_bytes=None, **ptrs):
     args = [ctypes.c_void_p(p[n]) if p[n] is not None else None for n in names]
     if ws_bytes is None:
         ws_bytes = lib.gdn_bwd_workspace_bytes(ctypes.byref(s)) if s is not None else 0
-    return lib.gdn_bwd(ctypes.byref(s) if s is not None else None, *args, ws_bytes, None)
+    return lib.gdn_bwd(ctypes.byref(s) if s is not None else None, *args[:6], _ck_bytes(lib, s, ck_bytes),
+                       *args[6:], ws_bytes, None)
 
 
 def test_exports_every_header_function(lib):
@@ -53,15 +60,16 @@ def test_exports_every_header_function(lib):
                           "gdn_strerror", "gdn_last_error", "gdn_version"}
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/gdn.h but not exported"
-    assert lib.gdn_version() == 1
+    assert lib.gdn_version() == 2
 
 
 def test_buffer_sizes_follow_the_plan(lib):
     """bf16 with chunk 64 and a supported Dk, Dv: the chunkwise form's saved buffer (larger than
-    states + residuals) and workspace (per value head dq, dk: no row-split factor). When the
-    chunked backward does not fit shared memory (Dk 128, Dv 256) the workspace is the
-    sequential backward's (row-split partials), while the saved buffer stays chunkwise. Dv above
-    256 takes the sequential kernels altogether."""
+    states + residuals) and workspace (per 64-row block of a value head: dbeta and f partials,
+    and the [dY; dU], Delta and dS operand tiles; no dq, dk partials). When the chunked backward
+    does not fit shared memory (Dk 128, Dv 256) the workspace is the sequential backward's
+    (row-split partials), while the saved buffer stays chunkwise. Dv above 256 takes the
+    sequential kernels altogether."""
     def sizes(**kw):
         s = shape(dtype=1, chunk=64, **kw)
         return lib.gdn_ckpt_bytes(ctypes.byref(s)), lib.gdn_bwd_workspace_bytes(ctypes.byref(s))
@@ -74,10 +82,13 @@ def test_buffer_sizes_follow_the_plan(lib):
         NC = -(-T // 64)
         states, resid = Hv * NC * Dv * Dk * 4, T * Hv * Dv * 4
         assert ck > states + resid + 256, (Dk, Dv)
-        per_head = 2 * T * Hv * Dk * 4
         row_split = 2 * T * Hv * (Dv // 64) * Dk * 4
         if chunked_bwd:
-            assert per_head <= ws < per_head + row_split // 2 + (8 << 20), (Dk, Dv, ws)
+            r = lambda x: -(-x // 256) * 256  # noqa: E731
+            ns = Dv // 64
+            nblk = Hv * NC * ns
+            want = 2 * r(T * Hv * ns * 4) + r(nblk * 128 * 64 * 2) + r(nblk * 64 * 64 * 2) + r(nblk * 64 * Dk * 2)
+            assert ws == want, (Dk, Dv, ws, want)
         else:
             assert ws >= row_split, (Dk, Dv, ws)
     for Dk in (64, 128, 192):
@@ -144,6 +155,27 @@ def test_workspace_too_small(lib):
     need = lib.gdn_bwd_workspace_bytes(ctypes.byref(s))
     assert bwd(lib, s, ws_bytes=need - 1) == WS_SMALL
     assert bwd(lib, s, ws_bytes=0) == WS_SMALL
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(dtype=1, chunk=64, T=150, Hk=1, Hv=2, Dk=192, Dv=128)])
+def test_checkpoint_buffer_too_small(lib, kw):
+    """A saved-for-backward buffer sized from the [B, Hv, NC, Dv, Dk] states alone (or one byte
+    short of gdn_ckpt_bytes) is refused on the host, before anything is enqueued, by both the
+    forward and the backward (the fake pointers are never touched). The tensor-core shape's
+    buffer holds more than the states, so the states-only size is short there too."""
+    s = shape(**kw)
+    need = lib.gdn_ckpt_bytes(ctypes.byref(s))
+    NC = -(-s.T // (s.chunk or 64))
+    states = s.B * s.Hv * NC * s.Dv * s.Dk * 4
+    assert states < need
+    for n in (need - 1, states, 0):
+        assert fwd(lib, s, ck_bytes=n) == WS_SMALL, n
+        assert bwd(lib, s, ck_bytes=n) == WS_SMALL, n
+        fake = ctypes.c_void_p(FAKE)
+        rc = lib.gdn_bwd_noalloc(ctypes.byref(s), *([fake] * 6), n, fake, None, *([fake] * 5), None, None)
+        assert rc == WS_SMALL or rc == -7, n   # or refused for its scratch size first
+    # no saved buffer (inference): its size is not looked at
+    assert fwd(lib, s, ck_bytes=0, ckpt=None, q=FAKE + 4) == MISALIGNED
 
 
 GATE_FWD = ("a", "b", "A_log", "dt_bias", "g", "beta")
@@ -245,3 +277,10 @@ def test_binding_checks_caller_outputs(lib):
     # all of it well formed: only the device is wrong
     with pytest.raises(ValueError, match="CUDA tensors"):
         gdn.gdn_bwd(q, k, v, g, beta, ck, dy, out=good, workspace=torch.empty(64, dtype=torch.uint8))
+
+
+def test_diagnostic_argument_checks(lib):
+    """Refused on the host before any CUDA call."""
+    assert lib.gdn_debug_wait_probe(0, None) == INVALID
+    assert lib.gdn_debug_wait_probe((1 << 24) + 1, None) == INVALID
+    assert lib.gdn_diag_fma_tflops(0, None) == INVALID

@@ -1,13 +1,12 @@
 """Host checks of bench.py's bookkeeping: the source hash that keys the measured DRAM traffic,
-the per-kernel roofline choice, and the gradient kernels' split-group bytes against the
-kernels' own cover of the value-head groups (mirrored in test_chunk_split_groups)."""
+the per-kernel roofline choice, and the per-kernel algorithmic bytes (each tensor of the
+method's byte count attributed to exactly one kernel of its pass)."""
 import os
 
 import pytest
 
 import bench
 import gdn_synthetic as gs
-from test_chunk_split_groups import ranges, written_parts
 
 CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                     "gated_delta_rule_22_gb300", "csrc")
@@ -45,21 +44,30 @@ def test_roofline_takes_the_slowest_bound():
     assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(500.0) and r["frac"] == pytest.approx(0.5)
 
 
-@pytest.mark.parametrize("name", [n for n, w in gs.WORKLOADS.items() if w.dtype == "bf16"])
-def test_split_group_bytes_bound_the_kernels_cover(name):
-    """bench.py counts, per CTA boundary, two fp32 [dq; dk] parts (gradient kernel writes,
-    reduction reads) and one bf16 group (reduction writes): an upper bound on what the
-    kernels' unit ranges actually split, for a GB300's 152 SMs."""
+FWD = {"q", "k", "v", "g", "beta", "S0", "y", "S_T", "ckpt"}
+BWD = {"q", "k", "v", "g", "beta", "ckpt", "dy", "dS_T", "dq", "dk", "dv", "dg", "dbeta", "dS0"}
+
+
+@pytest.mark.parametrize("kernels,tensors", [
+    (("chunk_prep", "chunk_sweep"), FWD), (("chunk_dsweep", "chunk_grad"), BWD),
+    (("seq_fwd",), FWD), (("seq_bwd", "seq_reduce"), BWD),
+])
+def test_each_tensor_of_a_pass_credited_to_one_kernel(kernels, tensors):
+    got = [n for k in kernels for n in bench.PASS_TENSORS[k]]
+    assert sorted(got) == sorted(tensors)
+
+
+@pytest.mark.parametrize("name", sorted(gs.WORKLOADS))
+def test_kernel_bytes_add_up_to_the_step(name):
     w = gs.WORKLOADS[name]
-    NC = -(-w.T // w.chunk)
-    units, rep, L, Dk = w.B * NC * w.Hv, w.Hv // w.Hk, w.chunk, w.Dk
-    ctas = min(units, 152)
-    assert len(ranges(units, ctas)) == ctas
-    parts, _ = written_parts(units, ctas, rep, w.Hv)
-    n_groups = len({g for g, _ in parts})
-    m = bench.kernel_model(w, sms=152)
-    part_bytes = 2 * L * Dk * 4                     # dq and dk partial of one part, fp32
-    assert len(parts) * part_bytes <= m["chunk_reduce"][0] - n_groups * 2 * L * Dk * 2
-    n_split = min(units, 152) - 1
-    assert n_groups <= n_split
-    assert m["chunk_reduce"][0] == pytest.approx(n_split * (2 * part_bytes + 2 * L * Dk * 2))
+    m = bench.kernel_model(w)
+    step = bench.bytes_per_step(w)
+    assert sum(m[k][0] for k in ("chunk_prep", "chunk_sweep", "chunk_dsweep", "chunk_grad")) == pytest.approx(step)
+    assert sum(m[k][0] for k in ("seq_fwd", "seq_bwd", "seq_reduce")) == pytest.approx(step)
+
+
+def test_step_bytes_at_the_headline_shape():
+    """linattn-T2048 (no S0, no dS_T): q, k 12.6 MB each, v, y, dy, dv 33.6 MB each, checkpoints
+    32 x 6.29 MB: 660.1 MB per step."""
+    w = gs.WORKLOADS["linattn-T2048"]
+    assert bench.bytes_per_step(w) == pytest.approx(660.1e6, rel=1e-3)

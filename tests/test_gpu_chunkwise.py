@@ -34,9 +34,9 @@ CASES = [
     # three batch rows with a ragged last chunk each and no GQA: the persistent gradient
     # kernel's unit ranges cross batch rows and kv heads
     gs.Workload("tc-B3-ragged-noGQA", 3, 190, 3, 3, 128, 128, "bf16", "strong", True, True, 64),
-    # 24 value heads on one kv head and one unit per gradient CTA: dq, dk of each chunk are the
-    # sum of 24 partials added by chunk_reduce_kernel
-    gs.Workload("tc-gqa24-one-unit-per-cta", 1, 100, 1, 24, 64, 64, "bf16", "weak", True, True, 64),
+    # 24 value heads on one kv head: dq, dk of each chunk are the sum of 24 heads, all taken by
+    # one gradient CTA
+    gs.Workload("tc-gqa24", 1, 100, 1, 24, 64, 64, "bf16", "weak", True, True, 64),
     # the chunked backward does not fit shared memory here: the sequential backward consumes
     # the chunkwise forward's saved buffer
     gs.Workload("tc-fwd-seq-bwd-Dv256", 1, 150, 1, 2, 128, 256, "bf16", "half", True, True, 64),

@@ -42,7 +42,7 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     shape = binding.make_shape(1, 2048, 16, 64, 192, 128, 64, 1)
     assert lib.gdn_bwd_workspace_bytes(ctypes.byref(shape)) > NOALLOC_BYTES
     fake = ctypes.c_void_p(0x7F0000000000)
-    rc = lib.gdn_bwd_noalloc(ctypes.byref(shape), *([fake] * 7), None, *([fake] * 5), None, None)
+    rc = lib.gdn_bwd_noalloc(ctypes.byref(shape), *([fake] * 6), 1 << 40, fake, None, *([fake] * 5), None, None)
     assert rc == SCRATCH_LIMIT
     assert "GDN_BWD_NOALLOC_SCRATCH_BYTES" in lib.gdn_strerror(SCRATCH_LIMIT).decode()
 
@@ -51,21 +51,27 @@ def _noalloc(lib, binding, shape, t, ckpt, out):
     P = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return lib.gdn_bwd_noalloc(ctypes.byref(shape), P(t["q"]), P(t["k"]), P(t["v"]), P(t["g"]), P(t["beta"]),
-                               P(ckpt), P(t["dy"]), P(t["dS_T"]), P(out["dq"]), P(out["dk"]), P(out["dv"]),
-                               P(out["dg"]), P(out["dbeta"]), P(out["dS0"]), stream)
+                               P(ckpt), binding._room(ckpt), P(t["dy"]), P(t["dS_T"]), P(out["dq"]), P(out["dk"]),
+                               P(out["dv"]), P(out["dg"]), P(out["dbeta"]), P(out["dS0"]), stream)
 
 
 @pytest.mark.gpu
 def test_noalloc_matches_gdn_bwd_on_consecutive_calls():
+    """Both entry points run the same kernels on the same grid, so their results must agree
+    bit for bit. The problems alternate between the two scratch layouts (the tensor-core
+    backward's and the sequential backward's), so that every call after the first starts
+    from scratch left dirty by a call of the other layout or of another shape."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     binding, lib = _lib()
     import gated_delta_rule_22_gb300 as gdn
     dev = torch.device("cuda:0")
     problems = [
-        gs.Workload("na-f32", 2, 61, 2, 6, 64, 40, "f32", "strong", True, True, 16),
-        gs.Workload("na-f32", 2, 61, 2, 6, 64, 40, "f32", "strong", True, True, 16),   # same again
-        gs.Workload("na-bf16", 1, 90, 1, 2, 128, 72, "bf16", "half", False, True, 32),  # then another
+        gs.Workload("na-tc", 1, 150, 1, 2, 128, 128, "bf16", "half", True, True, 64),     # tensor-core layout
+        gs.Workload("na-f32", 2, 61, 2, 6, 64, 40, "f32", "strong", True, True, 16),      # sequential layout
+        gs.Workload("na-f32", 2, 61, 2, 6, 64, 40, "f32", "strong", True, True, 16),      # same again
+        gs.Workload("na-bf16", 1, 90, 1, 2, 128, 72, "bf16", "half", False, True, 32),    # sequential, bf16
+        gs.Workload("na-tc2", 1, 200, 2, 4, 64, 64, "bf16", "strong", False, True, 64),   # tensor-core again
     ]
     for w in problems:
         inp = gs.make_inputs(w)
@@ -78,7 +84,11 @@ def test_noalloc_matches_gdn_bwd_on_consecutive_calls():
         rc = _noalloc(lib, binding, shape, t, ckpt, out)
         assert rc == 0, lib.gdn_strerror(rc).decode() + " " + lib.gdn_last_error().decode()
         torch.cuda.synchronize()
-        tol = H.TOL[w.dtype]
         for n in ref:
-            e = oracle.rel_l2(out[n].double().cpu().numpy(), ref[n].double().cpu().numpy())
-            assert e <= tol, (w.name, n, e)
+            assert torch.equal(out[n], ref[n]), (w.name, n)
+        # and the pair is right: the oracle on the same inputs, at the parity tolerance
+        want = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["dy"], inp["S0"], inp["dS_T"],
+                          chunk=w.chunk)
+        for n in ref:
+            e = oracle.rel_l2(out[n].double().cpu().numpy(), want[n])
+            assert e <= H.TOL[w.dtype], (w.name, n, e)
