@@ -166,8 +166,10 @@ def kernel_model(w):
     tb = tensor_bytes(w)
     nb = {k: float(sum(tb[n] for n in v)) for k, v in PASS_TENSORS.items()}
     m = {}
-    m["chunk_prep"] = (nb["chunk_prep"], ck * 2 * (2 * L * L * Dk) + ch * (2 * L * Dk * L + 2 * L * Dv * L), 0.0)
-    m["chunk_sweep"] = (nb["chunk_sweep"], ch * (2 * L * Dv * Dk * 3 + 2 * L * Dv * L * 2 + 2 * Dv * Dk * L), 0.0)
+    m["chunk_prep"] = (nb["chunk_prep"], ck * 2 * (2 * L * L * Dk) + ch * (2 * L * Dk * L), 0.0)
+    # per chunk and value head: U = (T diag(beta)) V, W S^T, [Q; K] S^T, [P; KKm] Delta, the update
+    m["chunk_sweep"] = (nb["chunk_sweep"], ch * (2 * L * L * Dv + 2 * L * Dv * Dk + 2 * 2 * L * Dv * Dk
+                                                 + 2 * 2 * L * L * Dv + 2 * Dv * Dk * L), 0.0)
     m["chunk_dsweep"] = (nb["chunk_dsweep"], ch * (2 * 2 * L * Dv * Dk + 2 * L * Dv * L * 2 + 2 * Dv * Dk * L * 2), 0.0)
     m["chunk_grad"] = (
         nb["chunk_grad"],

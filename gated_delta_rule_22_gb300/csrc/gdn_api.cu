@@ -75,11 +75,12 @@ size_t ckpt_state_bytes(const Plan &p) { return round_up((size_t)p.B * p.Hv * p.
 size_t ckpt_resid_bytes(const Plan &p) { return (size_t)p.B * p.T * p.Hv * p.Dv * sizeof(float); }
 
 // With the chunkwise forward the buffer continues (each part from a 256-byte boundary) with
-// the per-chunk data of every (b, h, chunk): Lam [64] fp32, the sweep's bf16 operands in their
-// core-matrix layout ([(Q K^T) o E; (K K^T) o E] [128][64], W [64][Dk], [diag(exp Lam) Q;
-// diag(exp Lam) K] [128][Dk]; K [64][Dk] per kv head) and U fp32 in [Dv/32][64][32] blocks.
+// the per-chunk data of every (b, h, chunk): Lam [64] fp32 and bf16 matrices in their
+// core-matrix layout ([(Q K^T) o E; (K K^T) o E] [128][64], -W [64][Dk], T [64][64],
+// T diag(beta) [64][64], the bf16 chunk-start state [Dv][Dk]), and per (b, kv head, chunk)
+// [Q; K] [128][Dk].
 struct ChunkLayout {
-    size_t lam, pkm, wm, qksm, ktm, um, tm, s0m, qkm, end;
+    size_t lam, pkm, wm, tm, tcm, s0m, qkm, end;
 };
 ChunkLayout chunk_layout(const Plan &p) {
     const size_t n = (size_t)p.B * p.Hv * p.NC * 64;   // chunk rows
@@ -88,10 +89,8 @@ ChunkLayout chunk_layout(const Plan &p) {
     c.lam = o; o += round_up(n * 4);
     c.pkm = o; o += round_up(n * 2 * 64 * 2);
     c.wm = o; o += round_up(n * p.Dk * 2);
-    c.qksm = o; o += round_up(n * 2 * p.Dk * 2);
-    c.ktm = o; o += round_up((size_t)p.B * p.Hk * p.NC * 64 * p.Dk * 2);   // per kv head
-    c.um = o; o += round_up(n * p.Dv * 4);
     c.tm = o; o += round_up(n * 64 * 2);
+    c.tcm = o; o += round_up(n * 64 * 2);
     c.s0m = o; o += round_up((size_t)p.B * p.Hv * p.NC * p.Dv * p.Dk * 2);
     c.qkm = o; o += round_up((size_t)p.B * p.Hk * p.NC * 128 * p.Dk * 2);
     c.end = o;
@@ -238,27 +237,6 @@ void release_timed() {
         if (t.stop) g_event_pool.push_back(t.stop);
     }
     g_timed.clear();
-}
-
-// 2-D fp32 tensor map [rows][cols] (row-major), box {box_c, box_r}, 128-byte swizzle.
-int make_f32_map_2d(CUtensorMap *map, void *ptr, size_t rows, size_t cols, int box_c, int box_r) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (enc == nullptr) {
-        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available from the driver");
-        return GDN_ERR_CUDA;
-    }
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)box_c, (cuuint32_t)box_r};
-    const cuuint32_t estride[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estride,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
-        return GDN_ERR_CUDA;
-    }
-    return GDN_OK;
 }
 
 // 4-D tensor map of a row-major [B][T][H][D] tensor (bf16 or fp32), box {box_d, 1, box_t, 1},
@@ -444,10 +422,8 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.lam = reinterpret_cast<float *>(sb + cl.lam);
         cp.pkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.pkm);
         cp.wm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.wm);
-        cp.qksm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qksm);
-        cp.ktm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.ktm);
-        cp.um = reinterpret_cast<float *>(sb + cl.um);
         cp.tm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tm);
+        cp.tcm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tcm);
         cp.s0m = reinterpret_cast<__nv_bfloat16 *>(sb + cl.s0m);
         cp.qkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qkm);
         cp.status = fp.status;
@@ -457,8 +433,7 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
                 GDN_OK ||
             (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
             (rc = make_colblock_map(&maps.r, fp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK ||
-            (rc = make_f32_map_2d(&maps.u, cp.um, (size_t)p.B * p.Hv * p.NC * 2 * p.Dv, 32, 32, 64)) != GDN_OK ||
-            (rc = make_colblock_map(&maps.v, v, true, p.B, p.T, p.Hv, p.Dv, 8, 64, p.Dv / 8, false)) != GDN_OK ||
+            (rc = make_colblock_map(&maps.vb, v, true, p.B, p.T, p.Hv, p.Dv, 8, 64, 8, false)) != GDN_OK ||
             (rc = make_colblock_map(&maps.k, k, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
             (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
             (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK)
@@ -496,8 +471,6 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.lam = reinterpret_cast<const float *>(sb + cl.lam);
         cp.tm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.tm);
         cp.pkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.pkm);
-        cp.qksm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qksm);
-        cp.ktm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.ktm);
         cp.s0m = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.s0m);
         cp.qkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qkm);
         cp.dS_T = dS_T; cp.dS0 = dS0;

@@ -69,14 +69,14 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 
 // ------------------------------------------------------------------ reverse sweep (dS)
 struct DSweepSmem {
-    size_t kt, qks, tm, pkm, ydu, rsm, lms, shl, rhs, dls, dvs, vec, red, bar, tslot, total;
+    size_t qk, tm, pkm, ydu, yds, rsm, lms, shl, rhs, dls, dvs, vec, red, bar, tslot, total;
     __host__ __device__ DSweepSmem(int DK) {
         size_t o = 0;
-        kt = o; o += (size_t)kL * DK * 2;    // K [64][DK]
-        qks = o; o += (size_t)2 * kL * DK * 2;   // [diag(exp Lam) Q; diag(exp Lam) K] [128][DK] (read MN-major)
+        qk = o; o += (size_t)2 * kL * DK * 2;    // [Q; K] [128][DK] (K-major rows 64-127: K; read MN-major whole)
         tm = o; o += (size_t)kL * kL * 2;    // T [64][64] (read MN-major as T^T)
         pkm = o; o += (size_t)2 * kL * kL * 2;   // [P; KKm] [128][64], P = (Q K^T) o E_incl (read MN-major)
         ydu = o; o += (size_t)2 * 2 * kL * kL * 2;   // [dY; dU] block [128][64 v] (rows 0-63 dY, 64-127 dU), two buffers
+        yds = o; o += (size_t)2 * kL * kL * 2;       // [diag(exp Lam) dY; diag(exp Lam) dU] [128][64 v] (read MN-major)
         rsm = alb(o, 1024); o = rsm + (size_t)2 * kL * 128;   // v - u block, fp32: two [64 t][32 v] boxes in the 128-byte swizzle
         lms = o; o += (size_t)2 * kL * 4;        // Lam, two buffers
         shl = o; o += (size_t)2 * kL * DK * 2;   // dS as [high; low] bf16 parts [128][DK] (rows 0-63 high, 64-127 dS - high)
@@ -85,7 +85,7 @@ struct DSweepSmem {
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
         vec = o; o += 4 * kL * 4;            // -, E(L, .), beta, -
         red = o; o += 2 * 2 * kL * 4;        // [f | dbeta][half][64]
-        bar = alb(o, 8); o = bar + 5 * 8;    // MMA, copies of (K, P), of T, of [Qs; Ks], of (dY, v - u, Lam)
+        bar = alb(o, 8); o = bar + 6 * 8;    // MMA, copies of [P; KKm], of T, of [Q; K], of (dY, v - u, Lam); drain
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -95,6 +95,8 @@ struct DSweepSmem {
 }  // namespace
 
 // One CTA per (block of 64 value rows, value head, batch row), over the chunks in reverse.
+// Warp 0 issues the products (from one elected lane, the warp converged); thread 32 issues the
+// copies and the stores.
 // Tensor memory (M = 64 layout: row r in lane r % 16 + 32 (r / 16)):
 //   [0, DK)              dS (value rows of this block)
 //   [DK, DK + 128)       K [dS_high; dS_low]^T (one N = 128 product: chunk row t, value column
@@ -117,14 +119,14 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
     const DSweepSmem L(DK);
-    unsigned char *kt = base + L.kt, *qks = base + L.qks, *tmm = base + L.tm, *pmm = base + L.pkm;
+    unsigned char *qk = base + L.qk, *tmm = base + L.tm, *pmm = base + L.pkm, *yds = base + L.yds;
     unsigned char *ydu2 = base + L.ydu, *shl = base + L.shl, *rhs = base + L.rhs, *dls = base + L.dls;
     unsigned char *dvs = base + L.dvs;
     float *rsm = reinterpret_cast<float *>(base + L.rsm), *lms = reinterpret_cast<float *>(base + L.lms);
     float *eL = reinterpret_cast<float *>(base + L.vec) + kL, *bt = eL + kL;
     float *red = reinterpret_cast<float *>(base + L.red);   // [2][2][64]
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
-    uint64_t *cbA = bar + 1, *cbT = bar + 2, *cbK = bar + 3, *cbY = bar + 4;
+    uint64_t *cbA = bar + 1, *cbT = bar + 2, *cbK = bar + 3, *cbY = bar + 4, *mX = bar + 5;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
@@ -134,8 +136,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     int nA = 0, nT = 0, nK = 0;
     auto copy_A = [&](int cc) {
         const size_t ck = head * p.NC + cc;
-        mbar_expect_tx(cbA, kL * DK * 2 + 2 * kL * kL * 2);
-        bulk_load(kt, p.ktm + (((size_t)b * p.Hk + h / (Hv / p.Hk)) * p.NC + cc) * kL * DK, kL * DK * 2, cbA);
+        mbar_expect_tx(cbA, 2 * kL * kL * 2);
         bulk_load(pmm, p.pkm + ck * 2 * kL * kL, 2 * kL * kL * 2, cbA);
         ++nA;
     };
@@ -145,21 +146,21 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         bulk_load(tmm, p.tm + ck * kL * kL, kL * kL * 2, cbT);
         ++nT;
     };
-    auto copy_K = [&](int cc) {
-        const size_t ck = head * p.NC + cc;
+    auto copy_K = [&](int cc) {               // [Q; K] of the chunk (kv head)
         mbar_expect_tx(cbK, 2 * kL * DK * 2);
-        bulk_load(qks, p.qksm + ck * 2 * kL * DK, 2 * kL * DK * 2, cbK);
+        bulk_load(qk, p.qkm + (((size_t)b * p.Hk + h / (Hv / p.Hk)) * p.NC + cc) * 2 * kL * DK, 2 * kL * DK * 2, cbK);
         ++nK;
     };
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(bar + i, 1);
+        for (int i = 0; i < 6; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
         tma_prefetch_map(&tm_dy);
         tma_prefetch_map(&tm_rs);
         tma_prefetch_map(&tm_dv);
     }
     if (warp == 0) tmem_alloc(tslot, 512);
+    const uint32_t lead = warp == 0 ? elect_one_sync() : 0u;   // the lane of warp 0 that issues products
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     int nY = 0, wY = 0;
     auto fetch_chunk = [&](int cc, int buf) {
         const int tt0 = cc * kL, ln = min(kL, T - tt0);
-        if (tid == 0) {
+        if (tid == 32) {
             unsigned char *yb = ydu2 + (size_t)buf * 2 * kL * kL * 2;
             // dY: one box of 128 rows in the [dY; dU] operand layout (8 core-matrix columns of
             // 128 rows); rows 64-127 (the following steps) land in the dU rows, which the chunk
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         ++nY;
         if (tid < kL) btn = beta[((size_t)b * T + tt0 + (tid < ln ? tid : 0)) * Hv + h];
     };
-    if (tid == 0) { copy_A(p.NC - 1); copy_T(p.NC - 1); copy_K(p.NC - 1); }
+    if (tid == 32) { copy_A(p.NC - 1); copy_T(p.NC - 1); copy_K(p.NC - 1); }
     fetch_chunk(p.NC - 1, 0);
     for (int c = p.NC - 1; c >= 0 && ok; --c) {
         const int t0 = c * kL, len = min(kL, T - t0);
@@ -222,6 +223,17 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
             if (!ok) break;
         }
         const float decay = expf(lmb[kL - 1]);
+        // diag(exp Lam) dY: rows 0-63 of the dS update's operand (the dU rows follow below)
+        for (int e = tid; e < kL * kL / 8; e += 256) {
+            const int t = e & (kL - 1);
+            const uint32_t o = cm_off(t, 16 * (e >> 6), 2 * kL);
+            float x8[8];
+            unpack8(*reinterpret_cast<const uint4 *>(ydu + o), x8);
+            const float gt = expf(lmb[t]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x8[i] *= gt;
+            *reinterpret_cast<uint4 *>(yds + o) = pack8(x8);
+        }
         // this lane's v - u (row lrow, 32 value columns: box `half`, 16-byte piece i of the row
         // at ((i ^ (row & 7)) << 4))
         float rs[32];
@@ -267,24 +279,23 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         fence_proxy_async();
         tc_fence_before();
         {
-            // the last chunk's stores have read [dY; dU], Delta and dv; K and [P; KKm] have landed
+            // the last chunk's stores have read [dY; dU], Delta and dv (thread 32); [Q; K] and
+            // [P; KKm] have landed (warp 0)
             bool w = true;
-            if (tid == 0) {
-                bulk_wait_read();
-                w = mbar_wait(cbA, cph & 1);
-            }
+            if (tid == 32) bulk_wait_read();
+            if (warp == 0) w = mbar_wait(cbA, cph & 1) && mbar_wait(cbK, cph & 1);
             ok = !__syncthreads_or(!w);
         }
         tc_fence_after();
         if (!ok) break;
         if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
-        // ---- K [dS_high; dS_low]^T (N = 128), P^T dY (P: rows 0-63 of [P; KKm])
-        if (tid == 0) {
+        // ---- K [dS_high; dS_low]^T (N = 128; K: rows 64-127 of [Q; K]), P^T dY (P: rows 0-63 of [P; KKm])
+        if (warp == 0) {
             constexpr uint32_t idX = umma_idesc_t(1, kL, 2 * kL, false, false);
             constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
-            umma_gemm(tX, CmOp{kt, kL, 0, 0, false}, CmOp{shl, 2 * kL, 0, 0, false}, DK, idX, false);
-            umma_gemm(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false);
-            umma_commit(bar);
+            umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl, 2 * kL, 0, 0, false}, DK, idX, false, lead);
+            umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false, lead);
+            umma_commit_w(bar, lead);
         }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
         ++ph;
@@ -322,23 +333,23 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         }
         fence_proxy_async();
         tc_fence_before();
-        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbT, cph & 1));   // and T has landed
+        ok = !__syncthreads_or(warp == 0 && !mbar_wait(cbT, cph & 1));   // and T has landed
         tc_fence_after();
         if (!ok) break;
-        // the buffers of K and [P; KKm] are free: the previous chunk's copies go out now
-        if (tid == 0 && c > 0) copy_A(c - 1);
+        // the buffer of [P; KKm] is free: the previous chunk's copy goes out now
+        if (tid == 32 && c > 0) copy_A(c - 1);
         if (tid < kL && tid < len) p.ws_f[((rowbase + tid) * Hv + h) * nsplit + split] = red[tid] + red[kL + tid];
         // ---- dD = T^T rhs
-        if (tid == 0) {
-            umma_gemm(tX, CmOp{tmm, kL, 0, 0, true}, CmOp{rhs, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, kL, true, true),
-                      false);
-            umma_commit(bar);
+        if (warp == 0) {
+            umma_gemm_w(tX, CmOp{tmm, kL, 0, 0, true}, CmOp{rhs, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, kL, true, true),
+                        false, lead);
+            umma_commit_w(bar, lead);
         }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
         ++ph;
         tc_fence_after();
         if (!ok) break;
-        if (tid == 0 && c > 0) copy_T(c - 1);
+        if (tid == 32 && c > 0) copy_T(c - 1);
         // ---- dv = beta dD, dbeta partial, dU = -beta dD (operand, and stored for the gradient kernel)
         {
             float x[32];
@@ -346,17 +357,21 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
             tmem_ld16f(tX + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(x + 16));
             tmem_wait_ld();
             if (rowlane) {
-                const float bb = bt[lrow];
-                float ds = 0.f, dvv[32], duu[32];
+                const float bb = bt[lrow], gt = expf(lmb[lrow]);
+                float ds = 0.f, dvv[32], duu[32], dus[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     ds = fmaf(x[i], rs[i], ds);
                     dvv[i] = bb * x[i];
                     duu[i] = -dvv[i];
+                    dus[i] = gt * duu[i];
                 }
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(ydu + cm_off(kL + lrow, 16 * (half * 4 + j), 2 * kL)) = pack8(duu + 8 * j);
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t o = cm_off(kL + lrow, 16 * (half * 4 + j), 2 * kL);
+                    *reinterpret_cast<uint4 *>(ydu + o) = pack8(duu + 8 * j);
+                    *reinterpret_cast<uint4 *>(yds + o) = pack8(dus + 8 * j);
+                }
                 // dv staged in the 128-byte swizzle for a TMA store (rows past T are clipped by it)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
@@ -366,34 +381,35 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         }
         fence_proxy_async();
         tc_fence_before();
-        ok = !__syncthreads_or(tid == 0 && !mbar_wait(cbK, cph & 1));   // and [Qs; Ks] has landed
+        tc_fence_before();
+        __syncthreads();
         tc_fence_after();
-        if (!ok) break;
         if (tid < kL && tid < len)
             p.ws_db[((rowbase + tid) * Hv + h) * nsplit + split] = red[2 * kL + tid] + red[3 * kL + tid];
-        // ---- dS += [dY; dU]^T [diag(exp Lam) Q; diag(exp Lam) K] (K = 128)
-        if (tid == 0) {
-            umma_gemm(tS, CmOp{ydu, 2 * kL, 0, 0, true}, CmOp{qks, 2 * kL, 0, 0, true}, 2 * kL,
-                      umma_idesc_t(1, kL, DK, true, true), true);
+        // ---- dS += [diag(exp Lam) dY; diag(exp Lam) dU]^T [Q; K] (K = 128)
+        if (warp == 0) {
+            umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, 2 * kL,
+                        umma_idesc_t(1, kL, DK, true, true), true, lead);
+            umma_commit_w(bar, lead);
+        }
+        if (tid == 32) {
             // [dY; dU] and Delta of the block for the gradient kernel, and dv
             const size_t blk = chk * nsplit + split;
             bulk_store(p.ws_yu + blk * 2 * kL * kL, ydu, 2 * kL * kL * 2);
             bulk_store(p.ws_dl + blk * kL * kL, dls, kL * kL * 2);
             tma_store_4d(&tm_dv, dvs, r0, h, t0, b);
             bulk_commit();
-            umma_commit(bar);
         }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
         ++ph;
         tc_fence_after();
         if (!ok) break;
-        if (tid == 0 && c > 0) copy_K(c - 1);
+        if (tid == 32 && c > 0) copy_K(c - 1);         // [Q; K] is free again
         ++cph;
         // no block barrier before the next chunk: nothing after this point reads what its first
         // section writes
     }
-    if (tid == 0) bulk_wait_all();                          // the block outputs are complete
-    cp_async_wait<0>();                                     // no copy still writes shared memory
+    if (tid == 32) bulk_wait_all();                         // the block outputs are complete
     if (ok && p.dS0 != nullptr) {
         for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
             float x[16];
@@ -406,13 +422,18 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
                         make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
         }
     }
-    if (!ok && tid == 0) {
+    if (!ok && tid == 32) {
         report_status(p.status, kStatusTimeout);
         // copies still in flight land before the CTA exits (each wait bounded)
-        if (nA > (int)cph) mbar_wait(cbA, (nA - 1) & 1);
-        if (nT > (int)cph) mbar_wait(cbT, (nT - 1) & 1);
-        if (nK > (int)cph) mbar_wait(cbK, (nK - 1) & 1);
-        if (nY > wY) mbar_wait(cbY, (nY - 1) & 1);
+        if (nA > 0) mbar_wait(cbA, (nA - 1) & 1);
+        if (nT > 0) mbar_wait(cbT, (nT - 1) & 1);
+        if (nK > 0) mbar_wait(cbK, (nK - 1) & 1);
+        if (nY > 0) mbar_wait(cbY, (nY - 1) & 1);
+    }
+    if (!ok && warp == 0) {
+        // products still in flight finish before the tensor memory is freed (bounded wait)
+        umma_commit_w(mX, lead);
+        mbar_wait(mX, 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -440,7 +461,7 @@ struct GradSmem {
         dsl = o; o += (size_t)Dv * DK * 2;                         // dS_L [Dv / 64][64][DK]
         vec = o; o += (6 * kL + 4 * kL + 16 + 12 * kL + 4 * kL) * 4;   // Lam, Lam_{t-1}, exp Lam, E(L,.), beta, f; ab [2][128]; c0 parts; dg parts [4][3][64]; Z column sums [4][64]
         stg = o; o += (size_t)32 * (DK + 4) * 4;                   // 32 output rows (fp32, padded) for coalesced stores
-        bar = alb(o, 8); o = bar + 4 * 8;                          // MMA; copies of (dY;dU, Delta, dS_L), of S0, of [Q; K]
+        bar = alb(o, 8); o = bar + 5 * 8;                          // MMA; copies of (dY;dU, Delta, dS_L), of S0, of [Q; K]; drain
         tslot = o; o += 16;
         total = o + 128;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -486,7 +507,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     float *stg = reinterpret_cast<float *>(base + L.stg);
     float *Lm = reinterpret_cast<float *>(base + L.vec), *LmP = Lm + kL, *gm = LmP + kL, *eL = gm + kL;
     float *bt = eL + kL, *fv = bt + kL, *abp = fv + kL, *c0p = abp + 4 * kL, *dgp = c0p + 16, *zq = dgp + 12 * kL;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbA = bar + 1, *cbS = bar + 2, *cbQ = bar + 3;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbA = bar + 1, *cbS = bar + 2, *cbQ = bar + 3, *mX = bar + 4;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
 
@@ -549,17 +570,18 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     };
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(bar + i, 1);
+        for (int i = 0; i < 5; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, 512);
+    const uint32_t lead = warp == 0 ? elect_one_sync() : 0u;   // the lane of warp 0 that issues products
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tR1 = tmem, tRS = tmem + DK, tS1 = tmem + 2 * DK, tS2 = tmem + 2 * DK + 64;
 
-    if (tid == 0 && u_begin < u_end) {
+    if (tid == 32 && u_begin < u_end) {
         copy_q(u_begin);
         copy_a(u_begin);
         copy_s(u_begin);
@@ -611,16 +633,16 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         const bool gfirst = hh == 0, glast = hh == rep - 1;
         // ---- first products: [Q; K] K^T (when the kv head or chunk changes), [dY; dU] Delta^T,
         // [dY; dU] S0
-        if (tid == 0) {
+        if (warp == 0) {
             if (newq)
-                umma_gemm(tS1, CmOp{qk, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, kL, 0, false}, DK,
-                          umma_idesc_t(1, 2 * kL, kL, false, false), false);
-            umma_gemm(tS2, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{dl, kL, 0, 0, false}, Dv,
-                      umma_idesc_t(1, 2 * kL, kL, false, false), false);
+                umma_gemm_w(tS1, CmOp{qk, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, kL, 0, false}, DK,
+                            umma_idesc_t(1, 2 * kL, kL, false, false), false, lead);
+            umma_gemm_w(tS2, CmOp{yu, 2 * kL, 0, 0, false}, CmOp{dl, kL, 0, 0, false}, Dv,
+                        umma_idesc_t(1, 2 * kL, kL, false, false), false, lead);
             for (int s = 0; s < nsplit; ++s)
-                umma_gemm(tR1, CmOp{yu, 2 * kL, 0, kL * s, false}, CmOp{s0 + (size_t)s * kSb, kL, 0, 0, true}, kL,
-                          umma_idesc_t(1, 2 * kL, DK, false, true), s > 0);
-            umma_commit(bar);
+                umma_gemm_w(tR1, CmOp{yu, 2 * kL, 0, kL * s, false}, CmOp{s0 + (size_t)s * kSb, kL, 0, 0, true}, kL,
+                            umma_idesc_t(1, 2 * kL, DK, false, true), s > 0, lead);
+            umma_commit_w(bar, lead);
         }
         // ---- c0 = <dS_L, S0> (both in the same layout) while the products run
         {
@@ -729,19 +751,19 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         tc_fence_after();
         // ---- second products: RS += [GE; HE] K; R1 = (diag(E_L) Delta) dS_L + GE^T Q + HE^T K;
         // Z = [W1; W2] M
-        if (tid == 0) {
-            umma_gemm(tRS, CmOp{gehe, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
-                      umma_idesc_t(1, 2 * kL, DK, false, true), true);
+        if (warp == 0) {
+            umma_gemm_w(tRS, CmOp{gehe, 2 * kL, 0, 0, false}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
+                        umma_idesc_t(1, 2 * kL, DK, false, true), true, lead);
             for (int s = 0; s < nsplit; ++s)
-                umma_gemm(tR1, CmOp{dl, kL, -kL, kL * s, false}, CmOp{dsl + (size_t)s * kSb, kL, 0, 0, true}, kL,
-                          umma_idesc_t(1, 2 * kL, DK, false, true), s > 0);
-            umma_gemm(tR1, CmOp{gehe, 2 * kL, -kL, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, kL,
-                      umma_idesc_t(1, 2 * kL, DK, true, true), true);
-            umma_gemm(tR1, CmOp{gehe, 2 * kL, -kL, kL, true}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
-                      umma_idesc_t(1, 2 * kL, DK, true, true), true);
-            umma_gemm(tS2, CmOp{wst, 2 * kL, 0, 0, false}, CmOp{mt, kL, 0, 0, false}, kL,
-                      umma_idesc_t(1, 2 * kL, kL, false, false), false);
-            umma_commit(bar);
+                umma_gemm_w(tR1, CmOp{dl, kL, -kL, kL * s, false}, CmOp{dsl + (size_t)s * kSb, kL, 0, 0, true}, kL,
+                            umma_idesc_t(1, 2 * kL, DK, false, true), s > 0, lead);
+            umma_gemm_w(tR1, CmOp{gehe, 2 * kL, -kL, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, kL,
+                        umma_idesc_t(1, 2 * kL, DK, true, true), true, lead);
+            umma_gemm_w(tR1, CmOp{gehe, 2 * kL, -kL, kL, true}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
+                        umma_idesc_t(1, 2 * kL, DK, true, true), true, lead);
+            umma_gemm_w(tS2, CmOp{wst, 2 * kL, 0, 0, false}, CmOp{mt, kL, 0, 0, false}, kL,
+                        umma_idesc_t(1, 2 * kL, kL, false, false), false, lead);
+            umma_commit_w(bar, lead);
         }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
         ++ph;
@@ -749,7 +771,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         if (!ok) break;
         // [dY; dU], Delta, dS_L, the S0 region (scratch) and, when the next unit needs another
         // [Q; K], its buffer are free: the next unit's go out now
-        if (tid == 0 && u + 1 < u_end) {
+        if (tid == 32 && u + 1 < u_end) {
             copy_a(u + 1);
             copy_s(u + 1);
             if (!same_qk(u, u + 1)) copy_q(u + 1);
@@ -856,12 +878,17 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         __syncthreads();
         tc_fence_after();
     }
-    if (!ok && tid == 0) {
+    if (!ok && tid == 32) {
         report_status(p.status, kStatusTimeout);
         // copies still in flight land before the CTA exits (each wait bounded)
         if (nA > wA) mbar_wait(cbA, (nA - 1) & 1);
         if (nS > wS) mbar_wait(cbS, (nS - 1) & 1);
         if (nQ > wQ) mbar_wait(cbQ, (nQ - 1) & 1);
+    }
+    if (!ok && warp == 0) {
+        // products still in flight finish before the tensor memory is freed (bounded wait)
+        umma_commit_w(mX, lead);
+        mbar_wait(mX, 0);
     }
     tc_fence_before();
     __syncthreads();

@@ -72,21 +72,18 @@ static_assert(kBwdComputeWarps * 32 * kBwdComputeRegs + 128 * kBwdServiceRegs <=
               "register split exceeds the launch's registers");
 
 // Chunkwise tensor-core forward (bf16 inputs, chunks of 64 steps). Per (b, h, chunk), in the
-// saved buffer: lam, the in-chunk log-decay prefix [64]; um, U fp32 in column blocks
-// [Dv / 32][64][32]; and the sweep's
-// tensor-core operands, bf16 in their shared-memory (core-matrix) layout: wm W [64][Dk],
-// qksm [diag(exp Lam) Q; diag(exp Lam) K] [128][Dk], ktm K [64][Dk] (per kv head),
-// pkm [(Q K^T) o E_incl; (K K^T) o E_strict] [128][64], tm T = (I + A)^-1 [64][64];
-// per (b, h, chunk, block of 64 value rows) s0m, the chunk-start state in bf16 [64][Dk]; and
-// per (b, kv head, chunk) qkm, [Q; K] of the chunk [128][Dk].
+// saved buffer: lam, the in-chunk log-decay prefix [64]; and bf16 matrices in their shared-memory
+// (core-matrix) layout: pkm [(Q K^T) o E_incl; (K K^T) o E_strict] [128][64], wm -W [64][Dk]
+// (W = T diag(beta exp Lam) K), tm T = (I + A)^-1 [64][64], tcm T diag(beta) [64][64]; per
+// (b, h, chunk, block of 64 value rows) s0m, the chunk-start state in bf16 [64][Dk]; and per
+// (b, kv head, chunk) qkm, [Q; K] of the chunk [128][Dk].
 struct ChunkParams {
     const void *q, *k, *v, *g, *beta;
     const float *S0;
     void *y;
     float *S_T, *ckpt, *resid;
     float *lam;
-    __nv_bfloat16 *pkm, *wm, *qksm, *ktm, *tm, *s0m, *qkm;
-    float *um;
+    __nv_bfloat16 *pkm, *wm, *tm, *tcm, *s0m, *qkm;
     int *status;
     int B, T, Hk, Hv, Dv, NC;
 };
@@ -96,7 +93,7 @@ struct ChunkParams {
 struct ChunkBwdParams {
     const void *dy, *beta;
     const float *resid, *lam;
-    const __nv_bfloat16 *tm, *pkm, *qksm, *ktm, *s0m, *qkm;
+    const __nv_bfloat16 *tm, *pkm, *s0m, *qkm;
     const float *dS_T;
     float *dS0;
     void *dv, *dg, *dq, *dk, *dbeta;
@@ -464,15 +461,14 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // Tensor maps. Written by TMA stores, 128-byte swizzle: ck the fp32 checkpoints as 5-D column
 // blocks {32, B*Hv*NC*Dv rows, Dk / 32, 1, 1}, box {32, 64, Dk / 32, 1, 1} (a 64-row block of
 // one chunk-start state); y as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1}; r (v - u) as 5-D
-// column blocks of [B][T][Hv][Dv] fp32 {32, T, Dv / 32, Hv, B}, box {32, 64, 2, 1, 1}; u (U)
-// as rows of 32 fp32 ([B*Hv*NC*Dv*2 rows][32], each chunk's [Dv/32][64][32] blocks in
-// order), box {32, 64}. Read by TMA loads,
-// no swizzle, box {8, 1, 64, 1} (one 1 KB core-matrix column of 64 rows): v as
-// [B][T][Hv][Dv], k and q as [B][T][Hk][Dk], bf16. Written by TMA stores from an operand
-// tile of 64 rows: qk, the [Q; K] buffer as {8, 64 rows, Dk / 8 chunks, 2 halves (Q, K),
-// B*Hk*NC blocks}, box {8, 64, Dk / 8, 1, 1}.
+// column blocks of [B][T][Hv][Dv] fp32 {32, T, Dv / 32, Hv, B}, box {32, 64, 2, 1, 1}. Read by
+// TMA loads, no swizzle, in 1 KB core-matrix columns of 64 rows: k and q as 5-D column blocks
+// of [B][T][Hk][Dk] {8, T, Dk / 8, Hk, B}, box {8, 64, Dk / 8, 1, 1}; vb, v as 5-D column
+// blocks of [B][T][Hv][Dv] {8, T, Dv / 8, Hv, B}, box {8, 64, 8, 1, 1} (64 value columns).
+// Written by TMA stores from an operand tile of 64 rows: qk, the [Q; K] buffer as {8, 64 rows,
+// Dk / 8 chunks, 2 halves (Q, K), B*Hk*NC blocks}, box {8, 64, Dk / 8, 1, 1}.
 struct ChunkFwdMaps {
-    CUtensorMap ck, y, r, u, v, k, q, qk;
+    CUtensorMap ck, y, r, vb, k, q, qk;
 };
 cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s);
 size_t chunk_prep_smem(int Dk, int Dv);

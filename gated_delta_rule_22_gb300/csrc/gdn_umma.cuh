@@ -147,6 +147,61 @@ __device__ __forceinline__ void umma_gemm(uint32_t d_tmem, const CmOp &A, const 
     }
 }
 
+// One lane of a converged warp, chosen by elect.sync: true in that lane only. The warp issues
+// tensor-core products through it (a product issued from a lone thread under `tid == 0` costs
+// about 50-60 cycles of issue on this GPU, from an elected lane of a converged warp about 30).
+__device__ __forceinline__ uint32_t elect_one_sync() {
+    uint32_t p;
+    asm volatile("{\n .reg .pred q;\n elect.sync _|q, 0xffffffff;\n selp.u32 %0, 1, 0, q;\n}" : "=r"(p));
+    return p;
+}
+
+// D (tensor memory) = A B (+ D if accumulate), bf16 operands: executed by a whole converged warp
+// (the descriptors are then warp-uniform), issued by the lane whose `lead` is nonzero.
+__device__ __forceinline__ void umma_bf16_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            bool accumulate, uint32_t lead) {
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+        " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate), "r"(lead)
+        : "memory");
+}
+
+// Completion of the `lead` lane's earlier products arrives once on `bar` (whole warp executes).
+__device__ __forceinline__ void umma_commit_w(uint64_t *bar, uint32_t lead) {
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.b32 q, %1, 0;\n"
+        " @q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(smem_addr(bar)),
+        "r"(lead)
+        : "memory");
+}
+
+// umma_gemm for a whole converged warp, issued by its `lead` lane.
+__device__ __forceinline__ void umma_gemm_w(uint32_t d_tmem, const CmOp &A, const CmOp &B, int K, uint32_t idesc,
+                                            bool accumulate, uint32_t lead) {
+    uint64_t a = A.desc(0), b = B.desc(0);
+    const uint64_t da = A.mn ? 16u : (uint64_t)(2 * A.R), db = B.mn ? 16u : (uint64_t)(2 * B.R);
+    for (int k = 0; k < K; k += 16) {
+        umma_bf16_w(d_tmem, a, b, idesc, accumulate || k > 0, lead);
+        a += da;
+        b += db;
+    }
+}
+
+// 16x256b tensor-memory load, four repetitions (32 columns) from lane base `taddr` (a multiple of
+// 16 within the warp's 32 lanes): thread t gets, for repetition j, v[4j], v[4j+1] = lane
+// base + t/4, columns 8j + 2 (t % 4) and + 1, and v[4j+2], v[4j+3] = the same columns of lane
+// base + 8 + t/4. Every thread of the warp holds data (a 32x32b load of an M = 64 accumulator
+// leaves half of the threads idle).
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, float *v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]),
+          "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 // 32x32b tensor-memory load of 16 consecutive columns.
 __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
     asm volatile(

@@ -92,9 +92,9 @@ enum {
  * residuals v_t - u_t (B*T*Hv*Dv*4 bytes). For bf16 inputs with chunk 64, Dk in
  * {64, 128, 192} and Dv a multiple of 64 (up to 256, shared memory permitting) the forward
  * runs in its chunkwise form on the tensor cores, and the buffer continues with that form's
- * per-chunk matrices ((3 Dk + 2 Dv + 194) * 128 + 2 Dv Dk bytes per chunk and value head,
- * and 384 Dk bytes per chunk and kv head, each part rounded up to 256 bytes; their layout
- * is internal). 0 for an invalid shape. */
+ * per-chunk matrices (33024 + 128 Dk + 2 Dv Dk bytes per chunk and value head, and 256 Dk
+ * bytes per chunk and kv head, each part rounded up to 256 bytes; their layout is internal).
+ * 0 for an invalid shape. */
 GDN_API size_t gdn_ckpt_bytes(const gdn_shape *shape);
 
 /* Bytes of device scratch gdn_bwd needs (fp32 partial sums for the fixed-order
