@@ -61,31 +61,12 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
     return u;
 }
 
-__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
 __device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&x)[8]) {
     x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
     x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
     x[4] = __uint_as_float(u.z << 16); x[5] = __uint_as_float(u.z & 0xffff0000u);
     x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
 }
-
-// Where a thread's values of an M = 64 accumulator of N columns lie when the 8 warps read it
-// with 16x256b loads: warp w reads rows 16 (w % 4) .. + 15 (tensor-memory lanes 32 (w % 4) ..
-// + 15) and columns [N/2 (w / 4), N/2 (w / 4 + 1)); value e = 4 j + k of the thread (j the
-// 8-column repetition, k = 0..3) is row m16_row(k) and column m16_col(j, k).
-struct M64Frag {
-    int row0, colbase;
-    __device__ __forceinline__ M64Frag(int warp, int lane, int N) {
-        row0 = 16 * (warp & 3) + (lane >> 2);
-        colbase = (N / 2) * (warp >> 2) + 2 * (lane & 3);
-    }
-    __device__ __forceinline__ int row(int k) const { return row0 + 8 * (k >> 1); }
-    __device__ __forceinline__ int col(int j, int k) const { return colbase + 8 * j + (k & 1); }
-};
 
 // T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kP), in two levels of 2 x 2
 // block recursion: the four diagonal 16 x 16 blocks by forward substitution (a column per
@@ -473,22 +454,24 @@ namespace gdn {
 namespace {
 
 struct SweepSmem {
-    size_t wc, tc, vb, qk, pk, sop, dt, de, ckst, ysg, rsg, vec, bar, tslot, total;
+    size_t wgrp, wc, tc, vb, qk, pk, sop, dt, de, ysg, rsg, vec, bar, tslot, total;
     __host__ __device__ SweepSmem(int DK) {
         size_t o = 0;
-        wc = o; o += (size_t)kL * DK * 2;      // -W of the chunk                    A [64][DK]
-        tc = o; o += (size_t)kL * kL * 2;      // T diag(beta)                       A [64][64]
-        vb = o; o += (size_t)kL * kL * 2;      // V of the chunk, this block's 64 columns [64 t][64 v] (read MN-major)
+        // group W, two buffers (chunks alternate): -W, T diag(beta), V
+        wgrp = (size_t)kL * DK * 2 + 2 * (size_t)kL * kL * 2;
+        wc = o;                                // -W of the chunk                    A [64][DK]
+        tc = wc + (size_t)kL * DK * 2;         // T diag(beta)                       A [64][64]
+        vb = tc + (size_t)kL * kL * 2;         // V of the chunk, this block's 64 columns [64 t][64 v] (read MN-major)
+        o += 2 * wgrp;
         qk = o; o += (size_t)2 * kL * DK * 2;  // [Q; K] of the chunk (kv head)      A [128][DK]; K read MN-major as B
         pk = o; o += (size_t)2 * kL * kL * 2;  // [(Q K^T) o E_incl; (K K^T) o E_strict]   A [128][64]
         sop = o; o += (size_t)kL * DK * 2;     // S (64 value rows)                  B [64][DK]
         dt = o; o += (size_t)kL * kL * 2;      // Delta [64 t][64 v], read MN-major (B)
         de = o; o += (size_t)kL * kL * 2;      // diag(E_L) Delta [64 t][64 v], read MN-major (A, transposed)
-        ckst = al(o, 1024); o = ckst + (size_t)kL * DK * 4;   // chunk-start state, fp32, boxes of [64][32] in the 128-byte swizzle
         ysg = al(o, 1024); o = ysg + (size_t)kL * 128;        // y of a chunk, bf16 [64][64] in the 128-byte swizzle
         rsg = al(o, 1024); o = rsg + (size_t)2 * kL * 128;    // v - u of a chunk, fp32 [2][64][32] in the 128-byte swizzle
         vec = o; o += 5 * kL * 4;              // Lam [2][64], exp Lam [2][64] (two chunks), E(L, .) [64]
-        bar = al(o, 8); o = bar + 6 * 8;       // copies (W, T diag(beta), V), copies ([Q; K], [P; KKm]), products D, U, Y, drain
+        bar = al(o, 8); o = bar + 7 * 8;       // copies of group W (two buffers), of group R ([Q; K], [P; KKm]); products D, U, Y; drain
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -524,27 +507,31 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 1024));
     const SweepSmem L(DK);
-    unsigned char *wc = base + L.wc, *tcs = base + L.tc, *vb = base + L.vb, *qk = base + L.qk, *pk = base + L.pk;
+    unsigned char *qk = base + L.qk, *pk = base + L.pk;
     unsigned char *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
-    unsigned char *ckst = base + L.ckst, *ysg = base + L.ysg, *rsg = base + L.rsg;
+    unsigned char *ysg = base + L.ysg, *rsg = base + L.rsg;
     float *Lm2 = reinterpret_cast<float *>(base + L.vec), *gm2 = Lm2 + 2 * kL, *eL = gm2 + 2 * kL;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
-    uint64_t *bW = bar, *bR = bar + 1, *mD = bar + 2, *mU = bar + 3, *mY = bar + 4, *mX = bar + 5;
+    uint64_t *bW = bar, *bR = bar + 2, *mD = bar + 3, *mU = bar + 4, *mY = bar + 5, *mX = bar + 6;   // bW[2]
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const size_t head = (size_t)b * Hv + h;
     const int hk = h / (Hv / p.Hk);
     // copies of chunk cc (thread 32): group W (-W, T diag(beta) and this block's V, read by the
-    // Delta products) and group R ([Q; K] and [P; KKm], read by the update and [y; u] products)
-    int nW = 0, nR = 0;
+    // Delta products; buffer cc % 2, fetched two chunks ahead) and group R ([Q; K] and [P; KKm],
+    // read by the update and [y; u] products)
+    int nW0 = 0, nW1 = 0, nR = 0;   // copies issued into group W's buffers 0 and 1, group R
+    auto wbuf = [&](int cc) { return base + L.wc + (size_t)(cc & 1) * L.wgrp; };
     auto issue_w = [&](int cc) {
         const size_t ck = head * NC + cc;
-        mbar_expect_tx(bW, kL * DK * 2 + 2 * kL * kL * 2);
-        bulk_load(wc, p.wm + ck * kL * DK, kL * DK * 2, bW);
-        bulk_load(tcs, p.tcm + ck * kL * kL, kL * kL * 2, bW);
-        tma_load_5d(vb, &maps.vb, bW, 0, cc * kL, r0 / 8, h, b);
-        ++nW;
+        unsigned char *g = wbuf(cc);
+        uint64_t *bw = bW + (cc & 1);
+        mbar_expect_tx(bw, kL * DK * 2 + 2 * kL * kL * 2);
+        bulk_load(g, p.wm + ck * kL * DK, kL * DK * 2, bw);
+        bulk_load(g + (L.tc - L.wc), p.tcm + ck * kL * kL, kL * kL * 2, bw);
+        tma_load_5d(g + (L.vb - L.wc), &maps.vb, bw, 0, cc * kL, r0 / 8, h, b);
+        if (cc & 1) ++nW1; else ++nW0;
     };
     auto issue_r = [&](int cc) {
         mbar_expect_tx(bR, 2 * kL * DK * 2 + 2 * kL * kL * 2);
@@ -554,13 +541,10 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     };
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(bar + i, 1);
+        for (int i = 0; i < 7; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
     }
-    if (tid == 32) {
-        tma_prefetch_map(&maps.ck);
-        tma_prefetch_map(&maps.vb);
-    }
+    if (tid == 32) tma_prefetch_map(&maps.vb);
     if (tid == 128) {
         tma_prefetch_map(&maps.y);
         tma_prefetch_map(&maps.r);
@@ -572,7 +556,11 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tSg = tmem, tD = tmem + DK, tQK = tmem + DK + 64, tPD = tmem + DK + 128;
-    if (tid == 32) { issue_w(0); issue_r(0); }
+    if (tid == 32) {
+        issue_w(0);
+        if (NC > 1) issue_w(1);
+        issue_r(0);
+    }
 
     // this thread's fragment of the state (rows fs.row(k), columns fs.col(j, k))
     const M64Frag fs(warp, lane, DK);
@@ -640,7 +628,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         }
     };
 
-    unsigned wW = 0, wR = 0;
+    unsigned wR = 0;
     bool ok = true, fail = false;   // fail: a bounded wait of this thread ran out (all learn it at the next block barrier)
     float lamn = 0.f;               // Lam of the next chunk (threads < 64)
     if (tid < kL) lamn = p.lam[head * NC * kL + tid];
@@ -648,8 +636,8 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     for (int c = 0; c < NC; ++c) {
         const size_t chk = head * NC + c;
         const int cb = c & 1;
-        // ---- (A) the previous chunk's stores have read sop, ckst (thread 32) and ysg, rsg
-        // (thread 128); this chunk's decays
+        // ---- (A) the previous chunk's stores have read sop (thread 32) and ysg, rsg (thread 128);
+        // this chunk's decays
         if (tid == 32 || tid == 128) bulk_wait_read();
         if (tid < kL) {
             Lm2[cb * kL + tid] = lamn;
@@ -660,10 +648,10 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         if (!ok) break;
         if (tid < kL) eL[tid] = expf(Lm2[cb * kL + kL - 1] - Lm2[cb * kL + tid]);
         // ---- (B) U = (T diag(beta)) V starts Delta's accumulator; S <- exp(Lam_L) S + Sigma of the
-        // previous chunk; S as an operand and staged for the checkpoint store
+        // previous chunk; S as an operand, and the fp32 checkpoint stored from registers
+        unsigned char *wc = wbuf(c), *tcs = wc + (L.tc - L.wc), *vb = wc + (L.vb - L.wc);
         if (warp == 0) {
-            fail = !mbar_wait(bW, wW & 1);
-            ++wW;
+            fail = !mbar_wait(bW + cb, (c >> 1) & 1);
             if (!fail)
                 umma_gemm_w(tD, CmOp{tcs, kL, 0, 0, false}, CmOp{vb, kL, 0, 0, true}, kL,
                             umma_idesc_t(1, kL, kL, false, true), false, lead);
@@ -685,31 +673,33 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
             tc_fence_after();
             if (tid == 32) issue_r(c);
         }
+        {
+            // a warp's store covers 8 rows x 32 contiguous bytes: whole 32-byte sectors; streamed
+            // (the backward reads the bf16 copy)
+            float *ck = p.ckpt + (chk * Dv + r0) * DK;
 #pragma unroll
-        for (int j = 0; j < NS / 4; ++j)
+            for (int j = 0; j < NS / 4; ++j)
 #pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int row = fs.row(2 * k2), col = fs.col(j, 0);
-                const float s0 = S[4 * j + 2 * k2], s1 = S[4 * j + 2 * k2 + 1];
-                *reinterpret_cast<uint32_t *>(sop + cm_off(row, 2 * col, kL)) = pack2_bf16(s0, s1);
-                // box col / 32: row at row * 128, 16-byte chunk (col % 32) / 4 at chunk ^ (row % 8)
-                *reinterpret_cast<float2 *>(ckst + (col >> 5) * (kL * 128) + row * 128 +
-                                            ((((col & 31) >> 2) ^ (row & 7)) << 4) + (col & 3) * 4) = make_float2(s0, s1);
-            }
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int row = fs.row(2 * k2), col = fs.col(j, 0);
+                    const float s0 = S[4 * j + 2 * k2], s1 = S[4 * j + 2 * k2 + 1];
+                    *reinterpret_cast<uint32_t *>(sop + cm_off(row, 2 * col, kL)) = pack2_bf16(s0, s1);
+                    __stcs(reinterpret_cast<float2 *>(ck + row * DK + col), make_float2(s0, s1));
+                }
+        }
         fence_proxy_async();
         tc_fence_before();
         ok = !__syncthreads_or(fail);
         tc_fence_after();
         if (!ok) break;
-        // ---- (C) Delta += (-W) S^T; the state leaves (bf16 operand for the backward, fp32
-        // checkpoint); y and v - u of the previous chunk
+        // ---- (C) Delta += (-W) S^T; the bf16 state leaves (the backward's operand); y and v - u of
+        // the previous chunk
         if (warp == 0) {
             umma_gemm_w(tD, CmOp{wc, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, umma_idesc(1, kL, kL), true, lead);
             umma_commit_w(mD, lead);
         }
         if (tid == 32) {
             bulk_store(p.s0m + (chk * gridDim.x + split) * kL * DK, sop, kL * DK * 2);
-            tma_store_5d(&maps.ck, ckst, 0, (int)(chk * Dv + r0), 0, 0, 0);
             bulk_commit();
         }
         if (warp >= 4) {
@@ -719,7 +709,7 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
         // ---- (D) Delta as operands: Delta (for [P; KKm] Delta) and diag(E_L) Delta (for the update)
         fail = !mbar_wait(mD, c & 1);
         tc_fence_after();
-        if (tid == 32 && c + 1 < NC) issue_w(c + 1);       // -W, T diag(beta) and V are free again
+        if (tid == 32 && c + 2 < NC) issue_w(c + 2);       // this buffer of group W is free again
         {
             float x[16];
             tmem_ld16x256_x4(tD + lane16 + 32 * (warp >> 2), x);
@@ -789,7 +779,8 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     if (!ok && tid == 32) {
         report_status(p.status, kStatusTimeout);
         // copies still in flight land before the CTA exits (each wait bounded)
-        if (nW > 0) mbar_wait(bW, (nW - 1) & 1);
+        if (nW0 > 0) mbar_wait(bW, (nW0 - 1) & 1);
+        if (nW1 > 0) mbar_wait(bW + 1, (nW1 - 1) & 1);
         if (nR > 0) mbar_wait(bR, (nR - 1) & 1);
     }
     if (!ok && warp == 0) {

@@ -95,26 +95,29 @@ struct DSweepSmem {
 }  // namespace
 
 // One CTA per (block of 64 value rows, value head, batch row), over the chunks in reverse.
-// Warp 0 issues the products (from one elected lane, the warp converged); thread 32 issues the
-// copies and the stores.
-// Tensor memory (M = 64 layout: row r in lane r % 16 + 32 (r / 16)):
-//   [0, DK)              dS (value rows of this block)
+// The adjoint dS (fp32) lives in registers (a thread holds the 16x256b fragment of an M = 64
+// accumulator: 2 rows x DK/8 columns); per chunk the products are (fp32 accumulators in tensor
+// memory, M = 64 layout: row r in lane r % 16 + 32 (r / 16)):
+//   [0, DK)              the chunk's part of the carry, [e^Lam dY; e^Lam dU]^T [Q; K]; the
+//                        next chunk's dS = exp(Lam_L) dS + this
 //   [DK, DK + 128)       K [dS_high; dS_low]^T (one N = 128 product: chunk row t, value column
 //                        of the high part, then of the low part); then dD in the first 64
 //   [DK + 128, DK + 192) P^T dY
+// Warp 0 issues the products (from one elected lane, the warp converged); thread 32 issues the
+// copies and the stores; every thread converts (all 32 lanes of a warp hold fragment values).
 template <int E>
 __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, const __grid_constant__ CUtensorMap tm_dv,
                                                               const __grid_constant__ CUtensorMap tm_dy,
                                                               const __grid_constant__ CUtensorMap tm_rs) {
     constexpr int DK = 32 * E;
+    constexpr int SC = DK / 2;                // dS columns per warp half
+    constexpr int NS = SC / 2;                // dS values per thread
     static_assert(DK + 192 <= 512, "tensor memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, r0 = split * kL, nsplit = p.nsplit;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int lrow = 16 * quarter + lane;                   // M = 64 row of this lane (lanes 0-15)
-    const bool rowlane = lane < 16;
-    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const int hw = warp >> 2;                                   // warp half: value columns [32 hw, 32 hw + 32)
+    const uint32_t lane16 = (uint32_t)(32 * (warp & 3)) << 16;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
@@ -122,7 +125,8 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     unsigned char *qk = base + L.qk, *tmm = base + L.tm, *pmm = base + L.pkm, *yds = base + L.yds;
     unsigned char *ydu2 = base + L.ydu, *shl = base + L.shl, *rhs = base + L.rhs, *dls = base + L.dls;
     unsigned char *dvs = base + L.dvs;
-    float *rsm = reinterpret_cast<float *>(base + L.rsm), *lms = reinterpret_cast<float *>(base + L.lms);
+    unsigned char *rsm = base + L.rsm;
+    float *lms = reinterpret_cast<float *>(base + L.lms);
     float *eL = reinterpret_cast<float *>(base + L.vec) + kL, *bt = eL + kL;
     float *red = reinterpret_cast<float *>(base + L.red);   // [2][2][64]
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
@@ -155,6 +159,8 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     if (tid == 0) {
         for (int i = 0; i < 6; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
+    }
+    if (tid == 32) {
         tma_prefetch_map(&tm_dy);
         tma_prefetch_map(&tm_rs);
         tma_prefetch_map(&tm_dv);
@@ -166,24 +172,28 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tS = tmem, tX = tmem + DK, tP = tmem + DK + 128;
-    constexpr int SC = DK / 2;                              // state columns per warp half
 
-    // dS_T into tensor memory
-    {
-        float x[16];
-        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
+    // this thread's fragment of dS (rows fs.row(k), columns fs.col(j, k)), from dS_T
+    const M64Frag fs(warp, lane, DK);
+    float dS[NS];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                x[i] = (p.dS_T != nullptr && rowlane && r0 + lrow < Dv)
-                           ? p.dS_T[(head * Dv + r0 + lrow) * DK + cc + i] : 0.f;
-            tmem_st16f(tS + lane_off + cc, x);
+    for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+            float2 s2 = make_float2(0.f, 0.f);
+            if (p.dS_T != nullptr)
+                s2 = *reinterpret_cast<const float2 *>(p.dS_T + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0));
+            dS[4 * j + 2 * k2] = s2.x;
+            dS[4 * j + 2 * k2 + 1] = s2.y;
         }
-        tmem_wait_st();
-    }
+    // this thread's fragment of the 64-column accumulators (chunk rows t, value columns)
+    const M64Frag fd(warp, lane, kL);
+    const int ta = fd.row(0), tb = fd.row(2);
+
     unsigned ph = 0, cph = 0;
     bool ok = true;
     // a chunk's dY block, its v - u (one TMA box of two 128-byte-swizzled [64][32] tiles) and
-    // Lam (a bulk copy) arrive one chunk ahead, issued by thread 0 (rows past T: zeros); beta
+    // Lam (a bulk copy) arrive one chunk ahead, issued by thread 32 (rows past T: zeros); beta
     // (threads < 64) by a load one chunk ahead
     __nv_bfloat16 btn = __float2bfloat16_rn(0.f);   // raw: converted where it is used, so that the load does not stall here
     int nY = 0, wY = 0;
@@ -202,8 +212,16 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         ++nY;
         if (tid < kL) btn = beta[((size_t)b * T + tt0 + (tid < ln ? tid : 0)) * Hv + h];
     };
+    // v - u of the thread's fragment: row t, value columns fd.col(j, 0), + 1 (box hw of rsm: row
+    // t at t * 128, 16-byte chunk (col % 32) / 4 at chunk ^ (t % 8))
+    auto rs_pair = [&](int t, int j) {
+        const int c32 = 8 * j + 2 * (lane & 3);
+        return *reinterpret_cast<const float2 *>(rsm + hw * (kL * 128) + t * 128 + (((c32 >> 2) ^ (t & 7)) << 4) +
+                                                 (c32 & 3) * 4);
+    };
     if (tid == 32) { copy_A(p.NC - 1); copy_T(p.NC - 1); copy_K(p.NC - 1); }
     fetch_chunk(p.NC - 1, 0);
+    float decay_next = 1.f;                       // exp(Lam_L) of the chunk processed before (later in time)
     for (int c = p.NC - 1; c >= 0 && ok; --c) {
         const int t0 = c * kL, len = min(kL, T - t0);
         const size_t chk = head * p.NC + c;
@@ -222,7 +240,24 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
             ok = !__syncthreads_or(!w);
             if (!ok) break;
         }
-        const float decay = expf(lmb[kL - 1]);
+        // this thread's v - u (rows ta, tb), read before the next chunk's copy overwrites rsm
+        float2 rsa[4], rsb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            rsa[j] = rs_pair(ta, j);
+            rsb[j] = rs_pair(tb, j);
+        }
+        // ---- dS of this chunk's end: exp(Lam_L) dS + the later chunk's part of the carry
+        if (c < p.NC - 1) {
+#pragma unroll
+            for (int i = 0; i < NS / 16; ++i) {
+                float x[16];
+                tmem_ld16x256_x4(tS + lane16 + SC * hw + 32 * i, x);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) dS[16 * i + e] = fmaf(decay_next, dS[16 * i + e], x[e]);
+            }
+        }
         // diag(exp Lam) dY: rows 0-63 of the dS update's operand (the dU rows follow below)
         for (int e = tid; e < kL * kL / 8; e += 256) {
             const int t = e & (kL - 1);
@@ -234,47 +269,23 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
             for (int i = 0; i < 8; ++i) x8[i] *= gt;
             *reinterpret_cast<uint4 *>(yds + o) = pack8(x8);
         }
-        // this lane's v - u (row lrow, 32 value columns: box `half`, 16-byte piece i of the row
-        // at ((i ^ (row & 7)) << 4))
-        float rs[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 f4 = rowlane ? *reinterpret_cast<const float4 *>(reinterpret_cast<const unsigned char *>(rsm) +
-                                                                          half * kL * 128 + lrow * 128 + ((i ^ (lrow & 7)) << 4))
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-            rs[4 * i] = f4.x; rs[4 * i + 1] = f4.y; rs[4 * i + 2] = f4.z; rs[4 * i + 3] = f4.w;
-        }
-        // ---- dS (the adjoint of the chunk-end state) as operands (high and low bf16 parts),
-        // the high part also stored for the gradient kernel ([64][DK] operand layout: a warp's
-        // 16 rows of one K chunk are 256 contiguous bytes); then dS <- exp(Lam_L) dS in place
+        // ---- dS as operands (high and low bf16 parts, [hi; lo] [128][DK]); the high part also
+        // stored for the gradient kernel ([64][DK] operand layout: a warp's store covers one
+        // 128-byte core matrix)
         {
             unsigned char *dsl_g = reinterpret_cast<unsigned char *>(p.ws_dsl + (chk * nsplit + split) * kL * DK);
-            // all of this thread's columns loaded from tensor memory before one wait
-            float xs[SC];
 #pragma unroll
-            for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tS + lane_off + half * SC + 32 * j, xs + 32 * j);
-            tmem_wait_ld();
-            if (rowlane) {
+            for (int j = 0; j < NS / 4; ++j)
 #pragma unroll
-                for (int j = 0; j < SC / 8; ++j) {
-                    float hi[8], lo[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        hi[i] = __bfloat162float(__float2bfloat16_rn(xs[8 * j + i]));
-                        lo[i] = xs[8 * j + i] - hi[i];
-                    }
-                    const uint4 hu = pack8(hi);
-                    const int kb = 2 * (half * SC + 8 * j);
-                    *reinterpret_cast<uint4 *>(shl + cm_off(lrow, kb, 2 * kL)) = hu;
-                    *reinterpret_cast<uint4 *>(shl + cm_off(kL + lrow, kb, 2 * kL)) = pack8(lo);
-                    *reinterpret_cast<uint4 *>(dsl_g + cm_off(lrow, kb, kL)) = hu;
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int row = fs.row(2 * k2), col = fs.col(j, 0);
+                    const float x0 = dS[4 * j + 2 * k2], x1 = dS[4 * j + 2 * k2 + 1];
+                    const uint32_t hu = pack2_bf16(x0, x1);
+                    const float h0 = __uint_as_float(hu << 16), h1 = __uint_as_float(hu & 0xffff0000u);
+                    *reinterpret_cast<uint32_t *>(shl + cm_off(row, 2 * col, 2 * kL)) = hu;
+                    *reinterpret_cast<uint32_t *>(shl + cm_off(kL + row, 2 * col, 2 * kL)) = pack2_bf16(x0 - h0, x1 - h1);
+                    *reinterpret_cast<uint32_t *>(dsl_g + cm_off(row, 2 * col, kL)) = hu;
                 }
-            }
-#pragma unroll
-            for (int i = 0; i < SC; ++i) xs[i] *= decay;
-#pragma unroll
-            for (int j = 0; j < SC / 32; ++j) tmem_st32f(tS + lane_off + half * SC + 32 * j, xs + 32 * j);
-            tmem_wait_st();
         }
         fence_proxy_async();
         tc_fence_before();
@@ -301,34 +312,38 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         ++ph;
         tc_fence_after();
         if (!ok) break;
-        // ---- rhs = diag(E_L) K dS^T + P^T dY as an operand; f partial = beta_t (v_t - u_t) . (dS k_t)
+        // ---- rhs = diag(E_L) K dS^T + P^T dY as an operand; Delta = beta (v - u) for the gradient
+        // kernel; f partial = beta_t (v_t - u_t) . (dS k_t)
         {
-            float x[32], xl[32], y2[32];
-            tmem_ld32f(tX + lane_off + half * 32, x);
-            tmem_ld32f(tX + lane_off + kL + half * 32, xl);
-            tmem_ld32f(tP + lane_off + half * 32, y2);
+            float xh[16], xl[16], pp[16];
+            tmem_ld16x256_x4(tX + lane16 + 32 * hw, xh);
+            tmem_ld16x256_x4(tX + lane16 + kL + 32 * hw, xl);
+            tmem_ld16x256_x4(tP + lane16 + 32 * hw, pp);
             tmem_wait_ld();
+            const float ela = eL[ta], elb = eL[tb], ba = bt[ta], bb = bt[tb];
+            float fa = 0.f, fb = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] += xl[i];           // K dS^T = K dS_high^T + K dS_low^T
-            if (rowlane) {
-                const float el = eL[lrow];
-                float fs = 0.f;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    fs = fmaf(rs[i], x[i], fs);
-                    y2[i] = fmaf(el, x[i], y2[i]);
-                }
-                const float bb = bt[lrow];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t o = cm_off(lrow, 2 * (half * 32 + 8 * j), kL);
-                    *reinterpret_cast<uint4 *>(rhs + o) = pack8(y2 + 8 * j);
-                    float dl8[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) dl8[i] = bb * rs[8 * j + i];
-                    *reinterpret_cast<uint4 *>(dls + o) = pack8(dl8);   // Delta for the gradient kernel
-                }
-                red[half * kL + lrow] = bb * fs;
+            for (int j = 0; j < 4; ++j) {
+                const float2 ra = rsa[j], rb = rsb[j];
+                const float x0 = xh[4 * j] + xl[4 * j], x1 = xh[4 * j + 1] + xl[4 * j + 1];
+                const float x2 = xh[4 * j + 2] + xl[4 * j + 2], x3 = xh[4 * j + 3] + xl[4 * j + 3];
+                fa = fmaf(ra.x, x0, fmaf(ra.y, x1, fa));
+                fb = fmaf(rb.x, x2, fmaf(rb.y, x3, fb));
+                const int col = fd.col(j, 0);
+                const uint32_t oa = cm_off(ta, 2 * col, kL), ob = cm_off(tb, 2 * col, kL);
+                *reinterpret_cast<uint32_t *>(rhs + oa) = pack2_bf16(fmaf(ela, x0, pp[4 * j]), fmaf(ela, x1, pp[4 * j + 1]));
+                *reinterpret_cast<uint32_t *>(rhs + ob) = pack2_bf16(fmaf(elb, x2, pp[4 * j + 2]), fmaf(elb, x3, pp[4 * j + 3]));
+                *reinterpret_cast<uint32_t *>(dls + oa) = pack2_bf16(ba * ra.x, ba * ra.y);
+                *reinterpret_cast<uint32_t *>(dls + ob) = pack2_bf16(bb * rb.x, bb * rb.y);
+            }
+            // the row sums over this warp's 32 columns: the four lanes that share a row
+            fa += __shfl_xor_sync(kFullMask, fa, 1);
+            fa += __shfl_xor_sync(kFullMask, fa, 2);
+            fb += __shfl_xor_sync(kFullMask, fb, 1);
+            fb += __shfl_xor_sync(kFullMask, fb, 2);
+            if ((lane & 3) == 0) {
+                red[hw * kL + ta] = ba * fa;
+                red[hw * kL + tb] = bb * fb;
             }
         }
         fence_proxy_async();
@@ -350,46 +365,52 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         tc_fence_after();
         if (!ok) break;
         if (tid == 32 && c > 0) copy_T(c - 1);
-        // ---- dv = beta dD, dbeta partial, dU = -beta dD (operand, and stored for the gradient kernel)
+        // ---- dv = beta dD, dbeta partial, dU = -beta dD (operand rows 64-127, stored for the
+        // gradient kernel) and exp(Lam) dU (the dS update's operand)
         {
-            float x[32];
-            tmem_ld16f(tX + lane_off + half * 32, *reinterpret_cast<float (*)[16]>(x));
-            tmem_ld16f(tX + lane_off + half * 32 + 16, *reinterpret_cast<float (*)[16]>(x + 16));
+            float x[16];
+            tmem_ld16x256_x4(tX + lane16 + 32 * hw, x);
             tmem_wait_ld();
-            if (rowlane) {
-                const float bb = bt[lrow], gt = expf(lmb[lrow]);
-                float ds = 0.f, dvv[32], duu[32], dus[32];
+            const float ba = bt[ta], bb = bt[tb], ga = expf(lmb[ta]), gb = expf(lmb[tb]);
+            float da = 0.f, db = 0.f;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    ds = fmaf(x[i], rs[i], ds);
-                    dvv[i] = bb * x[i];
-                    duu[i] = -dvv[i];
-                    dus[i] = gt * duu[i];
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t o = cm_off(kL + lrow, 16 * (half * 4 + j), 2 * kL);
-                    *reinterpret_cast<uint4 *>(ydu + o) = pack8(duu + 8 * j);
-                    *reinterpret_cast<uint4 *>(yds + o) = pack8(dus + 8 * j);
-                }
-                // dv staged in the 128-byte swizzle for a TMA store (rows past T are clipped by it)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(dvs + lrow * 128 + (((half * 4 + j) ^ (lrow & 7)) << 4)) = pack8(dvv + 8 * j);
-                red[2 * kL + half * kL + lrow] = ds;
+            for (int j = 0; j < 4; ++j) {
+                const float2 ra = rsa[j], rb = rsb[j];
+                da = fmaf(x[4 * j], ra.x, fmaf(x[4 * j + 1], ra.y, da));
+                db = fmaf(x[4 * j + 2], rb.x, fmaf(x[4 * j + 3], rb.y, db));
+                const int col = fd.col(j, 0);
+                const float va0 = ba * x[4 * j], va1 = ba * x[4 * j + 1], vb0 = bb * x[4 * j + 2], vb1 = bb * x[4 * j + 3];
+                const uint32_t oa = cm_off(kL + ta, 2 * col, 2 * kL), ob = cm_off(kL + tb, 2 * col, 2 * kL);
+                *reinterpret_cast<uint32_t *>(ydu + oa) = pack2_bf16(-va0, -va1);
+                *reinterpret_cast<uint32_t *>(ydu + ob) = pack2_bf16(-vb0, -vb1);
+                *reinterpret_cast<uint32_t *>(yds + oa) = pack2_bf16(-ga * va0, -ga * va1);
+                *reinterpret_cast<uint32_t *>(yds + ob) = pack2_bf16(-gb * vb0, -gb * vb1);
+                // dv staged in the 128-byte swizzle for a TMA store (rows past T are clipped by it):
+                // row t at t * 128, 16-byte chunk col / 8 at chunk ^ (t % 8)
+                *reinterpret_cast<uint32_t *>(dvs + ta * 128 + (((col >> 3) ^ (ta & 7)) << 4) + (col & 7) * 2) =
+                    pack2_bf16(va0, va1);
+                *reinterpret_cast<uint32_t *>(dvs + tb * 128 + (((col >> 3) ^ (tb & 7)) << 4) + (col & 7) * 2) =
+                    pack2_bf16(vb0, vb1);
+            }
+            da += __shfl_xor_sync(kFullMask, da, 1);
+            da += __shfl_xor_sync(kFullMask, da, 2);
+            db += __shfl_xor_sync(kFullMask, db, 1);
+            db += __shfl_xor_sync(kFullMask, db, 2);
+            if ((lane & 3) == 0) {
+                red[2 * kL + hw * kL + ta] = da;
+                red[2 * kL + hw * kL + tb] = db;
             }
         }
         fence_proxy_async();
-        tc_fence_before();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
         if (tid < kL && tid < len)
             p.ws_db[((rowbase + tid) * Hv + h) * nsplit + split] = red[2 * kL + tid] + red[3 * kL + tid];
-        // ---- dS += [diag(exp Lam) dY; diag(exp Lam) dU]^T [Q; K] (K = 128)
+        // ---- the chunk's part of the carry: [diag(exp Lam) dY; diag(exp Lam) dU]^T [Q; K] (K = 128)
         if (warp == 0) {
             umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, 2 * kL,
-                        umma_idesc_t(1, kL, DK, true, true), true, lead);
+                        umma_idesc_t(1, kL, DK, true, true), false, lead);
             umma_commit_w(bar, lead);
         }
         if (tid == 32) {
@@ -406,21 +427,27 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         if (!ok) break;
         if (tid == 32 && c > 0) copy_K(c - 1);         // [Q; K] is free again
         ++cph;
+        decay_next = expf(lmb[kL - 1]);
         // no block barrier before the next chunk: nothing after this point reads what its first
         // section writes
     }
     if (tid == 32) bulk_wait_all();                         // the block outputs are complete
     if (ok && p.dS0 != nullptr) {
-        for (int cc = half * SC; cc < half * SC + SC; cc += 16) {
-            float x[16];
-            tmem_ld16f(tS + lane_off + cc, x);
-            tmem_wait_ld();
-            if (rowlane && r0 + lrow < Dv)
+        // dS0 = exp(Lam_L) dS + the first chunk's part of the carry
 #pragma unroll
-                for (int i = 0; i < 16; i += 4)
-                    *reinterpret_cast<float4 *>(p.dS0 + (head * Dv + r0 + lrow) * DK + cc + i) =
-                        make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+        for (int i = 0; i < NS / 16; ++i) {
+            float x[16];
+            tmem_ld16x256_x4(tS + lane16 + SC * hw + 32 * i, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) dS[16 * i + e] = fmaf(decay_next, dS[16 * i + e], x[e]);
         }
+#pragma unroll
+        for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2)
+                *reinterpret_cast<float2 *>(p.dS0 + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0)) =
+                    make_float2(dS[4 * j + 2 * k2], dS[4 * j + 2 * k2 + 1]);
     }
     if (!ok && tid == 32) {
         report_status(p.status, kStatusTimeout);

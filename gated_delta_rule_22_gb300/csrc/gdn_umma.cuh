@@ -202,6 +202,26 @@ __device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, float *v) {
         : "memory");
 }
 
+// Where a thread's values of an M = 64 accumulator of N columns lie when the 8 warps of a
+// 256-thread CTA read it with 16x256b loads: warp w reads rows 16 (w % 4) .. + 15 (tensor-memory
+// lanes 32 (w % 4) .. + 15) and columns [N/2 (w / 4), N/2 (w / 4 + 1)); value e = 4 j + k of the
+// thread (j the 8-column repetition, k = 0..3) is row row(k) and column col(j, k).
+struct M64Frag {
+    int row0, colbase;
+    __device__ __forceinline__ M64Frag(int warp, int lane, int N) {
+        row0 = 16 * (warp & 3) + (lane >> 2);
+        colbase = (N / 2) * (warp >> 2) + 2 * (lane & 3);
+    }
+    __device__ __forceinline__ int row(int k) const { return row0 + 8 * (k >> 1); }
+    __device__ __forceinline__ int col(int j, int k) const { return colbase + 8 * j + (k & 1); }
+};
+
+// Two values as a bf16 pair (round to nearest even), the first in the low half.
+__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
 // 32x32b tensor-memory load of 16 consecutive columns.
 __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
     asm volatile(
