@@ -490,7 +490,11 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         if (rc != GDN_OK) return rc;
         rc = make_colblock_map(&tm_rs, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true);
         if (rc != GDN_OK) return rc;
-        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_rs, p.Dk, (cudaStream_t)stream));
+        CUtensorMap tm_dq, tm_dk;
+        if ((rc = make_btd_map(&tm_dq, dq, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK ||
+            (rc = make_btd_map(&tm_dk, dk, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK)
+            return rc;
+        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_rs, tm_dq, tm_dk, p.Dk, (cudaStream_t)stream));
     }
     const Workspace w = workspace_layout(p);
 

@@ -30,14 +30,15 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 
 __host__ __device__ inline size_t al(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Prep runs two CTAs per SM (each 256 tensor-memory columns and under half of the shared
+// memory), so that one CTA's serial steps (the inversion, the products' round trips) overlap
+// the other's.
 struct PrepSmem {
-    size_t kc, qc, kk, qk, am, ts, xs, tcw, tcu, lam, bar, tslot, total;
+    size_t kc, qc, am, ts, xs, tcw, tcu, lam, bar, tslot, total;
     __host__ __device__ PrepSmem(int DK) {
         size_t o = 0;
         kc = o; o += (size_t)kL * DK * 2;           // K of the chunk, bf16 operand [64][DK]
         qc = o; o += (size_t)kL * DK * 2;           // Q of the chunk
-        kk = o; o += (size_t)kL * kP * 4;           // K K^T, fp32
-        qk = o; o += (size_t)kL * kP * 4;           // Q K^T, fp32
         am = o; o += (size_t)kL * kP * 4;           // A
         ts = o; o += (size_t)kL * kP * 4;           // T = (I + A)^-1 (blocks above the diagonal not written)
         xs = o; o += (size_t)32 * 32 * 4;           // block products of the inversion
@@ -47,7 +48,6 @@ struct PrepSmem {
         bar = al(o, 8); o = bar + 2 * 8;            // MMA, copies of K and Q
         tslot = o; o += 16;
         total = o + 1024;
-        if (total < kOneCtaSmem) total = kOneCtaSmem;
     }
 };
 
@@ -150,18 +150,20 @@ __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid
 
 }  // namespace
 
-// Persistent: one CTA per SM over a contiguous range of units (batch row, chunk, kv head,
+// Persistent: two CTAs per SM, each over a contiguous range of units (batch row, chunk, kv head,
 // value head), value head fastest. When a unit starts a new (batch row, chunk, kv head) group
-// the CTA forms K K^T and Q K^T from K and Q (fetched by TMA while the previous group's last
-// unit was read back) and stores [Q; K] for the sweeps and the gradient kernel; per unit (value
-// head) it forms the decay-weighted matrices, T, and W = (T diag(beta exp Lam)) K (the row
-// scalings folded into T's columns, K read as an MN-major operand), stored negated for the
-// sweep's single Delta accumulation, and stores T and T diag(beta) (the sweep forms U from the
-// latter and V).
+// the CTA stores [Q; K] for the sweeps and the gradient kernel (K and Q fetched by TMA while the
+// previous group's last unit was read back). Per unit (value head) it forms K K^T and Q K^T on
+// the tensor cores (again per unit: tensor memory holds them only until the unit's W), reads
+// them straight from tensor memory into the decay-weighted matrices and A, inverts, and forms
+// W = (T diag(beta exp Lam)) K (the row scalings folded into T's columns, K read as an MN-major
+// operand), stored negated for the sweep's single Delta accumulation; it stores T and
+// T diag(beta) (the sweep forms U from the latter and V).
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int units,
+__global__ void __launch_bounds__(256, 2) chunk_prep_kernel(ChunkParams p, int units,
                                                             const __grid_constant__ ChunkFwdMaps maps) {
     constexpr int DK = 32 * E;
+    static_assert(DK <= 256, "W fits the 256 tensor-memory columns of a CTA");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T, Hv = p.Hv, Hk = p.Hk, NC = p.NC, rep = p.Hv / p.Hk;
     const int u_begin = (int)((long long)blockIdx.x * units / gridDim.x);
@@ -171,8 +173,6 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
     unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 1024));
     const PrepSmem L(DK);
     unsigned char *kc = base + L.kc, *qc = base + L.qc, *tcw = base + L.tcw, *tcu = base + L.tcu;
-    float *kk = reinterpret_cast<float *>(base + L.kk);
-    float *qk = reinterpret_cast<float *>(base + L.qk);
     float *am = reinterpret_cast<float *>(base + L.am);
     float *ts = reinterpret_cast<float *>(base + L.ts);
     float *xs = reinterpret_cast<float *>(base + L.xs);
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         tma_prefetch_map(&maps.q);
         tma_prefetch_map(&maps.qk);
     }
-    if (warp == 0) tmem_alloc(tslot, 512);
+    if (warp == 0) tmem_alloc(tslot, 256);
     const uint32_t lead = warp == 0 ? elect_one_sync() : 0u;   // the lane of warp 0 that issues products
     int nKQ = 0, wKQ = 0;
     // log g and beta of a unit (warp 0, two steps per lane), raw
@@ -237,55 +237,6 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
     unsigned phase = 0;
     bool ok = true;
     uint32_t tmem = 0;
-    // A (batch row, chunk, kv head) group whose K and Q were fetched into kc and qc: K K^T and
-    // Q K^T into kk and qk, and [Q; K] in the 128-row operand layout of the sweeps and the
-    // gradient kernel (two TMA stores by thread 32, which waits for their reads before kc and
-    // qc are refilled)
-    auto stage_group = [&](const Unit &x) {
-        {
-            const bool w = mbar_wait(cbKQ, wKQ & 1);
-            ++wKQ;
-            tc_fence_before();
-            ok = !__syncthreads_or(!w);
-            tc_fence_after();
-            if (!ok) return;
-        }
-        // K K^T -> columns [0, 64), Q K^T -> [64, 128) (M = 64: row m in lane m % 16 + 32 (m / 16))
-        if (warp == 0) {
-            constexpr uint32_t id = umma_idesc(1, kL, kL);
-            umma_gemm_w(tmem, CmOp{kc, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, false}, DK, id, false, lead);
-            umma_gemm_w(tmem + kL, CmOp{qc, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, false}, DK, id, false, lead);
-            umma_commit_w(bar, lead);
-        }
-        if (tid == 32) {
-            // K chunk j of [Q; K]: the 64 rows of Q, then the 64 rows of K. A group split between
-            // two CTAs is written by both, alike.
-            const size_t ckv = ((size_t)x.b * Hk + x.hk) * NC + x.c;
-            tma_store_5d(&maps.qk, qc, 0, 0, 0, 0, (int)ckv);
-            tma_store_5d(&maps.qk, kc, 0, 0, 0, 1, (int)ckv);
-            bulk_commit();
-        }
-        ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
-        ++phase;
-        tc_fence_after();
-        if (ok) {
-            // warps 0-3 read K K^T, warps 4-7 Q K^T; each warp its quarter's 16 valid lanes
-            const int quarter = warp & 3, row = 16 * quarter + lane;
-            float *dst = warp < 4 ? kk : qk;
-            const uint32_t col0 = warp < 4 ? 0u : (uint32_t)kL;
-            float xv[64];
-            tmem_ld32f(tmem + ((uint32_t)(32 * quarter) << 16) + col0, xv);
-            tmem_ld32f(tmem + ((uint32_t)(32 * quarter) << 16) + col0 + 32, xv + 32);
-            tmem_wait_ld();
-            if (lane < 16)
-#pragma unroll
-                for (int i = 0; i < 64; i += 4)
-                    *reinterpret_cast<float4 *>(dst + row * kP + i) = make_float4(xv[i], xv[i + 1], xv[i + 2], xv[i + 3]);
-        }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    };
     // the first unit's g and beta go out before anything else, its K and Q once the barriers
     // are initialised
     if (u_begin < u_end && warp == 0) fetch_gb(unit_of(u_begin));
@@ -295,15 +246,36 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
     tmem = *tslot;
     if (u_begin < u_end) fetch_kq(unit_of(u_begin));
 
-    const M64Frag fw(warp, lane, DK);   // this thread's values of W (M = 64, DK columns)
+    const uint32_t lo16 = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's M = 64 rows in tensor memory
+    const M64Frag fa(warp, lane, kL);   // this thread's values of K K^T and Q K^T (M = 64, 64 columns)
+    const M64Frag fw(warp, lane, DK);   // and of W (M = 64, DK columns)
     for (int u = u_begin, i = 0; u < u_end && ok; ++u, ++i) {
         const Unit x = unit_of(u);
         const int b = x.b, c = x.c, h = x.h, len = x.len;
-        if (i == 0 || (u - 1) / rep != u / rep) {
-            stage_group(x);
-            if (!ok) break;
-        }
+        const bool newg = i == 0 || (u - 1) / rep != u / rep;
         const size_t chk = ((size_t)b * Hv + h) * NC + c;   // (b, h, c)
+        if (newg) {
+            // K and Q of the group have landed; [Q; K] leaves for the sweeps and the gradient kernel
+            // (K chunk j: the 64 rows of Q, then the 64 rows of K; a group split between two CTAs is
+            // written by both, alike)
+            const bool w = mbar_wait(cbKQ, wKQ & 1);
+            ++wKQ;
+            ok = !__syncthreads_or(!w);
+            if (!ok) break;
+            if (tid == 32) {
+                const size_t ckv = ((size_t)b * Hk + x.hk) * NC + c;
+                tma_store_5d(&maps.qk, qc, 0, 0, 0, 0, (int)ckv);
+                tma_store_5d(&maps.qk, kc, 0, 0, 0, 1, (int)ckv);
+                bulk_commit();
+            }
+        }
+        // K K^T -> columns [0, 64), Q K^T -> [64, 128) (M = 64: row m in lane m % 16 + 32 (m / 16))
+        if (warp == 0) {
+            constexpr uint32_t id = umma_idesc(1, kL, kL);
+            umma_gemm_w(tmem, CmOp{kc, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, false}, DK, id, false, lead);
+            umma_gemm_w(tmem + kL, CmOp{qc, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, false}, DK, id, false, lead);
+            umma_commit_w(bar, lead);
+        }
         // log g, beta and the in-chunk prefix Lam (warp 0: two steps per lane, a shuffle scan)
         if (warp == 0) {
             float l2[2], b2[2];
@@ -332,34 +304,48 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
                 p.lam[chk * kL + t] = Lt;
             }
         }
-        __syncthreads();
-        // A, and the decay-weighted Q K^T (i <= t) and K K^T (i < t) as bf16 operands stacked
-        // in one 128-row core-matrix layout: columns 8 j .. + 7 of row t are 16-byte piece
-        // 128 j + t (P) and 128 j + 64 + t (KKm)
-        uint4 *PK = reinterpret_cast<uint4 *>(p.pkm + chk * 2 * kL * kL);
-        for (int e = tid; e < kL * 8; e += 256) {
-            const int t = e & (kL - 1), i0 = 8 * (e >> 6);
-            float kk8[8], qk8[8], a8[8], pv[8], kv8[8];
-            *reinterpret_cast<float4 *>(kk8) = *reinterpret_cast<const float4 *>(kk + t * kP + i0);
-            *reinterpret_cast<float4 *>(kk8 + 4) = *reinterpret_cast<const float4 *>(kk + t * kP + i0 + 4);
-            *reinterpret_cast<float4 *>(qk8) = *reinterpret_cast<const float4 *>(qk + t * kP + i0);
-            *reinterpret_cast<float4 *>(qk8 + 4) = *reinterpret_cast<const float4 *>(qk + t * kP + i0 + 4);
-            const float lt = Lm[t], bb = bt[t];
+        tc_fence_before();
+        ok = !__syncthreads_or(!mbar_wait(bar, phase & 1));
+        ++phase;
+        tc_fence_after();
+        if (!ok) break;
+        // A, and the decay-weighted Q K^T (i <= t) and K K^T (i < t) as bf16 operands stacked in
+        // one 128-row core-matrix layout ([P; KKm]: row t of P, row 64 + t of KKm), straight from
+        // tensor memory: a thread's 16x256b fragment, two columns per 4-byte store (a warp's store
+        // covers one 128-byte core matrix)
+        {
+            float kx[16], qx[16];
+            tmem_ld16x256_x4(tmem + lo16 + 32 * (warp >> 2), kx);
+            tmem_ld16x256_x4(tmem + lo16 + kL + 32 * (warp >> 2), qx);
+            tmem_wait_ld();
+            unsigned char *PK = reinterpret_cast<unsigned char *>(p.pkm + chk * 2 * kL * kL);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = i0 + j;
-                const float ex = i <= t ? expf(lt - Lm[i]) : 0.f;
-                a8[j] = i < t ? bb * kk8[j] * ex : 0.f;
-                pv[j] = qk8[j] * ex;
-                kv8[j] = i < t ? kk8[j] * ex : 0.f;
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int t = fa.row(2 * k2);
+                const float lt = Lm[t], bb = bt[t];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int i0 = fa.col(j, 0);
+                    float e2[2], a2[2], p2[2], m2[2];
+#pragma unroll
+                    for (int k1 = 0; k1 < 2; ++k1) {
+                        const int ii = i0 + k1;
+                        const float kk = kx[4 * j + 2 * k2 + k1], qq = qx[4 * j + 2 * k2 + k1];
+                        e2[k1] = ii <= t ? expf(lt - Lm[ii]) : 0.f;
+                        a2[k1] = ii < t ? bb * kk * e2[k1] : 0.f;
+                        p2[k1] = qq * e2[k1];
+                        m2[k1] = ii < t ? kk * e2[k1] : 0.f;
+                    }
+                    *reinterpret_cast<float2 *>(am + t * kP + i0) = make_float2(a2[0], a2[1]);
+                    *reinterpret_cast<uint32_t *>(PK + cm_off(t, 2 * i0, 2 * kL)) = pack2_bf16(p2[0], p2[1]);
+                    *reinterpret_cast<uint32_t *>(PK + cm_off(kL + t, 2 * i0, 2 * kL)) = pack2_bf16(m2[0], m2[1]);
+                }
             }
-            *reinterpret_cast<float4 *>(am + t * kP + i0) = *reinterpret_cast<const float4 *>(a8);
-            *reinterpret_cast<float4 *>(am + t * kP + i0 + 4) = *reinterpret_cast<const float4 *>(a8 + 4);
-            PK[(e >> 6) * 2 * kL + t] = pack8_bf16(pv);
-            PK[(e >> 6) * 2 * kL + kL + t] = pack8_bf16(kv8);
         }
         if (tid == 32) bulk_wait_read();   // the last unit's store of T diag(beta) has read tcu
+        tc_fence_before();
         __syncthreads();
+        tc_fence_after();
         // T = (I + A)^-1
         invert_unit_lower(am, ts, xs, tid, [] {});
         // T (for the backward), T diag(beta exp Lam) (W's operand) and T diag(beta) (stored for
@@ -393,9 +379,9 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // W -> columns [128, 128 + DK); T diag(beta) leaves by a bulk store
+        // W -> columns [0, DK) (K K^T and Q K^T are dead); T diag(beta) leaves by a bulk store
         if (warp == 0) {
-            umma_gemm_w(tmem + 2 * kL, CmOp{tcw, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, true}, kL,
+            umma_gemm_w(tmem, CmOp{tcw, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, true}, kL,
                         umma_idesc_t(1, kL, DK, false, true), false, lead);
             umma_commit_w(bar, lead);
         }
@@ -415,11 +401,10 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
             // -W in its operand layout: a 4-byte pair of columns per value, a warp's store
             // covering one 128-byte core matrix
             unsigned char *Wg = reinterpret_cast<unsigned char *>(p.wm + chk * kL * DK);
-            const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
 #pragma unroll
             for (int r = 0; r < DK / 64; ++r) {
                 float xw[16];
-                tmem_ld16x256_x4(tmem + lo + 2 * kL + (DK / 2) * (warp >> 2) + 32 * r, xw);
+                tmem_ld16x256_x4(tmem + lo16 + (DK / 2) * (warp >> 2) + 32 * r, xw);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
@@ -441,10 +426,15 @@ __global__ void __launch_bounds__(256, 1) chunk_prep_kernel(ChunkParams p, int u
         if (nKQ > wKQ) mbar_wait(cbKQ, (nKQ - 1) & 1);
     }
     if (tid == 32) bulk_wait_all();   // no store still reads shared memory when the CTA exits
+    if (!ok && warp == 0) {
+        // products still in flight finish before the tensor memory is freed (bounded wait)
+        umma_commit_w(bar, lead);
+        mbar_wait(bar, phase & 1);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 }  // namespace gdn
@@ -807,6 +797,9 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const ChunkFwdMaps &maps
     const size_t sp = PrepSmem(DK).total, ss = SweepSmem(DK).total;
     cudaError_t err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
     if (err != cudaSuccess) return err;
+    // two prep CTAs share an SM: ask for the largest shared-memory carve-out
+    err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(chunk_sweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_prep", 0, s);
@@ -816,7 +809,7 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const ChunkFwdMaps &maps
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    chunk_prep_kernel<E><<<units < sms ? units : sms, 256, sp, s>>>(p, units, maps);   // persistent: one CTA per SM
+    chunk_prep_kernel<E><<<units < 2 * sms ? units : 2 * sms, 256, sp, s>>>(p, units, maps);   // persistent: two CTAs per SM
     timing_mark("chunk_prep", 1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;

@@ -487,10 +487,14 @@ struct GradSmem {
         gehe = s0; wst = s0 + (size_t)2 * kL * kL * 2; mt = wst + (size_t)2 * kL * kL * 2;
         dsl = o; o += (size_t)Dv * DK * 2;                         // dS_L [Dv / 64][64][DK]
         vec = o; o += (6 * kL + 4 * kL + 16 + 12 * kL + 4 * kL) * 4;   // Lam, Lam_{t-1}, exp Lam, E(L,.), beta, f; ab [2][128]; c0 parts; dg parts [4][3][64]; Z column sums [4][64]
-        stg = o; o += (size_t)32 * (DK + 4) * 4;                   // 32 output rows (fp32, padded) for coalesced stores
+        stg = alb(o, 1024);                                        // the unit's decay table E [64][65] fp32; at the group's end
+        {                                                          // dq or dk [64 rows][DK] bf16 in 64-column 128-byte-swizzled boxes
+            const size_t a = (size_t)kL * DK * 2, b2 = (size_t)kL * (kL + 1) * 4;
+            o = stg + (a > b2 ? a : b2);
+        }
         bar = alb(o, 8); o = bar + 5 * 8;                          // MMA; copies of (dY;dU, Delta, dS_L), of S0, of [Q; K]; drain
         tslot = o; o += 16;
-        total = o + 128;
+        total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
     }
 };
@@ -514,7 +518,9 @@ struct GradSmem {
 //   [2 DK, 2 DK + 64)   [Q; K] K^T (M = 128), formed once per (b, chunk, kv head)
 //   [2 DK + 64, + 128)  [dY; dU] Delta^T = [G; H] (M = 128), later [W1; W2] M (M = 128)
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, int groups) {
+__global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, int groups,
+                                                            const __grid_constant__ CUtensorMap tm_dq,
+                                                            const __grid_constant__ CUtensorMap tm_dk) {
     constexpr int DK = 32 * E;
     constexpr int SC = DK / 2;
     static_assert(2 * DK + 128 <= 512, "tensor memory");
@@ -527,11 +533,12 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     const int u_end = (int)((long long)(blockIdx.x + 1) * groups / gridDim.x) * rep;
 
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 128));
+    unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
     const GradSmem L(DK, Dv);
     unsigned char *qk = base + L.qk, *yu = base + L.yu, *dl = base + L.dl, *s0 = base + L.s0, *dsl = base + L.dsl;
     unsigned char *gehe = base + L.gehe, *wst = base + L.wst, *mt = base + L.mt;
-    float *stg = reinterpret_cast<float *>(base + L.stg);
+    unsigned char *stg = base + L.stg;
+    float *Et = reinterpret_cast<float *>(stg);                // E [64][65], see below
     float *Lm = reinterpret_cast<float *>(base + L.vec), *LmP = Lm + kL, *gm = LmP + kL, *eL = gm + kL;
     float *bt = eL + kL, *fv = bt + kL, *abp = fv + kL, *c0p = abp + 4 * kL, *dgp = c0p + 16, *zq = dgp + 12 * kL;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar), *cbA = bar + 1, *cbS = bar + 2, *cbQ = bar + 3, *mX = bar + 4;
@@ -638,10 +645,17 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             for (int s = 0; s < kMaxSplit; ++s) db += s < nsplit ? vdb[s] : 0.f;
             if (in) static_cast<__nv_bfloat16 *>(p.dbeta)[(rowbase + tid) * Hv + h] = __float2bfloat16_rn(db);
         }
+        if (tid == 32) bulk_wait_read();                    // the last group's dq, dk stores have read stg
         __syncthreads();
         if (tid < kL) {
             LmP[tid] = tid > 0 ? Lm[tid - 1] : 0.f;
             eL[tid] = expf(Lm[kL - 1] - Lm[tid]);
+        }
+        // the unit's decay weights E(s, i) = exp(Lam_s - Lam_i) <= 1 for i <= s (0 above the
+        // diagonal), in the output tile (not used until this unit's dq, dk leave)
+        for (int e = tid; e < kL * kL; e += 256) {
+            const int s2 = e >> 6, i = e & (kL - 1);
+            Et[s2 * (kL + 1) + i] = i <= s2 ? expf(Lm[s2] - Lm[i]) : 0.f;
         }
         // ---- this unit's operands (every thread reads S0 and dS_L, and [Q; K] rows in pass 1)
         {
@@ -702,13 +716,13 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                 tmem_ld32f(tS1 + lane_off + half * 32, a);
                 tmem_ld32f(tS2 + lane_off + half * 32, g2);
                 tmem_wait_ld();
-                const float ls = Lm[s];
+                const float *Es = Et + s * (kL + 1) + half * 32;
                 float ge[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int col = half * 32 + i;
                     const bool keep = upper ? col < s : col <= s;
-                    ge[i] = keep ? g2[i] * expf(ls - Lm[col]) : 0.f;
+                    ge[i] = keep ? g2[i] * Es[i] : 0.f;
                     a[i] *= g2[i];
                 }
 #pragma unroll
@@ -767,7 +781,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                 const int t = e & (kL - 1), i0 = 8 * (e >> 6);
                 float m8[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) m8[j] = i0 + j < t ? expf(LmP[t] - Lm[i0 + j]) : 0.f;
+                for (int j = 0; j < 8; ++j) m8[j] = i0 + j < t ? Et[(t - 1) * (kL + 1) + i0 + j] : 0.f;
                 *reinterpret_cast<uint4 *>(mt + cm_off(t, 2 * i0, kL)) = pack8(m8);
             }
         }
@@ -810,29 +824,27 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             float z[32];
             tmem_ld32f(tS2 + lane_off + half * 32, z);
             tmem_wait_ld();
-            const float ls = Lm[s];
+            const float *Es = Et + s * (kL + 1) + half * 32;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int t = half * 32 + i;
-                z[i] = s >= t ? z[i] * expf(ls - Lm[t]) : 0.f;
-            }
+            for (int i = 0; i < 32; ++i) z[i] *= Es[i];   // E(s, t) = 0 for t > s
             zq[quarter * kL + half * 32 + lane] = transpose_reduce<32>(z, lane);
         }
         {
             // ---- dg_t: the sums over the chunk's steps, a quarter of the steps per thread
+            // s2 = sum_{j < t} E(t-1, j) f_j, s3 = exp(Lam_{t-1}) sum_{j >= t} E(j, t) (a_j + b_j)
             const int t = tid & (kL - 1), part = tid >> 6;
-            const float lt = Lm[t], lp = LmP[t];
+            const float *Ep = Et + (t > 0 ? t - 1 : 0) * (kL + 1);
             float s2 = 0.f, s3 = 0.f;
             for (int j = 16 * part; j < 16 * part + 16; ++j) {
                 if (j < t) {
-                    s2 = fmaf(expf(lp - Lm[j]), fv[j], s2);
+                    s2 = fmaf(Ep[j], fv[j], s2);
                 } else {
                     const float ab = abp[j] + abp[2 * kL + j] + abp[kL + j] + abp[3 * kL + j];
-                    s3 = fmaf(expf(lp + Lm[j] - lt), ab, s3);
+                    s3 = fmaf(Et[j * (kL + 1) + t], ab, s3);
                 }
             }
             dgp[(2 * part + 0) * kL + t] = s2;
-            dgp[(2 * part + 1) * kL + t] = s3;
+            dgp[(2 * part + 1) * kL + t] = expf(LmP[t]) * s3;
         }
         __syncthreads();
         if (tid < kL && tid < len) {
@@ -870,35 +882,33 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
-            // ---- dq (rows 0-63) and dk (rows 64-127) of the group, from RS, as bf16. A row
-            // quarter at a time passes through a padded shared-memory tile, so that each warp
-            // access covers 256 contiguous bytes of one row.
-            __nv_bfloat16 *outq = static_cast<__nv_bfloat16 *>(p.dq), *outk = static_cast<__nv_bfloat16 *>(p.dk);
-            const size_t hk = (size_t)(h / rep);
-            constexpr int NE = DK / 32;                     // float4 of a row quarter per thread
+            // ---- dq (rows 0-63) and then dk (rows 64-127) of the group, from RS, as bf16: each
+            // staged in 64-column boxes in the 128-byte swizzle (row r at r * 128, 16-byte chunk j at
+            // j ^ (r % 8)) and written by TMA stores (rows past T are clipped by them)
+            const int hk = h / rep;
             float x[SC];
 #pragma unroll
             for (int j = 0; j < SC / 32; ++j) tmem_ld32f(tRS + lane_off + half * SC + 32 * j, x + 32 * j);
             tmem_wait_ld();
-            constexpr int RSt = DK + 4;                     // padded row stride (floats)
-            for (int q = 0; q < 4; ++q) {
-                if (quarter == q) {
-                    float *row = stg + lane * RSt + half * SC;
+            const int r = 32 * quarter + lane, t = r & (kL - 1);
+            for (int pass = 0; pass < 2; ++pass) {
+                if ((quarter >> 1) == pass) {
 #pragma unroll
-                    for (int j = 0; j < SC / 4; ++j)
-                        *reinterpret_cast<float4 *>(row + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                    for (int j = 0; j < SC / 8; ++j) {
+                        const int col = half * SC + 8 * j;
+                        *reinterpret_cast<uint4 *>(stg + (col >> 6) * (kL * 128) + t * 128 +
+                                                   ((((col & 63) >> 3) ^ (t & 7)) << 4)) = pack8(x + 8 * j);
+                    }
                 }
+                fence_proxy_async();
                 __syncthreads();
-#pragma unroll
-                for (int i = 0; i < NE; ++i) {
-                    const int e = tid + 256 * i, rr = e / (DK / 4), c4 = e - rr * (DK / 4), r2 = 32 * q + rr, s = r2 & (kL - 1);
-                    if (s >= len) continue;
-                    const float4 v4 = *reinterpret_cast<const float4 *>(stg + rr * RSt + 4 * c4);
-                    __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>((r2 >= kL ? outk : outq) + ((rowbase + s) * Hk + hk) * DK + 4 * c4);
-                    o2[0] = __floats2bfloat162_rn(v4.x, v4.y);
-                    o2[1] = __floats2bfloat162_rn(v4.z, v4.w);
+                if (tid == 32) {
+                    for (int bx = 0; bx < DK / 64; ++bx)
+                        tma_store_4d(pass ? &tm_dk : &tm_dq, stg + bx * (kL * 128), 64 * bx, hk, t0, b);
+                    bulk_commit();
+                    if (pass == 0) bulk_wait_read();        // dk reuses the tile
                 }
-                __syncthreads();
+                if (pass == 0) __syncthreads();
             }
         }
         tc_fence_before();
@@ -928,7 +938,8 @@ size_t chunk_grad_smem(int Dk, int Dv) { return GradSmem(Dk, Dv).total; }
 
 template <int E>
 static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
-                                      const CUtensorMap &tm_rs, cudaStream_t s) {
+                                      const CUtensorMap &tm_rs, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk,
+                                      cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sd = DSweepSmem(DK).total, sg = GradSmem(DK, p.Dv).total;
     cudaError_t err = cudaFuncSetAttribute(chunk_dsweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd);
@@ -948,17 +959,18 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
     const int grid = groups < sms ? groups : sms;           // persistent: one CTA per SM
-    chunk_grad_kernel<E><<<grid, 256, sg, s>>>(p, groups);
+    chunk_grad_kernel<E><<<grid, 256, sg, s>>>(p, groups, tm_dq, tm_dk);
     timing_mark("chunk_grad", 1, s);
     return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
-                             const CUtensorMap &tm_rs, int Dk, cudaStream_t s) {
+                             const CUtensorMap &tm_rs, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk, int Dk,
+                             cudaStream_t s) {
     switch (Dk) {
-        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, tm_dy, tm_rs, s);
-        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, tm_dy, tm_rs, s);
-        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_rs, s);
+        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, tm_dy, tm_rs, tm_dq, tm_dk, s);
+        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, tm_dy, tm_rs, tm_dq, tm_dk, s);
+        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_rs, tm_dq, tm_dk, s);
         default: return cudaErrorInvalidValue;
     }
 }
