@@ -237,13 +237,14 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(ChunkParams p, int u
     unsigned phase = 0;
     bool ok = true;
     uint32_t tmem = 0;
-    // the first unit's g and beta go out before anything else, its K and Q once the barriers
-    // are initialised
-    if (u_begin < u_end && warp == 0) fetch_gb(unit_of(u_begin));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     tmem = *tslot;
+    griddep_wait();                                           // the previous kernel's writes are visible
+    griddep_launch();
+    // the first unit's g, beta, K and Q
+    if (u_begin < u_end && warp == 0) fetch_gb(unit_of(u_begin));
     if (u_begin < u_end) fetch_kq(unit_of(u_begin));
 
     const uint32_t lo16 = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's M = 64 rows in tensor memory
@@ -546,6 +547,8 @@ __global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, cons
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tSg = tmem, tD = tmem + DK, tQK = tmem + DK + 64, tPD = tmem + DK + 128;
+    griddep_wait();                                           // the previous kernel's writes are visible
+    griddep_launch();
     if (tid == 32) {
         issue_w(0);
         if (NC > 1) issue_w(1);
@@ -809,14 +812,14 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const ChunkFwdMaps &maps
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    chunk_prep_kernel<E><<<units < 2 * sms ? units : 2 * sms, 256, sp, s>>>(p, units, maps);   // persistent: two CTAs per SM
+    // persistent: two CTAs per SM
+    err = launch_pdl(chunk_prep_kernel<E>, dim3(units < 2 * sms ? units : 2 * sms), dim3(256), sp, s, p, units, maps);
     timing_mark("chunk_prep", 1, s);
-    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     timing_mark("chunk_sweep", 0, s);
-    chunk_sweep_kernel<E><<<dim3(p.Dv / kL, p.Hv, p.B), 256, ss, s>>>(p, maps);
+    err = launch_pdl(chunk_sweep_kernel<E>, dim3(p.Dv / kL, p.Hv, p.B), dim3(256), ss, s, p, maps);
     timing_mark("chunk_sweep", 1, s);
-    return cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s) {

@@ -79,7 +79,7 @@ struct DSweepSmem {
         yds = o; o += (size_t)2 * kL * kL * 2;       // [diag(exp Lam) dY; diag(exp Lam) dU] [128][64 v] (read MN-major)
         rsm = alb(o, 1024); o = rsm + (size_t)2 * kL * 128;   // v - u block, fp32: two [64 t][32 v] boxes in the 128-byte swizzle
         lms = o; o += (size_t)2 * kL * 4;        // Lam, two buffers
-        shl = o; o += (size_t)2 * kL * DK * 2;   // dS as [high; low] bf16 parts [128][DK] (rows 0-63 high, 64-127 dS - high)
+        shl = o; o += (size_t)2 * kL * DK * 2;   // dS as bf16 parts: high [64][DK], then low (dS - high) [64][DK]
         rhs = o; o += (size_t)kL * kL * 2;   // diag(E_L) K dS^T + P^T dY [64 t][64 v]
         dls = o; o += (size_t)kL * kL * 2;   // Delta block [64 t][64 v], for the gradient kernel
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
@@ -100,8 +100,8 @@ struct DSweepSmem {
 // memory, M = 64 layout: row r in lane r % 16 + 32 (r / 16)):
 //   [0, DK)              the chunk's part of the carry, [e^Lam dY; e^Lam dU]^T [Q; K]; the
 //                        next chunk's dS = exp(Lam_L) dS + this
-//   [DK, DK + 128)       K [dS_high; dS_low]^T (one N = 128 product: chunk row t, value column
-//                        of the high part, then of the low part); then dD in the first 64
+//   [DK, DK + 64)        K dS_high^T + K dS_low^T (chunk row t, value column; the two parts
+//                        accumulate in fp32); then dD
 //   [DK + 128, DK + 192) P^T dY
 // Warp 0 issues the products (from one elected lane, the warp converged); thread 32 issues the
 // copies and the stores; every thread converts (all 32 lanes of a warp hold fragment values).
@@ -172,6 +172,8 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tS = tmem, tX = tmem + DK, tP = tmem + DK + 128;
+    griddep_wait();                                           // the previous kernel's writes are visible
+    griddep_launch();
 
     // this thread's fragment of dS (rows fs.row(k), columns fs.col(j, k)), from dS_T
     const M64Frag fs(warp, lane, DK);
@@ -229,6 +231,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         const int buf = (p.NC - 1 - c) & 1;
         unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;   // [dY; dU] of this chunk
         const float *lmb = lms + buf * kL;                 // Lam of this chunk
+        if (tid == 32) bulk_wait_read();                    // the last chunk's stores have read their tiles
         {
             // this chunk's dY, v - u and Lam have landed (every thread waits: every thread reads them)
             const bool w = mbar_wait(cbY, wY & 1);
@@ -258,7 +261,48 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
                 for (int e = 0; e < 16; ++e) dS[16 * i + e] = fmaf(decay_next, dS[16 * i + e], x[e]);
             }
         }
-        // diag(exp Lam) dY: rows 0-63 of the dS update's operand (the dU rows follow below)
+        // ---- dS as operands: a bf16 high part and a bf16 low part (dS - high), each [64][DK]; the
+        // high part also leaves for the gradient kernel (a bulk store below)
+        {
+#pragma unroll
+            for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int row = fs.row(2 * k2), col = fs.col(j, 0);
+                    const float x0 = dS[4 * j + 2 * k2], x1 = dS[4 * j + 2 * k2 + 1];
+                    const uint32_t hu = pack2_bf16(x0, x1);
+                    const float h0 = __uint_as_float(hu << 16), h1 = __uint_as_float(hu & 0xffff0000u);
+                    const uint32_t o = cm_off(row, 2 * col, kL);
+                    *reinterpret_cast<uint32_t *>(shl + o) = hu;
+                    *reinterpret_cast<uint32_t *>(shl + kL * DK * 2 + o) = pack2_bf16(x0 - h0, x1 - h1);
+                }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        {
+            // [Q; K] and [P; KKm] have landed (warp 0)
+            bool w = true;
+            if (warp == 0) w = mbar_wait(cbA, cph & 1) && mbar_wait(cbK, cph & 1);
+            ok = !__syncthreads_or(!w);
+        }
+        tc_fence_after();
+        if (!ok) break;
+        if (tid == 32) {
+            bulk_store(p.ws_dsl + (chk * nsplit + split) * kL * DK, shl, kL * DK * 2);   // dS_L (high part) for the gradient kernel
+            bulk_commit();
+        }
+        if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
+        // ---- K dS_high^T + K dS_low^T (K: rows 64-127 of [Q; K]), P^T dY (P: rows 0-63 of [P; KKm])
+        if (warp == 0) {
+            constexpr uint32_t idX = umma_idesc(1, kL, kL);
+            constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
+            umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl, kL, 0, 0, false}, DK, idX, false, lead);
+            umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl + kL * DK * 2, kL, 0, 0, false}, DK, idX, true, lead);
+            umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false, lead);
+            umma_commit_w(bar, lead);
+        }
+        // diag(exp Lam) dY while the products run: rows 0-63 of the dS update's operand (the dU
+        // rows follow below)
         for (int e = tid; e < kL * kL / 8; e += 256) {
             const int t = e & (kL - 1);
             const uint32_t o = cm_off(t, 16 * (e >> 6), 2 * kL);
@@ -269,45 +313,6 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
             for (int i = 0; i < 8; ++i) x8[i] *= gt;
             *reinterpret_cast<uint4 *>(yds + o) = pack8(x8);
         }
-        // ---- dS as operands (high and low bf16 parts, [hi; lo] [128][DK]); the high part also
-        // stored for the gradient kernel ([64][DK] operand layout: a warp's store covers one
-        // 128-byte core matrix)
-        {
-            unsigned char *dsl_g = reinterpret_cast<unsigned char *>(p.ws_dsl + (chk * nsplit + split) * kL * DK);
-#pragma unroll
-            for (int j = 0; j < NS / 4; ++j)
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int row = fs.row(2 * k2), col = fs.col(j, 0);
-                    const float x0 = dS[4 * j + 2 * k2], x1 = dS[4 * j + 2 * k2 + 1];
-                    const uint32_t hu = pack2_bf16(x0, x1);
-                    const float h0 = __uint_as_float(hu << 16), h1 = __uint_as_float(hu & 0xffff0000u);
-                    *reinterpret_cast<uint32_t *>(shl + cm_off(row, 2 * col, 2 * kL)) = hu;
-                    *reinterpret_cast<uint32_t *>(shl + cm_off(kL + row, 2 * col, 2 * kL)) = pack2_bf16(x0 - h0, x1 - h1);
-                    *reinterpret_cast<uint32_t *>(dsl_g + cm_off(row, 2 * col, kL)) = hu;
-                }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        {
-            // the last chunk's stores have read [dY; dU], Delta and dv (thread 32); [Q; K] and
-            // [P; KKm] have landed (warp 0)
-            bool w = true;
-            if (tid == 32) bulk_wait_read();
-            if (warp == 0) w = mbar_wait(cbA, cph & 1) && mbar_wait(cbK, cph & 1);
-            ok = !__syncthreads_or(!w);
-        }
-        tc_fence_after();
-        if (!ok) break;
-        if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
-        // ---- K [dS_high; dS_low]^T (N = 128; K: rows 64-127 of [Q; K]), P^T dY (P: rows 0-63 of [P; KKm])
-        if (warp == 0) {
-            constexpr uint32_t idX = umma_idesc_t(1, kL, 2 * kL, false, false);
-            constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
-            umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl, 2 * kL, 0, 0, false}, DK, idX, false, lead);
-            umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false, lead);
-            umma_commit_w(bar, lead);
-        }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
         ++ph;
         tc_fence_after();
@@ -315,9 +320,8 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
         // ---- rhs = diag(E_L) K dS^T + P^T dY as an operand; Delta = beta (v - u) for the gradient
         // kernel; f partial = beta_t (v_t - u_t) . (dS k_t)
         {
-            float xh[16], xl[16], pp[16];
+            float xh[16], pp[16];
             tmem_ld16x256_x4(tX + lane16 + 32 * hw, xh);
-            tmem_ld16x256_x4(tX + lane16 + kL + 32 * hw, xl);
             tmem_ld16x256_x4(tP + lane16 + 32 * hw, pp);
             tmem_wait_ld();
             const float ela = eL[ta], elb = eL[tb], ba = bt[ta], bb = bt[tb];
@@ -325,8 +329,7 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float2 ra = rsa[j], rb = rsb[j];
-                const float x0 = xh[4 * j] + xl[4 * j], x1 = xh[4 * j + 1] + xl[4 * j + 1];
-                const float x2 = xh[4 * j + 2] + xl[4 * j + 2], x3 = xh[4 * j + 3] + xl[4 * j + 3];
+                const float x0 = xh[4 * j], x1 = xh[4 * j + 1], x2 = xh[4 * j + 2], x3 = xh[4 * j + 3];
                 fa = fmaf(ra.x, x0, fmaf(ra.y, x1, fa));
                 fb = fmaf(rb.x, x2, fmaf(rb.y, x3, fb));
                 const int col = fd.col(j, 0);
@@ -614,6 +617,8 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tR1 = tmem, tRS = tmem + DK, tS1 = tmem + 2 * DK, tS2 = tmem + 2 * DK + 64;
+    griddep_wait();                                           // the previous kernel's writes are visible
+    griddep_launch();
 
     if (tid == 32 && u_begin < u_end) {
         copy_q(u_begin);
@@ -947,9 +952,8 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     err = cudaFuncSetAttribute(chunk_grad_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_dsweep", 0, s);
-    chunk_dsweep_kernel<E><<<dim3(p.nsplit, p.Hv, p.B), 256, sd, s>>>(p, tm_dv, tm_dy, tm_rs);
+    err = launch_pdl(chunk_dsweep_kernel<E>, dim3(p.nsplit, p.Hv, p.B), dim3(256), sd, s, p, tm_dv, tm_dy, tm_rs);
     timing_mark("chunk_dsweep", 1, s);
-    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     timing_mark("chunk_grad", 0, s);
     const int groups = p.NC * p.Hk * p.B;                   // (b, chunk, kv head)
@@ -959,9 +963,9 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
     const int grid = groups < sms ? groups : sms;           // persistent: one CTA per SM
-    chunk_grad_kernel<E><<<grid, 256, sg, s>>>(p, groups, tm_dq, tm_dk);
+    err = launch_pdl(chunk_grad_kernel<E>, dim3(grid), dim3(256), sg, s, p, groups, tm_dq, tm_dk);
     timing_mark("chunk_grad", 1, s);
-    return cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
