@@ -183,3 +183,141 @@ def backward(q, k, v, g, beta, dy, S0=None, dS_T=None, chunk=64, rnd=None):
                     dg[b, t0:t1, h] = dgc
                 dS0[b, h] = dS
     return {"dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": dbeta, "dS0": dS0}
+
+
+# ------------------------------------------------------------------ segment scan over chunks
+# The state recurrence across chunks is affine: S_L = S0 M + S_L(S0 = 0), with the chunk's state
+# map M = exp(Lam_L) I - W^T diag(E(L, .)) K  [Dk, Dk],  W = T diag(beta exp Lam) K.
+# A run of whole chunks (a segment) composes its chunks' maps. So the forward over NC chunks can
+# run as (1) every segment from a zero start state (its end state B_j) and its composed map M_j,
+# all segments independently; (2) a scan over segments, S_start(j + 1) = S_start(j) M_j + B_j;
+# (3) every segment again from its true start state, independently. The VJP is linear in the
+# end cotangent with the transposed map: dS_start = dS_end M^T + (the part from the segment's dy,
+# D_j, its start cotangent from a zero end cotangent), so the backward scans in reverse,
+# dS_end(j) = dS_end(j + 1) M_{j+1}^T + D_{j+1}, from dS_end(last) = dS_T.
+
+def chunk_state_map(K, g, beta):
+    """The chunk's state map M [Dk, Dk]: S_L = S0 M + S_L(S0 = 0)."""
+    L = K.shape[0]
+    Lam, Dm = _decay(np.log(g))
+    idx = np.arange(1, L + 1)
+    Dloc = Dm[np.ix_(idx, idx)]
+    E_strict = np.exp(np.where(np.tril(np.ones((L, L)), -1) > 0, Dloc, -np.inf))
+    A = beta[:, None] * (K @ K.T) * E_strict
+    T = np.linalg.inv(np.eye(L) + A)
+    gam = np.exp(Lam[1:])
+    eL = np.exp(Lam[L] - Lam[1:])
+    W = T @ ((beta * gam)[:, None] * K)
+    return np.exp(Lam[L]) * np.eye(K.shape[1]) - W.T @ (eL[:, None] * K)
+
+
+def segment_bounds(NC, segments):
+    """Chunk index ranges [c0, c1) of `segments` runs of whole chunks (as even as possible)."""
+    edges = [round(j * NC / segments) for j in range(segments + 1)]
+    return [(edges[j], edges[j + 1]) for j in range(segments) if edges[j + 1] > edges[j]]
+
+
+def forward_segments(q, k, v, g, beta, S0=None, chunk=64, segments=2):
+    """The chunkwise forward as a scan over segments of chunks (see above). Returns y, S_T, ckpt."""
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    rep = Hv // Hk
+    NC = -(-T // chunk)
+    segs = segment_bounds(NC, segments)
+    y = np.zeros((B, T, Hv, Dv))
+    S_T = np.zeros((B, Hv, Dv, Dk))
+    ckpt = np.zeros((B, Hv, NC, Dv, Dk))
+
+    def run(b, h, S, c0, c1, out):
+        hk = h // rep
+        for c in range(c0, c1):
+            t0, t1 = c * chunk, min(T, (c + 1) * chunk)
+            if out:
+                ckpt[b, h, c] = S
+            Y, S, _, _, _ = chunk_forward(S, k[b, t0:t1, hk], q[b, t0:t1, hk], v[b, t0:t1, h], g[b, t0:t1, h],
+                                          beta[b, t0:t1, h])
+            if out:
+                y[b, t0:t1, h] = Y
+        return S
+
+    for b in range(B):
+        for h in range(Hv):
+            hk = h // rep
+            # (1) each segment from a zero start, and its composed map
+            ends, maps = [], []
+            for c0, c1 in segs:
+                ends.append(run(b, h, np.zeros((Dv, Dk)), c0, c1, False))
+                M = np.eye(Dk)
+                for c in range(c0, c1):
+                    t0, t1 = c * chunk, min(T, (c + 1) * chunk)
+                    M = M @ chunk_state_map(k[b, t0:t1, hk], g[b, t0:t1, h], beta[b, t0:t1, h])
+                maps.append(M)
+            # (2) the scan over segments
+            S = np.zeros((Dv, Dk)) if S0 is None else np.array(S0[b, h], dtype=np.float64)
+            starts = []
+            for Bj, Mj in zip(ends, maps):
+                starts.append(S)
+                S = S @ Mj + Bj
+            S_T[b, h] = S
+            # (3) each segment from its start state
+            for (c0, c1), Sj in zip(segs, starts):
+                run(b, h, Sj, c0, c1, True)
+    return {"y": y, "S_T": S_T, "ckpt": ckpt}
+
+
+def backward_segments(q, k, v, g, beta, dy, S0=None, dS_T=None, chunk=64, segments=2):
+    """The chunkwise VJP as a reverse scan over segments of chunks (see above). Returns dq, dk,
+    dv, dg, dbeta, dS0."""
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    rep = Hv // Hk
+    NC = -(-T // chunk)
+    segs = segment_bounds(NC, segments)
+    f = forward(q, k, v, g, beta, S0, chunk)
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    dg = np.zeros(g.shape)
+    dbeta = np.zeros(beta.shape)
+    dS0 = np.zeros((B, Hv, Dv, Dk))
+
+    def rerun(b, h, dS, c0, c1, out):
+        hk = h // rep
+        for c in reversed(range(c0, c1)):
+            t0, t1 = c * chunk, min(T, (c + 1) * chunk)
+            Kc, Qc, Vc = k[b, t0:t1, hk], q[b, t0:t1, hk], v[b, t0:t1, h]
+            gc, bc = g[b, t0:t1, h], beta[b, t0:t1, h]
+            S_start = f["ckpt"][b, h, c]
+            _, _, _, _, ctx = chunk_forward(S_start, Kc, Qc, Vc, gc, bc)
+            dQc, dKc, dVc, dbc, dgc, dS = chunk_backward(S_start, Kc, Qc, Vc, gc, bc, dy[b, t0:t1, h], dS, ctx)
+            if out:
+                dq[b, t0:t1, hk] += dQc
+                dk[b, t0:t1, hk] += dKc
+                dv[b, t0:t1, h] = dVc
+                dbeta[b, t0:t1, h] = dbc
+                dg[b, t0:t1, h] = dgc
+        return dS
+
+    for b in range(B):
+        for hk in range(Hk):
+            for h in range(hk * rep, (hk + 1) * rep):
+                # (1) each segment from a zero end cotangent, and its composed map
+                locs, maps = [], []
+                for c0, c1 in segs:
+                    locs.append(rerun(b, h, np.zeros((Dv, Dk)), c0, c1, False))
+                    M = np.eye(Dk)
+                    for c in range(c0, c1):
+                        t0, t1 = c * chunk, min(T, (c + 1) * chunk)
+                        M = M @ chunk_state_map(k[b, t0:t1, hk], g[b, t0:t1, h], beta[b, t0:t1, h])
+                    maps.append(M)
+                # (2) the reverse scan over segments
+                dS = np.zeros((Dv, Dk)) if dS_T is None else np.array(dS_T[b, h], dtype=np.float64)
+                ends = [None] * len(segs)
+                for j in reversed(range(len(segs))):
+                    ends[j] = dS
+                    dS = dS @ maps[j].T + locs[j]
+                dS0[b, h] = dS
+                # (3) each segment from its end cotangent
+                for (c0, c1), dSj in zip(segs, ends):
+                    rerun(b, h, dSj, c0, c1, True)
+    return {"dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": dbeta, "dS0": dS0}

@@ -80,3 +80,33 @@ def test_low_precision_operands_meet_the_bf16_bound(decay, name, rnd, bound):
     assert all(e <= 5e-3 for e in errs.values()), (name, decay, errs)
     raw = {n: oracle.rel_l2(bc[n], bo[n]) for n in bo}
     assert all(e <= bound for e in raw.values()), (name, decay, raw)
+
+
+def test_chunk_state_map_is_the_affine_part():
+    """S_L(S0) - S_L(0) = S0 M for the chunk's state map M, on a random start state (a wrong
+    sign, decay or transposition in M fails it)."""
+    w = gs.Workload("map", 1, 48, 1, 1, 16, 12, "f32", "half", True, False, 48)
+    a, _, S0, _ = _run(w)
+    q, k, v, g, beta = a
+    K, Q, V, gg, bb = k[0, :, 0], q[0, :, 0], v[0, :, 0], g[0, :, 0], beta[0, :, 0]
+    _, SL, _, _, _ = CF.chunk_forward(S0[0, 0], K, Q, V, gg, bb)
+    _, SL0, _, _, _ = CF.chunk_forward(np.zeros_like(S0[0, 0]), K, Q, V, gg, bb)
+    M = CF.chunk_state_map(K, gg, bb)
+    assert np.allclose(SL - SL0, S0[0, 0] @ M, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("segments", [1, 2, 3, 5])
+@pytest.mark.parametrize("decay", ["weak", "strong"])
+def test_segment_scan_is_the_recurrence(segments, decay):
+    """The forward and the VJP as scans over segments of chunks (the sequence-parallel form)
+    agree with the sequential oracle to rounding, on a ragged GQA shape with a start state and a
+    final-state cotangent."""
+    w = gs.Workload("seg", 1, 86, 1, 2, 12, 10, "f32", decay, True, True, 16)
+    a, dy, S0, dS = _run(w)
+    fo = oracle.fwd(*a, S0, chunk=16)
+    bo = oracle.bwd(*a, dy, S0, dS, chunk=16)
+    fs = CF.forward_segments(*a, S0, chunk=16, segments=segments)
+    bs = CF.backward_segments(*a, dy, S0, dS, chunk=16, segments=segments)
+    errs = {n: oracle.rel_l2(fs[n], fo[n]) for n in ("y", "S_T", "ckpt")}
+    errs.update({n: oracle.rel_l2(bs[n], bo[n]) for n in bo})
+    assert all(e <= 1e-11 for e in errs.values()), errs
