@@ -1,80 +1,124 @@
-"""Host-side check of the sweeps' store order (chunk_sweep_kernel, chunk_dsweep_kernel).
+"""Host-side model of the chunk kernels' store order: no shared-memory tile is rewritten while a
+bulk or TMA store that reads it may still be reading.
 
-Per chunk the sweep's thread 0 commits two groups of bulk stores: the chunk-start state (the
-bf16 operand `sop` and the fp32 checkpoint tile `ckst`), and, while the chunk's first product
-runs, the previous chunk's y and v - u (staging tiles `ysg`, `rsg`). Its waits: at the top of a
-chunk, all groups but the newest have read their tiles (all of them for the first two chunks);
-before the state stores, all groups; before the epilogue after the last chunk, all groups.
-
-This mirrors that order and checks that no staging tile is rewritten while a committed store may
-still read it, for one chunk and several; a control drops the wait before the last epilogue."""
+Bulk and TMA stores are grouped per issuing thread (`cp.async.bulk.commit_group`); a thread's
+`cp.async.bulk.wait_group.read N` returns once all but its N newest groups have read their
+sources. Each kernel issues its stores from fixed threads; this mirrors, per kernel, which
+thread commits which tiles and where it waits, and checks every rewrite of a tile (by any
+thread, after the block barrier that follows the wait) against the groups still reading it.
+The sequences are written by hand from the kernels' code (chunk_prep_kernel,
+chunk_sweep_kernel, chunk_dsweep_kernel, chunk_grad_kernel) and must be kept in step with it;
+each kernel has a control that drops one wait and must fail."""
 import pytest
 
-from test_prep_u_slots import Ring
+
+class Stores:
+    """The bulk groups of the store-issuing threads: lists of tile sets, oldest first."""
+
+    def __init__(self):
+        self.groups = {}
+
+    def commit(self, thread, tiles):
+        self.groups.setdefault(thread, []).append(set(tiles))
+
+    def wait_read(self, thread, but=0):
+        g = self.groups.get(thread, [])
+        self.groups[thread] = g[len(g) - but:] if but else []
+
+    def write(self, tiles, what):
+        busy = set().union(*[t for g in self.groups.values() for t in g]) if self.groups else set()
+        assert not (busy & set(tiles)), f"{what} rewritten while a store still reads it"
 
 
-def run_sweep(NC, final_wait=True):
-    ring = Ring()
-
-    def write(tiles, what):
-        assert not (ring.reading() & tiles), f"{what} rewritten while a store still reads it"
-
-    def epilogue(cc):
-        write({"ysg", "rsg"}, f"y / v - u staging of chunk {cc}")
-        ring.groups.append({"ysg", "rsg"})
-
+def sweep(NC, drop=None):
+    """chunk_sweep_kernel: thread 32 stores the bf16 state (sop) per chunk; thread 128 stores y and
+    v - u (ysg, rsg) of the previous chunk; both wait at the top of each chunk, thread 128 again
+    before the last epilogue."""
+    st = Stores()
     for c in range(NC):
-        ring.wait_read_but(1 if c >= 2 else 0)
-        write({"sop", "ckst"}, f"state staging of chunk {c}")
-        ring.wait_read_but(0)
-        ring.groups.append({"sop", "ckst"})
+        if drop != "top32":
+            st.wait_read(32)
+        if drop != "top128":
+            st.wait_read(128)
+        st.write({"sop"}, f"state operand of chunk {c}")
+        st.commit(32, {"sop"})
         if c > 0:
-            epilogue(c - 1)
-    if final_wait:
-        ring.wait_read_but(0)
-    epilogue(NC - 1)
+            st.write({"ysg", "rsg"}, f"y / v - u staging of chunk {c - 1}")
+            st.commit(128, {"ysg", "rsg"})
+    if drop != "final":
+        st.wait_read(128)
+    st.write({"ysg", "rsg"}, f"y / v - u staging of chunk {NC - 1}")
+    st.commit(128, {"ysg", "rsg"})
+
+
+def dsweep(NC, drop=None):
+    """chunk_dsweep_kernel: thread 32 stores dS_L (the high tile of shl) after the first products'
+    barrier, and [dY; dU], Delta and dv at the chunk's end; it waits at the top of each chunk."""
+    st = Stores()
+    for c in reversed(range(NC)):
+        buf = (NC - 1 - c) & 1
+        if drop != "top":
+            st.wait_read(32)
+        st.write({"shl"}, f"dS operands of chunk {c}")
+        st.commit(32, {"shl"})
+        st.write({f"ydu{buf}", "dls", "dvs", "yds"}, f"dU rows, Delta and dv of chunk {c}")
+        st.commit(32, {f"ydu{buf}", "dls", "dvs"})
+
+
+def grad(groups, rep, drop=None):
+    """chunk_grad_kernel: per unit the decay table is written to stg; with the group's last head,
+    thread 32 stores dq from stg, waits for that store's read, then stores dk from stg; it waits
+    again at the next unit's top before the table is rewritten."""
+    st = Stores()
+    for g in range(groups):
+        for hh in range(rep):
+            if drop != "top":
+                st.wait_read(32)
+            st.write({"stg"}, f"decay table of unit {g * rep + hh}")
+            if hh == rep - 1:
+                st.write({"stg"}, f"dq tile of group {g}")
+                st.commit(32, {"stg"})
+                if drop != "between":
+                    st.wait_read(32)
+                st.write({"stg"}, f"dk tile of group {g}")
+                st.commit(32, {"stg"})
+
+
+def prep(units, rep, drop=None):
+    """chunk_prep_kernel: thread 32 stores [Q; K] from kc, qc at a group's first unit and T diag(beta)
+    from tcu per unit; it waits before the inversion (tcu is rewritten after it; the wait also
+    covers the [Q; K] stores of the same unit) and, when the next unit starts another group,
+    again before K and Q are fetched into kc, qc."""
+    st = Stores()
+    for u in range(units):
+        if u % rep == 0:
+            st.commit(32, {"kc", "qc"})
+        if drop != "tcu":
+            st.wait_read(32)
+        st.write({"tcu"}, f"T diag(beta) of unit {u}")
+        st.commit(32, {"tcu"})
+        if u + 1 < units and (u + 1) % rep == 0:
+            if drop != "kq":
+                st.wait_read(32)
+            st.write({"kc", "qc"}, f"K and Q of unit {u + 1}")
 
 
 @pytest.mark.parametrize("NC", [1, 2, 3, 8, 32])
-def test_staging_tiles_are_never_rewritten_in_flight(NC):
-    run_sweep(NC)
+def test_sweeps_never_rewrite_a_tile_in_flight(NC):
+    sweep(NC)
+    dsweep(NC)
 
 
-@pytest.mark.parametrize("NC", [2, 5])
-def test_missing_wait_before_the_last_epilogue_is_caught(NC):
-    with pytest.raises(AssertionError, match="staging of chunk"):
-        run_sweep(NC, final_wait=False)
+@pytest.mark.parametrize("groups,rep", [(1, 1), (3, 4), (5, 2)])
+def test_grad_and_prep_never_rewrite_a_tile_in_flight(groups, rep):
+    grad(groups, rep)
+    prep(groups * rep, rep)
 
 
-def test_one_chunk_needs_no_final_wait():
-    run_sweep(1, final_wait=False)
-
-
-def run_dsweep(NC, wait_each_chunk=True):
-    """chunk_dsweep_kernel, chunks in reverse: [dY; dU] double-buffered (dY of the next chunk is
-    loaded into the other buffer), one group per chunk storing [dY; dU], Delta and dv from their
-    tiles. Thread 0 waits for all groups once per chunk, before that load and the tile writes."""
-    ring = Ring()
-
-    def write(tiles, what):
-        assert not (ring.reading() & tiles), f"{what} rewritten while a store still reads it"
-
-    write({"ydu0"}, "dY buffer 0")
-    for k in range(NC):
-        buf = k & 1
-        if wait_each_chunk:
-            ring.wait_read_but(0)
-        if k + 1 < NC:
-            write({f"ydu{buf ^ 1}"}, f"dY buffer {buf ^ 1}")
-        write({"dls", "dvs", f"ydu{buf}"}, f"Delta, dv and dU tiles of chunk {k}")
-        ring.groups.append({f"ydu{buf}", "dls", "dvs"})
-
-
-@pytest.mark.parametrize("NC", [1, 2, 3, 32])
-def test_reverse_sweep_tiles_are_never_rewritten_in_flight(NC):
-    run_dsweep(NC)
-
-
-def test_reverse_sweep_without_its_wait_is_caught():
+@pytest.mark.parametrize("fn,arg,drop", [
+    (sweep, 3, "top32"), (sweep, 3, "top128"), (sweep, 2, "final"), (dsweep, 2, "top"),
+    (grad, (2, 2), "top"), (grad, (1, 2), "between"), (prep, (8, 4), "tcu"),
+])
+def test_controls_without_a_wait_fail(fn, arg, drop):
     with pytest.raises(AssertionError, match="rewritten while a store still reads it"):
-        run_dsweep(3, wait_each_chunk=False)
+        fn(*arg, drop=drop) if isinstance(arg, tuple) else fn(arg, drop=drop)
