@@ -47,10 +47,10 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:^chunk_sweep -s 3 -c 1 python bench.py --steps 1 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("e3af9fbb3f034157", "chunk_prep"): 64842752 + 254524672,
-    ("e3af9fbb3f034157", "chunk_sweep"): 298368768 + 355436032,
-    ("d219379010413947", "chunk_dsweep"): 265115392 + 197458688,
-    ("d219379010413947", "chunk_grad"): 330593024 + 17440256,
+    ("c0b309d2e3521b0b", "chunk_prep"): 34835968 + 92986368,
+    ("c0b309d2e3521b0b", "chunk_sweep"): 159991040 + 350721024,
+    ("c8dd4f7b3b5dc9ab", "chunk_dsweep"): 177038080 + 192236032,
+    ("c8dd4f7b3b5dc9ab", "chunk_grad"): 330720256 + 17506304,
 }
 
 
