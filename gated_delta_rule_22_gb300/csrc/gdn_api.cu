@@ -116,8 +116,8 @@ Workspace workspace_layout(const Plan &p) {
     return w;
 }
 
-// Scratch of the chunkwise backward: dbeta and f partials per block of 64 value rows
-// [B,T,Hv,nsplit] fp32; [dY; dU] [B,Hv,NC,nsplit][128 x 64], Delta [B,Hv,NC,nsplit][64 x 64] and
+// Scratch of the chunkwise backward: dbeta and f partials per 32 value rows
+// [B,T,Hv,nsplit,2] fp32; [dY; dU] [B,Hv,NC,nsplit][128 x 64], Delta [B,Hv,NC,nsplit][64 x 64] and
 // dS at each chunk end [B,Hv,NC,nsplit][64 x Dk], bf16 in their operand layout. (dq, dk are
 // summed over value heads in the gradient kernel's tensor memory and need no scratch.)
 struct TcWorkspace {
@@ -126,7 +126,7 @@ struct TcWorkspace {
 
 TcWorkspace tc_workspace_layout(const Plan &p) {
     TcWorkspace w;
-    const size_t ngate = (size_t)p.B * p.T * p.Hv * p.nsplit;
+    const size_t ngate = (size_t)p.B * p.T * p.Hv * p.nsplit * 2;   // a partial per 32 value rows
     const size_t nblk = (size_t)p.B * p.Hv * p.NC * p.nsplit;
     size_t off = 0;
     w.db = off; off += round_up(ngate * 4);

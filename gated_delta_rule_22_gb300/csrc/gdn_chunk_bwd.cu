@@ -19,17 +19,17 @@
 //       with c0 = <dS_L, S0>, f_i = delta_i . (dS_L k_i), a_s = dy_s . S0 q_s,
 //       b_s = du_s . S0 k_s, Z = (G o (Q K^T) + H o (K K^T)) M, M[i,t] = E(t-1,i) [i < t].
 //
-// Three kernels:
+// Two kernels:
 //   chunk_dsweep_kernel  the reverse sweep over the chunks of one (b, h, block of 64 value
-//                        rows), carrying dS (fp32, tensor memory): dD, dv, dbeta and f
-//                        (partials over the value rows), dU and dS_L for the next kernel, dS0.
+//                        rows), carrying dS (fp32, registers): dD, dv, dbeta and f (partials
+//                        over 32 value rows), dU and dS_L for the next kernel, dS0.
 //                        K dS_L^T takes dS as a bf16 high part plus a bf16 low part (exact to
 //                        about 2^-16): with dS rounded once to bf16, dg under strong decay
 //                        misses the bf16 parity bound.
 //   chunk_grad_kernel    per (b, h, chunk), persistent over whole groups of units (the value
 //                        heads of one kv head and chunk): everything else. dq, dk summed over
 //                        the value heads of each kv head (ascending) in tensor memory, written
-//                        as bf16 once per group; dbeta summed over the value-row blocks
+//                        as bf16 once per group; dbeta and f summed over their partials
 //                        (ascending); dg.
 // Operands are bf16 in the core-matrix layout of gdn_umma.cuh, read K-major or MN-major (one
 // stored copy serves a matrix and its transpose); accumulators fp32 in tensor memory. No
@@ -68,8 +68,15 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float *x) {
 constexpr size_t kOneCtaSmem = 120 * 1024;
 
 // ------------------------------------------------------------------ reverse sweep (dS)
+constexpr int kSweepMathWarps = 8;      // hold dS (M = 64 fragment: 4 lane quarters x 2 column halves)
+constexpr int kSweepThreads = 384;      // + a warpgroup whose first warp is the control warp
+// registers: launched at 168 a thread; the control warpgroup gives up all but kSweepCtrlRegs,
+// the math warpgroups take kSweepMathRegs (2 x 128 x 216 + 128 x 72 = 384 x 168)
+constexpr int kSweepLaunchRegs = 168, kSweepMathRegs = 216, kSweepCtrlRegs = 72;
+static_assert(2 * 128 * kSweepMathRegs + 128 * kSweepCtrlRegs <= kSweepThreads * kSweepLaunchRegs, "register split");
+
 struct DSweepSmem {
-    size_t qk, tm, pkm, ydu, yds, rsm, lms, shl, rhs, dls, dvs, vec, red, bar, tslot, total;
+    size_t qk, tm, pkm, ydu, yds, rsm, lms, shl, rhs, dls, dvs, bar, tslot, total;
     __host__ __device__ DSweepSmem(int DK) {
         size_t o = 0;
         qk = o; o += (size_t)2 * kL * DK * 2;    // [Q; K] [128][DK] (K-major rows 64-127: K; read MN-major whole)
@@ -83,9 +90,7 @@ struct DSweepSmem {
         rhs = o; o += (size_t)kL * kL * 2;   // diag(E_L) K dS^T + P^T dY [64 t][64 v]
         dls = o; o += (size_t)kL * kL * 2;   // Delta block [64 t][64 v], for the gradient kernel
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
-        vec = o; o += 4 * kL * 4;            // -, E(L, .), beta, -
-        red = o; o += 2 * 2 * kL * 4;        // [f | dbeta][half][64]
-        bar = alb(o, 8); o = bar + 6 * 8;    // MMA, copies of [P; KKm], of T, of [Q; K], of (dY, v - u, Lam); drain
+        bar = alb(o, 8); o = bar + 13 * 8;   // see the kernel
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -95,28 +100,37 @@ struct DSweepSmem {
 }  // namespace
 
 // One CTA per (block of 64 value rows, value head, batch row), over the chunks in reverse.
-// The adjoint dS (fp32) lives in registers (a thread holds the 16x256b fragment of an M = 64
-// accumulator: 2 rows x DK/8 columns); per chunk the products are (fp32 accumulators in tensor
-// memory, M = 64 layout: row r in lane r % 16 + 32 (r / 16)):
+// Warps 0-7 hold the adjoint dS (fp32, registers: the 16x256b fragment of an M = 64
+// accumulator, 2 rows x DK/8 columns per thread) and do the element-wise work; warp 8 issues
+// the products (one elected lane), the copies and the stores, so that no math warp stalls on an
+// issue and no block barrier runs per chunk: each hand-off is an mbarrier. Per chunk the products
+// are (fp32 accumulators in tensor memory, M = 64 layout: row r in lane r % 16 + 32 (r / 16)):
 //   [0, DK)              the chunk's part of the carry, [e^Lam dY; e^Lam dU]^T [Q; K]; the
 //                        next chunk's dS = exp(Lam_L) dS + this
 //   [DK, DK + 64)        K dS_high^T + K dS_low^T (chunk row t, value column; the two parts
 //                        accumulate in fp32); then dD
 //   [DK + 128, DK + 192) P^T dY
-// Warp 0 issues the products (from one elected lane, the warp converged); thread 32 issues the
-// copies and the stores; every thread converts (all 32 lanes of a warp hold fragment values).
+// Hand-offs of chunk c (each completes once per chunk):
+//   math -> control (8 warp arrivals): bH  dS parts written;  bR  rhs and Delta written, v - u
+//                                      read;  bU  dU, [e^Lam dY; e^Lam dU], dv written
+//   control -> math: m1, mD, mS  the product groups (commits);  fS  the dS parts' tile is free
+//                    (products done, the dS_L store has read it);  fO  the Delta and dv staging
+//                    tiles are free (their stores have read them)
+// dbeta and f leave as one partial per 32 value columns (the two column halves of the block).
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, const __grid_constant__ CUtensorMap tm_dv,
-                                                              const __grid_constant__ CUtensorMap tm_dy,
-                                                              const __grid_constant__ CUtensorMap tm_rs) {
+__global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwdParams p,
+                                                                        const __grid_constant__ CUtensorMap tm_dv,
+                                                                        const __grid_constant__ CUtensorMap tm_dy,
+                                                                        const __grid_constant__ CUtensorMap tm_rs) {
     constexpr int DK = 32 * E;
     constexpr int SC = DK / 2;                // dS columns per warp half
     constexpr int NS = SC / 2;                // dS values per thread
     static_assert(DK + 192 <= 512, "tensor memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool math = warp < kSweepMathWarps, ctrl = warp == kSweepMathWarps;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, Dv = p.Dv, Hv = p.Hv, r0 = split * kL, nsplit = p.nsplit;
-    const int hw = warp >> 2;                                   // warp half: value columns [32 hw, 32 hw + 32)
+    const int T = p.T, Dv = p.Dv, Hv = p.Hv, NC = p.NC, r0 = split * kL, nsplit = p.nsplit;
+    const int hw = (warp >> 2) & 1;                             // warp half: value columns [32 hw, 32 hw + 32)
     const uint32_t lane16 = (uint32_t)(32 * (warp & 3)) << 16;
 
     extern __shared__ unsigned char smem_raw[];
@@ -124,49 +138,30 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     const DSweepSmem L(DK);
     unsigned char *qk = base + L.qk, *tmm = base + L.tm, *pmm = base + L.pkm, *yds = base + L.yds;
     unsigned char *ydu2 = base + L.ydu, *shl = base + L.shl, *rhs = base + L.rhs, *dls = base + L.dls;
-    unsigned char *dvs = base + L.dvs;
-    unsigned char *rsm = base + L.rsm;
+    unsigned char *dvs = base + L.dvs, *rsm = base + L.rsm;
     float *lms = reinterpret_cast<float *>(base + L.lms);
-    float *eL = reinterpret_cast<float *>(base + L.vec) + kL, *bt = eL + kL;
-    float *red = reinterpret_cast<float *>(base + L.red);   // [2][2][64]
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
-    uint64_t *cbA = bar + 1, *cbT = bar + 2, *cbK = bar + 3, *cbY = bar + 4, *mX = bar + 5;
+    uint64_t *m1 = bar, *mD = bar + 1, *mS = bar + 2, *cbA = bar + 3, *cbT = bar + 4, *cbK = bar + 5, *cbY = bar + 6;
+    uint64_t *bH = bar + 7, *bR = bar + 8, *bU = bar + 9, *fS = bar + 10, *fO = bar + 11, *mX = bar + 12;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
 
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t head = (size_t)b * Hv + h;
 
-    // bulk copies of chunk cc's operands, three groups (each freed at a different point)
-    int nA = 0, nT = 0, nK = 0;
-    auto copy_A = [&](int cc) {
-        const size_t ck = head * p.NC + cc;
-        mbar_expect_tx(cbA, 2 * kL * kL * 2);
-        bulk_load(pmm, p.pkm + ck * 2 * kL * kL, 2 * kL * kL * 2, cbA);
-        ++nA;
-    };
-    auto copy_T = [&](int cc) {
-        const size_t ck = head * p.NC + cc;
-        mbar_expect_tx(cbT, kL * kL * 2);
-        bulk_load(tmm, p.tm + ck * kL * kL, kL * kL * 2, cbT);
-        ++nT;
-    };
-    auto copy_K = [&](int cc) {               // [Q; K] of the chunk (kv head)
-        mbar_expect_tx(cbK, 2 * kL * DK * 2);
-        bulk_load(qk, p.qkm + (((size_t)b * p.Hk + h / (Hv / p.Hk)) * p.NC + cc) * 2 * kL * DK, 2 * kL * DK * 2, cbK);
-        ++nK;
-    };
-
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(bar + i, 1);
+        for (int i = 0; i < 7; ++i) mbar_init(bar + i, 1);
+        for (int i = 7; i < 10; ++i) mbar_init(bar + i, kSweepMathWarps);
+        for (int i = 10; i < 13; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
     }
-    if (tid == 32) {
-        tma_prefetch_map(&tm_dy);
-        tma_prefetch_map(&tm_rs);
-        tma_prefetch_map(&tm_dv);
+    if (ctrl) {
+        if (lane == 0) {
+            tma_prefetch_map(&tm_dy);
+            tma_prefetch_map(&tm_rs);
+            tma_prefetch_map(&tm_dv);
+        }
+        tmem_alloc(tslot, 512);
     }
-    if (warp == 0) tmem_alloc(tslot, 512);
-    const uint32_t lead = warp == 0 ? elect_one_sync() : 0u;   // the lane of warp 0 that issues products
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -175,95 +170,190 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
     griddep_wait();                                           // the previous kernel's writes are visible
     griddep_launch();
 
-    // this thread's fragment of dS (rows fs.row(k), columns fs.col(j, k)), from dS_T
-    const M64Frag fs(warp, lane, DK);
-    float dS[NS];
-#pragma unroll
-    for (int j = 0; j < NS / 4; ++j)
-#pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {
-            float2 s2 = make_float2(0.f, 0.f);
-            if (p.dS_T != nullptr)
-                s2 = *reinterpret_cast<const float2 *>(p.dS_T + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0));
-            dS[4 * j + 2 * k2] = s2.x;
-            dS[4 * j + 2 * k2 + 1] = s2.y;
-        }
-    // this thread's fragment of the 64-column accumulators (chunk rows t, value columns)
-    const M64Frag fd(warp, lane, kL);
-    const int ta = fd.row(0), tb = fd.row(2);
-
-    unsigned ph = 0, cph = 0;
-    bool ok = true;
-    // a chunk's dY block, its v - u (one TMA box of two 128-byte-swizzled [64][32] tiles) and
-    // Lam (a bulk copy) arrive one chunk ahead, issued by thread 32 (rows past T: zeros); beta
-    // (threads < 64) by a load one chunk ahead
-    __nv_bfloat16 btn = __float2bfloat16_rn(0.f);   // raw: converted where it is used, so that the load does not stall here
-    int nY = 0, wY = 0;
-    auto fetch_chunk = [&](int cc, int buf) {
-        const int tt0 = cc * kL, ln = min(kL, T - tt0);
-        if (tid == 32) {
-            unsigned char *yb = ydu2 + (size_t)buf * 2 * kL * kL * 2;
-            // dY: one box of 128 rows in the [dY; dU] operand layout (8 core-matrix columns of
-            // 128 rows); rows 64-127 (the following steps) land in the dU rows, which the chunk
-            // rewrites before reading them
+    bool fail = false;
+    if (!math) regs_dec<kSweepCtrlRegs>();
+    else regs_inc<kSweepMathRegs>();
+    if (ctrl) {
+        // ================================================================ control warp
+        const uint32_t lead = elect_one_sync();               // issues the products
+        const bool io = lane == 0;                            // issues the copies and the stores
+        int nA = 0, nT = 0, nK = 0, nY = 0;
+        auto copy_A = [&](int cc) {                          // [P; KKm] of chunk cc
+            mbar_expect_tx(cbA, 2 * kL * kL * 2);
+            bulk_load(pmm, p.pkm + (head * NC + cc) * 2 * kL * kL, 2 * kL * kL * 2, cbA);
+        };
+        auto copy_T = [&](int cc) {                          // T of chunk cc
+            mbar_expect_tx(cbT, kL * kL * 2);
+            bulk_load(tmm, p.tm + (head * NC + cc) * kL * kL, kL * kL * 2, cbT);
+        };
+        auto copy_K = [&](int cc) {                          // [Q; K] of chunk cc (kv head)
+            mbar_expect_tx(cbK, 2 * kL * DK * 2);
+            bulk_load(qk, p.qkm + (((size_t)b * p.Hk + h / (Hv / p.Hk)) * NC + cc) * 2 * kL * DK, 2 * kL * DK * 2, cbK);
+        };
+        // dY (one 128-row box in the [dY; dU] layout: rows 64-127, the following steps, land in
+        // the dU rows, which the math warps rewrite before anything reads them), v - u (one box
+        // of two 128-byte-swizzled [64][32] tiles) and Lam of chunk cc (rows past T: zeros)
+        auto fetch = [&](int cc, int buf) {
+            const int tt0 = cc * kL;
             mbar_expect_tx(cbY, 2 * kL * kL * 2 + kL * kL * 4 + kL * 4);
-            tma_load_5d(yb, &tm_dy, cbY, 0, tt0, r0 / 8, h, b);
+            tma_load_5d(ydu2 + (size_t)buf * 2 * kL * kL * 2, &tm_dy, cbY, 0, tt0, r0 / 8, h, b);
             tma_load_5d(rsm, &tm_rs, cbY, 0, tt0, r0 / 32, h, b);
-            bulk_load(lms + buf * kL, p.lam + (head * p.NC + cc) * kL, kL * 4, cbY);
+            bulk_load(lms + buf * kL, p.lam + (head * NC + cc) * kL, kL * 4, cbY);
+        };
+        if (io) {
+            copy_A(NC - 1);
+            copy_T(NC - 1);
+            copy_K(NC - 1);
+            fetch(NC - 1, 0);
         }
-        ++nY;
-        if (tid < kL) btn = beta[((size_t)b * T + tt0 + (tid < ln ? tid : 0)) * Hv + h];
-    };
-    // v - u of the thread's fragment: row t, value columns fd.col(j, 0), + 1 (box hw of rsm: row
-    // t at t * 128, 16-byte chunk (col % 32) / 4 at chunk ^ (t % 8))
-    auto rs_pair = [&](int t, int j) {
-        const int c32 = 8 * j + 2 * (lane & 3);
-        return *reinterpret_cast<const float2 *>(rsm + hw * (kL * 128) + t * 128 + (((c32 >> 2) ^ (t & 7)) << 4) +
-                                                 (c32 & 3) * 4);
-    };
-    if (tid == 32) { copy_A(p.NC - 1); copy_T(p.NC - 1); copy_K(p.NC - 1); }
-    fetch_chunk(p.NC - 1, 0);
-    float decay_next = 1.f;                       // exp(Lam_L) of the chunk processed before (later in time)
-    for (int c = p.NC - 1; c >= 0 && ok; --c) {
-        const int t0 = c * kL, len = min(kL, T - t0);
-        const size_t chk = head * p.NC + c;
-        const size_t rowbase = (size_t)b * T + t0;          // (b, t0) row of [B, T, ...]
-        const int buf = (p.NC - 1 - c) & 1;
-        unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;   // [dY; dU] of this chunk
-        const float *lmb = lms + buf * kL;                 // Lam of this chunk
-        if (tid == 32) bulk_wait_read();                    // the last chunk's stores have read their tiles
-        {
-            // this chunk's dY, v - u and Lam have landed (every thread waits: every thread reads them)
-            const bool w = mbar_wait(cbY, wY & 1);
-            ++wY;
-            if (tid < kL) {
-                bt[tid] = tid < len ? __bfloat162float(btn) : 0.f;
-                eL[tid] = expf(lmb[kL - 1] - lmb[tid]);
+        nA = nT = nK = nY = 1;
+        for (int k = 0; k < NC; ++k) {
+            const int c = NC - 1 - k, buf = k & 1;
+            const size_t chk = head * NC + c, blk = chk * nsplit + split;
+            unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;
+            // ---- K dS_high^T + K dS_low^T, P^T dY once the dS parts are written and the operands landed
+            bool w = mbar_wait(bH, k & 1);
+            if (io && w) {
+                bulk_store(p.ws_dsl + blk * kL * DK, shl, kL * DK * 2);   // dS_L (high part) for the gradient kernel
+                bulk_commit();
             }
-            ok = !__syncthreads_or(!w);
-            if (!ok) break;
-        }
-        // this thread's v - u (rows ta, tb), read before the next chunk's copy overwrites rsm
-        float2 rsa[4], rsb[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            rsa[j] = rs_pair(ta, j);
-            rsb[j] = rs_pair(tb, j);
-        }
-        // ---- dS of this chunk's end: exp(Lam_L) dS + the later chunk's part of the carry
-        if (c < p.NC - 1) {
-#pragma unroll
-            for (int i = 0; i < NS / 16; ++i) {
-                float x[16];
-                tmem_ld16x256_x4(tS + lane16 + SC * hw + 32 * i, x);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) dS[16 * i + e] = fmaf(decay_next, dS[16 * i + e], x[e]);
+            w = w && mbar_wait(cbA, k & 1) && mbar_wait(cbK, k & 1) && mbar_wait(cbY, k & 1);
+            if (__any_sync(kFullMask, !w)) { fail = true; break; }
+            tc_fence_after();
+            {
+                constexpr uint32_t idX = umma_idesc(1, kL, kL);
+                constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
+                umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl, kL, 0, 0, false}, DK, idX, false, lead);
+                umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl + kL * DK * 2, kL, 0, 0, false}, DK, idX, true,
+                            lead);
+                umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false, lead);
+                umma_commit_w(m1, lead);
             }
+            // ---- dD = T^T rhs once rhs is written (the math warps saw m1: [P; KKm] is free, and
+            // they have read v - u)
+            w = mbar_wait(bR, k & 1);
+            if (io && w) {
+                if (c > 0) { copy_A(c - 1); ++nA; }
+                bulk_wait_read();                           // the dS_L store (and the earlier ones) have read their tiles
+                mbar_arrive(fS);                            // the products that read the dS parts are done (m1)
+            }
+            w = w && mbar_wait(cbT, k & 1);
+            if (__any_sync(kFullMask, !w)) { fail = true; break; }
+            tc_fence_after();
+            umma_gemm_w(tX, CmOp{tmm, kL, 0, 0, true}, CmOp{rhs, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, kL, true, true),
+                        false, lead);
+            umma_commit_w(mD, lead);
+            // the next chunk's dY, v - u and Lam: its [dY; dU] buffer was stored and read out
+            // (bulk_wait_read above), and v - u was read (bR)
+            if (io && c > 0) { fetch(c - 1, buf ^ 1); ++nY; }
+            // ---- the carry once dU and the operands of the carry are written (the math warps
+            // saw mD: T is free)
+            w = mbar_wait(bU, k & 1);
+            if (__any_sync(kFullMask, !w)) { fail = true; break; }
+            tc_fence_after();
+            umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, 2 * kL,
+                        umma_idesc_t(1, kL, DK, true, true), false, lead);
+            umma_commit_w(mS, lead);
+            if (io) {
+                if (c > 0) { copy_T(c - 1); ++nT; }
+                // [dY; dU] and Delta of the block for the gradient kernel, and dv
+                bulk_store(p.ws_yu + blk * 2 * kL * kL, ydu, 2 * kL * kL * 2);
+                bulk_store(p.ws_dl + blk * kL * kL, dls, kL * kL * 2);
+                tma_store_4d(&tm_dv, dvs, r0, h, c * kL, b);
+                bulk_commit();
+            }
+            // [Q; K] is free once the carry is done
+            w = mbar_wait(mS, k & 1);
+            if (io && w) {
+                if (c > 0) { copy_K(c - 1); ++nK; }
+                bulk_wait_read();                           // Delta and dv staging read out
+                mbar_arrive(fO);
+            }
+            if (__any_sync(kFullMask, !w)) { fail = true; break; }
         }
-        // ---- dS as operands: a bf16 high part and a bf16 low part (dS - high), each [64][DK]; the
-        // high part also leaves for the gradient kernel (a bulk store below)
-        {
+        if (fail) {
+            if (io) {
+                // copies still in flight land before the CTA exits (each wait bounded)
+                mbar_wait(cbA, (nA - 1) & 1);
+                mbar_wait(cbT, (nT - 1) & 1);
+                mbar_wait(cbK, (nK - 1) & 1);
+                mbar_wait(cbY, (nY - 1) & 1);
+            }
+            // products still in flight finish before the tensor memory is freed (bounded wait)
+            umma_commit_w(mX, lead);
+            mbar_wait(mX, 0);
+        }
+        if (io) bulk_wait_all();                            // the block outputs are complete
+    } else if (math) {
+        // ================================================================ math warps
+        // this thread's fragment of dS (rows fs.row(k), columns fs.col(j, k)), from dS_T
+        const M64Frag fs(warp, lane, DK);
+        float dS[NS];
+#pragma unroll
+        for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                float2 s2 = make_float2(0.f, 0.f);
+                if (p.dS_T != nullptr)
+                    s2 = *reinterpret_cast<const float2 *>(p.dS_T + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0));
+                dS[4 * j + 2 * k2] = s2.x;
+                dS[4 * j + 2 * k2 + 1] = s2.y;
+            }
+        // this thread's fragment of the 64-column accumulators (chunk rows ta, tb, value columns)
+        const M64Frag fd(warp, lane, kL);
+        const int ta = fd.row(0), tb = fd.row(2);
+        // beta of rows ta, tb: loaded one chunk ahead, kept raw until used
+        auto load_beta = [&](int cc, __nv_bfloat16 &xa, __nv_bfloat16 &xb) {
+            const int tt0 = cc * kL, ln = min(kL, T - tt0);
+            const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+            xa = ta < ln ? beta[((size_t)b * T + tt0 + ta) * Hv + h] : z;
+            xb = tb < ln ? beta[((size_t)b * T + tt0 + tb) * Hv + h] : z;
+        };
+        // v - u of the thread's fragment: row t, value columns fd.col(j, 0), + 1 (box hw of rsm: row
+        // t at t * 128, 16-byte chunk (col % 32) / 4 at chunk ^ (t % 8))
+        auto rs_pair = [&](int t, int j) {
+            const int c32 = 8 * j + 2 * (lane & 3);
+            return *reinterpret_cast<const float2 *>(rsm + hw * (kL * 128) + t * 128 + (((c32 >> 2) ^ (t & 7)) << 4) +
+                                                     (c32 & 3) * 4);
+        };
+        // a warp's part is written: its lanes' shared-memory writes are visible to the
+        // products and copies, and its tensor-memory reads are complete
+        auto warp_done = [&](uint64_t *bar_) {
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_);
+        };
+        __nv_bfloat16 bna, bnb;
+        load_beta(NC - 1, bna, bnb);
+        float decay_next = 1.f;                       // exp(Lam_L) of the chunk processed before (later in time)
+        for (int k = 0; k < NC; ++k) {
+            const int c = NC - 1 - k, buf = k & 1;
+            const int t0 = c * kL, len = min(kL, T - t0);
+            const size_t rowbase = (size_t)b * T + t0;          // (b, t0) row of [B, T, ...]
+            unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;   // [dY; dU] of this chunk
+            const float *lmb = lms + buf * kL;                 // Lam of this chunk
+            const float ba = __bfloat162float(bna), bb = __bfloat162float(bnb);
+            if (c > 0) load_beta(c - 1, bna, bnb);
+            // ---- dS of this chunk's end: exp(Lam_L) dS + the later chunk's part of the carry
+            if (k > 0) {
+                const bool w = mbar_wait(mS, (k - 1) & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < NS / 16; ++i) {
+                    float x[16];
+                    tmem_ld16x256_x4(tS + lane16 + SC * hw + 32 * i, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) dS[16 * i + e] = fmaf(decay_next, dS[16 * i + e], x[e]);
+                }
+                // the tile of the dS parts: the later chunk's products and dS_L store are done with it
+                const bool w2 = mbar_wait(fS, (k - 1) & 1);
+                if (__any_sync(kFullMask, !w2)) { fail = true; break; }
+            }
+            // ---- dS as operands: a bf16 high part and a bf16 low part (dS - high), each [64][DK]; the
+            // high part also leaves for the gradient kernel (a bulk store by the control warp)
 #pragma unroll
             for (int j = 0; j < NS / 4; ++j)
 #pragma unroll
@@ -276,199 +366,144 @@ __global__ void __launch_bounds__(256, 1) chunk_dsweep_kernel(ChunkBwdParams p, 
                     *reinterpret_cast<uint32_t *>(shl + o) = hu;
                     *reinterpret_cast<uint32_t *>(shl + kL * DK * 2 + o) = pack2_bf16(x0 - h0, x1 - h1);
                 }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        {
-            // [Q; K] and [P; KKm] have landed (warp 0)
-            bool w = true;
-            if (warp == 0) w = mbar_wait(cbA, cph & 1) && mbar_wait(cbK, cph & 1);
-            ok = !__syncthreads_or(!w);
-        }
-        tc_fence_after();
-        if (!ok) break;
-        if (tid == 32) {
-            bulk_store(p.ws_dsl + (chk * nsplit + split) * kL * DK, shl, kL * DK * 2);   // dS_L (high part) for the gradient kernel
-            bulk_commit();
-        }
-        if (c > 0) fetch_chunk(c - 1, buf ^ 1);             // the other [dY; dU] buffer was stored and read out last chunk
-        // ---- K dS_high^T + K dS_low^T (K: rows 64-127 of [Q; K]), P^T dY (P: rows 0-63 of [P; KKm])
-        if (warp == 0) {
-            constexpr uint32_t idX = umma_idesc(1, kL, kL);
-            constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
-            umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl, kL, 0, 0, false}, DK, idX, false, lead);
-            umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl + kL * DK * 2, kL, 0, 0, false}, DK, idX, true, lead);
-            umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false, lead);
-            umma_commit_w(bar, lead);
-        }
-        // diag(exp Lam) dY while the products run: rows 0-63 of the dS update's operand (the dU
-        // rows follow below)
-        for (int e = tid; e < kL * kL / 8; e += 256) {
-            const int t = e & (kL - 1);
-            const uint32_t o = cm_off(t, 16 * (e >> 6), 2 * kL);
-            float x8[8];
-            unpack8(*reinterpret_cast<const uint4 *>(ydu + o), x8);
-            const float gt = expf(lmb[t]);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x8[i] *= gt;
-            *reinterpret_cast<uint4 *>(yds + o) = pack8(x8);
-        }
-        ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
-        ++ph;
-        tc_fence_after();
-        if (!ok) break;
-        // ---- rhs = diag(E_L) K dS^T + P^T dY as an operand; Delta = beta (v - u) for the gradient
-        // kernel; f partial = beta_t (v_t - u_t) . (dS k_t)
-        {
-            float xh[16], pp[16];
-            tmem_ld16x256_x4(tX + lane16 + 32 * hw, xh);
-            tmem_ld16x256_x4(tP + lane16 + 32 * hw, pp);
-            tmem_wait_ld();
-            const float ela = eL[ta], elb = eL[tb], ba = bt[ta], bb = bt[tb];
-            float fa = 0.f, fb = 0.f;
+            warp_done(bH);
+            // ---- this chunk's dY, v - u and Lam
+            {
+                const bool w = mbar_wait(cbY, k & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+            }
+            // this thread's v - u (rows ta, tb), read before the next chunk's copy overwrites rsm
+            float2 rsa[4], rsb[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float2 ra = rsa[j], rb = rsb[j];
-                const float x0 = xh[4 * j], x1 = xh[4 * j + 1], x2 = xh[4 * j + 2], x3 = xh[4 * j + 3];
-                fa = fmaf(ra.x, x0, fmaf(ra.y, x1, fa));
-                fb = fmaf(rb.x, x2, fmaf(rb.y, x3, fb));
-                const int col = fd.col(j, 0);
-                const uint32_t oa = cm_off(ta, 2 * col, kL), ob = cm_off(tb, 2 * col, kL);
-                *reinterpret_cast<uint32_t *>(rhs + oa) = pack2_bf16(fmaf(ela, x0, pp[4 * j]), fmaf(ela, x1, pp[4 * j + 1]));
-                *reinterpret_cast<uint32_t *>(rhs + ob) = pack2_bf16(fmaf(elb, x2, pp[4 * j + 2]), fmaf(elb, x3, pp[4 * j + 3]));
-                *reinterpret_cast<uint32_t *>(dls + oa) = pack2_bf16(ba * ra.x, ba * ra.y);
-                *reinterpret_cast<uint32_t *>(dls + ob) = pack2_bf16(bb * rb.x, bb * rb.y);
+                rsa[j] = rs_pair(ta, j);
+                rsb[j] = rs_pair(tb, j);
             }
-            // the row sums over this warp's 32 columns: the four lanes that share a row
-            fa += __shfl_xor_sync(kFullMask, fa, 1);
-            fa += __shfl_xor_sync(kFullMask, fa, 2);
-            fb += __shfl_xor_sync(kFullMask, fb, 1);
-            fb += __shfl_xor_sync(kFullMask, fb, 2);
-            if ((lane & 3) == 0) {
-                red[hw * kL + ta] = ba * fa;
-                red[hw * kL + tb] = bb * fb;
+            const float ela = expf(lmb[kL - 1] - lmb[ta]), elb = expf(lmb[kL - 1] - lmb[tb]);
+            const float ga = expf(lmb[ta]), gb = expf(lmb[tb]);
+            decay_next = expf(lmb[kL - 1]);
+            // diag(exp Lam) dY while the products run: rows 0-63 of the carry's operand (the dU
+            // rows follow below); its tile is free since the later chunk's carry is done (mS)
+            for (int e = tid; e < kL * kL / 8; e += kSweepMathWarps * 32) {
+                const int t = e & (kL - 1);
+                const uint32_t o = cm_off(t, 16 * (e >> 6), 2 * kL);
+                float x8[8];
+                unpack8(*reinterpret_cast<const uint4 *>(ydu + o), x8);
+                const float gt = expf(lmb[t]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x8[i] *= gt;
+                *reinterpret_cast<uint4 *>(yds + o) = pack8(x8);
+            }
+            // ---- rhs = diag(E_L) K dS^T + P^T dY as an operand; Delta = beta (v - u) for the gradient
+            // kernel; f partial = beta_t (v_t - u_t) . (dS k_t) over this warp's 32 value columns
+            {
+                bool w = mbar_wait(m1, k & 1);
+                if (k > 0) w = w && mbar_wait(fO, (k - 1) & 1);   // the Delta and dv tiles are free
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+            }
+            tc_fence_after();
+            {
+                float xh[16], pp[16];
+                tmem_ld16x256_x4(tX + lane16 + 32 * hw, xh);
+                tmem_ld16x256_x4(tP + lane16 + 32 * hw, pp);
+                tmem_wait_ld();
+                float fa = 0.f, fb = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 ra = rsa[j], rb = rsb[j];
+                    const float x0 = xh[4 * j], x1 = xh[4 * j + 1], x2 = xh[4 * j + 2], x3 = xh[4 * j + 3];
+                    fa = fmaf(ra.x, x0, fmaf(ra.y, x1, fa));
+                    fb = fmaf(rb.x, x2, fmaf(rb.y, x3, fb));
+                    const int col = fd.col(j, 0);
+                    const uint32_t oa = cm_off(ta, 2 * col, kL), ob = cm_off(tb, 2 * col, kL);
+                    *reinterpret_cast<uint32_t *>(rhs + oa) = pack2_bf16(fmaf(ela, x0, pp[4 * j]), fmaf(ela, x1, pp[4 * j + 1]));
+                    *reinterpret_cast<uint32_t *>(rhs + ob) = pack2_bf16(fmaf(elb, x2, pp[4 * j + 2]), fmaf(elb, x3, pp[4 * j + 3]));
+                    *reinterpret_cast<uint32_t *>(dls + oa) = pack2_bf16(ba * ra.x, ba * ra.y);
+                    *reinterpret_cast<uint32_t *>(dls + ob) = pack2_bf16(bb * rb.x, bb * rb.y);
+                }
+                warp_done(bR);
+                // the row sums over this warp's 32 columns: the four lanes that share a row
+                fa += __shfl_xor_sync(kFullMask, fa, 1);
+                fa += __shfl_xor_sync(kFullMask, fa, 2);
+                fb += __shfl_xor_sync(kFullMask, fb, 1);
+                fb += __shfl_xor_sync(kFullMask, fb, 2);
+                if ((lane & 3) == 0) {
+                    float *f = p.ws_f + (rowbase * Hv + h) * 2 * nsplit + 2 * split + hw;
+                    if (ta < len) f[(size_t)ta * Hv * 2 * nsplit] = ba * fa;
+                    if (tb < len) f[(size_t)tb * Hv * 2 * nsplit] = bb * fb;
+                }
+            }
+            // ---- dv = beta dD, dbeta partial, dU = -beta dD (operand rows 64-127, stored for the
+            // gradient kernel) and exp(Lam) dU (the carry's operand)
+            {
+                const bool w = mbar_wait(mD, k & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+            }
+            tc_fence_after();
+            {
+                float x[16];
+                tmem_ld16x256_x4(tX + lane16 + 32 * hw, x);
+                tmem_wait_ld();
+                float da = 0.f, db = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 ra = rsa[j], rb = rsb[j];
+                    da = fmaf(x[4 * j], ra.x, fmaf(x[4 * j + 1], ra.y, da));
+                    db = fmaf(x[4 * j + 2], rb.x, fmaf(x[4 * j + 3], rb.y, db));
+                    const int col = fd.col(j, 0);
+                    const float va0 = ba * x[4 * j], va1 = ba * x[4 * j + 1], vb0 = bb * x[4 * j + 2], vb1 = bb * x[4 * j + 3];
+                    const uint32_t oa = cm_off(kL + ta, 2 * col, 2 * kL), ob = cm_off(kL + tb, 2 * col, 2 * kL);
+                    *reinterpret_cast<uint32_t *>(ydu + oa) = pack2_bf16(-va0, -va1);
+                    *reinterpret_cast<uint32_t *>(ydu + ob) = pack2_bf16(-vb0, -vb1);
+                    *reinterpret_cast<uint32_t *>(yds + oa) = pack2_bf16(-ga * va0, -ga * va1);
+                    *reinterpret_cast<uint32_t *>(yds + ob) = pack2_bf16(-gb * vb0, -gb * vb1);
+                    // dv staged in the 128-byte swizzle for a TMA store (rows past T are clipped by it):
+                    // row t at t * 128, 16-byte chunk col / 8 at chunk ^ (t % 8)
+                    *reinterpret_cast<uint32_t *>(dvs + ta * 128 + (((col >> 3) ^ (ta & 7)) << 4) + (col & 7) * 2) =
+                        pack2_bf16(va0, va1);
+                    *reinterpret_cast<uint32_t *>(dvs + tb * 128 + (((col >> 3) ^ (tb & 7)) << 4) + (col & 7) * 2) =
+                        pack2_bf16(vb0, vb1);
+                }
+                warp_done(bU);
+                da += __shfl_xor_sync(kFullMask, da, 1);
+                da += __shfl_xor_sync(kFullMask, da, 2);
+                db += __shfl_xor_sync(kFullMask, db, 1);
+                db += __shfl_xor_sync(kFullMask, db, 2);
+                if ((lane & 3) == 0) {
+                    float *d = p.ws_db + (rowbase * Hv + h) * 2 * nsplit + 2 * split + hw;
+                    if (ta < len) d[(size_t)ta * Hv * 2 * nsplit] = da;
+                    if (tb < len) d[(size_t)tb * Hv * 2 * nsplit] = db;
+                }
             }
         }
-        fence_proxy_async();
-        tc_fence_before();
-        ok = !__syncthreads_or(warp == 0 && !mbar_wait(cbT, cph & 1));   // and T has landed
-        tc_fence_after();
-        if (!ok) break;
-        // the buffer of [P; KKm] is free: the previous chunk's copy goes out now
-        if (tid == 32 && c > 0) copy_A(c - 1);
-        if (tid < kL && tid < len) p.ws_f[((rowbase + tid) * Hv + h) * nsplit + split] = red[tid] + red[kL + tid];
-        // ---- dD = T^T rhs
-        if (warp == 0) {
-            umma_gemm_w(tX, CmOp{tmm, kL, 0, 0, true}, CmOp{rhs, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, kL, true, true),
-                        false, lead);
-            umma_commit_w(bar, lead);
-        }
-        ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
-        ++ph;
-        tc_fence_after();
-        if (!ok) break;
-        if (tid == 32 && c > 0) copy_T(c - 1);
-        // ---- dv = beta dD, dbeta partial, dU = -beta dD (operand rows 64-127, stored for the
-        // gradient kernel) and exp(Lam) dU (the dS update's operand)
-        {
-            float x[16];
-            tmem_ld16x256_x4(tX + lane16 + 32 * hw, x);
-            tmem_wait_ld();
-            const float ba = bt[ta], bb = bt[tb], ga = expf(lmb[ta]), gb = expf(lmb[tb]);
-            float da = 0.f, db = 0.f;
+        if (!fail && p.dS0 != nullptr) {
+            // dS0 = exp(Lam_L) dS + the first chunk's part of the carry
+            const bool w = mbar_wait(mS, (NC - 1) & 1);
+            fail = __any_sync(kFullMask, !w);
+            if (!fail) {
+                tc_fence_after();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 ra = rsa[j], rb = rsb[j];
-                da = fmaf(x[4 * j], ra.x, fmaf(x[4 * j + 1], ra.y, da));
-                db = fmaf(x[4 * j + 2], rb.x, fmaf(x[4 * j + 3], rb.y, db));
-                const int col = fd.col(j, 0);
-                const float va0 = ba * x[4 * j], va1 = ba * x[4 * j + 1], vb0 = bb * x[4 * j + 2], vb1 = bb * x[4 * j + 3];
-                const uint32_t oa = cm_off(kL + ta, 2 * col, 2 * kL), ob = cm_off(kL + tb, 2 * col, 2 * kL);
-                *reinterpret_cast<uint32_t *>(ydu + oa) = pack2_bf16(-va0, -va1);
-                *reinterpret_cast<uint32_t *>(ydu + ob) = pack2_bf16(-vb0, -vb1);
-                *reinterpret_cast<uint32_t *>(yds + oa) = pack2_bf16(-ga * va0, -ga * va1);
-                *reinterpret_cast<uint32_t *>(yds + ob) = pack2_bf16(-gb * vb0, -gb * vb1);
-                // dv staged in the 128-byte swizzle for a TMA store (rows past T are clipped by it):
-                // row t at t * 128, 16-byte chunk col / 8 at chunk ^ (t % 8)
-                *reinterpret_cast<uint32_t *>(dvs + ta * 128 + (((col >> 3) ^ (ta & 7)) << 4) + (col & 7) * 2) =
-                    pack2_bf16(va0, va1);
-                *reinterpret_cast<uint32_t *>(dvs + tb * 128 + (((col >> 3) ^ (tb & 7)) << 4) + (col & 7) * 2) =
-                    pack2_bf16(vb0, vb1);
-            }
-            da += __shfl_xor_sync(kFullMask, da, 1);
-            da += __shfl_xor_sync(kFullMask, da, 2);
-            db += __shfl_xor_sync(kFullMask, db, 1);
-            db += __shfl_xor_sync(kFullMask, db, 2);
-            if ((lane & 3) == 0) {
-                red[2 * kL + hw * kL + ta] = da;
-                red[2 * kL + hw * kL + tb] = db;
+                for (int i = 0; i < NS / 16; ++i) {
+                    float x[16];
+                    tmem_ld16x256_x4(tS + lane16 + SC * hw + 32 * i, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) dS[16 * i + e] = fmaf(decay_next, dS[16 * i + e], x[e]);
+                }
+#pragma unroll
+                for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+                    for (int k2 = 0; k2 < 2; ++k2)
+                        *reinterpret_cast<float2 *>(p.dS0 + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0)) =
+                            make_float2(dS[4 * j + 2 * k2], dS[4 * j + 2 * k2 + 1]);
             }
         }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid < kL && tid < len)
-            p.ws_db[((rowbase + tid) * Hv + h) * nsplit + split] = red[2 * kL + tid] + red[3 * kL + tid];
-        // ---- the chunk's part of the carry: [diag(exp Lam) dY; diag(exp Lam) dU]^T [Q; K] (K = 128)
-        if (warp == 0) {
-            umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, 2 * kL,
-                        umma_idesc_t(1, kL, DK, true, true), false, lead);
-            umma_commit_w(bar, lead);
-        }
-        if (tid == 32) {
-            // [dY; dU] and Delta of the block for the gradient kernel, and dv
-            const size_t blk = chk * nsplit + split;
-            bulk_store(p.ws_yu + blk * 2 * kL * kL, ydu, 2 * kL * kL * 2);
-            bulk_store(p.ws_dl + blk * kL * kL, dls, kL * kL * 2);
-            tma_store_4d(&tm_dv, dvs, r0, h, t0, b);
-            bulk_commit();
-        }
-        ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
-        ++ph;
-        tc_fence_after();
-        if (!ok) break;
-        if (tid == 32 && c > 0) copy_K(c - 1);         // [Q; K] is free again
-        ++cph;
-        decay_next = expf(lmb[kL - 1]);
-        // no block barrier before the next chunk: nothing after this point reads what its first
-        // section writes
     }
-    if (tid == 32) bulk_wait_all();                         // the block outputs are complete
-    if (ok && p.dS0 != nullptr) {
-        // dS0 = exp(Lam_L) dS + the first chunk's part of the carry
-#pragma unroll
-        for (int i = 0; i < NS / 16; ++i) {
-            float x[16];
-            tmem_ld16x256_x4(tS + lane16 + SC * hw + 32 * i, x);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) dS[16 * i + e] = fmaf(decay_next, dS[16 * i + e], x[e]);
-        }
-#pragma unroll
-        for (int j = 0; j < NS / 4; ++j)
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2)
-                *reinterpret_cast<float2 *>(p.dS0 + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0)) =
-                    make_float2(dS[4 * j + 2 * k2], dS[4 * j + 2 * k2 + 1]);
-    }
-    if (!ok && tid == 32) {
-        report_status(p.status, kStatusTimeout);
-        // copies still in flight land before the CTA exits (each wait bounded)
-        if (nA > 0) mbar_wait(cbA, (nA - 1) & 1);
-        if (nT > 0) mbar_wait(cbT, (nT - 1) & 1);
-        if (nK > 0) mbar_wait(cbK, (nK - 1) & 1);
-        if (nY > 0) mbar_wait(cbY, (nY - 1) & 1);
-    }
-    if (!ok && warp == 0) {
-        // products still in flight finish before the tensor memory is freed (bounded wait)
-        umma_commit_w(mX, lead);
-        mbar_wait(mX, 0);
-    }
+    if (fail && lane == 0) report_status(p.status, kStatusTimeout);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (ctrl) tmem_dealloc(tmem, 512);
 }
 
 namespace {
@@ -587,8 +622,9 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     auto same_qk = [&](int u1, int u2) { return u1 / rep == u2 / rep; };   // same (b, chunk, kv head)
     // decays, beta and the f partials of a unit (threads < 64), loaded one unit ahead and kept
     // raw (converted and summed where they are used, so that the loads do not stall here)
-    constexpr int kMaxSplit = 4;                            // Dv <= 256
-    float vlam = 0.f, vfp[kMaxSplit] = {0.f, 0.f, 0.f, 0.f}, vdb[kMaxSplit] = {0.f, 0.f, 0.f, 0.f};
+    constexpr int kMaxPart = 8;                             // two per block of 64 value rows, Dv <= 256
+    const int nparts = 2 * nsplit;
+    float vlam = 0.f, vfp[kMaxPart], vdb[kMaxPart];
     __nv_bfloat16 vbt = __float2bfloat16_rn(0.f);
     auto load_vec = [&](int u) {
         if (tid >= kL) return;
@@ -600,9 +636,9 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         vlam = p.lam[chk * kL + tid];
         vbt = beta[row];
 #pragma unroll
-        for (int s = 0; s < kMaxSplit; ++s) {
-            vfp[s] = s < nsplit ? p.ws_f[row * nsplit + s] : 0.f;
-            vdb[s] = s < nsplit ? p.ws_db[row * nsplit + s] : 0.f;
+        for (int s = 0; s < kMaxPart; ++s) {
+            vfp[s] = s < nparts ? p.ws_f[row * nparts + s] : 0.f;
+            vdb[s] = s < nparts ? p.ws_db[row * nparts + s] : 0.f;
         }
     };
 
@@ -642,12 +678,12 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             bt[tid] = in ? __bfloat162float(vbt) : 0.f;
             float f = 0.f;
 #pragma unroll
-            for (int s = 0; s < kMaxSplit; ++s) f += s < nsplit ? vfp[s] : 0.f;   // splits in ascending order
+            for (int s = 0; s < kMaxPart; ++s) f += s < nparts ? vfp[s] : 0.f;   // partials in ascending order
             fv[tid] = in ? f : 0.f;
             // dbeta of the row: its value-row block partials, in ascending order
             float db = 0.f;
 #pragma unroll
-            for (int s = 0; s < kMaxSplit; ++s) db += s < nsplit ? vdb[s] : 0.f;
+            for (int s = 0; s < kMaxPart; ++s) db += s < nparts ? vdb[s] : 0.f;
             if (in) static_cast<__nv_bfloat16 *>(p.dbeta)[(rowbase + tid) * Hv + h] = __float2bfloat16_rn(db);
         }
         if (tid == 32) bulk_wait_read();                    // the last group's dq, dk stores have read stg
@@ -947,12 +983,19 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
                                       cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sd = DSweepSmem(DK).total, sg = GradSmem(DK, p.Dv).total;
-    cudaError_t err = cudaFuncSetAttribute(chunk_dsweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd);
+    // the reverse sweep's register split waits for registers that only a launch of
+    // kSweepLaunchRegs per thread provides
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, chunk_dsweep_kernel<E>);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs < kSweepLaunchRegs || fa.maxThreadsPerBlock < kSweepThreads) return cudaErrorInvalidConfiguration;
+    err = cudaFuncSetAttribute(chunk_dsweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(chunk_grad_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_dsweep", 0, s);
-    err = launch_pdl(chunk_dsweep_kernel<E>, dim3(p.nsplit, p.Hv, p.B), dim3(256), sd, s, p, tm_dv, tm_dy, tm_rs);
+    err = launch_pdl(chunk_dsweep_kernel<E>, dim3(p.nsplit, p.Hv, p.B), dim3(kSweepThreads), sd, s, p, tm_dv, tm_dy,
+                     tm_rs);
     timing_mark("chunk_dsweep", 1, s);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_grad", 0, s);

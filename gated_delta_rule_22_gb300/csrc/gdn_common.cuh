@@ -97,7 +97,7 @@ struct ChunkBwdParams {
     const float *dS_T;
     float *dS0;
     void *dv, *dg, *dq, *dk, *dbeta;
-    float *ws_db, *ws_f;       // [B, T, Hv, nsplit]: per block of 64 value rows
+    float *ws_db, *ws_f;       // [B, T, Hv, nsplit, 2]: per 32 value rows (the halves of a 64-row block)
     __nv_bfloat16 *ws_yu;      // [B, Hv, NC, nsplit][128 x 64]: [dY; dU] of the block, operand layout
     __nv_bfloat16 *ws_dl;      // [B, Hv, NC, nsplit][64 x 64]: Delta = diag(beta) (v - u), operand layout
     __nv_bfloat16 *ws_dsl;     // [B, Hv, NC, nsplit][64 x Dk]: dS at each chunk end, operand layout

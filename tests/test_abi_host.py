@@ -65,8 +65,8 @@ def test_exports_every_header_function(lib):
 
 def test_buffer_sizes_follow_the_plan(lib):
     """bf16 with chunk 64 and a supported Dk, Dv: the chunkwise form's saved buffer (larger than
-    states + residuals) and workspace (per 64-row block of a value head: dbeta and f partials,
-    and the [dY; dU], Delta and dS operand tiles; no dq, dk partials). When the chunked backward
+    states + residuals) and workspace (dbeta and f partials per 32 value rows, and per 64-row block
+    of a value head the [dY; dU], Delta and dS operand tiles; no dq, dk partials). When the chunked backward
     does not fit shared memory (Dk 128, Dv 256) the workspace is the sequential backward's
     (row-split partials), while the saved buffer stays chunkwise. Dv above 256 takes the
     sequential kernels altogether."""
@@ -87,7 +87,7 @@ def test_buffer_sizes_follow_the_plan(lib):
             r = lambda x: -(-x // 256) * 256  # noqa: E731
             ns = Dv // 64
             nblk = Hv * NC * ns
-            want = 2 * r(T * Hv * ns * 4) + r(nblk * 128 * 64 * 2) + r(nblk * 64 * 64 * 2) + r(nblk * 64 * Dk * 2)
+            want = 2 * r(T * Hv * ns * 2 * 4) + r(nblk * 128 * 64 * 2) + r(nblk * 64 * 64 * 2) + r(nblk * 64 * Dk * 2)
             assert ws == want, (Dk, Dv, ws, want)
         else:
             assert ws >= row_split, (Dk, Dv, ws)
