@@ -485,16 +485,16 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         CUtensorMap tm_dv;
         rc = make_btd_map(&tm_dv, dv, true, p.B, p.T, p.Hv, p.Dv, 64, 64);
         if (rc != GDN_OK) return rc;
-        CUtensorMap tm_dy, tm_rs;
+        CUtensorMap tm_dy, tm_qk;
         rc = make_colblock_map(&tm_dy, dy, true, p.B, p.T, p.Hv, p.Dv, 8, 128, 8, false);
         if (rc != GDN_OK) return rc;
-        rc = make_colblock_map(&tm_rs, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true);
+        rc = make_qkm_map(&tm_qk, const_cast<__nv_bfloat16 *>(cp.qkm), (size_t)p.B * p.Hk * p.NC, p.Dk);
         if (rc != GDN_OK) return rc;
         CUtensorMap tm_dq, tm_dk;
         if ((rc = make_btd_map(&tm_dq, dq, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK ||
             (rc = make_btd_map(&tm_dk, dk, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK)
             return rc;
-        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_rs, tm_dq, tm_dk, p.Dk, (cudaStream_t)stream));
+        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_qk, tm_dq, tm_dk, p.Dk, (cudaStream_t)stream));
     }
     const Workspace w = workspace_layout(p);
 

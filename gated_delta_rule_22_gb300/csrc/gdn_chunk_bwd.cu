@@ -69,28 +69,28 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 
 // ------------------------------------------------------------------ reverse sweep (dS)
 constexpr int kSweepMathWarps = 8;      // hold dS (M = 64 fragment: 4 lane quarters x 2 column halves)
-constexpr int kSweepThreads = 384;      // + a warpgroup whose first warp is the control warp
+constexpr int kSweepThreads = 384;      // + a warpgroup: warp 8 issues the products, warp 9 the copies and stores
 // registers: launched at 168 a thread; the control warpgroup gives up all but kSweepCtrlRegs,
 // the math warpgroups take kSweepMathRegs (2 x 128 x 216 + 128 x 72 = 384 x 168)
 constexpr int kSweepLaunchRegs = 168, kSweepMathRegs = 216, kSweepCtrlRegs = 72;
 static_assert(2 * 128 * kSweepMathRegs + 128 * kSweepCtrlRegs <= kSweepThreads * kSweepLaunchRegs, "register split");
 
 struct DSweepSmem {
-    size_t qk, tm, pkm, ydu, yds, rsm, lms, shl, rhs, dls, dvs, bar, tslot, total;
+    size_t qb, kb, tm, pkm, ydu, yds, lms, shl, rhs, dls, dvs, bar, tslot, total;
     __host__ __device__ DSweepSmem(int DK) {
         size_t o = 0;
-        qk = o; o += (size_t)2 * kL * DK * 2;    // [Q; K] [128][DK] (K-major rows 64-127: K; read MN-major whole)
-        tm = o; o += (size_t)kL * kL * 2;    // T [64][64] (read MN-major as T^T)
+        qb = o; o += (size_t)kL * DK * 2;        // Q of the chunk (kv head) [64][DK] (read MN-major by the carry)
+        kb = o; o += (size_t)2 * kL * DK * 2;    // K, two buffers [64][DK] (K-major for K dS^T, MN-major for the carry)
+        tm = o; o += (size_t)kL * kL * 2;        // T [64][64] (read MN-major as T^T)
         pkm = o; o += (size_t)2 * kL * kL * 2;   // [P; KKm] [128][64], P = (Q K^T) o E_incl (read MN-major)
         ydu = o; o += (size_t)2 * 2 * kL * kL * 2;   // [dY; dU] block [128][64 v] (rows 0-63 dY, 64-127 dU), two buffers
         yds = o; o += (size_t)2 * kL * kL * 2;       // [diag(exp Lam) dY; diag(exp Lam) dU] [128][64 v] (read MN-major)
-        rsm = alb(o, 1024); o = rsm + (size_t)2 * kL * 128;   // v - u block, fp32: two [64 t][32 v] boxes in the 128-byte swizzle
         lms = o; o += (size_t)2 * kL * 4;        // Lam, two buffers
         shl = o; o += (size_t)2 * kL * DK * 2;   // dS as bf16 parts: high [64][DK], then low (dS - high) [64][DK]
-        rhs = o; o += (size_t)kL * kL * 2;   // diag(E_L) K dS^T + P^T dY [64 t][64 v]
-        dls = o; o += (size_t)kL * kL * 2;   // Delta block [64 t][64 v], for the gradient kernel
+        rhs = o; o += (size_t)kL * kL * 2;       // diag(E_L) K dS^T + P^T dY [64 t][64 v]
+        dls = o; o += (size_t)kL * kL * 2;       // Delta block [64 t][64 v], for the gradient kernel
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
-        bar = alb(o, 8); o = bar + 13 * 8;   // see the kernel
+        bar = alb(o, 8); o = bar + 16 * 8;       // see the kernel
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -102,32 +102,35 @@ struct DSweepSmem {
 // One CTA per (block of 64 value rows, value head, batch row), over the chunks in reverse.
 // Warps 0-7 hold the adjoint dS (fp32, registers: the 16x256b fragment of an M = 64
 // accumulator, 2 rows x DK/8 columns per thread) and do the element-wise work; warp 8 issues
-// the products (one elected lane), the copies and the stores, so that no math warp stalls on an
-// issue and no block barrier runs per chunk: each hand-off is an mbarrier. Per chunk the products
-// are (fp32 accumulators in tensor memory, M = 64 layout: row r in lane r % 16 + 32 (r / 16)):
-//   [0, DK)              the chunk's part of the carry, [e^Lam dY; e^Lam dU]^T [Q; K]; the
+// the products (one elected lane) and warp 9 the copies and stores, so that no math warp stalls
+// on an issue and no block barrier runs per chunk: every hand-off is an mbarrier. Per chunk the
+// products are (fp32 accumulators in tensor memory, M = 64 layout: row r in lane
+// r % 16 + 32 (r / 16)):
+//   [0, DK)              the chunk's part of the carry, (e^Lam dY)^T Q + (e^Lam dU)^T K; the
 //                        next chunk's dS = exp(Lam_L) dS + this
 //   [DK, DK + 64)        K dS_high^T + K dS_low^T (chunk row t, value column; the two parts
 //                        accumulate in fp32); then dD
 //   [DK + 128, DK + 192) P^T dY
 // Hand-offs of chunk c (each completes once per chunk):
-//   math -> control (8 warp arrivals): bH  dS parts written;  bR  rhs and Delta written, v - u
-//                                      read;  bU  dU, [e^Lam dY; e^Lam dU], dv written
+//   math -> control (8 warp arrivals): bH  dS parts written;  bR  rhs and Delta written;
+//                                      bU  dU, [e^Lam dY; e^Lam dU] and dv written
 //   control -> math: m1, mD, mS  the product groups (commits);  fS  the dS parts' tile is free
 //                    (products done, the dS_L store has read it);  fO  the Delta and dv staging
 //                    tiles are free (their stores have read them)
-// dbeta and f leave as one partial per 32 value columns (the two column halves of the block).
+// Q and K arrive as separate [64][DK] tiles (boxes of the [Q; K] block), K double-buffered and
+// fetched two chunks ahead. v - u is read by the math threads straight into registers, a chunk
+// ahead. dbeta and f leave as one partial per 32 value columns (the two column halves).
 template <int E>
 __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwdParams p,
                                                                         const __grid_constant__ CUtensorMap tm_dv,
                                                                         const __grid_constant__ CUtensorMap tm_dy,
-                                                                        const __grid_constant__ CUtensorMap tm_rs) {
+                                                                        const __grid_constant__ CUtensorMap tm_qk) {
     constexpr int DK = 32 * E;
     constexpr int SC = DK / 2;                // dS columns per warp half
     constexpr int NS = SC / 2;                // dS values per thread
     static_assert(DK + 192 <= 512, "tensor memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool math = warp < kSweepMathWarps, ctrl = warp == kSweepMathWarps;
+    const bool math = warp < kSweepMathWarps;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, NC = p.NC, r0 = split * kL, nsplit = p.nsplit;
     const int hw = (warp >> 2) & 1;                             // warp half: value columns [32 hw, 32 hw + 32)
@@ -136,32 +139,33 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
     const DSweepSmem L(DK);
-    unsigned char *qk = base + L.qk, *tmm = base + L.tm, *pmm = base + L.pkm, *yds = base + L.yds;
+    unsigned char *qb = base + L.qb, *kb2 = base + L.kb, *tmm = base + L.tm, *pmm = base + L.pkm, *yds = base + L.yds;
     unsigned char *ydu2 = base + L.ydu, *shl = base + L.shl, *rhs = base + L.rhs, *dls = base + L.dls;
-    unsigned char *dvs = base + L.dvs, *rsm = base + L.rsm;
+    unsigned char *dvs = base + L.dvs;
     float *lms = reinterpret_cast<float *>(base + L.lms);
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
-    uint64_t *m1 = bar, *mD = bar + 1, *mS = bar + 2, *cbA = bar + 3, *cbT = bar + 4, *cbK = bar + 5, *cbY = bar + 6;
-    uint64_t *bH = bar + 7, *bR = bar + 8, *bU = bar + 9, *fS = bar + 10, *fO = bar + 11, *mX = bar + 12;
+    uint64_t *m1 = bar, *mD = bar + 1, *mS = bar + 2, *cbA = bar + 3, *cbT = bar + 4, *cbQ = bar + 5, *cbY = bar + 6;
+    uint64_t *cbK = bar + 7;                                    // [2]
+    uint64_t *bH = bar + 9, *bR = bar + 10, *bU = bar + 11, *fS = bar + 12, *fO = bar + 13, *mX = bar + 14;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
+    auto kbuf = [&](int k) { return kb2 + (size_t)(k & 1) * kL * DK * 2; };   // K of the chunk handled k-th
 
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t head = (size_t)b * Hv + h;
+    const int qkblk0 = (b * p.Hk + h / (Hv / p.Hk)) * NC;     // [Q; K] block of chunk 0 of this kv head
 
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(bar + i, 1);
-        for (int i = 7; i < 10; ++i) mbar_init(bar + i, kSweepMathWarps);
-        for (int i = 10; i < 13; ++i) mbar_init(bar + i, 1);
+        for (int i = 0; i < 9; ++i) mbar_init(bar + i, 1);
+        for (int i = 9; i < 12; ++i) mbar_init(bar + i, kSweepMathWarps);
+        for (int i = 12; i < 15; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
     }
-    if (ctrl) {
-        if (lane == 0) {
-            tma_prefetch_map(&tm_dy);
-            tma_prefetch_map(&tm_rs);
-            tma_prefetch_map(&tm_dv);
-        }
-        tmem_alloc(tslot, 512);
+    if (warp == kSweepMathWarps + 1 && lane == 0) {
+        tma_prefetch_map(&tm_dy);
+        tma_prefetch_map(&tm_qk);
+        tma_prefetch_map(&tm_dv);
     }
+    if (warp == kSweepMathWarps) tmem_alloc(tslot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -171,120 +175,135 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
     griddep_launch();
 
     bool fail = false;
-    if (!math) regs_dec<kSweepCtrlRegs>();
-    else regs_inc<kSweepMathRegs>();
-    if (ctrl) {
-        // ================================================================ control warp
-        const uint32_t lead = elect_one_sync();               // issues the products
-        const bool io = lane == 0;                            // issues the copies and the stores
-        int nA = 0, nT = 0, nK = 0, nY = 0;
-        auto copy_A = [&](int cc) {                          // [P; KKm] of chunk cc
-            mbar_expect_tx(cbA, 2 * kL * kL * 2);
-            bulk_load(pmm, p.pkm + (head * NC + cc) * 2 * kL * kL, 2 * kL * kL * 2, cbA);
-        };
-        auto copy_T = [&](int cc) {                          // T of chunk cc
-            mbar_expect_tx(cbT, kL * kL * 2);
-            bulk_load(tmm, p.tm + (head * NC + cc) * kL * kL, kL * kL * 2, cbT);
-        };
-        auto copy_K = [&](int cc) {                          // [Q; K] of chunk cc (kv head)
-            mbar_expect_tx(cbK, 2 * kL * DK * 2);
-            bulk_load(qk, p.qkm + (((size_t)b * p.Hk + h / (Hv / p.Hk)) * NC + cc) * 2 * kL * DK, 2 * kL * DK * 2, cbK);
-        };
-        // dY (one 128-row box in the [dY; dU] layout: rows 64-127, the following steps, land in
-        // the dU rows, which the math warps rewrite before anything reads them), v - u (one box
-        // of two 128-byte-swizzled [64][32] tiles) and Lam of chunk cc (rows past T: zeros)
-        auto fetch = [&](int cc, int buf) {
-            const int tt0 = cc * kL;
-            mbar_expect_tx(cbY, 2 * kL * kL * 2 + kL * kL * 4 + kL * 4);
-            tma_load_5d(ydu2 + (size_t)buf * 2 * kL * kL * 2, &tm_dy, cbY, 0, tt0, r0 / 8, h, b);
-            tma_load_5d(rsm, &tm_rs, cbY, 0, tt0, r0 / 32, h, b);
-            bulk_load(lms + buf * kL, p.lam + (head * NC + cc) * kL, kL * 4, cbY);
-        };
-        if (io) {
-            copy_A(NC - 1);
-            copy_T(NC - 1);
-            copy_K(NC - 1);
-            fetch(NC - 1, 0);
+    if (!math) {
+        regs_dec<kSweepCtrlRegs>();            // the whole control warpgroup, at one point of the code
+        if (warp == kSweepMathWarps) {
+            // ================================================================ product warp
+            const uint32_t lead = elect_one_sync();
+            for (int k = 0; k < NC; ++k) {
+                const int buf = k & 1;
+                unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2, *kb = kbuf(k);
+                // ---- K dS_high^T + K dS_low^T, P^T dY once the dS parts are written and the operands landed
+                bool w = mbar_wait(bH, k & 1) && mbar_wait(cbA, k & 1) && mbar_wait(cbK + buf, (k >> 1) & 1) &&
+                         mbar_wait(cbY, k & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+                {
+                    constexpr uint32_t idX = umma_idesc(1, kL, kL);
+                    constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
+                    umma_gemm_w(tX, CmOp{kb, kL, 0, 0, false}, CmOp{shl, kL, 0, 0, false}, DK, idX, false, lead);
+                    umma_gemm_w(tX, CmOp{kb, kL, 0, 0, false}, CmOp{shl + kL * DK * 2, kL, 0, 0, false}, DK, idX, true, lead);
+                    umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false, lead);
+                    umma_commit_w(m1, lead);
+                }
+                // ---- dD = T^T rhs once rhs is written
+                w = mbar_wait(bR, k & 1) && mbar_wait(cbT, k & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+                umma_gemm_w(tX, CmOp{tmm, kL, 0, 0, true}, CmOp{rhs, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, kL, true, true),
+                            false, lead);
+                umma_commit_w(mD, lead);
+                // ---- the carry once dU and the carry's operands are written
+                w = mbar_wait(bU, k & 1) && mbar_wait(cbQ, k & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+                {
+                    constexpr uint32_t idS = umma_idesc_t(1, kL, DK, true, true);
+                    umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, 0, true}, CmOp{qb, kL, 0, 0, true}, kL, idS, false, lead);
+                    umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, kL, true}, CmOp{kb, kL, 0, 0, true}, kL, idS, true, lead);
+                    umma_commit_w(mS, lead);
+                }
+            }
+            if (fail) {
+                // products still in flight finish before the tensor memory is freed (bounded wait)
+                umma_commit_w(mX, lead);
+                mbar_wait(mX, 0);
+            }
+        } else if (warp == kSweepMathWarps + 1) {
+            // ================================================================ copy warp (lane 0)
+            if (lane == 0) {
+                int nA = 0, nT = 0, nQ = 0, nK0 = 0, nK1 = 0, nY = 0;
+                auto copy_A = [&](int cc) {                      // [P; KKm] of chunk cc
+                    mbar_expect_tx(cbA, 2 * kL * kL * 2);
+                    bulk_load(pmm, p.pkm + (head * NC + cc) * 2 * kL * kL, 2 * kL * kL * 2, cbA);
+                    ++nA;
+                };
+                auto copy_T = [&](int cc) {                      // T of chunk cc
+                    mbar_expect_tx(cbT, kL * kL * 2);
+                    bulk_load(tmm, p.tm + (head * NC + cc) * kL * kL, kL * kL * 2, cbT);
+                    ++nT;
+                };
+                auto copy_Q = [&](int cc) {                      // Q of chunk cc: rows 0-63 of its [Q; K] block
+                    mbar_expect_tx(cbQ, kL * DK * 2);
+                    tma_load_5d(qb, &tm_qk, cbQ, 0, 0, 0, 0, qkblk0 + cc);
+                    ++nQ;
+                };
+                auto copy_K = [&](int kk) {                      // K of the chunk handled kk-th: rows 64-127
+                    mbar_expect_tx(cbK + (kk & 1), kL * DK * 2);
+                    tma_load_5d(kbuf(kk), &tm_qk, cbK + (kk & 1), 0, 0, 0, 1, qkblk0 + NC - 1 - kk);
+                    if (kk & 1) ++nK1; else ++nK0;
+                };
+                // dY (one 128-row box in the [dY; dU] layout: rows 64-127, the following steps, land in
+                // the dU rows, which the math warps rewrite before anything reads them) and Lam of
+                // chunk cc (rows past T: zeros)
+                auto fetch = [&](int cc, int buf) {
+                    mbar_expect_tx(cbY, 2 * kL * kL * 2 + kL * 4);
+                    tma_load_5d(ydu2 + (size_t)buf * 2 * kL * kL * 2, &tm_dy, cbY, 0, cc * kL, r0 / 8, h, b);
+                    bulk_load(lms + buf * kL, p.lam + (head * NC + cc) * kL, kL * 4, cbY);
+                    ++nY;
+                };
+                copy_K(0);
+                fetch(NC - 1, 0);
+                copy_A(NC - 1);
+                if (NC > 1) copy_K(1);
+                copy_T(NC - 1);
+                copy_Q(NC - 1);
+                for (int k = 0; k < NC; ++k) {
+                    const int c = NC - 1 - k, buf = k & 1;
+                    const size_t chk = head * NC + c, blk = chk * nsplit + split;
+                    unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;
+                    // dS_L (high part) for the gradient kernel once written
+                    if (!mbar_wait(bH, k & 1)) { fail = true; break; }
+                    bulk_store(p.ws_dsl + blk * kL * DK, shl, kL * DK * 2);
+                    bulk_commit();
+                    // rhs written: the math warps saw m1, so [P; KKm] is free; the next chunk's dY and
+                    // Lam go to the other buffers (its [dY; dU] was stored and read out, see fO)
+                    if (!mbar_wait(bR, k & 1)) { fail = true; break; }
+                    if (c > 0) {
+                        copy_A(c - 1);
+                        fetch(c - 1, buf ^ 1);
+                    }
+                    bulk_wait_read();                           // the dS_L store has read the dS parts
+                    mbar_arrive(fS);
+                    // dU written: the math warps saw mD, so T is free; the block's outputs leave
+                    if (!mbar_wait(bU, k & 1)) { fail = true; break; }
+                    if (c > 0) copy_T(c - 1);
+                    bulk_store(p.ws_yu + blk * 2 * kL * kL, ydu, 2 * kL * kL * 2);
+                    bulk_store(p.ws_dl + blk * kL * kL, dls, kL * kL * 2);
+                    tma_store_4d(&tm_dv, dvs, r0, h, c * kL, b);
+                    bulk_commit();
+                    // the carry is done: Q, and this chunk's K buffer (for the chunk two ahead), are free
+                    if (!mbar_wait(mS, k & 1)) { fail = true; break; }
+                    if (c > 0) copy_Q(c - 1);
+                    if (k + 2 < NC) copy_K(k + 2);
+                    bulk_wait_read();                           // [dY; dU], Delta and dv staging read out
+                    mbar_arrive(fO);
+                }
+                if (fail) {
+                    // copies still in flight land before the CTA exits (each wait bounded)
+                    if (nA > 0) mbar_wait(cbA, (nA - 1) & 1);
+                    if (nT > 0) mbar_wait(cbT, (nT - 1) & 1);
+                    if (nQ > 0) mbar_wait(cbQ, (nQ - 1) & 1);
+                    if (nK0 > 0) mbar_wait(cbK, (nK0 - 1) & 1);
+                    if (nK1 > 0) mbar_wait(cbK + 1, (nK1 - 1) & 1);
+                    if (nY > 0) mbar_wait(cbY, (nY - 1) & 1);
+                }
+                bulk_wait_all();                                // the block outputs are complete
+            }
+            fail = __shfl_sync(kFullMask, fail, 0);
         }
-        nA = nT = nK = nY = 1;
-        for (int k = 0; k < NC; ++k) {
-            const int c = NC - 1 - k, buf = k & 1;
-            const size_t chk = head * NC + c, blk = chk * nsplit + split;
-            unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;
-            // ---- K dS_high^T + K dS_low^T, P^T dY once the dS parts are written and the operands landed
-            bool w = mbar_wait(bH, k & 1);
-            if (io && w) {
-                bulk_store(p.ws_dsl + blk * kL * DK, shl, kL * DK * 2);   // dS_L (high part) for the gradient kernel
-                bulk_commit();
-            }
-            w = w && mbar_wait(cbA, k & 1) && mbar_wait(cbK, k & 1) && mbar_wait(cbY, k & 1);
-            if (__any_sync(kFullMask, !w)) { fail = true; break; }
-            tc_fence_after();
-            {
-                constexpr uint32_t idX = umma_idesc(1, kL, kL);
-                constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
-                umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl, kL, 0, 0, false}, DK, idX, false, lead);
-                umma_gemm_w(tX, CmOp{qk, 2 * kL, kL, 0, false}, CmOp{shl + kL * DK * 2, kL, 0, 0, false}, DK, idX, true,
-                            lead);
-                umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false, lead);
-                umma_commit_w(m1, lead);
-            }
-            // ---- dD = T^T rhs once rhs is written (the math warps saw m1: [P; KKm] is free, and
-            // they have read v - u)
-            w = mbar_wait(bR, k & 1);
-            if (io && w) {
-                if (c > 0) { copy_A(c - 1); ++nA; }
-                bulk_wait_read();                           // the dS_L store (and the earlier ones) have read their tiles
-                mbar_arrive(fS);                            // the products that read the dS parts are done (m1)
-            }
-            w = w && mbar_wait(cbT, k & 1);
-            if (__any_sync(kFullMask, !w)) { fail = true; break; }
-            tc_fence_after();
-            umma_gemm_w(tX, CmOp{tmm, kL, 0, 0, true}, CmOp{rhs, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, kL, true, true),
-                        false, lead);
-            umma_commit_w(mD, lead);
-            // the next chunk's dY, v - u and Lam: its [dY; dU] buffer was stored and read out
-            // (bulk_wait_read above), and v - u was read (bR)
-            if (io && c > 0) { fetch(c - 1, buf ^ 1); ++nY; }
-            // ---- the carry once dU and the operands of the carry are written (the math warps
-            // saw mD: T is free)
-            w = mbar_wait(bU, k & 1);
-            if (__any_sync(kFullMask, !w)) { fail = true; break; }
-            tc_fence_after();
-            umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, 0, true}, CmOp{qk, 2 * kL, 0, 0, true}, 2 * kL,
-                        umma_idesc_t(1, kL, DK, true, true), false, lead);
-            umma_commit_w(mS, lead);
-            if (io) {
-                if (c > 0) { copy_T(c - 1); ++nT; }
-                // [dY; dU] and Delta of the block for the gradient kernel, and dv
-                bulk_store(p.ws_yu + blk * 2 * kL * kL, ydu, 2 * kL * kL * 2);
-                bulk_store(p.ws_dl + blk * kL * kL, dls, kL * kL * 2);
-                tma_store_4d(&tm_dv, dvs, r0, h, c * kL, b);
-                bulk_commit();
-            }
-            // [Q; K] is free once the carry is done
-            w = mbar_wait(mS, k & 1);
-            if (io && w) {
-                if (c > 0) { copy_K(c - 1); ++nK; }
-                bulk_wait_read();                           // Delta and dv staging read out
-                mbar_arrive(fO);
-            }
-            if (__any_sync(kFullMask, !w)) { fail = true; break; }
-        }
-        if (fail) {
-            if (io) {
-                // copies still in flight land before the CTA exits (each wait bounded)
-                mbar_wait(cbA, (nA - 1) & 1);
-                mbar_wait(cbT, (nT - 1) & 1);
-                mbar_wait(cbK, (nK - 1) & 1);
-                mbar_wait(cbY, (nY - 1) & 1);
-            }
-            // products still in flight finish before the tensor memory is freed (bounded wait)
-            umma_commit_w(mX, lead);
-            mbar_wait(mX, 0);
-        }
-        if (io) bulk_wait_all();                            // the block outputs are complete
-    } else if (math) {
+    } else {
+        regs_inc<kSweepMathRegs>();
         // ================================================================ math warps
         // this thread's fragment of dS (rows fs.row(k), columns fs.col(j, k)), from dS_T
         const M64Frag fs(warp, lane, DK);
@@ -302,19 +321,22 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
         // this thread's fragment of the 64-column accumulators (chunk rows ta, tb, value columns)
         const M64Frag fd(warp, lane, kL);
         const int ta = fd.row(0), tb = fd.row(2);
-        // beta of rows ta, tb: loaded one chunk ahead, kept raw until used
-        auto load_beta = [&](int cc, __nv_bfloat16 &xa, __nv_bfloat16 &xb) {
+        // beta and v - u of rows ta, tb (value columns fd.col(j, 0), + 1): loaded one chunk ahead,
+        // kept raw until used (rows past T: zeros)
+        __nv_bfloat16 bna, bnb;
+        float2 rna[4], rnb[4];
+        auto load_rows = [&](int cc) {
             const int tt0 = cc * kL, ln = min(kL, T - tt0);
             const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
-            xa = ta < ln ? beta[((size_t)b * T + tt0 + ta) * Hv + h] : z;
-            xb = tb < ln ? beta[((size_t)b * T + tt0 + tb) * Hv + h] : z;
-        };
-        // v - u of the thread's fragment: row t, value columns fd.col(j, 0), + 1 (box hw of rsm: row
-        // t at t * 128, 16-byte chunk (col % 32) / 4 at chunk ^ (t % 8))
-        auto rs_pair = [&](int t, int j) {
-            const int c32 = 8 * j + 2 * (lane & 3);
-            return *reinterpret_cast<const float2 *>(rsm + hw * (kL * 128) + t * 128 + (((c32 >> 2) ^ (t & 7)) << 4) +
-                                                     (c32 & 3) * 4);
+            const size_t ra = ((size_t)b * T + tt0 + ta) * Hv + h, rb = ((size_t)b * T + tt0 + tb) * Hv + h;
+            bna = ta < ln ? beta[ra] : z;
+            bnb = tb < ln ? beta[rb] : z;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = r0 + fd.col(j, 0);
+                rna[j] = ta < ln ? *reinterpret_cast<const float2 *>(p.resid + ra * Dv + col) : make_float2(0.f, 0.f);
+                rnb[j] = tb < ln ? *reinterpret_cast<const float2 *>(p.resid + rb * Dv + col) : make_float2(0.f, 0.f);
+            }
         };
         // a warp's part is written: its lanes' shared-memory writes are visible to the
         // products and copies, and its tensor-memory reads are complete
@@ -324,8 +346,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_);
         };
-        __nv_bfloat16 bna, bnb;
-        load_beta(NC - 1, bna, bnb);
+        load_rows(NC - 1);
         float decay_next = 1.f;                       // exp(Lam_L) of the chunk processed before (later in time)
         for (int k = 0; k < NC; ++k) {
             const int c = NC - 1 - k, buf = k & 1;
@@ -334,7 +355,13 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
             unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;   // [dY; dU] of this chunk
             const float *lmb = lms + buf * kL;                 // Lam of this chunk
             const float ba = __bfloat162float(bna), bb = __bfloat162float(bnb);
-            if (c > 0) load_beta(c - 1, bna, bnb);
+            float2 rsa[4], rsb[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                rsa[j] = rna[j];
+                rsb[j] = rnb[j];
+            }
+            if (c > 0) load_rows(c - 1);
             // ---- dS of this chunk's end: exp(Lam_L) dS + the later chunk's part of the carry
             if (k > 0) {
                 const bool w = mbar_wait(mS, (k - 1) & 1);
@@ -353,7 +380,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
                 if (__any_sync(kFullMask, !w2)) { fail = true; break; }
             }
             // ---- dS as operands: a bf16 high part and a bf16 low part (dS - high), each [64][DK]; the
-            // high part also leaves for the gradient kernel (a bulk store by the control warp)
+            // high part also leaves for the gradient kernel (a bulk store by the copy warp)
 #pragma unroll
             for (int j = 0; j < NS / 4; ++j)
 #pragma unroll
@@ -367,17 +394,10 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
                     *reinterpret_cast<uint32_t *>(shl + kL * DK * 2 + o) = pack2_bf16(x0 - h0, x1 - h1);
                 }
             warp_done(bH);
-            // ---- this chunk's dY, v - u and Lam
+            // ---- this chunk's dY and Lam
             {
                 const bool w = mbar_wait(cbY, k & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
-            }
-            // this thread's v - u (rows ta, tb), read before the next chunk's copy overwrites rsm
-            float2 rsa[4], rsb[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                rsa[j] = rs_pair(ta, j);
-                rsb[j] = rs_pair(tb, j);
             }
             const float ela = expf(lmb[kL - 1] - lmb[ta]), elb = expf(lmb[kL - 1] - lmb[tb]);
             const float ga = expf(lmb[ta]), gb = expf(lmb[tb]);
@@ -503,7 +523,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (ctrl) tmem_dealloc(tmem, 512);
+    if (warp == kSweepMathWarps) tmem_dealloc(tmem, 512);
 }
 
 namespace {
@@ -979,7 +999,7 @@ size_t chunk_grad_smem(int Dk, int Dv) { return GradSmem(Dk, Dv).total; }
 
 template <int E>
 static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
-                                      const CUtensorMap &tm_rs, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk,
+                                      const CUtensorMap &tm_qk, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk,
                                       cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sd = DSweepSmem(DK).total, sg = GradSmem(DK, p.Dv).total;
@@ -995,7 +1015,7 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     if (err != cudaSuccess) return err;
     timing_mark("chunk_dsweep", 0, s);
     err = launch_pdl(chunk_dsweep_kernel<E>, dim3(p.nsplit, p.Hv, p.B), dim3(kSweepThreads), sd, s, p, tm_dv, tm_dy,
-                     tm_rs);
+                     tm_qk);
     timing_mark("chunk_dsweep", 1, s);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_grad", 0, s);
@@ -1012,12 +1032,12 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
 }
 
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
-                             const CUtensorMap &tm_rs, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk, int Dk,
+                             const CUtensorMap &tm_qk, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk, int Dk,
                              cudaStream_t s) {
     switch (Dk) {
-        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, tm_dy, tm_rs, tm_dq, tm_dk, s);
-        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, tm_dy, tm_rs, tm_dq, tm_dk, s);
-        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_rs, tm_dq, tm_dk, s);
+        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, tm_dy, tm_qk, tm_dq, tm_dk, s);
+        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, tm_dy, tm_qk, tm_dq, tm_dk, s);
+        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_qk, tm_dq, tm_dk, s);
         default: return cudaErrorInvalidValue;
     }
 }

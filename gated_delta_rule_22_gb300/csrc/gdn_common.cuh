@@ -501,11 +501,11 @@ size_t chunk_sweep_smem(int Dk);
 // and the fixed-order sums over value heads and row blocks.
 // Tensor maps of [B][T][Hv][Dv] tensors: tm_dv dv (bf16, 4-D, box {64, 1, 64, 1}, 128-byte
 // swizzle); tm_dy dy (bf16, 5-D column blocks {8, T, Dv / 8, Hv, B}, box {8, 128, 8, 1, 1}, no
-// swizzle); tm_rs v - u (fp32, 5-D column blocks {32, T, Dv / 32, Hv, B}, box
+// swizzle); tm_qk v - u (fp32, 5-D column blocks {32, T, Dv / 32, Hv, B}, box
 // {32, 64, 2, 1, 1}, 128-byte swizzle).
 // tm_dq, tm_dk: dq and dk as [B][T][Hk][Dk] bf16, 4-D, box {64, 1, 64, 1}, 128-byte swizzle.
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
-                             const CUtensorMap &tm_rs, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk, int Dk,
+                             const CUtensorMap &tm_qk, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk, int Dk,
                              cudaStream_t s);
 size_t chunk_dsweep_smem(int Dk);
 size_t chunk_grad_smem(int Dk, int Dv);
