@@ -71,8 +71,8 @@ constexpr size_t kOneCtaSmem = 120 * 1024;
 constexpr int kSweepMathWarps = 8;      // hold dS (M = 64 fragment: 4 lane quarters x 2 column halves)
 constexpr int kSweepThreads = 384;      // + a warpgroup: warp 8 issues the products, warp 9 the copies and stores
 // registers: launched at 168 a thread; the control warpgroup gives up all but kSweepCtrlRegs,
-// the math warpgroups take kSweepMathRegs (2 x 128 x 216 + 128 x 72 = 384 x 168)
-constexpr int kSweepLaunchRegs = 168, kSweepMathRegs = 216, kSweepCtrlRegs = 72;
+// the math warpgroups take kSweepMathRegs (2 x 128 x 176 + 128 x 152 = 384 x 168)
+constexpr int kSweepLaunchRegs = 168, kSweepMathRegs = 176, kSweepCtrlRegs = 152;
 static_assert(2 * 128 * kSweepMathRegs + 128 * kSweepCtrlRegs <= kSweepThreads * kSweepLaunchRegs, "register split");
 
 struct DSweepSmem {
@@ -180,22 +180,28 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
         if (warp == kSweepMathWarps) {
             // ================================================================ product warp
             const uint32_t lead = elect_one_sync();
-            for (int k = 0; k < NC; ++k) {
-                const int buf = k & 1;
-                unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2, *kb = kbuf(k);
-                // ---- K dS_high^T + K dS_low^T, P^T dY once the dS parts are written and the operands landed
-                bool w = mbar_wait(bH, k & 1) && mbar_wait(cbA, k & 1) && mbar_wait(cbK + buf, (k >> 1) & 1) &&
-                         mbar_wait(cbY, k & 1);
+            constexpr uint32_t idX = umma_idesc(1, kL, kL);
+            constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
+            constexpr uint32_t idS = umma_idesc_t(1, kL, DK, true, true);
+            // P^T dY needs no dS: each chunk's is issued a chunk ahead (the first one here), so that
+            // only K dS^T is on the path from dS to the next chunk
+            {
+                const bool w = mbar_wait(cbA, 0) && mbar_wait(cbY, 0);
+                fail = __any_sync(kFullMask, !w);
+                if (!fail) {
+                    tc_fence_after();
+                    umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu2, 2 * kL, 0, 0, true}, kL, idP, false, lead);
+                }
+            }
+            for (int k = 0; k < NC && !fail; ++k) {
+                unsigned char *kb = kbuf(k);
+                // ---- K dS_high^T + K dS_low^T once the dS parts are written and K landed
+                bool w = mbar_wait(bH, k & 1) && mbar_wait(cbK + (k & 1), (k >> 1) & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
-                {
-                    constexpr uint32_t idX = umma_idesc(1, kL, kL);
-                    constexpr uint32_t idP = umma_idesc_t(1, kL, kL, true, true);
-                    umma_gemm_w(tX, CmOp{kb, kL, 0, 0, false}, CmOp{shl, kL, 0, 0, false}, DK, idX, false, lead);
-                    umma_gemm_w(tX, CmOp{kb, kL, 0, 0, false}, CmOp{shl + kL * DK * 2, kL, 0, 0, false}, DK, idX, true, lead);
-                    umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu, 2 * kL, 0, 0, true}, kL, idP, false, lead);
-                    umma_commit_w(m1, lead);
-                }
+                umma_gemm_w(tX, CmOp{kb, kL, 0, 0, false}, CmOp{shl, kL, 0, 0, false}, DK, idX, false, lead);
+                umma_gemm_w(tX, CmOp{kb, kL, 0, 0, false}, CmOp{shl + kL * DK * 2, kL, 0, 0, false}, DK, idX, true, lead);
+                umma_commit_w(m1, lead);
                 // ---- dD = T^T rhs once rhs is written
                 w = mbar_wait(bR, k & 1) && mbar_wait(cbT, k & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
@@ -203,15 +209,25 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
                 umma_gemm_w(tX, CmOp{tmm, kL, 0, 0, true}, CmOp{rhs, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, kL, true, true),
                             false, lead);
                 umma_commit_w(mD, lead);
-                // ---- the carry once dU and the carry's operands are written
-                w = mbar_wait(bU, k & 1) && mbar_wait(cbQ, k & 1);
+                // ---- the carry: its dY part (e^Lam dY)^T Q now (its operand rows were written before
+                // bR; the math warps read the later chunk's carry before bH), its dU part
+                // (e^Lam dU)^T K once dU is written
+                w = mbar_wait(cbQ, k & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, 0, true}, CmOp{qb, kL, 0, 0, true}, kL, idS, false, lead);
+                w = mbar_wait(bU, k & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
-                {
-                    constexpr uint32_t idS = umma_idesc_t(1, kL, DK, true, true);
-                    umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, 0, true}, CmOp{qb, kL, 0, 0, true}, kL, idS, false, lead);
-                    umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, kL, true}, CmOp{kb, kL, 0, 0, true}, kL, idS, true, lead);
-                    umma_commit_w(mS, lead);
+                umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, kL, true}, CmOp{kb, kL, 0, 0, true}, kL, idS, true, lead);
+                umma_commit_w(mS, lead);
+                // ---- P^T dY of the next chunk: its [P; KKm] and dY landed (copied after bR), and the
+                // math warps read this chunk's (before bR)
+                if (k + 1 < NC) {
+                    w = mbar_wait(cbA, (k + 1) & 1) && mbar_wait(cbY, (k + 1) & 1);
+                    if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                    tc_fence_after();
+                    umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu2 + (size_t)((k + 1) & 1) * 2 * kL * kL * 2, 2 * kL, 0, 0, true},
+                                kL, idP, false, lead);
                 }
             }
             if (fail) {
@@ -382,17 +398,18 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
             // ---- dS as operands: a bf16 high part and a bf16 low part (dS - high), each [64][DK]; the
             // high part also leaves for the gradient kernel (a bulk store by the copy warp)
 #pragma unroll
-            for (int j = 0; j < NS / 4; ++j)
+            for (int j = 0; j < NS / 4; j += 2) {
+                uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int row = fs.row(2 * k2), col = fs.col(j, 0);
-                    const float x0 = dS[4 * j + 2 * k2], x1 = dS[4 * j + 2 * k2 + 1];
-                    const uint32_t hu = pack2_bf16(x0, x1);
-                    const float h0 = __uint_as_float(hu << 16), h1 = __uint_as_float(hu & 0xffff0000u);
-                    const uint32_t o = cm_off(row, 2 * col, kL);
-                    *reinterpret_cast<uint32_t *>(shl + o) = hu;
-                    *reinterpret_cast<uint32_t *>(shl + kL * DK * 2 + o) = pack2_bf16(x0 - h0, x1 - h1);
+                for (int m = 0; m < 4; ++m) {
+                    const float x0 = dS[4 * j + 2 * m], x1 = dS[4 * j + 2 * m + 1];
+                    hi[m] = pack2_bf16(x0, x1);
+                    lo[m] = pack2_bf16(x0 - __uint_as_float(hi[m] << 16), x1 - __uint_as_float(hi[m] & 0xffff0000u));
                 }
+                const uint32_t a = frag_row_addr(smem_addr(shl), kL, 16 * (warp & 3), (DK / 16) * hw + j, lane);
+                stmatrix_x4(a, hi[0], hi[1], hi[2], hi[3]);
+                stmatrix_x4(a + kL * DK * 2, lo[0], lo[1], lo[2], lo[3]);
+            }
             warp_done(bH);
             // ---- this chunk's dY and Lam
             {
@@ -428,18 +445,23 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
                 tmem_ld16x256_x4(tP + lane16 + 32 * hw, pp);
                 tmem_wait_ld();
                 float fa = 0.f, fb = 0.f;
+                uint32_t rv[8], dl[8];   // pairs (j, row ta), (j, row tb) for j = 0..3
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float2 ra = rsa[j], rb = rsb[j];
                     const float x0 = xh[4 * j], x1 = xh[4 * j + 1], x2 = xh[4 * j + 2], x3 = xh[4 * j + 3];
                     fa = fmaf(ra.x, x0, fmaf(ra.y, x1, fa));
                     fb = fmaf(rb.x, x2, fmaf(rb.y, x3, fb));
-                    const int col = fd.col(j, 0);
-                    const uint32_t oa = cm_off(ta, 2 * col, kL), ob = cm_off(tb, 2 * col, kL);
-                    *reinterpret_cast<uint32_t *>(rhs + oa) = pack2_bf16(fmaf(ela, x0, pp[4 * j]), fmaf(ela, x1, pp[4 * j + 1]));
-                    *reinterpret_cast<uint32_t *>(rhs + ob) = pack2_bf16(fmaf(elb, x2, pp[4 * j + 2]), fmaf(elb, x3, pp[4 * j + 3]));
-                    *reinterpret_cast<uint32_t *>(dls + oa) = pack2_bf16(ba * ra.x, ba * ra.y);
-                    *reinterpret_cast<uint32_t *>(dls + ob) = pack2_bf16(bb * rb.x, bb * rb.y);
+                    rv[2 * j] = pack2_bf16(fmaf(ela, x0, pp[4 * j]), fmaf(ela, x1, pp[4 * j + 1]));
+                    rv[2 * j + 1] = pack2_bf16(fmaf(elb, x2, pp[4 * j + 2]), fmaf(elb, x3, pp[4 * j + 3]));
+                    dl[2 * j] = pack2_bf16(ba * ra.x, ba * ra.y);
+                    dl[2 * j + 1] = pack2_bf16(bb * rb.x, bb * rb.y);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; j += 2) {
+                    const uint32_t o = frag_row_addr(0, kL, 16 * (warp & 3), 4 * hw + j, lane);
+                    stmatrix_x4(smem_addr(rhs) + o, rv[2 * j], rv[2 * j + 1], rv[2 * j + 2], rv[2 * j + 3]);
+                    stmatrix_x4(smem_addr(dls) + o, dl[2 * j], dl[2 * j + 1], dl[2 * j + 2], dl[2 * j + 3]);
                 }
                 warp_done(bR);
                 // the row sums over this warp's 32 columns: the four lanes that share a row
@@ -465,24 +487,32 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
                 tmem_ld16x256_x4(tX + lane16 + 32 * hw, x);
                 tmem_wait_ld();
                 float da = 0.f, db = 0.f;
+                uint32_t du[8], us[8], dv[8];   // pairs (j, row ta), (j, row tb) for j = 0..3
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float2 ra = rsa[j], rb = rsb[j];
                     da = fmaf(x[4 * j], ra.x, fmaf(x[4 * j + 1], ra.y, da));
                     db = fmaf(x[4 * j + 2], rb.x, fmaf(x[4 * j + 3], rb.y, db));
-                    const int col = fd.col(j, 0);
                     const float va0 = ba * x[4 * j], va1 = ba * x[4 * j + 1], vb0 = bb * x[4 * j + 2], vb1 = bb * x[4 * j + 3];
-                    const uint32_t oa = cm_off(kL + ta, 2 * col, 2 * kL), ob = cm_off(kL + tb, 2 * col, 2 * kL);
-                    *reinterpret_cast<uint32_t *>(ydu + oa) = pack2_bf16(-va0, -va1);
-                    *reinterpret_cast<uint32_t *>(ydu + ob) = pack2_bf16(-vb0, -vb1);
-                    *reinterpret_cast<uint32_t *>(yds + oa) = pack2_bf16(-ga * va0, -ga * va1);
-                    *reinterpret_cast<uint32_t *>(yds + ob) = pack2_bf16(-gb * vb0, -gb * vb1);
-                    // dv staged in the 128-byte swizzle for a TMA store (rows past T are clipped by it):
-                    // row t at t * 128, 16-byte chunk col / 8 at chunk ^ (t % 8)
-                    *reinterpret_cast<uint32_t *>(dvs + ta * 128 + (((col >> 3) ^ (ta & 7)) << 4) + (col & 7) * 2) =
-                        pack2_bf16(va0, va1);
-                    *reinterpret_cast<uint32_t *>(dvs + tb * 128 + (((col >> 3) ^ (tb & 7)) << 4) + (col & 7) * 2) =
-                        pack2_bf16(vb0, vb1);
+                    du[2 * j] = pack2_bf16(-va0, -va1);
+                    du[2 * j + 1] = pack2_bf16(-vb0, -vb1);
+                    us[2 * j] = pack2_bf16(-ga * va0, -ga * va1);
+                    us[2 * j + 1] = pack2_bf16(-gb * vb0, -gb * vb1);
+                    dv[2 * j] = pack2_bf16(va0, va1);
+                    dv[2 * j + 1] = pack2_bf16(vb0, vb1);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; j += 2) {
+                    // dU: rows 64-127 of [dY; dU] (stored for the gradient kernel) and of the carry's
+                    // operand (scaled by exp Lam)
+                    const uint32_t o = frag_row_addr(0, 2 * kL, kL + 16 * (warp & 3), 4 * hw + j, lane);
+                    stmatrix_x4(smem_addr(ydu) + o, du[2 * j], du[2 * j + 1], du[2 * j + 2], du[2 * j + 3]);
+                    stmatrix_x4(smem_addr(yds) + o, us[2 * j], us[2 * j + 1], us[2 * j + 2], us[2 * j + 3]);
+                    // dv staged in the 128-byte swizzle for a TMA store (rows past T are clipped by
+                    // it): row t at t * 128, 16-byte chunk c (8 columns) at c ^ (t % 8)
+                    const int m = lane >> 3, t = 16 * (warp & 3) + 8 * (m & 1) + (lane & 7), cc = 4 * hw + j + (m >> 1);
+                    stmatrix_x4(smem_addr(dvs) + t * 128 + ((cc ^ (t & 7)) << 4), dv[2 * j], dv[2 * j + 1], dv[2 * j + 2],
+                                dv[2 * j + 3]);
                 }
                 warp_done(bU);
                 da += __shfl_xor_sync(kFullMask, da, 1);

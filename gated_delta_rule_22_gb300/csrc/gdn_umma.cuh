@@ -222,6 +222,25 @@ __device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// stmatrix m8n8.x4 (whole warp): four 8x8 matrices of 16-bit values to shared memory. Lane l
+// gives the address of row l % 8 of matrix l / 8 (16 contiguous bytes) and holds, in r0..r3,
+// row l / 4, columns 2 (l % 4) and + 1 of matrices 0..3: the layout in which an M64Frag holds
+// a pair of values, so a fragment goes to any tile whose 8x8 blocks have 16-byte rows.
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
+}
+
+// The row address that `lane` gives to stmatrix_x4 for the M64Frag values of column blocks cb
+// and cb + 1 (8 columns each) in an R-row core-matrix tile (shared-memory address `tile`), the
+// warp's 16 rows starting at row16: matrices (cb, rows row16..+7), (cb, row16+8..+15),
+// (cb + 1, row16..), (cb + 1, row16+8..) -- r0..r3 = the value pairs 4j, 4j+2, 4j+4, 4j+6.
+__device__ __forceinline__ uint32_t frag_row_addr(uint32_t tile, int R, int row16, int cb, int lane) {
+    const int m = lane >> 3;
+    return tile + cm_off(row16 + 8 * (m & 1) + (lane & 7), 16 * (cb + (m >> 1)), R);
+}
+
 // 32x32b tensor-memory load of 16 consecutive columns.
 __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
     asm volatile(
