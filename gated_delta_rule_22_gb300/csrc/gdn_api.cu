@@ -293,19 +293,22 @@ int make_colblock_map(CUtensorMap *map, const void *ptr, bool bf16, int B, int T
     return GDN_OK;
 }
 
-// 5-D tensor map of the [Q; K] buffer of the chunkwise forward (nblk blocks of [128][Dk] bf16
-// in the core-matrix layout: K chunk j holds 64 rows of Q, then 64 rows of K): dimensions
-// {8, 64 rows, Dk / 8 chunks, 2 halves, nblk}, box {8, 64, Dk / 8, 1, 1}, so that one box is a
-// [64][Dk] operand tile of Q or of K.
+// 5-D tensor map of a buffer of stacked operand blocks of the chunkwise forward (nblk blocks of
+// [128][Dk] bf16 in the core-matrix layout, K chunk j holding 64 rows of the top half, then 64
+// of the bottom half: [Q; K] with Dk columns, [P; KKm] with 64): dimensions
+// {256, 2, 2 halves, Dk / 8 chunks, nblk} (a half's rows of a K chunk are 1 KB contiguous, two
+// runs of 256 elements), box {256, 2, 1, Dk / 8, 1}, so that one box, at coordinates
+// (0, 0, half, 0, block), is a [64][Dk] operand tile of one half (Q or K; P or KKm).
 int make_qkm_map(CUtensorMap *map, void *ptr, size_t nblk, int Dk) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) {
         snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available from the driver");
         return GDN_ERR_CUDA;
     }
-    const cuuint64_t dims[5] = {8, 64, (cuuint64_t)(Dk / 8), 2, (cuuint64_t)nblk};
-    const cuuint64_t strides[4] = {16, 128 * 16, 64 * 16, (cuuint64_t)128 * Dk * 2};
-    const cuuint32_t box[5] = {8, 64, (cuuint32_t)(Dk / 8), 1, 1};
+    // a half's 64 rows of one K chunk are 1 KB contiguous: two runs of 256 elements
+    const cuuint64_t dims[5] = {256, 2, 2, (cuuint64_t)(Dk / 8), (cuuint64_t)nblk};
+    const cuuint64_t strides[4] = {512, 1024, 2048, (cuuint64_t)256 * Dk};
+    const cuuint32_t box[5] = {256, 2, 1, (cuuint32_t)(Dk / 8), 1};
     const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, ptr, dims, strides, box, estride,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -485,16 +488,18 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         CUtensorMap tm_dv;
         rc = make_btd_map(&tm_dv, dv, true, p.B, p.T, p.Hv, p.Dv, 64, 64);
         if (rc != GDN_OK) return rc;
-        CUtensorMap tm_dy, tm_qk;
+        CUtensorMap tm_dy, tm_qk, tm_pk;
         rc = make_colblock_map(&tm_dy, dy, true, p.B, p.T, p.Hv, p.Dv, 8, 128, 8, false);
         if (rc != GDN_OK) return rc;
         rc = make_qkm_map(&tm_qk, const_cast<__nv_bfloat16 *>(cp.qkm), (size_t)p.B * p.Hk * p.NC, p.Dk);
+        if (rc != GDN_OK) return rc;
+        rc = make_qkm_map(&tm_pk, const_cast<__nv_bfloat16 *>(cp.pkm), (size_t)p.B * p.Hv * p.NC, 64);
         if (rc != GDN_OK) return rc;
         CUtensorMap tm_dq, tm_dk;
         if ((rc = make_btd_map(&tm_dq, dq, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK ||
             (rc = make_btd_map(&tm_dk, dk, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK)
             return rc;
-        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_qk, tm_dq, tm_dk, p.Dk, (cudaStream_t)stream));
+        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, p.Dk, (cudaStream_t)stream));
     }
     const Workspace w = workspace_layout(p);
 

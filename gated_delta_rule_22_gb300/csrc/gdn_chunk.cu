@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(ChunkParams p, int u
             if (tid == 32) {
                 const size_t ckv = ((size_t)b * Hk + x.hk) * NC + c;
                 tma_store_5d(&maps.qk, qc, 0, 0, 0, 0, (int)ckv);
-                tma_store_5d(&maps.qk, kc, 0, 0, 0, 1, (int)ckv);
+                tma_store_5d(&maps.qk, kc, 0, 0, 1, 0, (int)ckv);
                 bulk_commit();
             }
         }

@@ -76,13 +76,13 @@ constexpr int kSweepLaunchRegs = 168, kSweepMathRegs = 176, kSweepCtrlRegs = 152
 static_assert(2 * 128 * kSweepMathRegs + 128 * kSweepCtrlRegs <= kSweepThreads * kSweepLaunchRegs, "register split");
 
 struct DSweepSmem {
-    size_t qb, kb, tm, pkm, ydu, yds, lms, shl, rhs, dls, dvs, bar, tslot, total;
+    size_t qb, kb, tm, pb, ydu, yds, lms, shl, rhs, dls, dvs, bar, tslot, total;
     __host__ __device__ DSweepSmem(int DK) {
         size_t o = 0;
         qb = o; o += (size_t)kL * DK * 2;        // Q of the chunk (kv head) [64][DK] (read MN-major by the carry)
         kb = o; o += (size_t)2 * kL * DK * 2;    // K, two buffers [64][DK] (K-major for K dS^T, MN-major for the carry)
         tm = o; o += (size_t)kL * kL * 2;        // T [64][64] (read MN-major as T^T)
-        pkm = o; o += (size_t)2 * kL * kL * 2;   // [P; KKm] [128][64], P = (Q K^T) o E_incl (read MN-major)
+        pb = o; o += (size_t)2 * kL * kL * 2;    // P = (Q K^T) o E_incl, two buffers [64][64] (read MN-major)
         ydu = o; o += (size_t)2 * 2 * kL * kL * 2;   // [dY; dU] block [128][64 v] (rows 0-63 dY, 64-127 dU), two buffers
         yds = o; o += (size_t)2 * kL * kL * 2;       // [diag(exp Lam) dY; diag(exp Lam) dU] [128][64 v] (read MN-major)
         lms = o; o += (size_t)2 * kL * 4;        // Lam, two buffers
@@ -90,7 +90,7 @@ struct DSweepSmem {
         rhs = o; o += (size_t)kL * kL * 2;       // diag(E_L) K dS^T + P^T dY [64 t][64 v]
         dls = o; o += (size_t)kL * kL * 2;       // Delta block [64 t][64 v], for the gradient kernel
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
-        bar = alb(o, 8); o = bar + 16 * 8;       // see the kernel
+        bar = alb(o, 8); o = bar + 17 * 8;       // see the kernel
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -124,7 +124,8 @@ template <int E>
 __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwdParams p,
                                                                         const __grid_constant__ CUtensorMap tm_dv,
                                                                         const __grid_constant__ CUtensorMap tm_dy,
-                                                                        const __grid_constant__ CUtensorMap tm_qk) {
+                                                                        const __grid_constant__ CUtensorMap tm_qk,
+                                                                        const __grid_constant__ CUtensorMap tm_pk) {
     constexpr int DK = 32 * E;
     constexpr int SC = DK / 2;                // dS columns per warp half
     constexpr int NS = SC / 2;                // dS values per thread
@@ -139,30 +140,34 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
     const DSweepSmem L(DK);
-    unsigned char *qb = base + L.qb, *kb2 = base + L.kb, *tmm = base + L.tm, *pmm = base + L.pkm, *yds = base + L.yds;
+    unsigned char *qb = base + L.qb, *kb2 = base + L.kb, *tmm = base + L.tm, *pb2 = base + L.pb, *yds = base + L.yds;
     unsigned char *ydu2 = base + L.ydu, *shl = base + L.shl, *rhs = base + L.rhs, *dls = base + L.dls;
     unsigned char *dvs = base + L.dvs;
     float *lms = reinterpret_cast<float *>(base + L.lms);
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
-    uint64_t *m1 = bar, *mD = bar + 1, *mS = bar + 2, *cbA = bar + 3, *cbT = bar + 4, *cbQ = bar + 5, *cbY = bar + 6;
-    uint64_t *cbK = bar + 7;                                    // [2]
-    uint64_t *bH = bar + 9, *bR = bar + 10, *bU = bar + 11, *fS = bar + 12, *fO = bar + 13, *mX = bar + 14;
+    uint64_t *m1 = bar, *mD = bar + 1, *mS = bar + 2, *cbT = bar + 3, *cbQ = bar + 4;
+    uint64_t *cbP = bar + 5, *cbK = bar + 7, *cbY = bar + 9;   // [2] each: one per buffer
+    uint64_t *bH = bar + 11, *bR = bar + 12, *bU = bar + 13, *fS = bar + 14, *fO = bar + 15, *mX = bar + 16;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
-    auto kbuf = [&](int k) { return kb2 + (size_t)(k & 1) * kL * DK * 2; };   // K of the chunk handled k-th
+    // the buffers of the chunk handled k-th (chunk NC - 1 - k): K, P, [dY; dU], Lam
+    auto kbuf = [&](int k) { return kb2 + (size_t)(k & 1) * kL * DK * 2; };
+    auto pbuf = [&](int k) { return pb2 + (size_t)(k & 1) * kL * kL * 2; };
+    auto ybuf = [&](int k) { return ydu2 + (size_t)(k & 1) * 2 * kL * kL * 2; };
 
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(p.beta);
     const size_t head = (size_t)b * Hv + h;
     const int qkblk0 = (b * p.Hk + h / (Hv / p.Hk)) * NC;     // [Q; K] block of chunk 0 of this kv head
 
     if (tid == 0) {
-        for (int i = 0; i < 9; ++i) mbar_init(bar + i, 1);
-        for (int i = 9; i < 12; ++i) mbar_init(bar + i, kSweepMathWarps);
-        for (int i = 12; i < 15; ++i) mbar_init(bar + i, 1);
+        for (int i = 0; i < 11; ++i) mbar_init(bar + i, 1);
+        for (int i = 11; i < 14; ++i) mbar_init(bar + i, kSweepMathWarps);
+        for (int i = 14; i < 17; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
     }
     if (warp == kSweepMathWarps + 1 && lane == 0) {
         tma_prefetch_map(&tm_dy);
         tma_prefetch_map(&tm_qk);
+        tma_prefetch_map(&tm_pk);
         tma_prefetch_map(&tm_dv);
     }
     if (warp == kSweepMathWarps) tmem_alloc(tslot, 512);
@@ -186,11 +191,11 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
             // P^T dY needs no dS: each chunk's is issued a chunk ahead (the first one here), so that
             // only K dS^T is on the path from dS to the next chunk
             {
-                const bool w = mbar_wait(cbA, 0) && mbar_wait(cbY, 0);
+                const bool w = mbar_wait(cbP, 0) && mbar_wait(cbY, 0);
                 fail = __any_sync(kFullMask, !w);
                 if (!fail) {
                     tc_fence_after();
-                    umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu2, 2 * kL, 0, 0, true}, kL, idP, false, lead);
+                    umma_gemm_w(tP, CmOp{pbuf(0), kL, 0, 0, true}, CmOp{ybuf(0), 2 * kL, 0, 0, true}, kL, idP, false, lead);
                 }
             }
             for (int k = 0; k < NC && !fail; ++k) {
@@ -220,14 +225,14 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
                 tc_fence_after();
                 umma_gemm_w(tS, CmOp{yds, 2 * kL, 0, kL, true}, CmOp{kb, kL, 0, 0, true}, kL, idS, true, lead);
                 umma_commit_w(mS, lead);
-                // ---- P^T dY of the next chunk: its [P; KKm] and dY landed (copied after bR), and the
+                // ---- P^T dY of the next chunk: its P and dY landed (copied two chunks ahead), and the
                 // math warps read this chunk's (before bR)
                 if (k + 1 < NC) {
-                    w = mbar_wait(cbA, (k + 1) & 1) && mbar_wait(cbY, (k + 1) & 1);
+                    const int k1 = k + 1;
+                    w = mbar_wait(cbP + (k1 & 1), (k1 >> 1) & 1) && mbar_wait(cbY + (k1 & 1), (k1 >> 1) & 1);
                     if (__any_sync(kFullMask, !w)) { fail = true; break; }
                     tc_fence_after();
-                    umma_gemm_w(tP, CmOp{pmm, 2 * kL, 0, 0, true}, CmOp{ydu2 + (size_t)((k + 1) & 1) * 2 * kL * kL * 2, 2 * kL, 0, 0, true},
-                                kL, idP, false, lead);
+                    umma_gemm_w(tP, CmOp{pbuf(k1), kL, 0, 0, true}, CmOp{ybuf(k1), 2 * kL, 0, 0, true}, kL, idP, false, lead);
                 }
             }
             if (fail) {
@@ -238,12 +243,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
         } else if (warp == kSweepMathWarps + 1) {
             // ================================================================ copy warp (lane 0)
             if (lane == 0) {
-                int nA = 0, nT = 0, nQ = 0, nK0 = 0, nK1 = 0, nY = 0;
-                auto copy_A = [&](int cc) {                      // [P; KKm] of chunk cc
-                    mbar_expect_tx(cbA, 2 * kL * kL * 2);
-                    bulk_load(pmm, p.pkm + (head * NC + cc) * 2 * kL * kL, 2 * kL * kL * 2, cbA);
-                    ++nA;
-                };
+                int nT = 0, nQ = 0, nP[2] = {0, 0}, nK[2] = {0, 0}, nY[2] = {0, 0};
                 auto copy_T = [&](int cc) {                      // T of chunk cc
                     mbar_expect_tx(cbT, kL * kL * 2);
                     bulk_load(tmm, p.tm + (head * NC + cc) * kL * kL, kL * kL * 2, cbT);
@@ -254,65 +254,73 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
                     tma_load_5d(qb, &tm_qk, cbQ, 0, 0, 0, 0, qkblk0 + cc);
                     ++nQ;
                 };
-                auto copy_K = [&](int kk) {                      // K of the chunk handled kk-th: rows 64-127
+                // the chunk handled kk-th: K (rows 64-127 of its [Q; K] block), P (rows 0-63 of its
+                // [P; KKm] block), and dY (one 128-row box in the [dY; dU] layout: rows 64-127, the
+                // following steps, land in the dU rows, which the math warps rewrite before anything
+                // reads them) with Lam (rows past T: zeros)
+                auto copy_K = [&](int kk) {
                     mbar_expect_tx(cbK + (kk & 1), kL * DK * 2);
-                    tma_load_5d(kbuf(kk), &tm_qk, cbK + (kk & 1), 0, 0, 0, 1, qkblk0 + NC - 1 - kk);
-                    if (kk & 1) ++nK1; else ++nK0;
+                    tma_load_5d(kbuf(kk), &tm_qk, cbK + (kk & 1), 0, 0, 1, 0, qkblk0 + NC - 1 - kk);
+                    ++nK[kk & 1];
                 };
-                // dY (one 128-row box in the [dY; dU] layout: rows 64-127, the following steps, land in
-                // the dU rows, which the math warps rewrite before anything reads them) and Lam of
-                // chunk cc (rows past T: zeros)
-                auto fetch = [&](int cc, int buf) {
-                    mbar_expect_tx(cbY, 2 * kL * kL * 2 + kL * 4);
-                    tma_load_5d(ydu2 + (size_t)buf * 2 * kL * kL * 2, &tm_dy, cbY, 0, cc * kL, r0 / 8, h, b);
-                    bulk_load(lms + buf * kL, p.lam + (head * NC + cc) * kL, kL * 4, cbY);
-                    ++nY;
+                auto copy_P = [&](int kk) {
+                    mbar_expect_tx(cbP + (kk & 1), kL * kL * 2);
+                    tma_load_5d(pbuf(kk), &tm_pk, cbP + (kk & 1), 0, 0, 0, 0, (int)(head * NC) + NC - 1 - kk);
+                    ++nP[kk & 1];
                 };
-                copy_K(0);
-                fetch(NC - 1, 0);
-                copy_A(NC - 1);
-                if (NC > 1) copy_K(1);
+                auto fetch = [&](int kk) {
+                    const int cc = NC - 1 - kk;
+                    mbar_expect_tx(cbY + (kk & 1), 2 * kL * kL * 2 + kL * 4);
+                    tma_load_5d(ybuf(kk), &tm_dy, cbY + (kk & 1), 0, cc * kL, r0 / 8, h, b);
+                    bulk_load(lms + (kk & 1) * kL, p.lam + (head * NC + cc) * kL, kL * 4, cbY + (kk & 1));
+                    ++nY[kk & 1];
+                };
+                for (int kk = 0; kk < 2 && kk < NC; ++kk) {
+                    copy_K(kk);
+                    fetch(kk);
+                    copy_P(kk);
+                }
                 copy_T(NC - 1);
                 copy_Q(NC - 1);
                 for (int k = 0; k < NC; ++k) {
-                    const int c = NC - 1 - k, buf = k & 1;
+                    const int c = NC - 1 - k;
                     const size_t chk = head * NC + c, blk = chk * nsplit + split;
-                    unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;
                     // dS_L (high part) for the gradient kernel once written
                     if (!mbar_wait(bH, k & 1)) { fail = true; break; }
                     bulk_store(p.ws_dsl + blk * kL * DK, shl, kL * DK * 2);
                     bulk_commit();
-                    // rhs written: the math warps saw m1, so [P; KKm] is free; the next chunk's dY and
-                    // Lam go to the other buffers (its [dY; dU] was stored and read out, see fO)
+                    // rhs written: the math warps saw m1, so this chunk's P buffer is free (the
+                    // chunk two ahead)
                     if (!mbar_wait(bR, k & 1)) { fail = true; break; }
-                    if (c > 0) {
-                        copy_A(c - 1);
-                        fetch(c - 1, buf ^ 1);
-                    }
+                    if (k + 2 < NC) copy_P(k + 2);
                     bulk_wait_read();                           // the dS_L store has read the dS parts
                     mbar_arrive(fS);
                     // dU written: the math warps saw mD, so T is free; the block's outputs leave
                     if (!mbar_wait(bU, k & 1)) { fail = true; break; }
                     if (c > 0) copy_T(c - 1);
-                    bulk_store(p.ws_yu + blk * 2 * kL * kL, ydu, 2 * kL * kL * 2);
+                    bulk_store(p.ws_yu + blk * 2 * kL * kL, ybuf(k), 2 * kL * kL * 2);
                     bulk_store(p.ws_dl + blk * kL * kL, dls, kL * kL * 2);
                     tma_store_4d(&tm_dv, dvs, r0, h, c * kL, b);
                     bulk_commit();
-                    // the carry is done: Q, and this chunk's K buffer (for the chunk two ahead), are free
+                    // the carry is done: Q and this chunk's K buffer are free; once the stores have
+                    // read them, so are the [dY; dU] buffer and the staging tiles (Lam was read
+                    // before bR)
                     if (!mbar_wait(mS, k & 1)) { fail = true; break; }
                     if (c > 0) copy_Q(c - 1);
                     if (k + 2 < NC) copy_K(k + 2);
-                    bulk_wait_read();                           // [dY; dU], Delta and dv staging read out
+                    bulk_wait_read();
                     mbar_arrive(fO);
+                    if (k + 2 < NC) fetch(k + 2);
                 }
                 if (fail) {
                     // copies still in flight land before the CTA exits (each wait bounded)
-                    if (nA > 0) mbar_wait(cbA, (nA - 1) & 1);
                     if (nT > 0) mbar_wait(cbT, (nT - 1) & 1);
                     if (nQ > 0) mbar_wait(cbQ, (nQ - 1) & 1);
-                    if (nK0 > 0) mbar_wait(cbK, (nK0 - 1) & 1);
-                    if (nK1 > 0) mbar_wait(cbK + 1, (nK1 - 1) & 1);
-                    if (nY > 0) mbar_wait(cbY, (nY - 1) & 1);
+                    for (int i = 0; i < 2; ++i) {
+                        if (nP[i] > 0) mbar_wait(cbP + i, (nP[i] - 1) & 1);
+                        if (nK[i] > 0) mbar_wait(cbK + i, (nK[i] - 1) & 1);
+                        if (nY[i] > 0) mbar_wait(cbY + i, (nY[i] - 1) & 1);
+                    }
                 }
                 bulk_wait_all();                                // the block outputs are complete
             }
@@ -368,7 +376,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
             const int c = NC - 1 - k, buf = k & 1;
             const int t0 = c * kL, len = min(kL, T - t0);
             const size_t rowbase = (size_t)b * T + t0;          // (b, t0) row of [B, T, ...]
-            unsigned char *ydu = ydu2 + (size_t)buf * 2 * kL * kL * 2;   // [dY; dU] of this chunk
+            unsigned char *ydu = ybuf(k);                      // [dY; dU] of this chunk
             const float *lmb = lms + buf * kL;                 // Lam of this chunk
             const float ba = __bfloat162float(bna), bb = __bfloat162float(bnb);
             float2 rsa[4], rsb[4];
@@ -413,7 +421,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
             warp_done(bH);
             // ---- this chunk's dY and Lam
             {
-                const bool w = mbar_wait(cbY, k & 1);
+                const bool w = mbar_wait(cbY + buf, (k >> 1) & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
             }
             const float ela = expf(lmb[kL - 1] - lmb[ta]), elb = expf(lmb[kL - 1] - lmb[tb]);
@@ -1029,8 +1037,8 @@ size_t chunk_grad_smem(int Dk, int Dv) { return GradSmem(Dk, Dv).total; }
 
 template <int E>
 static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
-                                      const CUtensorMap &tm_qk, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk,
-                                      cudaStream_t s) {
+                                      const CUtensorMap &tm_qk, const CUtensorMap &tm_pk, const CUtensorMap &tm_dq,
+                                      const CUtensorMap &tm_dk, cudaStream_t s) {
     constexpr int DK = 32 * E;
     const size_t sd = DSweepSmem(DK).total, sg = GradSmem(DK, p.Dv).total;
     // the reverse sweep's register split waits for registers that only a launch of
@@ -1045,7 +1053,7 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     if (err != cudaSuccess) return err;
     timing_mark("chunk_dsweep", 0, s);
     err = launch_pdl(chunk_dsweep_kernel<E>, dim3(p.nsplit, p.Hv, p.B), dim3(kSweepThreads), sd, s, p, tm_dv, tm_dy,
-                     tm_qk);
+                     tm_qk, tm_pk);
     timing_mark("chunk_dsweep", 1, s);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_grad", 0, s);
@@ -1062,12 +1070,13 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
 }
 
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
-                             const CUtensorMap &tm_qk, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk, int Dk,
+                             const CUtensorMap &tm_qk, const CUtensorMap &tm_pk, const CUtensorMap &tm_dq,
+                             const CUtensorMap &tm_dk, int Dk,
                              cudaStream_t s) {
     switch (Dk) {
-        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, tm_dy, tm_qk, tm_dq, tm_dk, s);
-        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, tm_dy, tm_qk, tm_dq, tm_dk, s);
-        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_qk, tm_dq, tm_dk, s);
+        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s);
+        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s);
+        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -489,8 +489,9 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // TMA loads, no swizzle, in 1 KB core-matrix columns of 64 rows: k and q as 5-D column blocks
 // of [B][T][Hk][Dk] {8, T, Dk / 8, Hk, B}, box {8, 64, Dk / 8, 1, 1}; vb, v as 5-D column
 // blocks of [B][T][Hv][Dv] {8, T, Dv / 8, Hv, B}, box {8, 64, 8, 1, 1} (64 value columns).
-// Written by TMA stores from an operand tile of 64 rows: qk, the [Q; K] buffer as {8, 64 rows,
-// Dk / 8 chunks, 2 halves (Q, K), B*Hk*NC blocks}, box {8, 64, Dk / 8, 1, 1}.
+// Written by TMA stores from an operand tile of 64 rows: qk, the [Q; K] buffer as {256, 2,
+// 2 halves (Q, K), Dk / 8 chunks, B*Hk*NC blocks}, box {256, 2, 1, Dk / 8, 1} (a half's 64 rows of
+// a K chunk are 1 KB contiguous).
 struct ChunkFwdMaps {
     CUtensorMap y, r, vb, k, q, qk;
 };
@@ -501,11 +502,13 @@ size_t chunk_sweep_smem(int Dk);
 // and the fixed-order sums over value heads and row blocks.
 // Tensor maps of [B][T][Hv][Dv] tensors: tm_dv dv (bf16, 4-D, box {64, 1, 64, 1}, 128-byte
 // swizzle); tm_dy dy (bf16, 5-D column blocks {8, T, Dv / 8, Hv, B}, box {8, 128, 8, 1, 1}, no
-// swizzle); tm_qk v - u (fp32, 5-D column blocks {32, T, Dv / 32, Hv, B}, box
-// {32, 64, 2, 1, 1}, 128-byte swizzle).
+// swizzle). tm_qk, tm_pk: the saved [Q; K] blocks (per b, kv head, chunk) and [P; KKm] blocks
+// (per b, value head, chunk) as {256, 2, 2 halves, columns / 8, blocks}, box one half: a
+// [64][columns] operand tile (Q or K; P).
 // tm_dq, tm_dk: dq and dk as [B][T][Hk][Dk] bf16, 4-D, box {64, 1, 64, 1}, 128-byte swizzle.
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
-                             const CUtensorMap &tm_qk, const CUtensorMap &tm_dq, const CUtensorMap &tm_dk, int Dk,
+                             const CUtensorMap &tm_qk, const CUtensorMap &tm_pk, const CUtensorMap &tm_dq,
+                             const CUtensorMap &tm_dk, int Dk,
                              cudaStream_t s);
 size_t chunk_dsweep_smem(int Dk);
 size_t chunk_grad_smem(int Dk, int Dv);
