@@ -444,8 +444,15 @@ namespace gdn {
 
 namespace {
 
+constexpr int kFwdMathWarps = 8;     // hold S (M = 64 fragment: 4 lane quarters x 2 column halves)
+constexpr int kFwdThreads = 384;     // + a warpgroup: warp 8 issues the products, warp 9 the copies and stores
+// registers: launched at 168 a thread; the control warpgroup gives up all but kFwdCtrlRegs, the
+// math warpgroups take kFwdMathRegs (2 x 128 x 176 + 128 x 152 = 384 x 168)
+constexpr int kFwdLaunchRegs = 168, kFwdMathRegs = 176, kFwdCtrlRegs = 152;
+static_assert(2 * 128 * kFwdMathRegs + 128 * kFwdCtrlRegs <= kFwdThreads * kFwdLaunchRegs, "register split");
+
 struct SweepSmem {
-    size_t wgrp, wc, tc, vb, qk, pk, sop, dt, de, ysg, rsg, vec, bar, tslot, total;
+    size_t wgrp, wc, tc, vb, qb, kb, pk, sop, dt, de, bar, tslot, total;
     __host__ __device__ SweepSmem(int DK) {
         size_t o = 0;
         // group W, two buffers (chunks alternate): -W, T diag(beta), V
@@ -454,15 +461,13 @@ struct SweepSmem {
         tc = wc + (size_t)kL * DK * 2;         // T diag(beta)                       A [64][64]
         vb = tc + (size_t)kL * kL * 2;         // V of the chunk, this block's 64 columns [64 t][64 v] (read MN-major)
         o += 2 * wgrp;
-        qk = o; o += (size_t)2 * kL * DK * 2;  // [Q; K] of the chunk (kv head)      A [128][DK]; K read MN-major as B
+        qb = o; o += (size_t)kL * DK * 2;      // Q of the chunk (kv head)           A [64][DK]
+        kb = o; o += (size_t)2 * kL * DK * 2;  // K, two buffers                     A [64][DK]; read MN-major as B
         pk = o; o += (size_t)2 * kL * kL * 2;  // [(Q K^T) o E_incl; (K K^T) o E_strict]   A [128][64]
         sop = o; o += (size_t)kL * DK * 2;     // S (64 value rows)                  B [64][DK]
         dt = o; o += (size_t)kL * kL * 2;      // Delta [64 t][64 v], read MN-major (B)
         de = o; o += (size_t)kL * kL * 2;      // diag(E_L) Delta [64 t][64 v], read MN-major (A, transposed)
-        ysg = al(o, 1024); o = ysg + (size_t)kL * 128;        // y of a chunk, bf16 [64][64] in the 128-byte swizzle
-        rsg = al(o, 1024); o = rsg + (size_t)2 * kL * 128;    // v - u of a chunk, fp32 [2][64][32] in the 128-byte swizzle
-        vec = o; o += 5 * kL * 4;              // Lam [2][64], exp Lam [2][64] (two chunks), E(L, .) [64]
-        bar = al(o, 8); o = bar + 7 * 8;       // copies of group W (two buffers), of group R ([Q; K], [P; KKm]); products D, U, Y; drain
+        bar = al(o, 8); o = bar + 16 * 8;      // see the kernel
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -472,320 +477,430 @@ struct SweepSmem {
 }  // namespace
 
 // One CTA per (64-row block of the state, value head, batch row), carrying that block of the
-// state through the chunks. The fp32 state lives in registers (a thread holds 2 rows x DK/8
-// columns, the 16x256b fragment of an M = 64 accumulator); per chunk the products are
-// (fp32 accumulators in tensor memory, M = 64: value row r in lane r % 16 + 32 (r / 16)):
-//   [0, DK)              Sigma = (diag(E_L) Delta)^T K, the chunk's update: S <- exp(Lam_L) S + Sigma
-//   [DK, DK + 64)        Delta = (T diag(beta)) V + (-W) S^T (chunk row t, value column)
-//   [DK + 64, DK + 128)  [Q; K] S^T (M = 128: chunk row t of Q in lane t, of K in lane 64 + t)
-//   [DK + 128, DK + 192) [P; KKm] Delta (M = 128)
+// state through the chunks. Warps 0-7 hold the fp32 state (registers: the 16x256b fragment of
+// an M = 64 accumulator, 2 rows x DK/8 columns per thread) and do the element-wise work; warp 8
+// issues the products (one elected lane) and warp 9 the copies and the bf16 state's stores, so
+// that no math warp stalls on an issue and no block barrier runs per chunk: every hand-off is an
+// mbarrier. Per chunk the products are (fp32 accumulators in tensor memory, M = 64: row r in
+// lane r % 16 + 32 (r / 16)):
+//   [0, DK)               Sigma = (diag(E_L) Delta)^T K: S <- exp(Lam_L) S + Sigma
+//   [DK, DK + 64)         Delta = (T diag(beta)) V + (-W) S^T (chunk row t, value column)
+//   [DK + 64, + 128)      Q S^T, then K S^T
+//   [DK + 192, + 256)     P Delta, then KKm Delta
 // and y = diag(exp Lam) (Q S^T) + P Delta, u = diag(exp Lam) (K S^T) + KKm Delta.
-// Roles: warp 0 issues the products (from one elected lane, the warp converged); thread 32
-// issues the copies and the state's stores; warps 4-7 write y and v - u of the previous chunk
-// while the next products run (thread 128 stores them); every thread converts the state and
-// Delta.
+// Hand-offs of chunk c (each completes once per chunk):
+//   math -> control (8 warp arrivals): bS  S written as an operand;  bE  the previous chunk's
+//                                      y and u read out;  bDt  Delta written as operands
+//   control -> math: mD, mQ, mU, mY  the product groups (commits);  fS  the state operand's
+//                    tile is free (the products that read it are done, its store has read it)
+// Q and K arrive as separate [64][DK] tiles (boxes of the [Q; K] block), K double-buffered and
+// fetched two chunks ahead, as is group W. y and v - u leave from registers.
 template <int E>
-__global__ void __launch_bounds__(256, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ ChunkFwdMaps maps) {
+__global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ ChunkFwdMaps maps) {
     constexpr int DK = 32 * E;
     constexpr int SC = DK / 2;                // state columns per warp half
     constexpr int NS = SC / 2;                // state values per thread (2 rows x 2 columns x SC / 8 repetitions)
-    static_assert(DK + 192 <= 512, "tensor memory holds Sigma, Delta, [Q; K] S^T and [P; KKm] Delta");
+    static_assert(DK + 320 <= 512, "tensor memory holds Sigma, Delta, Q S^T, K S^T, P Delta and KKm Delta");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool math = warp < kFwdMathWarps;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, r0 = split * kL, NC = p.NC;
+    const int hw = (warp >> 2) & 1;                             // warp half
     const uint32_t lane16 = (uint32_t)(32 * (warp & 3)) << 16;   // tensor-memory lane base of this warp's M = 64 rows
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 1024));
     const SweepSmem L(DK);
-    unsigned char *qk = base + L.qk, *pk = base + L.pk;
+    unsigned char *qb = base + L.qb, *kb2 = base + L.kb, *pk = base + L.pk;
     unsigned char *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
-    unsigned char *ysg = base + L.ysg, *rsg = base + L.rsg;
-    float *Lm2 = reinterpret_cast<float *>(base + L.vec), *gm2 = Lm2 + 2 * kL, *eL = gm2 + 2 * kL;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
-    uint64_t *bW = bar, *bR = bar + 2, *mD = bar + 3, *mU = bar + 4, *mY = bar + 5, *mX = bar + 6;   // bW[2]
+    uint64_t *mD = bar, *mQ = bar + 1, *mU = bar + 2, *mY = bar + 3, *cbQ = bar + 4, *cbP = bar + 5;
+    uint64_t *bW = bar + 6, *cbK = bar + 8;                     // [2] each: one per buffer
+    uint64_t *bS = bar + 10, *bE = bar + 11, *bDt = bar + 12, *fS = bar + 13, *mX = bar + 14;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
+    // the buffers of chunk c: group W (-W, T diag(beta), V) and K
+    auto wbuf = [&](int c) { return base + L.wc + (size_t)(c & 1) * L.wgrp; };
+    auto kbuf = [&](int c) { return kb2 + (size_t)(c & 1) * kL * DK * 2; };
 
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
     const size_t head = (size_t)b * Hv + h;
     const int hk = h / (Hv / p.Hk);
-    // copies of chunk cc (thread 32): group W (-W, T diag(beta) and this block's V, read by the
-    // Delta products; buffer cc % 2, fetched two chunks ahead) and group R ([Q; K] and [P; KKm],
-    // read by the update and [y; u] products)
-    int nW0 = 0, nW1 = 0, nR = 0;   // copies issued into group W's buffers 0 and 1, group R
-    auto wbuf = [&](int cc) { return base + L.wc + (size_t)(cc & 1) * L.wgrp; };
-    auto issue_w = [&](int cc) {
-        const size_t ck = head * NC + cc;
-        unsigned char *g = wbuf(cc);
-        uint64_t *bw = bW + (cc & 1);
-        mbar_expect_tx(bw, kL * DK * 2 + 2 * kL * kL * 2);
-        bulk_load(g, p.wm + ck * kL * DK, kL * DK * 2, bw);
-        bulk_load(g + (L.tc - L.wc), p.tcm + ck * kL * kL, kL * kL * 2, bw);
-        tma_load_5d(g + (L.vb - L.wc), &maps.vb, bw, 0, cc * kL, r0 / 8, h, b);
-        if (cc & 1) ++nW1; else ++nW0;
-    };
-    auto issue_r = [&](int cc) {
-        mbar_expect_tx(bR, 2 * kL * DK * 2 + 2 * kL * kL * 2);
-        bulk_load(qk, p.qkm + (((size_t)b * p.Hk + hk) * NC + cc) * 2 * kL * DK, 2 * kL * DK * 2, bR);
-        bulk_load(pk, p.pkm + (head * NC + cc) * 2 * kL * kL, 2 * kL * kL * 2, bR);
-        ++nR;
-    };
+    const int qkblk0 = (b * p.Hk + hk) * NC;                   // [Q; K] block of chunk 0 of this kv head
 
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(bar + i, 1);
+        for (int i = 0; i < 10; ++i) mbar_init(bar + i, 1);
+        for (int i = 10; i < 13; ++i) mbar_init(bar + i, kFwdMathWarps);
+        for (int i = 13; i < 15; ++i) mbar_init(bar + i, 1);
         fence_mbar_init();
     }
-    if (tid == 32) tma_prefetch_map(&maps.vb);
-    if (tid == 128) {
-        tma_prefetch_map(&maps.y);
-        tma_prefetch_map(&maps.r);
+    if (warp == kFwdMathWarps + 1 && lane == 0) {
+        tma_prefetch_map(&maps.vb);
+        tma_prefetch_map(&maps.qk);
     }
-    if (warp == 0) tmem_alloc(tslot, 512);
-    const uint32_t lead = warp == 0 ? elect_one_sync() : 0u;   // the lane of warp 0 that issues products
+    if (warp == kFwdMathWarps) tmem_alloc(tslot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tSg = tmem, tD = tmem + DK, tQK = tmem + DK + 64, tPD = tmem + DK + 128;
+    const uint32_t tSg = tmem, tD = tmem + DK, tY = tmem + DK + 64, tU = tmem + DK + 128, tPy = tmem + DK + 192,
+                   tPu = tmem + DK + 256;
     griddep_wait();                                           // the previous kernel's writes are visible
     griddep_launch();
-    if (tid == 32) {
-        issue_w(0);
-        if (NC > 1) issue_w(1);
-        issue_r(0);
-    }
 
-    // this thread's fragment of the state (rows fs.row(k), columns fs.col(j, k))
-    const M64Frag fs(warp, lane, DK);
-    float S[NS];
-#pragma unroll
-    for (int j = 0; j < NS / 4; ++j)
-#pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {
-            float2 s2 = make_float2(0.f, 0.f);
-            if (p.S0 != nullptr)
-                s2 = *reinterpret_cast<const float2 *>(p.S0 + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0));
-            S[4 * j + 2 * k2] = s2.x;
-            S[4 * j + 2 * k2 + 1] = s2.y;
-        }
-    const M64Frag fd(warp, lane, kL);         // this thread's fragment of Delta (64 value columns)
-
-    // y and v - u of chunk cc (warps 4-7, one [y; u] row per thread: row t of y for warps 4-5,
-    // of u for warps 6-7), from tensor memory, staged in the 128-byte swizzle for TMA stores by
-    // thread 128. v of the chunk (u rows) was loaded one chunk earlier.
-    uint4 vx[8];
-    auto load_v = [&](int cc) {
-        const int r = 32 * (warp & 3) + lane, t = r & (kL - 1), tt0 = cc * kL;
-        const bool mine = r >= kL && tt0 + t < T;
-        const size_t o = (((size_t)b * T + tt0 + t) * Hv + h) * Dv + r0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) vx[i] = mine ? reinterpret_cast<const uint4 *>(v + o)[i] : make_uint4(0u, 0u, 0u, 0u);
-    };
-    auto epilogue = [&](int cc) {
-        const int r = 32 * (warp & 3) + lane, t = r & (kL - 1), sw = t & 7;
-        const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
-        const float gt = gm2[(cc & 1) * kL + t];
-#pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-            float a[32], bq[32];
-            tmem_ld32f(tQK + lo + 32 * hc, a);
-            tmem_ld32f(tPD + lo + 32 * hc, bq);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = fmaf(gt, a[i], bq[i]);
-            if (r < kL) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(ysg + t * 128 + (((4 * hc + j) ^ sw) << 4)) =
-                        pack8_bf16(*reinterpret_cast<const float (*)[8]>(a + 8 * j));
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float va[8];
-                    unpack8_bf16(vx[4 * hc + j], va);
-#pragma unroll
-                    for (int q4 = 0; q4 < 2; ++q4)
-                        *reinterpret_cast<float4 *>(rsg + hc * (kL * 128) + t * 128 + (((2 * j + q4) ^ sw) << 4)) =
-                            make_float4(va[4 * q4] - a[8 * j + 4 * q4], va[4 * q4 + 1] - a[8 * j + 4 * q4 + 1],
-                                        va[4 * q4 + 2] - a[8 * j + 4 * q4 + 2], va[4 * q4 + 3] - a[8 * j + 4 * q4 + 3]);
+    bool fail = false;
+    if (!math) {
+        regs_dec<kFwdCtrlRegs>();            // the whole control warpgroup, at one point of the code
+        if (warp == kFwdMathWarps) {
+            // ================================================================ product warp
+            const uint32_t lead = elect_one_sync();
+            constexpr uint32_t id64 = umma_idesc(1, kL, kL);
+            // U = (T diag(beta)) V starts Delta's accumulator (the first chunk's here, each later
+            // one once the previous Delta is read out)
+            {
+                const bool w = mbar_wait(bW, 0);
+                fail = __any_sync(kFullMask, !w);
+                if (!fail) {
+                    tc_fence_after();
+                    unsigned char *g = wbuf(0);
+                    umma_gemm_w(tD, CmOp{g + (L.tc - L.wc), kL, 0, 0, false}, CmOp{g + (L.vb - L.wc), kL, 0, 0, true}, kL,
+                                umma_idesc_t(1, kL, kL, false, true), false, lead);
                 }
             }
-        }
-        fence_proxy_async();
-        named_bar_sync(1, 128);
-        if (tid == 128) {
-            const int tt0 = cc * kL;
-            tma_store_4d(&maps.y, ysg, r0, h, tt0, b);
-            tma_store_5d(&maps.r, rsg, 0, tt0, r0 / 32, h, b);
-            bulk_commit();
-        }
-    };
-
-    unsigned wR = 0;
-    bool ok = true, fail = false;   // fail: a bounded wait of this thread ran out (all learn it at the next block barrier)
-    float lamn = 0.f;               // Lam of the next chunk (threads < 64)
-    if (tid < kL) lamn = p.lam[head * NC * kL + tid];
-    if (warp >= 4) load_v(0);
-    for (int c = 0; c < NC; ++c) {
-        const size_t chk = head * NC + c;
-        const int cb = c & 1;
-        // ---- (A) the previous chunk's stores have read sop (thread 32) and ysg, rsg (thread 128);
-        // this chunk's decays
-        if (tid == 32 || tid == 128) bulk_wait_read();
-        if (tid < kL) {
-            Lm2[cb * kL + tid] = lamn;
-            gm2[cb * kL + tid] = expf(lamn);
-            if (c + 1 < NC) lamn = p.lam[(chk + 1) * kL + tid];
-        }
-        ok = !__syncthreads_or(fail);
-        if (!ok) break;
-        if (tid < kL) eL[tid] = expf(Lm2[cb * kL + kL - 1] - Lm2[cb * kL + tid]);
-        // ---- (B) U = (T diag(beta)) V starts Delta's accumulator; S <- exp(Lam_L) S + Sigma of the
-        // previous chunk; S as an operand, and the fp32 checkpoint stored from registers
-        unsigned char *wc = wbuf(c), *tcs = wc + (L.tc - L.wc), *vb = wc + (L.vb - L.wc);
-        if (warp == 0) {
-            fail = !mbar_wait(bW + cb, (c >> 1) & 1);
-            if (!fail)
-                umma_gemm_w(tD, CmOp{tcs, kL, 0, 0, false}, CmOp{vb, kL, 0, 0, true}, kL,
+            for (int c = 0; c < NC && !fail; ++c) {
+                unsigned char *wc = wbuf(c), *kb = kbuf(c);
+                // ---- Delta += (-W) S^T once S is written
+                bool w = mbar_wait(bS, c & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+                umma_gemm_w(tD, CmOp{wc, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, true, lead);
+                umma_commit_w(mD, lead);
+                // ---- Q S^T and K S^T once the previous chunk's are read out and Q, K landed
+                w = (c == 0 || mbar_wait(bE, (c - 1) & 1)) && mbar_wait(cbQ, c & 1) && mbar_wait(cbK + (c & 1), (c >> 1) & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+                umma_gemm_w(tY, CmOp{qb, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, false, lead);
+                umma_gemm_w(tU, CmOp{kb, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, false, lead);
+                umma_commit_w(mQ, lead);
+                // ---- Sigma = (diag(E_L) Delta)^T K once Delta is written; then P Delta and KKm Delta
+                w = mbar_wait(bDt, c & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+                umma_gemm_w(tSg, CmOp{de, kL, 0, 0, true}, CmOp{kb, kL, 0, 0, true}, kL, umma_idesc_t(1, kL, DK, true, true),
+                            false, lead);
+                umma_commit_w(mU, lead);
+                w = mbar_wait(cbP, c & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+                umma_gemm_w(tPy, CmOp{pk, 2 * kL, 0, 0, false}, CmOp{dt, kL, 0, 0, true}, kL,
                             umma_idesc_t(1, kL, kL, false, true), false, lead);
+                umma_gemm_w(tPu, CmOp{pk, 2 * kL, kL, 0, false}, CmOp{dt, kL, 0, 0, true}, kL,
+                            umma_idesc_t(1, kL, kL, false, true), false, lead);
+                umma_commit_w(mY, lead);
+                // ---- U of the next chunk (Delta was read out before bDt)
+                if (c + 1 < NC) {
+                    w = mbar_wait(bW + ((c + 1) & 1), ((c + 1) >> 1) & 1);
+                    if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                    tc_fence_after();
+                    unsigned char *g = wbuf(c + 1);
+                    umma_gemm_w(tD, CmOp{g + (L.tc - L.wc), kL, 0, 0, false}, CmOp{g + (L.vb - L.wc), kL, 0, 0, true}, kL,
+                                umma_idesc_t(1, kL, kL, false, true), false, lead);
+                }
+            }
+            if (fail) {
+                // products still in flight finish before the tensor memory is freed (bounded wait)
+                umma_commit_w(mX, lead);
+                mbar_wait(mX, 0);
+            }
+        } else if (warp == kFwdMathWarps + 1) {
+            // ================================================================ copy warp (lane 0)
+            if (lane == 0) {
+                int nQ = 0, nP = 0, nW[2] = {0, 0}, nK[2] = {0, 0};
+                auto issue_w = [&](int cc) {               // group W of chunk cc: -W, T diag(beta), V of this block
+                    const size_t ck = head * NC + cc;
+                    unsigned char *g = wbuf(cc);
+                    uint64_t *bw = bW + (cc & 1);
+                    mbar_expect_tx(bw, kL * DK * 2 + 2 * kL * kL * 2);
+                    bulk_load(g, p.wm + ck * kL * DK, kL * DK * 2, bw);
+                    bulk_load(g + (L.tc - L.wc), p.tcm + ck * kL * kL, kL * kL * 2, bw);
+                    tma_load_5d(g + (L.vb - L.wc), &maps.vb, bw, 0, cc * kL, r0 / 8, h, b);
+                    ++nW[cc & 1];
+                };
+                auto copy_Q = [&](int cc) {                // Q of chunk cc: rows 0-63 of its [Q; K] block
+                    mbar_expect_tx(cbQ, kL * DK * 2);
+                    tma_load_5d(qb, &maps.qk, cbQ, 0, 0, 0, 0, qkblk0 + cc);
+                    ++nQ;
+                };
+                auto copy_K = [&](int cc) {                // K of chunk cc: rows 64-127
+                    mbar_expect_tx(cbK + (cc & 1), kL * DK * 2);
+                    tma_load_5d(kbuf(cc), &maps.qk, cbK + (cc & 1), 0, 0, 1, 0, qkblk0 + cc);
+                    ++nK[cc & 1];
+                };
+                auto copy_P = [&](int cc) {                // [P; KKm] of chunk cc
+                    mbar_expect_tx(cbP, 2 * kL * kL * 2);
+                    bulk_load(pk, p.pkm + (head * NC + cc) * 2 * kL * kL, 2 * kL * kL * 2, cbP);
+                    ++nP;
+                };
+                for (int cc = 0; cc < 2 && cc < NC; ++cc) {
+                    issue_w(cc);
+                    copy_K(cc);
+                }
+                copy_Q(0);
+                copy_P(0);
+                for (int c = 0; c < NC; ++c) {
+                    const size_t chk = head * NC + c;
+                    // the bf16 state leaves (the backward's operand) once written
+                    if (!mbar_wait(bS, c & 1)) { fail = true; break; }
+                    bulk_store(p.s0m + (chk * gridDim.x + split) * kL * DK, sop, kL * DK * 2);
+                    bulk_commit();
+                    // Q S^T and K S^T are done: Q is free
+                    if (!mbar_wait(mQ, c & 1)) { fail = true; break; }
+                    if (c + 1 < NC) copy_Q(c + 1);
+                    // Sigma is done: this K buffer is free (the chunk two ahead); Delta was read out
+                    // (bDt, before Sigma), so group W's buffer is free too; once the state's store
+                    // has read it, the state operand's tile is free
+                    if (!mbar_wait(mU, c & 1) || !mbar_wait(bDt, c & 1)) { fail = true; break; }
+                    bulk_wait_read();
+                    mbar_arrive(fS);
+                    if (c + 2 < NC) {
+                        copy_K(c + 2);
+                        issue_w(c + 2);
+                    }
+                    // P Delta and KKm Delta are done: [P; KKm] is free
+                    if (!mbar_wait(mY, c & 1)) { fail = true; break; }
+                    if (c + 1 < NC) copy_P(c + 1);
+                }
+                if (fail) {
+                    // copies still in flight land before the CTA exits (each wait bounded)
+                    if (nQ > 0) mbar_wait(cbQ, (nQ - 1) & 1);
+                    if (nP > 0) mbar_wait(cbP, (nP - 1) & 1);
+                    for (int i = 0; i < 2; ++i) {
+                        if (nW[i] > 0) mbar_wait(bW + i, (nW[i] - 1) & 1);
+                        if (nK[i] > 0) mbar_wait(cbK + i, (nK[i] - 1) & 1);
+                    }
+                }
+                bulk_wait_all();                            // the bf16 states are complete
+            }
+            fail = __shfl_sync(kFullMask, fail, 0);
         }
-        if (c > 0) {
-            fail = !mbar_wait(mU, (c - 1) & 1) || fail;
-            tc_fence_after();
-            const float decay = gm2[(cb ^ 1) * kL + kL - 1];
+    } else {
+        regs_inc<kFwdMathRegs>();
+        // ================================================================ math warps
+        // this thread's fragment of the state (rows fs.row(k), columns fs.col(j, k)) and of the
+        // 64-column accumulators (chunk rows ta, tb, value columns fd.col(j, 0), + 1)
+        const M64Frag fs(warp, lane, DK), fd(warp, lane, kL);
+        const int ta = fd.row(0), tb = fd.row(2);
+        float S[NS];
 #pragma unroll
-            for (int i = 0; i < NS / 16; ++i) {
-                float x[16];
-                tmem_ld16x256_x4(tSg + lane16 + SC * (warp >> 2) + 32 * i, x);
+        for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                float2 s2 = make_float2(0.f, 0.f);
+                if (p.S0 != nullptr)
+                    s2 = *reinterpret_cast<const float2 *>(p.S0 + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0));
+                S[4 * j + 2 * k2] = s2.x;
+                S[4 * j + 2 * k2 + 1] = s2.y;
+            }
+        const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
+        __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
+        // Lam_L, Lam_ta, Lam_tb and v of rows ta, tb (this thread's columns) of chunk cc, loaded
+        // a chunk ahead and kept raw until used (rows past T: v zeros)
+        float nlL, nla, nlb;
+        uint32_t nva[4], nvb[4];
+        auto load_lam = [&](int cc) {
+            const float *lm = p.lam + (head * NC + cc) * kL;
+            nlL = lm[kL - 1];
+            nla = lm[ta];
+            nlb = lm[tb];
+        };
+        auto load_v = [&](int cc) {
+            const int tt0 = cc * kL, ln = min(kL, T - tt0);
+            const size_t ra = (((size_t)b * T + tt0 + ta) * Hv + h) * Dv + r0, rb = (((size_t)b * T + tt0 + tb) * Hv + h) * Dv + r0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = fd.col(j, 0);
+                nva[j] = ta < ln ? *reinterpret_cast<const uint32_t *>(v + ra + col) : 0u;
+                nvb[j] = tb < ln ? *reinterpret_cast<const uint32_t *>(v + rb + col) : 0u;
+            }
+        };
+        // the state as a bf16 operand (stmatrix: 4 8x8 blocks per instruction)
+        auto write_sop = [&]() {
+#pragma unroll
+            for (int j = 0; j < NS / 4; j += 2) {
+                const uint32_t a = frag_row_addr(smem_addr(sop), kL, 16 * (warp & 3), (DK / 16) * hw + j, lane);
+                stmatrix_x4(a, pack2_bf16(S[4 * j], S[4 * j + 1]), pack2_bf16(S[4 * j + 2], S[4 * j + 3]),
+                            pack2_bf16(S[4 * j + 4], S[4 * j + 5]), pack2_bf16(S[4 * j + 6], S[4 * j + 7]));
+            }
+        };
+        auto warp_done = [&](uint64_t *bar_) {
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_);
+        };
+        // y and v - u of chunk cc from tensor memory (its decays: ga, gb = exp(Lam) of rows ta,
+        // tb; v pairs va, vb), stored from registers (rows past T are not written)
+        auto epilogue = [&](int cc, float ga, float gb, const uint32_t (&va)[4], const uint32_t (&vb)[4]) {
+            const int tt0 = cc * kL, ln = min(kL, T - tt0);
+            const size_t ra = ((size_t)b * T + tt0 + ta) * Hv + h, rb = ((size_t)b * T + tt0 + tb) * Hv + h;
+            {
+                float q[16], pq[16];
+                tmem_ld16x256_x4(tY + lane16 + 32 * hw, q);
+                tmem_ld16x256_x4(tPy + lane16 + 32 * hw, pq);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) S[16 * i + e] = fmaf(decay, S[16 * i + e], x[e]);
+                for (int j = 0; j < 4; ++j) {
+                    const int col = r0 + fd.col(j, 0);
+                    if (ta < ln)
+                        *reinterpret_cast<uint32_t *>(y + ra * Dv + col) =
+                            pack2_bf16(fmaf(ga, q[4 * j], pq[4 * j]), fmaf(ga, q[4 * j + 1], pq[4 * j + 1]));
+                    if (tb < ln)
+                        *reinterpret_cast<uint32_t *>(y + rb * Dv + col) =
+                            pack2_bf16(fmaf(gb, q[4 * j + 2], pq[4 * j + 2]), fmaf(gb, q[4 * j + 3], pq[4 * j + 3]));
+                }
             }
-            // the previous chunk's [y; u] products are done: sop, [Q; K] and [P; KKm] are free
-            fail = !mbar_wait(mY, (c - 1) & 1) || fail;
+            {
+                float k[16], pu[16];
+                tmem_ld16x256_x4(tU + lane16 + 32 * hw, k);
+                tmem_ld16x256_x4(tPu + lane16 + 32 * hw, pu);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int col = r0 + fd.col(j, 0);
+                    const float2 xa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&va[j]));
+                    const float2 xb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&vb[j]));
+                    if (ta < ln)
+                        *reinterpret_cast<float2 *>(p.resid + ra * Dv + col) =
+                            make_float2(xa.x - fmaf(ga, k[4 * j], pu[4 * j]), xa.y - fmaf(ga, k[4 * j + 1], pu[4 * j + 1]));
+                    if (tb < ln)
+                        *reinterpret_cast<float2 *>(p.resid + rb * Dv + col) =
+                            make_float2(xb.x - fmaf(gb, k[4 * j + 2], pu[4 * j + 2]), xb.y - fmaf(gb, k[4 * j + 3], pu[4 * j + 3]));
+                }
+            }
+        };
+        load_lam(0);
+        load_v(0);
+        float decay = 1.f, pga = 1.f, pgb = 1.f;     // exp(Lam_L), exp(Lam_ta), exp(Lam_tb) of the previous chunk
+        uint32_t pva[4], pvb[4];                      // v pairs of the previous chunk
+        for (int c = 0; c < NC; ++c) {
+            const size_t chk = head * NC + c;
+            const float lL = nlL, la = nla, lb = nlb;
+            uint32_t cva[4], cvb[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                cva[j] = nva[j];
+                cvb[j] = nvb[j];
+            }
+            if (c + 1 < NC) {
+                load_lam(c + 1);
+                load_v(c + 1);
+            }
+            // ---- S <- exp(Lam_L) S + Sigma of the previous chunk; S as an operand, and the fp32
+            // checkpoint stored from registers
+            if (c > 0) {
+                const bool w = mbar_wait(mU, (c - 1) & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < NS / 16; ++i) {
+                    float x[16];
+                    tmem_ld16x256_x4(tSg + lane16 + SC * hw + 32 * i, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) S[16 * i + e] = fmaf(decay, S[16 * i + e], x[e]);
+                }
+                // the state operand's tile: the previous chunk's products and store are done with it
+                const bool w2 = mbar_wait(fS, (c - 1) & 1);
+                if (__any_sync(kFullMask, !w2)) { fail = true; break; }
+            }
+            write_sop();
+            warp_done(bS);
+            {
+                // a warp's store covers 8 rows x 32 contiguous bytes: whole 32-byte sectors; streamed
+                // (the backward reads the bf16 copy)
+                float *ck = p.ckpt + (chk * Dv + r0) * DK;
+#pragma unroll
+                for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+                    for (int k2 = 0; k2 < 2; ++k2)
+                        __stcs(reinterpret_cast<float2 *>(ck + fs.row(2 * k2) * DK + fs.col(j, 0)),
+                               make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]));
+            }
+            // ---- y and v - u of the previous chunk
+            if (c > 0) {
+                const bool w = mbar_wait(mY, (c - 1) & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
+                epilogue(c - 1, pga, pgb, pva, pvb);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bE);
+            }
+            // ---- Delta as operands: Delta (for P Delta, KKm Delta) and diag(E_L) Delta (for the
+            // update); their tiles are free since the previous chunk's products are done (mY)
+            {
+                const bool w = mbar_wait(mD, c & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+            }
             tc_fence_after();
-            if (tid == 32) issue_r(c);
-        }
-        {
-            // a warp's store covers 8 rows x 32 contiguous bytes: whole 32-byte sectors; streamed
-            // (the backward reads the bf16 copy)
-            float *ck = p.ckpt + (chk * Dv + r0) * DK;
+            {
+                float x[16];
+                tmem_ld16x256_x4(tD + lane16 + 32 * hw, x);
+                tmem_wait_ld();
+                const float ea = expf(lL - la), eb = expf(lL - lb);
 #pragma unroll
-            for (int j = 0; j < NS / 4; ++j)
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int row = fs.row(2 * k2), col = fs.col(j, 0);
-                    const float s0 = S[4 * j + 2 * k2], s1 = S[4 * j + 2 * k2 + 1];
-                    *reinterpret_cast<uint32_t *>(sop + cm_off(row, 2 * col, kL)) = pack2_bf16(s0, s1);
-                    __stcs(reinterpret_cast<float2 *>(ck + row * DK + col), make_float2(s0, s1));
+                for (int j = 0; j < 4; j += 2) {
+                    const uint32_t o = frag_row_addr(0, kL, 16 * (warp & 3), 4 * hw + j, lane);
+                    stmatrix_x4(smem_addr(dt) + o, pack2_bf16(x[4 * j], x[4 * j + 1]), pack2_bf16(x[4 * j + 2], x[4 * j + 3]),
+                                pack2_bf16(x[4 * j + 4], x[4 * j + 5]), pack2_bf16(x[4 * j + 6], x[4 * j + 7]));
+                    stmatrix_x4(smem_addr(de) + o, pack2_bf16(ea * x[4 * j], ea * x[4 * j + 1]),
+                                pack2_bf16(eb * x[4 * j + 2], eb * x[4 * j + 3]), pack2_bf16(ea * x[4 * j + 4], ea * x[4 * j + 5]),
+                                pack2_bf16(eb * x[4 * j + 6], eb * x[4 * j + 7]));
                 }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        ok = !__syncthreads_or(fail);
-        tc_fence_after();
-        if (!ok) break;
-        // ---- (C) Delta += (-W) S^T; the bf16 state leaves (the backward's operand); y and v - u of
-        // the previous chunk
-        if (warp == 0) {
-            umma_gemm_w(tD, CmOp{wc, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, umma_idesc(1, kL, kL), true, lead);
-            umma_commit_w(mD, lead);
-        }
-        if (tid == 32) {
-            bulk_store(p.s0m + (chk * gridDim.x + split) * kL * DK, sop, kL * DK * 2);
-            bulk_commit();
-        }
-        if (warp >= 4) {
-            if (c > 0) epilogue(c - 1);
-            load_v(c);
-        }
-        // ---- (D) Delta as operands: Delta (for [P; KKm] Delta) and diag(E_L) Delta (for the update)
-        fail = !mbar_wait(mD, c & 1);
-        tc_fence_after();
-        if (tid == 32 && c + 2 < NC) issue_w(c + 2);       // this buffer of group W is free again
-        {
-            float x[16];
-            tmem_ld16x256_x4(tD + lane16 + 32 * (warp >> 2), x);
-            tmem_wait_ld();
-            const float ea = eL[fd.row(0)], eb = eL[fd.row(2)];
+            }
+            warp_done(bDt);
+            decay = expf(lL);
+            pga = expf(la);
+            pgb = expf(lb);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int t = fd.row(2 * k2), col = fd.col(j, 0);
-                    const float d0 = x[4 * j + 2 * k2], d1 = x[4 * j + 2 * k2 + 1], el = k2 ? eb : ea;
-                    const uint32_t o = cm_off(t, 2 * col, kL);
-                    *reinterpret_cast<uint32_t *>(dt + o) = pack2_bf16(d0, d1);
-                    *reinterpret_cast<uint32_t *>(de + o) = pack2_bf16(el * d0, el * d1);
-                }
+            for (int j = 0; j < 4; ++j) {
+                pva[j] = cva[j];
+                pvb[j] = cvb[j];
+            }
         }
-        fence_proxy_async();
-        tc_fence_before();
-        ok = !__syncthreads_or(fail);
-        tc_fence_after();
-        if (!ok) break;
-        // ---- (E) Sigma = (diag(E_L) Delta)^T K (the next chunk's state waits only for this), then
-        // [Q; K] S^T and [P; KKm] Delta. No block barrier follows: the next chunk's first section
-        // waits for what it reads.
-        if (warp == 0) {
-            fail = !mbar_wait(bR, wR & 1);
-            ++wR;
+        if (!fail) {
+            // the last chunk: its update, S_T, and its y and v - u
+            bool w = mbar_wait(mU, (NC - 1) & 1);
+            fail = __any_sync(kFullMask, !w);
             if (!fail) {
-                umma_gemm_w(tSg, CmOp{de, kL, 0, 0, true}, CmOp{qk, 2 * kL, 0, kL, true}, kL,
-                            umma_idesc_t(1, kL, DK, true, true), false, lead);
-                umma_commit_w(mU, lead);
-                umma_gemm_w(tQK, CmOp{qk, 2 * kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK,
-                            umma_idesc(1, 2 * kL, kL), false, lead);
-                umma_gemm_w(tPD, CmOp{pk, 2 * kL, 0, 0, false}, CmOp{dt, kL, 0, 0, true}, kL,
-                            umma_idesc_t(1, 2 * kL, kL, false, true), false, lead);
-                umma_commit_w(mY, lead);
+                tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < NS / 16; ++i) {
+                    float x[16];
+                    tmem_ld16x256_x4(tSg + lane16 + SC * hw + 32 * i, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) S[16 * i + e] = fmaf(decay, S[16 * i + e], x[e]);
+                }
+                if (p.S_T != nullptr)
+#pragma unroll
+                    for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+                        for (int k2 = 0; k2 < 2; ++k2)
+                            *reinterpret_cast<float2 *>(p.S_T + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0)) =
+                                make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]);
+                w = mbar_wait(mY, (NC - 1) & 1);
+                fail = __any_sync(kFullMask, !w);
+                if (!fail) {
+                    tc_fence_after();
+                    epilogue(NC - 1, pga, pgb, pva, pvb);
+                }
             }
         }
     }
-    if (ok) ok = !__syncthreads_or(fail);                  // a wait of the last chunk's products group
-    if (ok) {
-        // the last chunk: its update, S_T, and its y and v - u
-        fail = !mbar_wait(mU, (NC - 1) & 1);
-        tc_fence_after();
-        const float decay = gm2[((NC - 1) & 1) * kL + kL - 1];
-#pragma unroll
-        for (int i = 0; i < NS / 16; ++i) {
-            float x[16];
-            tmem_ld16x256_x4(tSg + lane16 + SC * (warp >> 2) + 32 * i, x);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) S[16 * i + e] = fmaf(decay, S[16 * i + e], x[e]);
-        }
-        if (p.S_T != nullptr)
-#pragma unroll
-            for (int j = 0; j < NS / 4; ++j)
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2)
-                    *reinterpret_cast<float2 *>(p.S_T + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0)) =
-                        make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]);
-        fail = !mbar_wait(mY, (NC - 1) & 1) || fail;
-        tc_fence_after();
-        if (tid == 128) bulk_wait_read();                   // the previous y and v - u stores have read ysg, rsg
-        ok = !__syncthreads_or(fail);
-        if (ok && warp >= 4) epilogue(NC - 1);
-    }
-    if (!ok && tid == 32) {
-        report_status(p.status, kStatusTimeout);
-        // copies still in flight land before the CTA exits (each wait bounded)
-        if (nW0 > 0) mbar_wait(bW, (nW0 - 1) & 1);
-        if (nW1 > 0) mbar_wait(bW + 1, (nW1 - 1) & 1);
-        if (nR > 0) mbar_wait(bR, (nR - 1) & 1);
-    }
-    if (!ok && warp == 0) {
-        // products still in flight finish before the tensor memory is freed (bounded wait)
-        umma_commit_w(mX, lead);
-        mbar_wait(mX, 0);
-    }
-    if (tid == 32 || tid == 128) bulk_wait_all();           // no store still reads shared memory
+    if (fail && lane == 0) report_status(p.status, kStatusTimeout);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == kFwdMathWarps) tmem_dealloc(tmem, 512);
 }
 
 size_t chunk_prep_smem(int Dk, int Dv) {
@@ -803,6 +918,12 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const ChunkFwdMaps &maps
     // two prep CTAs share an SM: ask for the largest shared-memory carve-out
     err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (err != cudaSuccess) return err;
+    // the sweep's register split waits for registers that only a launch of kFwdLaunchRegs per
+    // thread provides
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, chunk_sweep_kernel<E>);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs < kFwdLaunchRegs || fa.maxThreadsPerBlock < kFwdThreads) return cudaErrorInvalidConfiguration;
     err = cudaFuncSetAttribute(chunk_sweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_prep", 0, s);
@@ -817,7 +938,7 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const ChunkFwdMaps &maps
     timing_mark("chunk_prep", 1, s);
     if (err != cudaSuccess) return err;
     timing_mark("chunk_sweep", 0, s);
-    err = launch_pdl(chunk_sweep_kernel<E>, dim3(p.Dv / kL, p.Hv, p.B), dim3(256), ss, s, p, maps);
+    err = launch_pdl(chunk_sweep_kernel<E>, dim3(p.Dv / kL, p.Hv, p.B), dim3(kFwdThreads), ss, s, p, maps);
     timing_mark("chunk_sweep", 1, s);
     return err;
 }
