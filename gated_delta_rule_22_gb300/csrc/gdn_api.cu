@@ -432,7 +432,7 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         cp.status = fp.status;
         cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
         gdn::ChunkFwdMaps maps;
-        if ((rc = make_colblock_map(&maps.vb, v, true, p.B, p.T, p.Hv, p.Dv, 8, 64, 8, false)) != GDN_OK ||
+        if ((rc = make_btd_map(&maps.vb, v, true, p.B, p.T, p.Hv, p.Dv, 64, 64, true)) != GDN_OK ||
             (rc = make_colblock_map(&maps.k, k, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
             (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
             (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK)

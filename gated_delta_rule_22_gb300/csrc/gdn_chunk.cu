@@ -459,7 +459,7 @@ struct SweepSmem {
         wgrp = (size_t)kL * DK * 2 + 2 * (size_t)kL * kL * 2;
         wc = o;                                // -W of the chunk                    A [64][DK]
         tc = wc + (size_t)kL * DK * 2;         // T diag(beta)                       A [64][64]
-        vb = tc + (size_t)kL * kL * 2;         // V of the chunk, this block's 64 columns [64 t][64 v] (read MN-major)
+        vb = tc + (size_t)kL * kL * 2;         // V of the chunk, this block's 64 columns [64 t][64 v], 128-byte swizzle (read MN-major)
         o += 2 * wgrp;
         qb = o; o += (size_t)kL * DK * 2;      // Q of the chunk (kv head)           A [64][DK]
         kb = o; o += (size_t)2 * kL * DK * 2;  // K, two buffers                     A [64][DK]; read MN-major as B
@@ -468,6 +468,8 @@ struct SweepSmem {
         dt = o; o += (size_t)kL * kL * 2;      // Delta [64 t][64 v], read MN-major (B)
         de = o; o += (size_t)kL * kL * 2;      // diag(E_L) Delta [64 t][64 v], read MN-major (A, transposed)
         bar = al(o, 8); o = bar + 16 * 8;      // see the kernel
+        // (V is read in the 128-byte swizzle: its tiles start at 1024-byte boundaries, as do both
+        // groups W for every DK here: the W tile is a multiple of 8 KB)
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -561,8 +563,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 if (!fail) {
                     tc_fence_after();
                     unsigned char *g = wbuf(0);
-                    umma_gemm_w(tD, CmOp{g + (L.tc - L.wc), kL, 0, 0, false}, CmOp{g + (L.vb - L.wc), kL, 0, 0, true}, kL,
-                                umma_idesc_t(1, kL, kL, false, true), false, lead);
+                    umma_gemm_wd(tD, CmOp{g + (L.tc - L.wc), kL, 0, 0, false}, sw128_mnmajor(g + (L.vb - L.wc)), 2048 >> 4,
+                                 kL, umma_idesc_t(1, kL, kL, false, true), false, lead);
                 }
             }
             for (int c = 0; c < NC && !fail; ++c) {
@@ -601,8 +603,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     if (__any_sync(kFullMask, !w)) { fail = true; break; }
                     tc_fence_after();
                     unsigned char *g = wbuf(c + 1);
-                    umma_gemm_w(tD, CmOp{g + (L.tc - L.wc), kL, 0, 0, false}, CmOp{g + (L.vb - L.wc), kL, 0, 0, true}, kL,
-                                umma_idesc_t(1, kL, kL, false, true), false, lead);
+                    umma_gemm_wd(tD, CmOp{g + (L.tc - L.wc), kL, 0, 0, false}, sw128_mnmajor(g + (L.vb - L.wc)), 2048 >> 4,
+                                 kL, umma_idesc_t(1, kL, kL, false, true), false, lead);
                 }
             }
             if (fail) {
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     mbar_expect_tx(bw, kL * DK * 2 + 2 * kL * kL * 2);
                     bulk_load(g, p.wm + ck * kL * DK, kL * DK * 2, bw);
                     bulk_load(g + (L.tc - L.wc), p.tcm + ck * kL * kL, kL * kL * 2, bw);
-                    tma_load_5d(g + (L.vb - L.wc), &maps.vb, bw, 0, cc * kL, r0 / 8, h, b);
+                    tma_load_4d(g + (L.vb - L.wc), &maps.vb, bw, r0, h, cc * kL, b);
                     ++nW[cc & 1];
                 };
                 auto copy_Q = [&](int cc) {                // Q of chunk cc: rows 0-63 of its [Q; K] block

@@ -483,10 +483,10 @@ size_t bwd_smem_bytes(int Dk, int C, int dtype, int slots);
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // Chunkwise forward: Dk in {64, 128, 192}, Dv a multiple of 64 up to 256, bf16, C = 64.
-// Tensor maps, no swizzle. Read by TMA loads in 1 KB core-matrix columns of 64 rows: k and q as
-// 5-D column blocks of [B][T][Hk][Dk] {8, T, Dk / 8, Hk, B}, box {8, 64, Dk / 8, 1, 1}; vb, v as
-// 5-D column blocks of [B][T][Hv][Dv] {8, T, Dv / 8, Hv, B}, box {8, 64, 8, 1, 1} (64 value
-// columns). qk, the [Q; K] buffer as {256, 2, 2 halves (Q, K), Dk / 8 chunks, B*Hk*NC blocks},
+// Tensor maps. Read by TMA loads in 1 KB core-matrix columns of 64 rows (no swizzle): k and q as
+// 5-D column blocks of [B][T][Hk][Dk] {8, T, Dk / 8, Hk, B}, box {8, 64, Dk / 8, 1, 1}. vb: v as
+// [B][T][Hv][Dv] bf16, 4-D {Dv, Hv, T, B}, box {64, 1, 64, 1} (64 value columns of 64 steps),
+// 128-byte swizzle. qk, the [Q; K] buffer as {256, 2, 2 halves (Q, K), Dk / 8 chunks, B*Hk*NC blocks},
 // box {256, 2, 1, Dk / 8, 1} (a half's 64 rows of a K chunk are 1 KB contiguous): written by
 // TMA stores from an operand tile of 64 rows, read back the same way.
 struct ChunkFwdMaps {

@@ -53,6 +53,18 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t start, uint32_t lbo, uin
     return d;
 }
 
+// MN-major operand in the 128-byte swizzle (what a TMA box of 64 bf16 columns x rows with
+// CU_TENSOR_MAP_SWIZZLE_128B writes at a 1024-byte aligned address): K index = tile row (128
+// bytes, the 16-byte chunks of row r permuted by r % 8), MN index = column (64 of them, one
+// swizzle atom wide). Atoms of 8 rows follow each other at 1024 bytes along K (the stride
+// field); along MN there is one atom (the leading field is not used). A step of 16 along K
+// moves the start by 2048 bytes.
+__device__ __forceinline__ uint64_t sw128_mnmajor(const void *tile) {
+    uint64_t d = umma_sdesc(smem_addr(tile), 1024u, 1024u);
+    d |= (uint64_t)2 << 61;   // layout: 128-byte swizzle
+    return d;
+}
+
 // K-major view of an array with R rows: operand rows from array row r0, K from byte kb0.
 __device__ __forceinline__ uint64_t cm_kmajor(const void *base, int R, int r0, int kb0) {
     return umma_sdesc(smem_addr(base) + (uint32_t)(((kb0 >> 4) * (R >> 3) + (r0 >> 3)) * 128), (uint32_t)(R * 16),
@@ -181,6 +193,19 @@ __device__ __forceinline__ void umma_gemm_w(uint32_t d_tmem, const CmOp &A, cons
                                             bool accumulate, uint32_t lead) {
     uint64_t a = A.desc(0), b = B.desc(0);
     const uint64_t da = A.mn ? 16u : (uint64_t)(2 * A.R), db = B.mn ? 16u : (uint64_t)(2 * B.R);
+    for (int k = 0; k < K; k += 16) {
+        umma_bf16_w(d_tmem, a, b, idesc, accumulate || k > 0, lead);
+        a += da;
+        b += db;
+    }
+}
+
+// The same with B given by a descriptor and its step per 16 along K (in the start field's
+// 16-byte units), e.g. a swizzled operand.
+__device__ __forceinline__ void umma_gemm_wd(uint32_t d_tmem, const CmOp &A, uint64_t b, uint64_t db, int K,
+                                             uint32_t idesc, bool accumulate, uint32_t lead) {
+    uint64_t a = A.desc(0);
+    const uint64_t da = A.mn ? 16u : (uint64_t)(2 * A.R);
     for (int k = 0; k < K; k += 16) {
         umma_bf16_w(d_tmem, a, b, idesc, accumulate || k > 0, lead);
         a += da;
