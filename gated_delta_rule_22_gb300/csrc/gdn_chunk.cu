@@ -795,8 +795,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 load_lam(c + 1);
                 load_v(c + 1);
             }
-            // ---- S <- exp(Lam_L) S + Sigma of the previous chunk; S as an operand, and the fp32
-            // checkpoint stored from registers
+            // ---- S <- exp(Lam_L) S + Sigma of the previous chunk; S as an operand
             if (c > 0) {
                 const bool w = mbar_wait(mU, (c - 1) & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
@@ -815,17 +814,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             }
             write_sop();
             warp_done(bS);
-            {
-                // a warp's store covers 8 rows x 32 contiguous bytes: whole 32-byte sectors; streamed
-                // (the backward reads the bf16 copy)
-                float *ck = p.ckpt + (chk * Dv + r0) * DK;
-#pragma unroll
-                for (int j = 0; j < NS / 4; ++j)
-#pragma unroll
-                    for (int k2 = 0; k2 < 2; ++k2)
-                        __stcs(reinterpret_cast<float2 *>(ck + fs.row(2 * k2) * DK + fs.col(j, 0)),
-                               make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]));
-            }
             // ---- y and v - u of the previous chunk
             if (c > 0) {
                 const bool w = mbar_wait(mY, (c - 1) & 1);
@@ -859,6 +847,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 }
             }
             warp_done(bDt);
+            {
+                // the fp32 checkpoint from registers while Sigma runs (off the path from S to the
+                // next chunk's products): a warp's store covers 8 rows x 32 contiguous bytes, whole
+                // 32-byte sectors; streamed (the backward reads the bf16 copy)
+                float *ck = p.ckpt + (chk * Dv + r0) * DK;
+#pragma unroll
+                for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+                    for (int k2 = 0; k2 < 2; ++k2)
+                        __stcs(reinterpret_cast<float2 *>(ck + fs.row(2 * k2) * DK + fs.col(j, 0)),
+                               make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]));
+            }
             decay = expf(lL);
             pga = expf(la);
             pgb = expf(lb);
