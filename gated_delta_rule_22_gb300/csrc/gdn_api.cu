@@ -435,7 +435,9 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         if ((rc = make_btd_map(&maps.vb, v, true, p.B, p.T, p.Hv, p.Dv, 64, 64, true)) != GDN_OK ||
             (rc = make_colblock_map(&maps.k, k, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
             (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
-            (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK)
+            (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK ||
+            (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
+            (rc = make_colblock_map(&maps.r, fp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK)
             return rc;
         return cuda_status(gdn::launch_chunk_fwd(cp, maps, p.Dk, (cudaStream_t)stream));
     }

@@ -61,13 +61,6 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
     return u;
 }
 
-__device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&x)[8]) {
-    x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
-    x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
-    x[4] = __uint_as_float(u.z << 16); x[5] = __uint_as_float(u.z & 0xffff0000u);
-    x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
-}
-
 // T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kP), in two levels of 2 x 2
 // block recursion: the four diagonal 16 x 16 blocks by forward substitution (a column per
 // thread); then the two 32 x 32 diagonal blocks, and then the 64 x 64, each by
@@ -452,7 +445,7 @@ constexpr int kFwdLaunchRegs = 168, kFwdMathRegs = 176, kFwdCtrlRegs = 152;
 static_assert(2 * 128 * kFwdMathRegs + 128 * kFwdCtrlRegs <= kFwdThreads * kFwdLaunchRegs, "register split");
 
 struct SweepSmem {
-    size_t wgrp, wc, tc, vb, qb, kb, pk, sop, dt, de, bar, tslot, total;
+    size_t wgrp, wc, tc, vb, qb, kb, pk, sop, dt, de, ysg, rsg, bar, tslot, total;
     __host__ __device__ SweepSmem(int DK) {
         size_t o = 0;
         // group W, two buffers (chunks alternate): -W, T diag(beta), V
@@ -462,11 +455,13 @@ struct SweepSmem {
         vb = tc + (size_t)kL * kL * 2;         // V of the chunk, this block's 64 columns [64 t][64 v], 128-byte swizzle (read MN-major)
         o += 2 * wgrp;
         qb = o; o += (size_t)kL * DK * 2;      // Q of the chunk (kv head)           A [64][DK]
-        kb = o; o += (size_t)2 * kL * DK * 2;  // K, two buffers                     A [64][DK]; read MN-major as B
+        kb = o; o += (size_t)kL * DK * 2;      // K of the chunk                     A [64][DK]; read MN-major as B
         pk = o; o += (size_t)2 * kL * kL * 2;  // [(Q K^T) o E_incl; (K K^T) o E_strict]   A [128][64]
         sop = o; o += (size_t)kL * DK * 2;     // S (64 value rows)                  B [64][DK]
         dt = o; o += (size_t)kL * kL * 2;      // Delta [64 t][64 v], read MN-major (B)
         de = o; o += (size_t)kL * kL * 2;      // diag(E_L) Delta [64 t][64 v], read MN-major (A, transposed)
+        ysg = al(o, 1024); o = ysg + (size_t)kL * 128;       // y of a chunk, bf16 [64][64] in the 128-byte swizzle
+        rsg = al(o, 1024); o = rsg + (size_t)2 * kL * 128;   // v - u of a chunk, fp32 [2][64][32] in the 128-byte swizzle
         bar = al(o, 8); o = bar + 16 * 8;      // see the kernel
         // (V is read in the 128-byte swizzle: its tiles start at 1024-byte boundaries, as do both
         // groups W for every DK here: the W tile is a multiple of 8 KB)
@@ -495,8 +490,9 @@ struct SweepSmem {
 //                                      y and u read out;  bDt  Delta written as operands
 //   control -> math: mD, mQ, mU, mY  the product groups (commits);  fS  the state operand's
 //                    tile is free (the products that read it are done, its store has read it)
-// Q and K arrive as separate [64][DK] tiles (boxes of the [Q; K] block), K double-buffered and
-// fetched two chunks ahead, as is group W. y and v - u leave from registers.
+// Q and K arrive as separate [64][DK] tiles (boxes of the [Q; K] block); group W is
+// double-buffered and fetched two chunks ahead. y and v - u leave by TMA stores from staging
+// tiles (the copy warp, once bE says they are written).
 template <int E>
 __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ ChunkFwdMaps maps) {
     constexpr int DK = 32 * E;
@@ -513,16 +509,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(al(reinterpret_cast<size_t>(smem_raw), 1024));
     const SweepSmem L(DK);
-    unsigned char *qb = base + L.qb, *kb2 = base + L.kb, *pk = base + L.pk;
-    unsigned char *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de;
+    unsigned char *qb = base + L.qb, *kb = base + L.kb, *pk = base + L.pk;
+    unsigned char *sop = base + L.sop, *dt = base + L.dt, *de = base + L.de, *ysg = base + L.ysg, *rsg = base + L.rsg;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
     uint64_t *mD = bar, *mQ = bar + 1, *mU = bar + 2, *mY = bar + 3, *cbQ = bar + 4, *cbP = bar + 5;
-    uint64_t *bW = bar + 6, *cbK = bar + 8;                     // [2] each: one per buffer
+    uint64_t *bW = bar + 6, *cbK = bar + 8;                     // bW[2]: one per buffer
     uint64_t *bS = bar + 10, *bE = bar + 11, *bDt = bar + 12, *fS = bar + 13, *mX = bar + 14;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
-    // the buffers of chunk c: group W (-W, T diag(beta), V) and K
+    // the buffer of chunk c's group W (-W, T diag(beta), V)
     auto wbuf = [&](int c) { return base + L.wc + (size_t)(c & 1) * L.wgrp; };
-    auto kbuf = [&](int c) { return kb2 + (size_t)(c & 1) * kL * DK * 2; };
 
     const size_t head = (size_t)b * Hv + h;
     const int hk = h / (Hv / p.Hk);
@@ -537,6 +532,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
     if (warp == kFwdMathWarps + 1 && lane == 0) {
         tma_prefetch_map(&maps.vb);
         tma_prefetch_map(&maps.qk);
+        tma_prefetch_map(&maps.y);
+        tma_prefetch_map(&maps.r);
     }
     if (warp == kFwdMathWarps) tmem_alloc(tslot, 512);
     tc_fence_before();
@@ -568,7 +565,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 }
             }
             for (int c = 0; c < NC && !fail; ++c) {
-                unsigned char *wc = wbuf(c), *kb = kbuf(c);
+                unsigned char *wc = wbuf(c);
                 // ---- Delta += (-W) S^T once S is written
                 bool w = mbar_wait(bS, c & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
@@ -576,7 +573,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 umma_gemm_w(tD, CmOp{wc, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, true, lead);
                 umma_commit_w(mD, lead);
                 // ---- Q S^T and K S^T once the previous chunk's are read out and Q, K landed
-                w = (c == 0 || mbar_wait(bE, (c - 1) & 1)) && mbar_wait(cbQ, c & 1) && mbar_wait(cbK + (c & 1), (c >> 1) & 1);
+                w = (c == 0 || mbar_wait(bE, (c - 1) & 1)) && mbar_wait(cbQ, c & 1) && mbar_wait(cbK, c & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
                 umma_gemm_w(tY, CmOp{qb, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, false, lead);
@@ -615,7 +612,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
         } else if (warp == kFwdMathWarps + 1) {
             // ================================================================ copy warp (lane 0)
             if (lane == 0) {
-                int nQ = 0, nP = 0, nW[2] = {0, 0}, nK[2] = {0, 0};
+                int nQ = 0, nP = 0, nK = 0, nW[2] = {0, 0};
                 auto issue_w = [&](int cc) {               // group W of chunk cc: -W, T diag(beta), V of this block
                     const size_t ck = head * NC + cc;
                     unsigned char *g = wbuf(cc);
@@ -632,19 +629,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     ++nQ;
                 };
                 auto copy_K = [&](int cc) {                // K of chunk cc: rows 64-127
-                    mbar_expect_tx(cbK + (cc & 1), kL * DK * 2);
-                    tma_load_5d(kbuf(cc), &maps.qk, cbK + (cc & 1), 0, 0, 1, 0, qkblk0 + cc);
-                    ++nK[cc & 1];
+                    mbar_expect_tx(cbK, kL * DK * 2);
+                    tma_load_5d(kb, &maps.qk, cbK, 0, 0, 1, 0, qkblk0 + cc);
+                    ++nK;
+                };
+                // y and v - u of chunk cc leave from their staging tiles
+                auto store_out = [&](int cc) {
+                    tma_store_4d(&maps.y, ysg, r0, h, cc * kL, b);
+                    tma_store_5d(&maps.r, rsg, 0, cc * kL, r0 / 32, h, b);
+                    bulk_commit();
                 };
                 auto copy_P = [&](int cc) {                // [P; KKm] of chunk cc
                     mbar_expect_tx(cbP, 2 * kL * kL * 2);
                     bulk_load(pk, p.pkm + (head * NC + cc) * 2 * kL * kL, 2 * kL * kL * 2, cbP);
                     ++nP;
                 };
-                for (int cc = 0; cc < 2 && cc < NC; ++cc) {
-                    issue_w(cc);
-                    copy_K(cc);
-                }
+                for (int cc = 0; cc < 2 && cc < NC; ++cc) issue_w(cc);
+                copy_K(0);
                 copy_Q(0);
                 copy_P(0);
                 for (int c = 0; c < NC; ++c) {
@@ -653,19 +654,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     if (!mbar_wait(bS, c & 1)) { fail = true; break; }
                     bulk_store(p.s0m + (chk * gridDim.x + split) * kL * DK, sop, kL * DK * 2);
                     bulk_commit();
+                    // the previous chunk's y and v - u once staged
+                    if (c > 0) {
+                        if (!mbar_wait(bE, (c - 1) & 1)) { fail = true; break; }
+                        store_out(c - 1);
+                    }
                     // Q S^T and K S^T are done: Q is free
                     if (!mbar_wait(mQ, c & 1)) { fail = true; break; }
                     if (c + 1 < NC) copy_Q(c + 1);
-                    // Sigma is done: this K buffer is free (the chunk two ahead); Delta was read out
-                    // (bDt, before Sigma), so group W's buffer is free too; once the state's store
-                    // has read it, the state operand's tile is free
+                    // Sigma is done: K is free; Delta was read out (bDt, before Sigma), so group W's
+                    // buffer is free too (the chunk two ahead); once the stores have read them, the
+                    // state operand's tile and the y, v - u staging are free
                     if (!mbar_wait(mU, c & 1) || !mbar_wait(bDt, c & 1)) { fail = true; break; }
+                    if (c + 1 < NC) copy_K(c + 1);
+                    if (c + 2 < NC) issue_w(c + 2);
                     bulk_wait_read();
                     mbar_arrive(fS);
-                    if (c + 2 < NC) {
-                        copy_K(c + 2);
-                        issue_w(c + 2);
-                    }
                     // P Delta and KKm Delta are done: [P; KKm] is free
                     if (!mbar_wait(mY, c & 1)) { fail = true; break; }
                     if (c + 1 < NC) copy_P(c + 1);
@@ -674,10 +678,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     // copies still in flight land before the CTA exits (each wait bounded)
                     if (nQ > 0) mbar_wait(cbQ, (nQ - 1) & 1);
                     if (nP > 0) mbar_wait(cbP, (nP - 1) & 1);
-                    for (int i = 0; i < 2; ++i) {
+                    if (nK > 0) mbar_wait(cbK, (nK - 1) & 1);
+                    for (int i = 0; i < 2; ++i)
                         if (nW[i] > 0) mbar_wait(bW + i, (nW[i] - 1) & 1);
-                        if (nK[i] > 0) mbar_wait(cbK + i, (nK[i] - 1) & 1);
-                    }
+                } else if (mbar_wait(bE, (NC - 1) & 1)) {
+                    store_out(NC - 1);                      // the last chunk's y and v - u
+                } else {
+                    fail = true;
                 }
                 bulk_wait_all();                            // the bf16 states are complete
             }
@@ -702,7 +709,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 S[4 * j + 2 * k2 + 1] = s2.y;
             }
         const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
-        __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(p.y);
         // Lam_L, Lam_ta, Lam_tb and v of rows ta, tb (this thread's columns) of chunk cc, loaded
         // a chunk ahead and kept raw until used (rows past T: v zeros)
         float nlL, nla, nlb;
@@ -739,24 +745,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             if (lane == 0) mbar_arrive(bar_);
         };
         // y and v - u of chunk cc from tensor memory (its decays: ga, gb = exp(Lam) of rows ta,
-        // tb; v pairs va, vb), stored from registers (rows past T are not written)
-        auto epilogue = [&](int cc, float ga, float gb, const uint32_t (&va)[4], const uint32_t (&vb)[4]) {
-            const int tt0 = cc * kL, ln = min(kL, T - tt0);
-            const size_t ra = ((size_t)b * T + tt0 + ta) * Hv + h, rb = ((size_t)b * T + tt0 + tb) * Hv + h;
+        // tb; v pairs va, vb), staged in the 128-byte swizzle for the copy warp's TMA stores (rows
+        // past T are clipped by them): y row t at t * 128, 16-byte chunk j (8 columns) at
+        // j ^ (t % 8); v - u in two boxes of 32 columns, 16-byte chunk j (4 columns) likewise
+        auto epilogue = [&](float ga, float gb, const uint32_t (&va)[4], const uint32_t (&vb)[4]) {
             {
                 float q[16], pq[16];
                 tmem_ld16x256_x4(tY + lane16 + 32 * hw, q);
                 tmem_ld16x256_x4(tPy + lane16 + 32 * hw, pq);
                 tmem_wait_ld();
+                uint32_t yv[8];   // pairs (j, row ta), (j, row tb)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int col = r0 + fd.col(j, 0);
-                    if (ta < ln)
-                        *reinterpret_cast<uint32_t *>(y + ra * Dv + col) =
-                            pack2_bf16(fmaf(ga, q[4 * j], pq[4 * j]), fmaf(ga, q[4 * j + 1], pq[4 * j + 1]));
-                    if (tb < ln)
-                        *reinterpret_cast<uint32_t *>(y + rb * Dv + col) =
-                            pack2_bf16(fmaf(gb, q[4 * j + 2], pq[4 * j + 2]), fmaf(gb, q[4 * j + 3], pq[4 * j + 3]));
+                    yv[2 * j] = pack2_bf16(fmaf(ga, q[4 * j], pq[4 * j]), fmaf(ga, q[4 * j + 1], pq[4 * j + 1]));
+                    yv[2 * j + 1] = pack2_bf16(fmaf(gb, q[4 * j + 2], pq[4 * j + 2]), fmaf(gb, q[4 * j + 3], pq[4 * j + 3]));
+                }
+#pragma unroll
+                for (int j = 0; j < 4; j += 2) {
+                    const int m = lane >> 3, t = 16 * (warp & 3) + 8 * (m & 1) + (lane & 7), cb = 4 * hw + j + (m >> 1);
+                    stmatrix_x4(smem_addr(ysg) + t * 128 + ((cb ^ (t & 7)) << 4), yv[2 * j], yv[2 * j + 1], yv[2 * j + 2],
+                                yv[2 * j + 3]);
                 }
             }
             {
@@ -766,15 +774,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int col = r0 + fd.col(j, 0);
+                    const int col = fd.col(j, 0);
+                    const uint32_t oc = (col >> 5) * (kL * 128) + (col & 3) * 4;
                     const float2 xa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&va[j]));
                     const float2 xb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&vb[j]));
-                    if (ta < ln)
-                        *reinterpret_cast<float2 *>(p.resid + ra * Dv + col) =
-                            make_float2(xa.x - fmaf(ga, k[4 * j], pu[4 * j]), xa.y - fmaf(ga, k[4 * j + 1], pu[4 * j + 1]));
-                    if (tb < ln)
-                        *reinterpret_cast<float2 *>(p.resid + rb * Dv + col) =
-                            make_float2(xb.x - fmaf(gb, k[4 * j + 2], pu[4 * j + 2]), xb.y - fmaf(gb, k[4 * j + 3], pu[4 * j + 3]));
+                    *reinterpret_cast<float2 *>(rsg + oc + ta * 128 + ((((col & 31) >> 2) ^ (ta & 7)) << 4)) =
+                        make_float2(xa.x - fmaf(ga, k[4 * j], pu[4 * j]), xa.y - fmaf(ga, k[4 * j + 1], pu[4 * j + 1]));
+                    *reinterpret_cast<float2 *>(rsg + oc + tb * 128 + ((((col & 31) >> 2) ^ (tb & 7)) << 4)) =
+                        make_float2(xb.x - fmaf(gb, k[4 * j + 2], pu[4 * j + 2]), xb.y - fmaf(gb, k[4 * j + 3], pu[4 * j + 3]));
                 }
             }
         };
@@ -819,10 +826,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 const bool w = mbar_wait(mY, (c - 1) & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
-                epilogue(c - 1, pga, pgb, pva, pvb);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bE);
+                epilogue(pga, pgb, pva, pvb);
+                warp_done(bE);
             }
             // ---- Delta as operands: Delta (for P Delta, KKm Delta) and diag(E_L) Delta (for the
             // update); their tiles are free since the previous chunk's products are done (mY)
@@ -889,11 +894,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                         for (int k2 = 0; k2 < 2; ++k2)
                             *reinterpret_cast<float2 *>(p.S_T + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0)) =
                                 make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]);
-                w = mbar_wait(mY, (NC - 1) & 1);
+                // (the staging tiles are free once the previous chunk's stores have read them: fS)
+                w = mbar_wait(mY, (NC - 1) & 1) && mbar_wait(fS, (NC - 1) & 1);
                 fail = __any_sync(kFullMask, !w);
                 if (!fail) {
                     tc_fence_after();
-                    epilogue(NC - 1, pga, pgb, pva, pvb);
+                    epilogue(pga, pgb, pva, pvb);
+                    warp_done(bE);
                 }
             }
         }

@@ -489,8 +489,10 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // 128-byte swizzle. qk, the [Q; K] buffer as {256, 2, 2 halves (Q, K), Dk / 8 chunks, B*Hk*NC blocks},
 // box {256, 2, 1, Dk / 8, 1} (a half's 64 rows of a K chunk are 1 KB contiguous): written by
 // TMA stores from an operand tile of 64 rows, read back the same way.
+// Written by TMA stores, 128-byte swizzle: y as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1}; r (v - u)
+// as 5-D column blocks of [B][T][Hv][Dv] fp32 {32, T, Dv / 32, Hv, B}, box {32, 64, 2, 1, 1}.
 struct ChunkFwdMaps {
-    CUtensorMap vb, k, q, qk;
+    CUtensorMap vb, k, q, qk, y, r;
 };
 cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s);
 size_t chunk_prep_smem(int Dk, int Dv);
