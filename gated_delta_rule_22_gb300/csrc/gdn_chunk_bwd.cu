@@ -784,13 +784,14 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                             umma_idesc_t(1, 2 * kL, DK, false, true), s > 0, lead);
             umma_commit_w(bar, lead);
         }
-        // ---- c0 = <dS_L, S0> (both in the same layout) while the products run
-        {
+        // ---- c0 = <dS_L, S0> (both in the same layout) while the products run, by warps 1-7 (warp
+        // 0 is issuing them)
+        if (warp > 0) {
             float c0s = 0.f;
             const uint4 *a4 = reinterpret_cast<const uint4 *>(s0), *d4 = reinterpret_cast<const uint4 *>(dsl);
             const int n8 = Dv * DK / 8;
 #pragma unroll 4
-            for (int e = tid; e < n8; e += 256) {
+            for (int e = tid - 32; e < n8; e += 224) {
                 float x[8], d[8];
                 unpack8(a4[e], x);
                 unpack8(d4[e], d);
@@ -799,6 +800,8 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             }
             c0s = warp_sum(c0s);
             if (lane == 0) c0p[warp] = c0s;
+        } else if (lane == 0) {
+            c0p[0] = 0.f;
         }
         tc_fence_before();
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
@@ -905,6 +908,24 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                         umma_idesc_t(1, 2 * kL, kL, false, false), false, lead);
             umma_commit_w(bar, lead);
         }
+        {
+            // ---- dg_t: the sums over the chunk's steps, a quarter of the steps per thread (while
+            // the second products run: they need none of them)
+            // s2 = sum_{j < t} E(t-1, j) f_j, s3 = exp(Lam_{t-1}) sum_{j >= t} E(j, t) (a_j + b_j)
+            const int t = tid & (kL - 1), part = tid >> 6;
+            const float *Ep = Et + (t > 0 ? t - 1 : 0) * (kL + 1);
+            float s2 = 0.f, s3 = 0.f;
+            for (int j = 16 * part; j < 16 * part + 16; ++j) {
+                if (j < t) {
+                    s2 = fmaf(Ep[j], fv[j], s2);
+                } else {
+                    const float ab = abp[j] + abp[2 * kL + j] + abp[kL + j] + abp[3 * kL + j];
+                    s3 = fmaf(Et[j * (kL + 1) + t], ab, s3);
+                }
+            }
+            dgp[(2 * part + 0) * kL + t] = s2;
+            dgp[(2 * part + 1) * kL + t] = expf(LmP[t]) * s3;
+        }
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
         ++ph;
         tc_fence_after();
@@ -927,23 +948,6 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] *= Es[i];   // E(s, t) = 0 for t > s
             zq[quarter * kL + half * 32 + lane] = transpose_reduce<32>(z, lane);
-        }
-        {
-            // ---- dg_t: the sums over the chunk's steps, a quarter of the steps per thread
-            // s2 = sum_{j < t} E(t-1, j) f_j, s3 = exp(Lam_{t-1}) sum_{j >= t} E(j, t) (a_j + b_j)
-            const int t = tid & (kL - 1), part = tid >> 6;
-            const float *Ep = Et + (t > 0 ? t - 1 : 0) * (kL + 1);
-            float s2 = 0.f, s3 = 0.f;
-            for (int j = 16 * part; j < 16 * part + 16; ++j) {
-                if (j < t) {
-                    s2 = fmaf(Ep[j], fv[j], s2);
-                } else {
-                    const float ab = abp[j] + abp[2 * kL + j] + abp[kL + j] + abp[3 * kL + j];
-                    s3 = fmaf(Et[j * (kL + 1) + t], ab, s3);
-                }
-            }
-            dgp[(2 * part + 0) * kL + t] = s2;
-            dgp[(2 * part + 1) * kL + t] = expf(LmP[t]) * s3;
         }
         __syncthreads();
         if (tid < kL && tid < len) {
