@@ -47,10 +47,10 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:^chunk_sweep -s 3 -c 1 python bench.py --steps 1 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("c0b309d2e3521b0b", "chunk_prep"): 34835968 + 92986368,
-    ("c0b309d2e3521b0b", "chunk_sweep"): 159991040 + 350721024,
-    ("c8dd4f7b3b5dc9ab", "chunk_dsweep"): 177038080 + 192236032,
-    ("c8dd4f7b3b5dc9ab", "chunk_grad"): 330720256 + 17506304,
+    ("c0d6d83aa3cb6a4d", "chunk_prep"): 35572224 + 91652608,
+    ("c0d6d83aa3cb6a4d", "chunk_sweep"): 160041472 + 351680512,
+    ("f4f941bbf6baa363", "chunk_dsweep"): 160389888 + 192155904,
+    ("f4f941bbf6baa363", "chunk_grad"): 333497088 + 17523456,
 }
 
 
