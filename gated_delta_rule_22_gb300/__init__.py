@@ -6,7 +6,8 @@ The compute lives in libgdn.so, a C-ABI library of hand-written CUDA kernels
 from .binding import (  # noqa: F401
     GDN_BF16, GDN_F32, GdnError, GdnShape, gdn_bwd, gdn_bwd_noalloc, gdn_bwd_workspace_bytes,
     gdn_ckpt_bytes, gdn_debug_wait_probe, gdn_device_status, gdn_diag_fma_tflops, gdn_fwd,
-    gdn_gates_bwd, gdn_gates_fwd, gdn_last_error,
+    gdn_bwd_seg, gdn_fwd_seg, gdn_gates_bwd, gdn_gates_fwd, gdn_last_error, gdn_seg_ckpt_bytes,
+    gdn_seg_workspace_bytes,
     gdn_strerror, gdn_timing_enable, gdn_timing_read, gdn_version,
     header_functions, load_library, make_shape, new_ckpt,
 )

@@ -59,6 +59,14 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_bwd.argtypes = [SP] + [_VP] * 6 + [_SZ] + [_VP] * 9 + [_SZ, _VP]
     lib.gdn_bwd_noalloc.restype = ctypes.c_int
     lib.gdn_bwd_noalloc.argtypes = [SP] + [_VP] * 6 + [_SZ] + [_VP] * 9
+    lib.gdn_seg_ckpt_bytes.restype = ctypes.c_size_t
+    lib.gdn_seg_ckpt_bytes.argtypes = [SP, ctypes.c_int]
+    lib.gdn_seg_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_seg_workspace_bytes.argtypes = [SP, ctypes.c_int]
+    lib.gdn_fwd_seg.restype = ctypes.c_int
+    lib.gdn_fwd_seg.argtypes = [SP, ctypes.c_int] + [_VP] * 9 + [_SZ, _VP, _SZ, _VP]
+    lib.gdn_bwd_seg.restype = ctypes.c_int
+    lib.gdn_bwd_seg.argtypes = [SP, ctypes.c_int] + [_VP] * 6 + [_SZ] + [_VP] * 9 + [_SZ, _VP]
     lib.gdn_gates_fwd.restype = ctypes.c_int
     lib.gdn_gates_fwd.argtypes = [SP] + [_VP] * 7
     lib.gdn_gates_bwd.restype = ctypes.c_int
@@ -282,6 +290,92 @@ def gdn_bwd(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, workspace=None, 
                      workspace.numel() * workspace.element_size(), _stream(stream, q.device))
     if rc != GDN_OK:
         raise GdnError("gdn_bwd", rc, lib)
+    return out
+
+
+def gdn_seg_ckpt_bytes(shape: GdnShape, segments: int) -> int:
+    return int(load_library().gdn_seg_ckpt_bytes(ctypes.byref(shape), segments))
+
+
+def gdn_seg_workspace_bytes(shape: GdnShape, segments: int) -> int:
+    return int(load_library().gdn_seg_workspace_bytes(ctypes.byref(shape), segments))
+
+
+def gdn_fwd_seg(q, k, v, g, beta, S0=None, segments=2, *, y=None, S_T=None, ckpt=None, workspace=None,
+                want_S_T=True, stream=None):
+    """y, S_T, ckpt = gdn_fwd_seg(q, k, v, g, beta[, S0], segments) on CUDA tensors: the
+    sequence-parallel forward (see include/gdn.h). ckpt is a uint8 device tensor of
+    gdn_seg_ckpt_bytes bytes (allocated here when None); workspace likewise
+    (gdn_seg_workspace_bytes, allocated here for this call when None)."""
+    torch = _torch()
+    lib = load_library()
+    shape = _shape_of(q, v, 64)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    dev, dt = q.device, q.dtype
+    for name, t, shp in (("q", q, q.shape), ("k", k, q.shape), ("v", v, (B, T, Hv, Dv)),
+                         ("g", g, (B, T, Hv)), ("beta", beta, (B, T, Hv))):
+        _check(name, t, shp, dt, dev)
+    if S0 is not None:
+        _check("S0", S0, (B, Hv, Dv, Dk), torch.float32, dev)
+    if y is not None:
+        _check("y", y, (B, T, Hv, Dv), dt, dev)
+    if S_T is not None:
+        _check("S_T", S_T, (B, Hv, Dv, Dk), torch.float32, dev)
+    for name, t in (("ckpt", ckpt), ("workspace", workspace)):
+        if t is not None and (t.device != dev or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous tensor on {dev}")
+    _require_cuda(q)
+    need_ck = lib.gdn_seg_ckpt_bytes(ctypes.byref(shape), segments)
+    need_ws = lib.gdn_seg_workspace_bytes(ctypes.byref(shape), segments)
+    if y is None:
+        y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
+    if S_T is None and want_S_T:
+        S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
+    if ckpt is None:
+        ckpt = torch.empty(max(need_ck, 16), dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(need_ws, 16), dtype=torch.uint8, device=dev)
+    rc = lib.gdn_fwd_seg(ctypes.byref(shape), segments, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0),
+                         _ptr(y), _ptr(S_T), _ptr(ckpt), _room(ckpt), _ptr(workspace), _room(workspace),
+                         _stream(stream, dev))
+    if rc != GDN_OK:
+        raise GdnError("gdn_fwd_seg", rc, lib)
+    return y, S_T, ckpt
+
+
+def gdn_bwd_seg(q, k, v, g, beta, ckpt, dy, dS_T=None, segments=2, *, workspace=None, out=None, want_dS0=True,
+                stream=None):
+    """dict(dq, dk, dv, dg, dbeta, dS0) = gdn_bwd_seg(...): the sequence-parallel backward for
+    the saved buffer of gdn_fwd_seg with the same segments (see include/gdn.h)."""
+    torch = _torch()
+    lib = load_library()
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    dev, dt = q.device, q.dtype
+    shape = _shape_of(q, v, 64)
+    for name, t, shp in (("q", q, q.shape), ("k", k, q.shape), ("v", v, (B, T, Hv, Dv)),
+                         ("g", g, (B, T, Hv)), ("beta", beta, (B, T, Hv)), ("dy", dy, (B, T, Hv, Dv))):
+        _check(name, t, shp, dt, dev)
+    if dS_T is not None:
+        _check("dS_T", dS_T, (B, Hv, Dv, Dk), torch.float32, dev)
+    for name, t in (("ckpt", ckpt), ("workspace", workspace)):
+        if t is not None and (t.device != dev or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous tensor on {dev}")
+    _require_cuda(q)
+    if out is None:
+        out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+               "dg": torch.empty_like(g), "dbeta": torch.empty_like(beta),
+               "dS0": torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev) if want_dS0 else None}
+    if workspace is None:
+        need = lib.gdn_seg_workspace_bytes(ctypes.byref(shape), segments)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib.gdn_bwd_seg(ctypes.byref(shape), segments, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ckpt),
+                         _room(ckpt), _ptr(dy), _ptr(dS_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                         _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out.get("dS0")), _ptr(workspace),
+                         _room(workspace), _stream(stream, dev))
+    if rc != GDN_OK:
+        raise GdnError("gdn_bwd_seg", rc, lib)
     return out
 
 

@@ -396,6 +396,85 @@ size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
     return bwd_workspace_total(p);
 }
 
+// The chunkwise forward on the tensor cores for plan p (a segmented call passes its view): the
+// stages of launch_chunk_fwd; maps_out receives the maps stage's output ([B][Hv][Dk][Dk]).
+static int tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const void *g, const void *beta,
+                  const float *S0, void *y, float *S_T, float *ckpt, float *maps_out, int stages, cudaStream_t stream) {
+    const ChunkLayout cl = chunk_layout(p);
+    char *sb = reinterpret_cast<char *>(ckpt);
+    gdn::ChunkParams cp;
+    cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.S0 = S0; cp.y = y; cp.S_T = S_T;
+    cp.ckpt = ckpt; cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
+    cp.lam = reinterpret_cast<float *>(sb + cl.lam);
+    cp.pkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.pkm);
+    cp.wm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.wm);
+    cp.tm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tm);
+    cp.tcm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tcm);
+    cp.s0m = reinterpret_cast<__nv_bfloat16 *>(sb + cl.s0m);
+    cp.qkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qkm);
+    cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
+    g_last_error[0] = '\0';
+    int rc = device_status_address(&cp.status);
+    if (rc != GDN_OK) return rc;
+    gdn::ChunkFwdMaps maps;
+    if ((rc = make_btd_map(&maps.vb, v, true, p.B, p.T, p.Hv, p.Dv, 64, 64, true)) != GDN_OK ||
+        (rc = make_colblock_map(&maps.k, k, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
+        (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
+        (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK ||
+        (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
+        (rc = make_colblock_map(&maps.r, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK)
+        return rc;
+    const int first = stages & (gdn::kStagePrep | gdn::kStageSweep);
+    if (first) {
+        rc = cuda_status(gdn::launch_chunk_fwd(cp, maps, p.Dk, stream, first));
+        if (rc != GDN_OK) return rc;
+    }
+    if (stages & gdn::kStageMaps) {
+        gdn::ChunkParams cm = cp;
+        cm.Dv = p.Dk;                      // the identity's rows
+        cm.S0 = nullptr;
+        cm.S_T = maps_out;
+        rc = cuda_status(gdn::launch_chunk_fwd(cm, maps, p.Dk, stream, gdn::kStageMaps));
+    }
+    return rc;
+}
+
+// The chunkwise backward on the tensor cores for plan p: the stages of launch_chunk_bwd.
+static int tc_bwd(const Plan &p, const void *beta, const float *ckpt, const void *dy, const float *dS_T, void *dq,
+                  void *dk, void *dv, void *dg, void *dbeta, float *dS0, char *ws, int stages, cudaStream_t stream) {
+    const ChunkLayout cl = chunk_layout(p);
+    const TcWorkspace tw = tc_workspace_layout(p);
+    const char *sb = reinterpret_cast<const char *>(ckpt);
+    gdn::ChunkBwdParams cp;
+    cp.dy = dy; cp.beta = beta;
+    cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
+    cp.lam = reinterpret_cast<const float *>(sb + cl.lam);
+    cp.tm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.tm);
+    cp.pkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.pkm);
+    cp.s0m = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.s0m);
+    cp.qkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qkm);
+    cp.dS_T = dS_T; cp.dS0 = dS0;
+    cp.dv = dv; cp.dg = dg; cp.dq = dq; cp.dk = dk; cp.dbeta = dbeta;
+    cp.ws_db = reinterpret_cast<float *>(ws + tw.db);
+    cp.ws_f = reinterpret_cast<float *>(ws + tw.f);
+    cp.ws_yu = reinterpret_cast<__nv_bfloat16 *>(ws + tw.yu);
+    cp.ws_dl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dl);
+    cp.ws_dsl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dsl);
+    cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC; cp.nsplit = p.nsplit;
+    g_last_error[0] = '\0';
+    int rc = device_status_address(&cp.status);
+    if (rc != GDN_OK) return rc;
+    CUtensorMap tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk;
+    if ((rc = make_btd_map(&tm_dv, dv, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
+        (rc = make_colblock_map(&tm_dy, dy, true, p.B, p.T, p.Hv, p.Dv, 8, 128, 8, false)) != GDN_OK ||
+        (rc = make_qkm_map(&tm_qk, const_cast<__nv_bfloat16 *>(cp.qkm), (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK ||
+        (rc = make_qkm_map(&tm_pk, const_cast<__nv_bfloat16 *>(cp.pkm), (size_t)p.B * p.Hv * p.NC, 64)) != GDN_OK ||
+        (rc = make_btd_map(&tm_dq, dq, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK ||
+        (rc = make_btd_map(&tm_dk, dk, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK)
+        return rc;
+    return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, p.Dk, stream, stages));
+}
+
 int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
             const void *beta, const float *S0, void *y, float *S_T, float *ckpt, size_t ckpt_bytes,
             void *stream) {
@@ -415,32 +494,9 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     fp.B = p.B; fp.T = p.T; fp.Hk = p.Hk; fp.Hv = p.Hv; fp.Dv = p.Dv; fp.C = p.C; fp.NC = p.NC;
     rc = device_status_address(&fp.status);
     if (rc != GDN_OK) return rc;
-    if (p.tc && ckpt != nullptr) {
-        // chunkwise form on the tensor cores
-        const ChunkLayout cl = chunk_layout(p);
-        char *sb = reinterpret_cast<char *>(ckpt);
-        gdn::ChunkParams cp;
-        cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.S0 = S0; cp.y = y; cp.S_T = S_T;
-        cp.ckpt = ckpt; cp.resid = fp.resid;
-        cp.lam = reinterpret_cast<float *>(sb + cl.lam);
-        cp.pkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.pkm);
-        cp.wm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.wm);
-        cp.tm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tm);
-        cp.tcm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tcm);
-        cp.s0m = reinterpret_cast<__nv_bfloat16 *>(sb + cl.s0m);
-        cp.qkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qkm);
-        cp.status = fp.status;
-        cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
-        gdn::ChunkFwdMaps maps;
-        if ((rc = make_btd_map(&maps.vb, v, true, p.B, p.T, p.Hv, p.Dv, 64, 64, true)) != GDN_OK ||
-            (rc = make_colblock_map(&maps.k, k, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
-            (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
-            (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK ||
-            (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
-            (rc = make_colblock_map(&maps.r, fp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK)
-            return rc;
-        return cuda_status(gdn::launch_chunk_fwd(cp, maps, p.Dk, (cudaStream_t)stream));
-    }
+    if (p.tc && ckpt != nullptr)       // chunkwise form on the tensor cores
+        return tc_fwd(p, q, k, v, g, beta, S0, y, S_T, ckpt, nullptr, gdn::kStagePrep | gdn::kStageSweep,
+                      (cudaStream_t)stream);
     CUtensorMap tm_q, tm_k;
     if ((rc = make_qk_map(&tm_q, q, p, gdn::kFwdTile)) != GDN_OK) return rc;
     if ((rc = make_qk_map(&tm_k, k, p, gdn::kFwdTile)) != GDN_OK) return rc;
@@ -461,46 +517,9 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
         if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
     if (ckpt_bytes < ckpt_total(p) || workspace_bytes < bwd_workspace_total(p)) return GDN_ERR_BUFFER_TOO_SMALL;
     char *ws = static_cast<char *>(workspace);
-    if (p.tcb) {
-        // chunkwise form on the tensor cores, reading the chunkwise forward's saved buffer
-        const ChunkLayout cl = chunk_layout(p);
-        const TcWorkspace tw = tc_workspace_layout(p);
-        const char *sb = reinterpret_cast<const char *>(ckpt);
-        gdn::ChunkBwdParams cp;
-        cp.dy = dy; cp.beta = beta;
-        cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
-        cp.lam = reinterpret_cast<const float *>(sb + cl.lam);
-        cp.tm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.tm);
-        cp.pkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.pkm);
-        cp.s0m = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.s0m);
-        cp.qkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qkm);
-        cp.dS_T = dS_T; cp.dS0 = dS0;
-        cp.dv = dv; cp.dg = dg; cp.dq = dq; cp.dk = dk; cp.dbeta = dbeta;
-        cp.ws_db = reinterpret_cast<float *>(ws + tw.db);
-        cp.ws_f = reinterpret_cast<float *>(ws + tw.f);
-        cp.ws_yu = reinterpret_cast<__nv_bfloat16 *>(ws + tw.yu);
-        cp.ws_dl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dl);
-        cp.ws_dsl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dsl);
-        cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC; cp.nsplit = p.nsplit;
-        g_last_error[0] = '\0';
-        rc = device_status_address(&cp.status);
-        if (rc != GDN_OK) return rc;
-        CUtensorMap tm_dv;
-        rc = make_btd_map(&tm_dv, dv, true, p.B, p.T, p.Hv, p.Dv, 64, 64);
-        if (rc != GDN_OK) return rc;
-        CUtensorMap tm_dy, tm_qk, tm_pk;
-        rc = make_colblock_map(&tm_dy, dy, true, p.B, p.T, p.Hv, p.Dv, 8, 128, 8, false);
-        if (rc != GDN_OK) return rc;
-        rc = make_qkm_map(&tm_qk, const_cast<__nv_bfloat16 *>(cp.qkm), (size_t)p.B * p.Hk * p.NC, p.Dk);
-        if (rc != GDN_OK) return rc;
-        rc = make_qkm_map(&tm_pk, const_cast<__nv_bfloat16 *>(cp.pkm), (size_t)p.B * p.Hv * p.NC, 64);
-        if (rc != GDN_OK) return rc;
-        CUtensorMap tm_dq, tm_dk;
-        if ((rc = make_btd_map(&tm_dq, dq, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK ||
-            (rc = make_btd_map(&tm_dk, dk, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK)
-            return rc;
-        return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, p.Dk, (cudaStream_t)stream));
-    }
+    if (p.tcb)                         // chunkwise form on the tensor cores, reading the chunkwise forward's saved buffer
+        return tc_bwd(p, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, gdn::kStageDsweep | gdn::kStageGrad,
+                      (cudaStream_t)stream);
     const Workspace w = workspace_layout(p);
 
     gdn::BwdParams bp;
@@ -529,6 +548,102 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     rc = cuda_status(gdn::launch_bwd(bp, tm_q, tm_k, p.Dk, p.dtype, (cudaStream_t)stream));
     if (rc != GDN_OK) return rc;
     return cuda_status(gdn::launch_reduce(rp, p.dtype, (cudaStream_t)stream));
+}
+
+// ---- sequence-parallel form: the problem seen as B * P rows of T / P steps (segments of whole
+// chunks are contiguous in [B][T][...], so every tensor keeps its address)
+static int seg_plans(const gdn_shape *shape, int segments, Plan *p, Plan *pv) {
+    int rc = make_plan(shape, p);
+    if (rc != GDN_OK) return rc;
+    if (segments < 1 || !p->tc || !p->tcb || p->T % (64 * segments) != 0 ||
+        (long long)p->B * segments > (1LL << 30))
+        return GDN_ERR_UNSUPPORTED_SHAPE;
+    gdn_shape v = *shape;
+    v.B = shape->B * segments;
+    v.T = shape->T / segments;
+    rc = make_plan(&v, pv);
+    if (rc != GDN_OK) return rc;
+    return pv->tc && pv->tcb ? GDN_OK : GDN_ERR_UNSUPPORTED_SHAPE;
+}
+
+static size_t seg_maps_offset(const Plan &pv) { return round_up(ckpt_total(pv)); }
+static size_t seg_state_bytes(const Plan &pv) { return round_up((size_t)pv.B * pv.Hv * pv.Dv * pv.Dk * 4); }
+
+size_t gdn_seg_ckpt_bytes(const gdn_shape *shape, int segments) {
+    Plan p, pv;
+    if (shape == nullptr || seg_plans(shape, segments, &p, &pv) != GDN_OK) return 0;
+    return seg_maps_offset(pv) + round_up((size_t)pv.B * pv.Hv * pv.Dk * pv.Dk * 4);
+}
+
+size_t gdn_seg_workspace_bytes(const gdn_shape *shape, int segments) {
+    Plan p, pv;
+    if (shape == nullptr || seg_plans(shape, segments, &p, &pv) != GDN_OK) return 0;
+    return 2 * seg_state_bytes(pv) + bwd_workspace_total(pv);
+}
+
+// dst[b] = src[b * P + s] for every b: blocks of `blk` bytes
+static int seg_pick(void *dst, const void *src, size_t blk, int B, int P, int s, cudaStream_t stream) {
+    return cuda_status(cudaMemcpy2DAsync(dst, blk, static_cast<const char *>(src) + (size_t)s * blk, (size_t)P * blk, blk,
+                                         (size_t)B, cudaMemcpyDeviceToDevice, stream));
+}
+
+int gdn_fwd_seg(const gdn_shape *shape, int segments, const void *q, const void *k, const void *v, const void *g,
+                const void *beta, const float *S0, void *y, float *S_T, float *ckpt, size_t ckpt_bytes,
+                void *workspace, size_t workspace_bytes, void *stream) {
+    if (shape == nullptr) return GDN_ERR_INVALID_ARG;
+    Plan p, pv;
+    int rc = seg_plans(shape, segments, &p, &pv);
+    if (rc != GDN_OK) return rc;
+    if (!q || !k || !v || !g || !beta || !y || !ckpt || !workspace) return GDN_ERR_INVALID_ARG;
+    const void *all[] = {q, k, v, g, beta, S0, y, S_T, ckpt, workspace};
+    for (const void *ptr : all)
+        if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    if (ckpt_bytes < gdn_seg_ckpt_bytes(shape, segments) || workspace_bytes < gdn_seg_workspace_bytes(shape, segments))
+        return GDN_ERR_BUFFER_TOO_SMALL;
+    const cudaStream_t st = (cudaStream_t)stream;
+    float *maps = reinterpret_cast<float *>(reinterpret_cast<char *>(ckpt) + seg_maps_offset(pv));
+    float *C = static_cast<float *>(workspace);
+    float *X = reinterpret_cast<float *>(static_cast<char *>(workspace) + seg_state_bytes(pv));
+    // every segment from a zero state (its end state: C) and as maps, then the scan of the
+    // start states, then every segment again from its start state
+    rc = tc_fwd(pv, q, k, v, g, beta, nullptr, y, C, ckpt, maps, gdn::kStagePrep | gdn::kStageSweep | gdn::kStageMaps, st);
+    if (rc != GDN_OK) return rc;
+    rc = cuda_status(gdn::launch_segment_scan(S0, maps, C, X, p.B, segments, p.Hv, p.Dv, p.Dk, false, st));
+    if (rc != GDN_OK) return rc;
+    rc = tc_fwd(pv, q, k, v, g, beta, X, y, C, ckpt, nullptr, gdn::kStageSweep, st);
+    if (rc != GDN_OK || S_T == nullptr) return rc;
+    return seg_pick(S_T, C, (size_t)p.Hv * p.Dv * p.Dk * 4, p.B, segments, segments - 1, st);
+}
+
+int gdn_bwd_seg(const gdn_shape *shape, int segments, const void *q, const void *k, const void *v, const void *g,
+                const void *beta, const float *ckpt, size_t ckpt_bytes, const void *dy, const float *dS_T, void *dq,
+                void *dk, void *dv, void *dg, void *dbeta, float *dS0, void *workspace, size_t workspace_bytes,
+                void *stream) {
+    if (shape == nullptr) return GDN_ERR_INVALID_ARG;
+    Plan p, pv;
+    int rc = seg_plans(shape, segments, &p, &pv);
+    if (rc != GDN_OK) return rc;
+    if (!q || !k || !v || !g || !beta || !ckpt || !dy || !dq || !dk || !dv || !dg || !dbeta || !workspace)
+        return GDN_ERR_INVALID_ARG;
+    const void *all[] = {q, k, v, g, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace};
+    for (const void *ptr : all)
+        if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    if (ckpt_bytes < gdn_seg_ckpt_bytes(shape, segments) || workspace_bytes < gdn_seg_workspace_bytes(shape, segments))
+        return GDN_ERR_BUFFER_TOO_SMALL;
+    const cudaStream_t st = (cudaStream_t)stream;
+    const float *maps = reinterpret_cast<const float *>(reinterpret_cast<const char *>(ckpt) + seg_maps_offset(pv));
+    float *D = static_cast<float *>(workspace);
+    float *Y = reinterpret_cast<float *>(static_cast<char *>(workspace) + seg_state_bytes(pv));
+    char *ws = static_cast<char *>(workspace) + 2 * seg_state_bytes(pv);
+    // every segment's reverse sweep from a zero end adjoint (its start adjoint: D), the reverse
+    // scan of the end adjoints, then the backward proper from them
+    rc = tc_bwd(pv, beta, ckpt, dy, nullptr, dq, dk, dv, dg, dbeta, D, ws, gdn::kStageDsweep, st);
+    if (rc != GDN_OK) return rc;
+    rc = cuda_status(gdn::launch_segment_scan(dS_T, maps, D, Y, p.B, segments, p.Hv, p.Dv, p.Dk, true, st));
+    if (rc != GDN_OK) return rc;
+    rc = tc_bwd(pv, beta, ckpt, dy, Y, dq, dk, dv, dg, dbeta, D, ws, gdn::kStageDsweep | gdn::kStageGrad, st);
+    if (rc != GDN_OK || dS0 == nullptr) return rc;
+    return seg_pick(dS0, D, (size_t)p.Hv * p.Dv * p.Dk * 4, p.B, segments, 0, st);
 }
 
 int gdn_gates_fwd(const gdn_shape *shape, const void *a, const void *b, const float *A_log,

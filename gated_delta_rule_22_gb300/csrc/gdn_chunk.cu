@@ -493,7 +493,12 @@ struct SweepSmem {
 // Q and K arrive as separate [64][DK] tiles (boxes of the [Q; K] block); group W is
 // double-buffered and fetched two chunks ahead. y and v - u leave by TMA stores from staging
 // tiles (the copy warp, once bE says they are written).
-template <int E>
+//
+// With kMaps, the same sweep computes instead each chunk range's state map (the sequence-parallel
+// form): the "state" is the Dk x Dk identity (rows r0 .. r0 + 63 of it per CTA; p.Dv = Dk) and V
+// counts as zero, so the chunks compose S <- S (exp(Lam_L) I - W^T diag(E_L) K); only S_T (the
+// map) is written -- no checkpoints, states, y or v - u.
+template <int E, bool kMaps>
 __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ ChunkFwdMaps maps) {
     constexpr int DK = 32 * E;
     constexpr int SC = DK / 2;                // state columns per warp half
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             constexpr uint32_t id64 = umma_idesc(1, kL, kL);
             // U = (T diag(beta)) V starts Delta's accumulator (the first chunk's here, each later
             // one once the previous Delta is read out)
-            {
+            if constexpr (!kMaps) {
                 const bool w = mbar_wait(bW, 0);
                 fail = __any_sync(kFullMask, !w);
                 if (!fail) {
@@ -566,12 +571,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             }
             for (int c = 0; c < NC && !fail; ++c) {
                 unsigned char *wc = wbuf(c);
-                // ---- Delta += (-W) S^T once S is written
-                bool w = mbar_wait(bS, c & 1);
+                // ---- Delta += (-W) S^T once S is written (the maps: Delta = (-W) S^T)
+                bool w = mbar_wait(bS, c & 1) && (!kMaps || mbar_wait(bW + (c & 1), (c >> 1) & 1));
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
-                umma_gemm_w(tD, CmOp{wc, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, true, lead);
+                umma_gemm_w(tD, CmOp{wc, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, !kMaps, lead);
                 umma_commit_w(mD, lead);
+                if constexpr (kMaps) {
+                    // ---- Sigma = (diag(E_L) Delta)^T K once Delta is written
+                    w = mbar_wait(bDt, c & 1) && mbar_wait(cbK, c & 1);
+                    if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                    tc_fence_after();
+                    umma_gemm_w(tSg, CmOp{de, kL, 0, 0, true}, CmOp{kb, kL, 0, 0, true}, kL,
+                                umma_idesc_t(1, kL, DK, true, true), false, lead);
+                    umma_commit_w(mU, lead);
+                    continue;
+                }
                 // ---- Q S^T and K S^T once the previous chunk's are read out and Q, K landed
                 w = (c == 0 || mbar_wait(bE, (c - 1) & 1)) && mbar_wait(cbQ, c & 1) && mbar_wait(cbK, c & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
@@ -617,10 +632,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     const size_t ck = head * NC + cc;
                     unsigned char *g = wbuf(cc);
                     uint64_t *bw = bW + (cc & 1);
-                    mbar_expect_tx(bw, kL * DK * 2 + 2 * kL * kL * 2);
+                    mbar_expect_tx(bw, kMaps ? kL * DK * 2 : kL * DK * 2 + 2 * kL * kL * 2);
                     bulk_load(g, p.wm + ck * kL * DK, kL * DK * 2, bw);
-                    bulk_load(g + (L.tc - L.wc), p.tcm + ck * kL * kL, kL * kL * 2, bw);
-                    tma_load_4d(g + (L.vb - L.wc), &maps.vb, bw, r0, h, cc * kL, b);
+                    if constexpr (!kMaps) {
+                        bulk_load(g + (L.tc - L.wc), p.tcm + ck * kL * kL, kL * kL * 2, bw);
+                        tma_load_4d(g + (L.vb - L.wc), &maps.vb, bw, r0, h, cc * kL, b);
+                    }
                     ++nW[cc & 1];
                 };
                 auto copy_Q = [&](int cc) {                // Q of chunk cc: rows 0-63 of its [Q; K] block
@@ -646,9 +663,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 };
                 for (int cc = 0; cc < 2 && cc < NC; ++cc) issue_w(cc);
                 copy_K(0);
-                copy_Q(0);
-                copy_P(0);
-                for (int c = 0; c < NC; ++c) {
+                if constexpr (!kMaps) {
+                    copy_Q(0);
+                    copy_P(0);
+                }
+                for (int c = 0; c < NC && kMaps; ++c) {
+                    // the maps: K and group W (-W only) only; Sigma done frees K, Delta read out
+                    // frees -W, and the state operand's tile is free once Sigma is done
+                    if (!mbar_wait(mU, c & 1) || !mbar_wait(bDt, c & 1)) { fail = true; break; }
+                    if (c + 1 < NC) copy_K(c + 1);
+                    if (c + 2 < NC) issue_w(c + 2);
+                    mbar_arrive(fS);
+                }
+                for (int c = 0; c < NC && !kMaps; ++c) {
                     const size_t chk = head * NC + c;
                     // the bf16 state leaves (the backward's operand) once written
                     if (!mbar_wait(bS, c & 1)) { fail = true; break; }
@@ -681,6 +708,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     if (nK > 0) mbar_wait(cbK, (nK - 1) & 1);
                     for (int i = 0; i < 2; ++i)
                         if (nW[i] > 0) mbar_wait(bW + i, (nW[i] - 1) & 1);
+                } else if (kMaps) {
                 } else if (mbar_wait(bE, (NC - 1) & 1)) {
                     store_out(NC - 1);                      // the last chunk's y and v - u
                 } else {
@@ -703,8 +731,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
 #pragma unroll
             for (int k2 = 0; k2 < 2; ++k2) {
                 float2 s2 = make_float2(0.f, 0.f);
-                if (p.S0 != nullptr)
-                    s2 = *reinterpret_cast<const float2 *>(p.S0 + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0));
+                const int row = r0 + fs.row(2 * k2), col = fs.col(j, 0);
+                if (kMaps)
+                    s2 = make_float2(row == col ? 1.f : 0.f, row == col + 1 ? 1.f : 0.f);
+                else if (p.S0 != nullptr)
+                    s2 = *reinterpret_cast<const float2 *>(p.S0 + (head * Dv + row) * DK + col);
                 S[4 * j + 2 * k2] = s2.x;
                 S[4 * j + 2 * k2 + 1] = s2.y;
             }
@@ -786,7 +817,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             }
         };
         load_lam(0);
-        load_v(0);
+        if (!kMaps) load_v(0);
         float decay = 1.f, pga = 1.f, pgb = 1.f;     // exp(Lam_L), exp(Lam_ta), exp(Lam_tb) of the previous chunk
         uint32_t pva[4], pvb[4];                      // v pairs of the previous chunk
         for (int c = 0; c < NC; ++c) {
@@ -800,7 +831,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             }
             if (c + 1 < NC) {
                 load_lam(c + 1);
-                load_v(c + 1);
+                if (!kMaps) load_v(c + 1);
             }
             // ---- S <- exp(Lam_L) S + Sigma of the previous chunk; S as an operand
             if (c > 0) {
@@ -822,7 +853,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             write_sop();
             warp_done(bS);
             // ---- y and v - u of the previous chunk
-            if (c > 0) {
+            if (!kMaps && c > 0) {
                 const bool w = mbar_wait(mY, (c - 1) & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
@@ -844,15 +875,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
 #pragma unroll
                 for (int j = 0; j < 4; j += 2) {
                     const uint32_t o = frag_row_addr(0, kL, 16 * (warp & 3), 4 * hw + j, lane);
-                    stmatrix_x4(smem_addr(dt) + o, pack2_bf16(x[4 * j], x[4 * j + 1]), pack2_bf16(x[4 * j + 2], x[4 * j + 3]),
-                                pack2_bf16(x[4 * j + 4], x[4 * j + 5]), pack2_bf16(x[4 * j + 6], x[4 * j + 7]));
+                    if (!kMaps)
+                        stmatrix_x4(smem_addr(dt) + o, pack2_bf16(x[4 * j], x[4 * j + 1]),
+                                    pack2_bf16(x[4 * j + 2], x[4 * j + 3]), pack2_bf16(x[4 * j + 4], x[4 * j + 5]),
+                                    pack2_bf16(x[4 * j + 6], x[4 * j + 7]));
                     stmatrix_x4(smem_addr(de) + o, pack2_bf16(ea * x[4 * j], ea * x[4 * j + 1]),
                                 pack2_bf16(eb * x[4 * j + 2], eb * x[4 * j + 3]), pack2_bf16(ea * x[4 * j + 4], ea * x[4 * j + 5]),
                                 pack2_bf16(eb * x[4 * j + 6], eb * x[4 * j + 7]));
                 }
             }
             warp_done(bDt);
-            {
+            if (!kMaps) {
                 // the fp32 checkpoint from registers while Sigma runs (off the path from S to the
                 // next chunk's products): a warp's store covers 8 rows x 32 contiguous bytes, whole
                 // 32-byte sectors; streamed (the backward reads the bf16 copy)
@@ -895,9 +928,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                             *reinterpret_cast<float2 *>(p.S_T + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0)) =
                                 make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]);
                 // (the staging tiles are free once the previous chunk's stores have read them: fS)
-                w = mbar_wait(mY, (NC - 1) & 1) && mbar_wait(fS, (NC - 1) & 1);
+                w = kMaps || (mbar_wait(mY, (NC - 1) & 1) && mbar_wait(fS, (NC - 1) & 1));
                 fail = __any_sync(kFullMask, !w);
-                if (!fail) {
+                if (!fail && !kMaps) {
                     tc_fence_after();
                     epilogue(pga, pgb, pva, pvb);
                     warp_done(bE);
@@ -918,45 +951,64 @@ size_t chunk_prep_smem(int Dk, int Dv) {
 }
 size_t chunk_sweep_smem(int Dk) { return SweepSmem(Dk).total; }
 
-template <int E>
-static cudaError_t launch_chunk_t(const ChunkParams &p, const ChunkFwdMaps &maps, cudaStream_t s) {
-    constexpr int DK = 32 * E;
-    const size_t sp = PrepSmem(DK).total, ss = SweepSmem(DK).total;
-    cudaError_t err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
-    if (err != cudaSuccess) return err;
-    // two prep CTAs share an SM: ask for the largest shared-memory carve-out
-    err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (err != cudaSuccess) return err;
+template <int E, bool kMaps>
+static cudaError_t prepare_sweep(size_t ss) {
     // the sweep's register split waits for registers that only a launch of kFwdLaunchRegs per
     // thread provides
     cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, chunk_sweep_kernel<E>);
+    cudaError_t err = cudaFuncGetAttributes(&fa, chunk_sweep_kernel<E, kMaps>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs < kFwdLaunchRegs || fa.maxThreadsPerBlock < kFwdThreads) return cudaErrorInvalidConfiguration;
-    err = cudaFuncSetAttribute(chunk_sweep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
-    if (err != cudaSuccess) return err;
-    timing_mark("chunk_prep", 0, s);
-    const int units = p.NC * p.Hv * p.B;
-    int dev = 0, sms = 0;
-    err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err != cudaSuccess) return err;
-    // persistent: two CTAs per SM
-    err = launch_pdl(chunk_prep_kernel<E>, dim3(units < 2 * sms ? units : 2 * sms), dim3(256), sp, s, p, units, maps);
-    timing_mark("chunk_prep", 1, s);
-    if (err != cudaSuccess) return err;
-    timing_mark("chunk_sweep", 0, s);
-    err = launch_pdl(chunk_sweep_kernel<E>, dim3(p.Dv / kL, p.Hv, p.B), dim3(kFwdThreads), ss, s, p, maps);
-    timing_mark("chunk_sweep", 1, s);
+    return cudaFuncSetAttribute(chunk_sweep_kernel<E, kMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+}
+
+template <int E>
+static cudaError_t launch_chunk_t(const ChunkParams &p, const ChunkFwdMaps &maps, cudaStream_t s, int stages) {
+    constexpr int DK = 32 * E;
+    const size_t sp = PrepSmem(DK).total, ss = SweepSmem(DK).total;
+    cudaError_t err = cudaSuccess;
+    if (stages & kStagePrep) {
+        err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
+        if (err != cudaSuccess) return err;
+        // two prep CTAs share an SM: ask for the largest shared-memory carve-out
+        err = cudaFuncSetAttribute(chunk_prep_kernel<E>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (err != cudaSuccess) return err;
+        timing_mark("chunk_prep", 0, s);
+        const int units = p.NC * p.Hv * p.B;
+        int dev = 0, sms = 0;
+        err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+        // persistent: two CTAs per SM
+        err = launch_pdl(chunk_prep_kernel<E>, dim3(units < 2 * sms ? units : 2 * sms), dim3(256), sp, s, p, units, maps);
+        timing_mark("chunk_prep", 1, s);
+        if (err != cudaSuccess) return err;
+    }
+    if (stages & kStageSweep) {
+        err = prepare_sweep<E, false>(ss);
+        if (err != cudaSuccess) return err;
+        timing_mark("chunk_sweep", 0, s);
+        err = launch_pdl(chunk_sweep_kernel<E, false>, dim3(p.Dv / kL, p.Hv, p.B), dim3(kFwdThreads), ss, s, p, maps);
+        timing_mark("chunk_sweep", 1, s);
+        if (err != cudaSuccess) return err;
+    }
+    if (stages & kStageMaps) {
+        // the maps: p.Dv is Dk (the identity's rows), p.S_T receives them
+        err = prepare_sweep<E, true>(ss);
+        if (err != cudaSuccess) return err;
+        timing_mark("chunk_maps", 0, s);
+        err = launch_pdl(chunk_sweep_kernel<E, true>, dim3(DK / kL, p.Hv, p.B), dim3(kFwdThreads), ss, s, p, maps);
+        timing_mark("chunk_maps", 1, s);
+    }
     return err;
 }
 
-cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s) {
+cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s, int stages) {
     switch (Dk) {
-        case 64: return launch_chunk_t<2>(p, maps, s);
-        case 128: return launch_chunk_t<4>(p, maps, s);
-        case 192: return launch_chunk_t<6>(p, maps, s);
+        case 64: return launch_chunk_t<2>(p, maps, s, stages);
+        case 128: return launch_chunk_t<4>(p, maps, s, stages);
+        case 192: return launch_chunk_t<6>(p, maps, s, stages);
         default: return cudaErrorInvalidValue;
     }
 }

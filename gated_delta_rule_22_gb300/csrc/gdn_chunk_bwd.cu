@@ -1042,7 +1042,7 @@ size_t chunk_grad_smem(int Dk, int Dv) { return GradSmem(Dk, Dv).total; }
 template <int E>
 static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
                                       const CUtensorMap &tm_qk, const CUtensorMap &tm_pk, const CUtensorMap &tm_dq,
-                                      const CUtensorMap &tm_dk, cudaStream_t s) {
+                                      const CUtensorMap &tm_dk, cudaStream_t s, int stages) {
     constexpr int DK = 32 * E;
     const size_t sd = DSweepSmem(DK).total, sg = GradSmem(DK, p.Dv).total;
     // the reverse sweep's register split waits for registers that only a launch of
@@ -1055,11 +1055,14 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(chunk_grad_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
     if (err != cudaSuccess) return err;
-    timing_mark("chunk_dsweep", 0, s);
-    err = launch_pdl(chunk_dsweep_kernel<E>, dim3(p.nsplit, p.Hv, p.B), dim3(kSweepThreads), sd, s, p, tm_dv, tm_dy,
-                     tm_qk, tm_pk);
-    timing_mark("chunk_dsweep", 1, s);
-    if (err != cudaSuccess) return err;
+    if (stages & kStageDsweep) {
+        timing_mark("chunk_dsweep", 0, s);
+        err = launch_pdl(chunk_dsweep_kernel<E>, dim3(p.nsplit, p.Hv, p.B), dim3(kSweepThreads), sd, s, p, tm_dv, tm_dy,
+                         tm_qk, tm_pk);
+        timing_mark("chunk_dsweep", 1, s);
+        if (err != cudaSuccess) return err;
+    }
+    if (!(stages & kStageGrad)) return err;
     timing_mark("chunk_grad", 0, s);
     const int groups = p.NC * p.Hk * p.B;                   // (b, chunk, kv head)
     int dev = 0, sms = 0;
@@ -1075,12 +1078,11 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
 
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
                              const CUtensorMap &tm_qk, const CUtensorMap &tm_pk, const CUtensorMap &tm_dq,
-                             const CUtensorMap &tm_dk, int Dk,
-                             cudaStream_t s) {
+                             const CUtensorMap &tm_dk, int Dk, cudaStream_t s, int stages) {
     switch (Dk) {
-        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s);
-        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s);
-        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s);
+        case 64: return launch_chunk_bwd_t<2>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s, stages);
+        case 128: return launch_chunk_bwd_t<4>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s, stages);
+        case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s, stages);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -494,7 +494,12 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 struct ChunkFwdMaps {
     CUtensorMap vb, k, q, qk, y, r;
 };
-cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s);
+// The chunkwise forward's kernels to launch (a bit set): prep (per-chunk products into the saved
+// buffer), the sweep (states, checkpoints, y, v - u, S_T), and the maps (the sweep's state maps
+// of the sequence-parallel form: p.Dv = Dk rows of the identity, S_T receives them, [B][Hv][Dk][Dk]).
+constexpr int kStagePrep = 1, kStageSweep = 2, kStageMaps = 4;
+cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s,
+                             int stages = kStagePrep | kStageSweep);
 size_t chunk_prep_smem(int Dk, int Dv);
 size_t chunk_sweep_smem(int Dk);
 // Chunkwise backward: the reverse sweep over chunks (dS), the per-chunk gradient products
@@ -505,10 +510,17 @@ size_t chunk_sweep_smem(int Dk);
 // (per b, value head, chunk) as {256, 2, 2 halves, columns / 8, blocks}, box one half: a
 // [64][columns] operand tile (Q or K; P).
 // tm_dq, tm_dk: dq and dk as [B][T][Hk][Dk] bf16, 4-D, box {64, 1, 64, 1}, 128-byte swizzle.
+// stages: the reverse sweep (dS, dD, dv, dbeta, f, dS0, the workspace) and the gradient kernel.
+constexpr int kStageDsweep = 1, kStageGrad = 2;
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
                              const CUtensorMap &tm_qk, const CUtensorMap &tm_pk, const CUtensorMap &tm_dq,
-                             const CUtensorMap &tm_dk, int Dk,
-                             cudaStream_t s);
+                             const CUtensorMap &tm_dk, int Dk, cudaStream_t s, int stages = kStageDsweep | kStageGrad);
+// The scan over segments of the sequence-parallel form: forward X_0 = X0 (zero if null),
+// X_s = X_{s-1} M_{s-1} + C_{s-1}; reverse X_{P-1} = X0, X_s = X_{s+1} M_{s+1}^T + C_{s+1}. X, C:
+// [B*P][Hv][rows][Dk] fp32 (rows a multiple of 64), M: [B*P][Hv][Dk][Dk] fp32, X0: [B][Hv][rows][Dk].
+cudaError_t launch_segment_scan(const float *X0, const float *M, const float *C, float *X, int B, int P, int Hv,
+                                int rows, int Dk, bool reverse, cudaStream_t s);
+size_t segment_scan_smem(int Dk);
 size_t chunk_dsweep_smem(int Dk);
 size_t chunk_grad_smem(int Dk, int Dv);
 cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s);

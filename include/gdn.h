@@ -180,6 +180,39 @@ GDN_API int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k
                             void *dg, void *dbeta, float *dS0, void *stream);
 
 /*
+ * Sequence-parallel form (mlx-lm PR #1217, "Scope", names prefix scans as later work). The
+ * state map of a run of chunks is affine, S -> S M + C (M a Dk x Dk matrix); splitting the
+ * sequence into `segments` equal runs of whole chunks, every segment's chunks are swept from a
+ * zero state (C) and as maps (M) side by side, the segments' start states follow from a scan
+ * over the segments (X_0 = S0, X_s = X_{s-1} M_{s-1} + C_{s-1}), and the segments are swept
+ * again from their start states; the backward runs the reverse sweep twice around the reverse
+ * scan (with the transposed maps). Same results as gdn_fwd / gdn_bwd within the bf16 tolerance;
+ * it pays where the plain sweep leaves SMs idle (few heads, long sequences): the segments add
+ * parallelism at the price of about three times the sweeps' work.
+ *   shape     bf16, chunk 64, a shape the tensor-core path takes both ways (else
+ *             GDN_ERR_UNSUPPORTED_SHAPE), T a multiple of 64 * segments, segments >= 1.
+ *   saved     ckpt of gdn_seg_ckpt_bytes(shape, segments) bytes: the saved buffer of the
+ *             problem seen as B * segments rows of T / segments steps (view row b * segments
+ *             + s is segment s of row b: the chunk-start states of segment s of row b, value
+ *             head h, are ckpt[(b * segments + s), h, c] for its chunks c), then the maps
+ *             [B * segments][Hv][Dk][Dk] float32 (from a 256-byte boundary).
+ *   scratch   workspace of gdn_seg_workspace_bytes(shape, segments) bytes (device, 16-byte
+ *             aligned; contents on entry do not matter): two [B * segments][Hv][Dv][Dk]
+ *             float32 arrays, then the backward's workspace of the viewed problem.
+ * Other arguments as for gdn_fwd / gdn_bwd (S0, S_T, dS_T, dS0 may be NULL). Returns GDN_OK or an
+ * error code; a size query returns 0 for a shape or segment count it does not take.
+ */
+GDN_API size_t gdn_seg_ckpt_bytes(const gdn_shape *shape, int segments);
+GDN_API size_t gdn_seg_workspace_bytes(const gdn_shape *shape, int segments);
+GDN_API int gdn_fwd_seg(const gdn_shape *shape, int segments, const void *q, const void *k, const void *v,
+                        const void *g, const void *beta, const float *S0, void *y, float *S_T, float *ckpt,
+                        size_t ckpt_bytes, void *workspace, size_t workspace_bytes, void *stream);
+GDN_API int gdn_bwd_seg(const gdn_shape *shape, int segments, const void *q, const void *k, const void *v,
+                        const void *g, const void *beta, const float *ckpt, size_t ckpt_bytes, const void *dy,
+                        const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta, float *dS0,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Gates of the layer: the decay g and write strength beta from its raw gate inputs, and the
  * VJP back to them (mlx-lm PR #1217, "Correctness", trains through q, k, v, a, b, A_log,
  * dt_bias and the state; no page prints the gate map, and the one taken is the public
