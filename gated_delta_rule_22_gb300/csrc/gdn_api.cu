@@ -397,7 +397,8 @@ size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
 }
 
 // The chunkwise forward on the tensor cores for plan p (a segmented call passes its view): the
-// stages of launch_chunk_fwd; maps_out receives the maps stage's output ([B][Hv][Dk][Dk]).
+// stages of launch_chunk_fwd; maps_out receives the lite stage's maps ([B][Hv][Dk][Dk], then the
+// same transposed) and S_T its end states.
 static int tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const void *g, const void *beta,
                   const float *S0, void *y, float *S_T, float *ckpt, float *maps_out, int stages, cudaStream_t stream) {
     const ChunkLayout cl = chunk_layout(p);
@@ -405,6 +406,8 @@ static int tc_fwd(const Plan &p, const void *q, const void *k, const void *v, co
     gdn::ChunkParams cp;
     cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.S0 = S0; cp.y = y; cp.S_T = S_T;
     cp.ckpt = ckpt; cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
+    cp.maps_M = maps_out;
+    cp.maps_Mt = maps_out != nullptr ? maps_out + (size_t)p.B * p.Hv * p.Dk * p.Dk : nullptr;
     cp.lam = reinterpret_cast<float *>(sb + cl.lam);
     cp.pkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.pkm);
     cp.wm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.wm);
@@ -424,19 +427,7 @@ static int tc_fwd(const Plan &p, const void *q, const void *k, const void *v, co
         (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
         (rc = make_colblock_map(&maps.r, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK)
         return rc;
-    const int first = stages & (gdn::kStagePrep | gdn::kStageSweep);
-    if (first) {
-        rc = cuda_status(gdn::launch_chunk_fwd(cp, maps, p.Dk, stream, first));
-        if (rc != GDN_OK) return rc;
-    }
-    if (stages & gdn::kStageMaps) {
-        gdn::ChunkParams cm = cp;
-        cm.Dv = p.Dk;                      // the identity's rows
-        cm.S0 = nullptr;
-        cm.S_T = maps_out;
-        rc = cuda_status(gdn::launch_chunk_fwd(cm, maps, p.Dk, stream, gdn::kStageMaps));
-    }
-    return rc;
+    return cuda_status(gdn::launch_chunk_fwd(cp, maps, p.Dk, stream, stages));
 }
 
 // The chunkwise backward on the tensor cores for plan p: the stages of launch_chunk_bwd.
@@ -572,7 +563,7 @@ static size_t seg_state_bytes(const Plan &pv) { return round_up((size_t)pv.B * p
 size_t gdn_seg_ckpt_bytes(const gdn_shape *shape, int segments) {
     Plan p, pv;
     if (shape == nullptr || seg_plans(shape, segments, &p, &pv) != GDN_OK) return 0;
-    return seg_maps_offset(pv) + round_up((size_t)pv.B * pv.Hv * pv.Dk * pv.Dk * 4);
+    return seg_maps_offset(pv) + round_up(2 * (size_t)pv.B * pv.Hv * pv.Dk * pv.Dk * 4);
 }
 
 size_t gdn_seg_workspace_bytes(const gdn_shape *shape, int segments) {
@@ -581,10 +572,15 @@ size_t gdn_seg_workspace_bytes(const gdn_shape *shape, int segments) {
     return 2 * seg_state_bytes(pv) + bwd_workspace_total(pv);
 }
 
-// dst[b] = src[b * P + s] for every b: blocks of `blk` bytes
+// dst[b] = src[b * P + s] for every b: blocks of `blk` bytes, one copy per batch row
 static int seg_pick(void *dst, const void *src, size_t blk, int B, int P, int s, cudaStream_t stream) {
-    return cuda_status(cudaMemcpy2DAsync(dst, blk, static_cast<const char *>(src) + (size_t)s * blk, (size_t)P * blk, blk,
-                                         (size_t)B, cudaMemcpyDeviceToDevice, stream));
+    for (int b = 0; b < B; ++b) {
+        const int rc = cuda_status(cudaMemcpyAsync(static_cast<char *>(dst) + (size_t)b * blk,
+                                                   static_cast<const char *>(src) + ((size_t)b * P + s) * blk, blk,
+                                                   cudaMemcpyDeviceToDevice, stream));
+        if (rc != GDN_OK) return rc;
+    }
+    return GDN_OK;
 }
 
 int gdn_fwd_seg(const gdn_shape *shape, int segments, const void *q, const void *k, const void *v, const void *g,
@@ -604,11 +600,13 @@ int gdn_fwd_seg(const gdn_shape *shape, int segments, const void *q, const void 
     float *maps = reinterpret_cast<float *>(reinterpret_cast<char *>(ckpt) + seg_maps_offset(pv));
     float *C = static_cast<float *>(workspace);
     float *X = reinterpret_cast<float *>(static_cast<char *>(workspace) + seg_state_bytes(pv));
-    // every segment from a zero state (its end state: C) and as maps, then the scan of the
-    // start states, then every segment again from its start state
-    rc = tc_fwd(pv, q, k, v, g, beta, nullptr, y, C, ckpt, maps, gdn::kStagePrep | gdn::kStageSweep | gdn::kStageMaps, st);
+    // every segment from a zero state (its end state: C) and as maps (the lite sweep), then the
+    // scan of the start states, then every segment again from its start state
+    rc = tc_fwd(pv, q, k, v, g, beta, nullptr, y, C, ckpt, maps, gdn::kStagePrep | gdn::kStageLite, st);
     if (rc != GDN_OK) return rc;
-    rc = cuda_status(gdn::launch_segment_scan(S0, maps, C, X, p.B, segments, p.Hv, p.Dv, p.Dk, false, st));
+    int *status = nullptr;
+    if ((rc = device_status_address(&status)) != GDN_OK) return rc;
+    rc = cuda_status(gdn::launch_segment_scan(S0, maps, C, X, p.B, segments, p.Hv, p.Dv, p.Dk, false, status, st));
     if (rc != GDN_OK) return rc;
     rc = tc_fwd(pv, q, k, v, g, beta, X, y, C, ckpt, nullptr, gdn::kStageSweep, st);
     if (rc != GDN_OK || S_T == nullptr) return rc;
@@ -639,7 +637,10 @@ int gdn_bwd_seg(const gdn_shape *shape, int segments, const void *q, const void 
     // scan of the end adjoints, then the backward proper from them
     rc = tc_bwd(pv, beta, ckpt, dy, nullptr, dq, dk, dv, dg, dbeta, D, ws, gdn::kStageDsweep, st);
     if (rc != GDN_OK) return rc;
-    rc = cuda_status(gdn::launch_segment_scan(dS_T, maps, D, Y, p.B, segments, p.Hv, p.Dv, p.Dk, true, st));
+    int *status = nullptr;
+    if ((rc = device_status_address(&status)) != GDN_OK) return rc;
+    const float *maps_t = maps + (size_t)pv.B * pv.Hv * pv.Dk * pv.Dk;
+    rc = cuda_status(gdn::launch_segment_scan(dS_T, maps_t, D, Y, p.B, segments, p.Hv, p.Dv, p.Dk, true, status, st));
     if (rc != GDN_OK) return rc;
     rc = tc_bwd(pv, beta, ckpt, dy, Y, dq, dk, dv, dg, dbeta, D, ws, gdn::kStageDsweep | gdn::kStageGrad, st);
     if (rc != GDN_OK || dS0 == nullptr) return rc;

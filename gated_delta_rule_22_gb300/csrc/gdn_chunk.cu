@@ -494,11 +494,13 @@ struct SweepSmem {
 // double-buffered and fetched two chunks ahead. y and v - u leave by TMA stores from staging
 // tiles (the copy warp, once bE says they are written).
 //
-// With kMaps, the same sweep computes instead each chunk range's state map (the sequence-parallel
-// form): the "state" is the Dk x Dk identity (rows r0 .. r0 + 63 of it per CTA; p.Dv = Dk) and V
-// counts as zero, so the chunks compose S <- S (exp(Lam_L) I - W^T diag(E_L) K); only S_T (the
-// map) is written -- no checkpoints, states, y or v - u.
-template <int E, bool kMaps>
+// With kLite, the same sweep takes only the state through the chunks, for the sequence-parallel
+// form: no checkpoints, bf16 states, y or v - u, so no Q S^T, K S^T, P Delta or KKm Delta
+// products. Its first Dv / 64 CTAs of a head (the "ends") start from zero and write the end state
+// to S_T; the next Dk / 64 (the "maps") take rows r0 .. r0 + 63 of the Dk x Dk identity with V
+// counted as zero, so the chunks compose S <- S (exp(Lam_L) I - W^T diag(E_L) K), and write that
+// map to maps_M and its transpose to maps_Mt.
+template <int E, bool kLite>
 __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams p, const __grid_constant__ ChunkFwdMaps maps) {
     constexpr int DK = 32 * E;
     constexpr int SC = DK / 2;                // state columns per warp half
@@ -507,7 +509,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool math = warp < kFwdMathWarps;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, Dv = p.Dv, Hv = p.Hv, r0 = split * kL, NC = p.NC;
+    const int T = p.T, Dv = p.Dv, Hv = p.Hv, NC = p.NC;
+    const bool ends = !kLite || split < Dv / kL;               // a block of value rows (else of the identity)
+    const bool maps_cta = kLite && !ends;
+    const int r0 = (ends ? split : split - Dv / kL) * kL;
     const int hw = (warp >> 2) & 1;                             // warp half
     const uint32_t lane16 = (uint32_t)(32 * (warp & 3)) << 16;   // tensor-memory lane base of this warp's M = 64 rows
 
@@ -559,7 +564,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             constexpr uint32_t id64 = umma_idesc(1, kL, kL);
             // U = (T diag(beta)) V starts Delta's accumulator (the first chunk's here, each later
             // one once the previous Delta is read out)
-            if constexpr (!kMaps) {
+            if (ends) {
                 const bool w = mbar_wait(bW, 0);
                 fail = __any_sync(kFullMask, !w);
                 if (!fail) {
@@ -572,19 +577,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             for (int c = 0; c < NC && !fail; ++c) {
                 unsigned char *wc = wbuf(c);
                 // ---- Delta += (-W) S^T once S is written (the maps: Delta = (-W) S^T)
-                bool w = mbar_wait(bS, c & 1) && (!kMaps || mbar_wait(bW + (c & 1), (c >> 1) & 1));
+                bool w = mbar_wait(bS, c & 1) && (!maps_cta || mbar_wait(bW + (c & 1), (c >> 1) & 1));
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
-                umma_gemm_w(tD, CmOp{wc, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, !kMaps, lead);
+                umma_gemm_w(tD, CmOp{wc, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, ends, lead);
                 umma_commit_w(mD, lead);
-                if constexpr (kMaps) {
-                    // ---- Sigma = (diag(E_L) Delta)^T K once Delta is written
+                if constexpr (kLite) {
+                    // ---- Sigma = (diag(E_L) Delta)^T K once Delta is written; then U of the next
+                    // chunk (the ends)
                     w = mbar_wait(bDt, c & 1) && mbar_wait(cbK, c & 1);
                     if (__any_sync(kFullMask, !w)) { fail = true; break; }
                     tc_fence_after();
                     umma_gemm_w(tSg, CmOp{de, kL, 0, 0, true}, CmOp{kb, kL, 0, 0, true}, kL,
                                 umma_idesc_t(1, kL, DK, true, true), false, lead);
                     umma_commit_w(mU, lead);
+                    if (ends && c + 1 < NC) {
+                        w = mbar_wait(bW + ((c + 1) & 1), ((c + 1) >> 1) & 1);
+                        if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                        tc_fence_after();
+                        unsigned char *g = wbuf(c + 1);
+                        umma_gemm_wd(tD, CmOp{g + (L.tc - L.wc), kL, 0, 0, false}, sw128_mnmajor(g + (L.vb - L.wc)),
+                                     2048 >> 4, kL, umma_idesc_t(1, kL, kL, false, true), false, lead);
+                    }
                     continue;
                 }
                 // ---- Q S^T and K S^T once the previous chunk's are read out and Q, K landed
@@ -632,9 +646,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     const size_t ck = head * NC + cc;
                     unsigned char *g = wbuf(cc);
                     uint64_t *bw = bW + (cc & 1);
-                    mbar_expect_tx(bw, kMaps ? kL * DK * 2 : kL * DK * 2 + 2 * kL * kL * 2);
+                    mbar_expect_tx(bw, maps_cta ? kL * DK * 2 : kL * DK * 2 + 2 * kL * kL * 2);
                     bulk_load(g, p.wm + ck * kL * DK, kL * DK * 2, bw);
-                    if constexpr (!kMaps) {
+                    if (ends) {
                         bulk_load(g + (L.tc - L.wc), p.tcm + ck * kL * kL, kL * kL * 2, bw);
                         tma_load_4d(g + (L.vb - L.wc), &maps.vb, bw, r0, h, cc * kL, b);
                     }
@@ -663,19 +677,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 };
                 for (int cc = 0; cc < 2 && cc < NC; ++cc) issue_w(cc);
                 copy_K(0);
-                if constexpr (!kMaps) {
+                if constexpr (!kLite) {
                     copy_Q(0);
                     copy_P(0);
                 }
-                for (int c = 0; c < NC && kMaps; ++c) {
-                    // the maps: K and group W (-W only) only; Sigma done frees K, Delta read out
-                    // frees -W, and the state operand's tile is free once Sigma is done
+                for (int c = 0; c < NC && kLite; ++c) {
+                    // K and group W only. Sigma done (mU) frees K; it also means that every product
+                    // issued before it is done (U and Delta of chunk c), so group W's buffer of
+                    // chunk c takes chunk c + 2; and the state operand's tile is free
                     if (!mbar_wait(mU, c & 1) || !mbar_wait(bDt, c & 1)) { fail = true; break; }
                     if (c + 1 < NC) copy_K(c + 1);
                     if (c + 2 < NC) issue_w(c + 2);
                     mbar_arrive(fS);
                 }
-                for (int c = 0; c < NC && !kMaps; ++c) {
+                for (int c = 0; c < NC && !kLite; ++c) {
                     const size_t chk = head * NC + c;
                     // the bf16 state leaves (the backward's operand) once written
                     if (!mbar_wait(bS, c & 1)) { fail = true; break; }
@@ -708,7 +723,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     if (nK > 0) mbar_wait(cbK, (nK - 1) & 1);
                     for (int i = 0; i < 2; ++i)
                         if (nW[i] > 0) mbar_wait(bW + i, (nW[i] - 1) & 1);
-                } else if (kMaps) {
+                } else if (kLite) {
                 } else if (mbar_wait(bE, (NC - 1) & 1)) {
                     store_out(NC - 1);                      // the last chunk's y and v - u
                 } else {
@@ -732,9 +747,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             for (int k2 = 0; k2 < 2; ++k2) {
                 float2 s2 = make_float2(0.f, 0.f);
                 const int row = r0 + fs.row(2 * k2), col = fs.col(j, 0);
-                if (kMaps)
+                if (maps_cta)
                     s2 = make_float2(row == col ? 1.f : 0.f, row == col + 1 ? 1.f : 0.f);
-                else if (p.S0 != nullptr)
+                else if (!kLite && p.S0 != nullptr)
                     s2 = *reinterpret_cast<const float2 *>(p.S0 + (head * Dv + row) * DK + col);
                 S[4 * j + 2 * k2] = s2.x;
                 S[4 * j + 2 * k2 + 1] = s2.y;
@@ -817,7 +832,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             }
         };
         load_lam(0);
-        if (!kMaps) load_v(0);
+        if (!kLite) load_v(0);
         float decay = 1.f, pga = 1.f, pgb = 1.f;     // exp(Lam_L), exp(Lam_ta), exp(Lam_tb) of the previous chunk
         uint32_t pva[4], pvb[4];                      // v pairs of the previous chunk
         for (int c = 0; c < NC; ++c) {
@@ -831,7 +846,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             }
             if (c + 1 < NC) {
                 load_lam(c + 1);
-                if (!kMaps) load_v(c + 1);
+                if (!kLite) load_v(c + 1);
             }
             // ---- S <- exp(Lam_L) S + Sigma of the previous chunk; S as an operand
             if (c > 0) {
@@ -853,7 +868,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             write_sop();
             warp_done(bS);
             // ---- y and v - u of the previous chunk
-            if (!kMaps && c > 0) {
+            if (!kLite && c > 0) {
                 const bool w = mbar_wait(mY, (c - 1) & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
@@ -875,7 +890,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
 #pragma unroll
                 for (int j = 0; j < 4; j += 2) {
                     const uint32_t o = frag_row_addr(0, kL, 16 * (warp & 3), 4 * hw + j, lane);
-                    if (!kMaps)
+                    if (!kLite)
                         stmatrix_x4(smem_addr(dt) + o, pack2_bf16(x[4 * j], x[4 * j + 1]),
                                     pack2_bf16(x[4 * j + 2], x[4 * j + 3]), pack2_bf16(x[4 * j + 4], x[4 * j + 5]),
                                     pack2_bf16(x[4 * j + 6], x[4 * j + 7]));
@@ -885,7 +900,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 }
             }
             warp_done(bDt);
-            if (!kMaps) {
+            if (!kLite) {
                 // the fp32 checkpoint from registers while Sigma runs (off the path from S to the
                 // next chunk's products): a warp's store covers 8 rows x 32 contiguous bytes, whole
                 // 32-byte sectors; streamed (the backward reads the bf16 copy)
@@ -920,17 +935,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
 #pragma unroll
                     for (int e = 0; e < 16; ++e) S[16 * i + e] = fmaf(decay, S[16 * i + e], x[e]);
                 }
-                if (p.S_T != nullptr)
+                float *out = maps_cta ? p.maps_M : p.S_T;
+                const int orows = maps_cta ? DK : Dv;
+                if (out != nullptr)
 #pragma unroll
                     for (int j = 0; j < NS / 4; ++j)
 #pragma unroll
                         for (int k2 = 0; k2 < 2; ++k2)
-                            *reinterpret_cast<float2 *>(p.S_T + (head * Dv + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0)) =
+                            *reinterpret_cast<float2 *>(out + (head * orows + r0 + fs.row(2 * k2)) * DK + fs.col(j, 0)) =
                                 make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]);
+                // the map also transposed (the reverse scan's operand)
+                if (maps_cta && p.maps_Mt != nullptr)
+#pragma unroll
+                    for (int j = 0; j < NS / 4; ++j)
+#pragma unroll
+                        for (int k2 = 0; k2 < 2; ++k2) {
+                            const int row = r0 + fs.row(2 * k2), col = fs.col(j, 0);
+                            p.maps_Mt[(head * DK + col) * DK + row] = S[4 * j + 2 * k2];
+                            p.maps_Mt[(head * DK + col + 1) * DK + row] = S[4 * j + 2 * k2 + 1];
+                        }
                 // (the staging tiles are free once the previous chunk's stores have read them: fS)
-                w = kMaps || (mbar_wait(mY, (NC - 1) & 1) && mbar_wait(fS, (NC - 1) & 1));
+                w = kLite || (mbar_wait(mY, (NC - 1) & 1) && mbar_wait(fS, (NC - 1) & 1));
                 fail = __any_sync(kFullMask, !w);
-                if (!fail && !kMaps) {
+                if (!fail && !kLite) {
                     tc_fence_after();
                     epilogue(pga, pgb, pva, pvb);
                     warp_done(bE);
@@ -951,15 +978,15 @@ size_t chunk_prep_smem(int Dk, int Dv) {
 }
 size_t chunk_sweep_smem(int Dk) { return SweepSmem(Dk).total; }
 
-template <int E, bool kMaps>
+template <int E, bool kLite>
 static cudaError_t prepare_sweep(size_t ss) {
     // the sweep's register split waits for registers that only a launch of kFwdLaunchRegs per
     // thread provides
     cudaFuncAttributes fa;
-    cudaError_t err = cudaFuncGetAttributes(&fa, chunk_sweep_kernel<E, kMaps>);
+    cudaError_t err = cudaFuncGetAttributes(&fa, chunk_sweep_kernel<E, kLite>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs < kFwdLaunchRegs || fa.maxThreadsPerBlock < kFwdThreads) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(chunk_sweep_kernel<E, kMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+    return cudaFuncSetAttribute(chunk_sweep_kernel<E, kLite>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
 }
 
 template <int E>
@@ -993,13 +1020,14 @@ static cudaError_t launch_chunk_t(const ChunkParams &p, const ChunkFwdMaps &maps
         timing_mark("chunk_sweep", 1, s);
         if (err != cudaSuccess) return err;
     }
-    if (stages & kStageMaps) {
-        // the maps: p.Dv is Dk (the identity's rows), p.S_T receives them
+    if (stages & kStageLite) {
+        // the end states from zero (Dv / 64 CTAs of a head) and the maps (Dk / 64) in one launch
         err = prepare_sweep<E, true>(ss);
         if (err != cudaSuccess) return err;
-        timing_mark("chunk_maps", 0, s);
-        err = launch_pdl(chunk_sweep_kernel<E, true>, dim3(DK / kL, p.Hv, p.B), dim3(kFwdThreads), ss, s, p, maps);
-        timing_mark("chunk_maps", 1, s);
+        timing_mark("chunk_lite", 0, s);
+        err = launch_pdl(chunk_sweep_kernel<E, true>, dim3(p.Dv / kL + DK / kL, p.Hv, p.B), dim3(kFwdThreads), ss, s, p,
+                         maps);
+        timing_mark("chunk_lite", 1, s);
     }
     return err;
 }

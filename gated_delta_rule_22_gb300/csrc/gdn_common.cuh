@@ -82,6 +82,7 @@ struct ChunkParams {
     const float *S0;
     void *y;
     float *S_T, *ckpt, *resid;
+    float *maps_M, *maps_Mt;   // the lite sweep's maps and their transposes ([B][Hv][Dk][Dk] each)
     float *lam;
     __nv_bfloat16 *pkm, *wm, *tm, *tcm, *s0m, *qkm;
     int *status;
@@ -495,9 +496,10 @@ struct ChunkFwdMaps {
     CUtensorMap vb, k, q, qk, y, r;
 };
 // The chunkwise forward's kernels to launch (a bit set): prep (per-chunk products into the saved
-// buffer), the sweep (states, checkpoints, y, v - u, S_T), and the maps (the sweep's state maps
-// of the sequence-parallel form: p.Dv = Dk rows of the identity, S_T receives them, [B][Hv][Dk][Dk]).
-constexpr int kStagePrep = 1, kStageSweep = 2, kStageMaps = 4;
+// buffer), the sweep (states, checkpoints, y, v - u, S_T), and the lite sweep of the
+// sequence-parallel form (every row's end state from a zero start into p.S_T, the state maps into
+// p.maps_M and their transposes into p.maps_Mt, [B][Hv][Dk][Dk] each; nothing else is written).
+constexpr int kStagePrep = 1, kStageSweep = 2, kStageLite = 4;
 cudaError_t launch_chunk_fwd(const ChunkParams &p, const ChunkFwdMaps &maps, int Dk, cudaStream_t s,
                              int stages = kStagePrep | kStageSweep);
 size_t chunk_prep_smem(int Dk, int Dv);
@@ -517,10 +519,11 @@ cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, 
                              const CUtensorMap &tm_dk, int Dk, cudaStream_t s, int stages = kStageDsweep | kStageGrad);
 // The scan over segments of the sequence-parallel form: forward X_0 = X0 (zero if null),
 // X_s = X_{s-1} M_{s-1} + C_{s-1}; reverse X_{P-1} = X0, X_s = X_{s+1} M_{s+1}^T + C_{s+1}. X, C:
-// [B*P][Hv][rows][Dk] fp32 (rows a multiple of 64), M: [B*P][Hv][Dk][Dk] fp32, X0: [B][Hv][rows][Dk].
+// [B*P][Hv][rows][Dk] fp32 (rows a multiple of 64), X0: [B][Hv][rows][Dk]. M: [B*P][Hv][Dk][Dk]
+// fp32, the maps for the forward scan and their transposes for the reverse one (the kernel reads
+// M row by row either way). A bounded wait that gives up writes kStatusTimeout to *status.
 cudaError_t launch_segment_scan(const float *X0, const float *M, const float *C, float *X, int B, int P, int Hv,
-                                int rows, int Dk, bool reverse, cudaStream_t s);
-size_t segment_scan_smem(int Dk);
+                                int rows, int Dk, bool reverse, int *status, cudaStream_t s);
 size_t chunk_dsweep_smem(int Dk);
 size_t chunk_grad_smem(int Dk, int Dv);
 cudaError_t launch_gates_bwd(const GatesParams &p, int dtype, cudaStream_t s);

@@ -182,20 +182,21 @@ GDN_API int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k
 /*
  * Sequence-parallel form (mlx-lm PR #1217, "Scope", names prefix scans as later work). The
  * state map of a run of chunks is affine, S -> S M + C (M a Dk x Dk matrix); splitting the
- * sequence into `segments` equal runs of whole chunks, every segment's chunks are swept from a
- * zero state (C) and as maps (M) side by side, the segments' start states follow from a scan
- * over the segments (X_0 = S0, X_s = X_{s-1} M_{s-1} + C_{s-1}), and the segments are swept
- * again from their start states; the backward runs the reverse sweep twice around the reverse
- * scan (with the transposed maps). Same results as gdn_fwd / gdn_bwd within the bf16 tolerance;
- * it pays where the plain sweep leaves SMs idle (few heads, long sequences): the segments add
- * parallelism at the price of about three times the sweeps' work.
+ * sequence into `segments` equal runs of whole chunks, one sweep takes every segment from a zero
+ * state to its end state (C) and through its map (M) -- the state alone, none of the other
+ * outputs -- then a scan over the segments gives their start states (X_0 = S0, X_s = X_{s-1}
+ * M_{s-1} + C_{s-1}), and the segments are swept again from them, now writing y and the saved
+ * buffer. The backward runs the reverse sweep from zero end adjoints, the reverse scan (with the
+ * transposed maps), then the backward proper. Same results as gdn_fwd / gdn_bwd within the
+ * bf16 tolerance; it pays where the plain sweep leaves SMs idle (few heads, long sequences).
  *   shape     bf16, chunk 64, a shape the tensor-core path takes both ways (else
  *             GDN_ERR_UNSUPPORTED_SHAPE), T a multiple of 64 * segments, segments >= 1.
  *   saved     ckpt of gdn_seg_ckpt_bytes(shape, segments) bytes: the saved buffer of the
  *             problem seen as B * segments rows of T / segments steps (view row b * segments
  *             + s is segment s of row b: the chunk-start states of segment s of row b, value
  *             head h, are ckpt[(b * segments + s), h, c] for its chunks c), then the maps
- *             [B * segments][Hv][Dk][Dk] float32 (from a 256-byte boundary).
+ *             [B * segments][Hv][Dk][Dk] float32 (from a 256-byte boundary) and their
+ *             transposes (the same layout, right after them).
  *   scratch   workspace of gdn_seg_workspace_bytes(shape, segments) bytes (device, 16-byte
  *             aligned; contents on entry do not matter): two [B * segments][Hv][Dv][Dk]
  *             float32 arrays, then the backward's workspace of the viewed problem.

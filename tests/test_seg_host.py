@@ -32,11 +32,12 @@ def r256(x):
 
 def test_sizes_are_those_of_the_viewed_problem(lib):
     """Segments of whole chunks: the saved buffer is the viewed problem's (B * P rows of T / P
-    steps) followed by the maps; the workspace is two state arrays and the viewed backward's."""
+    steps) followed by the maps and their transposes; the workspace is two state arrays and the
+    viewed backward's."""
     for P in (1, 2, 4, 8):
         s = shape()
         v = shape(B=2 * P, T=512 // P)
-        maps = 2 * P * 4 * 128 * 128 * 4
+        maps = 2 * (2 * P * 4 * 128 * 128 * 4)           # the maps and their transposes
         states = 2 * P * 4 * 128 * 128 * 4
         assert lib.gdn_seg_ckpt_bytes(ctypes.byref(s), P) == r256(lib.gdn_ckpt_bytes(ctypes.byref(v))) + r256(maps)
         assert lib.gdn_seg_workspace_bytes(ctypes.byref(s), P) == (
