@@ -72,6 +72,8 @@ KERNEL_FILES = {
     "chunk_sweep": ("gdn_chunk.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
     "chunk_dsweep": ("gdn_chunk_bwd.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
     "chunk_grad": ("gdn_chunk_bwd.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
+    "chunk_lite": ("gdn_chunk.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
+    "segment_scan": ("gdn_segments.cu", "gdn_common.cuh", "gdn_api.cu"),
     "seq_fwd": ("gdn_fwd.cu", "gdn_common.cuh", "gdn_api.cu"),
     "seq_bwd": ("gdn_bwd.cu", "gdn_common.cuh", "gdn_api.cu"),
     "seq_reduce": ("gdn_bwd.cu", "gdn_common.cuh", "gdn_api.cu"),
@@ -356,18 +358,41 @@ def run_ours(args, w):
     torch.cuda.reset_peak_memory_stats(dev)
     y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
     S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
-    ckpt = gdn.new_ckpt(t["q"], t["v"], w.chunk)
     grads = {"dq": torch.empty_like(t["q"]), "dk": torch.empty_like(t["k"]), "dv": torch.empty_like(t["v"]),
              "dg": torch.empty_like(t["g"]), "dbeta": torch.empty_like(t["beta"]),
              "dS0": torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)}
     shape = gdn.make_shape(B, T, Hk, Hv, Dk, Dv, w.chunk, 1 if w.dtype == "bf16" else 0)
-    ws = torch.empty(gdn.gdn_bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    P = args.segments
+    if P:
+        # the sequence-parallel form: its own saved buffer and workspace
+        def new_saved(q, v):
+            return torch.empty(gdn.gdn_seg_ckpt_bytes(shape, P), dtype=torch.uint8, device=dev)
+        ws = torch.empty(gdn.gdn_seg_workspace_bytes(shape, P), dtype=torch.uint8, device=dev)
+    else:
+        def new_saved(q, v):
+            return gdn.new_ckpt(q, v, w.chunk)
+        ws = torch.empty(gdn.gdn_bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    ckpt = new_saved(t["q"], t["v"])
     stream = torch.cuda.current_stream()
 
+    def fwd(d, y_, S_T_, ck):
+        if P:
+            gdn.gdn_fwd_seg(d["q"], d["k"], d["v"], d["g"], d["beta"], t["S0"], P, y=y_, S_T=S_T_, ckpt=ck,
+                            workspace=ws)
+        else:
+            gdn.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], t["S0"], w.chunk, y=y_, S_T=S_T_, ckpt=ck)
+
+    def bwd(d, ck, out):
+        if P:
+            gdn.gdn_bwd_seg(d["q"], d["k"], d["v"], d["g"], d["beta"], ck, d["dy"], t["dS_T"], P, workspace=ws,
+                            out=out)
+        else:
+            gdn.gdn_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], ck, d["dy"], t["dS_T"], w.chunk, workspace=ws,
+                        out=out)
+
     def step():
-        gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"], w.chunk, y=y, S_T=S_T, ckpt=ckpt)
-        gdn.gdn_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], ckpt, t["dy"], t["dS_T"], w.chunk,
-                    workspace=ws, out=grads)
+        fwd(t, y, S_T, ckpt)
+        bwd(t, ckpt, grads)
 
     step()
     torch.cuda.synchronize()
@@ -387,10 +412,9 @@ def run_ours(args, w):
         for i in range(K):
             flush.fill_(i & 0xFF)                       # untimed: evicts L2 between steps
             ev[i][0].record(stream)
-            gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"], w.chunk, y=y, S_T=S_T, ckpt=ckpt)
+            fwd(t, y, S_T, ckpt)
             ev[i][1].record(stream)
-            gdn.gdn_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], ckpt, t["dy"], t["dS_T"], w.chunk,
-                        workspace=ws, out=grads)
+            bwd(t, ckpt, grads)
             ev[i][2].record(stream)
         torch.cuda.synchronize()
         if world > 1:
@@ -433,7 +457,7 @@ def run_ours(args, w):
             d_in = {n: torch.empty(host_in[n].shape, dtype=dt, device=dev) for n in names}
             d_out = {n: torch.empty(sh, dtype=dty, device=dev) for n, sh, dty in out_shapes}
             h_out = {n: torch.empty(sh, dtype=dty).pin_memory() for n, sh, dty in out_shapes}
-            ck = gdn.new_ckpt(d_in["q"], d_in["v"], w.chunk)
+            ck = new_saved(d_in["q"], d_in["v"])
             slots.append(dict(d_in=d_in, d_out=d_out, h_out=h_out, ck=ck, up=torch.cuda.Event(),
                               done=torch.cuda.Event(), down=torch.cuda.Event()))
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -455,10 +479,8 @@ def run_ours(args, w):
             if i >= nslot:
                 comp.wait_event(sl["down"])              # step i - nslot's results have left
             d, o = sl["d_in"], sl["d_out"]
-            gdn.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], t["S0"], w.chunk, y=o["y"], S_T=o["S_T"],
-                        ckpt=sl["ck"])
-            gdn.gdn_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], sl["ck"], d["dy"], t["dS_T"], w.chunk,
-                        workspace=ws, out={n: o[n] for n in grads})
+            fwd(d, o["y"], o["S_T"], sl["ck"])
+            bwd(d, sl["ck"], {n: o[n] for n in grads})
             sl["done"].record(comp)
             if i + 1 < K:
                 upload(i + 1)
@@ -491,7 +513,10 @@ def run_ours(args, w):
     model = kernel_model(w)
     kernels = {}
     for name, (n, ms) in ktimes.items():
-        kernels[name] = kernel_roofline(name, ms / n, model.get(name, (0.0, 0.0, 0.0)), peaks)
+        # per launch; the sequence-parallel form launches some families twice a step, and its
+        # families are taken per step against the plain form's model of them
+        per = K if P else n
+        kernels[name] = kernel_roofline(name, ms / per, model.get(name, (0.0, 0.0, 0.0)), peaks)
         kernels[name]["launches_per_step"] = n / K
         kernels[name]["share"] = ms / sum(t for _, t in ktimes.values())
         kernels[name]["traffic"] = traffic_of(name)
@@ -529,9 +554,9 @@ def run_ours(args, w):
                            "head at the measured FP32 rate); the chunkwise form that ran does other work, so "
                            "this is not a bound of this step"}
     NCk = -(-w.T // w.chunk)
-    memory = {"ckpt_buffer_bytes": gdn.gdn_ckpt_bytes(shape),
+    memory = {"ckpt_buffer_bytes": gdn.gdn_seg_ckpt_bytes(shape, P) if P else gdn.gdn_ckpt_bytes(shape),
               "ckpt_states_bytes": w.B * w.Hv * NCk * w.Dv * w.Dk * 4,
-              "bwd_workspace_bytes": gdn.gdn_bwd_workspace_bytes(shape),
+              "bwd_workspace_bytes": gdn.gdn_seg_workspace_bytes(shape, P) if P else gdn.gdn_bwd_workspace_bytes(shape),
               "peak_allocated_bytes": peak_alloc,
               "note": "peak_allocated_bytes: torch's peak device allocation over one fwd + bwd step "
                       "(inputs, outputs, saved buffer and workspace)"}
@@ -544,7 +569,10 @@ def run_ours(args, w):
         "dtype_note": ("bf16 tensor-core operands, f32 state and accumulation" if mma > 0
                        else "f32 arithmetic on the sequential kernels"),
         "data": "synthetic",
-        "config": config_of(w, l2="flushed between steps by an untimed 256 MiB write"),
+        "config": {**config_of(w, l2="flushed between steps by an untimed 256 MiB write"),
+                   **({"segments": P, "form": "sequence-parallel (gdn_fwd_seg / gdn_bwd_seg)",
+                       "kernels_note": "per-family figures are per step, against the plain form's model"}
+                      if P else {})},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "roofline": roof,
         "roofline_step": roofline_step,
@@ -581,6 +609,8 @@ def main():
     ap.add_argument("--workload", default="linattn-T2048", choices=sorted(gs.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--segments", type=int, default=0,
+                    help="time the sequence-parallel form with this many segments (0: the plain calls)")
     args = ap.parse_args()
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps

@@ -74,6 +74,9 @@ WORKLOADS = {
     "linattn-T2048": Workload("linattn-T2048", 1, 2048, 16, 64, 192, 128, "bf16", "weak"),
     "batched": Workload("batched", 8, 4096, 16, 32, 128, 128, "bf16", "half", True, True),
     "long": Workload("long", 1, 32768, 16, 64, 192, 128, "bf16", "weak", chunk=64),
+    # the long-context layer's share of one GPU when its heads are split eight ways (2 of the 16
+    # kv heads and their 8 value heads): few heads, so the sequence-parallel form has SMs to fill
+    "long-tp8": Workload("long-tp8", 1, 32768, 2, 8, 192, 128, "bf16", "weak", chunk=64),
 }
 
 

@@ -6,8 +6,8 @@ its end adjoint), and the chunkwise kernels run on the B * P segment rows.
 Checked against the float64 oracle run on the WHOLE sequence (no segments): y, S_T, the
 chunk-start checkpoints (the segment rows' checkpoints put back in [B, Hv, NC, Dv, Dk] order)
 and every gradient, with start states and final-state cotangents, GQA, every supported key
-width, 2 to 16 segments, one chunk per segment, and the long-context workload (two kv-head
-groups compared). One segment gives the plain chunkwise call's outputs bit for bit, and two
+width, 2 to 16 segments, one chunk per segment, and the long-context workloads at full size
+(two kv-head groups compared). One segment gives the plain chunkwise call's outputs bit for bit, and two
 runs agree bit for bit. Tolerance 5e-3 relative L2 (bf16 inputs)."""
 import os
 
@@ -105,17 +105,20 @@ def test_segmented_is_deterministic(dev):
         assert torch.equal(a[n], b[n]), n
 
 
-def test_segmented_long_context(dev):
-    """The long-context workload (T = 32768, 64 value heads on 16 kv heads, Dk = 192) in 4
-    segments: two kv-head groups of every output against the oracle on those groups."""
-    w = gs.WORKLOADS["long"]
+@pytest.mark.parametrize("name,P", [("long", 4), ("long-tp8", 8)])
+def test_segmented_long_context(dev, name, P):
+    """The long-context workloads at full size, in the segment counts the benchmark times: T =
+    32768, Dk = 192 (64 value heads on 16 kv heads in 4 segments; the 8-way head split, 8 value
+    heads on 2 kv heads, in 8): the first and last kv-head groups of every output against the
+    oracle on those groups."""
+    w = gs.WORKLOADS[name]
     inp = gs.make_inputs(w)
-    out = run_seg(inp, 4, dev)
+    out = run_seg(inp, P, dev)
     for hk in (0, w.Hk - 1):
         got = H.group_outputs(out, w, 0, hk)
         ref = H.oracle_group(inp, 0, hk)
         errs = H.errors(got, ref)
-        print("long P4 group", hk, {n: f"{e:.2e}" for n, e in errs.items()})
-        H.log_errors(f"long-P4-group{hk}", errs)
+        print(name, "P", P, "group", hk, {n: f"{e:.2e}" for n, e in errs.items()})
+        H.log_errors(f"{name}-P{P}-group{hk}", errs)
         bad = {n: e for n, e in errs.items() if not e <= H.TOL["bf16"]}
         assert not bad, (hk, bad)
