@@ -264,6 +264,27 @@ int make_btd_map(CUtensorMap *map, const void *ptr, bool bf16, int B, int T, int
     return GDN_OK;
 }
 
+// 2-D tensor map of a row-major fp32 [rows][cols] array, box {32, box_rows}, 128-byte swizzle.
+int make_rows_map(CUtensorMap *map, void *ptr, size_t rows, int cols, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available from the driver");
+        return GDN_ERR_CUDA;
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 // 5-D tensor map of a row-major [B][T][H][D] tensor (bf16 or fp32) whose box lands in shared
 // memory column block by column block: dimensions {inner, T, D / inner, H, B}, box
 // {inner, box_t, box_c, 1, 1}, so that one box holds box_c blocks of `inner` columns, each
@@ -425,8 +446,10 @@ static int tc_fwd(const Plan &p, const void *q, const void *k, const void *v, co
         (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
         (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK ||
         (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
-        (rc = make_colblock_map(&maps.r, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK)
+        (rc = make_colblock_map(&maps.r, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK ||
+        (rc = make_rows_map(&maps.ck, ckpt, (size_t)p.B * p.Hv * p.NC * p.Dv, p.Dk, 64)) != GDN_OK)
         return rc;
+    if ((size_t)p.B * p.Hv * p.NC * p.Dv > 0x7fffffffu) return GDN_ERR_UNSUPPORTED_SHAPE;   // TMA row coordinates
     return cuda_status(gdn::launch_chunk_fwd(cp, maps, p.Dk, stream, stages));
 }
 

@@ -444,8 +444,11 @@ constexpr int kFwdThreads = 384;     // + a warpgroup: warp 8 issues the product
 constexpr int kFwdLaunchRegs = 168, kFwdMathRegs = 176, kFwdCtrlRegs = 152;
 static_assert(2 * 128 * kFwdMathRegs + 128 * kFwdCtrlRegs <= kFwdThreads * kFwdLaunchRegs, "register split");
 
+constexpr size_t kCkBox = (size_t)kL * 32 * 4;   // a [64][32] fp32 box of the checkpoint
+
 struct SweepSmem {
-    size_t wgrp, wc, tc, vb, qb, kb, pk, sop, dt, de, ysg, rsg, bar, tslot, total;
+    size_t wgrp, wc, tc, vb, qb, kb, pk, sop, dt, de, ysg, rsg, ckx, bar, tslot, total;
+    int ck_in_w;
     __host__ __device__ SweepSmem(int DK) {
         size_t o = 0;
         // group W, two buffers (chunks alternate): -W, T diag(beta), V
@@ -462,6 +465,11 @@ struct SweepSmem {
         de = o; o += (size_t)kL * kL * 2;      // diag(E_L) Delta [64 t][64 v], read MN-major (A, transposed)
         ysg = al(o, 1024); o = ysg + (size_t)kL * 128;       // y of a chunk, bf16 [64][64] in the 128-byte swizzle
         rsg = al(o, 1024); o = rsg + (size_t)2 * kL * 128;   // v - u of a chunk, fp32 [2][64][32] in the 128-byte swizzle
+        // the fp32 checkpoint of a chunk, staged for TMA stores as DK / 32 boxes [64][32] fp32 in
+        // the 128-byte swizzle (8 KB each): the first ck_in_w in the chunk's group W buffer (free
+        // once Delta is formed), the rest here, two buffers (chunks alternate)
+        ck_in_w = (int)(wgrp / kCkBox) < DK / 32 ? (int)(wgrp / kCkBox) : DK / 32;
+        ckx = al(o, 1024); o = ckx + 2 * (size_t)(DK / 32 - ck_in_w) * kCkBox;
         bar = al(o, 8); o = bar + 16 * 8;      // see the kernel
         // (V is read in the 128-byte swizzle: its tiles start at 1024-byte boundaries, as do both
         // groups W for every DK here: the W tile is a multiple of 8 KB)
@@ -524,10 +532,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bar);
     uint64_t *mD = bar, *mQ = bar + 1, *mU = bar + 2, *mY = bar + 3, *cbQ = bar + 4, *cbP = bar + 5;
     uint64_t *bW = bar + 6, *cbK = bar + 8;                     // bW[2]: one per buffer
-    uint64_t *bS = bar + 10, *bE = bar + 11, *bDt = bar + 12, *fS = bar + 13, *mX = bar + 14;
+    uint64_t *bS = bar + 10, *bE = bar + 11, *bDt = bar + 12, *fS = bar + 13, *mX = bar + 14, *bK = bar + 15;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
     // the buffer of chunk c's group W (-W, T diag(beta), V)
     auto wbuf = [&](int c) { return base + L.wc + (size_t)(c & 1) * L.wgrp; };
+    // box q of chunk c's staged fp32 checkpoint
+    auto ck_box = [&](int c, int q) {
+        return q < L.ck_in_w ? wbuf(c) + q * kCkBox
+                             : base + L.ckx + ((size_t)(c & 1) * (DK / 32 - L.ck_in_w) + (q - L.ck_in_w)) * kCkBox;
+    };
 
     const size_t head = (size_t)b * Hv + h;
     const int hk = h / (Hv / p.Hk);
@@ -537,6 +550,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
         for (int i = 0; i < 10; ++i) mbar_init(bar + i, 1);
         for (int i = 10; i < 13; ++i) mbar_init(bar + i, kFwdMathWarps);
         for (int i = 13; i < 15; ++i) mbar_init(bar + i, 1);
+        mbar_init(bK, kFwdMathWarps);
         fence_mbar_init();
     }
     if (warp == kFwdMathWarps + 1 && lane == 0) {
@@ -704,14 +718,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     // Q S^T and K S^T are done: Q is free
                     if (!mbar_wait(mQ, c & 1)) { fail = true; break; }
                     if (c + 1 < NC) copy_Q(c + 1);
-                    // Sigma is done: K is free; Delta was read out (bDt, before Sigma), so group W's
-                    // buffer is free too (the chunk two ahead); once the stores have read them, the
-                    // state operand's tile and the y, v - u staging are free
+                    // Sigma is done: K is free
                     if (!mbar_wait(mU, c & 1) || !mbar_wait(bDt, c & 1)) { fail = true; break; }
                     if (c + 1 < NC) copy_K(c + 1);
-                    if (c + 2 < NC) issue_w(c + 2);
-                    bulk_wait_read();
+                    // the staged fp32 checkpoint leaves; once the stores before it have read the
+                    // state operand's tile and the y, v - u staging, they are free (fS); once it
+                    // has been read too, group W's buffer takes chunk c + 2
+                    if (!mbar_wait(bK, c & 1)) { fail = true; break; }
+                    for (int q = 0; q < DK / 32; ++q) tma_store_2d(&maps.ck, ck_box(c, q), 32 * q, (int)(chk * Dv + r0));
+                    bulk_commit();
+                    bulk_wait_read_but<1>();
                     mbar_arrive(fS);
+                    bulk_wait_read();
+                    if (c + 2 < NC) issue_w(c + 2);
                     // P Delta and KKm Delta are done: [P; KKm] is free
                     if (!mbar_wait(mY, c & 1)) { fail = true; break; }
                     if (c + 1 < NC) copy_P(c + 1);
@@ -836,7 +855,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
         float decay = 1.f, pga = 1.f, pgb = 1.f;     // exp(Lam_L), exp(Lam_ta), exp(Lam_tb) of the previous chunk
         uint32_t pva[4], pvb[4];                      // v pairs of the previous chunk
         for (int c = 0; c < NC; ++c) {
-            const size_t chk = head * NC + c;
             const float lL = nlL, la = nla, lb = nlb;
             uint32_t cva[4], cvb[4];
 #pragma unroll
@@ -901,16 +919,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             }
             warp_done(bDt);
             if (!kLite) {
-                // the fp32 checkpoint from registers while Sigma runs (off the path from S to the
-                // next chunk's products): a warp's store covers 8 rows x 32 contiguous bytes, whole
-                // 32-byte sectors; streamed (the backward reads the bf16 copy)
-                float *ck = p.ckpt + (chk * Dv + r0) * DK;
+                // the fp32 checkpoint while Sigma runs (off the path from S to the next chunk's
+                // products), staged for the copy warp's TMA stores: box q = col / 32 holds row r,
+                // 16-byte piece j = (col % 32) / 4 at r * 128 + ((j ^ (r % 8)) << 4); the group W
+                // buffer of this chunk is free (Delta is formed, mD) until the copy warp refills it
+                // after these stores have read it
 #pragma unroll
                 for (int j = 0; j < NS / 4; ++j)
 #pragma unroll
-                    for (int k2 = 0; k2 < 2; ++k2)
-                        __stcs(reinterpret_cast<float2 *>(ck + fs.row(2 * k2) * DK + fs.col(j, 0)),
-                               make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]));
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        const int row = fs.row(2 * k2), col = fs.col(j, 0);
+                        unsigned char *box = ck_box(c, col >> 5);
+                        *reinterpret_cast<float2 *>(box + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4) + (col & 3) * 4) =
+                            make_float2(S[4 * j + 2 * k2], S[4 * j + 2 * k2 + 1]);
+                    }
+                warp_done(bK);
             }
             decay = expf(lL);
             pga = expf(la);

@@ -492,8 +492,10 @@ cudaError_t launch_gates_fwd(const GatesParams &p, int dtype, cudaStream_t s);
 // TMA stores from an operand tile of 64 rows, read back the same way.
 // Written by TMA stores, 128-byte swizzle: y as [B][T][Hv][Dv] bf16, box {64, 1, 64, 1}; r (v - u)
 // as 5-D column blocks of [B][T][Hv][Dv] fp32 {32, T, Dv / 32, Hv, B}, box {32, 64, 2, 1, 1}.
+// ck, the fp32 checkpoints [B][Hv][NC][Dv][Dk] as 2-D {Dk, B*Hv*NC*Dv}, box {32, 64}, 128-byte
+// swizzle: written by TMA stores from staged [64][32] boxes.
 struct ChunkFwdMaps {
-    CUtensorMap vb, k, q, qk, y, r;
+    CUtensorMap vb, k, q, qk, y, r, ck;
 };
 // The chunkwise forward's kernels to launch (a bit set): prep (per-chunk products into the saved
 // buffer), the sweep (states, checkpoints, y, v - u, S_T), and the lite sweep of the
