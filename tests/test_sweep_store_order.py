@@ -8,7 +8,9 @@ thread commits which tiles and where it waits, and checks every rewrite of a til
 thread, after the block barrier that follows the wait) against the groups still reading it.
 The sequences are written by hand from the kernels' code (chunk_prep_kernel,
 chunk_sweep_kernel, chunk_dsweep_kernel, chunk_grad_kernel) and must be kept in step with it;
-each kernel has a control that drops one wait and must fail."""
+each kernel has a control that drops one wait and must fail. In the sweeps the math warps'
+rewrites follow the copy warp's waits through mbarrier hand-offs; the model places each
+rewrite at the earliest point those hand-offs allow."""
 import pytest
 
 
@@ -31,38 +33,57 @@ class Stores:
 
 
 def sweep(NC, drop=None):
-    """chunk_sweep_kernel: thread 32 stores the bf16 state (sop) per chunk; thread 128 stores y and
-    v - u (ysg, rsg) of the previous chunk; both wait at the top of each chunk, thread 128 again
-    before the last epilogue."""
+    """chunk_sweep_kernel: the copy warp's issuing lane stores every tile. Per chunk c it stores the
+    bf16 state (sop) once the math warps have written it, the previous chunk's y and v - u (ysg,
+    rsg), and the staged fp32 checkpoint (group W's buffer c % 2 and the extra box ckx c % 2);
+    then it waits until all but that newest group have read their tiles and releases sop, ysg
+    and rsg to the math warps (fS), which go on with the next chunk, while it waits for the rest
+    and refills group W's buffer c % 2 with chunk c + 2's operands."""
     st = Stores()
+    T = "copy"
+    st.write({"sop"}, "state operand of chunk 0")
     for c in range(NC):
-        if drop != "top32":
-            st.wait_read(32)
-        if drop != "top128":
-            st.wait_read(128)
-        st.write({"sop"}, f"state operand of chunk {c}")
-        st.commit(32, {"sop"})
+        st.commit(T, {"sop"})
         if c > 0:
-            st.write({"ysg", "rsg"}, f"y / v - u staging of chunk {c - 1}")
-            st.commit(128, {"ysg", "rsg"})
-    if drop != "final":
-        st.wait_read(128)
+            st.commit(T, {"ysg", "rsg"})
+        st.write({f"W{c % 2}", f"ckx{c % 2}"}, f"staged checkpoint of chunk {c}")
+        st.commit(T, {f"W{c % 2}", f"ckx{c % 2}"})
+        if drop != "fS":
+            st.wait_read(T, but=1)
+        if c + 1 < NC:
+            st.write({"sop"}, f"state operand of chunk {c + 1}")
+            st.write({"ysg", "rsg"}, f"y / v - u staging of chunk {c}")
+        if drop != "W":
+            st.wait_read(T)
+        if c + 2 < NC:
+            st.write({f"W{c % 2}"}, f"group W of chunk {c + 2}")
     st.write({"ysg", "rsg"}, f"y / v - u staging of chunk {NC - 1}")
-    st.commit(128, {"ysg", "rsg"})
+    st.commit(T, {"ysg", "rsg"})
 
 
 def dsweep(NC, drop=None):
-    """chunk_dsweep_kernel: thread 32 stores dS_L (the high tile of shl) after the first products'
-    barrier, and [dY; dU], Delta and dv at the chunk's end; it waits at the top of each chunk."""
+    """chunk_dsweep_kernel: the copy warp's issuing lane stores every tile. Per chunk (in reverse
+    order) it stores dS_L (the high tile of shl) once the math warps have written it and releases
+    shl (fS) after that store has read it; then it stores the chunk's [dY; dU] buffer, Delta and
+    dv (dls, dvs) and, after they have been read, releases dls and dvs (fO) and refills that
+    [dY; dU] buffer with the dY of the chunk two ahead. The math warps write the next chunk's dS
+    operands after fS and the carry, its Delta and dv tiles after fO."""
     st = Stores()
-    for c in reversed(range(NC)):
-        buf = (NC - 1 - c) & 1
-        if drop != "top":
-            st.wait_read(32)
-        st.write({"shl"}, f"dS operands of chunk {c}")
-        st.commit(32, {"shl"})
-        st.write({f"ydu{buf}", "dls", "dvs", "yds"}, f"dU rows, Delta and dv of chunk {c}")
-        st.commit(32, {f"ydu{buf}", "dls", "dvs"})
+    T = "copy"
+    st.write({"shl"}, f"dS operands of chunk {NC - 1}")
+    for k in range(NC):
+        c, buf = NC - 1 - k, k & 1
+        st.commit(T, {"shl"})
+        if drop != "fS":
+            st.wait_read(T)
+        st.write({f"ydu{buf}", "dls", "dvs"}, f"dU rows, Delta and dv of chunk {c}")
+        st.commit(T, {f"ydu{buf}", "dls", "dvs"})
+        if k + 1 < NC:
+            st.write({"shl"}, f"dS operands of chunk {c - 1}")
+        if drop != "fO":
+            st.wait_read(T)
+        if k + 2 < NC:
+            st.write({f"ydu{buf}"}, f"dY of chunk {c - 2}")
 
 
 def grad(groups, rep, drop=None):
@@ -116,7 +137,7 @@ def test_grad_and_prep_never_rewrite_a_tile_in_flight(groups, rep):
 
 
 @pytest.mark.parametrize("fn,arg,drop", [
-    (sweep, 3, "top32"), (sweep, 3, "top128"), (sweep, 2, "final"), (dsweep, 2, "top"),
+    (sweep, 3, "fS"), (sweep, 3, "W"), (dsweep, 2, "fS"), (dsweep, 3, "fO"),
     (grad, (2, 2), "top"), (grad, (1, 2), "between"), (prep, (8, 4), "tcu"),
 ])
 def test_controls_without_a_wait_fail(fn, arg, drop):
