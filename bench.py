@@ -73,6 +73,7 @@ KERNEL_FILES = {
     "chunk_dsweep": ("gdn_chunk_bwd.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
     "chunk_grad": ("gdn_chunk_bwd.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
     "chunk_lite": ("gdn_chunk.cu", "gdn_common.cuh", "gdn_umma.cuh", "gdn_api.cu"),
+    "decode": ("gdn_decode.cu", "gdn_common.cuh", "gdn_api.cu"),
     "segment_scan": ("gdn_segments.cu", "gdn_common.cuh", "gdn_api.cu"),
     "seq_fwd": ("gdn_fwd.cu", "gdn_common.cuh", "gdn_api.cu"),
     "seq_bwd": ("gdn_bwd.cu", "gdn_common.cuh", "gdn_api.cu"),
@@ -600,6 +601,96 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+DECODE_METRIC = "gated-delta decode tokens/s (one step, state in and out; Hv64,Dk192,Dv128 bf16)"
+
+
+def run_decode(args, w):
+    """One decode step of B sequences per call: gdn_fwd with T = 1, no saved buffer, the state
+    passed in (S0) and returned (S_T), ping-ponged between two device arrays. HBM-bound: each
+    step reads and writes every state once (2 B Hv Dv Dk fp32) plus the step's small tensors."""
+    import torch
+    import gated_delta_rule_22_gb300 as gdn
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    gdn.load_library()
+    inp = gs.make_inputs(w)
+    dt = torch.bfloat16
+    names = ("q", "k", "v", "g", "beta")
+    t = {n: torch.from_numpy(inp[n]).to(dev).to(dt) for n in names}
+    S = [torch.from_numpy(inp["S0"]).to(dev), torch.empty_like(torch.from_numpy(inp["S0"])).to(dev)]
+    y = torch.empty((w.B, 1, w.Hv, w.Dv), dtype=dt, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], S[i & 1], w.chunk, y=y, S_T=S[(i + 1) & 1],
+                    want_ckpt=False)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    K = max(args.steps, 50)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    with ClockSampler(dev.index) as clk:
+        for i in range(K):
+            flush.fill_(i & 0xFF)                       # untimed: evicts L2 between steps
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    gdn.gdn_timing_read()
+    gdn.gdn_timing_enable(True)
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        step(i)
+    torch.cuda.synchronize()
+    kt = gdn.gdn_timing_read()
+    gdn.gdn_timing_enable(False)
+    # end to end: the step's inputs up from pinned host memory, y back down; the state stays
+    host_in = {n: torch.from_numpy(inp[n]).to(dt).pin_memory() for n in names}
+    h_y = torch.empty(y.shape, dtype=dt).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = y.numel() * y.element_size()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(K):
+        for n in names:
+            t[n].copy_(host_in[n], non_blocking=True)
+        step(i)
+        h_y.copy_(y, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = start.elapsed_time(end) / K
+    e = 2
+    state = w.B * w.Hv * w.Dv * w.Dk * 4
+    nbytes = 2 * state + w.B * (2 * w.Hk * w.Dk + 2 * w.Hv * w.Dv + 2 * w.Hv) * e
+    peaks = load_peaks()
+    kname = "decode" if "decode" in kt else "seq_fwd"
+    n_fwd, ms_fwd = kt.get(kname, (K, ms * K))
+    per_launch = ms_fwd / n_fwd
+    achieved = nbytes / (per_launch * 1e-3) / 1e9
+    line = {
+        "metric": DECODE_METRIC, "value": w.B / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**config_of(w, l2="flushed between steps by an untimed 256 MiB write"), "form": "decode"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_of(kname), "kernel": kname,
+                     "ms_per_launch": per_launch, "per_launch": nbytes,
+                     "per_launch_note": "the state read and written once (fp32), q, k, v, g, beta read and y written once",
+                     "peak_source": peaks["source"]},
+        "kernels": {k: {"launches_per_step": n / K, "ms_per_launch": m / n} for k, (n, m) in kt.items()},
+        "e2e": {"value": w.B / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "mode": "one stream: the step's inputs up, the step, y down; the state stays on the device"},
+        "gpu_launches": int(round(sum(n for n, _ in kt.values()))),
+        "clocks": clk.summary(),
+        "kernel_sources": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -617,6 +708,8 @@ def main():
     w = gs.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.T == 1:
+        run_decode(args, w)
     else:
         run_ours(args, w)
 

@@ -17,7 +17,7 @@ LIB = os.path.join(PKG, "libgdn.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 SOURCES = ["gdn_api.cu", "gdn_fwd.cu", "gdn_bwd.cu", "gdn_gates.cu", "gdn_chunk.cu", "gdn_chunk_bwd.cu",
-           "gdn_diag.cu", "gdn_segments.cu"]
+           "gdn_diag.cu", "gdn_segments.cu", "gdn_decode.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
     "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -511,6 +511,8 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     if (p.tc && ckpt != nullptr)       // chunkwise form on the tensor cores
         return tc_fwd(p, q, k, v, g, beta, S0, y, S_T, ckpt, nullptr, gdn::kStagePrep | gdn::kStageSweep,
                       (cudaStream_t)stream);
+    if (p.T == 1 && ckpt == nullptr && gdn::decode_takes(p.Dk))   // a decode step: one streaming pass
+        return cuda_status(gdn::launch_decode(fp, p.Dk, p.dtype, (cudaStream_t)stream));
     CUtensorMap tm_q, tm_k;
     if ((rc = make_qk_map(&tm_q, q, p, gdn::kFwdTile)) != GDN_OK) return rc;
     if ((rc = make_qk_map(&tm_k, k, p, gdn::kFwdTile)) != GDN_OK) return rc;

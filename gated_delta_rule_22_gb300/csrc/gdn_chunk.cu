@@ -63,7 +63,7 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
 
 // T = (I + A)^-1 for the strictly lower 64 x 64 A (row stride kP), in two levels of 2 x 2
 // block recursion: the four diagonal 16 x 16 blocks by forward substitution (a column per
-// thread); then the two 32 x 32 diagonal blocks, and then the 64 x 64, each by
+// thread, rows above the column's diagonal exactly zero); then the two 32 x 32 diagonal blocks, and then the 64 x 64, each by
 //     T_21 = -T_22 (A_21 T_11)
 // as two dependent products with four consecutive columns of one row per thread (a scalar
 // and a float4 load per four multiply-adds). Blocks of T above the diagonal are not written,
@@ -73,17 +73,20 @@ template <class Other>
 __device__ void invert_unit_lower(const float *am, float *ts, float *xs, int tid, Other &&other) {
     if (tid >= kL) other();
     if (tid < kL) {
+        // column c of the block's inverse, right-looking: once x_i is final it updates every
+        // later row at once, so the dependent chain is 16 multiply-adds long (not 120)
         const int b0 = 16 * (tid >> 4), c = tid & 15;
-        float col[16];
+        float acc[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float x = r == c ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) acc[r] = r == c ? 1.f : 0.f;
 #pragma unroll
-            for (int i = 0; i < r; ++i) x = fmaf(-am[(b0 + r) * kP + b0 + i], col[i], x);
-            col[r] = r < c ? 0.f : x;
+        for (int i = 0; i < 15; ++i) {
+            const float xi = acc[i];
+#pragma unroll
+            for (int r = i + 1; r < 16; ++r) acc[r] = fmaf(-am[(b0 + r) * kP + b0 + i], xi, acc[r]);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) ts[(b0 + r) * kP + b0 + c] = col[r];
+        for (int r = 0; r < 16; ++r) ts[(b0 + r) * kP + b0 + c] = acc[r];
     }
     __syncthreads();
     // ---- level 1: the 32 x 32 diagonal blocks b = 0, 1 (threads 0-127)

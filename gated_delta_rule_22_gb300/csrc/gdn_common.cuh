@@ -469,6 +469,10 @@ void timing_mark(const char *kernel, int phase, cudaStream_t s);
 
 // Launchers (one per kernel family); each returns the cudaError_t of its launch.
 // tm_q / tm_k: 4-D tensor maps of q and k ([B, T, Hk, Dk], box {Dk, 1, kFwdTile, 1}).
+// One decode step (T = 1, nothing saved): a streaming pass over the state (gdn_decode.cu), for
+// Dk in {64, 128, 192, 256} (decode_takes).
+bool decode_takes(int Dk);
+cudaError_t launch_decode(const FwdParams &p, int Dk, int dtype, cudaStream_t s);
 cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k, int Dk, int dtype,
                        int warps, cudaStream_t s);
 // tm_q / tm_k: tensor maps with box {Dk, 1, bwd_sub(Dk) + 1, 1}.

@@ -77,6 +77,9 @@ WORKLOADS = {
     # the long-context layer's share of one GPU when its heads are split eight ways (2 of the 16
     # kv heads and their 8 value heads): few heads, so the sequence-parallel form has SMs to fill
     "long-tp8": Workload("long-tp8", 1, 32768, 2, 8, 192, 128, "bf16", "weak", chunk=64),
+    # decode: one step of the same layer for B sequences, the state carried in and out (S0, S_T)
+    "decode-B1": Workload("decode-B1", 1, 1, 16, 64, 192, 128, "bf16", "weak", True, False),
+    "decode-B64": Workload("decode-B64", 64, 1, 16, 64, 192, 128, "bf16", "weak", True, False),
 }
 
 

@@ -105,7 +105,9 @@ GDN_API size_t gdn_bwd_workspace_bytes(const gdn_shape *shape);
 /*
  * Forward with checkpoints (or, with ckpt = NULL, without: inference and decode, where no
  * backward follows; a decode step is T = 1 with the carried state passed as S0 and read
- * back from S_T).
+ * back from S_T). A decode step with Dk in {64, 128, 192, 256} runs as one streaming pass
+ * over the state (every state element read once and written once); for that call, and only
+ * that one, S_T may be S0 itself (the state updated in place).
  *   in : q, k, v, g, beta            (dtype)
  *        S0                          (float32, may be NULL: zeros)
  *   out: y                           (dtype)

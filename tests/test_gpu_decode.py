@@ -58,3 +58,47 @@ def test_decode_steps_match_the_oracle(dev, dtype):
     e_y = oracle.rel_l2(y.double().cpu().numpy(), ref["y"])
     e_s = oracle.rel_l2(S.double().cpu().numpy(), ref["S_T"])
     assert e_y <= tol and e_s <= tol, (dtype, e_y, e_s)
+
+
+@pytest.mark.parametrize("name", ["decode-B1", "decode-B64"])
+def test_decode_step_at_the_benchmark_shapes(dev, name):
+    """One decode step of the layer (Hv = 64 on Hk = 16, Dk = 192, Dv = 128) for 1 and 64
+    sequences, as `bench.py --workload decode-B*` times it: y and the carried state, whole
+    tensors, against the oracle."""
+    import gated_delta_rule_22_gb300 as gdn
+    w = gs.WORKLOADS[name]
+    inp = gs.make_inputs(w)
+    t = H.to_device(inp, dev)
+    y, S_T, ck = gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"], want_ckpt=False)
+    torch.cuda.synchronize()
+    assert ck is None
+    ref = oracle.fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["S0"], chunk=w.chunk)
+    e_y = oracle.rel_l2(y.double().cpu().numpy(), ref["y"])
+    e_s = oracle.rel_l2(S_T.double().cpu().numpy(), ref["S_T"])
+    print(name, f"y {e_y:.2e} S_T {e_s:.2e}")
+    assert e_y <= H.TOL["bf16"] and e_s <= H.TOL["bf16"], (e_y, e_s)
+
+
+@pytest.mark.parametrize("w", [
+    gs.Workload("dec-f32-Dv40-noS0", 3, 1, 2, 6, 128, 40, "f32", "strong", False, False),
+    gs.Workload("dec-f32-Dk256", 2, 1, 1, 2, 256, 64, "f32", "weak", True, False),
+    gs.Workload("dec-bf16-Dk96-seq", 2, 1, 1, 3, 96, 64, "bf16", "weak", True, False),   # the sequential kernel
+    gs.Workload("dec-bf16-gqa8", 1, 1, 1, 8, 64, 200, "bf16", "half", True, False),
+], ids=lambda w: w.name)
+def test_decode_step_shapes(dev, w):
+    """The decode step on ragged value widths, no incoming state, every key width it takes (and
+    one it leaves to the sequential kernel), GQA; the state updated in place gives the same."""
+    import gated_delta_rule_22_gb300 as gdn
+    inp = gs.make_inputs(w)
+    t = H.to_device(inp, dev)
+    y, S_T, _ = gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"], want_ckpt=False)
+    ref = oracle.fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["S0"], chunk=w.chunk)
+    tol = H.TOL[w.dtype]
+    e_y = oracle.rel_l2(y.double().cpu().numpy(), ref["y"])
+    e_s = oracle.rel_l2(S_T.double().cpu().numpy(), ref["S_T"])
+    assert e_y <= tol and e_s <= tol, (e_y, e_s)
+    if t["S0"] is not None:
+        S = t["S0"].clone()
+        y2, S2, _ = gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], S, S_T=S, want_ckpt=False)
+        torch.cuda.synchronize()
+        assert torch.equal(y2, y) and torch.equal(S, S_T)
