@@ -90,7 +90,7 @@ struct DSweepSmem {
         rhs = o; o += (size_t)kL * kL * 2;       // diag(E_L) K dS^T + P^T dY [64 t][64 v]
         dls = o; o += (size_t)kL * kL * 2;       // Delta block [64 t][64 v], for the gradient kernel
         dvs = alb(o, 1024); o = dvs + (size_t)kL * 128;   // dv block, bf16 [64][64] in the 128-byte swizzle
-        bar = alb(o, 8); o = bar + 17 * 8;       // see the kernel
+        bar = alb(o, 8); o = bar + 18 * 8;       // see the kernel
         tslot = o; o += 16;
         total = o + 1024;
         if (total < kOneCtaSmem) total = kOneCtaSmem;
@@ -112,7 +112,8 @@ struct DSweepSmem {
 //                        accumulate in fp32); then dD
 //   [DK + 128, DK + 192) P^T dY
 // Hand-offs of chunk c (each completes once per chunk):
-//   math -> control (8 warp arrivals): bH  dS parts written;  bR  rhs and Delta written;
+//   math -> control (8 warp arrivals): bHi the dS high part written;  bH  both dS parts written;
+//                                      bR  rhs and Delta written;
 //                                      bU  dU, [e^Lam dY; e^Lam dU] and dv written
 //   control -> math: m1, mD, mS  the product groups (commits);  fS  the dS parts' tile is free
 //                    (products done, the dS_L store has read it);  fO  the Delta and dv staging
@@ -148,6 +149,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
     uint64_t *m1 = bar, *mD = bar + 1, *mS = bar + 2, *cbT = bar + 3, *cbQ = bar + 4;
     uint64_t *cbP = bar + 5, *cbK = bar + 7, *cbY = bar + 9;   // [2] each: one per buffer
     uint64_t *bH = bar + 11, *bR = bar + 12, *bU = bar + 13, *fS = bar + 14, *fO = bar + 15, *mX = bar + 16;
+    uint64_t *bHi = bar + 17;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + L.tslot);
     // the buffers of the chunk handled k-th (chunk NC - 1 - k): K, P, [dY; dU], Lam
     auto kbuf = [&](int k) { return kb2 + (size_t)(k & 1) * kL * DK * 2; };
@@ -162,6 +164,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
         for (int i = 0; i < 11; ++i) mbar_init(bar + i, 1);
         for (int i = 11; i < 14; ++i) mbar_init(bar + i, kSweepMathWarps);
         for (int i = 14; i < 17; ++i) mbar_init(bar + i, 1);
+        mbar_init(bHi, kSweepMathWarps);
         fence_mbar_init();
     }
     if (warp == kSweepMathWarps + 1 && lane == 0) {
@@ -200,11 +203,15 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
             }
             for (int k = 0; k < NC && !fail; ++k) {
                 unsigned char *kb = kbuf(k);
-                // ---- K dS_high^T + K dS_low^T once the dS parts are written and K landed
-                bool w = mbar_wait(bH, k & 1) && mbar_wait(cbK + (k & 1), (k >> 1) & 1);
+                // ---- K dS_high^T once the high part is written and K landed, then + K dS_low^T
+                // once the low part is (it is formed while the first product runs)
+                bool w = mbar_wait(bHi, k & 1) && mbar_wait(cbK + (k & 1), (k >> 1) & 1);
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
                 umma_gemm_w(tX, CmOp{kb, kL, 0, 0, false}, CmOp{shl, kL, 0, 0, false}, DK, idX, false, lead);
+                w = mbar_wait(bH, k & 1);
+                if (__any_sync(kFullMask, !w)) { fail = true; break; }
+                tc_fence_after();
                 umma_gemm_w(tX, CmOp{kb, kL, 0, 0, false}, CmOp{shl + kL * DK * 2, kL, 0, 0, false}, DK, idX, true, lead);
                 umma_commit_w(m1, lead);
                 // ---- dD = T^T rhs once rhs is written
@@ -403,20 +410,29 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
                 const bool w2 = mbar_wait(fS, (k - 1) & 1);
                 if (__any_sync(kFullMask, !w2)) { fail = true; break; }
             }
-            // ---- dS as operands: a bf16 high part and a bf16 low part (dS - high), each [64][DK]; the
-            // high part also leaves for the gradient kernel (a bulk store by the copy warp)
+            // ---- dS as operands: a bf16 high part and a bf16 low part (dS - high), each [64][DK],
+            // the high part first (its product starts while the low part is formed); the high part
+            // also leaves for the gradient kernel (a bulk store by the copy warp)
 #pragma unroll
             for (int j = 0; j < NS / 4; j += 2) {
-                uint32_t hi[4], lo[4];
+                uint32_t hi[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) hi[m] = pack2_bf16(dS[4 * j + 2 * m], dS[4 * j + 2 * m + 1]);
+                stmatrix_x4(frag_row_addr(smem_addr(shl), kL, 16 * (warp & 3), (DK / 16) * hw + j, lane), hi[0], hi[1],
+                            hi[2], hi[3]);
+            }
+            warp_done(bHi);
+#pragma unroll
+            for (int j = 0; j < NS / 4; j += 2) {
+                uint32_t lo[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const float x0 = dS[4 * j + 2 * m], x1 = dS[4 * j + 2 * m + 1];
-                    hi[m] = pack2_bf16(x0, x1);
-                    lo[m] = pack2_bf16(x0 - __uint_as_float(hi[m] << 16), x1 - __uint_as_float(hi[m] & 0xffff0000u));
+                    const uint32_t hi = pack2_bf16(x0, x1);
+                    lo[m] = pack2_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
                 }
-                const uint32_t a = frag_row_addr(smem_addr(shl), kL, 16 * (warp & 3), (DK / 16) * hw + j, lane);
-                stmatrix_x4(a, hi[0], hi[1], hi[2], hi[3]);
-                stmatrix_x4(a + kL * DK * 2, lo[0], lo[1], lo[2], lo[3]);
+                stmatrix_x4(frag_row_addr(smem_addr(shl), kL, 16 * (warp & 3), (DK / 16) * hw + j, lane) + kL * DK * 2,
+                            lo[0], lo[1], lo[2], lo[3]);
             }
             warp_done(bH);
             // ---- this chunk's dY and Lam
