@@ -47,10 +47,12 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:^chunk_sweep -s 3 -c 1 python bench.py --steps 1 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("c0d6d83aa3cb6a4d", "chunk_prep"): 35572224 + 91652608,
-    ("c0d6d83aa3cb6a4d", "chunk_sweep"): 160041472 + 351680512,
-    ("f4f941bbf6baa363", "chunk_dsweep"): 160389888 + 192155904,
-    ("f4f941bbf6baa363", "chunk_grad"): 333497088 + 17523456,
+    ("080b603c4c1816c2", "chunk_prep"): 35603200 + 91677952,
+    ("080b603c4c1816c2", "chunk_sweep"): 160029184 + 349472512,
+    ("c170ff145cf0856d", "chunk_dsweep"): 160440064 + 191649792,
+    ("c170ff145cf0856d", "chunk_grad"): 333473024 + 17518848,
+    # the decode-B64 workload (`-k regex:^decode`, `--workload decode-B64`)
+    ("b6d0755b616a5439", "decode"): 404523008 + 349285888,
 }
 
 
