@@ -366,7 +366,12 @@ def run_ours(args, w):
              "dS0": torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)}
     shape = gdn.make_shape(B, T, Hk, Hv, Dk, Dv, w.chunk, 1 if w.dtype == "bf16" else 0)
     P = args.segments
-    if P:
+    RC = args.recompute and not P
+    if RC:
+        def new_saved(q, v):
+            return gdn.new_rc_ckpt(q, v)
+        ws = torch.empty(gdn.gdn_rc_bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    elif P:
         # the sequence-parallel form: its own saved buffer and workspace
         def new_saved(q, v):
             return torch.empty(gdn.gdn_seg_ckpt_bytes(shape, P), dtype=torch.uint8, device=dev)
@@ -379,14 +384,18 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
 
     def fwd(d, y_, S_T_, ck):
-        if P:
+        if RC:
+            gdn.gdn_fwd_rc(d["q"], d["k"], d["v"], d["g"], d["beta"], t["S0"], y=y_, S_T=S_T_, ckpt=ck, workspace=ws)
+        elif P:
             gdn.gdn_fwd_seg(d["q"], d["k"], d["v"], d["g"], d["beta"], t["S0"], P, y=y_, S_T=S_T_, ckpt=ck,
                             workspace=ws)
         else:
             gdn.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], t["S0"], w.chunk, y=y_, S_T=S_T_, ckpt=ck)
 
     def bwd(d, ck, out):
-        if P:
+        if RC:
+            gdn.gdn_bwd_rc(d["q"], d["k"], d["v"], d["g"], d["beta"], ck, d["dy"], t["dS_T"], workspace=ws, out=out)
+        elif P:
             gdn.gdn_bwd_seg(d["q"], d["k"], d["v"], d["g"], d["beta"], ck, d["dy"], t["dS_T"], P, workspace=ws,
                             out=out)
         else:
@@ -518,7 +527,7 @@ def run_ours(args, w):
     for name, (n, ms) in ktimes.items():
         # per launch; the sequence-parallel form launches some families twice a step, and its
         # families are taken per step against the plain form's model of them
-        per = K if P else n
+        per = K if (P or RC) else n
         kernels[name] = kernel_roofline(name, ms / per, model.get(name, (0.0, 0.0, 0.0)), peaks)
         kernels[name]["launches_per_step"] = n / K
         kernels[name]["share"] = ms / sum(t for _, t in ktimes.values())
@@ -557,9 +566,11 @@ def run_ours(args, w):
                            "head at the measured FP32 rate); the chunkwise form that ran does other work, so "
                            "this is not a bound of this step"}
     NCk = -(-w.T // w.chunk)
-    memory = {"ckpt_buffer_bytes": gdn.gdn_seg_ckpt_bytes(shape, P) if P else gdn.gdn_ckpt_bytes(shape),
+    memory = {"ckpt_buffer_bytes": (gdn.gdn_rc_ckpt_bytes(shape) if RC else gdn.gdn_seg_ckpt_bytes(shape, P) if P
+                                    else gdn.gdn_ckpt_bytes(shape)),
               "ckpt_states_bytes": w.B * w.Hv * NCk * w.Dv * w.Dk * 4,
-              "bwd_workspace_bytes": gdn.gdn_seg_workspace_bytes(shape, P) if P else gdn.gdn_bwd_workspace_bytes(shape),
+              "bwd_workspace_bytes": (gdn.gdn_rc_bwd_workspace_bytes(shape) if RC else
+                                      gdn.gdn_seg_workspace_bytes(shape, P) if P else gdn.gdn_bwd_workspace_bytes(shape)),
               "peak_allocated_bytes": peak_alloc,
               "note": "peak_allocated_bytes: torch's peak device allocation over one fwd + bwd step "
                       "(inputs, outputs, saved buffer and workspace)"}
@@ -575,7 +586,11 @@ def run_ours(args, w):
         "config": {**config_of(w, l2="flushed between steps by an untimed 256 MiB write"),
                    **({"segments": P, "form": "sequence-parallel (gdn_fwd_seg / gdn_bwd_seg)",
                        "kernels_note": "per-family figures are per step, against the plain form's model"}
-                      if P else {})},
+                      if P else {}),
+                   **({"form": "re-computation (gdn_fwd_rc / gdn_bwd_rc: the saved buffer holds checkpoints "
+                               "and residuals; the backward forms the per-chunk products again)",
+                       "kernels_note": "per-family figures are per step, against the plain form's model"}
+                      if RC else {})},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "roofline": roof,
         "roofline_step": roofline_step,
@@ -704,6 +719,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--segments", type=int, default=0,
                     help="time the sequence-parallel form with this many segments (0: the plain calls)")
+    ap.add_argument("--recompute", action="store_true",
+                    help="time the re-computation mode (saved buffer: checkpoints and residuals only)")
     args = ap.parse_args()
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps

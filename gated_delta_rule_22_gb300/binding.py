@@ -16,6 +16,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "gdn.h")
 
 GDN_F32, GDN_BF16 = 0, 1
 GDN_OK = 0
+GDN_ERR_UNSUPPORTED_SHAPE = -3
 
 
 class GdnShape(ctypes.Structure):
@@ -67,6 +68,13 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_fwd_seg.argtypes = [SP, ctypes.c_int] + [_VP] * 9 + [_SZ, _VP, _SZ, _VP]
     lib.gdn_bwd_seg.restype = ctypes.c_int
     lib.gdn_bwd_seg.argtypes = [SP, ctypes.c_int] + [_VP] * 6 + [_SZ] + [_VP] * 9 + [_SZ, _VP]
+    for name in ("gdn_rc_ckpt_bytes", "gdn_rc_fwd_workspace_bytes", "gdn_rc_bwd_workspace_bytes"):
+        getattr(lib, name).restype = ctypes.c_size_t
+        getattr(lib, name).argtypes = [SP]
+    lib.gdn_fwd_rc.restype = ctypes.c_int
+    lib.gdn_fwd_rc.argtypes = [SP] + [_VP] * 9 + [_SZ, _VP, _SZ, _VP]
+    lib.gdn_bwd_rc.restype = ctypes.c_int
+    lib.gdn_bwd_rc.argtypes = [SP] + [_VP] * 6 + [_SZ] + [_VP] * 9 + [_SZ, _VP]
     lib.gdn_gates_fwd.restype = ctypes.c_int
     lib.gdn_gates_fwd.argtypes = [SP] + [_VP] * 7
     lib.gdn_gates_bwd.restype = ctypes.c_int
@@ -299,6 +307,101 @@ def gdn_seg_ckpt_bytes(shape: GdnShape, segments: int) -> int:
 
 def gdn_seg_workspace_bytes(shape: GdnShape, segments: int) -> int:
     return int(load_library().gdn_seg_workspace_bytes(ctypes.byref(shape), segments))
+
+
+def gdn_rc_ckpt_bytes(shape: GdnShape) -> int:
+    return int(load_library().gdn_rc_ckpt_bytes(ctypes.byref(shape)))
+
+
+def gdn_rc_fwd_workspace_bytes(shape: GdnShape) -> int:
+    return int(load_library().gdn_rc_fwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def gdn_rc_bwd_workspace_bytes(shape: GdnShape) -> int:
+    return int(load_library().gdn_rc_bwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def new_rc_ckpt(q, v):
+    """The saved buffer of gdn_fwd_rc for inputs shaped like q and v (gdn_rc_ckpt_bytes bytes),
+    returned as its leading [B, Hv, NC, Dv, Dk] fp32 view of chunk-start states."""
+    torch = _torch()
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    NC = -(-T // 64)
+    need = gdn_rc_ckpt_bytes(_shape_of(q, v, 64))
+    if need == 0:
+        raise GdnError("gdn_rc_ckpt_bytes", GDN_ERR_UNSUPPORTED_SHAPE, load_library())
+    buf = torch.empty(-(-need // 4), dtype=torch.float32, device=q.device)
+    return buf[: B * Hv * NC * Dv * Dk].view(B, Hv, NC, Dv, Dk)
+
+
+def _workspace(t, need, dev):
+    torch = _torch()
+    if t is None:
+        return torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if t.device != dev or not t.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {dev}")
+    return t
+
+
+def gdn_fwd_rc(q, k, v, g, beta, S0=None, *, y=None, S_T=None, ckpt=None, workspace=None, want_S_T=True,
+               stream=None):
+    """y, S_T, ckpt = gdn_fwd_rc(...): the forward of the re-computation mode (include/gdn.h):
+    ckpt holds only the chunk-start states and the residuals (new_rc_ckpt when None); the
+    per-chunk products go to `workspace` (gdn_rc_fwd_workspace_bytes, allocated here when None)."""
+    torch = _torch()
+    lib = load_library()
+    shape = _shape_of(q, v, 64)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    dev, dt = q.device, q.dtype
+    for name, t, shp in (("q", q, q.shape), ("k", k, q.shape), ("v", v, (B, T, Hv, Dv)),
+                         ("g", g, (B, T, Hv)), ("beta", beta, (B, T, Hv))):
+        _check(name, t, shp, dt, dev)
+    if S0 is not None:
+        _check("S0", S0, (B, Hv, Dv, Dk), torch.float32, dev)
+    _require_cuda(q)
+    if y is None:
+        y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
+    if S_T is None and want_S_T:
+        S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
+    if ckpt is None:
+        ckpt = new_rc_ckpt(q, v)
+    workspace = _workspace(workspace, lib.gdn_rc_fwd_workspace_bytes(ctypes.byref(shape)), dev)
+    rc = lib.gdn_fwd_rc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(y),
+                        _ptr(S_T), _ptr(ckpt), _room(ckpt), _ptr(workspace), _room(workspace), _stream(stream, dev))
+    if rc != GDN_OK:
+        raise GdnError("gdn_fwd_rc", rc, lib)
+    return y, S_T, ckpt
+
+
+def gdn_bwd_rc(q, k, v, g, beta, ckpt, dy, dS_T=None, *, workspace=None, out=None, want_dS0=True, stream=None):
+    """dict(dq, dk, dv, dg, dbeta, dS0) = gdn_bwd_rc(...): the backward of the re-computation
+    mode for the saved buffer of gdn_fwd_rc (include/gdn.h)."""
+    torch = _torch()
+    lib = load_library()
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    dev, dt = q.device, q.dtype
+    shape = _shape_of(q, v, 64)
+    for name, t, shp in (("q", q, q.shape), ("k", k, q.shape), ("v", v, (B, T, Hv, Dv)),
+                         ("g", g, (B, T, Hv)), ("beta", beta, (B, T, Hv)), ("dy", dy, (B, T, Hv, Dv))):
+        _check(name, t, shp, dt, dev)
+    if dS_T is not None:
+        _check("dS_T", dS_T, (B, Hv, Dv, Dk), torch.float32, dev)
+    _require_cuda(q)
+    if out is None:
+        out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+               "dg": torch.empty_like(g), "dbeta": torch.empty_like(beta),
+               "dS0": torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev) if want_dS0 else None}
+    workspace = _workspace(workspace, lib.gdn_rc_bwd_workspace_bytes(ctypes.byref(shape)), dev)
+    rc = lib.gdn_bwd_rc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ckpt),
+                        _room(ckpt), _ptr(dy), _ptr(dS_T), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                        _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out.get("dS0")), _ptr(workspace),
+                        _room(workspace), _stream(stream, dev))
+    if rc != GDN_OK:
+        raise GdnError("gdn_bwd_rc", rc, lib)
+    return out
 
 
 def gdn_fwd_seg(q, k, v, g, beta, S0=None, segments=2, *, y=None, S_T=None, ckpt=None, workspace=None,

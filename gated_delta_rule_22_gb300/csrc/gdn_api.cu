@@ -140,6 +140,15 @@ TcWorkspace tc_workspace_layout(const Plan &p) {
 
 size_t ckpt_total(const Plan &p) { return p.tc ? chunk_layout(p).end : ckpt_state_bytes(p) + ckpt_resid_bytes(p); }
 
+// The chunkwise form's per-chunk products (Lam onwards) of a saved buffer, and their size.
+char *chunk_products(const Plan &p, const float *ckpt) {
+    return const_cast<char *>(reinterpret_cast<const char *>(ckpt)) + chunk_layout(p).lam;
+}
+size_t chunk_products_bytes(const Plan &p) {
+    const ChunkLayout cl = chunk_layout(p);
+    return cl.end - cl.lam;
+}
+
 size_t bwd_workspace_total(const Plan &p) { return p.tcb ? tc_workspace_layout(p).total : workspace_layout(p).total; }
 
 bool aligned(const void *ptr) { return ((uintptr_t)ptr & 15u) == 0; }
@@ -421,52 +430,55 @@ size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
 // stages of launch_chunk_fwd; maps_out receives the lite stage's maps ([B][Hv][Dk][Dk], then the
 // same transposed) and S_T its end states.
 static int tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const void *g, const void *beta,
-                  const float *S0, void *y, float *S_T, float *ckpt, float *maps_out, int stages, cudaStream_t stream) {
+                  const float *S0, void *y, float *S_T, float *ckpt, char *prod, float *maps_out, int stages,
+                  cudaStream_t stream) {
     const ChunkLayout cl = chunk_layout(p);
-    char *sb = reinterpret_cast<char *>(ckpt);
     gdn::ChunkParams cp;
     cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.S0 = S0; cp.y = y; cp.S_T = S_T;
     cp.ckpt = ckpt; cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
     cp.maps_M = maps_out;
     cp.maps_Mt = maps_out != nullptr ? maps_out + (size_t)p.B * p.Hv * p.Dk * p.Dk : nullptr;
-    cp.lam = reinterpret_cast<float *>(sb + cl.lam);
-    cp.pkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.pkm);
-    cp.wm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.wm);
-    cp.tm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tm);
-    cp.tcm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.tcm);
-    cp.s0m = reinterpret_cast<__nv_bfloat16 *>(sb + cl.s0m);
-    cp.qkm = reinterpret_cast<__nv_bfloat16 *>(sb + cl.qkm);
+    cp.lam = reinterpret_cast<float *>(prod);
+    cp.pkm = reinterpret_cast<__nv_bfloat16 *>(prod + (cl.pkm - cl.lam));
+    cp.wm = reinterpret_cast<__nv_bfloat16 *>(prod + (cl.wm - cl.lam));
+    cp.tm = reinterpret_cast<__nv_bfloat16 *>(prod + (cl.tm - cl.lam));
+    cp.tcm = reinterpret_cast<__nv_bfloat16 *>(prod + (cl.tcm - cl.lam));
+    cp.s0m = reinterpret_cast<__nv_bfloat16 *>(prod + (cl.s0m - cl.lam));
+    cp.qkm = reinterpret_cast<__nv_bfloat16 *>(prod + (cl.qkm - cl.lam));
     cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC;
     g_last_error[0] = '\0';
     int rc = device_status_address(&cp.status);
     if (rc != GDN_OK) return rc;
-    gdn::ChunkFwdMaps maps;
-    if ((rc = make_btd_map(&maps.vb, v, true, p.B, p.T, p.Hv, p.Dv, 64, 64, true)) != GDN_OK ||
-        (rc = make_colblock_map(&maps.k, k, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
+    gdn::ChunkFwdMaps maps = {};
+    if ((rc = make_colblock_map(&maps.k, k, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
         (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
-        (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK ||
-        (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
-        (rc = make_colblock_map(&maps.r, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK ||
-        (rc = make_rows_map(&maps.ck, ckpt, (size_t)p.B * p.Hv * p.NC * p.Dv, p.Dk, 64)) != GDN_OK)
+        (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK)
+        return rc;
+    // the sweeps' maps (prep alone reads K and Q and writes [Q; K])
+    if ((stages & (gdn::kStageSweep | gdn::kStageLite)) &&
+        ((rc = make_btd_map(&maps.vb, v, true, p.B, p.T, p.Hv, p.Dv, 64, 64, true)) != GDN_OK ||
+         (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
+         (rc = make_colblock_map(&maps.r, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK ||
+         (rc = make_rows_map(&maps.ck, ckpt, (size_t)p.B * p.Hv * p.NC * p.Dv, p.Dk, 64)) != GDN_OK))
         return rc;
     if ((size_t)p.B * p.Hv * p.NC * p.Dv > 0x7fffffffu) return GDN_ERR_UNSUPPORTED_SHAPE;   // TMA row coordinates
     return cuda_status(gdn::launch_chunk_fwd(cp, maps, p.Dk, stream, stages));
 }
 
 // The chunkwise backward on the tensor cores for plan p: the stages of launch_chunk_bwd.
-static int tc_bwd(const Plan &p, const void *beta, const float *ckpt, const void *dy, const float *dS_T, void *dq,
-                  void *dk, void *dv, void *dg, void *dbeta, float *dS0, char *ws, int stages, cudaStream_t stream) {
+static int tc_bwd(const Plan &p, const void *beta, const float *ckpt, const char *prod, const void *dy,
+                  const float *dS_T, void *dq, void *dk, void *dv, void *dg, void *dbeta, float *dS0, char *ws,
+                  int stages, cudaStream_t stream) {
     const ChunkLayout cl = chunk_layout(p);
     const TcWorkspace tw = tc_workspace_layout(p);
-    const char *sb = reinterpret_cast<const char *>(ckpt);
     gdn::ChunkBwdParams cp;
     cp.dy = dy; cp.beta = beta;
     cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
-    cp.lam = reinterpret_cast<const float *>(sb + cl.lam);
-    cp.tm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.tm);
-    cp.pkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.pkm);
-    cp.s0m = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.s0m);
-    cp.qkm = reinterpret_cast<const __nv_bfloat16 *>(sb + cl.qkm);
+    cp.lam = reinterpret_cast<const float *>(prod);
+    cp.tm = reinterpret_cast<const __nv_bfloat16 *>(prod + (cl.tm - cl.lam));
+    cp.pkm = reinterpret_cast<const __nv_bfloat16 *>(prod + (cl.pkm - cl.lam));
+    cp.s0m = reinterpret_cast<const __nv_bfloat16 *>(prod + (cl.s0m - cl.lam));
+    cp.qkm = reinterpret_cast<const __nv_bfloat16 *>(prod + (cl.qkm - cl.lam));
     cp.dS_T = dS_T; cp.dS0 = dS0;
     cp.dv = dv; cp.dg = dg; cp.dq = dq; cp.dk = dk; cp.dbeta = dbeta;
     cp.ws_db = reinterpret_cast<float *>(ws + tw.db);
@@ -509,7 +521,8 @@ int gdn_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     rc = device_status_address(&fp.status);
     if (rc != GDN_OK) return rc;
     if (p.tc && ckpt != nullptr)       // chunkwise form on the tensor cores
-        return tc_fwd(p, q, k, v, g, beta, S0, y, S_T, ckpt, nullptr, gdn::kStagePrep | gdn::kStageSweep,
+        return tc_fwd(p, q, k, v, g, beta, S0, y, S_T, ckpt, chunk_products(p, ckpt), nullptr,
+                      gdn::kStagePrep | gdn::kStageSweep,
                       (cudaStream_t)stream);
     if (p.T == 1 && ckpt == nullptr && gdn::decode_takes(p.Dk))   // a decode step: one streaming pass
         return cuda_status(gdn::launch_decode(fp, p.Dk, p.dtype, (cudaStream_t)stream));
@@ -534,7 +547,8 @@ int gdn_bwd(const gdn_shape *shape, const void *q, const void *k, const void *v,
     if (ckpt_bytes < ckpt_total(p) || workspace_bytes < bwd_workspace_total(p)) return GDN_ERR_BUFFER_TOO_SMALL;
     char *ws = static_cast<char *>(workspace);
     if (p.tcb)                         // chunkwise form on the tensor cores, reading the chunkwise forward's saved buffer
-        return tc_bwd(p, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, gdn::kStageDsweep | gdn::kStageGrad,
+        return tc_bwd(p, beta, ckpt, chunk_products(p, ckpt), dy, dS_T, dq, dk, dv, dg, dbeta, dS0, ws,
+                      gdn::kStageDsweep | gdn::kStageGrad,
                       (cudaStream_t)stream);
     const Workspace w = workspace_layout(p);
 
@@ -627,13 +641,14 @@ int gdn_fwd_seg(const gdn_shape *shape, int segments, const void *q, const void 
     float *X = reinterpret_cast<float *>(static_cast<char *>(workspace) + seg_state_bytes(pv));
     // every segment from a zero state (its end state: C) and as maps (the lite sweep), then the
     // scan of the start states, then every segment again from its start state
-    rc = tc_fwd(pv, q, k, v, g, beta, nullptr, y, C, ckpt, maps, gdn::kStagePrep | gdn::kStageLite, st);
+    rc = tc_fwd(pv, q, k, v, g, beta, nullptr, y, C, ckpt, chunk_products(pv, ckpt), maps, gdn::kStagePrep | gdn::kStageLite,
+                st);
     if (rc != GDN_OK) return rc;
     int *status = nullptr;
     if ((rc = device_status_address(&status)) != GDN_OK) return rc;
     rc = cuda_status(gdn::launch_segment_scan(S0, maps, C, X, p.B, segments, p.Hv, p.Dv, p.Dk, false, status, st));
     if (rc != GDN_OK) return rc;
-    rc = tc_fwd(pv, q, k, v, g, beta, X, y, C, ckpt, nullptr, gdn::kStageSweep, st);
+    rc = tc_fwd(pv, q, k, v, g, beta, X, y, C, ckpt, chunk_products(pv, ckpt), nullptr, gdn::kStageSweep, st);
     if (rc != GDN_OK || S_T == nullptr) return rc;
     return seg_pick(S_T, C, (size_t)p.Hv * p.Dv * p.Dk * 4, p.B, segments, segments - 1, st);
 }
@@ -660,16 +675,89 @@ int gdn_bwd_seg(const gdn_shape *shape, int segments, const void *q, const void 
     char *ws = static_cast<char *>(workspace) + 2 * seg_state_bytes(pv);
     // every segment's reverse sweep from a zero end adjoint (its start adjoint: D), the reverse
     // scan of the end adjoints, then the backward proper from them
-    rc = tc_bwd(pv, beta, ckpt, dy, nullptr, dq, dk, dv, dg, dbeta, D, ws, gdn::kStageDsweep, st);
+    rc = tc_bwd(pv, beta, ckpt, chunk_products(pv, ckpt), dy, nullptr, dq, dk, dv, dg, dbeta, D, ws, gdn::kStageDsweep, st);
     if (rc != GDN_OK) return rc;
     int *status = nullptr;
     if ((rc = device_status_address(&status)) != GDN_OK) return rc;
     const float *maps_t = maps + (size_t)pv.B * pv.Hv * pv.Dk * pv.Dk;
     rc = cuda_status(gdn::launch_segment_scan(dS_T, maps_t, D, Y, p.B, segments, p.Hv, p.Dv, p.Dk, true, status, st));
     if (rc != GDN_OK) return rc;
-    rc = tc_bwd(pv, beta, ckpt, dy, Y, dq, dk, dv, dg, dbeta, D, ws, gdn::kStageDsweep | gdn::kStageGrad, st);
+    rc = tc_bwd(pv, beta, ckpt, chunk_products(pv, ckpt), dy, Y, dq, dk, dv, dg, dbeta, D, ws,
+                gdn::kStageDsweep | gdn::kStageGrad, st);
     if (rc != GDN_OK || dS0 == nullptr) return rc;
     return seg_pick(dS0, D, (size_t)p.Hv * p.Dv * p.Dk * 4, p.B, segments, 0, st);
+}
+
+// ---- re-computation mode: the saved buffer holds only the checkpoints and the residuals
+static int rc_plan(const gdn_shape *shape, Plan *p) {
+    if (shape == nullptr) return GDN_ERR_INVALID_ARG;
+    const int rc = make_plan(shape, p);
+    if (rc != GDN_OK) return rc;
+    return p->tc && p->tcb ? GDN_OK : GDN_ERR_UNSUPPORTED_SHAPE;
+}
+
+size_t gdn_rc_ckpt_bytes(const gdn_shape *shape) {
+    Plan p;
+    if (rc_plan(shape, &p) != GDN_OK) return 0;
+    return ckpt_state_bytes(p) + round_up(ckpt_resid_bytes(p));
+}
+
+size_t gdn_rc_fwd_workspace_bytes(const gdn_shape *shape) {
+    Plan p;
+    if (rc_plan(shape, &p) != GDN_OK) return 0;
+    return round_up(chunk_products_bytes(p));
+}
+
+size_t gdn_rc_bwd_workspace_bytes(const gdn_shape *shape) {
+    Plan p;
+    if (rc_plan(shape, &p) != GDN_OK) return 0;
+    return round_up(chunk_products_bytes(p)) + bwd_workspace_total(p);
+}
+
+int gdn_fwd_rc(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g, const void *beta,
+               const float *S0, void *y, float *S_T, float *ckpt, size_t ckpt_bytes, void *workspace,
+               size_t workspace_bytes, void *stream) {
+    Plan p;
+    int rc = rc_plan(shape, &p);
+    if (rc != GDN_OK) return rc;
+    if (!q || !k || !v || !g || !beta || !y || !ckpt || !workspace) return GDN_ERR_INVALID_ARG;
+    const void *all[] = {q, k, v, g, beta, S0, y, S_T, ckpt, workspace};
+    for (const void *ptr : all)
+        if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    if (ckpt_bytes < gdn_rc_ckpt_bytes(shape) || workspace_bytes < gdn_rc_fwd_workspace_bytes(shape))
+        return GDN_ERR_BUFFER_TOO_SMALL;
+    // the chunkwise forward with its per-chunk products in the workspace (dropped afterwards)
+    return tc_fwd(p, q, k, v, g, beta, S0, y, S_T, ckpt, static_cast<char *>(workspace), nullptr,
+                  gdn::kStagePrep | gdn::kStageSweep, (cudaStream_t)stream);
+}
+
+int gdn_bwd_rc(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g, const void *beta,
+               const float *ckpt, size_t ckpt_bytes, const void *dy, const float *dS_T, void *dq, void *dk, void *dv,
+               void *dg, void *dbeta, float *dS0, void *workspace, size_t workspace_bytes, void *stream) {
+    Plan p;
+    int rc = rc_plan(shape, &p);
+    if (rc != GDN_OK) return rc;
+    if (!q || !k || !v || !g || !beta || !ckpt || !dy || !dq || !dk || !dv || !dg || !dbeta || !workspace)
+        return GDN_ERR_INVALID_ARG;
+    const void *all[] = {q, k, v, g, beta, ckpt, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace};
+    for (const void *ptr : all)
+        if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    if (ckpt_bytes < gdn_rc_ckpt_bytes(shape) || workspace_bytes < gdn_rc_bwd_workspace_bytes(shape))
+        return GDN_ERR_BUFFER_TOO_SMALL;
+    const cudaStream_t st = (cudaStream_t)stream;
+    char *prod = static_cast<char *>(workspace);
+    char *ws = prod + round_up(chunk_products_bytes(p));
+    // every chunk's forward products again (prep), the checkpoints as the gradient kernel's bf16
+    // operands, then the backward proper
+    rc = tc_fwd(p, q, k, v, g, beta, nullptr, nullptr, nullptr, const_cast<float *>(ckpt), prod, nullptr,
+                gdn::kStagePrep, st);
+    if (rc != GDN_OK) return rc;
+    const ChunkLayout cl = chunk_layout(p);
+    rc = cuda_status(gdn::launch_state_operands(ckpt, reinterpret_cast<__nv_bfloat16 *>(prod + (cl.s0m - cl.lam)),
+                                                (size_t)p.B * p.Hv * p.NC * (p.Dv / 64), p.Dk, st));
+    if (rc != GDN_OK) return rc;
+    return tc_bwd(p, beta, ckpt, prod, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, gdn::kStageDsweep | gdn::kStageGrad,
+                  st);
 }
 
 int gdn_gates_fwd(const gdn_shape *shape, const void *a, const void *b, const float *A_log,

@@ -216,6 +216,35 @@ GDN_API int gdn_bwd_seg(const gdn_shape *shape, int segments, const void *q, con
                         void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Re-computation mode (mlx-lm PR #1217, "What this PR adds": checkpoints on fixed-size chunks,
+ * the forward recomputed within each chunk during the reverse sweep). For a shape the
+ * chunkwise tensor-core kernels take both ways (bf16, chunk 64; else
+ * GDN_ERR_UNSUPPORTED_SHAPE), the saved buffer holds only what the method saves -- the fp32
+ * chunk-start states and the residuals v_t - u_t, the layout gdn_fwd describes, without the
+ * chunkwise form's per-chunk products -- and gdn_bwd_rc forms those products again from q, k,
+ * g, beta (and the checkpoints' bf16 operand copies) before its reverse sweep. Results equal
+ * those of gdn_fwd / gdn_bwd bit for bit.
+ *   ckpt       gdn_rc_ckpt_bytes(shape) bytes: [B,Hv,NC,Dv,Dk] fp32 states, then from the next
+ *              256-byte boundary [B,T,Hv,Dv] fp32 residuals.
+ *   workspace  gdn_rc_fwd_workspace_bytes / gdn_rc_bwd_workspace_bytes bytes (device, 16-byte
+ *              aligned, contents on entry do not matter): the per-chunk products, and for the
+ *              backward then its own workspace. Two calls that overlap on the GPU must not
+ *              share one.
+ * Other arguments as for gdn_fwd / gdn_bwd (S0, S_T, dS_T, dS0 may be NULL). Returns GDN_OK or an
+ * error code; a size query returns 0 for a shape it does not take.
+ */
+GDN_API size_t gdn_rc_ckpt_bytes(const gdn_shape *shape);
+GDN_API size_t gdn_rc_fwd_workspace_bytes(const gdn_shape *shape);
+GDN_API size_t gdn_rc_bwd_workspace_bytes(const gdn_shape *shape);
+GDN_API int gdn_fwd_rc(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
+                       const void *beta, const float *S0, void *y, float *S_T, float *ckpt, size_t ckpt_bytes,
+                       void *workspace, size_t workspace_bytes, void *stream);
+GDN_API int gdn_bwd_rc(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
+                       const void *beta, const float *ckpt, size_t ckpt_bytes, const void *dy, const float *dS_T,
+                       void *dq, void *dk, void *dv, void *dg, void *dbeta, float *dS0, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
  * Gates of the layer: the decay g and write strength beta from its raw gate inputs, and the
  * VJP back to them (mlx-lm PR #1217, "Correctness", trains through q, k, v, a, b, A_log,
  * dt_bias and the state; no page prints the gate map, and the one taken is the public
