@@ -431,12 +431,13 @@ size_t gdn_bwd_workspace_bytes(const gdn_shape *shape) {
 // same transposed) and S_T its end states.
 static int tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const void *g, const void *beta,
                   const float *S0, void *y, float *S_T, float *ckpt, char *prod, float *maps_out, int stages,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const float *conv = nullptr) {
     const ChunkLayout cl = chunk_layout(p);
     gdn::ChunkParams cp;
     cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.S0 = S0; cp.y = y; cp.S_T = S_T;
     cp.ckpt = ckpt; cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
     cp.maps_M = maps_out;
+    cp.conv = conv;
     cp.maps_Mt = maps_out != nullptr ? maps_out + (size_t)p.B * p.Hv * p.Dk * p.Dk : nullptr;
     cp.lam = reinterpret_cast<float *>(prod);
     cp.pkm = reinterpret_cast<__nv_bfloat16 *>(prod + (cl.pkm - cl.lam));
@@ -747,14 +748,10 @@ int gdn_bwd_rc(const gdn_shape *shape, const void *q, const void *k, const void 
     const cudaStream_t st = (cudaStream_t)stream;
     char *prod = static_cast<char *>(workspace);
     char *ws = prod + round_up(chunk_products_bytes(p));
-    // every chunk's forward products again (prep), the checkpoints as the gradient kernel's bf16
-    // operands, then the backward proper
+    // every chunk's forward products again (prep, which also turns the checkpoints into the
+    // gradient kernel's bf16 operand tiles), then the backward proper
     rc = tc_fwd(p, q, k, v, g, beta, nullptr, nullptr, nullptr, const_cast<float *>(ckpt), prod, nullptr,
-                gdn::kStagePrep, st);
-    if (rc != GDN_OK) return rc;
-    const ChunkLayout cl = chunk_layout(p);
-    rc = cuda_status(gdn::launch_state_operands(ckpt, reinterpret_cast<__nv_bfloat16 *>(prod + (cl.s0m - cl.lam)),
-                                                (size_t)p.B * p.Hv * p.NC * (p.Dv / 64), p.Dk, st));
+                gdn::kStagePrep, st, ckpt);
     if (rc != GDN_OK) return rc;
     return tc_bwd(p, beta, ckpt, prod, dy, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, gdn::kStageDsweep | gdn::kStageGrad,
                   st);

@@ -273,6 +273,23 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(ChunkParams p, int u
             umma_gemm_w(tmem + kL, CmOp{qc, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, false}, DK, id, false, lead);
             umma_commit_w(bar, lead);
         }
+        // the re-computation backward: this unit's checkpoint rows as the gradient kernel's bf16
+        // operand tiles while the products run (block of 64 rows s: element (r, c) at
+        // s * 64 * DK + (c / 8) * 512 + r * 8 + c % 8; a warp writes 512 contiguous bytes)
+        if (p.conv != nullptr && warp > 0) {
+            const float *src = p.conv + chk * p.Dv * DK;
+            __nv_bfloat16 *dst = p.s0m + chk * p.Dv * DK;
+            const int per_blk = kL * (DK / 8), items = (p.Dv / kL) * per_blk;
+#pragma unroll 4
+            for (int it = tid - 32; it < items; it += 224) {
+                const int blk = it / per_blk, w = it - blk * per_blk, ch = w / kL, row = w - ch * kL;
+                const float *sp = src + (size_t)(blk * kL + row) * DK + 8 * ch;
+                const float4 a = __ldcs(reinterpret_cast<const float4 *>(sp));
+                const float4 b2 = __ldcs(reinterpret_cast<const float4 *>(sp + 4));
+                const float x8[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+                *reinterpret_cast<uint4 *>(dst + (size_t)blk * kL * DK + ch * (kL * 8) + row * 8) = pack8_bf16(x8);
+            }
+        }
         // log g, beta and the in-chunk prefix Lam (warp 0: two steps per lane, a shuffle scan)
         if (warp == 0) {
             float l2[2], b2[2];
@@ -367,8 +384,10 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(ChunkParams p, int u
                     w8[j] = u8[j] * gm[col];
                 }
                 const uint32_t o = cm_off(t, 16 * ch, kL);
-                *reinterpret_cast<uint4 *>(tcw + o) = pack8_bf16(w8);
-                *reinterpret_cast<uint4 *>(tcu + o) = pack8_bf16(u8);
+                if (p.conv == nullptr) {
+                    *reinterpret_cast<uint4 *>(tcw + o) = pack8_bf16(w8);
+                    *reinterpret_cast<uint4 *>(tcu + o) = pack8_bf16(u8);
+                }
                 *reinterpret_cast<uint4 *>(Tg + o) = pack8_bf16(x8);
             }
         }
@@ -376,6 +395,17 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(ChunkParams p, int u
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        const bool kq_next = u + 1 < u_end && (u + 1) / rep != u / rep;
+        if (p.conv != nullptr) {
+            // the re-computation backward needs neither W nor T diag(beta); K and Q are free
+            // (their products are done) once the stores of [Q; K] have read them
+            if (tid == 32 && kq_next) bulk_wait_read();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (kq_next) fetch_kq(unit_of(u + 1));
+            continue;
+        }
         // W -> columns [0, DK) (K K^T and Q K^T are dead); T diag(beta) leaves by a bulk store
         if (warp == 0) {
             umma_gemm_w(tmem, CmOp{tcw, kL, 0, 0, false}, CmOp{kc, kL, 0, 0, true}, kL,
@@ -384,7 +414,6 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(ChunkParams p, int u
         }
         // when the next unit starts another group, its K and Q are fetched into kc and qc
         // (free once this product is done) while this unit's W is read back
-        const bool kq_next = u + 1 < u_end && (u + 1) / rep != u / rep;
         if (tid == 32) {
             bulk_store(p.tcm + chk * kL * kL, tcu, kL * kL * 2);
             bulk_commit();

@@ -67,31 +67,6 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float *x) {
 // than half of the shared memory.
 constexpr size_t kOneCtaSmem = 120 * 1024;
 
-// ------------------------------------------------------------------ chunk-start states as operands
-// The fp32 chunk-start states of a saved buffer (the checkpoints, [B][Hv][NC][Dv][Dk]) as the
-// bf16 operand tiles the gradient kernel reads -- what the forward sweep stores beside them when
-// the forward's products are kept: per 64-row block (b, h, chunk, block of value rows) a [64][Dk]
-// tile in the core-matrix layout, element (r, c) at (c / 8) * 512 + r * 8 + c % 8, rounded to
-// nearest even like the sweep's own copy. A warp takes 32 consecutive rows of one 8-column
-// chunk: each lane reads its row's 32 bytes (whole sectors) and the warp writes 512 contiguous
-// bytes.
-__global__ void __launch_bounds__(256) state_operands_kernel(const float *__restrict__ ckpt,
-                                                             __nv_bfloat16 *__restrict__ s0m, int Dk) {
-    const size_t blk = blockIdx.x;
-    const float *src = ckpt + blk * kL * Dk;
-    __nv_bfloat16 *dst = s0m + blk * kL * Dk;
-    griddep_wait();
-    griddep_launch();
-    for (int it = threadIdx.x; it < kL * (Dk / 8); it += 256) {
-        const int row = it & (kL - 1), ch = it / kL;
-        float x[8];
-        const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + row * Dk + 8 * ch));
-        const float4 b = __ldcs(reinterpret_cast<const float4 *>(src + row * Dk + 8 * ch + 4));
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-        *reinterpret_cast<uint4 *>(dst + ch * (kL * 8) + row * 8) = pack8(x);
-    }
-}
-
 // ------------------------------------------------------------------ reverse sweep (dS)
 constexpr int kSweepMathWarps = 8;      // hold dS (M = 64 fragment: 4 lane quarters x 2 column halves)
 constexpr int kSweepThreads = 384;      // + a warpgroup: warp 8 issues the products, warp 9 the copies and stores
@@ -1126,15 +1101,6 @@ cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, 
         case 192: return launch_chunk_bwd_t<6>(p, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, s, stages);
         default: return cudaErrorInvalidValue;
     }
-}
-
-cudaError_t launch_state_operands(const float *ckpt, __nv_bfloat16 *s0m, size_t blocks, int Dk, cudaStream_t s) {
-    if (blocks == 0) return cudaSuccess;
-    if (blocks > 0x7fffffffu || Dk % 8 != 0) return cudaErrorInvalidValue;
-    timing_mark("state_operands", 0, s);
-    cudaError_t err = launch_pdl(state_operands_kernel, dim3((unsigned)blocks), dim3(256), 0, s, ckpt, s0m, Dk);
-    timing_mark("state_operands", 1, s);
-    return err;
 }
 
 }  // namespace gdn

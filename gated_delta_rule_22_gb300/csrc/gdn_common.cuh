@@ -83,6 +83,8 @@ struct ChunkParams {
     void *y;
     float *S_T, *ckpt, *resid;
     float *maps_M, *maps_Mt;   // the lite sweep's maps and their transposes ([B][Hv][Dk][Dk] each)
+    const float *conv;         // prep in the re-computation backward: these fp32 checkpoints go to
+                               // s0m as operand tiles, and W and T diag(beta) are not formed (else null)
     float *lam;
     __nv_bfloat16 *pkm, *wm, *tm, *tcm, *s0m, *qkm;
     int *status;
@@ -523,9 +525,6 @@ constexpr int kStageDsweep = 1, kStageGrad = 2;
 cudaError_t launch_chunk_bwd(const ChunkBwdParams &p, const CUtensorMap &tm_dv, const CUtensorMap &tm_dy,
                              const CUtensorMap &tm_qk, const CUtensorMap &tm_pk, const CUtensorMap &tm_dq,
                              const CUtensorMap &tm_dk, int Dk, cudaStream_t s, int stages = kStageDsweep | kStageGrad);
-// The fp32 chunk-start states of a saved buffer as the gradient kernel's bf16 operand tiles
-// (`blocks` = B * Hv * NC * Dv / 64 blocks of 64 rows; gdn_chunk_bwd.cu).
-cudaError_t launch_state_operands(const float *ckpt, __nv_bfloat16 *s0m, size_t blocks, int Dk, cudaStream_t s);
 // The scan over segments of the sequence-parallel form: forward X_0 = X0 (zero if null),
 // X_s = X_{s-1} M_{s-1} + C_{s-1}; reverse X_{P-1} = X0, X_s = X_{s+1} M_{s+1}^T + C_{s+1}. X, C:
 // [B*P][Hv][rows][Dk] fp32 (rows a multiple of 64), X0: [B][Hv][rows][Dk]. M: [B*P][Hv][Dk][Dk]
