@@ -47,12 +47,12 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:^chunk_sweep -s 3 -c 1 python bench.py --steps 1 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("080b603c4c1816c2", "chunk_prep"): 35603200 + 91677952,
-    ("080b603c4c1816c2", "chunk_sweep"): 160029184 + 349472512,
-    ("c170ff145cf0856d", "chunk_dsweep"): 160440064 + 191649792,
-    ("c170ff145cf0856d", "chunk_grad"): 333473024 + 17518848,
+    ("ecb6c934c2475ab2", "chunk_prep"): 35597312 + 92107776,
+    ("ecb6c934c2475ab2", "chunk_sweep"): 160100096 + 349601280,
+    ("cb5dffa187b2cde5", "chunk_dsweep"): 160413696 + 191879936,
+    ("cb5dffa187b2cde5", "chunk_grad"): 333471232 + 17644032,
     # the decode-B64 workload (`-k regex:^decode`, `--workload decode-B64`)
-    ("b6d0755b616a5439", "decode"): 404523008 + 349285888,
+    ("45ae3085db5ac2ab", "decode"): 404603904 + 348921856,
 }
 
 
