@@ -365,7 +365,11 @@ def run_ours(args, w):
              "dg": torch.empty_like(t["g"]), "dbeta": torch.empty_like(t["beta"]),
              "dS0": torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)}
     shape = gdn.make_shape(B, T, Hk, Hv, Dk, Dv, w.chunk, 1 if w.dtype == "bf16" else 0)
-    P = args.segments
+    if args.segments == "auto":
+        P = gdn.gdn_seg_choose(shape, torch.cuda.get_device_properties(dev).multi_processor_count)
+        P = 0 if P <= 1 else P
+    else:
+        P = int(args.segments)
     RC = args.recompute and not P
     if RC:
         def new_saved(q, v):
@@ -717,8 +721,9 @@ def main():
     ap.add_argument("--workload", default="linattn-T2048", choices=sorted(gs.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--segments", type=int, default=0,
-                    help="time the sequence-parallel form with this many segments (0: the plain calls)")
+    ap.add_argument("--segments", default="0",
+                    help="time the sequence-parallel form with this many segments (0: the plain calls; "
+                         "auto: the count gdn_seg_choose gives for this GPU)")
     ap.add_argument("--recompute", action="store_true",
                     help="time the re-computation mode (saved buffer: checkpoints and residuals only)")
     args = ap.parse_args()

@@ -60,6 +60,8 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_bwd.argtypes = [SP] + [_VP] * 6 + [_SZ] + [_VP] * 9 + [_SZ, _VP]
     lib.gdn_bwd_noalloc.restype = ctypes.c_int
     lib.gdn_bwd_noalloc.argtypes = [SP] + [_VP] * 6 + [_SZ] + [_VP] * 9
+    lib.gdn_seg_choose.restype = ctypes.c_int
+    lib.gdn_seg_choose.argtypes = [SP, ctypes.c_int]
     lib.gdn_seg_ckpt_bytes.restype = ctypes.c_size_t
     lib.gdn_seg_ckpt_bytes.argtypes = [SP, ctypes.c_int]
     lib.gdn_seg_workspace_bytes.restype = ctypes.c_size_t
@@ -299,6 +301,10 @@ def gdn_bwd(q, k, v, g, beta, ckpt, dy, dS_T=None, chunk=64, *, workspace=None, 
     if rc != GDN_OK:
         raise GdnError("gdn_bwd", rc, lib)
     return out
+
+
+def gdn_seg_choose(shape: GdnShape, sm_count: int) -> int:
+    return int(load_library().gdn_seg_choose(ctypes.byref(shape), sm_count))
 
 
 def gdn_seg_ckpt_bytes(shape: GdnShape, segments: int) -> int:

@@ -612,6 +612,16 @@ size_t gdn_seg_workspace_bytes(const gdn_shape *shape, int segments) {
     return 2 * seg_state_bytes(pv) + bwd_workspace_total(pv);
 }
 
+int gdn_seg_choose(const gdn_shape *shape, int sm_count) {
+    Plan p;
+    if (shape == nullptr || make_plan(shape, &p) != GDN_OK || !p.tc || !p.tcb || sm_count < 1) return 1;
+    // the sweep's grid for P segments: (Dv / 64) * Hv * B * P CTAs, one per SM
+    const long long base = (long long)(p.Dv / 64) * p.Hv * p.B;
+    int P = 1;
+    while (base * 2 * P <= sm_count && p.T % (64 * 2 * P) == 0 && P < (1 << 20)) P *= 2;
+    return P;
+}
+
 // dst[b] = src[b * P + s] for every b: blocks of `blk` bytes, one copy per batch row
 static int seg_pick(void *dst, const void *src, size_t blk, int B, int P, int s, cudaStream_t stream) {
     for (int b = 0; b < B; ++b) {

@@ -205,6 +205,11 @@ GDN_API int gdn_bwd_noalloc(const gdn_shape *shape, const void *q, const void *k
  * Other arguments as for gdn_fwd / gdn_bwd (S0, S_T, dS_T, dS0 may be NULL). Returns GDN_OK or an
  * error code; a size query returns 0 for a shape or segment count it does not take.
  */
+/* The segment count for a GPU of `sm_count` SMs: the largest power of two P (T a multiple of
+ * 64 P) whose sweeps' grid, (Dv / 64) * Hv * B * P CTAs of one SM each, still fits the GPU;
+ * 1 (the plain calls) where the plain sweeps already fill it or the shape is not taken.
+ * Host logic only. */
+GDN_API int gdn_seg_choose(const gdn_shape *shape, int sm_count);
 GDN_API size_t gdn_seg_ckpt_bytes(const gdn_shape *shape, int segments);
 GDN_API size_t gdn_seg_workspace_bytes(const gdn_shape *shape, int segments);
 GDN_API int gdn_fwd_seg(const gdn_shape *shape, int segments, const void *q, const void *k, const void *v,

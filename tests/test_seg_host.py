@@ -98,3 +98,22 @@ def test_argument_checks(lib):
     assert seg_fwd(lib, s, P, y=None) == INVALID
     assert seg_bwd(lib, s, P, dy=None) == INVALID
     assert lib.gdn_fwd_seg(None, P, *([None] * 9), 0, None, 0, None) == INVALID
+
+
+def test_segment_count_fills_the_gpu(lib):
+    """The chosen count fills 152 SMs with the sweeps' grid and no more: the long workload's
+    8-way head split takes 8 segments, a 4-head Dk = Dv = 128 case 16, and the layer with all 64
+    value heads (128 sweep CTAs already) none."""
+    tp8 = B.GdnShape(B=1, T=32768, Hk=2, Hv=8, Dk=192, Dv=128, chunk=64, dtype=1)
+    h4 = B.GdnShape(B=1, T=32768, Hk=4, Hv=4, Dk=128, Dv=128, chunk=64, dtype=1)
+    full = B.GdnShape(B=1, T=32768, Hk=16, Hv=64, Dk=192, Dv=128, chunk=64, dtype=1)
+    assert lib.gdn_seg_choose(ctypes.byref(tp8), 152) == 8
+    assert lib.gdn_seg_choose(ctypes.byref(h4), 152) == 16
+    assert lib.gdn_seg_choose(ctypes.byref(full), 152) == 1
+    # T limits the count: 128 steps hold two chunks
+    short = B.GdnShape(B=1, T=128, Hk=2, Hv=8, Dk=192, Dv=128, chunk=64, dtype=1)
+    assert lib.gdn_seg_choose(ctypes.byref(short), 152) == 2
+    # shapes the tensor-core kernels do not take, and nonsense SM counts: the plain calls
+    assert lib.gdn_seg_choose(ctypes.byref(shape(dtype=0)), 152) == 1
+    assert lib.gdn_seg_choose(ctypes.byref(tp8), 0) == 1
+    assert lib.gdn_seg_choose(None, 152) == 1
