@@ -47,12 +47,12 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:^chunk_sweep -s 3 -c 1 python bench.py --steps 1 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("ecb6c934c2475ab2", "chunk_prep"): 35597312 + 92107776,
-    ("ecb6c934c2475ab2", "chunk_sweep"): 160100096 + 349601280,
-    ("cb5dffa187b2cde5", "chunk_dsweep"): 160413696 + 191879936,
-    ("cb5dffa187b2cde5", "chunk_grad"): 333471232 + 17644032,
+    ("6b6e0cef09561d11", "chunk_prep"): 35600384 + 91748096,
+    ("6b6e0cef09561d11", "chunk_sweep"): 160040192 + 349540352,
+    ("16d0e1b944d60de2", "chunk_dsweep"): 160416512 + 192061184,
+    ("16d0e1b944d60de2", "chunk_grad"): 333489152 + 17624064,
     # the decode-B64 workload (`-k regex:^decode`, `--workload decode-B64`)
-    ("45ae3085db5ac2ab", "decode"): 404603904 + 348921856,
+    ("813e00840969e5b0", "decode"): 404530688 + 349271552,
 }
 
 
