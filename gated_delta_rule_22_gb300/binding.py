@@ -70,6 +70,10 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_fwd_seg.argtypes = [SP, ctypes.c_int] + [_VP] * 9 + [_SZ, _VP, _SZ, _VP]
     lib.gdn_bwd_seg.restype = ctypes.c_int
     lib.gdn_bwd_seg.argtypes = [SP, ctypes.c_int] + [_VP] * 6 + [_SZ] + [_VP] * 9 + [_SZ, _VP]
+    lib.gdn_infer_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_infer_workspace_bytes.argtypes = [SP]
+    lib.gdn_fwd_infer.restype = ctypes.c_int
+    lib.gdn_fwd_infer.argtypes = [SP] + [_VP] * 9 + [_SZ, _VP]
     for name in ("gdn_rc_ckpt_bytes", "gdn_rc_fwd_workspace_bytes", "gdn_rc_bwd_workspace_bytes"):
         getattr(lib, name).restype = ctypes.c_size_t
         getattr(lib, name).argtypes = [SP]
@@ -313,6 +317,38 @@ def gdn_seg_ckpt_bytes(shape: GdnShape, segments: int) -> int:
 
 def gdn_seg_workspace_bytes(shape: GdnShape, segments: int) -> int:
     return int(load_library().gdn_seg_workspace_bytes(ctypes.byref(shape), segments))
+
+
+def gdn_infer_workspace_bytes(shape: GdnShape) -> int:
+    return int(load_library().gdn_infer_workspace_bytes(ctypes.byref(shape)))
+
+
+def gdn_fwd_infer(q, k, v, g, beta, S0=None, *, y=None, S_T=None, workspace=None, want_S_T=True, stream=None):
+    """y, S_T = gdn_fwd_infer(q, k, v, g, beta[, S0]): the inference forward on the tensor cores
+    (include/gdn.h): nothing saved; the per-chunk products go to `workspace`
+    (gdn_infer_workspace_bytes, allocated here when None)."""
+    torch = _torch()
+    lib = load_library()
+    shape = _shape_of(q, v, 64)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    dev, dt = q.device, q.dtype
+    for name, t, shp in (("q", q, q.shape), ("k", k, q.shape), ("v", v, (B, T, Hv, Dv)),
+                         ("g", g, (B, T, Hv)), ("beta", beta, (B, T, Hv))):
+        _check(name, t, shp, dt, dev)
+    if S0 is not None:
+        _check("S0", S0, (B, Hv, Dv, Dk), torch.float32, dev)
+    _require_cuda(q)
+    if y is None:
+        y = torch.empty((B, T, Hv, Dv), dtype=dt, device=dev)
+    if S_T is None and want_S_T:
+        S_T = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
+    workspace = _workspace(workspace, lib.gdn_infer_workspace_bytes(ctypes.byref(shape)), dev)
+    rc = lib.gdn_fwd_infer(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(y),
+                           _ptr(S_T), _ptr(workspace), _room(workspace), _stream(stream, dev))
+    if rc != GDN_OK:
+        raise GdnError("gdn_fwd_infer", rc, lib)
+    return y, S_T
 
 
 def gdn_rc_ckpt_bytes(shape: GdnShape) -> int:

@@ -435,7 +435,7 @@ static int tc_fwd(const Plan &p, const void *q, const void *k, const void *v, co
     const ChunkLayout cl = chunk_layout(p);
     gdn::ChunkParams cp;
     cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.S0 = S0; cp.y = y; cp.S_T = S_T;
-    cp.ckpt = ckpt; cp.resid = ckpt + ckpt_state_bytes(p) / sizeof(float);
+    cp.ckpt = ckpt; cp.resid = ckpt != nullptr ? ckpt + ckpt_state_bytes(p) / sizeof(float) : nullptr;
     cp.maps_M = maps_out;
     cp.conv = conv;
     cp.maps_Mt = maps_out != nullptr ? maps_out + (size_t)p.B * p.Hv * p.Dk * p.Dk : nullptr;
@@ -455,11 +455,14 @@ static int tc_fwd(const Plan &p, const void *q, const void *k, const void *v, co
         (rc = make_colblock_map(&maps.q, q, true, p.B, p.T, p.Hk, p.Dk, 8, 64, p.Dk / 8, false)) != GDN_OK ||
         (rc = make_qkm_map(&maps.qk, cp.qkm, (size_t)p.B * p.Hk * p.NC, p.Dk)) != GDN_OK)
         return rc;
-    // the sweeps' maps (prep alone reads K and Q and writes [Q; K])
+    // the sweeps' maps (prep alone reads K and Q and writes [Q; K]); without a saved buffer (an
+    // inference forward) nothing goes to the residual or checkpoint maps
     if ((stages & (gdn::kStageSweep | gdn::kStageLite)) &&
         ((rc = make_btd_map(&maps.vb, v, true, p.B, p.T, p.Hv, p.Dv, 64, 64, true)) != GDN_OK ||
-         (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK ||
-         (rc = make_colblock_map(&maps.r, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK ||
+         (rc = make_btd_map(&maps.y, y, true, p.B, p.T, p.Hv, p.Dv, 64, 64)) != GDN_OK))
+        return rc;
+    if ((stages & (gdn::kStageSweep | gdn::kStageLite)) && ckpt != nullptr &&
+        ((rc = make_colblock_map(&maps.r, cp.resid, false, p.B, p.T, p.Hv, p.Dv, 32, 64, 2, true)) != GDN_OK ||
          (rc = make_rows_map(&maps.ck, ckpt, (size_t)p.B * p.Hv * p.NC * p.Dv, p.Dk, 64)) != GDN_OK))
         return rc;
     if ((size_t)p.B * p.Hv * p.NC * p.Dv > 0x7fffffffu) return GDN_ERR_UNSUPPORTED_SHAPE;   // TMA row coordinates
@@ -697,6 +700,30 @@ int gdn_bwd_seg(const gdn_shape *shape, int segments, const void *q, const void 
                 gdn::kStageDsweep | gdn::kStageGrad, st);
     if (rc != GDN_OK || dS0 == nullptr) return rc;
     return seg_pick(dS0, D, (size_t)p.Hv * p.Dv * p.Dk * 4, p.B, segments, 0, st);
+}
+
+// ---- inference forward on the tensor cores: the per-chunk products in a workspace, nothing saved
+size_t gdn_infer_workspace_bytes(const gdn_shape *shape) {
+    Plan p;
+    if (shape == nullptr || make_plan(shape, &p) != GDN_OK || !p.tc) return 0;
+    return round_up(chunk_products_bytes(p));
+}
+
+int gdn_fwd_infer(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
+                  const void *beta, const float *S0, void *y, float *S_T, void *workspace, size_t workspace_bytes,
+                  void *stream) {
+    if (shape == nullptr) return GDN_ERR_INVALID_ARG;
+    Plan p;
+    int rc = make_plan(shape, &p);
+    if (rc != GDN_OK) return rc;
+    if (!p.tc) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!q || !k || !v || !g || !beta || !y || !workspace) return GDN_ERR_INVALID_ARG;
+    const void *all[] = {q, k, v, g, beta, S0, y, S_T, workspace};
+    for (const void *ptr : all)
+        if (ptr && !aligned(ptr)) return GDN_ERR_MISALIGNED;
+    if (workspace_bytes < gdn_infer_workspace_bytes(shape)) return GDN_ERR_BUFFER_TOO_SMALL;
+    return tc_fwd(p, q, k, v, g, beta, S0, y, S_T, nullptr, static_cast<char *>(workspace), nullptr,
+                  gdn::kStagePrep | gdn::kStageSweep, (cudaStream_t)stream);
 }
 
 // ---- re-computation mode: the saved buffer holds only the checkpoints and the residuals

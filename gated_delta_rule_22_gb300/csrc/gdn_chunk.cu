@@ -550,6 +550,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
     const bool math = warp < kFwdMathWarps;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, Dv = p.Dv, Hv = p.Hv, NC = p.NC;
+    const bool infer = !kLite && p.ckpt == nullptr;            // inference: nothing saved, no v - u
     const bool ends = !kLite || split < Dv / kL;               // a block of value rows (else of the identity)
     const bool maps_cta = kLite && !ends;
     const int r0 = (ends ? split : split - Dv / kL) * kL;
@@ -652,7 +653,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 if (__any_sync(kFullMask, !w)) { fail = true; break; }
                 tc_fence_after();
                 umma_gemm_w(tY, CmOp{qb, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, false, lead);
-                umma_gemm_w(tU, CmOp{kb, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, false, lead);
+                if (!infer) umma_gemm_w(tU, CmOp{kb, kL, 0, 0, false}, CmOp{sop, kL, 0, 0, false}, DK, id64, false, lead);
                 umma_commit_w(mQ, lead);
                 // ---- Sigma = (diag(E_L) Delta)^T K once Delta is written; then P Delta and KKm Delta
                 w = mbar_wait(bDt, c & 1);
@@ -666,6 +667,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 tc_fence_after();
                 umma_gemm_w(tPy, CmOp{pk, 2 * kL, 0, 0, false}, CmOp{dt, kL, 0, 0, true}, kL,
                             umma_idesc_t(1, kL, kL, false, true), false, lead);
+                if (!infer)
                 umma_gemm_w(tPu, CmOp{pk, 2 * kL, kL, 0, false}, CmOp{dt, kL, 0, 0, true}, kL,
                             umma_idesc_t(1, kL, kL, false, true), false, lead);
                 umma_commit_w(mY, lead);
@@ -713,7 +715,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 // y and v - u of chunk cc leave from their staging tiles
                 auto store_out = [&](int cc) {
                     tma_store_4d(&maps.y, ysg, r0, h, cc * kL, b);
-                    tma_store_5d(&maps.r, rsg, 0, cc * kL, r0 / 32, h, b);
+                    if (!infer) tma_store_5d(&maps.r, rsg, 0, cc * kL, r0 / 32, h, b);
                     bulk_commit();
                 };
                 auto copy_P = [&](int cc) {                // [P; KKm] of chunk cc
@@ -740,8 +742,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     const size_t chk = head * NC + c;
                     // the bf16 state leaves (the backward's operand) once written
                     if (!mbar_wait(bS, c & 1)) { fail = true; break; }
-                    bulk_store(p.s0m + (chk * gridDim.x + split) * kL * DK, sop, kL * DK * 2);
-                    bulk_commit();
+                    if (!infer) {
+                        bulk_store(p.s0m + (chk * gridDim.x + split) * kL * DK, sop, kL * DK * 2);
+                        bulk_commit();
+                    }
                     // the previous chunk's y and v - u once staged
                     if (c > 0) {
                         if (!mbar_wait(bE, (c - 1) & 1)) { fail = true; break; }
@@ -757,9 +761,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                     // state operand's tile and the y, v - u staging, they are free (fS); once it
                     // has been read too, group W's buffer takes chunk c + 2
                     if (!mbar_wait(bK, c & 1)) { fail = true; break; }
-                    for (int q = 0; q < DK / 32; ++q) tma_store_2d(&maps.ck, ck_box(c, q), 32 * q, (int)(chk * Dv + r0));
-                    bulk_commit();
-                    bulk_wait_read_but<1>();
+                    if (!infer) {
+                        for (int q = 0; q < DK / 32; ++q) tma_store_2d(&maps.ck, ck_box(c, q), 32 * q, (int)(chk * Dv + r0));
+                        bulk_commit();
+                        bulk_wait_read_but<1>();
+                    } else {
+                        bulk_wait_read();                   // no checkpoint store: the newest group is y's
+                    }
                     mbar_arrive(fS);
                     bulk_wait_read();
                     if (c + 2 < NC) issue_w(c + 2);
@@ -864,7 +872,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                                 yv[2 * j + 3]);
                 }
             }
-            {
+            if (!infer) {
                 float k[16], pu[16];
                 tmem_ld16x256_x4(tU + lane16 + 32 * hw, k);
                 tmem_ld16x256_x4(tPu + lane16 + 32 * hw, pu);
@@ -883,7 +891,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             }
         };
         load_lam(0);
-        if (!kLite) load_v(0);
+        if (!kLite && !infer) load_v(0);
         float decay = 1.f, pga = 1.f, pgb = 1.f;     // exp(Lam_L), exp(Lam_ta), exp(Lam_tb) of the previous chunk
         uint32_t pva[4], pvb[4];                      // v pairs of the previous chunk
         for (int c = 0; c < NC; ++c) {
@@ -896,7 +904,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
             }
             if (c + 1 < NC) {
                 load_lam(c + 1);
-                if (!kLite) load_v(c + 1);
+                if (!kLite && !infer) load_v(c + 1);
             }
             // ---- S <- exp(Lam_L) S + Sigma of the previous chunk; S as an operand
             if (c > 0) {
@@ -957,7 +965,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) chunk_sweep_kernel(ChunkParams
                 // buffer of this chunk is free (Delta is formed, mD) until the copy warp refills it
                 // after these stores have read it
 #pragma unroll
-                for (int j = 0; j < NS / 4; ++j)
+                for (int j = 0; j < NS / 4 && !infer; ++j)
 #pragma unroll
                     for (int k2 = 0; k2 < 2; ++k2) {
                         const int row = fs.row(2 * k2), col = fs.col(j, 0);

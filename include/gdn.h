@@ -221,6 +221,21 @@ GDN_API int gdn_bwd_seg(const gdn_shape *shape, int segments, const void *q, con
                         void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Inference forward on the tensor cores (no backward follows): for a shape the chunkwise forward
+ * takes (bf16, chunk 64, Dk in {64, 128, 192}, Dv a multiple of 64; else
+ * GDN_ERR_UNSUPPORTED_SHAPE), the forward with its per-chunk products in `workspace`
+ * (gdn_infer_workspace_bytes(shape) bytes, device, 16-byte aligned, contents on entry do not
+ * matter) and nothing saved: y and S_T as gdn_fwd gives them (the same bits), without the
+ * checkpoints, the bf16 states or v - u, so faster. gdn_fwd with ckpt = NULL, which has no
+ * workspace, runs the sequential kernels instead (or, for T = 1, the decode step). Returns GDN_OK
+ * or an error code; the size query returns 0 for a shape it does not take.
+ */
+GDN_API size_t gdn_infer_workspace_bytes(const gdn_shape *shape);
+GDN_API int gdn_fwd_infer(const gdn_shape *shape, const void *q, const void *k, const void *v, const void *g,
+                          const void *beta, const float *S0, void *y, float *S_T, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/*
  * Re-computation mode (mlx-lm PR #1217, "What this PR adds": checkpoints on fixed-size chunks,
  * the forward recomputed within each chunk during the reverse sweep). For a shape the
  * chunkwise tensor-core kernels take both ways (bf16, chunk 64; else

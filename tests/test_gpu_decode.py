@@ -102,3 +102,26 @@ def test_decode_step_shapes(dev, w):
         y2, S2, _ = gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], S, S_T=S, want_ckpt=False)
         torch.cuda.synchronize()
         assert torch.equal(y2, y) and torch.equal(S, S_T)
+
+
+@pytest.mark.parametrize("w", [
+    gs.Workload("inf-Dk64-Dv64-ragged", 2, 130, 2, 4, 64, 64, "bf16", "strong", True, False),
+    gs.Workload("inf-Dk128-Dv256", 1, 200, 1, 2, 128, 256, "bf16", "weak", True, False),
+    gs.Workload("inf-Dk192-gqa", 1, 300, 2, 6, 192, 128, "bf16", "half", False, False),
+    gs.WORKLOADS["linattn-T2048"],
+], ids=lambda w: w.name)
+def test_inference_forward_is_the_forward(dev, w):
+    """gdn_fwd_infer (the chunkwise forward with nothing saved) gives y and S_T bit for bit as
+    gdn_fwd does with its saved buffer, and matches the oracle."""
+    import gated_delta_rule_22_gb300 as gdn
+    inp = gs.make_inputs(w)
+    t = H.to_device(inp, dev)
+    y, S_T = gdn.gdn_fwd_infer(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"])
+    y0, S0_T, _ = gdn.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["S0"])
+    torch.cuda.synchronize()
+    assert torch.equal(y, y0) and torch.equal(S_T, S0_T)
+    if w.T <= 300:
+        ref = oracle.fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["S0"], chunk=w.chunk)
+        e_y = oracle.rel_l2(y.double().cpu().numpy(), ref["y"])
+        e_s = oracle.rel_l2(S_T.double().cpu().numpy(), ref["S_T"])
+        assert e_y <= H.TOL["bf16"] and e_s <= H.TOL["bf16"], (e_y, e_s)

@@ -89,3 +89,32 @@ def test_argument_checks(lib):
     assert rc_bwd(lib, s, dy=None) == INVALID
     assert lib.gdn_fwd_rc(None, *([None] * 9), 0, None, 0, None) == INVALID
     assert lib.gdn_bwd_rc(None, *([None] * 6), 0, *([None] * 9), 0, None) == INVALID
+
+
+def test_inference_forward_sizes_and_checks(lib):
+    """gdn_fwd_infer: its workspace is the per-chunk products only; it takes the shapes the
+    chunkwise forward takes (including value widths the chunkwise backward does not)."""
+    s = shape()
+    assert lib.gdn_infer_workspace_bytes(ctypes.byref(s)) == lib.gdn_rc_fwd_workspace_bytes(ctypes.byref(s))
+    wide = shape(Dk=128, Dv=256)
+    assert lib.gdn_infer_workspace_bytes(ctypes.byref(wide)) > 0
+    for kw in (dict(dtype=0), dict(chunk=32), dict(Dk=96)):
+        bad = shape(**kw)
+        assert lib.gdn_infer_workspace_bytes(ctypes.byref(bad)) == 0
+    f = ctypes.c_void_p(FAKE)
+    need = lib.gdn_infer_workspace_bytes(ctypes.byref(s))
+
+    def call(sh=s, ws=need, **ptrs):
+        names = ("q", "k", "v", "g", "beta", "S0", "y", "S_T", "work")
+        p = {n: FAKE for n in names}
+        p.update(S0=None, S_T=None)
+        p.update(ptrs)
+        a = [ctypes.c_void_p(p[n]) if p[n] is not None else None for n in names]
+        return lib.gdn_fwd_infer(ctypes.byref(sh), *a[:8], a[8], ws, None)
+
+    assert call(sh=shape(dtype=0)) == UNSUPPORTED
+    assert call(ws=need - 1) == SMALL
+    assert call(v=FAKE + 8) == MISALIGNED
+    assert call(y=None) == INVALID
+    assert call(work=None) == INVALID
+    assert lib.gdn_fwd_infer(None, f, f, f, f, f, None, f, None, f, need, None) == INVALID

@@ -32,24 +32,31 @@ class Stores:
         assert not (busy & set(tiles)), f"{what} rewritten while a store still reads it"
 
 
-def sweep(NC, drop=None):
+def sweep(NC, drop=None, infer=False):
     """chunk_sweep_kernel: the copy warp's issuing lane stores every tile. Per chunk c it stores the
     bf16 state (sop) once the math warps have written it, the previous chunk's y and v - u (ysg,
     rsg), and the staged fp32 checkpoint (group W's buffer c % 2 and the extra box ckx c % 2);
     then it waits until all but that newest group have read their tiles and releases sop, ysg
     and rsg to the math warps (fS), which go on with the next chunk, while it waits for the rest
-    and refills group W's buffer c % 2 with chunk c + 2's operands."""
+    and refills group W's buffer c % 2 with chunk c + 2's operands. The inference forward
+    (`infer`) stores only y: its release waits for every group, as the newest is y's."""
     st = Stores()
     T = "copy"
     st.write({"sop"}, "state operand of chunk 0")
     for c in range(NC):
-        st.commit(T, {"sop"})
+        if not infer:                                  # the inference forward saves no state
+            st.commit(T, {"sop"})
         if c > 0:
-            st.commit(T, {"ysg", "rsg"})
-        st.write({f"W{c % 2}", f"ckx{c % 2}"}, f"staged checkpoint of chunk {c}")
-        st.commit(T, {f"W{c % 2}", f"ckx{c % 2}"})
-        if drop != "fS":
-            st.wait_read(T, but=1)
+            st.commit(T, {"ysg"} if infer else {"ysg", "rsg"})
+        if not infer:
+            st.write({f"W{c % 2}", f"ckx{c % 2}"}, f"staged checkpoint of chunk {c}")
+            st.commit(T, {f"W{c % 2}", f"ckx{c % 2}"})
+            if drop != "fS":
+                st.wait_read(T, but=1)
+        elif drop == "fS":
+            st.wait_read(T, but=1)                     # the wait that is right only with a checkpoint store
+        else:
+            st.wait_read(T)
         if c + 1 < NC:
             st.write({"sop"}, f"state operand of chunk {c + 1}")
             st.write({"ysg", "rsg"}, f"y / v - u staging of chunk {c}")
@@ -127,6 +134,7 @@ def prep(units, rep, drop=None):
 @pytest.mark.parametrize("NC", [1, 2, 3, 8, 32])
 def test_sweeps_never_rewrite_a_tile_in_flight(NC):
     sweep(NC)
+    sweep(NC, infer=True)
     dsweep(NC)
 
 
@@ -143,3 +151,10 @@ def test_grad_and_prep_never_rewrite_a_tile_in_flight(groups, rep):
 def test_controls_without_a_wait_fail(fn, arg, drop):
     with pytest.raises(AssertionError, match="rewritten while a store still reads it"):
         fn(*arg, drop=drop) if isinstance(arg, tuple) else fn(arg, drop=drop)
+
+
+def test_inference_release_must_wait_for_every_store():
+    """With no checkpoint store the newest group is y's: releasing the staging tiles after
+    `wait_group.read 1` (the training forward's wait) would let y's staging be rewritten."""
+    with pytest.raises(AssertionError, match="rewritten while a store still reads it"):
+        sweep(3, drop="fS", infer=True)
