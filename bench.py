@@ -47,12 +47,12 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:^chunk_sweep -s 3 -c 1 python bench.py --steps 1 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("6b6e0cef09561d11", "chunk_prep"): 35600384 + 91748096,
-    ("6b6e0cef09561d11", "chunk_sweep"): 160040192 + 349540352,
-    ("16d0e1b944d60de2", "chunk_dsweep"): 160416512 + 192061184,
-    ("16d0e1b944d60de2", "chunk_grad"): 333489152 + 17624064,
+    ("fcce6927467827bf", "chunk_prep"): 35607808 + 91348224,
+    ("fcce6927467827bf", "chunk_sweep"): 160033024 + 349473024,
+    ("8f9bf5c65dda4f34", "chunk_dsweep"): 160422912 + 191624448,
+    ("8f9bf5c65dda4f34", "chunk_grad"): 333489152 + 17540864,
     # the decode-B64 workload (`-k regex:^decode`, `--workload decode-B64`)
-    ("813e00840969e5b0", "decode"): 404530688 + 349271552,
+    ("f63c92b466fa9389", "decode"): 404528896 + 349212416,
 }
 
 
