@@ -121,7 +121,7 @@ Workspace workspace_layout(const Plan &p) {
 // dS at each chunk end [B,Hv,NC,nsplit][64 x Dk], bf16 in their operand layout. (dq, dk are
 // summed over value heads in the gradient kernel's tensor memory and need no scratch.)
 struct TcWorkspace {
-    size_t db, f, yu, dl, dsl, total;
+    size_t db, f, yu, dl, dsl, sync, total;
 };
 
 TcWorkspace tc_workspace_layout(const Plan &p) {
@@ -134,6 +134,7 @@ TcWorkspace tc_workspace_layout(const Plan &p) {
     w.yu = off; off += round_up(nblk * 128 * 64 * 2);
     w.dl = off; off += round_up(nblk * 64 * 64 * 2);
     w.dsl = off; off += round_up(nblk * 64 * p.Dk * 2);
+    w.sync = off; off += round_up(((size_t)p.B * p.Hv * p.NC + 1) * 4);   // ready counters, group counter
     w.total = off;
     return w;
 }
@@ -490,6 +491,8 @@ static int tc_bwd(const Plan &p, const void *beta, const float *ckpt, const char
     cp.ws_yu = reinterpret_cast<__nv_bfloat16 *>(ws + tw.yu);
     cp.ws_dl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dl);
     cp.ws_dsl = reinterpret_cast<__nv_bfloat16 *>(ws + tw.dsl);
+    cp.ready = nullptr;
+    cp.next = nullptr;
     cp.B = p.B; cp.T = p.T; cp.Hk = p.Hk; cp.Hv = p.Hv; cp.Dv = p.Dv; cp.NC = p.NC; cp.nsplit = p.nsplit;
     g_last_error[0] = '\0';
     int rc = device_status_address(&cp.status);
@@ -502,6 +505,15 @@ static int tc_bwd(const Plan &p, const void *beta, const float *ckpt, const char
         (rc = make_btd_map(&tm_dq, dq, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK ||
         (rc = make_btd_map(&tm_dk, dk, true, p.B, p.T, p.Hk, p.Dk, 64, 64)) != GDN_OK)
         return rc;
+    if (stages & gdn::kStageGrad) {
+        // the gradient kernel runs alongside the reverse sweep of the same call, on the counters
+        // it publishes: both start from zero
+        if (!(stages & gdn::kStageDsweep)) return GDN_ERR_INVALID_ARG;
+        const size_t n = (size_t)p.B * p.Hv * p.NC;
+        cp.ready = reinterpret_cast<unsigned *>(ws + tw.sync);
+        cp.next = reinterpret_cast<int *>(cp.ready + n);
+        if ((rc = cuda_status(cudaMemsetAsync(cp.ready, 0, (n + 1) * 4, stream))) != GDN_OK) return rc;
+    }
     return cuda_status(gdn::launch_chunk_bwd(cp, tm_dv, tm_dy, tm_qk, tm_pk, tm_dq, tm_dk, p.Dk, stream, stages));
 }
 

@@ -43,6 +43,9 @@ namespace gdn {
 namespace {
 
 constexpr int kL = 64;           // chunk length
+// Polls of one ready counter before the gradient kernel gives up (each a round trip to L2 and
+// a short sleep: about a second in all, far above a chunk of the reverse sweep).
+constexpr unsigned kReadyWaitLimit = 1u << 21;
 
 __host__ __device__ inline size_t alb(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -318,6 +321,16 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
                     bulk_wait_read();
                     mbar_arrive(fO);
                     if (k + 2 < NC) fetch(k + 2);
+                    // every second chunk: the two chunks handled three and two before (c + 3, c + 2)
+                    // are complete for the gradient kernel -- their bulk stores (committed a chunk
+                    // or more ago: every group but the last four) and the math warps' f and dbeta
+                    // partials (written before they arrived at a later chunk's bU). Publishing
+                    // every chunk, or with a lag of one, held the copy warp up on its chain.
+                    if (p.ready != nullptr && k > 1 && (k & 1) == 1) {
+                        bulk_wait_but<4>();
+                        add_release_gpu(p.ready + head * NC + c + 3, 1u);
+                        add_release_gpu(p.ready + head * NC + c + 2, 1u);
+                    }
                 }
                 if (fail) {
                     // copies still in flight land before the CTA exits (each wait bounded)
@@ -577,6 +590,12 @@ __global__ void __launch_bounds__(kSweepThreads, 1) chunk_dsweep_kernel(ChunkBwd
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the chunks the loop left (the last two or three) for the gradient kernel: the copy warp's
+    // stores completed (bulk_wait_all) and the math warps' partials precede the barrier
+    if (warp == kSweepMathWarps + 1 && lane == 0 && !fail && p.ready != nullptr) {
+        for (int cc = ((NC - 1) & 1) == 1 ? 1 : 2; cc >= 0; --cc)   // what the loop left
+            if (cc < NC) add_release_gpu(p.ready + head * NC + cc, 1u);
+    }
     if (warp == kSweepMathWarps) tmem_dealloc(tmem, 512);
 }
 
@@ -613,9 +632,14 @@ struct GradSmem {
 
 }  // namespace
 
-// Persistent: one CTA per SM, each over a contiguous range of whole groups of units (b, chunk,
-// value head), value head fastest, so that consecutive units share [Q; K] and the value heads
-// of a kv head are summed by one CTA, in ascending order, whatever the grid. Every operand arrives by bulk
+// Persistent: one CTA per SM, each taking whole groups of units (b, chunk, value heads of one kv
+// head) from a counter, last chunk first, and the units of a group in ascending value head, so
+// that they share [Q; K] and the value heads of a kv head are summed by one CTA, in ascending
+// order, whatever the grid or the order the groups are taken in. The kernel runs alongside the
+// reverse sweep (it does not wait for it to finish): the sweep goes through the chunks from the
+// last, publishing each (ready counters), and a group starts once every CTA of the sweep has
+// published its chunk for the group's value heads, so that the SMs the sweep leaves free work
+// from its first chunks on. Every operand arrives by bulk
 // copy, the next unit's as soon as its buffers are free, all after the second products:
 // [dY; dU], Delta (scaled in place by E_L for the second products) and dS_L, S0 (whose region
 // then holds the scratch operands) and [Q; K] (when the kv head or chunk changes).
@@ -641,8 +665,6 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     const int quarter = warp & 3, half = warp >> 2;
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     // unit u = ((b * NC + c) * Hk + hk) * rep + (h % rep): group u / rep
-    const int u_begin = (int)((long long)blockIdx.x * groups / gridDim.x) * rep;
-    const int u_end = (int)((long long)(blockIdx.x + 1) * groups / gridDim.x) * rep;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(alb(reinterpret_cast<size_t>(smem_raw), 1024));
@@ -693,7 +715,41 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         bulk_load(qk, p.qkm + (((size_t)b * Hk + h / rep) * NC + c) * 2 * kL * DK, kQkb, cbQ);
         ++nQ;
     };
-    auto same_qk = [&](int u1, int u2) { return u1 / rep == u2 / rep; };   // same (b, chunk, kv head)
+    // the group taken i-th: chunks from the last (the reverse sweep's order), then batch row and
+    // kv head
+    auto group_of = [&](int i) {
+        const int per_c = p.B * Hk, c = NC - 1 - i / per_c, r = i % per_c;
+        return ((r / Hk) * NC + c) * Hk + r % Hk;
+    };
+    // thread 32 (which issues the copies): the group taken as index i (>= groups when none is
+    // left) once every value head of it has the chunk published by all nsplit CTAs of the
+    // reverse sweep (the heads' counters polled together, bounded), into next_slot for every
+    // thread once a barrier has passed (-1 when the wait ran out); then what the sweep published
+    // is visible to this thread's copies and, past the barrier, to every thread's loads
+    int *next_slot = reinterpret_cast<int *>(tslot + 1);
+    auto resolve_group = [&](int i) {
+        bool okw = true;
+        if (i < groups) {
+            const int g = group_of(i), hk = g % Hk, c = (g / Hk) % NC, b = g / Hk / NC;
+            const unsigned *f = p.ready + ((size_t)b * Hv + hk * rep) * NC + c;   // head hk rep + hh at + hh NC
+            for (int h0 = 0; h0 < rep && okw; h0 += 4) {
+                for (unsigned it = 0;; ++it) {
+                    unsigned v[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[j] = h0 + j < rep ? load_relaxed_gpu(f + (size_t)(h0 + j) * NC) : nsplit;
+                    bool all = true;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) all = all && v[j] >= (unsigned)nsplit;
+                    if (all) break;
+                    if (it >= kReadyWaitLimit) { okw = false; break; }
+                    __nanosleep(64);
+                }
+            }
+            fence_acquire_gpu();
+            fence_proxy_async_global();
+        }
+        *next_slot = okw ? i : -1;
+    };
     // decays, beta and the f partials of a unit (threads < 64), loaded one unit ahead and kept
     // raw (converted and summed where they are used, so that the loads do not stall here)
     constexpr int kMaxPart = 8;                             // two per block of 64 value rows, Dv <= 256
@@ -727,23 +783,30 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tR1 = tmem, tRS = tmem + DK, tS1 = tmem + 2 * DK, tS2 = tmem + 2 * DK + 64;
-    griddep_wait();                                           // the previous kernel's writes are visible
+    // No wait for the previous kernel (the reverse sweep) to finish: its outputs are taken chunk
+    // by chunk through the ready counters, and everything else it reads was written before the
+    // reverse sweep began.
     griddep_launch();
 
-    if (tid == 32 && u_begin < u_end) {
-        copy_q(u_begin);
-        copy_a(u_begin);
-        copy_s(u_begin);
+    if (tid == 32) resolve_group(atomicAdd(p.next, 1));
+    __syncthreads();
+    bool ok = *next_slot >= 0;
+    int un = ok && *next_slot < groups ? group_of(*next_slot) * rep : -1;   // the next unit
+    if (tid == 32 && un >= 0) {
+        copy_q(un);
+        copy_a(un);
+        copy_s(un);
     }
-    if (u_begin < u_end) load_vec(u_begin);
+    if (un >= 0) load_vec(un);
     unsigned ph = 0;
-    bool ok = true;
-    for (int u = u_begin; u < u_end && ok; ++u) {
+    int taken = 0;      // thread 32: the index of the group after this one, taken at this group's first unit
+    int nxt = 0;        // every thread: that index once resolved (in the first unit's second products)
+    for (int u = un; u >= 0 && ok; u = un) {
         int b, c, h;
         chunk_of(u, b, c, h);
         const int t0 = c * kL, len = min(kL, T - t0);
         const size_t rowbase = (size_t)b * T + t0;
-        const bool newq = u == u_begin || !same_qk(u - 1, u);
+        const bool newq = u % rep == 0;                     // a new group: its [Q; K]
         // ---- decays, beta, f
         if (tid < kL) {
             Lm[tid] = vlam;
@@ -800,6 +863,9 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
                             umma_idesc_t(1, 2 * kL, DK, false, true), s > 0, lead);
             umma_commit_w(bar, lead);
         }
+        // ---- the group after this one, taken at this group's first unit (thread 32; resolved in
+        // the second products)
+        if (gfirst && tid == 32) taken = atomicAdd(p.next, 1);
         // ---- c0 = <dS_L, S0> (both in the same layout) while the products run, by warps 1-7 (warp
         // 0 is issuing them)
         if (warp > 0) {
@@ -824,7 +890,13 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
         ++ph;
         tc_fence_after();
         if (!ok) break;
-        if (u + 1 < u_end) load_vec(u + 1);                // used at the next unit's start
+        un = u + 1;
+        if (glast && !gfirst) {                            // the next group, resolved at an earlier unit
+            ok = nxt >= 0;
+            if (!ok) break;
+            un = nxt < groups ? group_of(nxt) * rep : -1;
+        }
+        if (un >= 0 && !(glast && gfirst)) load_vec(un);   // used at the next unit's start
         {
             // ---- G o E_incl, H o E_strict and [W1; W2] = [G o QK^T; H o KK^T] as operands
             const int r = 32 * quarter + lane, s = r & (kL - 1);
@@ -942,16 +1014,24 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
             dgp[(2 * part + 0) * kL + t] = s2;
             dgp[(2 * part + 1) * kL + t] = expf(LmP[t]) * s3;
         }
+        if (gfirst && tid == 32) resolve_group(taken);
         ok = !__syncthreads_or(!mbar_wait(bar, ph & 1));
         ++ph;
         tc_fence_after();
         if (!ok) break;
         // [dY; dU], Delta, dS_L, the S0 region (scratch) and, when the next unit needs another
         // [Q; K], its buffer are free: the next unit's go out now
-        if (tid == 32 && u + 1 < u_end) {
-            copy_a(u + 1);
-            copy_s(u + 1);
-            if (!same_qk(u, u + 1)) copy_q(u + 1);
+        if (gfirst) nxt = *next_slot;
+        if (glast && gfirst) {                             // one unit per group: resolved just now
+            ok = nxt >= 0;
+            if (!ok) break;
+            un = nxt < groups ? group_of(nxt) * rep : -1;
+            if (un >= 0) load_vec(un);                     // used at the next unit's start
+        }
+        if (tid == 32 && un >= 0) {
+            copy_a(un);
+            copy_s(un);
+            if (glast) copy_q(un);
         }
         {
             // ---- Z weighted by E(s, t) (s >= t), summed over the rows of both halves: a
@@ -1050,6 +1130,8 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
+    // this kernel completes after the reverse sweep, so that what follows on the stream sees both
+    griddep_wait();
 }
 
 size_t chunk_dsweep_smem(int Dk) { return DSweepSmem(Dk).total; }

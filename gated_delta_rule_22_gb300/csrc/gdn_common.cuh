@@ -104,6 +104,12 @@ struct ChunkBwdParams {
     __nv_bfloat16 *ws_yu;      // [B, Hv, NC, nsplit][128 x 64]: [dY; dU] of the block, operand layout
     __nv_bfloat16 *ws_dl;      // [B, Hv, NC, nsplit][64 x 64]: Delta = diag(beta) (v - u), operand layout
     __nv_bfloat16 *ws_dsl;     // [B, Hv, NC, nsplit][64 x Dk]: dS at each chunk end, operand layout
+    // Hand-off from the reverse sweep to the gradient kernel, which runs alongside it: ready[(b *
+    // Hv + h) * NC + c] counts the reverse-sweep CTAs (nsplit in all) that have published chunk
+    // c of (b, h); next hands out the gradient kernel's groups. Both zero when the reverse sweep
+    // starts; ready null: the reverse sweep publishes nothing (no gradient kernel follows).
+    unsigned *ready;
+    int *next;
     int *status;
     int B, T, Hk, Hv, Dv, NC, nsplit;
 };
@@ -345,6 +351,9 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 template <int N>
 __device__ __forceinline__ void bulk_wait_read_but() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups are pending (the others' writes complete).
+template <int N>
+__device__ __forceinline__ void bulk_wait_but() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
 
 // 2-D tiled TMA store of one box from shared memory (the box's layout as the tensor map's
 // swizzle mode describes), in the issuing thread's current bulk async-group.
@@ -380,6 +389,27 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void 
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+
+// Counter hand-off between CTAs at GPU scope: the producer's earlier writes (its own, its bulk
+// stores once complete, and those of other threads of its CTA that it has synchronised with)
+// are visible to a consumer that reads the incremented value with load_acquire_gpu.
+__device__ __forceinline__ void add_release_gpu(unsigned *ctr, unsigned v) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned load_acquire_gpu(const unsigned *ctr) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    return v;
+}
+// Polling form: relaxed loads (several in flight at once), then fence_acquire_gpu once every
+// value read is the one waited for.
+__device__ __forceinline__ unsigned load_relaxed_gpu(const unsigned *ctr) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // ---------------------------------------------------------------- tensor memory
 // Allocation is warp-collective (one warp); the allocated base address is written to

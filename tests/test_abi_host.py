@@ -87,7 +87,8 @@ def test_buffer_sizes_follow_the_plan(lib):
             r = lambda x: -(-x // 256) * 256  # noqa: E731
             ns = Dv // 64
             nblk = Hv * NC * ns
-            want = 2 * r(T * Hv * ns * 2 * 4) + r(nblk * 128 * 64 * 2) + r(nblk * 64 * 64 * 2) + r(nblk * 64 * Dk * 2)
+            want = (2 * r(T * Hv * ns * 2 * 4) + r(nblk * 128 * 64 * 2) + r(nblk * 64 * 64 * 2) + r(nblk * 64 * Dk * 2)
+                    + r((Hv * NC + 1) * 4))   # the ready counters of the reverse sweep's chunks, the group counter
             assert ws == want, (Dk, Dv, ws, want)
         else:
             assert ws >= row_split, (Dk, Dv, ws)
