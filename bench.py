@@ -47,12 +47,12 @@ PAGES_TOKENS_PER_S = 2048 / 0.1498
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:^chunk_sweep -s 3 -c 1 python bench.py --steps 1 --warmup 3 --no-cpu-baseline
 TRAFFIC = {
-    ("fcce6927467827bf", "chunk_prep"): 35607808 + 91348224,
-    ("fcce6927467827bf", "chunk_sweep"): 160033024 + 349473024,
-    ("8f9bf5c65dda4f34", "chunk_dsweep"): 160422912 + 191624448,
-    ("8f9bf5c65dda4f34", "chunk_grad"): 333489152 + 17540864,
+    ("6bca51b51f2b99a8", "chunk_prep"): 35600896 + 91542272,
+    ("6bca51b51f2b99a8", "chunk_sweep"): 160030720 + 349309696,
+    ("d71abe6af8b106d7", "chunk_dsweep"): 160391168 + 191910400,
+    ("d71abe6af8b106d7", "chunk_grad"): 332331264 + 17533184,
     # the decode-B64 workload (`-k regex:^decode`, `--workload decode-B64`)
-    ("f63c92b466fa9389", "decode"): 404528896 + 349212416,
+    ("5f1ef1aadd121d75", "decode"): 404523264 + 349300224,
 }
 
 

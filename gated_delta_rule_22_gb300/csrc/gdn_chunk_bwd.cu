@@ -635,11 +635,11 @@ struct GradSmem {
 // Persistent: one CTA per SM, each taking whole groups of units (b, chunk, value heads of one kv
 // head) from a counter, last chunk first, and the units of a group in ascending value head, so
 // that they share [Q; K] and the value heads of a kv head are summed by one CTA, in ascending
-// order, whatever the grid or the order the groups are taken in. The kernel runs alongside the
-// reverse sweep (it does not wait for it to finish): the sweep goes through the chunks from the
-// last, publishing each (ready counters), and a group starts once every CTA of the sweep has
-// published its chunk for the group's value heads, so that the SMs the sweep leaves free work
-// from its first chunks on. Every operand arrives by bulk
+// order, whatever the grid or the order the groups are taken in. Given ready counters, the
+// kernel runs alongside the reverse sweep (it does not wait for it to finish): the sweep goes
+// through the chunks from the last, publishing them (ready counters), and a group starts once
+// every CTA of the sweep has published its chunk for the group's value heads, so that the SMs the
+// sweep leaves free work from its first chunks on. Every operand arrives by bulk
 // copy, the next unit's as soon as its buffers are free, all after the second products:
 // [dY; dU], Delta (scaled in place by E_L for the second products) and dS_L, S0 (whose region
 // then holds the scratch operands) and [Q; K] (when the kv head or chunk changes).
@@ -729,7 +729,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     int *next_slot = reinterpret_cast<int *>(tslot + 1);
     auto resolve_group = [&](int i) {
         bool okw = true;
-        if (i < groups) {
+        if (i < groups && p.ready != nullptr) {
             const int g = group_of(i), hk = g % Hk, c = (g / Hk) % NC, b = g / Hk / NC;
             const unsigned *f = p.ready + ((size_t)b * Hv + hk * rep) * NC + c;   // head hk rep + hh at + hh NC
             for (int h0 = 0; h0 < rep && okw; h0 += 4) {
@@ -783,9 +783,10 @@ __global__ void __launch_bounds__(256, 1) chunk_grad_kernel(ChunkBwdParams p, in
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tR1 = tmem, tRS = tmem + DK, tS1 = tmem + 2 * DK, tS2 = tmem + 2 * DK + 64;
-    // No wait for the previous kernel (the reverse sweep) to finish: its outputs are taken chunk
-    // by chunk through the ready counters, and everything else it reads was written before the
-    // reverse sweep began.
+    // With ready counters, no wait for the previous kernel (the reverse sweep) to finish: its
+    // outputs are taken chunk by chunk through them, and everything else this kernel reads was
+    // written before the reverse sweep began. Without, the sweep's writes are all visible first.
+    if (p.ready == nullptr) griddep_wait();
     griddep_launch();
 
     if (tid == 32) resolve_group(atomicAdd(p.next, 1));
@@ -1153,23 +1154,29 @@ static cudaError_t launch_chunk_bwd_t(const ChunkBwdParams &p, const CUtensorMap
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(chunk_grad_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
     if (err != cudaSuccess) return err;
-    if (stages & kStageDsweep) {
-        timing_mark("chunk_dsweep", 0, s);
-        err = launch_pdl(chunk_dsweep_kernel<E>, dim3(p.nsplit, p.Hv, p.B), dim3(kSweepThreads), sd, s, p, tm_dv, tm_dy,
-                         tm_qk, tm_pk);
-        timing_mark("chunk_dsweep", 1, s);
-        if (err != cudaSuccess) return err;
-    }
-    if (!(stages & kStageGrad)) return err;
-    timing_mark("chunk_grad", 0, s);
     const int groups = p.NC * p.Hk * p.B;                   // (b, chunk, kv head)
     int dev = 0, sms = 0;
     err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
+    // The gradient kernel runs alongside the reverse sweep (on the ready counters it publishes)
+    // where that pays: the sweep in one wave (all its rows publish their chunks in step) and more
+    // groups than SMs (a CTA that takes its next group early then keeps none from an idle CTA).
+    // Elsewhere it waits for the sweep to finish.
+    ChunkBwdParams q = p;
+    if (!(stages & kStageGrad) || (long long)p.B * p.Hv * p.nsplit > sms || groups <= sms) q.ready = nullptr;
+    if (stages & kStageDsweep) {
+        timing_mark("chunk_dsweep", 0, s);
+        err = launch_pdl(chunk_dsweep_kernel<E>, dim3(p.nsplit, p.Hv, p.B), dim3(kSweepThreads), sd, s, q, tm_dv, tm_dy,
+                         tm_qk, tm_pk);
+        timing_mark("chunk_dsweep", 1, s);
+        if (err != cudaSuccess) return err;
+    }
+    if (!(stages & kStageGrad)) return err;
+    timing_mark("chunk_grad", 0, s);
     const int grid = groups < sms ? groups : sms;           // persistent: one CTA per SM
-    err = launch_pdl(chunk_grad_kernel<E>, dim3(grid), dim3(256), sg, s, p, groups, tm_dq, tm_dk);
+    err = launch_pdl(chunk_grad_kernel<E>, dim3(grid), dim3(256), sg, s, q, groups, tm_dq, tm_dk);
     timing_mark("chunk_grad", 1, s);
     return err;
 }

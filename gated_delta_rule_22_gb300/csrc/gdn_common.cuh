@@ -104,10 +104,10 @@ struct ChunkBwdParams {
     __nv_bfloat16 *ws_yu;      // [B, Hv, NC, nsplit][128 x 64]: [dY; dU] of the block, operand layout
     __nv_bfloat16 *ws_dl;      // [B, Hv, NC, nsplit][64 x 64]: Delta = diag(beta) (v - u), operand layout
     __nv_bfloat16 *ws_dsl;     // [B, Hv, NC, nsplit][64 x Dk]: dS at each chunk end, operand layout
-    // Hand-off from the reverse sweep to the gradient kernel, which runs alongside it: ready[(b *
-    // Hv + h) * NC + c] counts the reverse-sweep CTAs (nsplit in all) that have published chunk
-    // c of (b, h); next hands out the gradient kernel's groups. Both zero when the reverse sweep
-    // starts; ready null: the reverse sweep publishes nothing (no gradient kernel follows).
+    // Hand-off from the reverse sweep to the gradient kernel when it runs alongside it: ready[(b
+    // * Hv + h) * NC + c] counts the reverse-sweep CTAs (nsplit in all) that have published chunk
+    // c of (b, h); ready null: the sweep publishes nothing and the gradient kernel waits for it
+    // to finish. next hands out the gradient kernel's groups. Both zero when the sweep starts.
     unsigned *ready;
     int *next;
     int *status;
